@@ -1,0 +1,225 @@
+"""ctypes wrapper around the C oracle (oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
+CPU-baseline leg of bench.py, never by the product package. All arrays are
+numpy; bf16 tensors travel as uint16 bit patterns.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+class OrcMat(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("g", ctypes.c_float),
+                ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        L.orc_e2m1_value.restype = ctypes.c_double
+        L.orc_e2m1_value.argtypes = [ctypes.c_int]
+        L.orc_e4m3_value.restype = ctypes.c_double
+        L.orc_e4m3_value.argtypes = [ctypes.c_int]
+        L.orc_e2m1_encode.restype = ctypes.c_int
+        L.orc_e2m1_encode.argtypes = [ctypes.c_float]
+        L.orc_e4m3_encode.restype = ctypes.c_int
+        L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        L.orc_bf16_round.restype = ctypes.c_uint16
+        L.orc_bf16_round.argtypes = [ctypes.c_double]
+        L.orc_bf16_value.restype = ctypes.c_double
+        L.orc_bf16_value.argtypes = [ctypes.c_uint16]
+        L.orc_quantize.restype = ctypes.c_int
+        L.orc_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P, P]
+        L.orc_dequantize.restype = None
+        L.orc_dequantize.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, P]
+        L.orc_route.restype = None
+        L.orc_route.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_int32,
+                                ctypes.c_int32, P, P, P, P, P]
+        L.orc_moe_layer.restype = None
+        L.orc_moe_layer.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P,
+                                    ctypes.c_int32, ctypes.c_int32, P, P]
+        L.orc_lm_head.restype = None
+        L.orc_lm_head.argtypes = [P, P, ctypes.c_int32, P]
+        L.orc_lm_head_rows.restype = None
+        L.orc_lm_head_rows.argtypes = [P, P, ctypes.c_int32, P, ctypes.c_int64, P]
+        L.orc_set_threads.restype = None
+        L.orc_set_threads.argtypes = [ctypes.c_int]
+        L.orc_get_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def set_threads(n: int):
+    lib().orc_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return lib().orc_get_threads()
+
+
+# ---- codecs ---------------------------------------------------------------
+def e2m1_value(code: int) -> float:
+    return lib().orc_e2m1_value(int(code))
+
+
+def e4m3_value(byte: int) -> float:
+    return lib().orc_e4m3_value(int(byte))
+
+
+def e2m1_encode(v: float) -> int:
+    return lib().orc_e2m1_encode(float(v))
+
+
+def e4m3_encode(v: float) -> int:
+    return lib().orc_e4m3_encode(float(v))
+
+
+def bf16_round(x: float) -> int:
+    return lib().orc_bf16_round(float(x))
+
+
+def bf16_value(b: int) -> float:
+    return lib().orc_bf16_value(int(b))
+
+
+def bf16_to_f32(a: np.ndarray) -> np.ndarray:
+    """uint16 bf16 bit patterns -> float32 (exact)."""
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+# ---- quantiser ------------------------------------------------------------
+PER_TENSOR, PER_ROW, GIVEN = 0, 1, 2
+
+
+def quantize(x: np.ndarray, mode: int = PER_TENSOR, g: float = None):
+    """x: float32 [rows][cols] (or uint16 bf16). Returns (codes, scales, g)."""
+    if x.dtype == np.uint16:
+        x = bf16_to_f32(x)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, cols // 16), np.uint8)
+    gio = np.zeros(rows if mode == PER_ROW else 1, np.float32)
+    if mode == GIVEN:
+        gio[0] = g
+    rc = lib().orc_quantize(_p(x), rows, cols, mode, _p(gio), _p(codes), _p(scales))
+    if rc != 0:
+        raise ValueError("orc_quantize rejected its arguments")
+    return codes, scales, gio
+
+
+def dequantize(codes, scales, g, cols: int = None) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    g = np.ascontiguousarray(np.atleast_1d(g), np.float32)
+    rows = codes.shape[0]
+    cols = codes.shape[1] * 2 if cols is None else cols
+    out = np.zeros((rows, cols), np.float64)
+    lib().orc_dequantize(_p(codes), _p(scales), _p(g), int(g.size > 1), rows, cols, _p(out))
+    return out
+
+
+class Mat:
+    """An NVFP4 matrix held by the oracle: codes [n][k/2], scales [n][k/16], global g."""
+
+    def __init__(self, codes, scales, g):
+        self.codes = np.ascontiguousarray(codes, np.uint8)
+        self.scales = np.ascontiguousarray(scales, np.uint8)
+        self.g = float(np.asarray(g).reshape(-1)[0])
+        self.n = self.codes.shape[0]
+        self.k = self.codes.shape[1] * 2
+
+    def c(self):
+        return OrcMat(self.codes.ctypes.data, self.scales.ctypes.data, self.g, self.n, self.k)
+
+    @staticmethod
+    def from_master(w):
+        c, s, g = quantize(w, PER_TENSOR)
+        return Mat(c, s, g[0])
+
+
+# ---- router ---------------------------------------------------------------
+def route(h_bf16: np.ndarray, Wg: np.ndarray, bias: np.ndarray, k: int):
+    """Returns dict(idx int32 [T][k], w f64 [T][k], z, c, tau f64 [T][E])."""
+    h = np.ascontiguousarray(h_bf16, np.uint16)
+    if h.ndim == 1:
+        h = h[None, :]
+    T, H = h.shape
+    Wg = np.ascontiguousarray(Wg, np.float32)
+    bias = np.ascontiguousarray(bias, np.float32)
+    E = Wg.shape[0]
+    idx = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    z = np.zeros((T, E), np.float64)
+    c = np.zeros((T, E), np.float64)
+    tau = np.zeros((T, E), np.float64)
+    lib().orc_route(_p(h), T, H, _p(Wg), _p(bias), E, k, _p(idx), _p(w), _p(z), _p(c), _p(tau))
+    return dict(idx=idx, w=w, z=z, c=c, tau=tau)
+
+
+# ---- MoE layer / lm_head --------------------------------------------------
+def moe_layer(h_bf16, idx, w, up: dict, down: dict, sh_up: Mat, sh_down: Mat, w4a4: bool,
+              residual: bool, num_experts: int):
+    """up/down: {expert_id: Mat}; only the experts named in idx are needed.
+    Returns (out_bf16 uint16 [T][H], out_f64 [T][H])."""
+    h = np.ascontiguousarray(h_bf16, np.uint16)
+    if h.ndim == 1:
+        h = h[None, :]
+    T, H = h.shape
+    idx = np.ascontiguousarray(idx, np.int32).reshape(T, -1)
+    k = idx.shape[1]
+    w = np.ascontiguousarray(w, np.float64).reshape(T, k)
+    ups = (OrcMat * num_experts)()
+    downs = (OrcMat * num_experts)()
+    for e in range(num_experts):
+        if e in up:
+            ups[e] = up[e].c()
+            downs[e] = down[e].c()
+    for e in np.unique(idx):
+        if int(e) not in up:
+            raise KeyError(f"expert {int(e)} weights not supplied")
+    shu, shd = sh_up.c(), sh_down.c()
+    out = np.zeros((T, H), np.uint16)
+    outf = np.zeros((T, H), np.float64)
+    lib().orc_moe_layer(_p(h), T, k, _p(idx), _p(w), ctypes.cast(ups, ctypes.c_void_p),
+                        ctypes.cast(downs, ctypes.c_void_p), ctypes.byref(shu), ctypes.byref(shd),
+                        int(w4a4), int(residual), _p(out), _p(outf))
+    return out, outf
+
+
+def lm_head(W: Mat, h_bf16) -> np.ndarray:
+    h = np.ascontiguousarray(h_bf16, np.uint16)
+    if h.ndim == 1:
+        h = h[None, :]
+    T = h.shape[0]
+    out = np.zeros((T, W.n), np.float64)
+    m = W.c()
+    lib().orc_lm_head(ctypes.byref(m), _p(h), T, _p(out))
+    return out
+
+
+def lm_head_rows(W: Mat, h_bf16, rows) -> np.ndarray:
+    h = np.ascontiguousarray(h_bf16, np.uint16)
+    if h.ndim == 1:
+        h = h[None, :]
+    T = h.shape[0]
+    rows = np.ascontiguousarray(rows, np.int64)
+    out = np.zeros((T, rows.size), np.float64)
+    m = W.c()
+    lib().orc_lm_head_rows(ctypes.byref(m), _p(h), T, _p(rows), rows.size, _p(out))
+    return out

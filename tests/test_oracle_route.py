@@ -1,0 +1,61 @@
+"""Pins for the oracle's sigmoid router: special cases whose answer is fixed
+by the definition, and the logits against a numpy float64 matmul."""
+import numpy as np
+from scipy.special import expit
+
+from gen import gen
+from oracle import oracle as orc
+
+
+def _setup(T=3, H=64, E=16, seed=0):
+    h = gen.hidden_bf16(T, H, seed, layer=9)
+    Wg = gen.router_w(seed, 9, E, H)
+    bias = gen.router_bias(seed, 9, E, -0.1, 0.1)
+    return h, Wg, bias
+
+
+def test_logits_and_scores_match_numpy():
+    h, Wg, bias = _setup()
+    r = orc.route(h, Wg, bias, 4)
+    hf = gen.bf16_bits_to_f32(h).astype(np.float64)
+    z = hf @ Wg.astype(np.float64).T
+    assert np.allclose(r["z"], z, rtol=1e-12, atol=1e-12)
+    assert np.allclose(r["c"], expit(z) + bias.astype(np.float64), rtol=1e-12, atol=1e-12)
+
+
+def test_selection_is_top_k_of_biased_scores():
+    h, Wg, bias = _setup(T=5, E=32)
+    r = orc.route(h, Wg, bias, 6)
+    for t in range(5):
+        order = np.lexsort((np.arange(32), -r["c"][t]))   # c desc, index asc
+        assert list(r["idx"][t]) == list(order[:6])
+        sig = expit(r["z"][t][r["idx"][t]])
+        assert np.allclose(r["w"][t], sig / sig.sum(), rtol=1e-12)
+        assert abs(r["w"][t].sum() - 1.0) < 1e-12
+
+
+def test_zero_hidden_selects_by_bias_with_equal_weights():
+    _, Wg, bias = _setup(E=16)
+    h = np.zeros((1, 64), np.uint16)
+    r = orc.route(h, Wg, bias, 6)
+    assert list(r["idx"][0]) == list(np.argsort(-bias.astype(np.float64), kind="stable")[:6])
+    assert np.allclose(r["w"][0], 1.0 / 6.0, rtol=0, atol=1e-15)
+
+
+def test_k_equals_E_is_a_permutation_and_k1_is_argmax():
+    h, Wg, bias = _setup(T=2, E=16)
+    r = orc.route(h, Wg, bias, 16)
+    for t in range(2):
+        assert sorted(r["idx"][t]) == list(range(16))
+        assert np.all(np.diff(r["c"][t][r["idx"][t]]) <= 0)
+    r1 = orc.route(h, Wg, bias, 1)
+    assert list(r1["idx"][:, 0]) == list(np.argmax(r["c"], axis=1))
+    assert np.all(r1["w"] == 1.0)
+
+
+def test_ties_go_to_lower_index():
+    Wg = np.zeros((8, 32), np.float32)
+    bias = np.array([0.1, 0.3, 0.3, 0.0, 0.3, 0.2, 0.2, 0.0], np.float32)
+    h = np.zeros((1, 32), np.uint16)
+    r = orc.route(h, Wg, bias, 4)
+    assert list(r["idx"][0]) == [1, 2, 4, 5]
