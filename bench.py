@@ -1,0 +1,374 @@
+"""Benchmark of the NVFP4 MoE decode hot path on GB300.
+
+Default workload (the headline): one batch-1 decode step through 23 W4A4
+NVFP4 MoE layers (hidden 2688, 128 experts of 1856, top-6 sigmoid router with
+correction bias, shared expert 3712, residual chain) and the NVFP4 weight-only
+lm_head 131072 x 2688 -> fp32 logits. Weights are synthetic (seeded bf16
+N(0, 0.02) masters quantised on the device), inputs are synthetic N(0, 1).
+
+The step is captured once as a CUDA graph (70 kernel launches: per layer the
+router, the up and the down kernel; then the lm_head) and replayed. Every
+step streams ~1.26 GB of weights, ten times the 129 MB L2, so no step finds
+its inputs in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+--impl reference times the CPU oracle (the plain reference implementation of
+the same computation) on the host cores on a bounded sample of the workload.
+One JSON line is printed by rank 0.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 NVFP4 MoE+lm_head decode µs/token and HBM GB/s (% of GB300 peak)"
+UNIT = "us/token"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), "measured"
+    return 6800.0, "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ dist
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def physical_gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+# ------------------------------------------------------------------ oracle timing
+class OracleSample:
+    """The CPU oracle on a bounded sample of the workload: the first n_layers
+    MoE layers of the chain (route + experts + shared + combine) and
+    1/lm_den of the lm_head rows. Weights are generated and quantised once,
+    outside the timed part; run() returns the time scaled to a full step, in
+    microseconds per token."""
+
+    def __init__(self, cfg_id, n_layers, lm_den, threads):
+        from gen import configs, gen
+        from oracle import oracle as orc
+        from oracle.workload import OracleLayer
+
+        self.orc = orc
+        self.c = c = configs.shape(cfg_id)
+        orc.set_threads(threads)
+        self.h0 = gen.hidden_bf16(c["T"], c["H"], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+        self.nl = min(n_layers, c["layers"])
+        self.layers = []
+        h = self.h0
+        for l in range(self.nl):
+            OL = OracleLayer(c["seed"], l, c["H"], c["I"], c["S"], c["E"], c["bias"])
+            h, _, _ = OL.forward(h, c["K"], c["w4a4"], True)
+            self.layers.append(OL)
+        self.rows = 0
+        if c["lm_head"]:
+            self.rows = c["V"] // lm_den
+            master = gen.lm_head_master(c["seed"], c["V"], c["H"], 0, self.rows)
+            cc, ss, gg = orc.quantize(master, orc.PER_TENSOR)
+            self.W = orc.Mat(cc, ss, gg[0])
+        self.desc = (f"{self.nl} of {c['layers']} MoE layers (route+experts+shared+combine) and "
+                     f"{self.rows} of {c['V']} lm_head rows at T={c['T']}, scaled to a full step")
+
+    def run(self):
+        c, orc = self.c, self.orc
+        h = self.h0
+        t0 = time.perf_counter()
+        for OL in self.layers:
+            r = OL.route(h, c["K"])
+            h, _ = orc.moe_layer(h, r["idx"], r["w"], OL.up, OL.down, OL.sh_up, OL.sh_down,
+                                 c["w4a4"], True, c["E"])
+        t_layers = time.perf_counter() - t0
+        t_lm = 0.0
+        if self.rows:
+            t0 = time.perf_counter()
+            orc.lm_head(self.W, h)
+            t_lm = time.perf_counter() - t0
+        per_step = t_layers / self.nl * c["layers"] + (t_lm * c["V"] / self.rows if self.rows else 0)
+        return per_step / c["T"] * 1e6, t_layers + t_lm
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    threads = len(os.sched_getaffinity(0))
+    sample = OracleSample(args.config, 1, 32, threads)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, _ = sample.run()
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    c = sample.c
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": value * c["T"] / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": c["name"], "T": c["T"], "layers": c["layers"], "hidden": c["H"],
+                       "experts": c["E"], "top_k": c["K"], "inter": c["I"], "shared_inter": c["S"],
+                       "vocab": c["V"] if c["lm_head"] else None, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample.desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, ws, rank, local):
+    import torch
+
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_quantized_moe_sigmoid_gb300 as nm
+    from nvfp4_quantized_moe_sigmoid_gb300 import roofline as rf
+    from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
+    from gen import configs, fill
+
+    c = configs.shape(args.config)
+    T, L, E, H, I, S, K, V = c["T"], c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], c["V"]
+    st = MoEDecodeStack(L, E, H, I, S, K, T, w4a4=c["w4a4"], V=V if c["lm_head"] else None)
+    st.register(*fill.fillers(c["seed"], c["bias"]))
+    fill.hidden(st.h[0], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+    h0 = st.h[0].clone()
+    torch.cuda.synchronize()
+    st.capture()
+    stream = torch.cuda.current_stream()
+
+    # warm-up
+    for _ in range(args.warmup):
+        st.replay()
+    torch.cuda.synchronize()
+    uniques = st.unique_experts()
+    assert nm.nvfp4_last_device_error() == 0
+
+    # timed region: K graph replays between events on the replay stream
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(physical_gpu_index(local)) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            st.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), ws)
+    ms_step = ms_total / args.steps
+    us_token = ms_step * 1e3 / (T * ws)  # whole job: ws replicas each ran T tokens per step
+    step_b = rf.step_bytes(T, uniques, E, H, I, S, K, V if c["lm_head"] else None)
+    peak, peak_kind = measured_peaks()
+    gbs_step = step_b / (ms_step * 1e-3) / 1e9
+
+    # per-call timing of the dominant call (eager, same stream, same kernels)
+    call_ms, lm_ms = [], []
+    for rep in range(3):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * L + 2)]
+        for l, Lw in enumerate(st.layers):
+            nm.moe_route_topk(st.h[l], Lw.router_w, Lw.router_b, K, st.topk_idx[l], st.topk_w[l])
+            evs[2 * l].record(stream)
+            nm.moe_expert_forward(Lw, st.h[l], st.topk_idx[l], st.topk_w[l], st.mode,
+                                  residual=st.h[l], out=st.h[l + 1], workspace=st.ws)
+            evs[2 * l + 1].record(stream)
+        if c["lm_head"]:
+            evs[2 * L].record(stream)
+            nm.lm_head_gemv(st.lm, st.h[L], st.logits)
+            evs[2 * L + 1].record(stream)
+        torch.cuda.synchronize()
+        if rep > 0:
+            call_ms += [evs[2 * l].elapsed_time(evs[2 * l + 1]) for l in range(L)]
+            if c["lm_head"]:
+                lm_ms.append(evs[2 * L].elapsed_time(evs[2 * L + 1]))
+    call_b = statistics.mean(rf.expert_call_bytes(T, u, H, I, S, K) for u in uniques)
+    call_avg_ms = statistics.mean(call_ms)
+    roof = {"bound": "hbm", "kernel": "moe_expert_forward (up + down kernels, per layer)",
+            "achieved": call_b / (call_avg_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+            "frac": None, "traffic": None, "algorithmic_bytes": call_b,
+            "avg_launch_us": call_avg_ms * 1e3, "peak_kind": peak_kind}
+    roof["frac"] = roof["achieved"] / peak
+    extra = {}
+    if lm_ms:
+        lb = rf.lm_head_bytes(T, V, H)
+        lmm = statistics.mean(lm_ms)
+        extra["lm_head"] = {"avg_us": lmm * 1e3, "achieved_gbs": lb / (lmm * 1e-3) / 1e9,
+                            "frac": lb / (lmm * 1e-3) / 1e9 / peak}
+
+    # end to end through the API: pinned host input -> step -> pinned host logits
+    e2e = None
+    if not args.no_e2e:
+        h_host = h0.cpu().pin_memory()
+        out_dev = st.logits if c["lm_head"] else st.h[L]
+        out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+        for _ in range(3):
+            st.h[0].copy_(h_host, non_blocking=True)
+            st.replay()
+            out_host.copy_(out_dev, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(args.steps):
+            st.h[0].copy_(h_host, non_blocking=True)
+            st.replay()
+            out_host.copy_(out_dev, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier(ws)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws) / args.steps
+        e2e = {"value": e2e_ms * 1e3 / (T * ws), "unit": UNIT,
+               "h2d_bytes_per_step": h_host.numel() * h_host.element_size(),
+               "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
+               "wall_us_per_step": wall / args.steps * 1e6}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = len(os.sched_getaffinity(0))
+        sample = OracleSample(args.config, 3, 8, threads)
+        v, secs = sample.run()
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample.desc,
+               "seconds": secs}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": us_token, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4(e2m1,e4m3)->f16 mma, f32 acc",
+                "data": "synthetic",
+                "config": {"workload": c["name"], "T": T, "layers": L, "hidden": H, "experts": E,
+                           "top_k": K, "inter": I, "shared_inter": S,
+                           "vocab": V if c["lm_head"] else None, "mode": "W4A4" if c["w4a4"] else "W4A16",
+                           "parallelism": "replicas" if ws > 1 else "single",
+                           "l2": "inputs larger than L2: each step streams %.2f GB vs 129 MB L2" % (step_b / 1e9),
+                           "graph": "one CUDA graph per step"},
+                "step_gbs": gbs_step, "step_frac_of_measured_hbm": gbs_step / peak,
+                "step_frac_of_8tbs": gbs_step / NOMINAL_HBM_GBS, "step_bytes": step_b,
+                "unique_experts_per_layer": uniques,
+                "roofline": roof, "cpu_baseline": cpu, "clocks": clk.summary(), "e2e": e2e,
+                "gpu_launches": args.steps * (3 * L + (1 if c["lm_head"] else 0)), **extra}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * nvfp4moe.h - C ABI of libnvfp4moe.so: the decode hot path of an
+ * NVFP4-quantised, sigmoid-routed Mixture-of-Experts layer and the NVFP4
+ * weight-only lm_head, as hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Sources (web pages on serving an NVFP4 Nemotron-3.5 MoE model):
+ *   [worklog]   "Let's optimize Nemotron 3.5 Lightning - a worklog": Step 1
+ *               (NVFP4: 4-bit values, group size 16; W4A16 keeps 16-bit
+ *               activations), Step 3 (routed experts W4A4 with dynamic NVFP4
+ *               activations), Step 4 (NVFP4 weight-only lm_head,
+ *               131072 x 2688), Interlude (batch-1 decode is a weight stream).
+ *   [card-w4a4] "nemotron35-w4a4-v13" model card, precision table.
+ *   [card-int4] "NVIDIA-Nemotron-3.5-Lightning-30B-A3B-W4A16" model card,
+ *               "Checkpoint layout" (per-expert up_proj / down_proj, no
+ *               gate_proj) and "Left at bfloat16" (router .gate and its fp32
+ *               e_score_correction_bias).
+ *   [super-q]   "Quantization (PTQ + QAD)", Precision Recipes (router compute
+ *               FP32; MoE and shared-expert GEMMs NVFP4) and Deployment
+ *               (Blackwell runs W4A4).
+ *
+ * NVFP4 tensor (the canonical layout every call takes), for a matrix of n rows
+ * and k columns (k % 16 == 0, element (r, c) = row r, reduction index c):
+ *   codes  uint8 [n][k/2]   E2M1 codes, element 2j in the low nibble of byte j
+ *   scales uint8 [n][k/16]  E4M3 (OCP "FN") scale of each 16-element block
+ *   global float [1]        per-tensor scale (per row for activations)
+ *   value(r, c) = E2M1(code) * E4M3(scale[r][c/16]) * global
+ * Quantisation rule (the pages name the format and block size; the scale
+ * formulas are this library's reading, stated once here):
+ *   global  = amax(tensor) / (6 * 448)
+ *   scale_b = E4M3_rn_satfinite( (amax(block b) / 6) / global )
+ *   code_i  = E2M1_rn_satfinite( x_i / (E4M3(scale_b) * global) )
+ * each step one IEEE binary32 operation, ties to even; a block whose
+ * E4M3(scale_b) * global is 0 gets codes 0; the sign of a value that rounds
+ * to 0 is kept (code 0x8).
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device pointers; the caller owns every
+ *     buffer. The library never allocates or frees memory.
+ *   - Every call is asynchronous on `stream`; arguments are checked on the host
+ *     before anything is launched, and a rejected call launches nothing.
+ *   - bf16 tensors are __nv_bfloat16 passed as `const void*` / `void*`.
+ *   - Returned status codes are below; NVFP4_ERR_CUDA means a launch failed
+ *     (cudaGetLastError() holds the CUDA error).
+ *   - Device-side waits are bounded (1 s); a wait that expires makes its kernel
+ *     stop early and sets a device error word, read by nvfp4_last_device_error.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside what the kernels handle */
+    NVFP4_ERR_MISALIGNED = 3,        /* a pointer breaks the stated alignment */
+    NVFP4_ERR_WORKSPACE = 4,         /* workspace too small */
+    NVFP4_ERR_CUDA = 5,              /* a CUDA launch failed */
+    NVFP4_ERR_TIMEOUT = 6            /* a bounded device wait expired */
+} nvfp4_status;
+
+typedef enum {
+    NVFP4_GLOBAL_PER_TENSOR = 0, /* one global for the whole tensor (weights)   */
+    NVFP4_GLOBAL_PER_ROW = 1,    /* one global per row (dynamic activations)    */
+    NVFP4_GLOBAL_GIVEN = 2       /* global supplied by the caller               */
+} nvfp4_global_mode;
+
+typedef enum {
+    NVFP4_W4A16 = 0, /* weights NVFP4, activations bf16 ([worklog] Step 1)        */
+    NVFP4_W4A4 = 1   /* weights and activations NVFP4 ([worklog] Step 3)          */
+} nvfp4_act_mode;
+
+/* One NVFP4 matrix in the canonical layout; all three pointers are device
+ * pointers; codes and scales 16-byte aligned. */
+typedef struct {
+    const uint8_t* codes;        /* [n][k/2]  */
+    const uint8_t* scales;       /* [n][k/16] */
+    const float* global_scale;   /* [1]       */
+    int64_t n, k;
+} nvfp4_matrix;
+
+/* The weights of one MoE layer ([card-int4] "Checkpoint layout": routed experts
+ * have up_proj [inter][hidden] and down_proj [hidden][inter], no gate_proj;
+ * one shared expert). Routed expert tensors are stacked along a leading
+ * expert axis; each expert matrix has its own per-tensor global. Device
+ * pointers, codes/scales 16-byte aligned. */
+typedef struct {
+    int32_t num_experts;          /* E (128 in the pages' model)         */
+    int32_t hidden;               /* H (2688)                            */
+    int32_t inter;                /* I, routed intermediate (1856)       */
+    int32_t shared_inter;         /* S, shared intermediate              */
+    const uint8_t* up_codes;      /* [E][I][H/2]   */
+    const uint8_t* up_scales;     /* [E][I][H/16]  */
+    const float* up_global;       /* [E]           */
+    const uint8_t* down_codes;    /* [E][H][I/2]   */
+    const uint8_t* down_scales;   /* [E][H][I/16]  */
+    const float* down_global;     /* [E]           */
+    nvfp4_matrix shared_up;       /* [S][H] */
+    nvfp4_matrix shared_down;     /* [H][S] */
+} moe_layer_weights;
+
+/*
+ * nvfp4_quantize - NVFP4 quantisation of a row-major matrix x[rows][cols]
+ * ([worklog] Step 1 format; per-row dynamic mode = [worklog] Step 3
+ * "nvfp4_dynamic" activations). Used for weight registration (per tensor) and
+ * for activations (per row).
+ *   x            device, [rows][cols] bf16 (x_is_bf16 = 1) or float32 (0),
+ *                16-byte aligned
+ *   rows, cols   rows >= 0, cols > 0, cols % 16 == 0
+ *   mode         PER_TENSOR: writes global_scale[0]; PER_ROW: writes
+ *                global_scale[rows]; GIVEN: reads global_scale[0]
+ *   codes        device out, [rows][cols/2], 8-byte aligned
+ *   scales       device out, [rows][cols/16]
+ * PER_TENSOR uses global_scale[0] as reduction scratch while it runs.
+ * Codes and scales are bit-exact with the rule in the file header.
+ */
+nvfp4_status nvfp4_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t cols,
+                            nvfp4_global_mode mode, float* global_scale, uint8_t* codes,
+                            uint8_t* scales, cudaStream_t stream);
+
+/*
+ * moe_route_topk - sigmoid router with correction bias ([card-int4] "Left at
+ * bfloat16": .gate and fp32 e_score_correction_bias; [super-q] router compute
+ * FP32), for T tokens:
+ *   z_e = sum_i h_i Wg[e][i] (FP32); sigma_e = 1 / (1 + exp(-z_e));
+ *   select the k largest sigma_e + bias_e (an exact tie goes to the lower
+ *   index), in descending order;
+ *   topk_w[j] = sigma_{e_j} / sum_l sigma_{e_l}.
+ *   hidden    device bf16 [T][H], 16-byte aligned
+ *   router_w  device float [E][H], 16-byte aligned
+ *   bias      device float [E]
+ *   T >= 1, H % 16 == 0, 1 <= k <= E <= 256, k <= 32
+ *   topk_idx  device out int32 [T][k];  topk_w device out float [T][k]
+ */
+nvfp4_status moe_route_topk(const void* hidden, const float* router_w, const float* bias,
+                            int32_t T, int32_t H, int32_t E, int32_t k, int32_t* topk_idx,
+                            float* topk_w, cudaStream_t stream);
+
+/*
+ * moe_expert_forward_workspace_size - bytes of device workspace that
+ * moe_expert_forward needs for these weights, T tokens, top-k and mode.
+ */
+size_t moe_expert_forward_workspace_size(const moe_layer_weights* w, int32_t T, int32_t k,
+                                         nvfp4_act_mode mode);
+
+/*
+ * moe_expert_forward_workspace_init - zero a workspace before its first use.
+ * moe_expert_forward keeps a small region of counters in the workspace and
+ * leaves it zeroed when a call completes normally; after a call that reported
+ * NVFP4_ERR_TIMEOUT, initialise the workspace again.
+ */
+nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace_bytes,
+                                               cudaStream_t stream);
+
+/*
+ * moe_expert_forward - routed experts + shared expert + combine of one MoE
+ * layer for T tokens, given the routing:
+ *   per token t, choice j, expert e = topk_idx[t][j]:
+ *     u = up_e . x_t            (x_t: bf16 hidden row, or its per-row NVFP4
+ *                                quantisation in W4A4)
+ *     a = bf16(max(u, 0)^2)     (relu^2; bf16 intermediate)
+ *     y = down_e . a'           (a': a, or its per-row NVFP4 quantisation)
+ *   out_t = bf16( shared(x_t) + sum_j topk_w[t][j] * y_{t,j} [+ residual_t] )
+ * with FP32 accumulation and one bf16 rounding at the end ([card-int4]
+ * "Checkpoint layout" for the non-gated MLP; [super-q] for NVFP4 on the
+ * shared expert too).
+ *   w          weights (host struct holding device pointers); shapes must
+ *              satisfy hidden, inter, shared_inter % 64 == 0
+ *   hidden     device bf16 [T][H], 16-byte aligned
+ *   topk_idx   device int32 [T][k], entries in [0, E) and distinct per token
+ *   topk_w     device float [T][k]
+ *   T >= 1, 1 <= k <= min(E, 16)
+ *   residual   device bf16 [T][H] or NULL
+ *   out        device bf16 [T][H]; may alias residual, must not alias hidden
+ *              unless hidden == residual
+ *   workspace  device, >= moe_expert_forward_workspace_size() bytes,
+ *              256-byte aligned, zeroed once by
+ *              moe_expert_forward_workspace_init; calls that share a
+ *              workspace must not overlap in time
+ */
+nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
+                                const int32_t* topk_idx, const float* topk_w, int32_t T,
+                                int32_t k, nvfp4_act_mode mode, const void* residual, void* out,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * lm_head_gemv - NVFP4 weight-only lm_head ([worklog] Step 4; [card-w4a4]
+ * "lm_head NVFP4 weight-only (W4A16)"):
+ *   logits[t][v] = sum_j W[v][j] * h[t][j], FP32 accumulation and output.
+ *   w        NVFP4 matrix [V][H] (device pointers), V % 16 == 0, H % 64 == 0
+ *   hidden   device bf16 [T][H], 16-byte aligned;  T >= 1
+ *   logits   device float [T][V]
+ */
+nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, float* logits,
+                          cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* nvfp4_status_string(nvfp4_status status);
+
+/* Synchronises `stream`, then reads and clears the device error word: returns
+ * NVFP4_ERR_TIMEOUT if a bounded device wait expired since the last read,
+ * NVFP4_ERR_CUDA if the synchronisation itself failed, else NVFP4_OK. */
+nvfp4_status nvfp4_last_device_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

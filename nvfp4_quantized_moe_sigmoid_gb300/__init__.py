@@ -1,0 +1,187 @@
+"""Python binding of libnvfp4moe.so: the NVFP4 sigmoid-routed MoE decode path
+and the NVFP4 weight-only lm_head as sm_103a CUDA kernels.
+
+The functions below carry the C-ABI names of include/nvfp4moe.h and only
+marshal arguments: torch CUDA tensors provide device memory and the current
+stream, every step of the computation runs in the library's kernels. There is
+no CPU or PyTorch fallback; importing this package without the built library
+raises ImportError.
+"""
+import ctypes
+
+import torch
+
+from . import _abi
+
+__all__ = ["NVFP4Matrix", "MoELayer", "NVFP4Error", "nvfp4_quantize", "moe_route_topk",
+           "moe_expert_forward_workspace_size", "moe_expert_forward_workspace_init",
+           "moe_expert_forward", "lm_head_gemv", "nvfp4_status_string", "nvfp4_last_device_error",
+           "W4A16", "W4A4", "PER_TENSOR", "PER_ROW", "GIVEN", "lib"]
+
+W4A16, W4A4 = 0, 1
+PER_TENSOR, PER_ROW, GIVEN = 0, 1, 2
+
+_L = _abi.load()
+
+
+def lib():
+    return _L
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {_abi.STATUS.get(status, status)} "
+                         f"({_L.nvfp4_status_string(status).decode()})")
+
+
+def _check(status, what):
+    if status != 0:
+        raise NVFP4Error(status, what)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def nvfp4_status_string(status: int) -> str:
+    return _L.nvfp4_status_string(int(status)).decode()
+
+
+def nvfp4_last_device_error(stream=None) -> int:
+    return _L.nvfp4_last_device_error(_stream(stream))
+
+
+class NVFP4Matrix:
+    """An NVFP4 matrix [n][k] in the canonical layout (device tensors)."""
+
+    def __init__(self, codes, scales, global_scale):
+        self.codes, self.scales, self.global_scale = codes, scales, global_scale
+        self.n, self.k = codes.shape[-2], codes.shape[-1] * 2
+
+    @staticmethod
+    def empty(n, k, device="cuda"):
+        return NVFP4Matrix(torch.empty((n, k // 2), dtype=torch.uint8, device=device),
+                           torch.empty((n, k // 16), dtype=torch.uint8, device=device),
+                           torch.empty(1, dtype=torch.float32, device=device))
+
+    def c(self):
+        return _abi.NVFP4Matrix(self.codes.data_ptr(), self.scales.data_ptr(),
+                                self.global_scale.data_ptr(), self.n, self.k)
+
+    def nbytes(self):
+        return self.codes.numel() + self.scales.numel()
+
+
+class MoELayer:
+    """Device weights of one MoE layer: router (fp32 gate + fp32 bias), stacked
+    routed experts (NVFP4 up [E][I][H], down [E][H][I]) and one shared expert."""
+
+    def __init__(self, E, H, I, S, device="cuda"):
+        self.E, self.H, self.I, self.S = E, H, I, S
+        u8 = dict(dtype=torch.uint8, device=device)
+        self.router_w = torch.empty((E, H), dtype=torch.float32, device=device)
+        self.router_b = torch.empty(E, dtype=torch.float32, device=device)
+        self.up_codes = torch.empty((E, I, H // 2), **u8)
+        self.up_scales = torch.empty((E, I, H // 16), **u8)
+        self.up_global = torch.empty(E, dtype=torch.float32, device=device)
+        self.down_codes = torch.empty((E, H, I // 2), **u8)
+        self.down_scales = torch.empty((E, H, I // 16), **u8)
+        self.down_global = torch.empty(E, dtype=torch.float32, device=device)
+        self.shared_up = NVFP4Matrix.empty(S, H, device)
+        self.shared_down = NVFP4Matrix.empty(H, S, device)
+        self._c = None
+
+    def expert_up(self, e):
+        return NVFP4Matrix(self.up_codes[e], self.up_scales[e], self.up_global[e:e + 1])
+
+    def expert_down(self, e):
+        return NVFP4Matrix(self.down_codes[e], self.down_scales[e], self.down_global[e:e + 1])
+
+    def c(self):
+        if self._c is None:
+            self._c = _abi.MoeLayerWeights(
+                self.E, self.H, self.I, self.S,
+                self.up_codes.data_ptr(), self.up_scales.data_ptr(), self.up_global.data_ptr(),
+                self.down_codes.data_ptr(), self.down_scales.data_ptr(), self.down_global.data_ptr(),
+                self.shared_up.c(), self.shared_down.c())
+        return self._c
+
+
+# ------------------------------------------------------------------ calls
+def nvfp4_quantize(x, mode=PER_TENSOR, out: NVFP4Matrix = None, global_scale=None, stream=None):
+    """Quantise x [rows][cols] (bf16 or float32, CUDA) to NVFP4. PER_ROW gives
+    one global per row. Returns an NVFP4Matrix (global_scale [1] or [rows])."""
+    x = x.contiguous()
+    rows, cols = x.shape
+    if out is None:
+        out = NVFP4Matrix.empty(rows, cols, x.device)
+        if mode == PER_ROW:
+            out.global_scale = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if mode == GIVEN:
+        out.global_scale.copy_(global_scale)
+    st = _L.nvfp4_quantize(_ptr(x), int(x.dtype == torch.bfloat16), rows, cols, mode,
+                           _ptr(out.global_scale), _ptr(out.codes), _ptr(out.scales), _stream(stream))
+    _check(st, "nvfp4_quantize")
+    return out
+
+
+def moe_route_topk(hidden, router_w, bias, k, topk_idx=None, topk_w=None, stream=None):
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=hidden.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=hidden.device)
+    st = _L.moe_route_topk(_ptr(hidden), _ptr(router_w), _ptr(bias), T, H, E, k, _ptr(topk_idx),
+                           _ptr(topk_w), _stream(stream))
+    _check(st, "moe_route_topk")
+    return topk_idx, topk_w
+
+
+def moe_expert_forward_workspace_size(layer: MoELayer, T, k, mode=W4A4) -> int:
+    w = layer.c()
+    return int(_L.moe_expert_forward_workspace_size(ctypes.byref(w), T, k, mode))
+
+
+def moe_expert_forward_workspace_init(workspace, stream=None):
+    _check(_L.moe_expert_forward_workspace_init(_ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_expert_forward_workspace_init")
+
+
+def make_workspace(layer: MoELayer, T, k, mode=W4A4, stream=None):
+    n = moe_expert_forward_workspace_size(layer, T, k, mode)
+    ws = torch.empty(n, dtype=torch.uint8, device=layer.up_codes.device)
+    moe_expert_forward_workspace_init(ws, stream)
+    return ws
+
+
+def moe_expert_forward(layer: MoELayer, hidden, topk_idx, topk_w, mode=W4A4, residual=None,
+                       out=None, workspace=None, stream=None):
+    T = hidden.shape[0]
+    k = topk_idx.shape[1]
+    if out is None:
+        out = torch.empty_like(hidden)
+    if workspace is None:
+        workspace = make_workspace(layer, T, k, mode, stream)
+    w = layer.c()
+    st = _L.moe_expert_forward(ctypes.byref(w), _ptr(hidden), _ptr(topk_idx), _ptr(topk_w), T, k,
+                               mode, _ptr(residual), _ptr(out), _ptr(workspace), workspace.numel(),
+                               _stream(stream))
+    _check(st, "moe_expert_forward")
+    return out
+
+
+def lm_head_gemv(w: NVFP4Matrix, hidden, logits=None, stream=None):
+    T = hidden.shape[0]
+    if logits is None:
+        logits = torch.empty((T, w.n), dtype=torch.float32, device=hidden.device)
+    m = w.c()
+    st = _L.lm_head_gemv(ctypes.byref(m), _ptr(hidden), T, _ptr(logits), _stream(stream))
+    _check(st, "lm_head_gemv")
+    return logits

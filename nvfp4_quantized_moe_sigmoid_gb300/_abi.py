@@ -1,0 +1,62 @@
+"""ctypes view of include/nvfp4moe.h. Loading fails loudly if the CUDA
+library has not been built: there is no fallback implementation."""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libnvfp4moe.so")
+
+P = ctypes.c_void_p
+I32, I64 = ctypes.c_int32, ctypes.c_int64
+
+EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_size",
+           "moe_expert_forward_workspace_init", "moe_expert_forward", "lm_head_gemv",
+           "nvfp4_status_string", "nvfp4_last_device_error"]
+
+STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED_SHAPE",
+          3: "NVFP4_ERR_MISALIGNED", 4: "NVFP4_ERR_WORKSPACE", 5: "NVFP4_ERR_CUDA",
+          6: "NVFP4_ERR_TIMEOUT"}
+
+
+class NVFP4Matrix(ctypes.Structure):
+    _fields_ = [("codes", P), ("scales", P), ("global_scale", P), ("n", I64), ("k", I64)]
+
+
+class MoeLayerWeights(ctypes.Structure):
+    _fields_ = [("num_experts", I32), ("hidden", I32), ("inter", I32), ("shared_inter", I32),
+                ("up_codes", P), ("up_scales", P), ("up_global", P),
+                ("down_codes", P), ("down_scales", P), ("down_global", P),
+                ("shared_up", NVFP4Matrix), ("shared_down", NVFP4Matrix)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libnvfp4moe.so is not built ({path}); run "
+                          "nvfp4_quantized_moe_sigmoid_gb300.build.build() first")
+    L = ctypes.CDLL(path)
+    L.nvfp4_quantize.argtypes = [P, ctypes.c_int, I64, I64, ctypes.c_int, P, P, P, P]
+    L.nvfp4_quantize.restype = ctypes.c_int
+    L.moe_route_topk.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P]
+    L.moe_route_topk.restype = ctypes.c_int
+    L.moe_expert_forward_workspace_size.argtypes = [ctypes.POINTER(MoeLayerWeights), I32, I32,
+                                                    ctypes.c_int]
+    L.moe_expert_forward_workspace_size.restype = ctypes.c_size_t
+    L.moe_expert_forward_workspace_init.argtypes = [P, ctypes.c_size_t, P]
+    L.moe_expert_forward_workspace_init.restype = ctypes.c_int
+    L.moe_expert_forward.argtypes = [ctypes.POINTER(MoeLayerWeights), P, P, P, I32, I32,
+                                     ctypes.c_int, P, P, P, ctypes.c_size_t, P]
+    L.moe_expert_forward.restype = ctypes.c_int
+    L.lm_head_gemv.argtypes = [ctypes.POINTER(NVFP4Matrix), P, I32, P, P]
+    L.lm_head_gemv.restype = ctypes.c_int
+    L.nvfp4_status_string.argtypes = [ctypes.c_int]
+    L.nvfp4_status_string.restype = ctypes.c_char_p
+    L.nvfp4_last_device_error.argtypes = [P]
+    L.nvfp4_last_device_error.restype = ctypes.c_int
+    _lib = L
+    return L

@@ -1,0 +1,225 @@
+// common.cuh - device helpers shared by the kernels of libnvfp4moe.so:
+// NVFP4 codecs (E2M1 values, E4M3 block scales), mbarrier + bulk-copy (TMA)
+// staging with bounded waits, and the f16 tensor-core MMA used by the GEMVs.
+//
+// Everything here is sm_103a inline PTX or plain CUDA; no vendor library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4moe {
+
+// Device error word (one per library instance): bounded waits that expire OR
+// a bit in here and stop their kernel early. Read and cleared by
+// nvfp4_last_device_error().
+__device__ unsigned int g_dev_error;
+
+enum : unsigned int {
+    kErrWaitFull = 1u,   // a consumer waited too long for a staged tile
+    kErrWaitEmpty = 2u,  // the producer waited too long for a free stage
+    kErrWaitDrain = 4u,  // copies still in flight at exit did not land
+    kErrBadInput = 8u,   // an expert index outside [0, E) or a broken plan
+};
+
+// 1 s: device waits in this library normally take microseconds.
+constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void set_dev_error(unsigned int bit) { atomicOr(&g_dev_error, bit); }
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait until phase `parity` of the barrier has completed; false after 1 s.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity) {
+    if (mbar_try_wait(b, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(b, parity)) return true;
+        if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
+// Bulk (non-tensor) TMA copy global -> this CTA's shared memory; completion is
+// signalled on `bar` as transaction bytes. dst, src 16-byte aligned; bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------- codecs
+// Four bytes of packed E2M1 pairs -> four f16x2 (byte b -> o[b]; in each byte
+// the low nibble becomes the low half). Exact.
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&o)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+
+// Two E4M3 bytes (low byte -> low half) -> f16x2. Exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+    uint32_t out;
+    uint16_t v = static_cast<uint16_t>(two_bytes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(v));
+    return out;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// {lo, lo} and {hi, hi} from an f16x2
+__device__ __forceinline__ uint32_t bcast_lo(uint32_t x) { return __byte_perm(x, x, 0x1010); }
+__device__ __forceinline__ uint32_t bcast_hi(uint32_t x) { return __byte_perm(x, x, 0x3232); }
+
+// E4M3 byte -> float (exact). Scales are never negative or NaN here.
+__device__ __forceinline__ float e4m3_to_float(uint32_t s) {
+    const uint32_t e = (s >> 3) & 15u, m = s & 7u;
+    return e == 0 ? static_cast<float>(m) * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Non-negative float -> E4M3 byte, round to nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t float_to_e4m3_pos(float v) {
+#if defined(NVFP4MOE_SOFT_CODECS)
+    if (!(v < 448.0f)) return 0x7Eu;
+    if (v < 0.015625f) return static_cast<uint32_t>(rintf(v * 512.0f));
+    const int e = static_cast<int>((__float_as_uint(v) >> 23) & 0xFFu) - 127;  // [-6, 8]
+    const float m = v * __uint_as_float(static_cast<uint32_t>(127 + 3 - e) << 23);  // [8, 16)
+    const uint32_t q = static_cast<uint32_t>(rintf(m));
+    return (static_cast<uint32_t>(e + 7) << 3) + (q - 8u);
+#else
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+    return r & 0xFFu;
+#endif
+}
+
+// Two floats -> one byte of E2M1 codes (x0 low nibble, x1 high nibble),
+// round to nearest even, saturating at 6, sign kept also for a zero result.
+__device__ __forceinline__ uint32_t float2_to_e2m1x2(float x0, float x1) {
+    const uint32_t sgn = ((__float_as_uint(x0) >> 28) & 0x8u) | ((__float_as_uint(x1) >> 24) & 0x80u);
+#if defined(NVFP4MOE_SOFT_CODECS)
+    auto mag = [](float x) -> uint32_t {
+        const float a = fabsf(x);
+        return (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) +
+               (a > 5.0f);
+    };
+    return (mag(x0) | (mag(x1) << 4)) | sgn;
+#else
+    uint16_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "mov.b16 %0, {t, 0};\n\t}"
+        : "=h"(r)
+        : "f"(fabsf(x1)), "f"(fabsf(x0)));
+    return (static_cast<uint32_t>(r) & 0xFFu) | sgn;
+#endif
+}
+
+// Quantise one 16-element block with global g (NVFP4 rule of nvfp4moe.h):
+//   s = E4M3((bamax / 6) / g); d = E4M3(s) * g; code_i = E2M1(x_i / d).
+// Returns the 8 code bytes in (lo, hi) and the scale byte.
+struct QBlock {
+    uint32_t lo, hi, scale;
+};
+__device__ __forceinline__ QBlock quantize_block16(const float (&x)[16], float g) {
+    float bamax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(x[i]));
+    uint32_t s = 0;
+    if (g > 0.0f) s = float_to_e4m3_pos(__fdiv_rn(__fdiv_rn(bamax, 6.0f), g));
+    const float d = __fmul_rn(e4m3_to_float(s), g);
+    QBlock q{0u, 0u, s};
+    if (d != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t byte = float2_to_e2m1x2(__fdiv_rn(x[2 * i], d), __fdiv_rn(x[2 * i + 1], d));
+            if (i < 4) q.lo |= byte << (8 * i);
+            else q.hi |= byte << (8 * (i - 4));
+        }
+    }
+    return q;
+}
+
+// Dequantised block values without the global (E2M1 * E4M3, exact in f16) as
+// eight f16x2 in element order.
+__device__ __forceinline__ void dequant_block16_f16(const QBlock& q, uint32_t (&o)[8]) {
+    const uint32_t sv = e4m3x2_to_f16x2(q.scale);  // low half = scale
+    const uint32_t s2 = bcast_lo(sv);
+    uint32_t a[4], b[4];
+    e2m1x8_to_f16x8(q.lo, a);
+    e2m1x8_to_f16x8(q.hi, b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[i] = hmul2(a[i], s2);
+        o[4 + i] = hmul2(b[i], s2);
+    }
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// ---------------------------------------------------------------- MMA
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col)
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+}  // namespace nvfp4moe

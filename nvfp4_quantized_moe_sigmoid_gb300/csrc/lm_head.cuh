@@ -1,0 +1,80 @@
+// lm_head.cuh - lm_head_gemv: NVFP4 weight-only lm_head ("Let's optimize
+// Nemotron 3.5 Lightning - a worklog", Step 4: the 131072 x 2688 vocabulary
+// matrix read once per step; "nemotron35-w4a4-v13" card, precision table:
+// lm_head NVFP4 weight-only W4A16).
+//
+// A pure HBM stream of the weight matrix: persistent CTAs each take a
+// contiguous range of 16-row tiles, one producer thread stages them with bulk
+// TMA copies, eight consumer warps run the tensor-core tile with up to 8 token
+// columns (bf16 activations converted once per CTA to f16).
+#pragma once
+
+#include "gemv_tile.cuh"
+
+namespace nvfp4moe {
+
+constexpr int kLmMaxT = 8;
+
+struct LmArgs {
+    const uint8_t* codes;   // [V][H/2]
+    const uint8_t* scales;  // [V][H/16]
+    const float* global;    // [1]
+    int64_t V;
+    int H;
+    const uint16_t* hidden;  // [T][H]
+    int T;                   // <= 8 per launch
+    float* logits;           // [T][ld]
+    int64_t ld;
+    int nstages, stage_bytes;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ Ring ring;
+    __shared__ const uint16_t* srcs[kLmMaxT];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ring_init(ring, a.nstages);
+    __syncthreads();
+
+    const int64_t N = a.V >> 4;
+    const int64_t ib = N * blockIdx.x / gridDim.x, ie = N * (blockIdx.x + 1) / gridDim.x;
+    const int n = static_cast<int>(ie - ib);
+    uint8_t* ring_base = smem;
+    __half* xb = reinterpret_cast<__half*>(smem + (size_t)a.nstages * a.stage_bytes);
+
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            for (int li = 0; li < n; ++li) {
+                const int64_t row = 16 * (ib + li);
+                if (!ring_fill(ring, ring_base, a.stage_bytes, a.nstages, li,
+                               a.codes + row * (a.H >> 1), a.scales + row * (a.H >> 4), a.H))
+                    break;
+            }
+        }
+    } else {
+        if (threadIdx.x < a.T) srcs[threadIdx.x] = a.hidden + (size_t)threadIdx.x * a.H;
+        consumer_bar();
+        prepare_b_rows<false>(srcs, a.T, a.H, xb, nullptr, nullptr);
+        const float gw = __ldg(a.global);
+        const int g = lane >> 2, q = lane & 3;
+        const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
+        for (int li = warp; li < n; li += kConsumerWarps) {
+            if (!ring_acquire(ring, a.nstages, li)) break;
+            const uint8_t* st = ring_base + (size_t)(li % a.nstages) * a.stage_bytes;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_mma_16x8(st, st + 16 * (a.H >> 1), a.H, bcol, acc);
+            ring_release(ring, a.nstages, li);
+            const int64_t row0 = 16 * (ib + li);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int t = 2 * q + (v & 1);
+                if (t < a.T) a.logits[(size_t)t * a.ld + row0 + g + 8 * (v >> 1)] = __fmul_rn(acc[v], gw);
+            }
+        }
+    }
+    __syncthreads();
+    ring_drain(ring, a.nstages);
+}
+
+}  // namespace nvfp4moe

@@ -1,0 +1,352 @@
+// nvfp4moe.cu - the C ABI of libnvfp4moe.so (declared in include/nvfp4moe.h):
+// argument checks on the host, launch configuration, and dispatch to the
+// kernels in the headers below. One translation unit, so that the device
+// error word is a single object.
+#include "nvfp4moe.h"
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "lm_head.cuh"
+#include "moe_decode.cuh"
+#include "quantize.cuh"
+#include "route.cuh"
+
+using namespace nvfp4moe;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+    int d = 0;
+    cudaGetDevice(&d);
+    return d;
+}
+
+int num_sms() {
+    static int cache[kMaxDevices] = {0};
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return 1;
+    if (cache[d] == 0) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d);
+        cache[d] = v > 0 ? v : 1;
+    }
+    return cache[d];
+}
+
+int smem_optin() {
+    static int cache[kMaxDevices] = {0};
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return 48 * 1024;
+    if (cache[d] == 0) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+        cache[d] = v > 0 ? v : 48 * 1024;
+    }
+    return cache[d];
+}
+
+// Largest dynamic shared memory a kernel may use (opt-in limit minus its
+// static shared memory); raises the kernel's limit to that value once per
+// device.
+template <typename Kernel>
+int dyn_smem_limit(Kernel k) {
+    static int cache[kMaxDevices] = {0};
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return 0;
+    if (cache[d] == 0) {
+        cudaFuncAttributes at;
+        if (cudaFuncGetAttributes(&at, k) != cudaSuccess) return 0;
+        const int lim = smem_optin() - static_cast<int>(at.sharedSizeBytes) - 64;
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, lim) != cudaSuccess)
+            return 0;
+        cache[d] = lim;
+    }
+    return cache[d];
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline nvfp4_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------ workspace
+struct DecodeWs {
+    size_t act, act_sh, ypart, ysh, tilecnt, total;
+};
+
+DecodeWs decode_ws(int T, int k, int H, int I, int S) {
+    DecodeWs w{};
+    size_t off = 0;
+    w.tilecnt = off;
+    off += align256(sizeof(int) * (size_t)(H / 16));
+    w.act = off;
+    off += align256((size_t)T * k * I * 2);
+    w.act_sh = off;
+    off += align256((size_t)T * S * 2);
+    w.ypart = off;
+    off += align256((size_t)T * k * H * 4);
+    w.ysh = off;
+    off += align256((size_t)T * H * 4);
+    w.total = off;
+    return w;
+}
+
+bool decode_path(const moe_layer_weights* w, int T, int k) {
+    return T >= 1 && T <= kDecodeMaxT && k <= kDecodeMaxK && w->num_experts <= 256;
+}
+
+nvfp4_status check_matrix(const nvfp4_matrix& m, int64_t n, int64_t k) {
+    if (!m.codes || !m.scales || !m.global_scale) return NVFP4_ERR_INVALID_ARG;
+    if (m.n != n || m.k != k) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(m.codes, 16) || !aligned(m.scales, 16)) return NVFP4_ERR_MISALIGNED;
+    return NVFP4_OK;
+}
+
+nvfp4_status check_layer(const moe_layer_weights* w) {
+    if (!w) return NVFP4_ERR_INVALID_ARG;
+    if (w->num_experts < 1 || w->hidden < 1 || w->inter < 1 || w->shared_inter < 1)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!w->up_codes || !w->up_scales || !w->up_global || !w->down_codes || !w->down_scales ||
+        !w->down_global)
+        return NVFP4_ERR_INVALID_ARG;
+    if (w->hidden % 64 || w->inter % 64 || w->shared_inter % 64) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(w->up_codes, 16) || !aligned(w->up_scales, 16) || !aligned(w->down_codes, 16) ||
+        !aligned(w->down_scales, 16))
+        return NVFP4_ERR_MISALIGNED;
+    nvfp4_status s = check_matrix(w->shared_up, w->shared_inter, w->hidden);
+    if (s != NVFP4_OK) return s;
+    return check_matrix(w->shared_down, w->hidden, w->shared_inter);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_status_string(nvfp4_status s) {
+    switch (s) {
+        case NVFP4_OK: return "ok";
+        case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+        case NVFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case NVFP4_ERR_MISALIGNED: return "misaligned pointer";
+        case NVFP4_ERR_WORKSPACE: return "workspace too small";
+        case NVFP4_ERR_CUDA: return "CUDA error";
+        case NVFP4_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+nvfp4_status nvfp4_last_device_error(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof(v)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return NVFP4_ERR_CUDA;
+        return NVFP4_ERR_TIMEOUT;
+    }
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t cols,
+                            nvfp4_global_mode mode, float* global_scale, uint8_t* codes,
+                            uint8_t* scales, cudaStream_t stream) {
+    if (!global_scale || rows < 0 || cols <= 0) return NVFP4_ERR_INVALID_ARG;
+    if (mode != NVFP4_GLOBAL_PER_TENSOR && mode != NVFP4_GLOBAL_PER_ROW && mode != NVFP4_GLOBAL_GIVEN)
+        return NVFP4_ERR_INVALID_ARG;
+    if (cols % 16) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) {
+        if (mode == NVFP4_GLOBAL_PER_TENSOR) {
+            if (cudaMemsetAsync(global_scale, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+        }
+        return NVFP4_OK;
+    }
+    if (!x || !codes || !scales) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(codes, 8)) return NVFP4_ERR_MISALIGNED;
+    const int64_t nblocks = rows * (cols / 16);
+    const int maxg = num_sms() * 8;
+    const int grid = static_cast<int>(std::min<int64_t>((nblocks + 255) / 256, maxg));
+    const bool bf16 = x_is_bf16 != 0;
+    if (mode == NVFP4_GLOBAL_PER_ROW) {
+        const int rgrid = static_cast<int>(std::min<int64_t>((rows + 7) / 8, maxg));
+        if (bf16) k_quantize_rows<true><<<rgrid, 256, 0, stream>>>(x, rows, cols, global_scale, codes, scales);
+        else k_quantize_rows<false><<<rgrid, 256, 0, stream>>>(x, rows, cols, global_scale, codes, scales);
+        return launch_status();
+    }
+    if (mode == NVFP4_GLOBAL_PER_TENSOR) {
+        if (cudaMemsetAsync(global_scale, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+        unsigned int* bits = reinterpret_cast<unsigned int*>(global_scale);
+        if (bf16) k_amax<true><<<grid, 256, 0, stream>>>(x, nblocks, bits);
+        else k_amax<false><<<grid, 256, 0, stream>>>(x, nblocks, bits);
+    }
+    const int from_amax = mode == NVFP4_GLOBAL_PER_TENSOR ? 1 : 0;
+    if (bf16) k_quantize_global<true><<<grid, 256, 0, stream>>>(x, nblocks, global_scale, from_amax, codes, scales);
+    else k_quantize_global<false><<<grid, 256, 0, stream>>>(x, nblocks, global_scale, from_amax, codes, scales);
+    if (mode == NVFP4_GLOBAL_PER_TENSOR) k_finalize_global<<<1, 1, 0, stream>>>(global_scale);
+    return launch_status();
+}
+
+nvfp4_status moe_route_topk(const void* hidden, const float* router_w, const float* bias, int32_t T,
+                            int32_t H, int32_t E, int32_t k, int32_t* topk_idx, float* topk_w,
+                            cudaStream_t stream) {
+    if (!hidden || !router_w || !bias || !topk_idx || !topk_w) return NVFP4_ERR_INVALID_ARG;
+    if (T < 1 || H < 16 || E < 1 || k < 1 || k > E) return NVFP4_ERR_INVALID_ARG;
+    if (H % 16 || E > 256 || k > 32) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(router_w, 16)) return NVFP4_ERR_MISALIGNED;
+    constexpr int TT = 8;
+    const int smem = TT * H * 2;
+    const int lim = dyn_smem_limit(k_route<TT>);
+    if (smem > lim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const int tiles = (T + TT - 1) / TT;
+    k_route<TT><<<tiles * kRouteCluster, kRouteWarps * 32, smem, stream>>>(
+        static_cast<const uint16_t*>(hidden), router_w, bias, T, H, E, k, topk_idx, topk_w);
+    return launch_status();
+}
+
+size_t moe_expert_forward_workspace_size(const moe_layer_weights* w, int32_t T, int32_t k,
+                                         nvfp4_act_mode mode) {
+    (void)mode;
+    if (!w || T < 1 || k < 1) return 0;
+    return decode_ws(T, k, w->hidden, w->inter, w->shared_inter).total;
+}
+
+nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace_bytes,
+                                               cudaStream_t stream) {
+    if (!workspace) return NVFP4_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, stream) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
+                                const int32_t* topk_idx, const float* topk_w, int32_t T, int32_t k,
+                                nvfp4_act_mode mode, const void* residual, void* out, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+    nvfp4_status st = check_layer(w);
+    if (st != NVFP4_OK) return st;
+    if (!hidden || !topk_idx || !topk_w || !out || !workspace) return NVFP4_ERR_INVALID_ARG;
+    if (T < 1 || k < 1 || k > w->num_experts) return NVFP4_ERR_INVALID_ARG;
+    if (mode != NVFP4_W4A16 && mode != NVFP4_W4A4) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(hidden, 16) || !aligned(out, 4) || !aligned(workspace, 256) ||
+        (residual && !aligned(residual, 4)))
+        return NVFP4_ERR_MISALIGNED;
+    if (hidden == out && residual != hidden) return NVFP4_ERR_INVALID_ARG;
+    if (!decode_path(w, T, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+
+    const int H = w->hidden, I = w->inter, S = w->shared_inter;
+    const DecodeWs ws = decode_ws(T, k, H, I, S);
+    if (workspace_bytes < ws.total) return NVFP4_ERR_WORKSPACE;
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    const bool w4a4 = mode == NVFP4_W4A4;
+    const int nsm = num_sms();
+    // enough CTAs that each one's item range spans at most two routed experts
+    const int grid = std::max(nsm, 2 * (T * k + (S + I - 1) / I) + 4);
+
+    UpArgs ua{};
+    ua.codes = w->up_codes;
+    ua.scales = w->up_scales;
+    ua.global = w->up_global;
+    ua.sh_codes = w->shared_up.codes;
+    ua.sh_scales = w->shared_up.scales;
+    ua.sh_global = w->shared_up.global_scale;
+    ua.E = w->num_experts;
+    ua.H = H;
+    ua.I = I;
+    ua.S = S;
+    ua.hidden = static_cast<const uint16_t*>(hidden);
+    ua.topk_idx = topk_idx;
+    ua.topk_w = topk_w;
+    ua.T = T;
+    ua.k = k;
+    ua.act = reinterpret_cast<uint16_t*>(wsb + ws.act);
+    ua.act_sh = reinterpret_cast<uint16_t*>(wsb + ws.act_sh);
+    ua.stage_bytes = 9 * H;
+    {
+        const int lim = w4a4 ? dyn_smem_limit(k_moe_up_decode<true>) : dyn_smem_limit(k_moe_up_decode<false>);
+        const int bbytes = T * H * 2;
+        ua.nstages = std::min(kMaxStages, (lim - bbytes) / ua.stage_bytes);
+        if (ua.nstages < 2) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        const int smem = ua.nstages * ua.stage_bytes + bbytes;
+        if (w4a4) k_moe_up_decode<true><<<grid, kThreads, smem, stream>>>(ua);
+        else k_moe_up_decode<false><<<grid, kThreads, smem, stream>>>(ua);
+        st = launch_status();
+        if (st != NVFP4_OK) return st;
+    }
+
+    DownArgs da{};
+    da.codes = w->down_codes;
+    da.scales = w->down_scales;
+    da.global = w->down_global;
+    da.sh_codes = w->shared_down.codes;
+    da.sh_scales = w->shared_down.scales;
+    da.sh_global = w->shared_down.global_scale;
+    da.E = w->num_experts;
+    da.H = H;
+    da.I = I;
+    da.S = S;
+    da.topk_idx = topk_idx;
+    da.topk_w = topk_w;
+    da.T = T;
+    da.k = k;
+    da.act = ua.act;
+    da.act_sh = ua.act_sh;
+    da.residual = static_cast<const uint16_t*>(residual);
+    da.out = static_cast<uint16_t*>(out);
+    da.ypart = reinterpret_cast<float*>(wsb + ws.ypart);
+    da.ysh = reinterpret_cast<float*>(wsb + ws.ysh);
+    da.tilecnt = reinterpret_cast<int*>(wsb + ws.tilecnt);
+    da.stage_bytes = 9 * std::max(I, S);
+    {
+        const int lim = w4a4 ? dyn_smem_limit(k_moe_down_decode<true>) : dyn_smem_limit(k_moe_down_decode<false>);
+        const int bbytes = (2 * T * I + T * S) * 2;
+        da.nstages = std::min(kMaxStages, (lim - bbytes) / da.stage_bytes);
+        if (da.nstages < 2) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        const int smem = da.nstages * da.stage_bytes + bbytes;
+        if (w4a4) k_moe_down_decode<true><<<grid, kThreads, smem, stream>>>(da);
+        else k_moe_down_decode<false><<<grid, kThreads, smem, stream>>>(da);
+        st = launch_status();
+    }
+    return st;
+}
+
+nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, float* logits,
+                          cudaStream_t stream) {
+    if (!w || !hidden || !logits || T < 1) return NVFP4_ERR_INVALID_ARG;
+    if (!w->codes || !w->scales || !w->global_scale || w->n < 16 || w->k < 64)
+        return NVFP4_ERR_INVALID_ARG;
+    if (w->n % 16 || w->k % 64 || w->k > (1 << 20)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(w->codes, 16) || !aligned(w->scales, 16) || !aligned(hidden, 16) || !aligned(logits, 4))
+        return NVFP4_ERR_MISALIGNED;
+    const int H = static_cast<int>(w->k);
+    LmArgs la{};
+    la.codes = w->codes;
+    la.scales = w->scales;
+    la.global = w->global_scale;
+    la.V = w->n;
+    la.H = H;
+    la.ld = w->n;
+    la.stage_bytes = 9 * H;
+    const int lim = dyn_smem_limit(k_lm_head);
+    const int bbytes = kLmMaxT * H * 2;
+    la.nstages = std::min(kMaxStages, (lim - bbytes) / la.stage_bytes);
+    if (la.nstages < 2) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const int smem = la.nstages * la.stage_bytes + bbytes;
+    const int64_t tiles = w->n / 16;
+    const int grid = static_cast<int>(std::min<int64_t>(num_sms(), tiles));
+    for (int t0 = 0; t0 < T; t0 += kLmMaxT) {
+        la.T = std::min(kLmMaxT, T - t0);
+        la.hidden = static_cast<const uint16_t*>(hidden) + (size_t)t0 * H;
+        la.logits = logits + (size_t)t0 * w->n;
+        k_lm_head<<<grid, kThreads, smem, stream>>>(la);
+        const nvfp4_status st = launch_status();
+        if (st != NVFP4_OK) return st;
+    }
+    return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+"""A stack of NVFP4 MoE layers plus the NVFP4 lm_head, resident in HBM, and the
+decode step that runs them through the C ABI:
+
+    for each layer l:  idx, w = moe_route_topk(h_l)
+                       h_{l+1} = moe_expert_forward(h_l, idx, w, residual=h_l)
+    logits = lm_head_gemv(h_L)
+
+("Let's optimize Nemotron 3.5 Lightning - a worklog": a decode step streams
+the active experts of every MoE layer and the lm_head; the chain keeps only
+the MoE layers and their residual adds.) Weights are registered once with
+nvfp4_quantize from bf16 masters supplied by the caller.
+"""
+import torch
+
+from . import (MoELayer, NVFP4Matrix, PER_TENSOR, W4A4, W4A16, lm_head_gemv, make_workspace,
+               moe_expert_forward, moe_route_topk, nvfp4_quantize)
+
+
+class MoEDecodeStack:
+    def __init__(self, layers, E, H, I, S, k, T, w4a4=True, V=None, device="cuda",
+                 weights_from=None):
+        """weights_from: another stack whose registered weights this one shares."""
+        self.L, self.E, self.H, self.I, self.S, self.k, self.T = layers, E, H, I, S, k, T
+        self.V = V
+        self.mode = W4A4 if w4a4 else W4A16
+        self.device = device
+        if weights_from is not None:
+            self.layers, self.lm = weights_from.layers, weights_from.lm
+        else:
+            self.layers = [MoELayer(E, H, I, S, device) for _ in range(layers)]
+            self.lm = NVFP4Matrix.empty(V, H, device) if V else None
+        self.h = torch.zeros((layers + 1, T, H), dtype=torch.bfloat16, device=device)
+        self.topk_idx = torch.zeros((layers, T, k), dtype=torch.int32, device=device)
+        self.topk_w = torch.zeros((layers, T, k), dtype=torch.float32, device=device)
+        self.logits = torch.zeros((T, V), dtype=torch.float32, device=device) if V else None
+        self.ws = None
+        self.graph = None
+
+    # ------------------------------------------------------------ weights
+    def register(self, fill_bf16, fill_router, fill_bias):
+        """fill_bf16(kind, layer, index, t) writes a bf16 master into t;
+        fill_router(layer, t) / fill_bias(layer, t) write the fp32 router."""
+        H, I, S = self.H, self.I, self.S
+        tmp = torch.empty(max(I * H, S * H), dtype=torch.bfloat16, device=self.device)
+        for l, Lw in enumerate(self.layers):
+            fill_router(l, Lw.router_w)
+            fill_bias(l, Lw.router_b)
+            for e in range(self.E):
+                m = tmp[:I * H].view(I, H)
+                fill_bf16("up", l, e, m)
+                nvfp4_quantize(m, PER_TENSOR, out=Lw.expert_up(e))
+                m = tmp[:H * I].view(H, I)
+                fill_bf16("down", l, e, m)
+                nvfp4_quantize(m, PER_TENSOR, out=Lw.expert_down(e))
+            m = tmp[:S * H].view(S, H)
+            fill_bf16("sh_up", l, 0, m)
+            nvfp4_quantize(m, PER_TENSOR, out=Lw.shared_up)
+            m = tmp[:H * S].view(H, S)
+            fill_bf16("sh_down", l, 0, m)
+            nvfp4_quantize(m, PER_TENSOR, out=Lw.shared_down)
+        if self.lm is not None:
+            full = torch.empty((self.V, H), dtype=torch.bfloat16, device=self.device)
+            fill_bf16("lm_head", 0, 0, full)
+            nvfp4_quantize(full, PER_TENSOR, out=self.lm)
+            del full
+        del tmp
+        self.make_workspace()
+
+    def make_workspace(self):
+        self.ws = make_workspace(self.layers[0], self.T, self.k, self.mode)
+
+    # ------------------------------------------------------------ the step
+    def step(self, stream=None):
+        """One decode step on self.h[0] -> self.h[L] (and logits)."""
+        for l, Lw in enumerate(self.layers):
+            moe_route_topk(self.h[l], Lw.router_w, Lw.router_b, self.k, self.topk_idx[l],
+                           self.topk_w[l], stream=stream)
+            moe_expert_forward(Lw, self.h[l], self.topk_idx[l], self.topk_w[l], self.mode,
+                               residual=self.h[l], out=self.h[l + 1], workspace=self.ws,
+                               stream=stream)
+        if self.lm is not None:
+            lm_head_gemv(self.lm, self.h[self.L], self.logits, stream=stream)
+
+    def capture(self):
+        """Capture one step in a CUDA graph (after one eager step)."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.step()
+        torch.cuda.synchronize()
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
+
+    # ------------------------------------------------------------ bytes
+    def unique_experts(self):
+        """Per layer, the number of distinct experts selected this step."""
+        idx = self.topk_idx.view(self.L, -1).cpu()
+        return [int(torch.unique(idx[l]).numel()) for l in range(self.L)]

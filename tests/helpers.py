@@ -1,0 +1,69 @@
+"""Shared helpers for the parity tests (test infrastructure)."""
+import os
+import re
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4moe.h")
+
+# floating-point parity bar: |gpu - ref| <= ATOL + RTOL * |ref|, elementwise
+ATOL, RTOL = 1e-2, 2e-2
+
+
+def header_functions():
+    """Names of the functions include/nvfp4moe.h declares."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-zA-Z_][\w\s\*]*?\b([a-z][a-z0-9_]+)\s*\(", src, re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "sizeof")))
+
+
+def bf16_bits(t):
+    """torch bf16 tensor -> numpy uint16 bit patterns."""
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().astype(np.uint16)
+
+
+def to_dev_bf16(a, device="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def bf16_to_f64(a):
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def assert_close(got, ref, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(got - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside {ATOL} + {RTOL}|ref|; "
+                           f"worst |err| {err.max():.4g} at {np.unravel_index(err.argmax(), err.shape)}")
+    return err.max()
+
+
+def check_routing(gpu_idx, gpu_w, orc, k):
+    """Routing parity: indices must equal the oracle's; a difference is allowed
+    only where the oracle's biased scores of the swapped experts are within
+    their binary32 error bounds (tau). Returns the number of exempted tokens."""
+    gpu_idx = np.asarray(gpu_idx)
+    T, E = orc["c"].shape
+    exempt = 0
+    for t in range(T):
+        gi = list(gpu_idx[t])
+        if gi == list(orc["idx"][t]):
+            np.testing.assert_allclose(gpu_w[t], orc["w"][t], rtol=1e-5, atol=1e-7)
+            continue
+        c, tau = orc["c"][t], orc["tau"][t]
+        assert len(set(gi)) == k and all(0 <= e < E for e in gi), f"token {t}: invalid {gi}"
+        inside = np.zeros(E, bool)
+        inside[gi] = True
+        lo = np.min(c[inside] + tau[inside])
+        hi = np.max(c[~inside] - tau[~inside]) if (~inside).any() else -np.inf
+        assert lo >= hi, f"token {t}: gpu set {gi} vs oracle {list(orc['idx'][t])} not a near-tie"
+        for a, b in zip(gi[:-1], gi[1:]):
+            assert c[a] + tau[a] >= c[b] - tau[b], f"token {t}: order {gi}"
+        exempt += 1
+    return exempt

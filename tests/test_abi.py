@@ -1,0 +1,106 @@
+"""The C-ABI library loads and exports every symbol include/nvfp4moe.h
+declares; host-side argument checks reject bad calls before any launch (no
+GPU is needed for these)."""
+import ctypes
+import os
+
+import pytest
+
+from tests.helpers import header_functions
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def abi():
+    import __graft_entry__
+    __graft_entry__.build()
+    from nvfp4_quantized_moe_sigmoid_gb300 import _abi
+    return _abi
+
+
+def test_header_lists_the_boundary():
+    names = header_functions()
+    for n in ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward", "lm_head_gemv",
+              "moe_expert_forward_workspace_size", "nvfp4_status_string",
+              "nvfp4_last_device_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(abi):
+    lib = ctypes.CDLL(abi.LIB_PATH)
+    for n in header_functions():
+        assert hasattr(lib, n), f"missing export {n}"
+    assert set(header_functions()) <= set(abi.EXPORTS)
+
+
+def test_status_strings(abi):
+    L = abi.load()
+    assert L.nvfp4_status_string(0) == b"ok"
+    assert L.nvfp4_status_string(6) == b"device wait timed out"
+    assert L.nvfp4_status_string(99) == b"unknown status"
+
+
+def test_host_validation_rejects_bad_arguments(abi):
+    L = abi.load()
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: calls are rejected first
+    odd = ctypes.c_void_p(0x10001)
+    # nvfp4_quantize: null global, bad cols, bad mode, misaligned input
+    assert L.nvfp4_quantize(fake, 1, 4, 32, 0, null, fake, fake, null) == 1
+    assert L.nvfp4_quantize(fake, 1, 4, 24, 0, fake, fake, fake, null) == 2
+    assert L.nvfp4_quantize(fake, 1, 4, 32, 7, fake, fake, fake, null) == 1
+    assert L.nvfp4_quantize(odd, 1, 4, 32, 0, fake, fake, fake, null) == 3
+    # moe_route_topk: k > E, H % 16, E > 256, misaligned hidden
+    assert L.moe_route_topk(fake, fake, fake, 1, 64, 8, 9, fake, fake, null) == 1
+    assert L.moe_route_topk(fake, fake, fake, 1, 72, 8, 2, fake, fake, null) == 2
+    assert L.moe_route_topk(fake, fake, fake, 1, 64, 300, 2, fake, fake, null) == 2
+    assert L.moe_route_topk(odd, fake, fake, 1, 64, 8, 2, fake, fake, null) == 3
+    assert L.moe_route_topk(null, fake, fake, 1, 64, 8, 2, fake, fake, null) == 1
+    # lm_head_gemv
+    m = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 100, 2688)
+    assert L.lm_head_gemv(ctypes.byref(m), fake, 1, fake, null) == 2
+    m = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 128, 2688)
+    assert L.lm_head_gemv(ctypes.byref(m), odd, 1, fake, null) == 3
+    assert L.lm_head_gemv(ctypes.byref(m), fake, 0, fake, null) == 1
+    # moe_expert_forward: shapes, workspace size, null weights
+    sh_up = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 3712, 2688)
+    sh_dn = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 2688, 3712)
+    w = abi.MoeLayerWeights(128, 2688, 1856, 3712, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000,
+                            0x10000, sh_up, sh_dn)
+    need = L.moe_expert_forward_workspace_size(ctypes.byref(w), 1, 6, 1)
+    assert need > 0
+    assert L.moe_expert_forward(ctypes.byref(w), fake, fake, fake, 1, 6, 1, null, ctypes.c_void_p(0x20000),
+                                ctypes.c_void_p(0x30000), need - 1, null) == 4
+    assert L.moe_expert_forward(ctypes.byref(w), fake, fake, fake, 1, 6, 5, null, ctypes.c_void_p(0x20000),
+                                ctypes.c_void_p(0x30000), need, null) == 1
+    bad = abi.MoeLayerWeights(128, 2688, 1850, 3712, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000,
+                              0x10000, sh_up, sh_dn)
+    assert L.moe_expert_forward(ctypes.byref(bad), fake, fake, fake, 1, 6, 1, null, fake, fake, need,
+                                null) == 2
+    nul = abi.MoeLayerWeights(128, 2688, 1856, 3712, 0, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000,
+                              sh_up, sh_dn)
+    assert L.moe_expert_forward(ctypes.byref(nul), fake, fake, fake, 1, 6, 1, null, fake, fake, need,
+                                null) == 1
+
+
+def test_workspace_size_grows_with_tokens(abi):
+    L = abi.load()
+    sh_up = abi.NVFP4Matrix(1, 1, 1, 3712, 2688)
+    sh_dn = abi.NVFP4Matrix(1, 1, 1, 2688, 3712)
+    w = abi.MoeLayerWeights(128, 2688, 1856, 3712, 1, 1, 1, 1, 1, 1, sh_up, sh_dn)
+    a = L.moe_expert_forward_workspace_size(ctypes.byref(w), 1, 6, 1)
+    b = L.moe_expert_forward_workspace_size(ctypes.byref(w), 4, 6, 1)
+    assert b > a > 6 * 1856 * 2
+
+
+def test_package_fails_loudly_without_library(abi, tmp_path):
+    with pytest.raises(ImportError):
+        abi.load.__wrapped__ if False else None
+        from nvfp4_quantized_moe_sigmoid_gb300 import _abi as a2
+        saved = a2._lib
+        a2._lib = None
+        try:
+            a2.load(str(tmp_path / "missing.so"))
+        finally:
+            a2._lib = saved

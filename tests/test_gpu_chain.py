@@ -1,0 +1,88 @@
+"""The full-depth decode step at the pages' sizes (23 W4A4 MoE layers +
+131072 x 2688 lm_head), in the launch configuration the benchmark times.
+
+Teacher forcing runs from the oracle to the GPU only: the oracle runs its own
+chain h_0 -> h_23; for every layer the GPU is given the oracle's h_l and must
+reproduce the oracle's routing (bit-exact up to near-ties) and h_{l+1}
+(within tolerance); the lm_head is checked on the oracle's h_23 at sampled
+rows. The free-running GPU chain (CUDA graph, as timed) must reproduce layer 0
+bit-for-bit against the teacher-forced call and stay finite."""
+import numpy as np
+import pytest
+import torch
+
+from gen import configs, fill, gen
+from oracle import oracle as orc
+from oracle.workload import OracleLayer
+from tests.gpu_fixtures import nm  # noqa: F401
+from tests.helpers import assert_close, bf16_bits, bf16_to_f64, check_routing, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def stack(nm):
+    from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
+    c = configs.shape(1)
+    st = MoEDecodeStack(c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], 4, w4a4=True, V=c["V"])
+    st.register(*fill.fillers(c["seed"], c["bias"]))
+    torch.cuda.synchronize()
+    return c, st
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_chain_teacher_forced(nm, stack, cfg):
+    c0, st = stack
+    c = configs.shape(cfg)
+    T = c["T"]
+    h = gen.hidden_bf16(T, c["H"], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+    ws = nm.make_workspace(st.layers[0], T, c["K"], nm.W4A4)
+    exempt = 0
+    for l in range(c["layers"]):
+        OL = OracleLayer(c["seed"], l, c["H"], c["I"], c["S"], c["E"], c["bias"])
+        ref, _, r = OL.forward(h, c["K"], True, True)
+        hd = to_dev_bf16(h)
+        idx, w = nm.moe_route_topk(hd, st.layers[l].router_w, st.layers[l].router_b, c["K"])
+        torch.cuda.synchronize()
+        e = check_routing(idx.cpu().numpy(), w.cpu().numpy(), r, c["K"])
+        exempt += e
+        if e == 0:
+            out = nm.moe_expert_forward(st.layers[l], hd, idx, w, nm.W4A4, residual=hd, workspace=ws)
+            torch.cuda.synchronize()
+            assert_close(bf16_to_f64(bf16_bits(out)), bf16_to_f64(ref), f"layer {l}")
+        h = ref
+    assert exempt <= 1
+    assert nm.nvfp4_last_device_error() == 0
+    # lm_head on the oracle's final hidden state
+    V, H = c["V"], c["H"]
+    logits = nm.lm_head_gemv(st.lm, to_dev_bf16(h)).cpu().numpy()
+    rows = np.unique(np.concatenate([np.arange(16), np.random.default_rng(2).integers(0, V, 512)]))
+    host = gen.lm_head_master(c["seed"], V, H)
+    g = np.float32(np.abs(gen.bf16_bits_to_f32(host)).max()) / np.float32(2688.0)
+    cc, ss, _ = orc.quantize(host[rows], orc.GIVEN, g=float(g))
+    assert_close(logits[:, rows], orc.lm_head(orc.Mat(cc, ss, g), h), "logits")
+
+
+def test_free_running_graph(nm, stack):
+    from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
+    c0, st4 = stack
+    c = configs.shape(1)
+    st = MoEDecodeStack(c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], 1, w4a4=True, V=c["V"],
+                        weights_from=st4)
+    st.make_workspace()
+    h0 = gen.hidden_bf16(1, c["H"], c["seed"], layer=configs.HIDDEN_LAYER)
+    st.h[0].copy_(to_dev_bf16(h0))
+    st.capture()
+    st.replay()
+    torch.cuda.synchronize()
+    first = st.h[1].clone()
+    st.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), st.h[1].view(torch.int16)), "replay not deterministic"
+    assert torch.isfinite(st.logits).all()
+    hd = to_dev_bf16(h0)
+    idx, w = nm.moe_route_topk(hd, st.layers[0].router_w, st.layers[0].router_b, c["K"])
+    out = nm.moe_expert_forward(st.layers[0], hd, idx, w, nm.W4A4, residual=hd, workspace=st.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), first.view(torch.int16))
+    assert nm.nvfp4_last_device_error() == 0

@@ -1,0 +1,87 @@
+"""moe_expert_forward (and the route + expert layer) on the GPU against the
+oracle, elementwise within |err| <= 1e-2 + 2e-2 |ref|: small shapes with
+several tiles and partial token groups, and the pages' full layer shape
+(hidden 2688, 128 experts of 1856, shared 3712, top-6) at 1 and 4 tokens."""
+import numpy as np
+import pytest
+import torch
+
+from gen import configs, gen
+from oracle.workload import OracleLayer
+from tests.gpu_fixtures import dev_routing, device_layer, nm  # noqa: F401
+from tests.helpers import assert_close, bf16_bits, bf16_to_f64, check_routing, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+SMALL = dict(E=16, H=256, I=128, S=192)
+
+
+def run_layer(nm, L, OL, h, k, w4a4, residual, gpu_routing=False):
+    hd = to_dev_bf16(h)
+    r = OL.route(h, k)
+    if gpu_routing:
+        idx, w = nm.moe_route_topk(hd, L.router_w, L.router_b, k)
+        torch.cuda.synchronize()
+        check_routing(idx.cpu().numpy(), w.cpu().numpy(), r, k)
+        assert np.array_equal(idx.cpu().numpy(), r["idx"]), "near-tie flip: layer output not comparable"
+    else:
+        idx, w = dev_routing(r)
+    mode = nm.W4A4 if w4a4 else nm.W4A16
+    ws = nm.make_workspace(L, h.shape[0], k, mode)
+    out = nm.moe_expert_forward(L, hd, idx, w, mode, residual=hd if residual else None, workspace=ws)
+    torch.cuda.synchronize()
+    assert nm.nvfp4_last_device_error() == 0
+    ref, ref64, _ = OL.forward(h, k, w4a4, residual, routing=r)
+    got = bf16_to_f64(bf16_bits(out))
+    err = assert_close(got, bf16_to_f64(ref), "layer output")
+    # the workspace counters are left zeroed: a second call gives the same bits
+    out2 = nm.moe_expert_forward(L, hd, idx, w, mode, residual=hd if residual else None, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    return err
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+@pytest.mark.parametrize("w4a4", [False, True])
+@pytest.mark.parametrize("residual", [False, True])
+def test_small_layer(nm, T, w4a4, residual):
+    c = SMALL
+    L = device_layer(nm, 7, 2, c["E"], c["H"], c["I"], c["S"], (-0.1, 0.1))
+    OL = OracleLayer(7, 2, c["H"], c["I"], c["S"], c["E"], (-0.1, 0.1))
+    h = gen.hidden_bf16(T, c["H"], 7, layer=2, rho=0.5)
+    run_layer(nm, L, OL, h, 4, w4a4, residual)
+
+
+def test_small_layer_odd_intermediate(nm):
+    # I = 192: the 128-wide k chunks end in a half chunk on the down GEMV
+    L = device_layer(nm, 8, 0, 8, 128, 192, 320, (-0.1, 0.1))
+    OL = OracleLayer(8, 0, 128, 192, 320, 8, (-0.1, 0.1))
+    h = gen.hidden_bf16(3, 128, 8, layer=0)
+    run_layer(nm, L, OL, h, 3, True, True)
+    run_layer(nm, L, OL, h, 3, False, False)
+
+
+@pytest.fixture(scope="module")
+def full_layer(nm):
+    c = configs.shape(0)
+    L = device_layer(nm, 0, 0, c["E"], c["H"], c["I"], c["S"], c["bias"])
+    OL = OracleLayer(0, 0, c["H"], c["I"], c["S"], c["E"], c["bias"])
+    return c, L, OL
+
+
+def test_full_layer_w4a16_one_token(nm, full_layer):
+    c, L, OL = full_layer
+    h = gen.hidden_bf16(1, c["H"], 0, layer=configs.HIDDEN_LAYER)
+    run_layer(nm, L, OL, h, c["K"], False, False, gpu_routing=True)
+
+
+def test_full_layer_w4a4_one_token(nm, full_layer):
+    c, L, OL = full_layer
+    h = gen.hidden_bf16(1, c["H"], 0, layer=configs.HIDDEN_LAYER)
+    run_layer(nm, L, OL, h, c["K"], True, True, gpu_routing=True)
+
+
+def test_full_layer_w4a4_four_tokens(nm, full_layer):
+    c, L, OL = full_layer
+    h = gen.hidden_bf16(4, c["H"], 0, layer=configs.HIDDEN_LAYER, rho=0.5)
+    run_layer(nm, L, OL, h, c["K"], True, True)
