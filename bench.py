@@ -168,7 +168,7 @@ class OracleSample:
         h = self.h0
         for l in range(self.nl):
             OL = OracleLayer(c["seed"], l, c["H"], c["I"], c["S"], c["E"], c["bias"])
-            h, _, _ = OL.forward(h, c["K"], c["w4a4"], True)
+            h, _, _ = OL.forward(h, c["K"], c["w4a4"], True, rms_eps=c["rms_eps"])
             self.layers.append(OL)
         self.rows = 0
         if c["lm_head"]:
@@ -183,15 +183,17 @@ class OracleSample:
         c, orc = self.c, self.orc
         h = self.h0
         t0 = time.perf_counter()
+        eps = c["rms_eps"]
         for OL in self.layers:
-            r = OL.route(h, c["K"])
-            h, _ = orc.moe_layer(h, r["idx"], r["w"], OL.up, OL.down, OL.sh_up, OL.sh_down,
-                                 c["w4a4"], True, c["E"])
+            x = orc.rms_norm(h, eps) if eps > 0 else h
+            r = orc.route(x, OL.Wg, OL.bias, c["K"])
+            h, _ = orc.moe_layer(x, r["idx"], r["w"], OL.up, OL.down, OL.sh_up, OL.sh_down,
+                                 c["w4a4"], h, c["E"])
         t_layers = time.perf_counter() - t0
         t_lm = 0.0
         if self.rows:
             t0 = time.perf_counter()
-            orc.lm_head(self.W, h)
+            orc.lm_head(self.W, orc.rms_norm(h, eps) if eps > 0 else h)
             t_lm = time.perf_counter() - t0
         per_step = t_layers / self.nl * c["layers"] + (t_lm * c["V"] / self.rows if self.rows else 0)
         return per_step / c["T"] * 1e6, t_layers + t_lm
@@ -236,7 +238,8 @@ def run_ours(args, ws, rank, local):
 
     c = configs.shape(args.config)
     T, L, E, H, I, S, K, V = c["T"], c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], c["V"]
-    st = MoEDecodeStack(L, E, H, I, S, K, T, w4a4=c["w4a4"], V=V if c["lm_head"] else None)
+    st = MoEDecodeStack(L, E, H, I, S, K, T, w4a4=c["w4a4"], V=V if c["lm_head"] else None,
+                        rms_eps=c["rms_eps"])
     st.register(*fill.fillers(c["seed"], c["bias"]))
     fill.hidden(st.h[0], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
     h0 = st.h[0].clone()
@@ -274,14 +277,16 @@ def run_ours(args, ws, rank, local):
     for rep in range(3):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * L + 2)]
         for l, Lw in enumerate(st.layers):
-            nm.moe_route_topk(st.h[l], Lw.router_w, Lw.router_b, K, st.topk_idx[l], st.topk_w[l])
+            nm.moe_route_topk(st.h[l], Lw.router_w, Lw.router_b, K, st.topk_idx[l], st.topk_w[l],
+                              rms_eps=st.rms_eps)
             evs[2 * l].record(stream)
             nm.moe_expert_forward(Lw, st.h[l], st.topk_idx[l], st.topk_w[l], st.mode,
-                                  residual=st.h[l], out=st.h[l + 1], workspace=st.ws)
+                                  residual=st.h[l], out=st.h[l + 1], workspace=st.ws,
+                                  rms_eps=st.rms_eps)
             evs[2 * l + 1].record(stream)
         if c["lm_head"]:
             evs[2 * L].record(stream)
-            nm.lm_head_gemv(st.lm, st.h[L], st.logits)
+            nm.lm_head_gemv(st.lm, st.h[L], st.logits, rms_eps=st.rms_eps)
             evs[2 * L + 1].record(stream)
         torch.cuda.synchronize()
         if rep > 0:

@@ -9,17 +9,20 @@ wide.
 """
 H, I, S, E, K, V, L = 2688, 1856, 3712, 128, 6, 131072, 23
 
+# rms_eps: the chained configs normalise each block's input (pre-norm) and
+# the lm_head input; a single layer on an N(0, 1) input is fed as is.
+RMS_EPS = 1e-5
 CONFIGS = {
     0: dict(name="decode_1tok_1layer_w4a16", T=1, layers=1, w4a4=False, lm_head=False,
-            bias=(-0.1, 0.1), rho=0.0, seed=0),
+            bias=(-0.1, 0.1), rho=0.0, seed=0, rms_eps=0.0),
     1: dict(name="decode_1tok_23layer_w4a4_lmhead", T=1, layers=L, w4a4=True, lm_head=True,
-            bias=(-0.1, 0.1), rho=0.0, seed=0),
+            bias=(-0.1, 0.1), rho=0.0, seed=0, rms_eps=RMS_EPS),
     2: dict(name="verify_4tok_23layer_w4a4_lmhead", T=4, layers=L, w4a4=True, lm_head=True,
-            bias=(-0.1, 0.1), rho=0.5, seed=0),
+            bias=(-0.1, 0.1), rho=0.5, seed=0, rms_eps=RMS_EPS),
     3: dict(name="prefill_1024tok_1layer_w4a4", T=1024, layers=1, w4a4=True, lm_head=False,
-            bias=(-0.5, 0.5), rho=0.0, seed=0),
+            bias=(-0.5, 0.5), rho=0.0, seed=0, rms_eps=0.0),
     4: dict(name="concurrent_256tok_23layer_w4a4_lmhead", T=256, layers=L, w4a4=True,
-            lm_head=True, bias=(-0.1, 0.1), rho=0.0, seed=0),
+            lm_head=True, bias=(-0.1, 0.1), rho=0.0, seed=0, rms_eps=RMS_EPS),
 }
 
 # the hidden states entering layer 0 are drawn under this layer id; a

@@ -133,15 +133,18 @@ nvfp4_status nvfp4_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t 
  *   select the k largest sigma_e + bias_e (an exact tie goes to the lower
  *   index), in descending order;
  *   topk_w[j] = sigma_{e_j} / sum_l sigma_{e_l}.
+ * h is the hidden row itself, or its RMS norm when rms_eps > 0 (see
+ * moe_expert_forward).
  *   hidden    device bf16 [T][H], 16-byte aligned
  *   router_w  device float [E][H], 16-byte aligned
  *   bias      device float [E]
  *   T >= 1, H % 16 == 0, 1 <= k <= E <= 256, k <= 32
+ *   rms_eps   > 0: normalise each hidden row first; <= 0: use it as is
  *   topk_idx  device out int32 [T][k];  topk_w device out float [T][k]
  */
 nvfp4_status moe_route_topk(const void* hidden, const float* router_w, const float* bias,
-                            int32_t T, int32_t H, int32_t E, int32_t k, int32_t* topk_idx,
-                            float* topk_w, cudaStream_t stream);
+                            int32_t T, int32_t H, int32_t E, int32_t k, float rms_eps,
+                            int32_t* topk_idx, float* topk_w, cudaStream_t stream);
 
 /*
  * moe_expert_forward_workspace_size - bytes of device workspace that
@@ -170,13 +173,17 @@ nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace
  *   out_t = bf16( shared(x_t) + sum_j topk_w[t][j] * y_{t,j} [+ residual_t] )
  * with FP32 accumulation and one bf16 rounding at the end ([card-int4]
  * "Checkpoint layout" for the non-gated MLP; [super-q] for NVFP4 on the
- * shared expert too).
+ * shared expert too). x_t is the hidden row, or, when rms_eps > 0, its
+ * unit-weight RMS norm bf16(h / sqrt(mean(h^2) + rms_eps)) -- the block input
+ * norm of the pre-norm model the pages serve, whose norms stay in bf16
+ * ([card-int4] "Left at bfloat16"); the residual is added un-normalised.
  *   w          weights (host struct holding device pointers); shapes must
  *              satisfy hidden, inter, shared_inter % 64 == 0
  *   hidden     device bf16 [T][H], 16-byte aligned
  *   topk_idx   device int32 [T][k], entries in [0, E) and distinct per token
  *   topk_w     device float [T][k]
  *   T >= 1, 1 <= k <= min(E, 16)
+ *   rms_eps    > 0: normalise each hidden row first; <= 0: use it as is
  *   residual   device bf16 [T][H] or NULL
  *   out        device bf16 [T][H]; may alias residual, must not alias hidden
  *              unless hidden == residual
@@ -187,26 +194,32 @@ nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace
  */
 nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
                                 const int32_t* topk_idx, const float* topk_w, int32_t T,
-                                int32_t k, nvfp4_act_mode mode, const void* residual, void* out,
-                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                                int32_t k, nvfp4_act_mode mode, float rms_eps, const void* residual,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
 
 /*
  * lm_head_gemv - NVFP4 weight-only lm_head ([worklog] Step 4; [card-w4a4]
  * "lm_head NVFP4 weight-only (W4A16)"):
- *   logits[t][v] = sum_j W[v][j] * h[t][j], FP32 accumulation and output.
+ *   logits[t][v] = sum_j W[v][j] * h[t][j], FP32 accumulation and output;
+ *   h is the hidden row, or its unit-weight RMS norm (the final norm before
+ *   the head) when rms_eps > 0.
  *   w        NVFP4 matrix [V][H] (device pointers), V % 16 == 0, H % 64 == 0
  *   hidden   device bf16 [T][H], 16-byte aligned;  T >= 1
+ *   rms_eps  > 0: normalise each hidden row first; <= 0: use it as is
  *   logits   device float [T][V]
  */
-nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, float* logits,
-                          cudaStream_t stream);
+nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, float rms_eps,
+                          float* logits, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* nvfp4_status_string(nvfp4_status status);
 
 /* Synchronises `stream`, then reads and clears the device error word: returns
  * NVFP4_ERR_TIMEOUT if a bounded device wait expired since the last read,
- * NVFP4_ERR_CUDA if the synchronisation itself failed, else NVFP4_OK. */
+ * NVFP4_ERR_INVALID_ARG if a kernel met an invalid device-side input (an
+ * expert index outside [0, E)), NVFP4_ERR_CUDA if the synchronisation itself
+ * failed, else NVFP4_OK. */
 nvfp4_status nvfp4_last_device_error(cudaStream_t stream);
 
 #ifdef __cplusplus

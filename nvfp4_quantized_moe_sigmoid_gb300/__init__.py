@@ -131,15 +131,15 @@ def nvfp4_quantize(x, mode=PER_TENSOR, out: NVFP4Matrix = None, global_scale=Non
     return out
 
 
-def moe_route_topk(hidden, router_w, bias, k, topk_idx=None, topk_w=None, stream=None):
+def moe_route_topk(hidden, router_w, bias, k, topk_idx=None, topk_w=None, rms_eps=0.0, stream=None):
     T, H = hidden.shape
     E = router_w.shape[0]
     if topk_idx is None:
         topk_idx = torch.empty((T, k), dtype=torch.int32, device=hidden.device)
     if topk_w is None:
         topk_w = torch.empty((T, k), dtype=torch.float32, device=hidden.device)
-    st = _L.moe_route_topk(_ptr(hidden), _ptr(router_w), _ptr(bias), T, H, E, k, _ptr(topk_idx),
-                           _ptr(topk_w), _stream(stream))
+    st = _L.moe_route_topk(_ptr(hidden), _ptr(router_w), _ptr(bias), T, H, E, k, float(rms_eps),
+                           _ptr(topk_idx), _ptr(topk_w), _stream(stream))
     _check(st, "moe_route_topk")
     return topk_idx, topk_w
 
@@ -162,7 +162,7 @@ def make_workspace(layer: MoELayer, T, k, mode=W4A4, stream=None):
 
 
 def moe_expert_forward(layer: MoELayer, hidden, topk_idx, topk_w, mode=W4A4, residual=None,
-                       out=None, workspace=None, stream=None):
+                       out=None, workspace=None, rms_eps=0.0, stream=None):
     T = hidden.shape[0]
     k = topk_idx.shape[1]
     if out is None:
@@ -171,17 +171,17 @@ def moe_expert_forward(layer: MoELayer, hidden, topk_idx, topk_w, mode=W4A4, res
         workspace = make_workspace(layer, T, k, mode, stream)
     w = layer.c()
     st = _L.moe_expert_forward(ctypes.byref(w), _ptr(hidden), _ptr(topk_idx), _ptr(topk_w), T, k,
-                               mode, _ptr(residual), _ptr(out), _ptr(workspace), workspace.numel(),
-                               _stream(stream))
+                               mode, float(rms_eps), _ptr(residual), _ptr(out), _ptr(workspace),
+                               workspace.numel(), _stream(stream))
     _check(st, "moe_expert_forward")
     return out
 
 
-def lm_head_gemv(w: NVFP4Matrix, hidden, logits=None, stream=None):
+def lm_head_gemv(w: NVFP4Matrix, hidden, logits=None, rms_eps=0.0, stream=None):
     T = hidden.shape[0]
     if logits is None:
         logits = torch.empty((T, w.n), dtype=torch.float32, device=hidden.device)
     m = w.c()
-    st = _L.lm_head_gemv(ctypes.byref(m), _ptr(hidden), T, _ptr(logits), _stream(stream))
+    st = _L.lm_head_gemv(ctypes.byref(m), _ptr(hidden), T, float(rms_eps), _ptr(logits), _stream(stream))
     _check(st, "lm_head_gemv")
     return logits

@@ -42,7 +42,7 @@ def load(path: str = LIB_PATH):
     L = ctypes.CDLL(path)
     L.nvfp4_quantize.argtypes = [P, ctypes.c_int, I64, I64, ctypes.c_int, P, P, P, P]
     L.nvfp4_quantize.restype = ctypes.c_int
-    L.moe_route_topk.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P]
+    L.moe_route_topk.argtypes = [P, P, P, I32, I32, I32, I32, ctypes.c_float, P, P, P]
     L.moe_route_topk.restype = ctypes.c_int
     L.moe_expert_forward_workspace_size.argtypes = [ctypes.POINTER(MoeLayerWeights), I32, I32,
                                                     ctypes.c_int]
@@ -50,9 +50,9 @@ def load(path: str = LIB_PATH):
     L.moe_expert_forward_workspace_init.argtypes = [P, ctypes.c_size_t, P]
     L.moe_expert_forward_workspace_init.restype = ctypes.c_int
     L.moe_expert_forward.argtypes = [ctypes.POINTER(MoeLayerWeights), P, P, P, I32, I32,
-                                     ctypes.c_int, P, P, P, ctypes.c_size_t, P]
+                                     ctypes.c_int, ctypes.c_float, P, P, P, ctypes.c_size_t, P]
     L.moe_expert_forward.restype = ctypes.c_int
-    L.lm_head_gemv.argtypes = [ctypes.POINTER(NVFP4Matrix), P, I32, P, P]
+    L.lm_head_gemv.argtypes = [ctypes.POINTER(NVFP4Matrix), P, I32, ctypes.c_float, P, P]
     L.lm_head_gemv.restype = ctypes.c_int
     L.nvfp4_status_string.argtypes = [ctypes.c_int]
     L.nvfp4_status_string.restype = ctypes.c_char_p

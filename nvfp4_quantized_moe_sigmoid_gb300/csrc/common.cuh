@@ -205,6 +205,44 @@ __device__ __forceinline__ void dequant_block16_f16(const QBlock& q, uint32_t (&
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
+// Unit-weight RMS norm of one bf16 row by one warp (the per-block input norm
+// of the pre-norm model the pages serve; its norms stay in bf16):
+//   inv = 1 / sqrt(sum_i x_i^2 / K + eps),  y_i = bf16(x_i * inv).
+// Lane l accumulates elements 8l + 256m .. 8l + 256m + 7 (m = 0, 1, ...) in
+// order with fused multiply-adds, then an xor-shuffle tree (commutative at
+// every level, so all lanes agree): the result does not depend on which
+// kernel runs it. K % 8 == 0; src/dst 16-byte aligned (dst may equal src).
+__device__ __forceinline__ void warp_rmsnorm_row(const uint16_t* src, uint16_t* dst, int K, float eps) {
+    const int lane = threadIdx.x & 31;
+    float ss = 0.0f;
+    for (int i = 8 * lane; i < K; i += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+            ss = __fmaf_rn(a, a, ss);
+            ss = __fmaf_rn(b, b, ss);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps)));
+    for (int i = 8 * lane; i < K; i += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat16 lo = __float2bfloat16_rn(__fmul_rn(__uint_as_float(w[j] << 16), inv));
+            const __nv_bfloat16 hi = __float2bfloat16_rn(__fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), inv));
+            o[j] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&lo)) |
+                   (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 // ---------------------------------------------------------------- MMA
 // D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col)
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,

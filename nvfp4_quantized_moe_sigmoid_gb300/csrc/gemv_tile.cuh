@@ -27,6 +27,37 @@ namespace nvfp4moe {
 // acc[2..3] = rows g+8, cols 2q, 2q+1. `bcol` points to the f16 row of column
 // g (K elements, 16-byte aligned) or is null for an all-zero column.
 // K % 64 == 0.
+//
+// Latency: the next chunk's code, scale and B words are loaded while the
+// current chunk is decoded, and the MMAs of a chunk go to four independent
+// accumulator sets (summed at the end), so one warp keeps several MMAs and
+// shared-memory loads in flight instead of one dependent chain.
+struct TileChunk {
+    uint4 wa, wb, b0, b1, b2, b3;
+    uint32_t sva, svb;
+};
+
+__device__ __forceinline__ void tile_load_chunk(TileChunk& t, const uint8_t* ca, const uint8_t* cb,
+                                                const uint8_t* sa, const uint8_t* sb, const __half* bp,
+                                                int c, bool valid) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    t.wa = t.wb = t.b0 = t.b1 = t.b2 = t.b3 = z;
+    t.sva = t.svb = 0;
+    if (valid) {
+        t.wa = *reinterpret_cast<const uint4*>(ca + 64 * c);
+        t.wb = *reinterpret_cast<const uint4*>(cb + 64 * c);
+        t.sva = *reinterpret_cast<const uint16_t*>(sa + 8 * c);
+        t.svb = *reinterpret_cast<const uint16_t*>(sb + 8 * c);
+        if (bp) {
+            const uint4* b = reinterpret_cast<const uint4*>(bp + 128 * c);
+            t.b0 = b[0];
+            t.b1 = b[1];
+            t.b2 = b[2];
+            t.b3 = b[3];
+        }
+    }
+}
+
 __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes,
                                               const uint8_t* __restrict__ tscales, int K,
                                               const __half* __restrict__ bcol, float (&acc)[4]) {
@@ -41,21 +72,23 @@ __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes
     const int nchunks = (K + 127) >> 7;
     const bool half_tail = (K & 127) != 0;
 
+    float a4[4][4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) a4[h][v] = 0.0f;
+
+    TileChunk cur, nxt;
+    tile_load_chunk(cur, ca, cb, sa, sb, bp, 0, !(half_tail && nchunks == 1 && q >= 2));
     for (int c = 0; c < nchunks; ++c) {
-        const bool valid = !(half_tail && c == nchunks - 1 && q >= 2);
-        uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
-        uint32_t sva = 0, svb = 0;
-        if (valid) {
-            wa = *reinterpret_cast<const uint4*>(ca + 64 * c);
-            wb = *reinterpret_cast<const uint4*>(cb + 64 * c);
-            sva = *reinterpret_cast<const uint16_t*>(sa + 8 * c);
-            svb = *reinterpret_cast<const uint16_t*>(sb + 8 * c);
-        }
-        const uint32_t sA = e4m3x2_to_f16x2(sva), sB = e4m3x2_to_f16x2(svb);
+        if (c + 1 < nchunks)
+            tile_load_chunk(nxt, ca, cb, sa, sb, bp, c + 1, !(half_tail && c + 2 == nchunks && q >= 2));
+        const uint32_t sA = e4m3x2_to_f16x2(cur.sva), sB = e4m3x2_to_f16x2(cur.svb);
         const uint32_t sA0 = bcast_lo(sA), sA1 = bcast_hi(sA);
         const uint32_t sB0 = bcast_lo(sB), sB1 = bcast_hi(sB);
-        const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
-        const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+        const uint32_t wA[4] = {cur.wa.x, cur.wa.y, cur.wa.z, cur.wa.w};
+        const uint32_t wB[4] = {cur.wb.x, cur.wb.y, cur.wb.z, cur.wb.w};
+        const uint4 bq[4] = {cur.b0, cur.b1, cur.b2, cur.b3};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             uint32_t fa[4], fb[4];
@@ -63,23 +96,28 @@ __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes
             e2m1x8_to_f16x8(wB[h], fb);
             const uint32_t scA = h < 2 ? sA0 : sA1;
             const uint32_t scB = h < 2 ? sB0 : sB1;
-            uint4 bv = make_uint4(0, 0, 0, 0);
-            if (valid && bp) bv = *reinterpret_cast<const uint4*>(bp + 128 * c + 8 * h);
-            mma_16816(acc, hmul2(fa[0], scA), hmul2(fb[0], scB), hmul2(fa[1], scA), hmul2(fb[1], scB),
-                      bv.x, bv.y);
-            mma_16816(acc, hmul2(fa[2], scA), hmul2(fb[2], scB), hmul2(fa[3], scA), hmul2(fb[3], scB),
-                      bv.z, bv.w);
+            mma_16816(a4[h], hmul2(fa[0], scA), hmul2(fb[0], scB), hmul2(fa[1], scA), hmul2(fb[1], scB),
+                      bq[h].x, bq[h].y);
+            mma_16816(a4[h], hmul2(fa[2], scA), hmul2(fb[2], scB), hmul2(fa[3], scA), hmul2(fb[3], scB),
+                      bq[h].z, bq[h].w);
         }
+        cur = nxt;
     }
+#pragma unroll
+    for (int v = 0; v < 4; ++v) acc[v] += (a4[0][v] + a4[1][v]) + (a4[2][v] + a4[3][v]);
 }
 
 // ------------------------------------------------------------------ staging
 // A ring of `nstages` shared-memory stages, each holding one 16-row tile
-// (codes then scales), filled by one producer thread with bulk TMA copies and
-// consumed by one warp per use. full[s] completes when the tile has landed;
-// empty[s] when its consumer has finished reading it.
-constexpr int kMaxStages = 12;
+// (codes then scales), filled by one producer thread with bulk TMA copies.
+// Stage s is owned by consumer warp s: local item li goes to stage and warp
+// li % nstages, so every stage's uses are waited on, in order, by one warp.
+// (An mbarrier parity wait names the current or the immediately preceding
+// phase; a waiter for use u must not start while the barrier is still in
+// phase u - 2, which single ownership guarantees.) full[s] completes when the
+// tile has landed, empty[s] when its warp has finished reading it.
 constexpr int kConsumerWarps = 8;
+constexpr int kMaxStages = kConsumerWarps;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 
 struct Ring {

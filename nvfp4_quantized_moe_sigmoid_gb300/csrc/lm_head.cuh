@@ -22,10 +22,11 @@ struct LmArgs {
     int64_t V;
     int H;
     const uint16_t* hidden;  // [T][H]
+    float rms_eps;           // > 0: logits of RMSNorm(hidden)
     int T;                   // <= 8 per launch
     float* logits;           // [T][ld]
     int64_t ld;
-    int nstages, stage_bytes;
+    int ring_bytes;          // shared memory for the staging ring; B rows follow it
 };
 
 __global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
@@ -34,37 +35,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
     __shared__ const uint16_t* srcs[kLmMaxT];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ring_init(ring, a.nstages);
+    const int stage_bytes = 9 * a.H;
+    const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
+    ring_init(ring, nst);
     __syncthreads();
 
     const int64_t N = a.V >> 4;
     const int64_t ib = N * blockIdx.x / gridDim.x, ie = N * (blockIdx.x + 1) / gridDim.x;
     const int n = static_cast<int>(ie - ib);
     uint8_t* ring_base = smem;
-    __half* xb = reinterpret_cast<__half*>(smem + (size_t)a.nstages * a.stage_bytes);
+    __half* xb = reinterpret_cast<__half*>(smem + a.ring_bytes);          // [T][H] f16
+    uint16_t* xn = reinterpret_cast<uint16_t*>(xb + (size_t)kLmMaxT * a.H);  // [T][H] bf16
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {
             for (int li = 0; li < n; ++li) {
                 const int64_t row = 16 * (ib + li);
-                if (!ring_fill(ring, ring_base, a.stage_bytes, a.nstages, li,
+                if (!ring_fill(ring, ring_base, stage_bytes, nst, li,
                                a.codes + row * (a.H >> 1), a.scales + row * (a.H >> 4), a.H))
                     break;
             }
         }
     } else {
-        if (threadIdx.x < a.T) srcs[threadIdx.x] = a.hidden + (size_t)threadIdx.x * a.H;
+        if (a.rms_eps > 0.0f) {
+            if (warp < a.T) warp_rmsnorm_row(a.hidden + (size_t)warp * a.H, xn + (size_t)warp * a.H, a.H, a.rms_eps);
+            if (threadIdx.x < a.T) srcs[threadIdx.x] = xn + (size_t)threadIdx.x * a.H;
+        } else {
+            if (threadIdx.x < a.T) srcs[threadIdx.x] = a.hidden + (size_t)threadIdx.x * a.H;
+        }
         consumer_bar();
         prepare_b_rows<false>(srcs, a.T, a.H, xb, nullptr, nullptr);
         const float gw = __ldg(a.global);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
-        for (int li = warp; li < n; li += kConsumerWarps) {
-            if (!ring_acquire(ring, a.nstages, li)) break;
-            const uint8_t* st = ring_base + (size_t)(li % a.nstages) * a.stage_bytes;
+        for (int li = warp; warp < nst && li < n; li += nst) {
+            if (!ring_acquire(ring, nst, li)) break;
+            const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             tile_mma_16x8(st, st + 16 * (a.H >> 1), a.H, bcol, acc);
-            ring_release(ring, a.nstages, li);
+            ring_release(ring, nst, li);
             const int64_t row0 = 16 * (ib + li);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -74,7 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
         }
     }
     __syncthreads();
-    ring_drain(ring, a.nstages);
+    ring_drain(ring, nst);
 }
 
 }  // namespace nvfp4moe

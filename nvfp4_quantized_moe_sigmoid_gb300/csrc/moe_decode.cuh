@@ -82,12 +82,13 @@ struct UpArgs {
     const float* sh_global;
     int E, H, I, S;
     const uint16_t* hidden;  // [T][H] bf16
+    float rms_eps;           // > 0: experts see RMSNorm(hidden)
     const int32_t* topk_idx;
     const float* topk_w;
     int T, k;
     uint16_t* act;     // [T*k][I] bf16
     uint16_t* act_sh;  // [T][S] bf16
-    int nstages, stage_bytes;
+    int ring_bytes;    // shared memory for the staging ring; B rows follow it
 };
 
 template <bool W4A4>
@@ -100,7 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_up_decode(const UpArgs a) {
     __shared__ const uint16_t* srcs[kDecodeMaxT];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ring_init(ring, a.nstages);
+    const int stage_bytes = 9 * a.H;  // 16 rows x (H/2 code bytes + H/16 scale bytes)
+    const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
+    ring_init(ring, nst);
     build_plan(plan, a.topk_idx, a.topk_w, a.T, a.k, a.E);  // contains __syncthreads
 
     const int RI = a.I >> 4, RS = a.S >> 4;
@@ -109,7 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_up_decode(const UpArgs a) {
     const int64_t ib = N * blockIdx.x / gridDim.x, ie = N * (blockIdx.x + 1) / gridDim.x;
     const int n = static_cast<int>(ie - ib);
     uint8_t* ring_base = smem;
-    __half* xb = reinterpret_cast<__half*>(smem + (size_t)a.nstages * a.stage_bytes);  // [T][H]
+    __half* xb = reinterpret_cast<__half*>(smem + a.ring_bytes);  // [T][H] f16 B operand
+    uint16_t* xn = reinterpret_cast<uint16_t*>(xb + (size_t)a.T * a.H);  // [T][H] normalised bf16
 
     auto item = [&](int64_t i, const uint8_t*& c, const uint8_t*& s) {
         if (i < (int64_t)U * RI) {
@@ -129,21 +133,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_up_decode(const UpArgs a) {
             for (int li = 0; li < n; ++li) {
                 const uint8_t *c, *s;
                 item(ib + li, c, s);
-                if (!ring_fill(ring, ring_base, a.stage_bytes, a.nstages, li, c, s, a.H)) break;
+                if (!ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, a.H)) break;
             }
         }
     } else {
-        if (threadIdx.x < a.T) srcs[threadIdx.x] = a.hidden + (size_t)threadIdx.x * a.H;
+        if (a.rms_eps > 0.0f) {
+            if (warp < a.T) warp_rmsnorm_row(a.hidden + (size_t)warp * a.H, xn + (size_t)warp * a.H, a.H, a.rms_eps);
+            if (threadIdx.x < a.T) srcs[threadIdx.x] = xn + (size_t)threadIdx.x * a.H;
+        } else {
+            if (threadIdx.x < a.T) srcs[threadIdx.x] = a.hidden + (size_t)threadIdx.x * a.H;
+        }
         consumer_bar();
         prepare_b_rows<W4A4>(srcs, a.T, a.H, xb, gx, red);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
-        for (int li = warp; li < n; li += kConsumerWarps) {
-            if (!ring_acquire(ring, a.nstages, li)) break;
-            const uint8_t* st = ring_base + (size_t)(li % a.nstages) * a.stage_bytes;
+        for (int li = warp; warp < nst && li < n; li += nst) {
+            if (!ring_acquire(ring, nst, li)) break;
+            const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             tile_mma_16x8(st, st + 16 * (a.H >> 1), a.H, bcol, acc);
-            ring_release(ring, a.nstages, li);
+            ring_release(ring, nst, li);
             const int64_t i = ib + li;
             const bool routed = i < (int64_t)U * RI;
             const int u = routed ? static_cast<int>(i / RI) : 0;
@@ -169,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_up_decode(const UpArgs a) {
         }
     }
     __syncthreads();
-    ring_drain(ring, a.nstages);
+    ring_drain(ring, nst);
 }
 
 struct DownArgs {
@@ -190,7 +199,7 @@ struct DownArgs {
     float* ypart;              // [T*k][H]
     float* ysh;                // [T][H]
     int* tilecnt;              // [H/16], zero on entry, zero on exit
-    int nstages, stage_bytes;
+    int ring_bytes;            // shared memory for the staging ring; B rows follow it
 };
 
 template <bool W4A4>
@@ -204,7 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
     __shared__ int slot_u[2];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ring_init(ring, a.nstages);
     build_plan(plan, a.topk_idx, a.topk_w, a.T, a.k, a.E);
 
     const int RH = a.H >> 4;
@@ -219,9 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
     const int64_t ib = first_item(C * blockIdx.x / gridDim.x);
     const int64_t ie = first_item(C * (blockIdx.x + 1) / gridDim.x);
     const int n = static_cast<int>(ie - ib);
+    // stage size from the widest item this CTA owns (routed K = I, shared K = S)
+    const bool has_routed = n > 0 && ib < NR, has_shared = n > 0 && ie > NR;
+    const int kmax = max(has_routed ? a.I : 0, has_shared ? a.S : 0);
+    const int stage_bytes = 9 * max(kmax, 64);
+    const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
+    ring_init(ring, nst);
+    __syncthreads();
 
     uint8_t* ring_base = smem;
-    __half* bsm = reinterpret_cast<__half*>(smem + (size_t)a.nstages * a.stage_bytes);
+    __half* bsm = reinterpret_cast<__half*>(smem + a.ring_bytes);
     // B slots: two routed experts [T][I] each, then the shared expert [T][S]
     __half* bslot[3] = {bsm, bsm + (size_t)a.T * a.I, bsm + (size_t)2 * a.T * a.I};
 
@@ -244,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
             for (int li = 0; li < n; ++li) {
                 const uint8_t *c, *s;
                 item(ib + li, c, s);
-                if (!ring_fill(ring, ring_base, a.stage_bytes, a.nstages, li, c, s, item_k(ib + li))) break;
+                if (!ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, item_k(ib + li))) break;
             }
         }
     } else {
@@ -278,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
         }
 
         const int g = lane >> 2, q = lane & 3;
-        for (int li = warp; li < n; li += kConsumerWarps) {
+        for (int li = warp; warp < nst && li < n; li += nst) {
             const int64_t i = ib + li;
             const bool routed = i < NR;
             const int u = routed ? static_cast<int>(i / RH) : -1;
@@ -291,11 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
             const int K = routed ? a.I : a.S;
             const __half* bcol = nullptr;
             if (g < a.T && (!routed || plan.choice[u][g] >= 0)) bcol = bslot[sl] + (size_t)g * K;
-            if (!ring_acquire(ring, a.nstages, li)) break;
-            const uint8_t* st = ring_base + (size_t)(li % a.nstages) * a.stage_bytes;
+            if (!ring_acquire(ring, nst, li)) break;
+            const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             tile_mma_16x8(st, st + 16 * (K >> 1), K, bcol, acc);
-            ring_release(ring, a.nstages, li);
+            ring_release(ring, nst, li);
             const float gw = routed ? __ldg(a.global + plan.expert[u]) : __ldg(a.sh_global);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -334,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
         }
     }
     __syncthreads();
-    ring_drain(ring, a.nstages);
+    ring_drain(ring, nst);
 }
 
 }  // namespace nvfp4moe

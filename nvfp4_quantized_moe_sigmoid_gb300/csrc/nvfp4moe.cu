@@ -52,21 +52,30 @@ int smem_optin() {
 
 // Largest dynamic shared memory a kernel may use (opt-in limit minus its
 // static shared memory); raises the kernel's limit to that value once per
-// device.
+// (kernel, device). Kernels are told apart by address: template instances
+// with one signature share a type.
+int dyn_smem_limit(const void* kernel) {
+    struct Entry {
+        const void* fn;
+        int dev, lim;
+    };
+    static Entry table[256];
+    static int used = 0;
+    const int d = current_device();
+    for (int i = 0; i < used; ++i)
+        if (table[i].fn == kernel && table[i].dev == d) return table[i].lim;
+    cudaFuncAttributes at;
+    if (cudaFuncGetAttributes(&at, kernel) != cudaSuccess) return 0;
+    const int lim = smem_optin() - static_cast<int>(at.sharedSizeBytes) - 64;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim) != cudaSuccess)
+        return 0;
+    if (used < 256) table[used++] = Entry{kernel, d, lim};
+    return lim;
+}
+
 template <typename Kernel>
 int dyn_smem_limit(Kernel k) {
-    static int cache[kMaxDevices] = {0};
-    const int d = current_device();
-    if (d < 0 || d >= kMaxDevices) return 0;
-    if (cache[d] == 0) {
-        cudaFuncAttributes at;
-        if (cudaFuncGetAttributes(&at, k) != cudaSuccess) return 0;
-        const int lim = smem_optin() - static_cast<int>(at.sharedSizeBytes) - 64;
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, lim) != cudaSuccess)
-            return 0;
-        cache[d] = lim;
-    }
-    return cache[d];
+    return dyn_smem_limit(reinterpret_cast<const void*>(k));
 }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -150,7 +159,8 @@ nvfp4_status nvfp4_last_device_error(cudaStream_t stream) {
     if (v != 0) {
         const unsigned int zero = 0;
         if (cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return NVFP4_ERR_CUDA;
-        return NVFP4_ERR_TIMEOUT;
+        return (v & (kErrWaitFull | kErrWaitEmpty | kErrWaitDrain)) ? NVFP4_ERR_TIMEOUT
+                                                                      : NVFP4_ERR_INVALID_ARG;
     }
     return NVFP4_OK;
 }
@@ -194,8 +204,8 @@ nvfp4_status nvfp4_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t 
 }
 
 nvfp4_status moe_route_topk(const void* hidden, const float* router_w, const float* bias, int32_t T,
-                            int32_t H, int32_t E, int32_t k, int32_t* topk_idx, float* topk_w,
-                            cudaStream_t stream) {
+                            int32_t H, int32_t E, int32_t k, float rms_eps, int32_t* topk_idx,
+                            float* topk_w, cudaStream_t stream) {
     if (!hidden || !router_w || !bias || !topk_idx || !topk_w) return NVFP4_ERR_INVALID_ARG;
     if (T < 1 || H < 16 || E < 1 || k < 1 || k > E) return NVFP4_ERR_INVALID_ARG;
     if (H % 16 || E > 256 || k > 32) return NVFP4_ERR_UNSUPPORTED_SHAPE;
@@ -206,7 +216,7 @@ nvfp4_status moe_route_topk(const void* hidden, const float* router_w, const flo
     if (smem > lim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     const int tiles = (T + TT - 1) / TT;
     k_route<TT><<<tiles * kRouteCluster, kRouteWarps * 32, smem, stream>>>(
-        static_cast<const uint16_t*>(hidden), router_w, bias, T, H, E, k, topk_idx, topk_w);
+        static_cast<const uint16_t*>(hidden), router_w, bias, T, H, E, k, rms_eps, topk_idx, topk_w);
     return launch_status();
 }
 
@@ -225,8 +235,8 @@ nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace
 
 nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
                                 const int32_t* topk_idx, const float* topk_w, int32_t T, int32_t k,
-                                nvfp4_act_mode mode, const void* residual, void* out, void* workspace,
-                                size_t workspace_bytes, cudaStream_t stream) {
+                                nvfp4_act_mode mode, float rms_eps, const void* residual, void* out,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     nvfp4_status st = check_layer(w);
     if (st != NVFP4_OK) return st;
     if (!hidden || !topk_idx || !topk_w || !out || !workspace) return NVFP4_ERR_INVALID_ARG;
@@ -259,19 +269,20 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
     ua.I = I;
     ua.S = S;
     ua.hidden = static_cast<const uint16_t*>(hidden);
+    ua.rms_eps = rms_eps;
     ua.topk_idx = topk_idx;
     ua.topk_w = topk_w;
     ua.T = T;
     ua.k = k;
     ua.act = reinterpret_cast<uint16_t*>(wsb + ws.act);
     ua.act_sh = reinterpret_cast<uint16_t*>(wsb + ws.act_sh);
-    ua.stage_bytes = 9 * H;
     {
         const int lim = w4a4 ? dyn_smem_limit(k_moe_up_decode<true>) : dyn_smem_limit(k_moe_up_decode<false>);
-        const int bbytes = T * H * 2;
-        ua.nstages = std::min(kMaxStages, (lim - bbytes) / ua.stage_bytes);
-        if (ua.nstages < 2) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-        const int smem = ua.nstages * ua.stage_bytes + bbytes;
+        const int bbytes = 2 * T * H * 2;  // f16 B rows + normalised bf16 rows
+        const int stage = 9 * H;
+        ua.ring_bytes = std::min(kMaxStages * stage, ((lim - bbytes) / 128) * 128);
+        if (ua.ring_bytes < 2 * stage) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        const int smem = ua.ring_bytes + bbytes;
         if (w4a4) k_moe_up_decode<true><<<grid, kThreads, smem, stream>>>(ua);
         else k_moe_up_decode<false><<<grid, kThreads, smem, stream>>>(ua);
         st = launch_status();
@@ -300,13 +311,13 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
     da.ypart = reinterpret_cast<float*>(wsb + ws.ypart);
     da.ysh = reinterpret_cast<float*>(wsb + ws.ysh);
     da.tilecnt = reinterpret_cast<int*>(wsb + ws.tilecnt);
-    da.stage_bytes = 9 * std::max(I, S);
     {
         const int lim = w4a4 ? dyn_smem_limit(k_moe_down_decode<true>) : dyn_smem_limit(k_moe_down_decode<false>);
         const int bbytes = (2 * T * I + T * S) * 2;
-        da.nstages = std::min(kMaxStages, (lim - bbytes) / da.stage_bytes);
-        if (da.nstages < 2) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-        const int smem = da.nstages * da.stage_bytes + bbytes;
+        const int stage = 9 * std::max(I, S);
+        da.ring_bytes = std::min(kMaxStages * stage, ((lim - bbytes) / 128) * 128);
+        if (da.ring_bytes < 2 * stage) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        const int smem = da.ring_bytes + bbytes;
         if (w4a4) k_moe_down_decode<true><<<grid, kThreads, smem, stream>>>(da);
         else k_moe_down_decode<false><<<grid, kThreads, smem, stream>>>(da);
         st = launch_status();
@@ -314,8 +325,8 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
     return st;
 }
 
-nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, float* logits,
-                          cudaStream_t stream) {
+nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, float rms_eps,
+                          float* logits, cudaStream_t stream) {
     if (!w || !hidden || !logits || T < 1) return NVFP4_ERR_INVALID_ARG;
     if (!w->codes || !w->scales || !w->global_scale || w->n < 16 || w->k < 64)
         return NVFP4_ERR_INVALID_ARG;
@@ -330,12 +341,13 @@ nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, 
     la.V = w->n;
     la.H = H;
     la.ld = w->n;
-    la.stage_bytes = 9 * H;
+    la.rms_eps = rms_eps;
     const int lim = dyn_smem_limit(k_lm_head);
-    const int bbytes = kLmMaxT * H * 2;
-    la.nstages = std::min(kMaxStages, (lim - bbytes) / la.stage_bytes);
-    if (la.nstages < 2) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    const int smem = la.nstages * la.stage_bytes + bbytes;
+    const int bbytes = 2 * kLmMaxT * H * 2;  // f16 B rows + normalised bf16 rows
+    const int stage = 9 * H;
+    la.ring_bytes = std::min(kMaxStages * stage, ((lim - bbytes) / 128) * 128);
+    if (la.ring_bytes < 2 * stage) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const int smem = la.ring_bytes + bbytes;
     const int64_t tiles = w->n / 16;
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), tiles));
     for (int t0 = 0; t0 < T; t0 += kLmMaxT) {

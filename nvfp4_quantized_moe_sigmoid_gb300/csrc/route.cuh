@@ -27,8 +27,8 @@ constexpr int kRouteMaxExpertsPerCta = 32;  // E <= 256
 template <int TT>
 __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteWarps * 32)
     k_route(const uint16_t* __restrict__ hidden, const float* __restrict__ Wg,
-            const float* __restrict__ bias, int T, int H, int E, int k, int32_t* __restrict__ topk_idx,
-            float* __restrict__ topk_w) {
+            const float* __restrict__ bias, int T, int H, int E, int k, float rms_eps,
+            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     uint16_t* hs = reinterpret_cast<uint16_t*>(smem_raw);  // [TT][H] bf16
     __shared__ float zs[TT][kRouteMaxExpertsPerCta];
@@ -40,8 +40,12 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteWa
     const int nt = min(TT, T - t0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // stage the token tile's hidden rows (bf16) in shared memory
-    {
+    // stage the token tile's hidden rows (bf16) in shared memory, RMS-normalised
+    // when rms_eps > 0 (the same warp routine as the expert kernels use)
+    if (rms_eps > 0.0f) {
+        for (int t = warp; t < nt; t += kRouteWarps)
+            warp_rmsnorm_row(hidden + (int64_t)(t0 + t) * H, hs + t * H, H, rms_eps);
+    } else {
         const int n16 = nt * H / 8;  // uint4 count (H % 16 == 0)
         const uint4* src = reinterpret_cast<const uint4*>(hidden + (int64_t)t0 * H);
         uint4* dst = reinterpret_cast<uint4*>(hs);
@@ -56,16 +60,27 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteWa
         float acc[TT];
 #pragma unroll
         for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
-        for (int i = lane; i < H / 4; i += 32) {
-            const float4 w4 = __ldg(wr + i);
+        // issue eight 16-byte gate loads per lane before using any of them
+        for (int i0 = lane; i0 < H / 4; i0 += 32 * 8) {
+            float4 w4[8];
 #pragma unroll
-            for (int t = 0; t < TT; ++t) {
-                if (t < nt) {
-                    const uint2 hv = *reinterpret_cast<const uint2*>(hs + t * H + 4 * i);
-                    acc[t] = fmaf(w4.x, __uint_as_float(hv.x << 16), acc[t]);
-                    acc[t] = fmaf(w4.y, __uint_as_float(hv.x & 0xFFFF0000u), acc[t]);
-                    acc[t] = fmaf(w4.z, __uint_as_float(hv.y << 16), acc[t]);
-                    acc[t] = fmaf(w4.w, __uint_as_float(hv.y & 0xFFFF0000u), acc[t]);
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + 32 * u;
+                w4[u] = i < H / 4 ? __ldg(wr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + 32 * u;
+                if (i >= H / 4) break;
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    if (t < nt) {
+                        const uint2 hv = *reinterpret_cast<const uint2*>(hs + t * H + 4 * i);
+                        acc[t] = fmaf(w4[u].x, __uint_as_float(hv.x << 16), acc[t]);
+                        acc[t] = fmaf(w4[u].y, __uint_as_float(hv.x & 0xFFFF0000u), acc[t]);
+                        acc[t] = fmaf(w4[u].z, __uint_as_float(hv.y << 16), acc[t]);
+                        acc[t] = fmaf(w4[u].w, __uint_as_float(hv.y & 0xFFFF0000u), acc[t]);
+                    }
                 }
             }
         }

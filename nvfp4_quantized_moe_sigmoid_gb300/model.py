@@ -1,9 +1,12 @@
 """A stack of NVFP4 MoE layers plus the NVFP4 lm_head, resident in HBM, and the
 decode step that runs them through the C ABI:
 
-    for each layer l:  idx, w = moe_route_topk(h_l)
-                       h_{l+1} = moe_expert_forward(h_l, idx, w, residual=h_l)
-    logits = lm_head_gemv(h_L)
+    for each layer l:  idx, w = moe_route_topk(norm(h_l))
+                       h_{l+1} = h_l + moe_expert_forward(norm(h_l), idx, w)
+    logits = lm_head_gemv(norm(h_L))
+
+where norm is the unit-weight RMS norm each block of the pre-norm model
+applies to its input (fused into the kernels; rms_eps = 0 disables it).
 
 ("Let's optimize Nemotron 3.5 Lightning - a worklog": a decode step streams
 the active experts of every MoE layer and the lm_head; the chain keeps only
@@ -18,9 +21,10 @@ from . import (MoELayer, NVFP4Matrix, PER_TENSOR, W4A4, W4A16, lm_head_gemv, mak
 
 class MoEDecodeStack:
     def __init__(self, layers, E, H, I, S, k, T, w4a4=True, V=None, device="cuda",
-                 weights_from=None):
+                 weights_from=None, rms_eps=1e-5):
         """weights_from: another stack whose registered weights this one shares."""
         self.L, self.E, self.H, self.I, self.S, self.k, self.T = layers, E, H, I, S, k, T
+        self.rms_eps = rms_eps
         self.V = V
         self.mode = W4A4 if w4a4 else W4A16
         self.device = device
@@ -74,12 +78,12 @@ class MoEDecodeStack:
         """One decode step on self.h[0] -> self.h[L] (and logits)."""
         for l, Lw in enumerate(self.layers):
             moe_route_topk(self.h[l], Lw.router_w, Lw.router_b, self.k, self.topk_idx[l],
-                           self.topk_w[l], stream=stream)
+                           self.topk_w[l], rms_eps=self.rms_eps, stream=stream)
             moe_expert_forward(Lw, self.h[l], self.topk_idx[l], self.topk_w[l], self.mode,
                                residual=self.h[l], out=self.h[l + 1], workspace=self.ws,
-                               stream=stream)
+                               rms_eps=self.rms_eps, stream=stream)
         if self.lm is not None:
-            lm_head_gemv(self.lm, self.h[self.L], self.logits, stream=stream)
+            lm_head_gemv(self.lm, self.h[self.L], self.logits, rms_eps=self.rms_eps, stream=stream)
 
     def capture(self):
         """Capture one step in a CUDA graph (after one eager step)."""

@@ -227,9 +227,10 @@ void orc_dequantize(const uint8_t* codes, const uint8_t* scales, const float* g,
  *   w_j = sigma_{e_j} / sum_l sigma_{e_l} (the unbiased sigmoids, renormalised).
  * Outputs per token: idx[k] and w[k] in descending c order; z[E], c[E]; and
  * tau[E], an a-priori bound on how far a binary32 evaluation of c_e may sit
- * from the exact one: 0.25 * 4 sqrt(H) 2^-24 sum_i |h_i Wg_ei| + 2^-22 (the
- * probabilistic dot-product bound times max sigma' = 1/4, plus sigmoid and
- * bias-add rounding). */
+ * from the exact one: 0.25 * (4 sqrt(H) 2^-24 sum_i |h_i Wg_ei| +
+ * 2 * 2^-8 max_i |h_i Wg_ei|) + 2^-22 (the probabilistic dot-product bound,
+ * plus one-ulp bf16 differences in up to two inputs from an RMS norm taken in
+ * binary32, times max sigma' = 1/4, plus sigmoid and bias-add rounding). */
 void orc_route(const uint16_t* h, int32_t T, int32_t H, const float* Wg, const float* bias,
                int32_t E, int32_t k, int32_t* idx, double* w, double* z, double* c,
                double* tau) {
@@ -241,16 +242,18 @@ void orc_route(const uint16_t* h, int32_t T, int32_t H, const float* Wg, const f
         double* sg = (double*)malloc(sizeof(double) * (size_t)E);
         unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
         for (int32_t e = 0; e < E; ++e) {
-            double acc = 0.0, aacc = 0.0;
+            double acc = 0.0, aacc = 0.0, amax = 0.0;
             for (int32_t i = 0; i < H; ++i) {
                 double p = orc_bf16_value(h[(int64_t)t * H + i]) * (double)Wg[(int64_t)e * H + i];
                 acc += p;
                 aacc += fabs(p);
+                if (fabs(p) > amax) amax = fabs(p);
             }
             zt[e] = acc;
             sg[e] = 1.0 / (1.0 + exp(-acc));
             ct[e] = sg[e] + (double)bias[e];
-            taut[e] = 0.25 * 4.0 * sqrt((double)H) * ldexp(1.0, -24) * aacc + ldexp(1.0, -22);
+            taut[e] = 0.25 * (4.0 * sqrt((double)H) * ldexp(1.0, -24) * aacc + 2.0 * ldexp(1.0, -8) * amax) +
+                      ldexp(1.0, -22);
         }
         double ssum = 0.0;
         for (int32_t j = 0; j < k; ++j) {
@@ -348,15 +351,33 @@ static void orc_expert(const orc_mat* up, const orc_mat* down, const double* x_b
     free(aa);
 }
 
+/* RMS normalisation with unit weight of each bf16 row (the per-block input
+ * norm of the pages' pre-norm hybrid model, whose norms stay in bf16:
+ * card-int4 "Left at bfloat16"): y_i = bf16( x_i / sqrt(mean_j x_j^2 + eps) ),
+ * binary64 arithmetic, one rounding. */
+void orc_rms_norm(const uint16_t* h, int32_t T, int64_t H, double eps, uint16_t* out) {
+    for (int32_t t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (int64_t i = 0; i < H; ++i) {
+            double x = orc_bf16_value(h[(int64_t)t * H + i]);
+            ss += x * x;
+        }
+        double inv = 1.0 / sqrt(ss / (double)H + eps);
+        for (int64_t i = 0; i < H; ++i)
+            out[(int64_t)t * H + i] = orc_bf16_round(orc_bf16_value(h[(int64_t)t * H + i]) * inv);
+    }
+}
+
 /* One MoE layer for T tokens given the routing (idx, w):
- *   out_t = bf16( shared(x_t) + sum_j w_tj * expert_{idx_tj}(x_t) [+ h_t] )
+ *   out_t = bf16( shared(x_t) + sum_j w_tj * expert_{idx_tj}(x_t) [+ residual_t] )
  * with one rounding at the end. `up`/`down` are indexed by expert id; only the
  * experts named in idx are read. The shared expert sees the same activation
  * treatment as the routed ones (super-q: MoE + shared-expert GEMMs NVFP4).
- * out_f64 (optional) receives the value before the final rounding. */
+ * residual (optional, bf16 [T][H]) is added before the rounding; out_f64
+ * (optional) receives the value before the final rounding. */
 void orc_moe_layer(const uint16_t* h, int32_t T, int32_t k, const int32_t* idx, const double* w,
                    const orc_mat* up, const orc_mat* down, const orc_mat* sh_up,
-                   const orc_mat* sh_down, int32_t w4a4, int32_t residual, uint16_t* out_bf16,
+                   const orc_mat* sh_down, int32_t w4a4, const uint16_t* residual, uint16_t* out_bf16,
                    double* out_f64) {
     int64_t H = sh_up->k;
     double* x = (double*)malloc(sizeof(double) * (size_t)H);
@@ -372,7 +393,7 @@ void orc_moe_layer(const uint16_t* h, int32_t T, int32_t k, const int32_t* idx, 
             for (int64_t i = 0; i < H; ++i) acc[i] += wj * y[i];
         }
         for (int64_t i = 0; i < H; ++i) {
-            double v = acc[i] + (residual ? x[i] : 0.0);
+            double v = acc[i] + (residual ? orc_bf16_value(residual[(int64_t)t * H + i]) : 0.0);
             if (out_f64) out_f64[(int64_t)t * H + i] = v;
             out_bf16[(int64_t)t * H + i] = orc_bf16_round(v);
         }

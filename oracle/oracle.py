@@ -46,7 +46,9 @@ def lib():
                                 ctypes.c_int32, P, P, P, P, P]
         L.orc_moe_layer.restype = None
         L.orc_moe_layer.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P,
-                                    ctypes.c_int32, ctypes.c_int32, P, P]
+                                    ctypes.c_int32, P, P, P]
+        L.orc_rms_norm.restype = None
+        L.orc_rms_norm.argtypes = [P, ctypes.c_int32, ctypes.c_int64, ctypes.c_double, P]
         L.orc_lm_head.restype = None
         L.orc_lm_head.argtypes = [P, P, ctypes.c_int32, P]
         L.orc_lm_head_rows.restype = None
@@ -173,9 +175,20 @@ def route(h_bf16: np.ndarray, Wg: np.ndarray, bias: np.ndarray, k: int):
 
 
 # ---- MoE layer / lm_head --------------------------------------------------
+def rms_norm(h_bf16, eps):
+    """Unit-weight RMS norm of each bf16 row -> bf16 (uint16 bits)."""
+    h = np.ascontiguousarray(h_bf16, np.uint16)
+    if h.ndim == 1:
+        h = h[None, :]
+    out = np.zeros_like(h)
+    lib().orc_rms_norm(_p(h), h.shape[0], h.shape[1], float(eps), _p(out))
+    return out
+
+
 def moe_layer(h_bf16, idx, w, up: dict, down: dict, sh_up: Mat, sh_down: Mat, w4a4: bool,
-              residual: bool, num_experts: int):
+              residual, num_experts: int):
     """up/down: {expert_id: Mat}; only the experts named in idx are needed.
+    residual: None, or a bf16 [T][H] array added before the final rounding.
     Returns (out_bf16 uint16 [T][H], out_f64 [T][H])."""
     h = np.ascontiguousarray(h_bf16, np.uint16)
     if h.ndim == 1:
@@ -196,9 +209,12 @@ def moe_layer(h_bf16, idx, w, up: dict, down: dict, sh_up: Mat, sh_down: Mat, w4
     shu, shd = sh_up.c(), sh_down.c()
     out = np.zeros((T, H), np.uint16)
     outf = np.zeros((T, H), np.float64)
+    res = None
+    if residual is not None:
+        res = np.ascontiguousarray(residual, np.uint16).reshape(T, H)
     lib().orc_moe_layer(_p(h), T, k, _p(idx), _p(w), ctypes.cast(ups, ctypes.c_void_p),
                         ctypes.cast(downs, ctypes.c_void_p), ctypes.byref(shu), ctypes.byref(shd),
-                        int(w4a4), int(residual), _p(out), _p(outf))
+                        int(w4a4), _p(res) if res is not None else None, _p(out), _p(outf))
     return out, outf
 
 

@@ -23,14 +23,18 @@ class OracleLayer:
                 self.up[e] = orc.Mat.from_master(gen.up_master(self.seed, self.layer, e, self.I, self.H))
                 self.down[e] = orc.Mat.from_master(gen.down_master(self.seed, self.layer, e, self.H, self.I))
 
-    def route(self, h, k):
-        return orc.route(h, self.Wg, self.bias, k)
+    def route(self, h, k, rms_eps=0.0):
+        x = orc.rms_norm(h, rms_eps) if rms_eps > 0 else h
+        return orc.route(x, self.Wg, self.bias, k)
 
-    def forward(self, h, k, w4a4, residual, routing=None):
-        r = self.route(h, k) if routing is None else routing
+    def forward(self, h, k, w4a4, residual, routing=None, rms_eps=0.0):
+        """One MoE block: x = RMSNorm(h) when rms_eps > 0 (else x = h), route(x),
+        experts(x), plus h when residual."""
+        x = orc.rms_norm(h, rms_eps) if rms_eps > 0 else h
+        r = orc.route(x, self.Wg, self.bias, k) if routing is None else routing
         self.ensure(r["idx"])
-        out, outf = orc.moe_layer(h, r["idx"], r["w"], self.up, self.down, self.sh_up,
-                                  self.sh_down, w4a4, residual, self.E)
+        out, outf = orc.moe_layer(x, r["idx"], r["w"], self.up, self.down, self.sh_up,
+                                  self.sh_down, w4a4, h if residual else None, self.E)
         return out, outf, r
 
 

@@ -52,17 +52,17 @@ def test_host_validation_rejects_bad_arguments(abi):
     assert L.nvfp4_quantize(fake, 1, 4, 32, 7, fake, fake, fake, null) == 1
     assert L.nvfp4_quantize(odd, 1, 4, 32, 0, fake, fake, fake, null) == 3
     # moe_route_topk: k > E, H % 16, E > 256, misaligned hidden
-    assert L.moe_route_topk(fake, fake, fake, 1, 64, 8, 9, fake, fake, null) == 1
-    assert L.moe_route_topk(fake, fake, fake, 1, 72, 8, 2, fake, fake, null) == 2
-    assert L.moe_route_topk(fake, fake, fake, 1, 64, 300, 2, fake, fake, null) == 2
-    assert L.moe_route_topk(odd, fake, fake, 1, 64, 8, 2, fake, fake, null) == 3
-    assert L.moe_route_topk(null, fake, fake, 1, 64, 8, 2, fake, fake, null) == 1
+    assert L.moe_route_topk(fake, fake, fake, 1, 64, 8, 9, 0.0, fake, fake, null) == 1
+    assert L.moe_route_topk(fake, fake, fake, 1, 72, 8, 2, 0.0, fake, fake, null) == 2
+    assert L.moe_route_topk(fake, fake, fake, 1, 64, 300, 2, 0.0, fake, fake, null) == 2
+    assert L.moe_route_topk(odd, fake, fake, 1, 64, 8, 2, 0.0, fake, fake, null) == 3
+    assert L.moe_route_topk(null, fake, fake, 1, 64, 8, 2, 0.0, fake, fake, null) == 1
     # lm_head_gemv
     m = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 100, 2688)
-    assert L.lm_head_gemv(ctypes.byref(m), fake, 1, fake, null) == 2
+    assert L.lm_head_gemv(ctypes.byref(m), fake, 1, 0.0, fake, null) == 2
     m = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 128, 2688)
-    assert L.lm_head_gemv(ctypes.byref(m), odd, 1, fake, null) == 3
-    assert L.lm_head_gemv(ctypes.byref(m), fake, 0, fake, null) == 1
+    assert L.lm_head_gemv(ctypes.byref(m), odd, 1, 0.0, fake, null) == 3
+    assert L.lm_head_gemv(ctypes.byref(m), fake, 0, 0.0, fake, null) == 1
     # moe_expert_forward: shapes, workspace size, null weights
     sh_up = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 3712, 2688)
     sh_dn = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 2688, 3712)
@@ -70,17 +70,17 @@ def test_host_validation_rejects_bad_arguments(abi):
                             0x10000, sh_up, sh_dn)
     need = L.moe_expert_forward_workspace_size(ctypes.byref(w), 1, 6, 1)
     assert need > 0
-    assert L.moe_expert_forward(ctypes.byref(w), fake, fake, fake, 1, 6, 1, null, ctypes.c_void_p(0x20000),
+    assert L.moe_expert_forward(ctypes.byref(w), fake, fake, fake, 1, 6, 1, 0.0, null, ctypes.c_void_p(0x20000),
                                 ctypes.c_void_p(0x30000), need - 1, null) == 4
-    assert L.moe_expert_forward(ctypes.byref(w), fake, fake, fake, 1, 6, 5, null, ctypes.c_void_p(0x20000),
+    assert L.moe_expert_forward(ctypes.byref(w), fake, fake, fake, 1, 6, 5, 0.0, null, ctypes.c_void_p(0x20000),
                                 ctypes.c_void_p(0x30000), need, null) == 1
     bad = abi.MoeLayerWeights(128, 2688, 1850, 3712, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000,
                               0x10000, sh_up, sh_dn)
-    assert L.moe_expert_forward(ctypes.byref(bad), fake, fake, fake, 1, 6, 1, null, fake, fake, need,
+    assert L.moe_expert_forward(ctypes.byref(bad), fake, fake, fake, 1, 6, 1, 0.0, null, fake, fake, need,
                                 null) == 2
     nul = abi.MoeLayerWeights(128, 2688, 1856, 3712, 0, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000,
                               sh_up, sh_dn)
-    assert L.moe_expert_forward(ctypes.byref(nul), fake, fake, fake, 1, 6, 1, null, fake, fake, need,
+    assert L.moe_expert_forward(ctypes.byref(nul), fake, fake, fake, 1, 6, 1, 0.0, null, fake, fake, need,
                                 null) == 1
 
 

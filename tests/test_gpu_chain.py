@@ -24,7 +24,8 @@ pytestmark = pytest.mark.gpu
 def stack(nm):
     from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
     c = configs.shape(1)
-    st = MoEDecodeStack(c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], 4, w4a4=True, V=c["V"])
+    st = MoEDecodeStack(c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], 4, w4a4=True, V=c["V"],
+                        rms_eps=c["rms_eps"])
     st.register(*fill.fillers(c["seed"], c["bias"]))
     torch.cuda.synchronize()
     return c, st
@@ -36,18 +37,23 @@ def test_chain_teacher_forced(nm, stack, cfg):
     c = configs.shape(cfg)
     T = c["T"]
     h = gen.hidden_bf16(T, c["H"], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+    assert np.isfinite(bf16_to_f64(h)).all(), "generated hidden state is not finite"
     ws = nm.make_workspace(st.layers[0], T, c["K"], nm.W4A4)
     exempt = 0
     for l in range(c["layers"]):
         OL = OracleLayer(c["seed"], l, c["H"], c["I"], c["S"], c["E"], c["bias"])
-        ref, _, r = OL.forward(h, c["K"], True, True)
+        assert np.isfinite(OL.Wg).all() and np.isfinite(OL.bias).all(), f"layer {l} router not finite"
+        ref, _, r = OL.forward(h, c["K"], True, True, rms_eps=c["rms_eps"])
+        assert np.isfinite(bf16_to_f64(ref)).all(), f"oracle layer {l} output not finite" 
         hd = to_dev_bf16(h)
-        idx, w = nm.moe_route_topk(hd, st.layers[l].router_w, st.layers[l].router_b, c["K"])
+        idx, w = nm.moe_route_topk(hd, st.layers[l].router_w, st.layers[l].router_b, c["K"],
+                                   rms_eps=c["rms_eps"])
         torch.cuda.synchronize()
         e = check_routing(idx.cpu().numpy(), w.cpu().numpy(), r, c["K"])
         exempt += e
         if e == 0:
-            out = nm.moe_expert_forward(st.layers[l], hd, idx, w, nm.W4A4, residual=hd, workspace=ws)
+            out = nm.moe_expert_forward(st.layers[l], hd, idx, w, nm.W4A4, residual=hd, workspace=ws,
+                                        rms_eps=c["rms_eps"])
             torch.cuda.synchronize()
             assert_close(bf16_to_f64(bf16_bits(out)), bf16_to_f64(ref), f"layer {l}")
         h = ref
@@ -55,12 +61,13 @@ def test_chain_teacher_forced(nm, stack, cfg):
     assert nm.nvfp4_last_device_error() == 0
     # lm_head on the oracle's final hidden state
     V, H = c["V"], c["H"]
-    logits = nm.lm_head_gemv(st.lm, to_dev_bf16(h)).cpu().numpy()
+    logits = nm.lm_head_gemv(st.lm, to_dev_bf16(h), rms_eps=c["rms_eps"]).cpu().numpy()
     rows = np.unique(np.concatenate([np.arange(16), np.random.default_rng(2).integers(0, V, 512)]))
     host = gen.lm_head_master(c["seed"], V, H)
     g = np.float32(np.abs(gen.bf16_bits_to_f32(host)).max()) / np.float32(2688.0)
     cc, ss, _ = orc.quantize(host[rows], orc.GIVEN, g=float(g))
-    assert_close(logits[:, rows], orc.lm_head(orc.Mat(cc, ss, g), h), "logits")
+    hn = orc.rms_norm(h, c["rms_eps"])
+    assert_close(logits[:, rows], orc.lm_head(orc.Mat(cc, ss, g), hn), "logits")
 
 
 def test_free_running_graph(nm, stack):
@@ -68,7 +75,7 @@ def test_free_running_graph(nm, stack):
     c0, st4 = stack
     c = configs.shape(1)
     st = MoEDecodeStack(c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], 1, w4a4=True, V=c["V"],
-                        weights_from=st4)
+                        weights_from=st4, rms_eps=c["rms_eps"])
     st.make_workspace()
     h0 = gen.hidden_bf16(1, c["H"], c["seed"], layer=configs.HIDDEN_LAYER)
     st.h[0].copy_(to_dev_bf16(h0))
@@ -81,8 +88,10 @@ def test_free_running_graph(nm, stack):
     assert torch.equal(first.view(torch.int16), st.h[1].view(torch.int16)), "replay not deterministic"
     assert torch.isfinite(st.logits).all()
     hd = to_dev_bf16(h0)
-    idx, w = nm.moe_route_topk(hd, st.layers[0].router_w, st.layers[0].router_b, c["K"])
-    out = nm.moe_expert_forward(st.layers[0], hd, idx, w, nm.W4A4, residual=hd, workspace=st.ws)
+    idx, w = nm.moe_route_topk(hd, st.layers[0].router_w, st.layers[0].router_b, c["K"],
+                               rms_eps=c["rms_eps"])
+    out = nm.moe_expert_forward(st.layers[0], hd, idx, w, nm.W4A4, residual=hd, workspace=st.ws,
+                                rms_eps=c["rms_eps"])
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), first.view(torch.int16))
     assert nm.nvfp4_last_device_error() == 0

@@ -16,11 +16,11 @@ pytestmark = pytest.mark.gpu
 SMALL = dict(E=16, H=256, I=128, S=192)
 
 
-def run_layer(nm, L, OL, h, k, w4a4, residual, gpu_routing=False):
+def run_layer(nm, L, OL, h, k, w4a4, residual, gpu_routing=False, rms_eps=0.0):
     hd = to_dev_bf16(h)
-    r = OL.route(h, k)
+    r = OL.route(h, k, rms_eps)
     if gpu_routing:
-        idx, w = nm.moe_route_topk(hd, L.router_w, L.router_b, k)
+        idx, w = nm.moe_route_topk(hd, L.router_w, L.router_b, k, rms_eps=rms_eps)
         torch.cuda.synchronize()
         check_routing(idx.cpu().numpy(), w.cpu().numpy(), r, k)
         assert np.array_equal(idx.cpu().numpy(), r["idx"]), "near-tie flip: layer output not comparable"
@@ -28,14 +28,16 @@ def run_layer(nm, L, OL, h, k, w4a4, residual, gpu_routing=False):
         idx, w = dev_routing(r)
     mode = nm.W4A4 if w4a4 else nm.W4A16
     ws = nm.make_workspace(L, h.shape[0], k, mode)
-    out = nm.moe_expert_forward(L, hd, idx, w, mode, residual=hd if residual else None, workspace=ws)
+    out = nm.moe_expert_forward(L, hd, idx, w, mode, residual=hd if residual else None, workspace=ws,
+                                rms_eps=rms_eps)
     torch.cuda.synchronize()
     assert nm.nvfp4_last_device_error() == 0
-    ref, ref64, _ = OL.forward(h, k, w4a4, residual, routing=r)
+    ref, ref64, _ = OL.forward(h, k, w4a4, residual, routing=r, rms_eps=rms_eps)
     got = bf16_to_f64(bf16_bits(out))
     err = assert_close(got, bf16_to_f64(ref), "layer output")
     # the workspace counters are left zeroed: a second call gives the same bits
-    out2 = nm.moe_expert_forward(L, hd, idx, w, mode, residual=hd if residual else None, workspace=ws)
+    out2 = nm.moe_expert_forward(L, hd, idx, w, mode, residual=hd if residual else None, workspace=ws,
+                                 rms_eps=rms_eps)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     return err
@@ -50,6 +52,10 @@ def test_small_layer(nm, T, w4a4, residual):
     OL = OracleLayer(7, 2, c["H"], c["I"], c["S"], c["E"], (-0.1, 0.1))
     h = gen.hidden_bf16(T, c["H"], 7, layer=2, rho=0.5)
     run_layer(nm, L, OL, h, 4, w4a4, residual)
+    if residual:  # the pre-normed block: x = RMSNorm(3 h), residual 3 h
+        h3 = gen.hidden_bf16(T, c["H"], 7, layer=2, rho=0.5)
+        h3 = (gen.bf16_bits_to_f32(h3) * 3.0).astype(np.float32).view(np.uint32) >> 16
+        run_layer(nm, L, OL, h3.astype(np.uint16), 4, w4a4, residual, gpu_routing=T == 1, rms_eps=1e-5)
 
 
 def test_small_layer_odd_intermediate(nm):
@@ -85,3 +91,10 @@ def test_full_layer_w4a4_four_tokens(nm, full_layer):
     c, L, OL = full_layer
     h = gen.hidden_bf16(4, c["H"], 0, layer=configs.HIDDEN_LAYER, rho=0.5)
     run_layer(nm, L, OL, h, c["K"], True, True)
+
+
+def test_full_layer_w4a4_prenorm(nm, full_layer):
+    c, L, OL = full_layer
+    h = gen.hidden_bf16(2, c["H"], 0, layer=9)
+    h = ((gen.bf16_bits_to_f32(h) * 7.0).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    run_layer(nm, L, OL, h, c["K"], True, True, gpu_routing=True, rms_eps=1e-5)

@@ -59,3 +59,21 @@ def test_ties_go_to_lower_index():
     h = np.zeros((1, 32), np.uint16)
     r = orc.route(h, Wg, bias, 4)
     assert list(r["idx"][0]) == [1, 2, 4, 5]
+
+
+def test_rms_norm_matches_numpy_and_torch_rounding():
+    import torch
+    h = gen.hidden_bf16(3, 2688, 0, layer=4)
+    hf = gen.bf16_bits_to_f32(h).astype(np.float64) * np.array([[1.0], [37.0], [1e-3]])
+    hb = torch.from_numpy(hf).to(torch.float32).to(torch.bfloat16)
+    h = hb.view(torch.int16).numpy().astype(np.uint16)
+    x = gen.bf16_bits_to_f32(h).astype(np.float64)
+    ref = x / np.sqrt((x ** 2).mean(axis=1, keepdims=True) + 1e-5)
+    got = gen.bf16_bits_to_f32(orc.rms_norm(h, 1e-5)).astype(np.float64)
+    # one bf16 rounding of the exact value: within half an ulp (2^-8 relative)
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+    # and it is the nearest bf16: torch's RNE of the float32 value agrees where
+    # the float32 rounding cannot straddle a bf16 midpoint
+    near = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    assert np.mean(near == got) > 0.999
+    assert np.allclose(np.sqrt((got[:2] ** 2).mean(axis=1)), 1.0, atol=5e-3)  # row 3: eps dominates
