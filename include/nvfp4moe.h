@@ -199,6 +199,39 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
                                 cudaStream_t stream);
 
 /*
+ * moe_expert_forward_noalloc - moe_expert_forward for callers that cannot
+ * allocate device memory. The pages have no counterpart to this call.
+ *
+ * Some hosts embed this layer without being able to give it a workspace:
+ * for example an operator plugin whose host passes only the operator's
+ * inputs and outputs and owns every device allocation, so the operator may
+ * neither call cudaMalloc nor receive an extra buffer. This variant takes
+ * the same arguments as moe_expert_forward minus the workspace and uses a
+ * fixed scratch array that the library itself holds in device memory.
+ *
+ *   - Limit: the scratch is NVFP4MOE_NOALLOC_SCRATCH_BYTES (1 MiB) per GPU,
+ *     held from library load until process exit. A call whose
+ *     moe_expert_forward_workspace_size exceeds it is rejected with
+ *     NVFP4_ERR_WORKSPACE before anything is launched (at the pages' layer
+ *     shape this admits 1-4 tokens with top-6).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (with that device current) and caches it; make that first call before
+ *     any stream capture.
+ *   - Each call clears the scratch region it uses on `stream` and leaves its
+ *     contents behind; all calls on a device share the one array, so calls
+ *     that overlap on the GPU (other streams, other threads) race. Order
+ *     them on one stream or otherwise serialise them.
+ *   - Nothing is allocated or freed: no cudaMalloc, cudaFree or allocating
+ *     library routine is called.
+ * Returns the same codes as moe_expert_forward.
+ */
+#define NVFP4MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+nvfp4_status moe_expert_forward_noalloc(const moe_layer_weights* w, const void* hidden,
+                                        const int32_t* topk_idx, const float* topk_w, int32_t T,
+                                        int32_t k, nvfp4_act_mode mode, float rms_eps,
+                                        const void* residual, void* out, cudaStream_t stream);
+
+/*
  * lm_head_gemv - NVFP4 weight-only lm_head ([worklog] Step 4; [card-w4a4]
  * "lm_head NVFP4 weight-only (W4A16)"):
  *   logits[t][v] = sum_j W[v][j] * h[t][j], FP32 accumulation and output;

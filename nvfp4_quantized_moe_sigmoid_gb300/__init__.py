@@ -15,7 +15,8 @@ from . import _abi
 
 __all__ = ["NVFP4Matrix", "MoELayer", "NVFP4Error", "nvfp4_quantize", "moe_route_topk",
            "moe_expert_forward_workspace_size", "moe_expert_forward_workspace_init",
-           "moe_expert_forward", "lm_head_gemv", "nvfp4_status_string", "nvfp4_last_device_error",
+           "moe_expert_forward", "moe_expert_forward_noalloc", "lm_head_gemv",
+           "nvfp4_status_string", "nvfp4_last_device_error",
            "W4A16", "W4A4", "PER_TENSOR", "PER_ROW", "GIVEN", "lib"]
 
 W4A16, W4A4 = 0, 1
@@ -174,6 +175,22 @@ def moe_expert_forward(layer: MoELayer, hidden, topk_idx, topk_w, mode=W4A4, res
                                mode, float(rms_eps), _ptr(residual), _ptr(out), _ptr(workspace),
                                workspace.numel(), _stream(stream))
     _check(st, "moe_expert_forward")
+    return out
+
+
+def moe_expert_forward_noalloc(layer: MoELayer, hidden, topk_idx, topk_w, mode=W4A4, residual=None,
+                               out=None, rms_eps=0.0, stream=None):
+    """moe_expert_forward without a workspace argument, for callers that cannot
+    allocate: the library's fixed device scratch array (1 MiB per GPU) is used
+    instead; calls that overlap on the GPU race on it."""
+    T = hidden.shape[0]
+    k = topk_idx.shape[1]
+    if out is None:
+        out = torch.empty_like(hidden)
+    w = layer.c()
+    st = _L.moe_expert_forward_noalloc(ctypes.byref(w), _ptr(hidden), _ptr(topk_idx), _ptr(topk_w), T, k,
+                                       mode, float(rms_eps), _ptr(residual), _ptr(out), _stream(stream))
+    _check(st, "moe_expert_forward_noalloc")
     return out
 
 

@@ -10,8 +10,11 @@ P = ctypes.c_void_p
 I32, I64 = ctypes.c_int32, ctypes.c_int64
 
 EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_size",
-           "moe_expert_forward_workspace_init", "moe_expert_forward", "lm_head_gemv",
+           "moe_expert_forward_workspace_init", "moe_expert_forward", "moe_expert_forward_noalloc",
+           "lm_head_gemv",
            "nvfp4_status_string", "nvfp4_last_device_error"]
+
+NOALLOC_SCRATCH_BYTES = 1 << 20  # NVFP4MOE_NOALLOC_SCRATCH_BYTES
 
 STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED_SHAPE",
           3: "NVFP4_ERR_MISALIGNED", 4: "NVFP4_ERR_WORKSPACE", 5: "NVFP4_ERR_CUDA",
@@ -52,6 +55,9 @@ def load(path: str = LIB_PATH):
     L.moe_expert_forward.argtypes = [ctypes.POINTER(MoeLayerWeights), P, P, P, I32, I32,
                                      ctypes.c_int, ctypes.c_float, P, P, P, ctypes.c_size_t, P]
     L.moe_expert_forward.restype = ctypes.c_int
+    L.moe_expert_forward_noalloc.argtypes = [ctypes.POINTER(MoeLayerWeights), P, P, P, I32, I32,
+                                             ctypes.c_int, ctypes.c_float, P, P, P]
+    L.moe_expert_forward_noalloc.restype = ctypes.c_int
     L.lm_head_gemv.argtypes = [ctypes.POINTER(NVFP4Matrix), P, I32, ctypes.c_float, P, P]
     L.lm_head_gemv.restype = ctypes.c_int
     L.nvfp4_status_string.argtypes = [ctypes.c_int]

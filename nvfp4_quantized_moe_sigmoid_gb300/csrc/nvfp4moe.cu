@@ -362,3 +362,52 @@ nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, 
 }
 
 }  // extern "C"
+
+// ------------------------------------------------ allocation-free variant
+// moe_expert_forward_noalloc: the same computation as moe_expert_forward for
+// callers that cannot allocate device memory. Its scratch is this file-scope
+// device array; the library holds it on every GPU that loads it until the
+// process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NVFP4MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current (in host code the symbol itself is only a host-side handle).
+void* noalloc_scratch(nvfp4_status* st) {
+    static void* cache[kMaxDevices] = {nullptr};
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) {
+        *st = NVFP4_ERR_CUDA;
+        return nullptr;
+    }
+    if (cache[d] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            *st = NVFP4_ERR_CUDA;
+            return nullptr;
+        }
+        cache[d] = p;
+    }
+    return cache[d];
+}
+
+}  // namespace
+
+extern "C" nvfp4_status moe_expert_forward_noalloc(const moe_layer_weights* w, const void* hidden,
+                                                   const int32_t* topk_idx, const float* topk_w,
+                                                   int32_t T, int32_t k, nvfp4_act_mode mode,
+                                                   float rms_eps, const void* residual, void* out,
+                                                   cudaStream_t stream) {
+    if (!w || T < 1 || k < 1) return NVFP4_ERR_INVALID_ARG;
+    const size_t need = moe_expert_forward_workspace_size(w, T, k, mode);
+    if (need == 0) return NVFP4_ERR_INVALID_ARG;
+    if (need > NVFP4MOE_NOALLOC_SCRATCH_BYTES) return NVFP4_ERR_WORKSPACE;  // beyond the fixed scratch
+    nvfp4_status st = NVFP4_OK;
+    void* scratch = noalloc_scratch(&st);
+    if (scratch == nullptr) return st;
+    // the previous call's contents remain: clear the region (its counters must start at zero)
+    if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    return moe_expert_forward(w, hidden, topk_idx, topk_w, T, k, mode, rms_eps, residual, out, scratch,
+                              need, stream);
+}
