@@ -199,6 +199,30 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
                                 cudaStream_t stream);
 
 /*
+ * moe_layer_forward - one whole MoE layer for 1..4 tokens in one call:
+ * moe_route_topk followed by moe_expert_forward (same arithmetic, same
+ * results), run as three kernels that hand their prepared operands to each
+ * other through the workspace (routing plan, quantised activations) and
+ * overlap each launch with the previous kernel's tail. The routing result is
+ * also returned in topk_idx / topk_w.
+ *   w, hidden, T, k, mode, rms_eps, residual, out: as moe_expert_forward
+ *   router_w, bias: as moe_route_topk (device float [E][H], [E])
+ *   topk_idx, topk_w: device out [T][k]
+ *   T <= 4, k <= 16, E <= 256 (NVFP4_ERR_UNSUPPORTED_SHAPE otherwise)
+ *   workspace: device, >= moe_layer_forward_workspace_size() bytes,
+ *              256-byte aligned, zeroed once by
+ *              moe_expert_forward_workspace_init and left zeroed by every
+ *              completed call; calls that share it must not overlap.
+ */
+size_t moe_layer_forward_workspace_size(const moe_layer_weights* w, int32_t T, int32_t k,
+                                        nvfp4_act_mode mode);
+nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w, const float* bias,
+                               const void* hidden, int32_t T, int32_t k, nvfp4_act_mode mode,
+                               float rms_eps, const void* residual, void* out, int32_t* topk_idx,
+                               float* topk_w, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/*
  * moe_expert_forward_noalloc - moe_expert_forward for callers that cannot
  * allocate device memory. The pages have no counterpart to this call.
  *

@@ -15,7 +15,8 @@ from . import _abi
 
 __all__ = ["NVFP4Matrix", "MoELayer", "NVFP4Error", "nvfp4_quantize", "moe_route_topk",
            "moe_expert_forward_workspace_size", "moe_expert_forward_workspace_init",
-           "moe_expert_forward", "moe_expert_forward_noalloc", "lm_head_gemv",
+           "moe_expert_forward", "moe_expert_forward_noalloc", "moe_layer_forward",
+           "moe_layer_forward_workspace_size", "lm_head_gemv",
            "nvfp4_status_string", "nvfp4_last_device_error",
            "W4A16", "W4A4", "PER_TENSOR", "PER_ROW", "GIVEN", "lib"]
 
@@ -176,6 +177,40 @@ def moe_expert_forward(layer: MoELayer, hidden, topk_idx, topk_w, mode=W4A4, res
                                workspace.numel(), _stream(stream))
     _check(st, "moe_expert_forward")
     return out
+
+
+def moe_layer_forward_workspace_size(layer: MoELayer, T, k, mode=W4A4) -> int:
+    w = layer.c()
+    return int(_L.moe_layer_forward_workspace_size(ctypes.byref(w), T, k, mode))
+
+
+def make_layer_workspace(layer: MoELayer, T, k, mode=W4A4, stream=None):
+    n = max(moe_layer_forward_workspace_size(layer, T, k, mode),
+            moe_expert_forward_workspace_size(layer, T, k, mode))
+    ws = torch.empty(n, dtype=torch.uint8, device=layer.up_codes.device)
+    moe_expert_forward_workspace_init(ws, stream)
+    return ws
+
+
+def moe_layer_forward(layer: MoELayer, hidden, k, mode=W4A4, residual=None, out=None, topk_idx=None,
+                      topk_w=None, workspace=None, rms_eps=0.0, stream=None):
+    """Router + experts + shared expert + combine of one layer (1..4 tokens);
+    returns (out, topk_idx, topk_w)."""
+    T = hidden.shape[0]
+    if out is None:
+        out = torch.empty_like(hidden)
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=hidden.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=hidden.device)
+    if workspace is None:
+        workspace = make_layer_workspace(layer, T, k, mode, stream)
+    w = layer.c()
+    st = _L.moe_layer_forward(ctypes.byref(w), _ptr(layer.router_w), _ptr(layer.router_b), _ptr(hidden), T, k,
+                              mode, float(rms_eps), _ptr(residual), _ptr(out), _ptr(topk_idx), _ptr(topk_w),
+                              _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "moe_layer_forward")
+    return out, topk_idx, topk_w
 
 
 def moe_expert_forward_noalloc(layer: MoELayer, hidden, topk_idx, topk_w, mode=W4A4, residual=None,

@@ -39,6 +39,14 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 
 __device__ __forceinline__ void set_dev_error(unsigned int bit) { atomicOr(&g_dev_error, bit); }
 
+// Programmatic dependent launch: the next kernel in the stream may start as
+// soon as every CTA of this one has called pdl_trigger(); pdl_wait() blocks
+// until the previous kernel has completed and its writes are visible. Code
+// before pdl_wait() may only touch arguments, read-only weights and shared
+// memory. Both are no-ops when the launch carries no programmatic edge.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
@@ -211,25 +219,38 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_
 // Lane l accumulates elements 8l + 256m .. 8l + 256m + 7 (m = 0, 1, ...) in
 // order with fused multiply-adds, then an xor-shuffle tree (commutative at
 // every level, so all lanes agree): the result does not depend on which
-// kernel runs it. K % 8 == 0; src/dst 16-byte aligned (dst may equal src).
+// kernel runs it. The row is read from global memory once, eight 16-byte
+// loads per lane in flight, parked raw in dst (shared memory), and normalised
+// there in place. K % 8 == 0; src (global) and dst (shared) 16-byte aligned.
 __device__ __forceinline__ void warp_rmsnorm_row(const uint16_t* src, uint16_t* dst, int K, float eps) {
     const int lane = threadIdx.x & 31;
     float ss = 0.0f;
-    for (int i = 8 * lane; i < K; i += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int i0 = 8 * lane; i0 < K; i0 += 256 * 8) {
+        uint4 v[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
-            ss = __fmaf_rn(a, a, ss);
-            ss = __fmaf_rn(b, b, ss);
+        for (int m = 0; m < 8; ++m) {
+            const int i = i0 + 256 * m;
+            v[m] = i < K ? __ldcg(reinterpret_cast<const uint4*>(src + i)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int i = i0 + 256 * m;
+            if (i >= K) break;
+            *reinterpret_cast<uint4*>(dst + i) = v[m];
+            const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+                ss = __fmaf_rn(a, a, ss);
+                ss = __fmaf_rn(b, b, ss);
+            }
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps)));
     for (int i = 8 * lane; i < K; i += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + i);
+        const uint4 v = *reinterpret_cast<const uint4*>(dst + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
 #pragma unroll
@@ -241,6 +262,27 @@ __device__ __forceinline__ void warp_rmsnorm_row(const uint16_t* src, uint16_t* 
         }
         *reinterpret_cast<uint4*>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
     }
+    __syncwarp();
+}
+
+// Copy one bf16 row (global, written by an earlier kernel) into dst, one warp,
+// eight 16-byte loads per lane in flight.
+__device__ __forceinline__ void warp_copy_row(const uint16_t* src, uint16_t* dst, int K) {
+    const int lane = threadIdx.x & 31;
+    for (int i0 = 8 * lane; i0 < K; i0 += 256 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int i = i0 + 256 * m;
+            v[m] = i < K ? __ldcg(reinterpret_cast<const uint4*>(src + i)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int i = i0 + 256 * m;
+            if (i < K) *reinterpret_cast<uint4*>(dst + i) = v[m];
+        }
+    }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------- MMA

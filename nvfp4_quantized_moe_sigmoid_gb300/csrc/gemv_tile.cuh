@@ -1,8 +1,8 @@
 // gemv_tile.cuh - the inner engine of every NVFP4 GEMV/skinny GEMM here:
-// one warp computes a 16-row x 8-column tile D = W_tile . B, where W_tile is
-// 16 rows x K of an NVFP4 matrix staged in shared memory (canonical layout:
-// codes [16][K/2], then scales [16][K/16]) and B holds up to 8 activation
-// columns as f16 rows of length K.
+// a 16-row x 8-column tile D = W_tile . B, where W_tile is 16 rows x K of an
+// NVFP4 matrix staged in shared memory (canonical layout: codes [16][K/2],
+// then scales [16][K/16]) and B holds up to 8 activation columns as f16 rows
+// of length K. Two warps share a tile, each taking half of its 128-k chunks.
 //
 // Arithmetic: each weight is decoded to f16 as E2M1 * E4M3 (cvt.rn.f16x2.e2m1x2
 // and cvt.rn.f16x2.e4m3x2, then one f16 multiply). The product has at most six
@@ -23,44 +23,58 @@
 
 namespace nvfp4moe {
 
-// Accumulates into acc: thread (g, q) holds acc[0..1] = rows g, cols 2q, 2q+1;
-// acc[2..3] = rows g+8, cols 2q, 2q+1. `bcol` points to the f16 row of column
-// g (K elements, 16-byte aligned) or is null for an all-zero column.
-// K % 64 == 0.
-//
-// Latency: the next chunk's code, scale and B words are loaded while the
-// current chunk is decoded, and the MMAs of a chunk go to four independent
-// accumulator sets (summed at the end), so one warp keeps several MMAs and
-// shared-memory loads in flight instead of one dependent chain.
-struct TileChunk {
-    uint4 wa, wb, b0, b1, b2, b3;
-    uint32_t sva, svb;
+struct ChunkRegs {
+    uint4 wa, wb;       // 16 code bytes of rows g and g + 8
+    uint32_t sva, svb;  // two scale bytes of rows g and g + 8
 };
 
-__device__ __forceinline__ void tile_load_chunk(TileChunk& t, const uint8_t* ca, const uint8_t* cb,
-                                                const uint8_t* sa, const uint8_t* sb, const __half* bp,
-                                                int c, bool valid) {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    t.wa = t.wb = t.b0 = t.b1 = t.b2 = t.b3 = z;
-    t.sva = t.svb = 0;
+__device__ __forceinline__ void chunk_load(ChunkRegs& r, const uint8_t* ca, const uint8_t* cb,
+                                           const uint8_t* sa, const uint8_t* sb, int c, bool valid) {
     if (valid) {
-        t.wa = *reinterpret_cast<const uint4*>(ca + 64 * c);
-        t.wb = *reinterpret_cast<const uint4*>(cb + 64 * c);
-        t.sva = *reinterpret_cast<const uint16_t*>(sa + 8 * c);
-        t.svb = *reinterpret_cast<const uint16_t*>(sb + 8 * c);
-        if (bp) {
-            const uint4* b = reinterpret_cast<const uint4*>(bp + 128 * c);
-            t.b0 = b[0];
-            t.b1 = b[1];
-            t.b2 = b[2];
-            t.b3 = b[3];
-        }
+        r.wa = *reinterpret_cast<const uint4*>(ca + 64 * c);
+        r.wb = *reinterpret_cast<const uint4*>(cb + 64 * c);
+        r.sva = *reinterpret_cast<const uint16_t*>(sa + 8 * c);
+        r.svb = *reinterpret_cast<const uint16_t*>(sb + 8 * c);
+    } else {
+        r.wa = r.wb = make_uint4(0, 0, 0, 0);
+        r.sva = r.svb = 0;
     }
 }
 
+// Four MMA accumulator sets (one per 32-k quarter of a chunk) keep four
+// independent dependency chains in flight.
+__device__ __forceinline__ void chunk_mma(const ChunkRegs& r, const __half* bp, int c, bool valid,
+                                          float (&a4)[4][4]) {
+    const uint32_t sA = e4m3x2_to_f16x2(r.sva), sB = e4m3x2_to_f16x2(r.svb);
+    const uint32_t sA0 = bcast_lo(sA), sA1 = bcast_hi(sA);
+    const uint32_t sB0 = bcast_lo(sB), sB1 = bcast_hi(sB);
+    const uint32_t wA[4] = {r.wa.x, r.wa.y, r.wa.z, r.wa.w};
+    const uint32_t wB[4] = {r.wb.x, r.wb.y, r.wb.z, r.wb.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        uint4 bv = make_uint4(0, 0, 0, 0);
+        if (valid && bp) bv = *reinterpret_cast<const uint4*>(bp + 128 * c + 8 * h);
+        uint32_t fa[4], fb[4];
+        e2m1x8_to_f16x8(wA[h], fa);
+        e2m1x8_to_f16x8(wB[h], fb);
+        const uint32_t scA = h < 2 ? sA0 : sA1;
+        const uint32_t scB = h < 2 ? sB0 : sB1;
+        mma_16816(a4[h], hmul2(fa[0], scA), hmul2(fb[0], scB), hmul2(fa[1], scA), hmul2(fb[1], scB), bv.x,
+                  bv.y);
+        mma_16816(a4[h], hmul2(fa[2], scA), hmul2(fb[2], scB), hmul2(fa[3], scA), hmul2(fb[3], scB), bv.z,
+                  bv.w);
+    }
+}
+
+// Accumulates chunks [c0, c1) of the tile into acc: thread (g, q) holds
+// acc[0..1] = rows g, cols 2q, 2q+1; acc[2..3] = rows g+8, cols 2q, 2q+1.
+// `bcol` points to the f16 row of column g (K elements, 16-byte aligned) or
+// is null for an all-zero column. K % 64 == 0. The next chunk's code and scale
+// words are loaded while the current one is decoded (ping-pong registers).
 __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes,
                                               const uint8_t* __restrict__ tscales, int K,
-                                              const __half* __restrict__ bcol, float (&acc)[4]) {
+                                              const __half* __restrict__ bcol, int c0, int c1,
+                                              float (&acc)[4]) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     const int KB = K >> 1, KS = K >> 4;
@@ -71,6 +85,7 @@ __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes
     const __half* bp = bcol ? bcol + 32 * q : nullptr;
     const int nchunks = (K + 127) >> 7;
     const bool half_tail = (K & 127) != 0;
+    auto valid = [&](int c) { return !(half_tail && c == nchunks - 1 && q >= 2); };
 
     float a4[4][4];
 #pragma unroll
@@ -78,31 +93,16 @@ __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes
 #pragma unroll
         for (int v = 0; v < 4; ++v) a4[h][v] = 0.0f;
 
-    TileChunk cur, nxt;
-    tile_load_chunk(cur, ca, cb, sa, sb, bp, 0, !(half_tail && nchunks == 1 && q >= 2));
-    for (int c = 0; c < nchunks; ++c) {
-        if (c + 1 < nchunks)
-            tile_load_chunk(nxt, ca, cb, sa, sb, bp, c + 1, !(half_tail && c + 2 == nchunks && q >= 2));
-        const uint32_t sA = e4m3x2_to_f16x2(cur.sva), sB = e4m3x2_to_f16x2(cur.svb);
-        const uint32_t sA0 = bcast_lo(sA), sA1 = bcast_hi(sA);
-        const uint32_t sB0 = bcast_lo(sB), sB1 = bcast_hi(sB);
-        const uint32_t wA[4] = {cur.wa.x, cur.wa.y, cur.wa.z, cur.wa.w};
-        const uint32_t wB[4] = {cur.wb.x, cur.wb.y, cur.wb.z, cur.wb.w};
-        const uint4 bq[4] = {cur.b0, cur.b1, cur.b2, cur.b3};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            uint32_t fa[4], fb[4];
-            e2m1x8_to_f16x8(wA[h], fa);
-            e2m1x8_to_f16x8(wB[h], fb);
-            const uint32_t scA = h < 2 ? sA0 : sA1;
-            const uint32_t scB = h < 2 ? sB0 : sB1;
-            mma_16816(a4[h], hmul2(fa[0], scA), hmul2(fb[0], scB), hmul2(fa[1], scA), hmul2(fb[1], scB),
-                      bq[h].x, bq[h].y);
-            mma_16816(a4[h], hmul2(fa[2], scA), hmul2(fb[2], scB), hmul2(fa[3], scA), hmul2(fb[3], scB),
-                      bq[h].z, bq[h].w);
-        }
-        cur = nxt;
+    ChunkRegs r0, r1;
+    if (c0 < c1) chunk_load(r0, ca, cb, sa, sb, c0, valid(c0));
+    int c = c0;
+    for (; c + 1 < c1; c += 2) {
+        chunk_load(r1, ca, cb, sa, sb, c + 1, valid(c + 1));
+        chunk_mma(r0, bp, c, valid(c), a4);
+        if (c + 2 < c1) chunk_load(r0, ca, cb, sa, sb, c + 2, valid(c + 2));
+        chunk_mma(r1, bp, c + 1, valid(c + 1), a4);
     }
+    if (c < c1) chunk_mma(r0, bp, c, valid(c), a4);
 #pragma unroll
     for (int v = 0; v < 4; ++v) acc[v] += (a4[0][v] + a4[1][v]) + (a4[2][v] + a4[3][v]);
 }
@@ -110,28 +110,31 @@ __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes
 // ------------------------------------------------------------------ staging
 // A ring of `nstages` shared-memory stages, each holding one 16-row tile
 // (codes then scales), filled by one producer thread with bulk TMA copies.
-// Stage s is owned by consumer warp s: local item li goes to stage and warp
-// li % nstages, so every stage's uses are waited on, in order, by one warp.
-// (An mbarrier parity wait names the current or the immediately preceding
-// phase; a waiter for use u must not start while the barrier is still in
-// phase u - 2, which single ownership guarantees.) full[s] completes when the
-// tile has landed, empty[s] when its warp has finished reading it.
-constexpr int kConsumerWarps = 8;
-constexpr int kMaxStages = kConsumerWarps;
+// Stage s is owned by the warp pair (s, s + 8): local item li goes to stage
+// li % nstages, whose two warps each take half of the tile's k-chunks and
+// both release the stage. Every use of a stage is therefore waited on, in
+// order, by the same warps. (An mbarrier parity wait names the current or
+// the immediately preceding phase; a waiter for use u must not start while
+// the barrier is still in phase u - 2, which fixed ownership guarantees.)
+constexpr int kPairs = 8;
+constexpr int kConsumerWarps = 2 * kPairs;
+constexpr int kMaxStages = kPairs;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kConsumerThreads = kConsumerWarps * 32;
 
 struct Ring {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     int uses[kMaxStages];  // producer-side count of fills per stage
     int abort;
+    float xred[kPairs][2][32][4];  // partial tiles passed from warp s+8 to warp s
 };
 
 __device__ __forceinline__ void ring_init(Ring& r, int nstages) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
             mbar_init(&r.full[s], 1);
-            mbar_init(&r.empty[s], 1);
+            mbar_init(&r.empty[s], 2);
             r.uses[s] = 0;
         }
         r.abort = 0;
@@ -139,7 +142,7 @@ __device__ __forceinline__ void ring_init(Ring& r, int nstages) {
     }
 }
 
-// Producer side: fill stage for local item li with a tile of 16 rows.
+// Producer side: fill the stage of local item li with a 16-row tile.
 // Returns false (and flags the ring) if the stage never became free.
 __device__ __forceinline__ bool ring_fill(Ring& r, uint8_t* ring_base, int stage_bytes, int nstages,
                                           int li, const uint8_t* codes, const uint8_t* scales, int K) {
@@ -183,68 +186,267 @@ __device__ __forceinline__ void ring_drain(Ring& r, int nstages) {
     }
 }
 
+// All consumer warps (named barrier 1).
 __device__ __forceinline__ void consumer_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// The two warps of pair s (named barrier 2 + s); returns the AND of `pred`
+// over both warps, so that both take the same decision.
+__device__ __forceinline__ bool pair_bar_and(int s, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.and.pred q, %2, 64, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"(pred ? 1u : 0u), "r"(2 + s)
+        : "memory");
+    return out != 0;
+}
+
+// One staged tile, split between the two warps of its pair: half h computes
+// its half of the k-chunks; half 1 hands its partial to half 0 through shared
+// memory. Returns true for the warp that holds the finished tile in acc (half
+// 0); `ok` is false for both warps if either one timed out waiting.
+__device__ __forceinline__ bool pair_tile(Ring& r, int nstages, int li, const uint8_t* st, int K,
+                                          const __half* bcol, float (&acc)[4], bool& ok) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = warp % kPairs, half = warp / kPairs;
+    const int nc = (K + 127) >> 7, mid = (nc + 1) >> 1;
+    const bool got = ring_acquire(r, nstages, li);
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+    if (got) tile_mma_16x8(st, st + 16 * (K >> 1), K, bcol, half ? mid : 0, half ? nc : mid, acc);
+    ring_release(r, nstages, li);
+    const int u = (li / nstages) & 1;
+    if (half) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) r.xred[s][u][lane][v] = acc[v];
+    }
+    ok = pair_bar_and(s, got);
+    if (half || !ok) return false;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) acc[v] += r.xred[s][u][lane][v];
+    return true;
 }
 
 // Quantise (W4A4) or convert (W4A16) nrows bf16 rows of length K into f16
 // B-operand rows; W4A4 also writes each row's global to gout. Rows with
-// src == null are zero-filled. Runs on the 256 consumer threads.
+// src == null are zero-filled. Runs on the consumer threads. GSRC: the rows
+// are global memory written by an earlier kernel (read through L2). Each
+// thread loads all of its blocks (up to kBRegBlocks) before using any, and
+// keeps them in registers between the row-amax and the quantisation passes.
+template <bool GSRC>
+__device__ __forceinline__ uint4 ld_row16(const uint16_t* p) {
+    if (GSRC) return __ldcg(reinterpret_cast<const uint4*>(p));
+    return *reinterpret_cast<const uint4*>(p);
+}
+
+constexpr int kBRegBlocks = 4;
+
 template <bool W4A4>
+__device__ __forceinline__ void b_block_store(const uint4& u0, const uint4& u1, float g, uint4* d) {
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        v[2 * j] = __uint_as_float(w[j] << 16);
+        v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    uint32_t o[8];
+    if (W4A4) {
+        dequant_block16_f16(quantize_block16(v, g), o);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const __half2 h2 = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+            o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+    }
+    d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <bool W4A4, bool GSRC>
 __device__ __forceinline__ void prepare_b_rows(const uint16_t* const* src, int nrows, int K,
                                                __half* dst, float* gout, unsigned int* red) {
-    const int ctid = threadIdx.x;  // 0..255
+    const int ctid = threadIdx.x;  // consumer thread index
     const int nb = K >> 4;
+    const int total = nrows * nb;
     if (W4A4) {
         if (ctid < nrows) red[ctid] = 0u;
         consumer_bar();
-        for (int i = ctid; i < nrows * nb; i += kConsumerWarps * 32) {
+    }
+    uint4 u[kBRegBlocks][2];
+#pragma unroll
+    for (int m = 0; m < kBRegBlocks; ++m) {
+        const int i = ctid + m * kConsumerThreads;
+        u[m][0] = u[m][1] = make_uint4(0, 0, 0, 0);
+        if (i < total) {
             const int r = i / nb, b = i % nb;
-            if (!src[r]) continue;
-            const uint4* p = reinterpret_cast<const uint4*>(src[r] + 16 * b);
-            const uint4 u0 = p[0], u1 = p[1];
-            const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-            float m = 0.0f;
+            if (src[r]) {
+                u[m][0] = ld_row16<GSRC>(src[r] + 16 * b);
+                u[m][1] = ld_row16<GSRC>(src[r] + 16 * b + 8);
+            }
+        }
+    }
+    if (W4A4) {
+#pragma unroll
+        for (int m = 0; m < kBRegBlocks; ++m) {
+            const int i = ctid + m * kConsumerThreads;
+            if (i >= total) break;
+            const uint32_t w[8] = {u[m][0].x, u[m][0].y, u[m][0].z, u[m][0].w,
+                                   u[m][1].x, u[m][1].y, u[m][1].z, u[m][1].w};
+            float mx = 0.0f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
-                m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+                mx = fmaxf(mx, fabsf(__uint_as_float(w[j] << 16)));
+                mx = fmaxf(mx, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
             }
-            atomicMax(&red[r], __float_as_uint(m));
+            atomicMax(&red[i / nb], __float_as_uint(mx));
+        }
+        // rows longer than the register window: amax over the rest, reloading
+        for (int i = ctid + kBRegBlocks * kConsumerThreads; i < total; i += kConsumerThreads) {
+            const int r = i / nb, b = i % nb;
+            if (!src[r]) continue;
+            const uint4 a0 = ld_row16<GSRC>(src[r] + 16 * b), a1 = ld_row16<GSRC>(src[r] + 16 * b + 8);
+            const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float mx = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                mx = fmaxf(mx, fabsf(__uint_as_float(w[j] << 16)));
+                mx = fmaxf(mx, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+            }
+            atomicMax(&red[r], __float_as_uint(mx));
         }
         consumer_bar();
         if (ctid < nrows) gout[ctid] = __fdiv_rn(__uint_as_float(red[ctid]), 2688.0f);
     }
-    for (int i = ctid; i < nrows * nb; i += kConsumerWarps * 32) {
+#pragma unroll
+    for (int m = 0; m < kBRegBlocks; ++m) {
+        const int i = ctid + m * kConsumerThreads;
+        if (i >= total) break;
         const int r = i / nb, b = i % nb;
-        uint4* d = reinterpret_cast<uint4*>(dst + (size_t)r * K + 16 * b);
-        if (!src[r]) {
-            d[0] = make_uint4(0, 0, 0, 0);
-            d[1] = make_uint4(0, 0, 0, 0);
-            continue;
+        const float g = W4A4 ? __fdiv_rn(__uint_as_float(red[r]), 2688.0f) : 0.0f;
+        b_block_store<W4A4>(u[m][0], u[m][1], g, reinterpret_cast<uint4*>(dst + (size_t)r * K + 16 * b));
+    }
+    for (int i = ctid + kBRegBlocks * kConsumerThreads; i < total; i += kConsumerThreads) {
+        const int r = i / nb, b = i % nb;
+        uint4 a0 = make_uint4(0, 0, 0, 0), a1 = make_uint4(0, 0, 0, 0);
+        if (src[r]) {
+            a0 = ld_row16<GSRC>(src[r] + 16 * b);
+            a1 = ld_row16<GSRC>(src[r] + 16 * b + 8);
         }
-        const uint4* p = reinterpret_cast<const uint4*>(src[r] + 16 * b);
-        const uint4 u0 = p[0], u1 = p[1];
-        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        float v[16];
+        const float g = W4A4 ? __fdiv_rn(__uint_as_float(red[r]), 2688.0f) : 0.0f;
+        b_block_store<W4A4>(a0, a1, g, reinterpret_cast<uint4*>(dst + (size_t)r * K + 16 * b));
+    }
+    consumer_bar();
+}
+
+
+// Unit-weight RMS norm of nrows bf16 rows (global, written by an earlier
+// kernel) into dst (shared memory), by the 16 consumer warps together:
+//   inv = 1 / sqrt(sum_i x_i^2 / K + eps),  y_i = bf16(x_i * inv).
+// The summation order is fixed by element index alone: chunk c holds elements
+// [256c, 256c + 256); lane l accumulates its eight elements 256c + 8l .. +7 in
+// order with fused multiply-adds; an xor-shuffle tree (commutative at each
+// level) gives the chunk sum; the chunk sums are added in chunk order. Every
+// kernel that calls this therefore computes the same bits. K % 8 == 0,
+// K <= 256 * kNormMaxChunks, nrows <= kNormMaxRows.
+constexpr int kNormMaxRows = 8;
+constexpr int kNormMaxChunks = 64;
+struct NormScratch {
+    float part[kNormMaxRows][kNormMaxChunks];
+    float inv[kNormMaxRows];
+};
+
+__device__ __forceinline__ void cta_rmsnorm_rows(const uint16_t* src, int nrows, int K, float eps, uint16_t* dst,
+                                                 NormScratch& ns) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nch = (K + 255) >> 8;
+    for (int item = warp; item < nrows * nch; item += kConsumerWarps) {
+        const int r = item / nch, c = item % nch;
+        const int i = 256 * c + 8 * lane;
+        float ss = 0.0f;
+        if (i < K) {
+            const uint4 v = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)r * K + i));
+            *reinterpret_cast<uint4*>(dst + (size_t)r * K + i) = v;
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            v[2 * j] = __uint_as_float(w[j] << 16);
-            v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-        }
-        uint32_t o[8];
-        if (W4A4) {
-            const float g = __fdiv_rn(__uint_as_float(red[r]), 2688.0f);
-            dequant_block16_f16(quantize_block16(v, g), o);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const __half2 h2 = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
-                o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            for (int j = 0; j < 4; ++j) {
+                const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+                ss = __fmaf_rn(a, a, ss);
+                ss = __fmaf_rn(b, b, ss);
             }
         }
-        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        if (lane == 0) ns.part[r][c] = ss;
+    }
+    consumer_bar();
+    if (threadIdx.x < nrows) {
+        float s = 0.0f;
+        for (int c = 0; c < nch; ++c) s = __fadd_rn(s, ns.part[threadIdx.x][c]);
+        ns.inv[threadIdx.x] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, static_cast<float>(K)), eps)));
+    }
+    consumer_bar();
+    for (int i = 8 * threadIdx.x; i < nrows * K; i += 8 * kConsumerThreads) {
+        const float inv = ns.inv[i / K];
+        const uint4 v = *reinterpret_cast<const uint4*>(dst + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat16 lo = __float2bfloat16_rn(__fmul_rn(__uint_as_float(w[j] << 16), inv));
+            const __nv_bfloat16 hi = __float2bfloat16_rn(__fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), inv));
+            o[j] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&lo)) |
+                   (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    consumer_bar();
+}
+
+// Copy nrows bf16 rows (global, written by an earlier kernel) into dst, all
+// consumer threads.
+__device__ __forceinline__ void cta_copy_rows(const uint16_t* src, int nrows, int K, uint16_t* dst) {
+    for (int i = 8 * threadIdx.x; i < nrows * K; i += 8 * kConsumerThreads)
+        *reinterpret_cast<uint4*>(dst + i) = __ldcg(reinterpret_cast<const uint4*>(src + i));
+    consumer_bar();
+}
+
+// B rows from global bf16 rows whose globals are already known: gk[r] holds
+// the row amax bits (W4A4; g = amax / 2688), so every block is quantised
+// independently in one pass. Rows with src == null are zero-filled.
+template <bool W4A4>
+__device__ __forceinline__ void prepare_b_rows_known_amax(const uint16_t* const* src, int nrows, int K, __half* dst,
+                                                          const unsigned int* amax_bits, float* gout) {
+    const int ctid = threadIdx.x;
+    const int nb = K >> 4;
+    if (W4A4 && ctid < nrows) gout[ctid] = __fdiv_rn(__uint_as_float(amax_bits[ctid]), 2688.0f);
+    for (int i0 = ctid; i0 < nrows * nb; i0 += kBRegBlocks * kConsumerThreads) {
+        uint4 u[kBRegBlocks][2];
+#pragma unroll
+        for (int m = 0; m < kBRegBlocks; ++m) {
+            const int i = i0 + m * kConsumerThreads;
+            u[m][0] = u[m][1] = make_uint4(0, 0, 0, 0);
+            if (i < nrows * nb) {
+                const int r = i / nb, b = i % nb;
+                if (src[r]) {
+                    u[m][0] = __ldcg(reinterpret_cast<const uint4*>(src[r] + 16 * b));
+                    u[m][1] = __ldcg(reinterpret_cast<const uint4*>(src[r] + 16 * b + 8));
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kBRegBlocks; ++m) {
+            const int i = i0 + m * kConsumerThreads;
+            if (i >= nrows * nb) break;
+            const int r = i / nb, b = i % nb;
+            const float g = W4A4 ? __fdiv_rn(__uint_as_float(amax_bits[r]), 2688.0f) : 0.0f;
+            b_block_store<W4A4>(u[m][0], u[m][1], g, reinterpret_cast<uint4*>(dst + (size_t)r * K + 16 * b));
+        }
     }
     consumer_bar();
 }

@@ -4,9 +4,10 @@
 // lm_head NVFP4 weight-only W4A16).
 //
 // A pure HBM stream of the weight matrix: persistent CTAs each take a
-// contiguous range of 16-row tiles, one producer thread stages them with bulk
-// TMA copies, eight consumer warps run the tensor-core tile with up to 8 token
-// columns (bf16 activations converted once per CTA to f16).
+// contiguous range of 16-row tiles; one producer thread stages them with bulk
+// TMA copies (the first ring-full before waiting on the previous kernel),
+// eight warp pairs run the tensor-core tile with up to 8 token columns
+// (bf16 activations, RMS-normalised when asked, converted once per CTA to f16).
 #pragma once
 
 #include "gemv_tile.cuh"
@@ -38,42 +39,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
     const int stage_bytes = 9 * a.H;
     const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
     ring_init(ring, nst);
+    pdl_trigger();
     __syncthreads();
 
     const int64_t N = a.V >> 4;
     const int64_t ib = N * blockIdx.x / gridDim.x, ie = N * (blockIdx.x + 1) / gridDim.x;
     const int n = static_cast<int>(ie - ib);
     uint8_t* ring_base = smem;
-    __half* xb = reinterpret_cast<__half*>(smem + a.ring_bytes);          // [T][H] f16
+    __half* xb = reinterpret_cast<__half*>(smem + a.ring_bytes);             // [T][H] f16
     uint16_t* xn = reinterpret_cast<uint16_t*>(xb + (size_t)kLmMaxT * a.H);  // [T][H] bf16
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {
+            // the weights do not depend on the previous kernel: a ring-full is
+            // issued before waiting on it
             for (int li = 0; li < n; ++li) {
+                if (li == nst) pdl_wait();
                 const int64_t row = 16 * (ib + li);
-                if (!ring_fill(ring, ring_base, stage_bytes, nst, li,
-                               a.codes + row * (a.H >> 1), a.scales + row * (a.H >> 4), a.H))
+                if (!ring_fill(ring, ring_base, stage_bytes, nst, li, a.codes + row * (a.H >> 1),
+                               a.scales + row * (a.H >> 4), a.H))
                     break;
             }
         }
+        pdl_wait();
     } else {
-        if (a.rms_eps > 0.0f) {
-            if (warp < a.T) warp_rmsnorm_row(a.hidden + (size_t)warp * a.H, xn + (size_t)warp * a.H, a.H, a.rms_eps);
-            if (threadIdx.x < a.T) srcs[threadIdx.x] = xn + (size_t)threadIdx.x * a.H;
-        } else {
-            if (threadIdx.x < a.T) srcs[threadIdx.x] = a.hidden + (size_t)threadIdx.x * a.H;
+        pdl_wait();
+        if (warp < a.T) {
+            if (a.rms_eps > 0.0f)
+                warp_rmsnorm_row(a.hidden + (size_t)warp * a.H, xn + (size_t)warp * a.H, a.H, a.rms_eps);
+            else
+                warp_copy_row(a.hidden + (size_t)warp * a.H, xn + (size_t)warp * a.H, a.H);
         }
+        if (threadIdx.x < a.T) srcs[threadIdx.x] = xn + (size_t)threadIdx.x * a.H;
         consumer_bar();
-        prepare_b_rows<false>(srcs, a.T, a.H, xb, nullptr, nullptr);
+        prepare_b_rows<false, false>(srcs, a.T, a.H, xb, nullptr, nullptr);
         const float gw = __ldg(a.global);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
-        for (int li = warp; warp < nst && li < n; li += nst) {
-            if (!ring_acquire(ring, nst, li)) break;
+        const int s = warp % kPairs;
+        for (int li = s; s < nst && li < n; li += nst) {
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma_16x8(st, st + 16 * (a.H >> 1), a.H, bcol, acc);
-            ring_release(ring, nst, li);
+            float acc[4];
+            bool ok;
+            const bool mine = pair_tile(ring, nst, li, st, a.H, bcol, acc, ok);
+            if (!ok) break;
+            if (!mine) continue;
             const int64_t row0 = 16 * (ib + li);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {

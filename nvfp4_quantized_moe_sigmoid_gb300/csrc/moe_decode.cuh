@@ -3,20 +3,23 @@
 // worklog", Step 5). At this size the layer is a stream of NVFP4 weights
 // (worklog, Interlude), so both kernels are persistent HBM streams:
 //
-//   up kernel   : items = 16-row tiles of every selected expert's up_proj and
-//                 of the shared expert's up_proj. Epilogue: relu^2 -> bf16
+//   up kernel   : items = 16-row tiles of the shared expert's up_proj and of
+//                 every selected expert's up_proj. Epilogue: relu^2 -> bf16
 //                 intermediate rows in the workspace.
-//   down kernel : items = 16-row tiles of every selected expert's down_proj
-//                 and of the shared expert's down_proj. Epilogue: gate-weighted
+//   down kernel : items = 16-row tiles of the shared expert's down_proj and of
+//                 every selected expert's down_proj. Epilogue: gate-weighted
 //                 FP32 partial rows; the warp that completes a 16-row output
 //                 tile (per-tile counter) sums the partials in a fixed order,
 //                 adds the residual and writes bf16.
 //
-// Each CTA takes a contiguous, cost-balanced range of items; one producer
-// thread streams the range through a ring of shared-memory stages with bulk
-// TMA copies, eight consumer warps run the tensor-core tile (gemv_tile.cuh).
-// Experts chosen by several tokens are read once per step: items are per
-// unique expert, and the MMA's columns are the tokens.
+// Each CTA takes an even share of the shared-expert tiles and an even share of
+// the routed tiles. The shared-expert tiles do not depend on the routing, so
+// their bulk copies are issued before the kernel waits on the previous one
+// (programmatic dependent launch); the routed ones follow once the plan is
+// built. One producer thread streams the tiles through the staging ring,
+// sixteen consumer warps (eight pairs) run the tensor-core tile. Experts
+// chosen by several tokens are read once per step: items are per unique
+// expert and the MMA's columns are the tokens.
 #pragma once
 
 #include "gemv_tile.cuh"
@@ -28,11 +31,11 @@ constexpr int kDecodeMaxK = 16;
 constexpr int kDecodeMaxU = kDecodeMaxT * kDecodeMaxK;
 
 struct DecodePlan {
-    int U;                                 // unique experts this step
-    int expert[kDecodeMaxU];               // ascending expert ids
+    int U;                                    // unique experts this step
+    int expert[kDecodeMaxU];                  // ascending expert ids
     int8_t choice[kDecodeMaxU][kDecodeMaxT];  // j with topk_idx[t][j] == expert, else -1
-    float gate[kDecodeMaxU][kDecodeMaxT];  // topk_w[t][j] or 0
-    unsigned int bits[8];                  // E <= 256 bitmap
+    float gate[kDecodeMaxU][kDecodeMaxT];     // topk_w[t][j] or 0
+    unsigned int bits[8];                     // E <= 256 bitmap
 };
 
 // Every CTA builds the same plan from topk_idx (T*k <= 64 entries).
@@ -49,7 +52,7 @@ __device__ __forceinline__ void build_plan(DecodePlan& p, const int32_t* __restr
     const int P = T * k;
     int e = -1;
     if (tid < P) {
-        e = __ldg(topk_idx + tid);
+        e = __ldcg(topk_idx + tid);
         if (e < 0 || e >= E) {
             if (blockIdx.x == 0) set_dev_error(kErrBadInput);
             e = -1;
@@ -63,7 +66,7 @@ __device__ __forceinline__ void build_plan(DecodePlan& p, const int32_t* __restr
         for (int w = 0; w < (e >> 5); ++w) slot += __popc(p.bits[w]);
         p.expert[slot] = e;
         p.choice[slot][tid / k] = static_cast<int8_t>(tid % k);
-        p.gate[slot][tid / k] = __ldg(topk_w + tid);
+        p.gate[slot][tid / k] = __ldcg(topk_w + tid);
     }
     if (tid == 0) {
         int u = 0;
@@ -72,6 +75,8 @@ __device__ __forceinline__ void build_plan(DecodePlan& p, const int32_t* __restr
     }
     __syncthreads();
 }
+
+__device__ __forceinline__ int64_t share_begin(int64_t n, int b, int G) { return n * b / G; }
 
 struct UpArgs {
     const uint8_t* codes;   // routed up [E][I][H/2]
@@ -104,59 +109,86 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_up_decode(const UpArgs a) {
     const int stage_bytes = 9 * a.H;  // 16 rows x (H/2 code bytes + H/16 scale bytes)
     const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
     ring_init(ring, nst);
+    pdl_trigger();
+    __syncthreads();
+
+    const int G = gridDim.x, b = blockIdx.x;
+    const int RI = a.I >> 4, RS = a.S >> 4;
+    const int64_t sb = share_begin(RS, b, G), se = share_begin(RS, b + 1, G);
+    const int n_sh = static_cast<int>(se - sb);
+    uint8_t* ring_base = smem;
+    __half* xb = reinterpret_cast<__half*>(smem + a.ring_bytes);             // [T][H] f16 B operand
+    uint16_t* xn = reinterpret_cast<uint16_t*>(xb + (size_t)a.T * a.H);      // [T][H] normalised bf16
+
+    auto sh_tile = [&](int64_t r, const uint8_t*& c, const uint8_t*& s) {
+        c = a.sh_codes + 16 * r * (a.H >> 1);
+        s = a.sh_scales + 16 * r * (a.H >> 4);
+    };
+    // shared-expert weights do not depend on the previous kernel: stage them first
+    const int pre = min(n_sh, nst);
+    if (warp == kConsumerWarps && lane == 0) {
+        for (int li = 0; li < pre; ++li) {
+            const uint8_t *c, *s;
+            sh_tile(sb + li, c, s);
+            ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, a.H);
+        }
+    }
+    pdl_wait();
     build_plan(plan, a.topk_idx, a.topk_w, a.T, a.k, a.E);  // contains __syncthreads
 
-    const int RI = a.I >> 4, RS = a.S >> 4;
     const int U = plan.U;
-    const int64_t N = (int64_t)U * RI + RS;
-    const int64_t ib = N * blockIdx.x / gridDim.x, ie = N * (blockIdx.x + 1) / gridDim.x;
-    const int n = static_cast<int>(ie - ib);
-    uint8_t* ring_base = smem;
-    __half* xb = reinterpret_cast<__half*>(smem + a.ring_bytes);  // [T][H] f16 B operand
-    uint16_t* xn = reinterpret_cast<uint16_t*>(xb + (size_t)a.T * a.H);  // [T][H] normalised bf16
-
-    auto item = [&](int64_t i, const uint8_t*& c, const uint8_t*& s) {
-        if (i < (int64_t)U * RI) {
+    const int64_t NR = (int64_t)U * RI;
+    const int64_t rb = share_begin(NR, b, G), re = share_begin(NR, b + 1, G);
+    const int n = n_sh + static_cast<int>(re - rb);
+    auto item = [&](int li, const uint8_t*& c, const uint8_t*& s) {
+        if (li < n_sh) {
+            sh_tile(sb + li, c, s);
+        } else {
+            const int64_t i = rb + (li - n_sh);
             const int u = static_cast<int>(i / RI), r = static_cast<int>(i % RI);
             const int64_t row = (int64_t)plan.expert[u] * a.I + 16 * r;
             c = a.codes + row * (a.H >> 1);
             s = a.scales + row * (a.H >> 4);
-        } else {
-            const int64_t row = 16 * (i - (int64_t)U * RI);
-            c = a.sh_codes + row * (a.H >> 1);
-            s = a.sh_scales + row * (a.H >> 4);
         }
     };
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {
-            for (int li = 0; li < n; ++li) {
+            for (int li = pre; li < n; ++li) {
                 const uint8_t *c, *s;
-                item(ib + li, c, s);
+                item(li, c, s);
                 if (!ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, a.H)) break;
             }
         }
     } else {
-        if (a.rms_eps > 0.0f) {
-            if (warp < a.T) warp_rmsnorm_row(a.hidden + (size_t)warp * a.H, xn + (size_t)warp * a.H, a.H, a.rms_eps);
-            if (threadIdx.x < a.T) srcs[threadIdx.x] = xn + (size_t)threadIdx.x * a.H;
-        } else {
-            if (threadIdx.x < a.T) srcs[threadIdx.x] = a.hidden + (size_t)threadIdx.x * a.H;
+        if (warp < a.T) {
+            if (a.rms_eps > 0.0f)
+                warp_rmsnorm_row(a.hidden + (size_t)warp * a.H, xn + (size_t)warp * a.H, a.H, a.rms_eps);
+            else
+                warp_copy_row(a.hidden + (size_t)warp * a.H, xn + (size_t)warp * a.H, a.H);
         }
+        if (threadIdx.x < a.T) srcs[threadIdx.x] = xn + (size_t)threadIdx.x * a.H;
         consumer_bar();
-        prepare_b_rows<W4A4>(srcs, a.T, a.H, xb, gx, red);
+        prepare_b_rows<W4A4, false>(srcs, a.T, a.H, xb, gx, red);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
-        for (int li = warp; warp < nst && li < n; li += nst) {
-            if (!ring_acquire(ring, nst, li)) break;
+        const int s = warp % kPairs;
+        for (int li = s; s < nst && li < n; li += nst) {
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma_16x8(st, st + 16 * (a.H >> 1), a.H, bcol, acc);
-            ring_release(ring, nst, li);
-            const int64_t i = ib + li;
-            const bool routed = i < (int64_t)U * RI;
-            const int u = routed ? static_cast<int>(i / RI) : 0;
-            const int r = routed ? static_cast<int>(i % RI) : static_cast<int>(i - (int64_t)U * RI);
+            float acc[4];
+            bool ok;
+            const bool mine = pair_tile(ring, nst, li, st, a.H, bcol, acc, ok);
+            if (!ok) break;
+            if (!mine) continue;
+            const bool routed = li >= n_sh;
+            int u = 0, r;
+            if (routed) {
+                const int64_t i = rb + (li - n_sh);
+                u = static_cast<int>(i / RI);
+                r = static_cast<int>(i % RI);
+            } else {
+                r = static_cast<int>(sb + li);
+            }
             const float gw = routed ? __ldg(a.global + plan.expert[u]) : __ldg(a.sh_global);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -192,8 +224,8 @@ struct DownArgs {
     const int32_t* topk_idx;
     const float* topk_w;
     int T, k;
-    const uint16_t* act;     // [T*k][I]
-    const uint16_t* act_sh;  // [T][S]
+    const uint16_t* act;       // [T*k][I]
+    const uint16_t* act_sh;    // [T][S]
     const uint16_t* residual;  // [T][H] or null
     uint16_t* out;             // [T][H]
     float* ypart;              // [T*k][H]
@@ -207,116 +239,134 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Ring ring;
     __shared__ DecodePlan plan;
-    __shared__ float gbf[3 * kDecodeMaxT];      // row globals of the B slots, [slot * T + t]
+    __shared__ float gbf[3 * kDecodeMaxT];  // row globals of the B slots, [slot * T + t]
     __shared__ unsigned int red[3 * kDecodeMaxT];
     __shared__ const uint16_t* srcs[3 * kDecodeMaxT];
     __shared__ int slot_u[2];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    build_plan(plan, a.topk_idx, a.topk_w, a.T, a.k, a.E);
-
+    const int G = gridDim.x, b = blockIdx.x;
     const int RH = a.H >> 4;
-    const int U = plan.U;
-    const int64_t cI = a.I >> 6, cS = a.S >> 6;  // item costs (K / 64)
-    const int64_t NR = (int64_t)U * RH;
-    const int64_t C = NR * cI + (int64_t)RH * cS;
-    auto first_item = [&](int64_t c0) -> int64_t {  // first item whose start cost >= c0
-        if (c0 <= NR * cI) return (c0 + cI - 1) / cI;
-        return NR + (c0 - NR * cI + cS - 1) / cS;
-    };
-    const int64_t ib = first_item(C * blockIdx.x / gridDim.x);
-    const int64_t ie = first_item(C * (blockIdx.x + 1) / gridDim.x);
-    const int n = static_cast<int>(ie - ib);
-    // stage size from the widest item this CTA owns (routed K = I, shared K = S)
-    const bool has_routed = n > 0 && ib < NR, has_shared = n > 0 && ie > NR;
-    const int kmax = max(has_routed ? a.I : 0, has_shared ? a.S : 0);
-    const int stage_bytes = 9 * max(kmax, 64);
+    const int64_t sb = share_begin(RH, b, G), se = share_begin(RH, b + 1, G);
+    const int n_sh = static_cast<int>(se - sb);
+    // stage size from the widest item this CTA can own (routed K = I, shared K = S)
+    const int kmax = n_sh > 0 ? max(a.I, a.S) : a.I;
+    const int stage_bytes = 9 * kmax;
     const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
     ring_init(ring, nst);
+    pdl_trigger();
     __syncthreads();
 
     uint8_t* ring_base = smem;
     __half* bsm = reinterpret_cast<__half*>(smem + a.ring_bytes);
     // B slots: two routed experts [T][I] each, then the shared expert [T][S]
-    __half* bslot[3] = {bsm, bsm + (size_t)a.T * a.I, bsm + (size_t)2 * a.T * a.I};
+    __half* const bslot0 = bsm;
+    __half* const bslot1 = bsm + (size_t)a.T * a.I;
+    __half* const bslot2 = bsm + (size_t)2 * a.T * a.I;
 
-    auto item_k = [&](int64_t i) { return i < NR ? a.I : a.S; };
-    auto item = [&](int64_t i, const uint8_t*& c, const uint8_t*& s) {
-        if (i < NR) {
+    auto sh_tile = [&](int64_t r, const uint8_t*& c, const uint8_t*& s) {
+        c = a.sh_codes + 16 * r * (a.S >> 1);
+        s = a.sh_scales + 16 * r * (a.S >> 4);
+    };
+    const int pre = min(n_sh, nst);
+    if (warp == kConsumerWarps && lane == 0) {
+        for (int li = 0; li < pre; ++li) {
+            const uint8_t *c, *s;
+            sh_tile(sb + li, c, s);
+            ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, a.S);
+        }
+    }
+    pdl_wait();
+    build_plan(plan, a.topk_idx, a.topk_w, a.T, a.k, a.E);
+
+    const int U = plan.U;
+    const int64_t NR = (int64_t)U * RH;
+    const int64_t rb = share_begin(NR, b, G), re = share_begin(NR, b + 1, G);
+    const int n = n_sh + static_cast<int>(re - rb);
+    auto item = [&](int li, const uint8_t*& c, const uint8_t*& s, int& K) {
+        if (li < n_sh) {
+            sh_tile(sb + li, c, s);
+            K = a.S;
+        } else {
+            const int64_t i = rb + (li - n_sh);
             const int u = static_cast<int>(i / RH), r = static_cast<int>(i % RH);
             const int64_t row = (int64_t)plan.expert[u] * a.H + 16 * r;
             c = a.codes + row * (a.I >> 1);
             s = a.scales + row * (a.I >> 4);
-        } else {
-            const int64_t row = 16 * (i - NR);
-            c = a.sh_codes + row * (a.S >> 1);
-            s = a.sh_scales + row * (a.S >> 4);
+            K = a.I;
         }
     };
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {
-            for (int li = 0; li < n; ++li) {
+            for (int li = pre; li < n; ++li) {
                 const uint8_t *c, *s;
-                item(ib + li, c, s);
-                if (!ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, item_k(ib + li))) break;
+                int K;
+                item(li, c, s, K);
+                if (!ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, K)) break;
             }
         }
     } else {
         // B operands of the experts this CTA touches (at most two routed + shared)
         if (threadIdx.x == 0) {
             slot_u[0] = slot_u[1] = -1;
-            if (n > 0 && ib < NR) slot_u[0] = static_cast<int>(ib / RH);
-            if (n > 0 && ib < NR) {
-                const int64_t last_routed = min(ie, NR) - 1;
-                const int u1 = static_cast<int>(last_routed / RH);
+            if (re > rb) {
+                slot_u[0] = static_cast<int>(rb / RH);
+                const int u1 = static_cast<int>((re - 1) / RH);
                 if (u1 != slot_u[0]) slot_u[1] = u1;
             }
         }
         consumer_bar();
-        const bool need_sh = n > 0 && ie > NR;
-        if (threadIdx.x < 3 * a.T) {
+        if (threadIdx.x < 2 * a.T) {
             const int sl = threadIdx.x / a.T, t = threadIdx.x % a.T;
             const uint16_t* p = nullptr;
-            if (sl < 2 && slot_u[sl] >= 0) {
+            if (slot_u[sl] >= 0) {
                 const int j = plan.choice[slot_u[sl]][t];
                 if (j >= 0) p = a.act + ((size_t)t * a.k + j) * a.I;
             }
             srcs[threadIdx.x] = p;
         }
         consumer_bar();
-        prepare_b_rows<W4A4>(srcs, 2 * a.T, a.I, bsm, gbf, red);
-        if (need_sh) {
+        prepare_b_rows<W4A4, true>(srcs, 2 * a.T, a.I, bsm, gbf, red);
+        if (n_sh > 0) {
             if (threadIdx.x < a.T) srcs[threadIdx.x] = a.act_sh + (size_t)threadIdx.x * a.S;
             consumer_bar();
-            prepare_b_rows<W4A4>(srcs, a.T, a.S, bslot[2], gbf + 2 * a.T, red);
+            prepare_b_rows<W4A4, true>(srcs, a.T, a.S, bslot2, gbf + 2 * a.T, red);
         }
 
         const int g = lane >> 2, q = lane & 3;
-        for (int li = warp; warp < nst && li < n; li += nst) {
-            const int64_t i = ib + li;
-            const bool routed = i < NR;
-            const int u = routed ? static_cast<int>(i / RH) : -1;
-            const int r = routed ? static_cast<int>(i % RH) : static_cast<int>(i - NR);
-            const int sl = routed ? (u == slot_u[0] ? 0 : (u == slot_u[1] ? 1 : -1)) : 2;
-            if (sl < 0) {  // the launch guarantees at most two routed experts per CTA
-                if (lane == 0) set_dev_error(kErrBadInput);
-                continue;
+        const int s = warp % kPairs;
+        for (int li = s; s < nst && li < n; li += nst) {
+            const bool routed = li >= n_sh;
+            int u = -1, r, sl, K;
+            if (routed) {
+                const int64_t i = rb + (li - n_sh);
+                u = static_cast<int>(i / RH);
+                r = static_cast<int>(i % RH);
+                sl = u == slot_u[0] ? 0 : (u == slot_u[1] ? 1 : -1);
+                K = a.I;
+            } else {
+                r = static_cast<int>(sb + li);
+                sl = 2;
+                K = a.S;
             }
-            const int K = routed ? a.I : a.S;
+            // the launch guarantees at most two routed experts per CTA
+            if (sl < 0 && lane == 0) set_dev_error(kErrBadInput);
+            __half* const bs = sl == 0 ? bslot0 : (sl == 1 ? bslot1 : bslot2);
             const __half* bcol = nullptr;
-            if (g < a.T && (!routed || plan.choice[u][g] >= 0)) bcol = bslot[sl] + (size_t)g * K;
-            if (!ring_acquire(ring, nst, li)) break;
+            if (sl >= 0 && g < a.T && (!routed || plan.choice[u][g] >= 0)) bcol = bs + (size_t)g * K;
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma_16x8(st, st + 16 * (K >> 1), K, bcol, acc);
-            ring_release(ring, nst, li);
+            float acc[4];
+            bool ok;
+            const bool mine = pair_tile(ring, nst, li, st, K, bcol, acc, ok);
+            if (!ok) break;
+            if (!mine) continue;
             const float gw = routed ? __ldg(a.global + plan.expert[u]) : __ldg(a.sh_global);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
                 const int t = 2 * q + (v & 1);
                 const int row = 16 * r + g + 8 * (v >> 1);
-                if (t >= a.T) continue;
+                if (t >= a.T || sl < 0) continue;
                 const float gs = W4A4 ? __fmul_rn(gw, gbf[sl * a.T + t]) : gw;
                 const float y = __fmul_rn(acc[v], gs);
                 if (routed) {
@@ -336,11 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
                 __threadfence();
                 for (int o = lane; o < 16 * a.T; o += 32) {
                     const int t = o >> 4, row = 16 * r + (o & 15);
+                    // all loads of this output first, then the fixed-order sum
+                    float yv[kDecodeMaxK];
+#pragma unroll
+                    for (int j = 0; j < kDecodeMaxK; ++j)
+                        yv[j] = j < a.k ? __ldcg(a.ypart + ((size_t)t * a.k + j) * a.H + row) : 0.0f;
                     float acc2 = __ldcg(a.ysh + (size_t)t * a.H + row);
-                    for (int j = 0; j < a.k; ++j)
-                        acc2 = __fadd_rn(acc2, __ldcg(a.ypart + ((size_t)t * a.k + j) * a.H + row));
-                    if (a.residual)
-                        acc2 = __fadd_rn(acc2, bf16_bits_to_float(a.residual[(size_t)t * a.H + row]));
+                    const float res = a.residual ? bf16_bits_to_float(__ldcg(a.residual + (size_t)t * a.H + row)) : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < kDecodeMaxK; ++j)
+                        if (j < a.k) acc2 = __fadd_rn(acc2, yv[j]);
+                    if (a.residual) acc2 = __fadd_rn(acc2, res);
                     const __nv_bfloat16 ob = __float2bfloat16_rn(acc2);
                     a.out[(size_t)t * a.H + row] = *reinterpret_cast<const uint16_t*>(&ob);
                 }

@@ -7,10 +7,12 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <utility>
 
 #include "common.cuh"
 #include "lm_head.cuh"
 #include "moe_decode.cuh"
+#include "moe_layer.cuh"
 #include "quantize.cuh"
 #include "route.cuh"
 
@@ -85,6 +87,26 @@ inline nvfp4_status launch_status() {
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous one in the stream finishes (it calls pdl_wait() before reading
+// that kernel's results).
+template <typename... KArgs, typename... Args>
+nvfp4_status launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t stream,
+                        Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) return NVFP4_ERR_CUDA;
+    return launch_status();
+}
 
 // ------------------------------------------------------------ workspace
 struct DecodeWs {
@@ -211,13 +233,17 @@ nvfp4_status moe_route_topk(const void* hidden, const float* router_w, const flo
     if (H % 16 || E > 256 || k > 32) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(hidden, 16) || !aligned(router_w, 16)) return NVFP4_ERR_MISALIGNED;
     constexpr int TT = 8;
-    const int smem = TT * H * 2;
     const int lim = dyn_smem_limit(k_route<TT>);
+    const int hbytes = TT * H * 2;
+    const int nj = (E + kRouteCluster - 1) / kRouteCluster;  // gate rows of CTA rank 0
+    const int stage_w = hbytes + nj * H * 4 <= lim ? 1 : 0;
+    const int smem = hbytes + (stage_w ? nj * H * 4 : 0);
     if (smem > lim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     const int tiles = (T + TT - 1) / TT;
-    k_route<TT><<<tiles * kRouteCluster, kRouteWarps * 32, smem, stream>>>(
-        static_cast<const uint16_t*>(hidden), router_w, bias, T, H, E, k, rms_eps, topk_idx, topk_w);
-    return launch_status();
+    return launch_pdl(k_route<TT>, tiles * kRouteCluster, kRouteWarps * 32, smem, stream,
+                      static_cast<const uint16_t*>(hidden), router_w, bias, T, H, E, k, rms_eps, stage_w,
+                      topk_idx, topk_w, static_cast<DecodePlan*>(nullptr), static_cast<__half*>(nullptr),
+                      static_cast<float*>(nullptr), 0);
 }
 
 size_t moe_expert_forward_workspace_size(const moe_layer_weights* w, int32_t T, int32_t k,
@@ -283,9 +309,8 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
         ua.ring_bytes = std::min(kMaxStages * stage, ((lim - bbytes) / 128) * 128);
         if (ua.ring_bytes < 2 * stage) return NVFP4_ERR_UNSUPPORTED_SHAPE;
         const int smem = ua.ring_bytes + bbytes;
-        if (w4a4) k_moe_up_decode<true><<<grid, kThreads, smem, stream>>>(ua);
-        else k_moe_up_decode<false><<<grid, kThreads, smem, stream>>>(ua);
-        st = launch_status();
+        st = w4a4 ? launch_pdl(k_moe_up_decode<true>, grid, kThreads, smem, stream, ua)
+                  : launch_pdl(k_moe_up_decode<false>, grid, kThreads, smem, stream, ua);
         if (st != NVFP4_OK) return st;
     }
 
@@ -318,9 +343,8 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
         da.ring_bytes = std::min(kMaxStages * stage, ((lim - bbytes) / 128) * 128);
         if (da.ring_bytes < 2 * stage) return NVFP4_ERR_UNSUPPORTED_SHAPE;
         const int smem = da.ring_bytes + bbytes;
-        if (w4a4) k_moe_down_decode<true><<<grid, kThreads, smem, stream>>>(da);
-        else k_moe_down_decode<false><<<grid, kThreads, smem, stream>>>(da);
-        st = launch_status();
+        st = w4a4 ? launch_pdl(k_moe_down_decode<true>, grid, kThreads, smem, stream, da)
+                  : launch_pdl(k_moe_down_decode<false>, grid, kThreads, smem, stream, da);
     }
     return st;
 }
@@ -354,14 +378,161 @@ nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, 
         la.T = std::min(kLmMaxT, T - t0);
         la.hidden = static_cast<const uint16_t*>(hidden) + (size_t)t0 * H;
         la.logits = logits + (size_t)t0 * w->n;
-        k_lm_head<<<grid, kThreads, smem, stream>>>(la);
-        const nvfp4_status st = launch_status();
+        const nvfp4_status st = launch_pdl(k_lm_head, grid, kThreads, smem, stream, la);
         if (st != NVFP4_OK) return st;
     }
     return NVFP4_OK;
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ fused layer
+namespace {
+
+struct LayerWsOffsets {
+    size_t plan, xq, gx, act, act_sh, aq, ga, aq_sh, gsh, ypart, ysh, ecnt, tilecnt, total;
+};
+
+LayerWsOffsets layer_ws(int T, int k, int H, int I, int S) {
+    LayerWsOffsets o{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    o.ecnt = take(sizeof(int) * (kDecodeMaxU + 1));
+    o.tilecnt = take(sizeof(int) * (size_t)(H / 16));
+    o.plan = take(sizeof(DecodePlan));
+    o.xq = take((size_t)T * H * 2);
+    o.gx = take((size_t)T * 4);
+    o.act = take((size_t)T * k * I * 2);
+    o.act_sh = take((size_t)T * S * 2);
+    o.aq = take((size_t)T * k * I * 2);
+    o.ga = take((size_t)T * k * 4);
+    o.aq_sh = take((size_t)T * S * 2);
+    o.gsh = take((size_t)T * 4);
+    o.ypart = take((size_t)T * k * H * 4);
+    o.ysh = take((size_t)T * H * 4);
+    o.total = off;
+    return o;
+}
+
+LayerWs layer_ws_ptrs(const LayerWsOffsets& o, uint8_t* base) {
+    LayerWs w{};
+    w.plan = reinterpret_cast<DecodePlan*>(base + o.plan);
+    w.xq = reinterpret_cast<__half*>(base + o.xq);
+    w.gx = reinterpret_cast<float*>(base + o.gx);
+    w.act = reinterpret_cast<uint16_t*>(base + o.act);
+    w.act_sh = reinterpret_cast<uint16_t*>(base + o.act_sh);
+    w.aq = reinterpret_cast<__half*>(base + o.aq);
+    w.ga = reinterpret_cast<float*>(base + o.ga);
+    w.aq_sh = reinterpret_cast<__half*>(base + o.aq_sh);
+    w.gsh = reinterpret_cast<float*>(base + o.gsh);
+    w.ypart = reinterpret_cast<float*>(base + o.ypart);
+    w.ysh = reinterpret_cast<float*>(base + o.ysh);
+    w.ecnt = reinterpret_cast<int*>(base + o.ecnt);
+    w.tilecnt = reinterpret_cast<int*>(base + o.tilecnt);
+    return w;
+}
+
+}  // namespace
+
+extern "C" size_t moe_layer_forward_workspace_size(const moe_layer_weights* w, int32_t T, int32_t k,
+                                                   nvfp4_act_mode mode) {
+    (void)mode;
+    if (!w || T < 1 || k < 1) return 0;
+    return layer_ws(T, k, w->hidden, w->inter, w->shared_inter).total;
+}
+
+extern "C" nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w, const float* bias,
+                                          const void* hidden, int32_t T, int32_t k, nvfp4_act_mode mode,
+                                          float rms_eps, const void* residual, void* out, int32_t* topk_idx,
+                                          float* topk_w, void* workspace, size_t workspace_bytes,
+                                          cudaStream_t stream) {
+    nvfp4_status st = check_layer(w);
+    if (st != NVFP4_OK) return st;
+    if (!router_w || !bias || !hidden || !out || !topk_idx || !topk_w || !workspace) return NVFP4_ERR_INVALID_ARG;
+    if (T < 1 || k < 1 || k > w->num_experts) return NVFP4_ERR_INVALID_ARG;
+    if (mode != NVFP4_W4A16 && mode != NVFP4_W4A4) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(hidden, 16) || !aligned(router_w, 16) || !aligned(out, 4) || !aligned(workspace, 256) ||
+        (residual && !aligned(residual, 4)))
+        return NVFP4_ERR_MISALIGNED;
+    if (hidden == out && residual != hidden) return NVFP4_ERR_INVALID_ARG;
+    if (T > kDecodeMaxT || k > kDecodeMaxK || k > 32 || w->num_experts > 256) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const int H = w->hidden, I = w->inter, S = w->shared_inter, E = w->num_experts;
+    const LayerWsOffsets o = layer_ws(T, k, H, I, S);
+    if (workspace_bytes < o.total) return NVFP4_ERR_WORKSPACE;
+    const LayerWs ws = layer_ws_ptrs(o, static_cast<uint8_t*>(workspace));
+    const bool w4a4 = mode == NVFP4_W4A4;
+
+    {  // route + plan + up-B rows (one cluster)
+        constexpr int TT = 8;
+        const int lim = dyn_smem_limit(k_route<TT>);
+        const int hbytes = TT * H * 2;
+        const int nj = (E + kRouteCluster - 1) / kRouteCluster;
+        const int stage_w = hbytes + nj * H * 4 <= lim ? 1 : 0;
+        const int smem = hbytes + (stage_w ? nj * H * 4 : 0);
+        if (smem > lim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        st = launch_pdl(k_route<TT>, kRouteCluster, kRouteWarps * 32, smem, stream,
+                        static_cast<const uint16_t*>(hidden), router_w, bias, T, H, E, k, rms_eps, stage_w, topk_idx,
+                        topk_w, ws.plan, ws.xq, ws.gx, w4a4 ? 1 : 0);
+        if (st != NVFP4_OK) return st;
+    }
+    const int grid = std::max(num_sms(), 2 * (T * k + (S + I - 1) / I) + 4);
+    {
+        LayerUpArgs ua{};
+        ua.codes = w->up_codes;
+        ua.scales = w->up_scales;
+        ua.global = w->up_global;
+        ua.sh_codes = w->shared_up.codes;
+        ua.sh_scales = w->shared_up.scales;
+        ua.sh_global = w->shared_up.global_scale;
+        ua.E = E;
+        ua.H = H;
+        ua.I = I;
+        ua.S = S;
+        ua.T = T;
+        ua.k = k;
+        ua.ws = ws;
+        const int lim = w4a4 ? dyn_smem_limit(k_layer_up<true>) : dyn_smem_limit(k_layer_up<false>);
+        const int bbytes = T * H * 2;
+        const int stage = 9 * H;
+        ua.ring_bytes = std::min(kMaxStages * stage, ((lim - bbytes) / 128) * 128);
+        if (ua.ring_bytes < 2 * stage) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        const int smem = ua.ring_bytes + bbytes;
+        st = w4a4 ? launch_pdl(k_layer_up<true>, grid, kThreads, smem, stream, ua)
+                  : launch_pdl(k_layer_up<false>, grid, kThreads, smem, stream, ua);
+        if (st != NVFP4_OK) return st;
+    }
+    {
+        LayerDownArgs da{};
+        da.codes = w->down_codes;
+        da.scales = w->down_scales;
+        da.global = w->down_global;
+        da.sh_codes = w->shared_down.codes;
+        da.sh_scales = w->shared_down.scales;
+        da.sh_global = w->shared_down.global_scale;
+        da.E = E;
+        da.H = H;
+        da.I = I;
+        da.S = S;
+        da.T = T;
+        da.k = k;
+        da.ws = ws;
+        da.residual = static_cast<const uint16_t*>(residual);
+        da.out = static_cast<uint16_t*>(out);
+        const int lim = w4a4 ? dyn_smem_limit(k_layer_down<true>) : dyn_smem_limit(k_layer_down<false>);
+        const int bbytes = (2 * T * I + T * S) * 2;
+        const int stage = 9 * std::max(I, S);
+        da.ring_bytes = std::min(kMaxStages * stage, ((lim - bbytes) / 128) * 128);
+        if (da.ring_bytes < 2 * stage) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        const int smem = da.ring_bytes + bbytes;
+        st = w4a4 ? launch_pdl(k_layer_down<true>, grid, kThreads, smem, stream, da)
+                  : launch_pdl(k_layer_down<false>, grid, kThreads, smem, stream, da);
+    }
+    return st;
+}
 
 // ------------------------------------------------ allocation-free variant
 // moe_expert_forward_noalloc: the same computation as moe_expert_forward for

@@ -5,16 +5,18 @@
 //
 // Design: one thread-block cluster of 8 CTAs per tile of TT tokens. The gate
 // matrix (E x H fp32, 1.38 MB at the pages' shape) is split by expert across
-// the 8 CTAs, one warp per expert, so the logits of a token come from 8 SMs
-// streaming the gate rows in parallel. Each CTA leaves its logits in shared
-// memory; after a hardware cluster barrier, CTA rank 0 reads all of them
-// through distributed shared memory and runs the top-k per token in one warp.
-// No global scratch and no spin-waits.
+// the 8 CTAs, one warp per expert. The gate rows are constant, so each CTA
+// stages its rows into shared memory with bulk TMA copies before it waits on
+// the kernel that produced the hidden state (programmatic dependent launch);
+// when they do not fit, they are read from global memory instead. Each CTA
+// leaves its logits in shared memory; after a hardware cluster barrier, CTA
+// rank 0 reads all of them through distributed shared memory and runs the
+// top-k per token in one warp. No global scratch.
 #pragma once
 
 #include <cooperative_groups.h>
 
-#include "common.cuh"
+#include "moe_decode.cuh"
 
 namespace nvfp4moe {
 
@@ -23,15 +25,24 @@ namespace cg = cooperative_groups;
 constexpr int kRouteCluster = 8;
 constexpr int kRouteWarps = 16;
 constexpr int kRouteMaxExpertsPerCta = 32;  // E <= 256
+constexpr int kRouteTile = 8;               // tokens per cluster
+
+// kRouteWarps * 32 threads == kConsumerThreads, so the consumer-barrier
+// helpers of the expert kernels serve this kernel's whole CTA too.
+static_assert(kRouteWarps * 32 == kConsumerThreads, "route CTA size must match the consumer barrier");
 
 template <int TT>
 __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteWarps * 32)
     k_route(const uint16_t* __restrict__ hidden, const float* __restrict__ Wg,
             const float* __restrict__ bias, int T, int H, int E, int k, float rms_eps,
-            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+            int stage_w, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+            DecodePlan* __restrict__ plan_out, __half* __restrict__ xq_out, float* __restrict__ gx_out,
+            int w4a4) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint16_t* hs = reinterpret_cast<uint16_t*>(smem_raw);  // [TT][H] bf16
+    uint16_t* hs = reinterpret_cast<uint16_t*>(smem_raw);             // [TT][H] bf16
+    float* wsm = reinterpret_cast<float*>(smem_raw + (size_t)TT * H * 2);  // [nj][H] gate rows
     __shared__ float zs[TT][kRouteMaxExpertsPerCta];
+    __shared__ __align__(8) uint64_t wbar;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
@@ -39,24 +50,42 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteWa
     const int t0 = tile * TT;
     const int nt = min(TT, T - t0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nj = (E - rank + kRouteCluster - 1) / kRouteCluster;  // experts of this CTA
+
+    if (threadIdx.x == 0) {
+        mbar_init(&wbar, 1);
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < TT * kRouteMaxExpertsPerCta; i += blockDim.x) (&zs[0][0])[i] = 0.0f;
+    pdl_trigger();
+    __syncthreads();
+    if (stage_w && threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&wbar, (uint32_t)(nj * H * 4));
+        for (int j = 0; j < nj; ++j)
+            bulk_g2s(wsm + (size_t)j * H, Wg + (int64_t)(j * kRouteCluster + rank) * H, (uint32_t)(H * 4), &wbar);
+    }
+    pdl_wait();
 
     // stage the token tile's hidden rows (bf16) in shared memory, RMS-normalised
     // when rms_eps > 0 (the same warp routine as the expert kernels use)
-    if (rms_eps > 0.0f) {
-        for (int t = warp; t < nt; t += kRouteWarps)
+    for (int t = warp; t < nt; t += kRouteWarps) {
+        if (rms_eps > 0.0f)
             warp_rmsnorm_row(hidden + (int64_t)(t0 + t) * H, hs + t * H, H, rms_eps);
-    } else {
-        const int n16 = nt * H / 8;  // uint4 count (H % 16 == 0)
-        const uint4* src = reinterpret_cast<const uint4*>(hidden + (int64_t)t0 * H);
-        uint4* dst = reinterpret_cast<uint4*>(hs);
-        for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = __ldg(src + i);
+        else
+            warp_copy_row(hidden + (int64_t)(t0 + t) * H, hs + t * H, H);
     }
     __syncthreads();
+    bool wok = true;
+    if (stage_w) {
+        wok = __all_sync(0xffffffffu, mbar_wait_bounded(&wbar, 0));
+        if (!wok && lane == 0) set_dev_error(kErrWaitFull);
+    }
 
     // logits: this CTA owns experts e = rank + 8 * j; warp w takes j = w, w + 16
-    for (int j = warp; j * kRouteCluster + rank < E; j += kRouteWarps) {
+    for (int j = warp; j * kRouteCluster + rank < E && wok; j += kRouteWarps) {
         const int e = j * kRouteCluster + rank;
-        const float4* wr = reinterpret_cast<const float4*>(Wg + (int64_t)e * H);
+        const float4* wr = stage_w ? reinterpret_cast<const float4*>(wsm + (size_t)j * H)
+                                   : reinterpret_cast<const float4*>(Wg + (int64_t)e * H);
         float acc[TT];
 #pragma unroll
         for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
@@ -66,7 +95,7 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteWa
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int i = i0 + 32 * u;
-                w4[u] = i < H / 4 ? __ldg(wr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                w4[u] = i < H / 4 ? (stage_w ? wr[i] : __ldg(wr + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -110,7 +139,7 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteWa
                     const float* zr = cluster.map_shared_rank(&zs[0][0], e % kRouteCluster);
                     const float z = zr[t * kRouteMaxExpertsPerCta + e / kRouteCluster];
                     sg[q] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
-                    c[q] = __fadd_rn(sg[q], __ldg(bias + e));
+                    c[q] = __fadd_rn(sg[q], __ldg(bias + e));  // constant weights
                     taken[q] = false;
                 }
             }
@@ -156,9 +185,30 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteWa
                 topk_w[(int64_t)(t0 + t) * k + lane] = __fdiv_rn(selsig, ssum);
             }
         }
+        if (plan_out != nullptr) {
+            // planning mode (one cluster holds every token): the step plan and
+            // the up kernel's B rows, prepared once for all of its CTAs
+            __shared__ DecodePlan plan;
+            __shared__ unsigned int red[kRouteTile];
+            __shared__ const uint16_t* srcs[kRouteTile];
+            __threadfence();
+            __syncthreads();
+            build_plan(plan, topk_idx, topk_w, T, k, E);
+            {
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(&plan);
+                uint32_t* dst = reinterpret_cast<uint32_t*>(plan_out);
+                for (int i = threadIdx.x; i < (int)(sizeof(DecodePlan) / 4); i += blockDim.x) dst[i] = src[i];
+            }
+            if (threadIdx.x < nt) srcs[threadIdx.x] = hs + threadIdx.x * H;
+            __syncthreads();
+            if (w4a4) prepare_b_rows<true, false>(srcs, nt, H, xq_out, gx_out, red);
+            else prepare_b_rows<false, false>(srcs, nt, H, xq_out, gx_out, red);
+        }
     }
-    // keep every CTA's shared memory alive until rank 0 has read it
+    // keep every CTA's shared memory alive until rank 0 has read it, and do not
+    // exit while a gate-row copy could still be landing
     cluster.sync();
+    if (stage_w && !wok && threadIdx.x == 0 && !mbar_wait_bounded(&wbar, 0)) set_dev_error(kErrWaitDrain);
 }
 
 }  // namespace nvfp4moe

@@ -15,8 +15,8 @@ nvfp4_quantize from bf16 masters supplied by the caller.
 """
 import torch
 
-from . import (MoELayer, NVFP4Matrix, PER_TENSOR, W4A4, W4A16, lm_head_gemv, make_workspace,
-               moe_expert_forward, moe_route_topk, nvfp4_quantize)
+from . import (MoELayer, NVFP4Matrix, PER_TENSOR, W4A4, W4A16, lm_head_gemv, make_layer_workspace,
+               moe_expert_forward, moe_layer_forward, moe_route_topk, nvfp4_quantize)
 
 
 class MoEDecodeStack:
@@ -71,12 +71,23 @@ class MoEDecodeStack:
         self.make_workspace()
 
     def make_workspace(self):
-        self.ws = make_workspace(self.layers[0], self.T, self.k, self.mode)
+        self.ws = make_layer_workspace(self.layers[0], self.T, self.k, self.mode)
+
+    @property
+    def fused(self):
+        """Layers run through moe_layer_forward (1..4 tokens); otherwise as
+        moe_route_topk + moe_expert_forward."""
+        return self.T <= 4 and getattr(self, "use_fused", True)
 
     # ------------------------------------------------------------ the step
     def step(self, stream=None):
         """One decode step on self.h[0] -> self.h[L] (and logits)."""
         for l, Lw in enumerate(self.layers):
+            if self.fused:
+                moe_layer_forward(Lw, self.h[l], self.k, self.mode, residual=self.h[l], out=self.h[l + 1],
+                                  topk_idx=self.topk_idx[l], topk_w=self.topk_w[l], workspace=self.ws,
+                                  rms_eps=self.rms_eps, stream=stream)
+                continue
             moe_route_topk(self.h[l], Lw.router_w, Lw.router_b, self.k, self.topk_idx[l],
                            self.topk_w[l], rms_eps=self.rms_eps, stream=stream)
             moe_expert_forward(Lw, self.h[l], self.topk_idx[l], self.topk_w[l], self.mode,

@@ -39,6 +39,7 @@ def test_chain_teacher_forced(nm, stack, cfg):
     h = gen.hidden_bf16(T, c["H"], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
     assert np.isfinite(bf16_to_f64(h)).all(), "generated hidden state is not finite"
     ws = nm.make_workspace(st.layers[0], T, c["K"], nm.W4A4)
+    lws = nm.make_layer_workspace(st.layers[0], T, c["K"], nm.W4A4)
     exempt = 0
     for l in range(c["layers"]):
         OL = OracleLayer(c["seed"], l, c["H"], c["I"], c["S"], c["E"], c["bias"])
@@ -56,6 +57,12 @@ def test_chain_teacher_forced(nm, stack, cfg):
                                         rms_eps=c["rms_eps"])
             torch.cuda.synchronize()
             assert_close(bf16_to_f64(bf16_bits(out)), bf16_to_f64(ref), f"layer {l}")
+            # the fused layer call, as the benchmark's step runs it
+            outf, idxf, _ = nm.moe_layer_forward(st.layers[l], hd, c["K"], nm.W4A4, residual=hd,
+                                                 workspace=lws, rms_eps=c["rms_eps"])
+            torch.cuda.synchronize()
+            assert torch.equal(idxf, idx)
+            assert_close(bf16_to_f64(bf16_bits(outf)), bf16_to_f64(ref), f"fused layer {l}")
         h = ref
     assert exempt <= 1
     assert nm.nvfp4_last_device_error() == 0
@@ -88,10 +95,8 @@ def test_free_running_graph(nm, stack):
     assert torch.equal(first.view(torch.int16), st.h[1].view(torch.int16)), "replay not deterministic"
     assert torch.isfinite(st.logits).all()
     hd = to_dev_bf16(h0)
-    idx, w = nm.moe_route_topk(hd, st.layers[0].router_w, st.layers[0].router_b, c["K"],
-                               rms_eps=c["rms_eps"])
-    out = nm.moe_expert_forward(st.layers[0], hd, idx, w, nm.W4A4, residual=hd, workspace=st.ws,
-                                rms_eps=c["rms_eps"])
+    out, _, _ = nm.moe_layer_forward(st.layers[0], hd, c["K"], nm.W4A4, residual=hd, workspace=st.ws,
+                                     rms_eps=c["rms_eps"])
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), first.view(torch.int16))
     assert nm.nvfp4_last_device_error() == 0

@@ -98,3 +98,47 @@ def test_full_layer_w4a4_prenorm(nm, full_layer):
     h = gen.hidden_bf16(2, c["H"], 0, layer=9)
     h = ((gen.bf16_bits_to_f32(h) * 7.0).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
     run_layer(nm, L, OL, h, c["K"], True, True, gpu_routing=True, rms_eps=1e-5)
+
+
+def run_fused(nm, L, OL, h, k, w4a4, residual, rms_eps):
+    hd = to_dev_bf16(h)
+    mode = nm.W4A4 if w4a4 else nm.W4A16
+    ws = nm.make_layer_workspace(L, h.shape[0], k, mode)
+    outs = []
+    for _ in range(2):  # the workspace counters are left zeroed: same bits again
+        out, idx, w = nm.moe_layer_forward(L, hd, k, mode, residual=hd if residual else None, workspace=ws,
+                                           rms_eps=rms_eps)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert nm.nvfp4_last_device_error() == 0
+    r = OL.route(h, k, rms_eps)
+    check_routing(idx.cpu().numpy(), w.cpu().numpy(), r, k)
+    assert np.array_equal(idx.cpu().numpy(), r["idx"]), "near-tie flip: layer output not comparable"
+    ref, _, _ = OL.forward(h, k, w4a4, residual, routing=r, rms_eps=rms_eps)
+    assert_close(bf16_to_f64(bf16_bits(outs[0])), bf16_to_f64(ref), "fused layer output")
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    # same result as the two-call path
+    idx2, w2 = nm.moe_route_topk(hd, L.router_w, L.router_b, k, rms_eps=rms_eps)
+    out2 = nm.moe_expert_forward(L, hd, idx2, w2, mode, residual=hd if residual else None, rms_eps=rms_eps)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2)
+    assert_close(bf16_to_f64(bf16_bits(out2)), bf16_to_f64(bf16_bits(outs[0])), "fused vs two-call")
+
+
+@pytest.mark.parametrize("T", [1, 3, 4])
+@pytest.mark.parametrize("w4a4,eps", [(False, 0.0), (True, 0.0), (True, 1e-5)])
+def test_small_fused_layer(nm, T, w4a4, eps):
+    c = SMALL
+    L = device_layer(nm, 7, 2, c["E"], c["H"], c["I"], c["S"], (-0.1, 0.1))
+    OL = OracleLayer(7, 2, c["H"], c["I"], c["S"], c["E"], (-0.1, 0.1))
+    h = gen.hidden_bf16(T, c["H"], 7, layer=2, rho=0.5)
+    run_fused(nm, L, OL, h, 4, w4a4, True, eps)
+
+
+def test_full_fused_layer(nm, full_layer):
+    c, L, OL = full_layer
+    h = gen.hidden_bf16(1, c["H"], 0, layer=configs.HIDDEN_LAYER)
+    run_fused(nm, L, OL, h, c["K"], False, False, 0.0)
+    run_fused(nm, L, OL, h, c["K"], True, True, 1e-5)
+    h4 = gen.hidden_bf16(4, c["H"], 0, layer=configs.HIDDEN_LAYER, rho=0.5)
+    run_fused(nm, L, OL, h4, c["K"], True, True, 1e-5)
