@@ -223,6 +223,54 @@ nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w
                                cudaStream_t stream);
 
 /*
+ * moe_stack_forward - L consecutive MoE decode layers for 1..4 tokens in one
+ * call: the residual chain of the pre-norm model the pages serve,
+ *   h_{l+1} = h_l + moe_l(x_l),  x_l = RMSNorm(h_l) (or h_l if rms_eps <= 0),
+ * where moe_l is the layer of moe_layer_forward (sigmoid + bias top-k router,
+ * routed experts up -> relu^2 -> down, shared expert, gate-weighted combine;
+ * [card-int4] "Checkpoint layout", [worklog] Interlude and Step 5). The
+ * pre-norm is this library's reading: the pages name the layers but not the
+ * blocks between them, and the bare chain overflows bf16 within a few
+ * layers at the pages' shapes. It
+ * runs as one persistent cooperative kernel with one CTA per SM: the layers'
+ * steps meet through counters in the workspace instead of kernel boundaries,
+ * and the next layer's router rows and shared-expert tiles are staged while
+ * the current layer still waits on its routing.
+ *   layers     host array [L] of per-layer device pointers (copied into the
+ *              launch; not read after the call returns); every layer has the
+ *              same E, H, I, S with H, I, S % 64 == 0, E % 8 == 0 and E <= 256
+ *   L          1 .. NVFP4MOE_STACK_MAX_LAYERS
+ *   hidden_in  device bf16 [T][H] h_0, 16-byte aligned
+ *   T, k       1 <= T <= 4, 1 <= k <= min(E, 16)
+ *   hidden_out device bf16 [L][T][H]: h_1 .. h_L, 16-byte aligned, must not
+ *              overlap hidden_in
+ *   topk_idx, topk_w: device out [L][T][k], each layer's routing
+ *   workspace  device, >= moe_stack_forward_workspace_size() bytes, 256-byte
+ *              aligned, zeroed once by moe_expert_forward_workspace_init and
+ *              left zeroed by every completed call; calls that share it must
+ *              not overlap.
+ * Summation orders differ from moe_layer_forward's (router dot products, the
+ * split of tile reductions), so results agree with it to FP32 rounding, not
+ * bit for bit. Returns NVFP4_ERR_UNSUPPORTED_SHAPE for shapes outside the
+ * limits above or when one CTA per SM does not fit, NVFP4_ERR_CUDA if the
+ * cooperative launch fails; a device wait that expires ends every CTA of the
+ * call early and is reported by nvfp4_last_device_error (NVFP4_ERR_TIMEOUT).
+ */
+#define NVFP4MOE_STACK_MAX_LAYERS 32
+typedef struct {
+    moe_layer_weights moe;
+    const float* router_w;    /* [E][H] */
+    const float* router_bias; /* [E] */
+} moe_stack_layer;
+
+size_t moe_stack_forward_workspace_size(const moe_stack_layer* layers, int32_t L, int32_t T, int32_t k,
+                                        nvfp4_act_mode mode);
+nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t L, const void* hidden_in, int32_t T,
+                               int32_t k, nvfp4_act_mode mode, float rms_eps, void* hidden_out,
+                               int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/*
  * moe_expert_forward_noalloc - moe_expert_forward for callers that cannot
  * allocate device memory. The pages have no counterpart to this call.
  *

@@ -16,7 +16,8 @@ from . import _abi
 __all__ = ["NVFP4Matrix", "MoELayer", "NVFP4Error", "nvfp4_quantize", "moe_route_topk",
            "moe_expert_forward_workspace_size", "moe_expert_forward_workspace_init",
            "moe_expert_forward", "moe_expert_forward_noalloc", "moe_layer_forward",
-           "moe_layer_forward_workspace_size", "lm_head_gemv",
+           "moe_layer_forward_workspace_size", "moe_stack_forward", "moe_stack_forward_workspace_size",
+           "make_stack_workspace", "lm_head_gemv",
            "nvfp4_status_string", "nvfp4_last_device_error",
            "W4A16", "W4A4", "PER_TENSOR", "PER_ROW", "GIVEN", "lib"]
 
@@ -211,6 +212,52 @@ def moe_layer_forward(layer: MoELayer, hidden, k, mode=W4A4, residual=None, out=
                               _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "moe_layer_forward")
     return out, topk_idx, topk_w
+
+
+def _stack_layers(layers):
+    """ctypes array of moe_stack_layer for a list of MoELayer (cached on the list's layers)."""
+    arr = (_abi.MoeStackLayer * len(layers))()
+    for i, Lw in enumerate(layers):
+        arr[i] = _abi.MoeStackLayer(Lw.c(), Lw.router_w.data_ptr(), Lw.router_b.data_ptr())
+    return arr
+
+
+def moe_stack_forward_workspace_size(layers, T, k, mode=W4A4) -> int:
+    arr = _stack_layers(layers)
+    return int(_L.moe_stack_forward_workspace_size(arr, len(layers), T, k, mode))
+
+
+def make_stack_workspace(layers, T, k, mode=W4A4, stream=None):
+    n = moe_stack_forward_workspace_size(layers, T, k, mode)
+    if n == 0:
+        raise NVFP4Error(2, "moe_stack_forward_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=layers[0].up_codes.device)
+    moe_expert_forward_workspace_init(ws, stream)
+    return ws
+
+
+def moe_stack_forward(layers, hidden, k, mode=W4A4, hidden_out=None, topk_idx=None, topk_w=None,
+                      workspace=None, rms_eps=0.0, stream=None, c_layers=None):
+    """L layers of the pre-norm residual chain h_{l+1} = h_l + moe_l(norm(h_l))
+    in one persistent kernel (1..4 tokens). Returns (hidden_out [L][T][H],
+    topk_idx [L][T][k], topk_w [L][T][k]); hidden_out[l] is h_{l+1}.
+    c_layers: a cached _stack_layers(layers) array, to skip rebuilding it."""
+    L = len(layers)
+    T, H = hidden.shape
+    dev = hidden.device
+    if hidden_out is None:
+        hidden_out = torch.empty((L, T, H), dtype=hidden.dtype, device=dev)
+    if topk_idx is None:
+        topk_idx = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((L, T, k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = make_stack_workspace(layers, T, k, mode, stream)
+    arr = c_layers if c_layers is not None else _stack_layers(layers)
+    st = _L.moe_stack_forward(arr, L, _ptr(hidden), T, k, mode, float(rms_eps), _ptr(hidden_out),
+                              _ptr(topk_idx), _ptr(topk_w), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "moe_stack_forward")
+    return hidden_out, topk_idx, topk_w
 
 
 def moe_expert_forward_noalloc(layer: MoELayer, hidden, topk_idx, topk_w, mode=W4A4, residual=None,

@@ -12,10 +12,12 @@ I32, I64 = ctypes.c_int32, ctypes.c_int64
 EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_size",
            "moe_expert_forward_workspace_init", "moe_expert_forward", "moe_expert_forward_noalloc",
            "moe_layer_forward", "moe_layer_forward_workspace_size",
+           "moe_stack_forward", "moe_stack_forward_workspace_size",
            "lm_head_gemv",
            "nvfp4_status_string", "nvfp4_last_device_error"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20  # NVFP4MOE_NOALLOC_SCRATCH_BYTES
+STACK_MAX_LAYERS = 32  # NVFP4MOE_STACK_MAX_LAYERS
 
 STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED_SHAPE",
           3: "NVFP4_ERR_MISALIGNED", 4: "NVFP4_ERR_WORKSPACE", 5: "NVFP4_ERR_CUDA",
@@ -31,6 +33,10 @@ class MoeLayerWeights(ctypes.Structure):
                 ("up_codes", P), ("up_scales", P), ("up_global", P),
                 ("down_codes", P), ("down_scales", P), ("down_global", P),
                 ("shared_up", NVFP4Matrix), ("shared_down", NVFP4Matrix)]
+
+
+class MoeStackLayer(ctypes.Structure):
+    _fields_ = [("moe", MoeLayerWeights), ("router_w", P), ("router_bias", P)]
 
 
 _lib = None
@@ -61,6 +67,11 @@ def load(path: str = LIB_PATH):
     L.moe_layer_forward.argtypes = [ctypes.POINTER(MoeLayerWeights), P, P, P, I32, I32, ctypes.c_int,
                                     ctypes.c_float, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_layer_forward.restype = ctypes.c_int
+    L.moe_stack_forward_workspace_size.argtypes = [ctypes.POINTER(MoeStackLayer), I32, I32, I32, ctypes.c_int]
+    L.moe_stack_forward_workspace_size.restype = ctypes.c_size_t
+    L.moe_stack_forward.argtypes = [ctypes.POINTER(MoeStackLayer), I32, P, I32, I32, ctypes.c_int, ctypes.c_float,
+                                    P, P, P, P, ctypes.c_size_t, P]
+    L.moe_stack_forward.restype = ctypes.c_int
     L.moe_expert_forward_noalloc.argtypes = [ctypes.POINTER(MoeLayerWeights), P, P, P, I32, I32,
                                              ctypes.c_int, ctypes.c_float, P, P, P]
     L.moe_expert_forward_noalloc.restype = ctypes.c_int

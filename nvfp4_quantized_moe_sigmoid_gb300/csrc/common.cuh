@@ -22,6 +22,7 @@ enum : unsigned int {
     kErrWaitEmpty = 2u,  // the producer waited too long for a free stage
     kErrWaitDrain = 4u,  // copies still in flight at exit did not land
     kErrBadInput = 8u,   // an expert index outside [0, E) or a broken plan
+    kErrWaitPeer = 16u,  // a wait on another CTA's progress expired
 };
 
 // 1 s: device waits in this library normally take microseconds.
@@ -177,18 +178,22 @@ __device__ __forceinline__ uint32_t float2_to_e2m1x2(float x0, float x1) {
 struct QBlock {
     uint32_t lo, hi, scale;
 };
+// x / d, IEEE round to nearest; a zero x is returned as it is (the quotient
+// is that same signed zero), which keeps it off the division's slow path.
+__device__ __forceinline__ float div_rn_or_zero(float x, float d) { return x == 0.0f ? x : __fdiv_rn(x, d); }
+
 __device__ __forceinline__ QBlock quantize_block16(const float (&x)[16], float g) {
     float bamax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(x[i]));
     uint32_t s = 0;
-    if (g > 0.0f) s = float_to_e4m3_pos(__fdiv_rn(__fdiv_rn(bamax, 6.0f), g));
+    if (g > 0.0f && bamax > 0.0f) s = float_to_e4m3_pos(__fdiv_rn(__fdiv_rn(bamax, 6.0f), g));
     const float d = __fmul_rn(e4m3_to_float(s), g);
     QBlock q{0u, 0u, s};
     if (d != 0.0f) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t byte = float2_to_e2m1x2(__fdiv_rn(x[2 * i], d), __fdiv_rn(x[2 * i + 1], d));
+            const uint32_t byte = float2_to_e2m1x2(div_rn_or_zero(x[2 * i], d), div_rn_or_zero(x[2 * i + 1], d));
             if (i < 4) q.lo |= byte << (8 * i);
             else q.hi |= byte << (8 * (i - 4));
         }

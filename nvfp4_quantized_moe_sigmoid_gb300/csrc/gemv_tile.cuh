@@ -110,31 +110,37 @@ __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes
 // ------------------------------------------------------------------ staging
 // A ring of `nstages` shared-memory stages, each holding one 16-row tile
 // (codes then scales), filled by one producer thread with bulk TMA copies.
-// Stage s is owned by the warp pair (s, s + 8): local item li goes to stage
-// li % nstages, whose two warps each take half of the tile's k-chunks and
-// both release the stage. Every use of a stage is therefore waited on, in
-// order, by the same warps. (An mbarrier parity wait names the current or
-// the immediately preceding phase; a waiter for use u must not start while
-// the barrier is still in phase u - 2, which fixed ownership guarantees.)
-constexpr int kPairs = 8;
-constexpr int kConsumerWarps = 2 * kPairs;
-constexpr int kMaxStages = kPairs;
+// Stage s is owned by the group of consumer warps w with w % nstages == s
+// (16 / nstages warps, rounded): local item li goes to stage li % nstages,
+// whose warps each take a contiguous share of the tile's k-chunks and all
+// release the stage; so every warp is busy whatever the stage count. Every
+// use of a stage is waited on, in order, by the same warps (an mbarrier parity
+// wait names the current or the immediately preceding phase; a waiter for use
+// u must not start while the barrier is still in phase u - 2, which fixed
+// ownership guarantees).
+constexpr int kConsumerWarps = 16;
+constexpr int kMaxStages = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kConsumerThreads = kConsumerWarps * 32;
+
+__device__ __forceinline__ int group_size(int s, int nstages) { return (kConsumerWarps - s + nstages - 1) / nstages; }
 
 struct Ring {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     int uses[kMaxStages];  // producer-side count of fills per stage
     int abort;
-    float xred[kPairs][2][32][4];  // partial tiles passed from warp s+8 to warp s
+    // partial tiles handed from the non-leading warps of a group to its
+    // leader, double-buffered by use parity; warp w >= nstages uses slot
+    // w - nstages
+    float4 xred[kConsumerWarps - 1][2][32];
 };
 
 __device__ __forceinline__ void ring_init(Ring& r, int nstages) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
             mbar_init(&r.full[s], 1);
-            mbar_init(&r.empty[s], 2);
+            mbar_init(&r.empty[s], group_size(s, nstages));
             r.uses[s] = 0;
         }
         r.abort = 0;
@@ -146,8 +152,8 @@ __device__ __forceinline__ void ring_init(Ring& r, int nstages) {
 // Returns false (and flags the ring) if the stage never became free.
 __device__ __forceinline__ bool ring_fill(Ring& r, uint8_t* ring_base, int stage_bytes, int nstages,
                                           int li, const uint8_t* codes, const uint8_t* scales, int K) {
-    const int s = li % nstages;
-    if (li >= nstages && !mbar_wait_bounded(&r.empty[s], ((li / nstages) - 1) & 1)) {
+    const int s = static_cast<int>(li % nstages);
+    if (li >= nstages && !mbar_wait_bounded(&r.empty[s], static_cast<uint32_t>(((li / nstages) - 1) & 1))) {
         set_dev_error(kErrWaitEmpty);
         r.abort = 1;
         return false;
@@ -163,8 +169,8 @@ __device__ __forceinline__ bool ring_fill(Ring& r, uint8_t* ring_base, int stage
 
 // Consumer side (whole warp): wait for local item li. False on timeout.
 __device__ __forceinline__ bool ring_acquire(Ring& r, int nstages, int li) {
-    const int s = li % nstages;
-    const bool ok = mbar_wait_bounded(&r.full[s], (li / nstages) & 1);
+    const int s = static_cast<int>(li % nstages);
+    const bool ok = mbar_wait_bounded(&r.full[s], static_cast<uint32_t>((li / nstages) & 1));
     const bool all_ok = __all_sync(0xffffffffu, ok);
     if (!all_ok && (threadIdx.x & 31) == 0) set_dev_error(kErrWaitFull);
     return all_ok;
@@ -191,44 +197,94 @@ __device__ __forceinline__ void consumer_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
-// The two warps of pair s (named barrier 2 + s); returns the AND of `pred`
-// over both warps, so that both take the same decision.
-__device__ __forceinline__ bool pair_bar_and(int s, bool pred) {
+// All consumer warps; returns the OR of `pred` over them (the same value in
+// every thread, so that all take the same branch).
+__device__ __forceinline__ bool consumer_bar_or(bool pred) {
     uint32_t out;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.and.pred q, %2, 64, p;\n\t"
+        "barrier.red.or.pred q, 1, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(out)
-        : "r"(pred ? 1u : 0u), "r"(2 + s)
+        : "r"(pred ? 1u : 0u), "n"(kConsumerThreads)
         : "memory");
     return out != 0;
 }
 
-// One staged tile, split between the two warps of its pair: half h computes
-// its half of the k-chunks; half 1 hands its partial to half 0 through shared
-// memory. Returns true for the warp that holds the finished tile in acc (half
-// 0); `ok` is false for both warps if either one timed out waiting.
-__device__ __forceinline__ bool pair_tile(Ring& r, int nstages, int li, const uint8_t* st, int K,
-                                          const __half* bcol, float (&acc)[4], bool& ok) {
+// The warps of stage group s (named barrier 2 + s, 32 * gs threads); returns
+// the AND of `pred` over them, so that all take the same decision.
+__device__ __forceinline__ bool group_bar_and(int s, int gs, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"(pred ? 1u : 0u), "r"(2 + s), "r"(32 * gs)
+        : "memory");
+    return out != 0;
+}
+
+// First local item index >= base that belongs to stage s.
+__device__ __forceinline__ int first_item(int base, int s, int nstages) {
+    return base + ((s - base % nstages) + nstages) % nstages;
+}
+
+// One staged tile, split between the warps of its stage group: rank p of gs
+// computes k-chunks [nc p / gs, nc (p + 1) / gs); the other warps hand their
+// partials to the leader (rank 0), which adds them in rank order. The leader
+// gets lead = 1 and the finished tile in acc; ok = 0 for every warp of the
+// group if any of them timed out waiting. Kept out of line: every kernel calls
+// it from several loops, and one shared copy keeps the instruction footprint
+// small.
+struct TileOut {
+    float4 acc;
+    int lead, ok;
+};
+
+__device__ __noinline__ TileOut group_tile_core(Ring* r, int nstages, int li, const uint8_t* st, int K,
+                                                const __half* bcol) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int s = warp % kPairs, half = warp / kPairs;
-    const int nc = (K + 127) >> 7, mid = (nc + 1) >> 1;
-    const bool got = ring_acquire(r, nstages, li);
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
-    if (got) tile_mma_16x8(st, st + 16 * (K >> 1), K, bcol, half ? mid : 0, half ? nc : mid, acc);
-    ring_release(r, nstages, li);
-    const int u = (li / nstages) & 1;
-    if (half) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v) r.xred[s][u][lane][v] = acc[v];
+    const int s = warp % nstages, rank = warp / nstages, gs = group_size(s, nstages);
+    const int nc = (K + 127) >> 7;
+    const bool got = ring_acquire(*r, nstages, li);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (got) tile_mma_16x8(st, st + 16 * (K >> 1), K, bcol, nc * rank / gs, nc * (rank + 1) / gs, acc);
+    ring_release(*r, nstages, li);
+    TileOut o;
+    o.acc = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    if (gs == 1) {
+        o.ok = got;
+        o.lead = got;
+        return o;
     }
-    ok = pair_bar_and(s, got);
-    if (half || !ok) return false;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) acc[v] += r.xred[s][u][lane][v];
-    return true;
+    const int u = static_cast<int>((li / nstages) & 1);
+    if (rank) r->xred[warp - nstages][u][lane] = o.acc;
+    o.ok = group_bar_and(s, gs, got);
+    o.lead = 0;
+    if (rank || !o.ok) return o;
+    for (int p = 1; p < gs; ++p) {
+        const float4 x = r->xred[s + p * nstages - nstages][u][lane];
+        o.acc.x += x.x;
+        o.acc.y += x.y;
+        o.acc.z += x.z;
+        o.acc.w += x.w;
+    }
+    o.lead = 1;
+    return o;
+}
+
+__device__ __forceinline__ bool group_tile(Ring& r, int nstages, int li, const uint8_t* st, int K,
+                                           const __half* bcol, float (&acc)[4], bool& ok) {
+    const TileOut o = group_tile_core(&r, nstages, li, st, K, bcol);
+    acc[0] = o.acc.x;
+    acc[1] = o.acc.y;
+    acc[2] = o.acc.z;
+    acc[3] = o.acc.w;
+    ok = o.ok != 0;
+    return o.lead != 0;
 }
 
 // Quantise (W4A4) or convert (W4A16) nrows bf16 rows of length K into f16
@@ -246,7 +302,7 @@ __device__ __forceinline__ uint4 ld_row16(const uint16_t* p) {
 constexpr int kBRegBlocks = 4;
 
 template <bool W4A4>
-__device__ __forceinline__ void b_block_store(const uint4& u0, const uint4& u1, float g, uint4* d) {
+__device__ __noinline__ void b_block_store(uint4 u0, uint4 u1, float g, uint4* d) {
     const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
     float v[16];
 #pragma unroll
@@ -269,7 +325,7 @@ __device__ __forceinline__ void b_block_store(const uint4& u0, const uint4& u1, 
 }
 
 template <bool W4A4, bool GSRC>
-__device__ __forceinline__ void prepare_b_rows(const uint16_t* const* src, int nrows, int K,
+__device__ __noinline__ void prepare_b_rows(const uint16_t* const* src, int nrows, int K,
                                                __half* dst, float* gout, unsigned int* red) {
     const int ctid = threadIdx.x;  // consumer thread index
     const int nb = K >> 4;
@@ -345,82 +401,11 @@ __device__ __forceinline__ void prepare_b_rows(const uint16_t* const* src, int n
 }
 
 
-// Unit-weight RMS norm of nrows bf16 rows (global, written by an earlier
-// kernel) into dst (shared memory), by the 16 consumer warps together:
-//   inv = 1 / sqrt(sum_i x_i^2 / K + eps),  y_i = bf16(x_i * inv).
-// The summation order is fixed by element index alone: chunk c holds elements
-// [256c, 256c + 256); lane l accumulates its eight elements 256c + 8l .. +7 in
-// order with fused multiply-adds; an xor-shuffle tree (commutative at each
-// level) gives the chunk sum; the chunk sums are added in chunk order. Every
-// kernel that calls this therefore computes the same bits. K % 8 == 0,
-// K <= 256 * kNormMaxChunks, nrows <= kNormMaxRows.
-constexpr int kNormMaxRows = 8;
-constexpr int kNormMaxChunks = 64;
-struct NormScratch {
-    float part[kNormMaxRows][kNormMaxChunks];
-    float inv[kNormMaxRows];
-};
-
-__device__ __forceinline__ void cta_rmsnorm_rows(const uint16_t* src, int nrows, int K, float eps, uint16_t* dst,
-                                                 NormScratch& ns) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nch = (K + 255) >> 8;
-    for (int item = warp; item < nrows * nch; item += kConsumerWarps) {
-        const int r = item / nch, c = item % nch;
-        const int i = 256 * c + 8 * lane;
-        float ss = 0.0f;
-        if (i < K) {
-            const uint4 v = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)r * K + i));
-            *reinterpret_cast<uint4*>(dst + (size_t)r * K + i) = v;
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
-                ss = __fmaf_rn(a, a, ss);
-                ss = __fmaf_rn(b, b, ss);
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-        if (lane == 0) ns.part[r][c] = ss;
-    }
-    consumer_bar();
-    if (threadIdx.x < nrows) {
-        float s = 0.0f;
-        for (int c = 0; c < nch; ++c) s = __fadd_rn(s, ns.part[threadIdx.x][c]);
-        ns.inv[threadIdx.x] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, static_cast<float>(K)), eps)));
-    }
-    consumer_bar();
-    for (int i = 8 * threadIdx.x; i < nrows * K; i += 8 * kConsumerThreads) {
-        const float inv = ns.inv[i / K];
-        const uint4 v = *reinterpret_cast<const uint4*>(dst + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat16 lo = __float2bfloat16_rn(__fmul_rn(__uint_as_float(w[j] << 16), inv));
-            const __nv_bfloat16 hi = __float2bfloat16_rn(__fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), inv));
-            o[j] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&lo)) |
-                   (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
-        }
-        *reinterpret_cast<uint4*>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    consumer_bar();
-}
-
-// Copy nrows bf16 rows (global, written by an earlier kernel) into dst, all
-// consumer threads.
-__device__ __forceinline__ void cta_copy_rows(const uint16_t* src, int nrows, int K, uint16_t* dst) {
-    for (int i = 8 * threadIdx.x; i < nrows * K; i += 8 * kConsumerThreads)
-        *reinterpret_cast<uint4*>(dst + i) = __ldcg(reinterpret_cast<const uint4*>(src + i));
-    consumer_bar();
-}
-
 // B rows from global bf16 rows whose globals are already known: gk[r] holds
 // the row amax bits (W4A4; g = amax / 2688), so every block is quantised
 // independently in one pass. Rows with src == null are zero-filled.
 template <bool W4A4>
-__device__ __forceinline__ void prepare_b_rows_known_amax(const uint16_t* const* src, int nrows, int K, __half* dst,
+__device__ __noinline__ void prepare_b_rows_known_amax(const uint16_t* const* src, int nrows, int K, __half* dst,
                                                           const unsigned int* amax_bits, float* gout) {
     const int ctid = threadIdx.x;
     const int nb = K >> 4;

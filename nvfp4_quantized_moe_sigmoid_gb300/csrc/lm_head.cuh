@@ -76,12 +76,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
         const float gw = __ldg(a.global);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
-        const int s = warp % kPairs;
-        for (int li = s; s < nst && li < n; li += nst) {
+        const int s = warp % nst;
+        for (int li = s; li < n; li += nst) {
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = pair_tile(ring, nst, li, st, a.H, bcol, acc, ok);
+            const bool mine = group_tile(ring, nst, li, st, a.H, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const int64_t row0 = 16 * (ib + li);

@@ -172,12 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_up_decode(const UpArgs a) {
         prepare_b_rows<W4A4, false>(srcs, a.T, a.H, xb, gx, red);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
-        const int s = warp % kPairs;
-        for (int li = s; s < nst && li < n; li += nst) {
+        const int s = warp % nst;
+        for (int li = s; li < n; li += nst) {
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = pair_tile(ring, nst, li, st, a.H, bcol, acc, ok);
+            const bool mine = group_tile(ring, nst, li, st, a.H, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const bool routed = li >= n_sh;
@@ -335,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
         }
 
         const int g = lane >> 2, q = lane & 3;
-        const int s = warp % kPairs;
-        for (int li = s; s < nst && li < n; li += nst) {
+        const int s = warp % nst;
+        for (int li = s; li < n; li += nst) {
             const bool routed = li >= n_sh;
             int u = -1, r, sl, K;
             if (routed) {
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = pair_tile(ring, nst, li, st, K, bcol, acc, ok);
+            const bool mine = group_tile(ring, nst, li, st, K, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const float gw = routed ? __ldg(a.global + plan.expert[u]) : __ldg(a.sh_global);

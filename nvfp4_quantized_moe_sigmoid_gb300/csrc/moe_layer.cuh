@@ -178,12 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_up(const LayerUpArgs a) {
         if (!bok && lane == 0) set_dev_error(kErrWaitFull);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = (bok && g < a.T) ? xb + (size_t)g * a.H : nullptr;
-        const int s = warp % kPairs;
-        for (int li = s; s < nst && li < n; li += nst) {
+        const int s = warp % nst;
+        for (int li = s; li < n; li += nst) {
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = pair_tile(ring, nst, li, st, a.H, bcol, acc, ok);
+            const bool mine = group_tile(ring, nst, li, st, a.H, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const bool routed = li >= n_sh;
@@ -389,8 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_down(const LayerDownArgs 
         const bool bok = __all_sync(0xffffffffu, mbar_wait_bounded(&bbar, 0));
         if (!bok && lane == 0) set_dev_error(kErrWaitFull);
         const int g = lane >> 2, q = lane & 3;
-        const int s = warp % kPairs;
-        for (int li = s; s < nst && li < n; li += nst) {
+        const int s = warp % nst;
+        for (int li = s; li < n; li += nst) {
             const bool routed = li >= n_sh;
             int u = -1, r, sl, K;
             if (routed) {
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_down(const LayerDownArgs 
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = pair_tile(ring, nst, li, st, K, bcol, acc, ok);
+            const bool mine = group_tile(ring, nst, li, st, K, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const float gw = routed ? __ldg(a.global + plan.expert[u]) : __ldg(a.sh_global);

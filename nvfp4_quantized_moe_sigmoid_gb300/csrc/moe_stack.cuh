@@ -1,0 +1,831 @@
+// moe_stack.cuh - moe_stack_forward: L consecutive MoE decode layers (1..4
+// tokens, pre-norm residual chain h_{l+1} = h_l + moe_l(norm(h_l))) in one
+// persistent cooperative kernel, one CTA per SM.
+//
+// Decode at this size is a stream of NVFP4 weights ("Let's optimize Nemotron
+// 3.5 Lightning - a worklog", Interlude), and between layers it is a chain of
+// small dependent steps (router, top-k, experts, combine). Separate kernels
+// pay a drain and a fill at every step; here every CTA runs the whole chain
+// and the steps meet through per-layer counters in the workspace:
+//
+//   per layer l, every CTA:
+//     1. wait until every 16-row tile of h_l is final (counter); load h_l;
+//     2. x = RMSNorm(h_l); B operand of the up tiles (NVFP4 in W4A4);
+//     3. router logits of this CTA's experts (gate rows staged in shared
+//        memory during the previous layer) -> workspace, count them;
+//     4. its share of the shared expert's up tiles (staged during the
+//        previous layer): relu^2 -> bf16 rows + row amax (W4A4);
+//     5. wait for all E logits; sigmoid + bias top-k (rank per expert, every
+//        CTA computes the same selection), the step plan (unique experts);
+//     6. its share of the routed up tiles (per-expert done counters);
+//     7. wait for the experts whose down tiles it owns; quantise their
+//        intermediate rows with the now final row amax (W4A4) as its B operand;
+//     8. its share of the shared and routed down tiles -> gate-weighted FP32
+//        partial rows; each tile counts its contribution to its 16 output
+//        rows, and the warp that brings the last one (U routed + 1 shared)
+//        combines them: h_{l+1} = bf16(shared + sum_j gate_j y_j + h_l).
+//
+// One producer thread streams every tile the CTA owns through the staging
+// ring in consumption order, and fills the next layer's constant tiles
+// (router rows, shared-expert up tiles) as soon as stages free up, so they
+// land while the current layer is still waiting on its dependencies.
+// Every wait is bounded; a CTA that gives up sets the workspace abort flag,
+// which ends every other CTA's waits, and the last CTA to leave resets the
+// counters for the next call.
+//
+// The steps are out-of-line functions sharing one per-CTA context in shared
+// memory, which keeps the code a layer runs small enough for the SM's
+// instruction cache to hold from one layer to the next.
+#pragma once
+
+#include "moe_decode.cuh"
+
+namespace nvfp4moe {
+
+constexpr int kStackMaxLayers = 32;
+
+struct StackLayer {
+    const uint8_t* up_codes;  // [E][I][H/2]
+    const uint8_t* up_scales;
+    const float* up_global;   // [E]
+    const uint8_t* down_codes;  // [E][H][I/2]
+    const uint8_t* down_scales;
+    const float* down_global;
+    const uint8_t* shu_codes;  // [S][H/2]
+    const uint8_t* shu_scales;
+    const float* shu_global;
+    const uint8_t* shd_codes;  // [H][S/2]
+    const uint8_t* shd_scales;
+    const float* shd_global;
+    const float* router_w;  // [E][H]
+    const float* router_b;  // [E]
+};
+
+// Per-layer counters: fixed slots, then one per unique expert, then one per
+// 16-row output tile.
+constexpr int kCntLogits = 0;  // router logits written (target E)
+constexpr int kCntShUp = 1;    // shared-expert up tiles done (target S/16)
+constexpr int kCntHDone = 2;   // output tiles of h_{l+1} final (target H/16)
+constexpr int kCntUp = 3;      // + u: up tiles of unique expert u done (target I/16)
+constexpr int kCntTile = kCntUp + kDecodeMaxU;  // + r: contributions to output tile r (target U + 1)
+__host__ __device__ constexpr int stack_cnt_per_layer(int H) { return kCntTile + H / 16; }
+
+struct StackWs {
+    int* cnt;            // [L][stack_cnt_per_layer], then the exit count and the abort flag
+    float* z;            // [L][T][E] router logits
+    uint16_t* act;       // [T*k][I] bf16 relu^2 rows of the routed experts
+    uint16_t* act_sh;    // [T][S] of the shared expert
+    unsigned int* amax;  // [2][T*k + T] row amax bits of act, then act_sh, by layer parity
+    float* ypart;        // [T*k][H] gate-weighted down rows
+    float* ysh;          // [T][H] shared-expert down rows
+};
+
+struct StackArgs {
+    StackLayer layer[kStackMaxLayers];
+    int L, E, H, I, S, T, k;
+    float rms_eps;
+    const uint16_t* hidden_in;  // [T][H] h_0
+    uint16_t* hidden_out;       // [L][T][H] h_1 .. h_L
+    int32_t* topk_idx;          // [L][T][k]
+    float* topk_w;              // [L][T][k]
+    StackWs ws;
+    int nst, stage_bytes;
+    int off_gate, off_uni, off_tk;  // dynamic shared-memory regions after the ring
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *p >= target. False if the wait expired (flags the error word and
+// the abort flag) or another CTA raised the abort flag.
+__device__ __noinline__ bool wait_geq(const int* p, int target, int* abort_g) {
+    const unsigned long long t0 = globaltimer();
+    for (int it = 0;; ++it) {
+        if (ld_acquire_gpu(p) >= target) return true;
+        if ((it & 15) == 15) {
+            if (ld_acquire_gpu(abort_g)) return false;
+            if (globaltimer() - t0 > kWaitTimeoutNs) {
+                set_dev_error(kErrWaitPeer);
+                atomicExch(abort_g, 1);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __noinline__ bool mbar_wait_abortable(uint64_t* b, uint32_t parity, volatile int* abort_s) {
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(b, parity)) return true;
+        if (*abort_s) return false;
+        if (globaltimer() - t0 > kWaitTimeoutNs) {
+            set_dev_error(kErrWaitFull);
+            return false;
+        }
+    }
+}
+
+constexpr int kNormMaxChunks = 64;  // H <= 16384
+
+// Per-CTA state of the stack kernel, in shared memory.
+struct StackCta {
+    Ring ring;
+    DecodePlan plan;
+    uint64_t gbar;  // router rows landed (one phase per layer)
+    uint64_t pbar;  // plan ready for the producer (one phase per layer)
+    uint64_t qbar;  // producer done reading the plan (one phase per layer)
+    int gate_issued;
+    int abort_s;
+    // geometry
+    int G, b, nst, stage_bytes, ng, amax_stride;
+    int su_b, su_e, sd_b, sd_e;  // shared-expert up / down tile ranges of this CTA
+    uint8_t* ring_base;
+    float* gsm;      // [ng][H] router rows
+    uint16_t* X;     // [T][H] h_l, then x_l
+    __half* xq;      // [T][H] up B operand
+    __half* bslot;   // down B: routed [T][I], [T][I], shared [T][S] (aliases X, xq)
+    float* tk_c;     // [T][E] biased scores
+    float* tk_s;     // [T][E] sigmoids
+    // step scratch
+    float norm_part[kDecodeMaxT][kNormMaxChunks];
+    float norm_inv[kDecodeMaxT];
+    float gx[kDecodeMaxT];
+    unsigned int red[kDecodeMaxT];
+    const uint16_t* srcs[3 * kDecodeMaxT];
+    unsigned int amx[3 * kDecodeMaxT];
+    float gbf[3 * kDecodeMaxT];
+    int sel_idx[kDecodeMaxT][kDecodeMaxK];
+    float sel_sig[kDecodeMaxT][kDecodeMaxK];
+    float sel_w[kDecodeMaxT][kDecodeMaxK];
+    float zred[kConsumerWarps][kDecodeMaxT];
+    int slot_u[2];
+};
+
+__device__ __forceinline__ bool cta_abort(StackCta& c) { return *static_cast<volatile int*>(&c.abort_s) != 0; }
+__device__ __forceinline__ void set_cta_abort(StackCta& c) { *static_cast<volatile int*>(&c.abort_s) = 1; }
+
+__device__ __forceinline__ int* layer_cnt(const StackArgs& a, int l) {
+    return a.ws.cnt + (size_t)l * stack_cnt_per_layer(a.H);
+}
+__device__ __forceinline__ int* abort_flag(const StackArgs& a) {
+    return a.ws.cnt + (size_t)a.L * stack_cnt_per_layer(a.H) + 1;
+}
+
+// Even share of n items: CTA b of G takes [n b / G, n (b + 1) / G) (n G < 2^31).
+__device__ __forceinline__ int share_begin32(int n, int b, int G) { return n * b / G; }
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    const __nv_bfloat16 x = __float2bfloat16_rn(lo), y = __float2bfloat16_rn(hi);
+    return static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&x)) |
+           (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&y)) << 16);
+}
+
+// ---------------------------------------------------------------- steps 1-2
+// h_l (global, final) -> X; x_l = RMSNorm(h_l) in place (or h_l); the up
+// tiles' B operand from x_l. RMS norm: inv = 1/sqrt(sum x^2 / H + eps),
+// y = bf16(x * inv); chunk c = elements [256c, 256c + 256), lane l sums its
+// eight elements 256c + 8l .. + 7 in order (fused multiply-add), an
+// xor-shuffle tree gives the chunk sum, chunk sums are added in chunk order.
+template <bool W4A4>
+__device__ __noinline__ void st_input(const StackArgs& a, StackCta& c, const uint16_t* h) {
+    const int ctid = threadIdx.x, warp = ctid >> 5, lane = ctid & 31;
+    const int T = a.T, H = a.H;
+    uint16_t* X = c.X;
+#pragma unroll 1
+    for (int i = 8 * ctid; i < T * H; i += 8 * kConsumerThreads)
+        *reinterpret_cast<uint4*>(X + i) = __ldcg(reinterpret_cast<const uint4*>(h + i));
+    consumer_bar();
+    if (a.rms_eps > 0.0f) {
+        const int nch = (H + 255) >> 8;
+#pragma unroll 1
+        for (int item = warp; item < T * nch; item += kConsumerWarps) {
+            const int r = item / nch, ch = item % nch;
+            const int i = 256 * ch + 8 * lane;
+            float ss = 0.0f;
+            if (i < H) {
+                const uint4 v = *reinterpret_cast<const uint4*>(X + (size_t)r * H + i);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float x0 = __uint_as_float(w[j] << 16), x1 = __uint_as_float(w[j] & 0xFFFF0000u);
+                    ss = __fmaf_rn(x0, x0, ss);
+                    ss = __fmaf_rn(x1, x1, ss);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+            if (lane == 0) c.norm_part[r][ch] = ss;
+        }
+        consumer_bar();
+        if (ctid < T) {
+            float sum = 0.0f;
+#pragma unroll 1
+            for (int ch = 0; ch < nch; ++ch) sum = __fadd_rn(sum, c.norm_part[ctid][ch]);
+            c.norm_inv[ctid] =
+                __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, static_cast<float>(H)), a.rms_eps)));
+        }
+        consumer_bar();
+#pragma unroll 1
+        for (int i = 8 * ctid; i < T * H; i += 8 * kConsumerThreads) {
+            const float inv = c.norm_inv[i / H];
+            const uint4 v = *reinterpret_cast<const uint4*>(X + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                o[j] = bf16x2_rn(__fmul_rn(__uint_as_float(w[j] << 16), inv),
+                                 __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), inv));
+            *reinterpret_cast<uint4*>(X + i) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    // B operand: per-row global = amax / 2688 (W4A4), then each 16-block
+    const int nb = H >> 4;
+    if (W4A4) {
+        if (ctid < T) c.red[ctid] = 0u;
+        consumer_bar();
+#pragma unroll 1
+        for (int i = ctid; i < T * nb; i += kConsumerThreads) {
+            const uint16_t* p = X + (size_t)(i / nb) * H + 16 * (i % nb);
+            const uint4 u0 = *reinterpret_cast<const uint4*>(p), u1 = *reinterpret_cast<const uint4*>(p + 8);
+            const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            float mx = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+            atomicMax(&c.red[i / nb], __float_as_uint(mx));
+        }
+    }
+    consumer_bar();
+    if (W4A4 && ctid < T) c.gx[ctid] = __fdiv_rn(__uint_as_float(c.red[ctid]), 2688.0f);
+#pragma unroll 1
+    for (int i = ctid; i < T * nb; i += kConsumerThreads) {
+        const int r = i / nb;
+        const uint16_t* p = X + (size_t)r * H + 16 * (i % nb);
+        const float g = W4A4 ? __fdiv_rn(__uint_as_float(c.red[r]), 2688.0f) : 0.0f;
+        b_block_store<W4A4>(*reinterpret_cast<const uint4*>(p), *reinterpret_cast<const uint4*>(p + 8), g,
+                            reinterpret_cast<uint4*>(c.xq + (size_t)r * H + 16 * (i % nb)));
+    }
+    consumer_bar();
+}
+
+// ---------------------------------------------------------------- step 3
+// z[t][e] = sum_i x[t][i] Wg[e][i] (FP32) for this CTA's experts e = b + j G.
+// Returns false if the router rows never landed.
+__device__ __noinline__ bool st_router(const StackArgs& a, StackCta& c, int l) {
+    const int ctid = threadIdx.x, warp = ctid >> 5, lane = ctid & 31;
+    const int T = a.T, H = a.H, E = a.E;
+    const bool ok = mbar_wait_bounded(&c.gbar, static_cast<uint32_t>(l & 1));
+    if (consumer_bar_or(!ok || cta_abort(c))) {
+        if (ctid == 0 && !ok) set_dev_error(kErrWaitFull);
+        return false;
+    }
+    float* z = a.ws.z + (size_t)l * T * E;
+#pragma unroll 1
+    for (int j = 0; j < c.ng; ++j) {
+        const float4* w4 = reinterpret_cast<const float4*>(c.gsm + (size_t)j * H);
+        float acc[kDecodeMaxT] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+        for (int i4 = ctid; i4 < H / 4; i4 += kConsumerThreads) {
+            const float4 w = w4[i4];
+#pragma unroll
+            for (int t = 0; t < kDecodeMaxT; ++t) {
+                if (t < T) {
+                    const uint2 hv = *reinterpret_cast<const uint2*>(c.X + (size_t)t * H + 4 * i4);
+                    acc[t] = fmaf(w.x, __uint_as_float(hv.x << 16), acc[t]);
+                    acc[t] = fmaf(w.y, __uint_as_float(hv.x & 0xFFFF0000u), acc[t]);
+                    acc[t] = fmaf(w.z, __uint_as_float(hv.y << 16), acc[t]);
+                    acc[t] = fmaf(w.w, __uint_as_float(hv.y & 0xFFFF0000u), acc[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t) {
+            float v = acc[t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) c.zred[warp][t] = v;
+        }
+        consumer_bar();
+        if (ctid < T) {
+            float s = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) s = __fadd_rn(s, c.zred[w][ctid]);
+            z[(size_t)ctid * E + c.b + j * c.G] = s;
+            __threadfence();
+        }
+        consumer_bar();
+    }
+    if (ctid == 0 && c.ng > 0) atomicAdd(layer_cnt(a, l) + kCntLogits, c.ng);
+    return true;
+}
+
+// ---------------------------------------------------------------- step 5
+// Top-k by (sigma + bias desc, index asc) for every token, its gates
+// sigma / sum(sigma), and the step plan. Every CTA computes the same result.
+__device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l) {
+    const int ctid = threadIdx.x;
+    const int T = a.T, E = a.E, k = a.k;
+    const float* z = a.ws.z + (size_t)l * T * E;
+    const float* bias = a.layer[l].router_b;
+#pragma unroll 1
+    for (int i = ctid; i < T * E; i += kConsumerThreads) {
+        const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-__ldcg(z + i))));
+        float s = __fadd_rn(sg, __ldg(bias + i % E));
+        if (s != s) s = -INFINITY;
+        c.tk_c[i] = s;
+        c.tk_s[i] = sg;
+    }
+    if (ctid < 8) c.plan.bits[ctid] = 0u;
+#pragma unroll 1
+    for (int i = ctid; i < kDecodeMaxU * kDecodeMaxT; i += kConsumerThreads) {
+        (&c.plan.choice[0][0])[i] = -1;
+        (&c.plan.gate[0][0])[i] = 0.0f;
+    }
+    consumer_bar();
+#pragma unroll 1
+    for (int i = ctid; i < T * E; i += kConsumerThreads) {
+        const int t = i / E, e = i % E;
+        const float* ct = c.tk_c + (size_t)t * E;
+        const float s = ct[e];
+        // rank = #{e2 : s2 > s or (s2 == s and e2 < e)}; four scores per
+        // 16-byte load (E % 4 == 0), two independent counts
+        int r0 = 0, r1 = 0;
+#pragma unroll 4
+        for (int e2 = 0; e2 < E; e2 += 8) {
+            const float4 p = *reinterpret_cast<const float4*>(ct + e2);
+            const float4 q = *reinterpret_cast<const float4*>(ct + e2 + 4);
+            r0 += (p.x > s || (p.x == s && e2 < e)) + (p.y > s || (p.y == s && e2 + 1 < e)) +
+                  (p.z > s || (p.z == s && e2 + 2 < e)) + (p.w > s || (p.w == s && e2 + 3 < e));
+            r1 += (q.x > s || (q.x == s && e2 + 4 < e)) + (q.y > s || (q.y == s && e2 + 5 < e)) +
+                  (q.z > s || (q.z == s && e2 + 6 < e)) + (q.w > s || (q.w == s && e2 + 7 < e));
+        }
+        const int rank = r0 + r1;
+        if (rank < k) {
+            c.sel_idx[t][rank] = e;
+            c.sel_sig[t][rank] = c.tk_s[i];
+        }
+    }
+    consumer_bar();
+    if (ctid < T) {
+        float ssum = 0.0f;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) ssum = __fadd_rn(ssum, c.sel_sig[ctid][j]);
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            const float w = __fdiv_rn(c.sel_sig[ctid][j], ssum);
+            c.sel_w[ctid][j] = w;
+            if (c.b == 0) {
+                a.topk_idx[((size_t)l * T + ctid) * k + j] = c.sel_idx[ctid][j];
+                a.topk_w[((size_t)l * T + ctid) * k + j] = w;
+            }
+        }
+    }
+    if (ctid < T * k) {
+        const int e = c.sel_idx[ctid / k][ctid % k];
+        atomicOr(&c.plan.bits[e >> 5], 1u << (e & 31));
+    }
+    consumer_bar();
+    if (ctid < T * k) {
+        const int t = ctid / k, j = ctid % k;
+        const int e = c.sel_idx[t][j];
+        int slot = __popc(c.plan.bits[e >> 5] & ((1u << (e & 31)) - 1u));
+#pragma unroll 1
+        for (int w = 0; w < (e >> 5); ++w) slot += __popc(c.plan.bits[w]);
+        c.plan.expert[slot] = e;
+        c.plan.choice[slot][t] = static_cast<int8_t>(j);
+        c.plan.gate[slot][t] = c.sel_w[t][j];
+    }
+    if (ctid == 0) {
+        int u = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) u += __popc(c.plan.bits[w]);
+        c.plan.U = u;
+    }
+    consumer_bar();
+}
+
+// ---------------------------------------------------------------- steps 4, 6
+// Up tiles [base, base + n): shared (routed == false, tiles su_b + i) or
+// routed (tiles i of the U x I/16 list from ru_b). relu^2 -> bf16 rows, row
+// amax (W4A4), one count per finished tile. Returns false on a timeout.
+template <bool W4A4>
+__device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l, int base, int n, bool routed,
+                                         int ru_b) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int T = a.T, k = a.k, H = a.H, I = a.I, S = a.S, RI = I >> 4;
+    const int nst = c.nst;
+    const StackLayer& P = a.layer[l];
+    unsigned int* const amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
+    int* const cnt = layer_cnt(a, l);
+    const __half* bcol = g < T ? c.xq + (size_t)g * H : nullptr;
+    const int end = base + n;
+#pragma unroll 1
+    for (int li = first_item(base, warp % nst, nst); li < end; li += nst) {
+        const uint8_t* st = c.ring_base + (size_t)(li % nst) * c.stage_bytes;
+        float acc[4];
+        bool ok;
+        const bool lead = group_tile(c.ring, nst, li, st, H, bcol, acc, ok);
+        if (!ok) return false;
+        if (!lead) continue;
+        int u = 0, r;
+        if (routed) {
+            const int i = ru_b + (li - base);
+            u = i / RI;
+            r = i % RI;
+        } else {
+            r = c.su_b + (li - base);
+        }
+        const float gw = routed ? __ldg(P.up_global + c.plan.expert[u]) : __ldg(P.shu_global);
+        float m[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int t = 2 * q + (v & 1);
+            if (t >= T) continue;
+            const int j = routed ? c.plan.choice[u][t] : 0;
+            if (j < 0) continue;
+            const float gs = W4A4 ? __fmul_rn(gw, c.gx[t]) : gw;
+            const float rl = fmaxf(__fmul_rn(acc[v], gs), 0.0f);
+            const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
+            const int row = 16 * r + g + 8 * (v >> 1);
+            uint16_t* dst = routed ? a.ws.act + ((size_t)t * k + j) * I : a.ws.act_sh + (size_t)t * S;
+            dst[row] = *reinterpret_cast<const uint16_t*>(&bv);
+            m[v & 1] = fmaxf(m[v & 1], __bfloat162float(bv));
+        }
+        if (W4A4) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], o));
+                m[1] = fmaxf(m[1], __shfl_xor_sync(0xffffffffu, m[1], o));
+            }
+            if (g == 0) {
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int t = 2 * q + p;
+                    if (t >= T) continue;
+                    if (routed) {
+                        const int j = c.plan.choice[u][t];
+                        if (j >= 0) atomicMax(amax + t * k + j, __float_as_uint(m[p]));
+                    } else {
+                        atomicMax(amax + T * k + t, __float_as_uint(m[p]));
+                    }
+                }
+            }
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(cnt + (routed ? kCntUp + u : kCntShUp), 1);
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------- step 7
+// B operands of this CTA's down tiles: routed experts slot_u[0..1] ([T][I]
+// each) and the shared expert ([T][S]), from the finished bf16 rows and their
+// final row amax. Returns false if a wait failed.
+template <bool W4A4>
+__device__ __noinline__ bool st_down_operands(const StackArgs& a, StackCta& c, int l, int rd_b, int rd_e) {
+    const int ctid = threadIdx.x;
+    const int T = a.T, k = a.k, I = a.I, S = a.S, RI = I >> 4, RS = S >> 4, RH = a.H >> 4;
+    const bool has_sd = c.sd_e > c.sd_b;
+    int* const cnt = layer_cnt(a, l);
+    const unsigned int* amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
+    if (ctid == 0) {
+        c.slot_u[0] = c.slot_u[1] = -1;
+        if (rd_e > rd_b) {
+            c.slot_u[0] = rd_b / RH;
+            const int u1 = (rd_e - 1) / RH;
+            if (u1 != c.slot_u[0]) c.slot_u[1] = u1;
+        }
+    }
+    consumer_bar();  // also: every up tile of this CTA is done, X / xq may be overwritten
+    bool ok = true;
+    if (ctid == 0 && has_sd) ok = wait_geq(cnt + kCntShUp, RS, abort_flag(a));
+    if (ctid == 32 && c.slot_u[0] >= 0) ok = wait_geq(cnt + kCntUp + c.slot_u[0], RI, abort_flag(a));
+    if (ctid == 64 && c.slot_u[1] >= 0) ok = wait_geq(cnt + kCntUp + c.slot_u[1], RI, abort_flag(a));
+    if (consumer_bar_or(!ok || cta_abort(c))) return false;
+    if (ctid < 2 * T) {
+        const int sl = ctid / T, t = ctid % T;
+        const uint16_t* p = nullptr;
+        unsigned int mx = 0u;
+        if (c.slot_u[sl] >= 0) {
+            const int j = c.plan.choice[c.slot_u[sl]][t];
+            if (j >= 0) {
+                p = a.ws.act + ((size_t)t * k + j) * I;
+                if (W4A4) mx = __ldcg(amax + t * k + j);
+            }
+        }
+        c.srcs[ctid] = p;
+        c.amx[ctid] = mx;
+    } else if (ctid >= 64 && ctid < 64 + T) {
+        const int t = ctid - 64;
+        c.srcs[2 * T + t] = a.ws.act_sh + (size_t)t * S;
+        c.amx[2 * T + t] = W4A4 ? __ldcg(amax + T * k + t) : 0u;
+    }
+    consumer_bar();
+    prepare_b_rows_known_amax<W4A4>(c.srcs, 2 * T, I, c.bslot, c.amx, c.gbf);
+    if (has_sd)
+        prepare_b_rows_known_amax<W4A4>(c.srcs + 2 * T, T, S, c.bslot + (size_t)2 * T * I, c.amx + 2 * T,
+                                        c.gbf + 2 * T);
+    return true;
+}
+
+// The warp that completes output tile r of layer l: its 16 rows of
+// h_{l+1} = bf16(((ysh + y_0) + y_1) + ... + y_{k-1} + h_l), FP32 in this order.
+__device__ __noinline__ void combine_tile(const StackArgs& a, StackCta& c, int l, int r) {
+    const int lane = threadIdx.x & 31;
+    const int T = a.T, k = a.k, H = a.H;
+    const uint16_t* res = l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H;
+    uint16_t* out = a.hidden_out + (size_t)l * T * H;
+    // the next layer's row amax buffer starts at zero: its last readers (layer
+    // l - 1) are done, and its first writers wait until every tile is final
+    unsigned int* am = a.ws.amax + (size_t)((l + 1) & 1) * c.amax_stride;
+#pragma unroll 1
+    for (int i = lane; i < c.amax_stride; i += 32) am[i] = 0u;
+#pragma unroll 1
+    for (int o = lane; o < 16 * T; o += 32) {
+        const int t = o >> 4, row = 16 * r + (o & 15);
+        float y[kDecodeMaxK];
+#pragma unroll
+        for (int j = 0; j < kDecodeMaxK; ++j)
+            if (j < k) y[j] = __ldcg(a.ws.ypart + ((size_t)t * k + j) * H + row);
+        float acc = __ldcg(a.ws.ysh + (size_t)t * H + row);
+        const float rv = bf16_bits_to_float(__ldcg(res + (size_t)t * H + row));
+#pragma unroll
+        for (int j = 0; j < kDecodeMaxK; ++j)
+            if (j < k) acc = __fadd_rn(acc, y[j]);
+        acc = __fadd_rn(acc, rv);
+        const __nv_bfloat16 ob = __float2bfloat16_rn(acc);
+        out[(size_t)t * H + row] = *reinterpret_cast<const uint16_t*>(&ob);
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) atomicAdd(layer_cnt(a, l) + kCntHDone, 1);
+}
+
+// ---------------------------------------------------------------- step 8
+template <bool W4A4>
+__device__ __noinline__ bool st_down_tiles(const StackArgs& a, StackCta& c, int l, int base, int rd_b, int n_rd) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int T = a.T, k = a.k, H = a.H, I = a.I, S = a.S, RH = H >> 4;
+    const int nst = c.nst;
+    const int n_sd = c.sd_e - c.sd_b;
+    const StackLayer& P = a.layer[l];
+    int* const cnt = layer_cnt(a, l);
+    const int U = c.plan.U;
+    const __half* bslot2 = c.bslot + (size_t)2 * T * I;
+    const int end = base + n_sd + n_rd;
+#pragma unroll 1
+    for (int li = first_item(base, warp % nst, nst); li < end; li += nst) {
+        const bool routed = li >= base + n_sd;
+        int u = -1, r, sl, K;
+        if (routed) {
+            const int i = rd_b + (li - base - n_sd);
+            u = i / RH;
+            r = i % RH;
+            sl = u == c.slot_u[0] ? 0 : (u == c.slot_u[1] ? 1 : -1);
+            K = I;
+        } else {
+            r = c.sd_b + (li - base);
+            sl = 2;
+            K = S;
+        }
+        if (sl < 0 && lane == 0) set_dev_error(kErrBadInput);
+        const __half* bs = sl == 2 ? bslot2 : c.bslot + (size_t)(sl < 0 ? 0 : sl) * T * I;
+        const __half* bcol = nullptr;
+        if (sl >= 0 && g < T && (!routed || c.plan.choice[u][g] >= 0)) bcol = bs + (size_t)g * K;
+        const uint8_t* st = c.ring_base + (size_t)(li % nst) * c.stage_bytes;
+        float acc[4];
+        bool ok;
+        const bool lead = group_tile(c.ring, nst, li, st, K, bcol, acc, ok);
+        if (!ok) return false;
+        if (!lead) continue;
+        const float gw = routed ? __ldg(P.down_global + c.plan.expert[u]) : __ldg(P.shd_global);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int t = 2 * q + (v & 1);
+            const int row = 16 * r + g + 8 * (v >> 1);
+            if (t >= T || sl < 0) continue;
+            const float gs = W4A4 ? __fmul_rn(gw, c.gbf[sl * T + t]) : gw;
+            const float y = __fmul_rn(acc[v], gs);
+            if (routed) {
+                const int j = c.plan.choice[u][t];
+                if (j >= 0) a.ws.ypart[((size_t)t * k + j) * H + row] = __fmul_rn(c.plan.gate[u][t], y);
+            } else {
+                a.ws.ysh[(size_t)t * H + row] = y;
+            }
+        }
+        // count this contribution to output tile r; the last one combines it
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(cnt + kCntTile + r, 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == U) {
+            __threadfence();
+            combine_tile(a, c, l, r);
+        }
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------- producer
+// One out-of-line fill (the producer streams four kinds of tile from one loop
+// each; a shared copy keeps its code small).
+__device__ __noinline__ bool fill_stage(StackCta& c, int li, const uint8_t* codes, const uint8_t* scales, int K) {
+    return ring_fill(c.ring, c.ring_base, c.stage_bytes, c.nst, li, codes, scales, K);
+}
+
+__device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
+    const int H = a.H, I = a.I, S = a.S, RI = I >> 4, RH = H >> 4;
+    const int G = c.G, b = c.b;
+    int pli = 0;
+    bool alive = true;
+    auto fill = [&](const uint8_t* codes, const uint8_t* scales, int K) {
+        if (!alive) return;
+        if (cta_abort(c) || !fill_stage(c, pli, codes, scales, K)) {
+            alive = false;
+            set_cta_abort(c);
+            return;
+        }
+        ++pli;
+    };
+    auto issue_gate = [&](int l) {
+        if (c.ng == 0) return;
+        mbar_arrive_expect_tx(&c.gbar, (uint32_t)(c.ng * H * 4));
+#pragma unroll 1
+        for (int j = 0; j < c.ng; ++j)
+            bulk_g2s(c.gsm + (size_t)j * H, a.layer[l].router_w + (size_t)(b + j * G) * H, (uint32_t)(H * 4),
+                     &c.gbar);
+        c.gate_issued += 1;
+    };
+    auto issue_shared_up = [&](int l) {
+        const StackLayer& P = a.layer[l];
+#pragma unroll 1
+        for (int r = c.su_b; r < c.su_e; ++r)
+            fill(P.shu_codes + (size_t)16 * r * (H >> 1), P.shu_scales + (size_t)16 * r * (H >> 4), H);
+    };
+    issue_gate(0);
+    issue_shared_up(0);
+#pragma unroll 1
+    for (int l = 0; l < a.L && alive; ++l) {
+        if (!mbar_wait_abortable(&c.pbar, l & 1, &c.abort_s)) {
+            set_cta_abort(c);
+            break;
+        }
+        if (l + 1 < a.L) issue_gate(l + 1);
+        const StackLayer& P = a.layer[l];
+        const int NU = c.plan.U * RI, ND = c.plan.U * RH;
+#pragma unroll 1
+        for (int i = share_begin32(NU, b, G), e = share_begin32(NU, b + 1, G); i < e; ++i) {
+            const int64_t row = (int64_t)c.plan.expert[i / RI] * I + 16 * (i % RI);
+            fill(P.up_codes + row * (H >> 1), P.up_scales + row * (H >> 4), H);
+        }
+#pragma unroll 1
+        for (int r = c.sd_b; r < c.sd_e; ++r)
+            fill(P.shd_codes + (size_t)16 * r * (S >> 1), P.shd_scales + (size_t)16 * r * (S >> 4), S);
+#pragma unroll 1
+        for (int i = share_begin32(ND, b, G), e = share_begin32(ND, b + 1, G); i < e; ++i) {
+            const int64_t row = (int64_t)c.plan.expert[i / RH] * H + 16 * (i % RH);
+            fill(P.down_codes + row * (I >> 1), P.down_scales + row * (I >> 4), I);
+        }
+        mbar_arrive(&c.qbar);  // the plan of layer l is no longer read here
+        if (l + 1 < a.L) issue_shared_up(l + 1);
+    }
+    if (!alive) atomicExch(abort_flag(a), 1);
+}
+
+// ---------------------------------------------------------------- consumers
+template <bool W4A4>
+__device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
+    const int ctid = threadIdx.x;
+    const int T = a.T, E = a.E, H = a.H, I = a.I, RI = I >> 4, RH = H >> 4;
+    const int G = c.G, b = c.b;
+    int base = 0;  // first ring item of the current step
+    bool bad = false;
+#pragma unroll 1
+    for (int l = 0; l < a.L; ++l) {
+        int* const cnt = layer_cnt(a, l);
+        // 1-2. the layer input, once every tile of it is final
+        if (l > 0) {
+            bool ok = true;
+            if (ctid == 0) ok = wait_geq(layer_cnt(a, l - 1) + kCntHDone, RH, abort_flag(a));
+            if (consumer_bar_or(!ok || cta_abort(c))) {
+                bad = true;
+                break;
+            }
+        }
+        st_input<W4A4>(a, c, l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H);
+        // 3. router logits
+        if (c.ng > 0 && !st_router(a, c, l)) {
+            bad = true;
+            break;
+        }
+        // 4. shared-expert up tiles
+        const int n_su = c.su_e - c.su_b;
+        if (!st_up_tiles<W4A4>(a, c, l, base, n_su, false, 0)) set_cta_abort(c);
+        base += n_su;
+        // 5. top-k and plan (once the producer has stopped reading the previous plan)
+        {
+            bool ok = true;
+            if (ctid == 0) ok = wait_geq(cnt + kCntLogits, E, abort_flag(a));
+            if (l > 0 && !mbar_wait_abortable(&c.qbar, static_cast<uint32_t>((l - 1) & 1), &c.abort_s)) ok = false;
+            if (consumer_bar_or(!ok || cta_abort(c))) {
+                bad = true;
+                break;
+            }
+        }
+        st_topk_plan(a, c, l);
+        if (ctid == 0) mbar_arrive(&c.pbar);  // the producer may stream the routed tiles now
+        // 6. routed up tiles
+        const int U = c.plan.U;
+        const int NU = U * RI, ND = U * RH;
+        const int ru_b = share_begin32(NU, b, G), ru_e = share_begin32(NU, b + 1, G);
+        const int rd_b = share_begin32(ND, b, G), rd_e = share_begin32(ND, b + 1, G);
+        if (!st_up_tiles<W4A4>(a, c, l, base, ru_e - ru_b, true, ru_b)) set_cta_abort(c);
+        base += ru_e - ru_b;
+        // 7. down operands
+        if (!st_down_operands<W4A4>(a, c, l, rd_b, rd_e)) {
+            bad = true;
+            break;
+        }
+        // 8. down tiles, counted per output tile; the last contribution combines it
+        if (!st_down_tiles<W4A4>(a, c, l, base, rd_b, rd_e - rd_b)) set_cta_abort(c);
+        base += (c.sd_e - c.sd_b) + (rd_e - rd_b);
+        if (consumer_bar_or(cta_abort(c))) {
+            bad = true;
+            break;
+        }
+    }
+    if (bad && ctid == 0) {
+        set_cta_abort(c);
+        atomicExch(abort_flag(a), 1);
+    }
+}
+
+template <bool W4A4>
+__global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant__ StackArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ StackCta c;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, b = blockIdx.x;
+
+    ring_init(c.ring, a.nst);
+    if (threadIdx.x == 0) {
+        mbar_init(&c.gbar, 1);
+        mbar_init(&c.pbar, 1);
+        mbar_init(&c.qbar, 1);
+        fence_mbar_init();
+        c.abort_s = 0;
+        c.gate_issued = 0;
+        c.G = G;
+        c.b = b;
+        c.nst = a.nst;
+        c.stage_bytes = a.stage_bytes;
+        c.ng = b < a.E ? (a.E - b + G - 1) / G : 0;
+        c.amax_stride = a.T * a.k + a.T;
+        const int RS = a.S >> 4, RH = a.H >> 4;
+        c.su_b = share_begin32(RS, b, G);
+        c.su_e = share_begin32(RS, b + 1, G);
+        c.sd_b = share_begin32(RH, b, G);
+        c.sd_e = share_begin32(RH, b + 1, G);
+        c.ring_base = smem;
+        c.gsm = reinterpret_cast<float*>(smem + a.off_gate);
+        c.X = reinterpret_cast<uint16_t*>(smem + a.off_uni);
+        c.xq = reinterpret_cast<__half*>(smem + a.off_uni + (size_t)a.T * a.H * 2);
+        c.bslot = reinterpret_cast<__half*>(smem + a.off_uni);
+        c.tk_c = reinterpret_cast<float*>(smem + a.off_tk);
+        c.tk_s = c.tk_c + (size_t)a.T * a.E;
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        if (lane == 0) st_producer(a, c);
+    } else {
+        st_consumers<W4A4>(a, c);
+    }
+
+    __syncthreads();
+    ring_drain(c.ring, c.nst);
+    if (threadIdx.x == 0 && c.gate_issued > 0 && !mbar_wait_bounded(&c.gbar, (c.gate_issued - 1) & 1))
+        set_dev_error(kErrWaitDrain);
+    // the last CTA to leave resets the counters and the row amax for the next call
+    if (threadIdx.x == 0) {
+        int* const cnt_exit = a.ws.cnt + (size_t)a.L * stack_cnt_per_layer(a.H);
+        __threadfence();
+        if (atomicAdd(cnt_exit, 1) == G - 1) {
+            for (int i = 0; i < a.L * stack_cnt_per_layer(a.H); ++i) a.ws.cnt[i] = 0;
+            for (int i = 0; i < 2 * (a.T * a.k + a.T); ++i) a.ws.amax[i] = 0u;
+            cnt_exit[1] = 0;
+            __threadfence();
+            *cnt_exit = 0;
+        }
+    }
+}
+
+}  // namespace nvfp4moe

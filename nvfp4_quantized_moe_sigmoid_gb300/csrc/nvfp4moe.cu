@@ -13,6 +13,7 @@
 #include "lm_head.cuh"
 #include "moe_decode.cuh"
 #include "moe_layer.cuh"
+#include "moe_stack.cuh"
 #include "quantize.cuh"
 #include "route.cuh"
 
@@ -181,7 +182,7 @@ nvfp4_status nvfp4_last_device_error(cudaStream_t stream) {
     if (v != 0) {
         const unsigned int zero = 0;
         if (cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return NVFP4_ERR_CUDA;
-        return (v & (kErrWaitFull | kErrWaitEmpty | kErrWaitDrain)) ? NVFP4_ERR_TIMEOUT
+        return (v & (kErrWaitFull | kErrWaitEmpty | kErrWaitDrain | kErrWaitPeer)) ? NVFP4_ERR_TIMEOUT
                                                                       : NVFP4_ERR_INVALID_ARG;
     }
     return NVFP4_OK;
@@ -581,4 +582,177 @@ extern "C" nvfp4_status moe_expert_forward_noalloc(const moe_layer_weights* w, c
     if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     return moe_expert_forward(w, hidden, topk_idx, topk_w, T, k, mode, rms_eps, residual, out, scratch,
                               need, stream);
+}
+
+// ------------------------------------------------ persistent layer stack
+namespace {
+
+struct StackWsOffsets {
+    size_t cnt, z, act, act_sh, amax, ypart, ysh, total;
+};
+
+StackWsOffsets stack_ws(int L, int T, int k, int E, int H, int I, int S) {
+    StackWsOffsets o{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    o.cnt = take(sizeof(int) * ((size_t)L * stack_cnt_per_layer(H) + 2));
+    o.amax = take(sizeof(unsigned int) * 2 * (size_t)(T * k + T));
+    o.z = take(sizeof(float) * (size_t)L * T * E);
+    o.act = take((size_t)T * k * I * 2);
+    o.act_sh = take((size_t)T * S * 2);
+    o.ypart = take((size_t)T * k * H * 4);
+    o.ysh = take((size_t)T * H * 4);
+    o.total = off;
+    return o;
+}
+
+// Dynamic shared memory of the stack kernel: the ring, then the router rows,
+// the operand union (layer input + up B / down B slots), the top-k scores.
+struct StackSmem {
+    int nst, stage_bytes, off_gate, off_uni, off_tk, total;
+};
+
+bool stack_smem(int lim, int E, int G, int T, int H, int I, int S, StackSmem* out) {
+    auto a128 = [](size_t x) { return static_cast<int>((x + 127) & ~size_t(127)); };
+    const int stage = 9 * std::max(std::max(H, I), S);
+    const int ng = (E + G - 1) / G;
+    const int gate = a128((size_t)ng * H * 4);
+    const int uni = a128(std::max((size_t)T * H * 4, ((size_t)2 * T * I + (size_t)T * S) * 2));
+    const int tk = a128((size_t)T * E * 8);
+    const int rest = gate + uni + tk;
+    const int nst = std::min(kMaxStages, (lim - rest) / stage);
+    if (nst < 2) return false;
+    out->nst = nst;
+    out->stage_bytes = stage;
+    out->off_gate = nst * stage;
+    out->off_uni = out->off_gate + gate;
+    out->off_tk = out->off_uni + uni;
+    out->total = out->off_tk + tk;
+    return true;
+}
+
+nvfp4_status check_stack(const moe_stack_layer* layers, int32_t L, int32_t T, int32_t k) {
+    if (!layers || L < 1 || T < 1 || k < 1) return NVFP4_ERR_INVALID_ARG;
+    if (L > NVFP4MOE_STACK_MAX_LAYERS || L > kStackMaxLayers) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const moe_layer_weights& w0 = layers[0].moe;
+    for (int l = 0; l < L; ++l) {
+        const moe_stack_layer& ly = layers[l];
+        const nvfp4_status st = check_layer(&ly.moe);
+        if (st != NVFP4_OK) return st;
+        if (ly.moe.num_experts != w0.num_experts || ly.moe.hidden != w0.hidden || ly.moe.inter != w0.inter ||
+            ly.moe.shared_inter != w0.shared_inter)
+            return NVFP4_ERR_INVALID_ARG;
+        if (!ly.router_w || !ly.router_bias) return NVFP4_ERR_INVALID_ARG;
+        if (!aligned(ly.router_w, 16) || !aligned(ly.router_bias, 4)) return NVFP4_ERR_MISALIGNED;
+    }
+    if (k > w0.num_experts) return NVFP4_ERR_INVALID_ARG;
+    if (T > kDecodeMaxT || k > kDecodeMaxK || w0.num_experts > 256 || w0.num_experts % 8) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" size_t moe_stack_forward_workspace_size(const moe_stack_layer* layers, int32_t L, int32_t T, int32_t k,
+                                                   nvfp4_act_mode mode) {
+    (void)mode;
+    if (check_stack(layers, L, T, k) != NVFP4_OK) return 0;
+    const moe_layer_weights& w = layers[0].moe;
+    return stack_ws(L, T, k, w.num_experts, w.hidden, w.inter, w.shared_inter).total;
+}
+
+extern "C" nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t L, const void* hidden_in, int32_t T,
+                                          int32_t k, nvfp4_act_mode mode, float rms_eps, void* hidden_out,
+                                          int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
+                                          cudaStream_t stream) {
+    nvfp4_status st = check_stack(layers, L, T, k);
+    if (st != NVFP4_OK) return st;
+    if (!hidden_in || !hidden_out || !topk_idx || !topk_w || !workspace) return NVFP4_ERR_INVALID_ARG;
+    if (mode != NVFP4_W4A16 && mode != NVFP4_W4A4) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(hidden_in, 16) || !aligned(hidden_out, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+        !aligned(workspace, 256))
+        return NVFP4_ERR_MISALIGNED;
+    const moe_layer_weights& w0 = layers[0].moe;
+    const int E = w0.num_experts, H = w0.hidden, I = w0.inter, S = w0.shared_inter;
+    {  // hidden_out must not overlap hidden_in
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(hidden_in), a1 = a0 + (size_t)T * H * 2;
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(hidden_out), b1 = b0 + (size_t)L * T * H * 2;
+        if (a0 < b1 && b0 < a1) return NVFP4_ERR_INVALID_ARG;
+    }
+    const StackWsOffsets o = stack_ws(L, T, k, E, H, I, S);
+    if (workspace_bytes < o.total) return NVFP4_ERR_WORKSPACE;
+    const bool w4a4 = mode == NVFP4_W4A4;
+    const void* kfn = w4a4 ? reinterpret_cast<const void*>(k_moe_stack<true>)
+                           : reinterpret_cast<const void*>(k_moe_stack<false>);
+    const int G = num_sms();
+    const int lim = dyn_smem_limit(kfn);
+    StackSmem sm{};
+    if (lim <= 0 || !stack_smem(lim, E, G, T, H, I, S, &sm)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kThreads, sm.total) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (per_sm < 1) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // one CTA per SM must fit for the cooperative grid
+
+    StackArgs a{};
+    for (int l = 0; l < L; ++l) {
+        const moe_stack_layer& ly = layers[l];
+        StackLayer& d = a.layer[l];
+        d.up_codes = ly.moe.up_codes;
+        d.up_scales = ly.moe.up_scales;
+        d.up_global = ly.moe.up_global;
+        d.down_codes = ly.moe.down_codes;
+        d.down_scales = ly.moe.down_scales;
+        d.down_global = ly.moe.down_global;
+        d.shu_codes = ly.moe.shared_up.codes;
+        d.shu_scales = ly.moe.shared_up.scales;
+        d.shu_global = ly.moe.shared_up.global_scale;
+        d.shd_codes = ly.moe.shared_down.codes;
+        d.shd_scales = ly.moe.shared_down.scales;
+        d.shd_global = ly.moe.shared_down.global_scale;
+        d.router_w = ly.router_w;
+        d.router_b = ly.router_bias;
+    }
+    a.L = L;
+    a.E = E;
+    a.H = H;
+    a.I = I;
+    a.S = S;
+    a.T = T;
+    a.k = k;
+    a.rms_eps = rms_eps;
+    a.hidden_in = static_cast<const uint16_t*>(hidden_in);
+    a.hidden_out = static_cast<uint16_t*>(hidden_out);
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    a.ws.cnt = reinterpret_cast<int*>(base + o.cnt);
+    a.ws.z = reinterpret_cast<float*>(base + o.z);
+    a.ws.act = reinterpret_cast<uint16_t*>(base + o.act);
+    a.ws.act_sh = reinterpret_cast<uint16_t*>(base + o.act_sh);
+    a.ws.amax = reinterpret_cast<unsigned int*>(base + o.amax);
+    a.ws.ypart = reinterpret_cast<float*>(base + o.ypart);
+    a.ws.ysh = reinterpret_cast<float*>(base + o.ysh);
+    a.nst = sm.nst;
+    a.stage_bytes = sm.stage_bytes;
+    a.off_gate = sm.off_gate;
+    a.off_uni = sm.off_uni;
+    a.off_tk = sm.off_tk;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sm.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = w4a4 ? cudaLaunchKernelEx(&cfg, k_moe_stack<true>, a)
+                               : cudaLaunchKernelEx(&cfg, k_moe_stack<false>, a);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    return launch_status();
 }

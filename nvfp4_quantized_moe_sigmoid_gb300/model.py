@@ -7,6 +7,9 @@ decode step that runs them through the C ABI:
 
 where norm is the unit-weight RMS norm each block of the pre-norm model
 applies to its input (fused into the kernels; rms_eps = 0 disables it).
+With 1..4 tokens all layers run as one moe_stack_forward call (path
+"stack"); "layer" runs one moe_layer_forward per layer and "split" the
+two calls above per layer.
 
 ("Let's optimize Nemotron 3.5 Lightning - a worklog": a decode step streams
 the active experts of every MoE layer and the lm_head; the chain keeps only
@@ -15,8 +18,9 @@ nvfp4_quantize from bf16 masters supplied by the caller.
 """
 import torch
 
-from . import (MoELayer, NVFP4Matrix, PER_TENSOR, W4A4, W4A16, lm_head_gemv, make_layer_workspace,
-               moe_expert_forward, moe_layer_forward, moe_route_topk, nvfp4_quantize)
+from . import (MoELayer, NVFP4Matrix, PER_TENSOR, W4A4, W4A16, _stack_layers, lm_head_gemv,
+               make_layer_workspace, make_stack_workspace, moe_expert_forward, moe_layer_forward,
+               moe_route_topk, moe_stack_forward, nvfp4_quantize)
 
 
 class MoEDecodeStack:
@@ -38,7 +42,10 @@ class MoEDecodeStack:
         self.topk_w = torch.zeros((layers, T, k), dtype=torch.float32, device=device)
         self.logits = torch.zeros((T, V), dtype=torch.float32, device=device) if V else None
         self.ws = None
+        self.stack_ws = None
+        self.c_layers = None
         self.graph = None
+        self.path = "stack" if T <= 4 else "split"
 
     # ------------------------------------------------------------ weights
     def register(self, fill_bf16, fill_router, fill_bias):
@@ -72,18 +79,19 @@ class MoEDecodeStack:
 
     def make_workspace(self):
         self.ws = make_layer_workspace(self.layers[0], self.T, self.k, self.mode)
-
-    @property
-    def fused(self):
-        """Layers run through moe_layer_forward (1..4 tokens); otherwise as
-        moe_route_topk + moe_expert_forward."""
-        return self.T <= 4 and getattr(self, "use_fused", True)
+        if self.T <= 4:
+            self.stack_ws = make_stack_workspace(self.layers, self.T, self.k, self.mode)
+            self.c_layers = _stack_layers(self.layers)
 
     # ------------------------------------------------------------ the step
     def step(self, stream=None):
         """One decode step on self.h[0] -> self.h[L] (and logits)."""
-        for l, Lw in enumerate(self.layers):
-            if self.fused:
+        if self.path == "stack":
+            moe_stack_forward(self.layers, self.h[0], self.k, self.mode, hidden_out=self.h[1:],
+                              topk_idx=self.topk_idx, topk_w=self.topk_w, workspace=self.stack_ws,
+                              rms_eps=self.rms_eps, stream=stream, c_layers=self.c_layers)
+        for l, Lw in enumerate(self.layers if self.path != "stack" else []):
+            if self.path == "layer":
                 moe_layer_forward(Lw, self.h[l], self.k, self.mode, residual=self.h[l], out=self.h[l + 1],
                                   topk_idx=self.topk_idx[l], topk_w=self.topk_w[l], workspace=self.ws,
                                   rms_eps=self.rms_eps, stream=stream)

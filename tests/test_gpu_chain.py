@@ -1,12 +1,14 @@
 """The full-depth decode step at the pages' sizes (23 W4A4 MoE layers +
 131072 x 2688 lm_head), in the launch configuration the benchmark times.
 
-Teacher forcing runs from the oracle to the GPU only: the oracle runs its own
-chain h_0 -> h_23; for every layer the GPU is given the oracle's h_l and must
+The per-layer calls are teacher-forced from the oracle to the GPU: the oracle
+runs its own chain h_0 -> h_23; for every layer the GPU is given its h_l and must
 reproduce the oracle's routing (bit-exact up to near-ties) and h_{l+1}
 (within tolerance); the lm_head is checked on the oracle's h_23 at sampled
-rows. The free-running GPU chain (CUDA graph, as timed) must reproduce layer 0
-bit-for-bit against the teacher-forced call and stay finite."""
+rows. The benchmark's own path (all layers in one moe_stack_forward call) is
+checked the other way round: the oracle is teacher-forced on the GPU's h_l.
+The free-running GPU chain (CUDA graph, as timed) must be deterministic and
+stay finite."""
 import numpy as np
 import pytest
 import torch
@@ -77,26 +79,50 @@ def test_chain_teacher_forced(nm, stack, cfg):
     assert_close(logits[:, rows], orc.lm_head(orc.Mat(cc, ss, g), hn), "logits")
 
 
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_stack_teacher_forced(nm, stack, cfg):
+    """The benchmark's path: all 23 layers in one moe_stack_forward call; the
+    oracle is teacher-forced on the GPU's own h_l of every layer."""
+    from tests.test_gpu_stack import teacher_forced
+    c0, st4 = stack
+    c = configs.shape(cfg)
+    T = c["T"]
+    h0 = gen.hidden_bf16(T, c["H"], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+    hd = to_dev_bf16(h0)
+    hout, idx, w = nm.moe_stack_forward(st4.layers, hd, c["K"], nm.W4A4, rms_eps=c["rms_eps"])
+    torch.cuda.synchronize()
+    assert nm.nvfp4_last_device_error() == 0
+    OLs = [OracleLayer(c["seed"], l, c["H"], c["I"], c["S"], c["E"], c["bias"]) for l in range(c["layers"])]
+    assert teacher_forced(nm, OLs, h0, hout, idx, w, c["K"], True, c["rms_eps"]) <= 1
+
+
 def test_free_running_graph(nm, stack):
+    """The timed step (CUDA graph: stack kernel + lm_head) is deterministic,
+    equals a direct moe_stack_forward call bit for bit, and its first layer
+    agrees with the per-layer call within tolerance."""
     from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
     c0, st4 = stack
     c = configs.shape(1)
     st = MoEDecodeStack(c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], 1, w4a4=True, V=c["V"],
                         weights_from=st4, rms_eps=c["rms_eps"])
     st.make_workspace()
+    assert st.path == "stack"
     h0 = gen.hidden_bf16(1, c["H"], c["seed"], layer=configs.HIDDEN_LAYER)
     st.h[0].copy_(to_dev_bf16(h0))
     st.capture()
     st.replay()
     torch.cuda.synchronize()
-    first = st.h[1].clone()
+    first = st.h[1:].clone()
     st.replay()
     torch.cuda.synchronize()
-    assert torch.equal(first.view(torch.int16), st.h[1].view(torch.int16)), "replay not deterministic"
+    assert torch.equal(first.view(torch.int16), st.h[1:].view(torch.int16)), "replay not deterministic"
     assert torch.isfinite(st.logits).all()
     hd = to_dev_bf16(h0)
+    hout, _, _ = nm.moe_stack_forward(st.layers, hd, c["K"], nm.W4A4, rms_eps=c["rms_eps"])
+    torch.cuda.synchronize()
+    assert torch.equal(hout.view(torch.int16), first.view(torch.int16))
     out, _, _ = nm.moe_layer_forward(st.layers[0], hd, c["K"], nm.W4A4, residual=hd, workspace=st.ws,
                                      rms_eps=c["rms_eps"])
     torch.cuda.synchronize()
-    assert torch.equal(out.view(torch.int16), first.view(torch.int16))
+    assert_close(bf16_to_f64(bf16_bits(out)), bf16_to_f64(bf16_bits(first[0])), "layer 0: layer call vs stack")
     assert nm.nvfp4_last_device_error() == 0
