@@ -182,7 +182,7 @@ nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace
  *   hidden     device bf16 [T][H], 16-byte aligned
  *   topk_idx   device int32 [T][k], entries in [0, E) and distinct per token
  *   topk_w     device float [T][k]
- *   T >= 1, 1 <= k <= min(E, 16)
+ *   T >= 1, 1 <= k <= E (k <= 16 for T <= 4), E <= 256
  *   rms_eps    > 0: normalise each hidden row first; <= 0: use it as is
  *   residual   device bf16 [T][H] or NULL
  *   out        device bf16 [T][H]; may alias residual, must not alias hidden
@@ -192,11 +192,36 @@ nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace
  *              moe_expert_forward_workspace_init; calls that share a
  *              workspace must not overlap in time
  */
+/* Paths: T <= 4 streams the weight tiles of the step's unique experts through
+ * persistent GEMV kernels (batch-1 decode and the 4-token verify, [worklog]
+ * Interlude and Step 5); T > 4 groups the (token, choice) pairs by expert
+ * (moe_permute) and runs the experts as one ragged grouped GEMM ([worklog]
+ * Step 3). Both compute the same arithmetic; their FP32 summation orders
+ * differ. */
 nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
                                 const int32_t* topk_idx, const float* topk_w, int32_t T,
                                 int32_t k, nvfp4_act_mode mode, float rms_eps, const void* residual,
                                 void* out, void* workspace, size_t workspace_bytes,
                                 cudaStream_t stream);
+
+/*
+ * moe_permute - the token permutation of the grouped expert path ([worklog]
+ * Step 3: the routed experts as a grouped GEMM over the tokens routed to
+ * them). The T*k (token, choice) pairs p = t*k + j are grouped by expert
+ * e = topk_idx[p], keeping pair order inside each expert:
+ *   offsets[e] = number of pairs routed to experts < e   (offsets[E] = T*k)
+ *   perm[pos]  = the pair at position pos                (position order)
+ *   inv[p]     = the position of pair p                  (perm[inv[p]] == p)
+ *   tile_offsets (optional, may be NULL): tile_offsets[e] = sum over experts
+ *              < e of ceil(count / 64), the first 64-position tile of e.
+ *   topk_idx   device int32 [T][k], entries in [0, E) (an entry outside is
+ *              counted as expert 0 and reported by nvfp4_last_device_error)
+ *   offsets    device int32 [E+1]; perm, inv: device int32 [T*k];
+ *              tile_offsets: device int32 [E+1] or NULL
+ *   1 <= k <= E <= 256 (NVFP4_ERR_UNSUPPORTED_SHAPE above 256)
+ */
+nvfp4_status moe_permute(const int32_t* topk_idx, int32_t T, int32_t k, int32_t E, int32_t* offsets,
+                         int32_t* perm, int32_t* inv, int32_t* tile_offsets, cudaStream_t stream);
 
 /*
  * moe_layer_forward - one whole MoE layer for 1..4 tokens in one call:

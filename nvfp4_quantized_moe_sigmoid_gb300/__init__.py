@@ -17,7 +17,7 @@ __all__ = ["NVFP4Matrix", "MoELayer", "NVFP4Error", "nvfp4_quantize", "moe_route
            "moe_expert_forward_workspace_size", "moe_expert_forward_workspace_init",
            "moe_expert_forward", "moe_expert_forward_noalloc", "moe_layer_forward",
            "moe_layer_forward_workspace_size", "moe_stack_forward", "moe_stack_forward_workspace_size",
-           "make_stack_workspace", "lm_head_gemv",
+           "make_stack_workspace", "moe_permute", "lm_head_gemv",
            "nvfp4_status_string", "nvfp4_last_device_error",
            "W4A16", "W4A4", "PER_TENSOR", "PER_ROW", "GIVEN", "lib"]
 
@@ -258,6 +258,22 @@ def moe_stack_forward(layers, hidden, k, mode=W4A4, hidden_out=None, topk_idx=No
                               _ptr(topk_idx), _ptr(topk_w), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "moe_stack_forward")
     return hidden_out, topk_idx, topk_w
+
+
+def moe_permute(topk_idx, num_experts, with_tiles=False, stream=None):
+    """Pairs (t, j) grouped by expert, stable: returns (offsets [E+1],
+    perm [T*k], inv [T*k]) and, with with_tiles, the 64-position tile
+    offsets [E+1]."""
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    tiles = torch.empty(num_experts + 1, dtype=torch.int32, device=dev) if with_tiles else None
+    st = _L.moe_permute(_ptr(topk_idx.contiguous()), T, k, num_experts, _ptr(offsets), _ptr(perm), _ptr(inv),
+                        _ptr(tiles), _stream(stream))
+    _check(st, "moe_permute")
+    return (offsets, perm, inv, tiles) if with_tiles else (offsets, perm, inv)
 
 
 def moe_expert_forward_noalloc(layer: MoELayer, hidden, topk_idx, topk_w, mode=W4A4, residual=None,

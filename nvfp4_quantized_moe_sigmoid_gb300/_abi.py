@@ -12,7 +12,7 @@ I32, I64 = ctypes.c_int32, ctypes.c_int64
 EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_size",
            "moe_expert_forward_workspace_init", "moe_expert_forward", "moe_expert_forward_noalloc",
            "moe_layer_forward", "moe_layer_forward_workspace_size",
-           "moe_stack_forward", "moe_stack_forward_workspace_size",
+           "moe_stack_forward", "moe_stack_forward_workspace_size", "moe_permute",
            "lm_head_gemv",
            "nvfp4_status_string", "nvfp4_last_device_error"]
 
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
     L.moe_stack_forward.argtypes = [ctypes.POINTER(MoeStackLayer), I32, P, I32, I32, ctypes.c_int, ctypes.c_float,
                                     P, P, P, P, ctypes.c_size_t, P]
     L.moe_stack_forward.restype = ctypes.c_int
+    L.moe_permute.argtypes = [P, I32, I32, I32, P, P, P, P, P]
+    L.moe_permute.restype = ctypes.c_int
     L.moe_expert_forward_noalloc.argtypes = [ctypes.POINTER(MoeLayerWeights), P, P, P, I32, I32,
                                              ctypes.c_int, ctypes.c_float, P, P, P]
     L.moe_expert_forward_noalloc.restype = ctypes.c_int

@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "lm_head.cuh"
 #include "moe_decode.cuh"
+#include "moe_grouped.cuh"
 #include "moe_layer.cuh"
 #include "moe_stack.cuh"
 #include "quantize.cuh"
@@ -130,6 +131,12 @@ DecodeWs decode_ws(int T, int k, int H, int I, int S) {
     w.total = off;
     return w;
 }
+
+// The grouped path (T > 4, moe_grouped.cuh), defined below.
+size_t grouped_ws_total(int T, int k, int E, int H, int I, int S);
+nvfp4_status grouped_forward(const moe_layer_weights* w, const void* hidden, const int32_t* topk_idx,
+                             const float* topk_w, int T, int k, bool w4a4, float rms_eps, const void* residual,
+                             void* out, uint8_t* ws, cudaStream_t stream);
 
 bool decode_path(const moe_layer_weights* w, int T, int k) {
     return T >= 1 && T <= kDecodeMaxT && k <= kDecodeMaxK && w->num_experts <= 256;
@@ -251,7 +258,8 @@ size_t moe_expert_forward_workspace_size(const moe_layer_weights* w, int32_t T, 
                                          nvfp4_act_mode mode) {
     (void)mode;
     if (!w || T < 1 || k < 1) return 0;
-    return decode_ws(T, k, w->hidden, w->inter, w->shared_inter).total;
+    if (decode_path(w, T, k)) return decode_ws(T, k, w->hidden, w->inter, w->shared_inter).total;
+    return grouped_ws_total(T, k, w->num_experts, w->hidden, w->inter, w->shared_inter);
 }
 
 nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace_bytes,
@@ -273,7 +281,14 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
         (residual && !aligned(residual, 4)))
         return NVFP4_ERR_MISALIGNED;
     if (hidden == out && residual != hidden) return NVFP4_ERR_INVALID_ARG;
-    if (!decode_path(w, T, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!decode_path(w, T, k)) {
+        // more than 4 tokens: grouped GEMM over the tokens each expert received
+        if (w->num_experts > 256) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        if (workspace_bytes < grouped_ws_total(T, k, w->num_experts, w->hidden, w->inter, w->shared_inter))
+            return NVFP4_ERR_WORKSPACE;
+        return grouped_forward(w, hidden, topk_idx, topk_w, T, k, mode == NVFP4_W4A4, rms_eps, residual, out,
+                               static_cast<uint8_t*>(workspace), stream);
+    }
 
     const int H = w->hidden, I = w->inter, S = w->shared_inter;
     const DecodeWs ws = decode_ws(T, k, H, I, S);
@@ -386,6 +401,171 @@ nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, 
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ grouped path (T > 4)
+namespace {
+
+struct GroupedWsOffsets {
+    size_t offsets, tiles, perm, inv, xq, gx, act, amax, act_sh, amax_sh, aq, ga, aq_sh, gsh, ypart, ysh, total;
+};
+
+GroupedWsOffsets grouped_ws(int T, int k, int E, int H, int I, int S) {
+    GroupedWsOffsets o{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    const size_t P = (size_t)T * k;
+    o.offsets = take(4 * (size_t)(E + 1));
+    o.tiles = take(4 * (size_t)(E + 1));
+    o.perm = take(4 * P);
+    o.inv = take(4 * P);
+    o.amax = take(4 * P);
+    o.amax_sh = take(4 * (size_t)T);
+    o.xq = take(2 * (size_t)T * H);
+    o.gx = take(4 * (size_t)T);
+    o.act = take(2 * P * I);
+    o.act_sh = take(2 * (size_t)T * S);
+    o.aq = take(2 * P * I);
+    o.ga = take(4 * P);
+    o.aq_sh = take(2 * (size_t)T * S);
+    o.gsh = take(4 * (size_t)T);
+    o.ypart = take(4 * P * H);
+    o.ysh = take(4 * (size_t)T * H);
+    o.total = off;
+    return o;
+}
+
+size_t grouped_ws_total(int T, int k, int E, int H, int I, int S) { return grouped_ws(T, k, E, H, I, S).total; }
+
+template <typename Kernel>
+nvfp4_status launch_plain(Kernel kernel, int grid, int block, size_t smem, cudaStream_t stream,
+                          const GroupedArgs& ga) {
+    kernel<<<grid, block, smem, stream>>>(ga);
+    return launch_status();
+}
+
+nvfp4_status grouped_forward(const moe_layer_weights* w, const void* hidden, const int32_t* topk_idx,
+                             const float* topk_w, int T, int k, bool w4a4, float rms_eps, const void* residual,
+                             void* out, uint8_t* ws, cudaStream_t stream) {
+    const int E = w->num_experts, H = w->hidden, I = w->inter, S = w->shared_inter;
+    const int P = T * k;
+    const GroupedWsOffsets o = grouped_ws(T, k, E, H, I, S);
+    auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+    auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    auto h16 = [&](size_t off) { return reinterpret_cast<__half*>(ws + off); };
+    auto b16 = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
+    auto u32 = [&](size_t off) { return reinterpret_cast<unsigned int*>(ws + off); };
+
+    // a7: pairs grouped by expert
+    k_permute<<<1, kPermThreads, 0, stream>>>(topk_idx, P, E, i32(o.offsets), i32(o.tiles), i32(o.perm),
+                                              i32(o.inv));
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    // amax words start at zero (amax and amax_sh are adjacent)
+    if (cudaMemsetAsync(ws + o.amax, 0, o.xq - o.amax, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    // a1: token rows (normalised when rms_eps > 0) -> B operand
+    if (w4a4) k_prep_rows<true><<<T, kGThreads, (size_t)H * 2, stream>>>(
+        static_cast<const uint16_t*>(hidden), H, T, rms_eps, nullptr, h16(o.xq), f32(o.gx));
+    else k_prep_rows<false><<<T, kGThreads, (size_t)H * 2, stream>>>(
+        static_cast<const uint16_t*>(hidden), H, T, rms_eps, nullptr, h16(o.xq), f32(o.gx));
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+
+    const size_t gsmem = (size_t)kGStages * kGStageBytes;
+    GroupedArgs ga{};
+    ga.E = E;
+    ga.T = T;
+    ga.k = k;
+    ga.offsets = i32(o.offsets);
+    ga.tiles = i32(o.tiles);
+    ga.perm = i32(o.perm);
+    ga.topk_w = topk_w;
+    // a3 + a5 (up): routed over the grouped token rows, shared over all tokens
+    ga.codes = w->up_codes;
+    ga.scales = w->up_scales;
+    ga.global = w->up_global;
+    ga.sh_codes = w->shared_up.codes;
+    ga.sh_scales = w->shared_up.scales;
+    ga.sh_global = w->shared_up.global_scale;
+    ga.M = I;
+    ga.K = H;
+    ga.MS = S;
+    ga.KS = H;
+    ga.b_routed = h16(o.xq);
+    ga.g_routed = f32(o.gx);
+    ga.b_shared = h16(o.xq);
+    ga.g_shared = f32(o.gx);
+    ga.act = b16(o.act);
+    ga.act_sh = b16(o.act_sh);
+    ga.amax = u32(o.amax);
+    ga.amax_sh = u32(o.amax_sh);
+    const int ggrid = num_sms() * 3;
+    nvfp4_status st;
+    if (w4a4) {
+        if (dyn_smem_limit(k_grouped<true, kGroupedUp>) < (int)gsmem) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        st = launch_plain(k_grouped<true, kGroupedUp>, ggrid, kGThreads, gsmem, stream, ga);
+    } else {
+        if (dyn_smem_limit(k_grouped<false, kGroupedUp>) < (int)gsmem) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        st = launch_plain(k_grouped<false, kGroupedUp>, ggrid, kGThreads, gsmem, stream, ga);
+    }
+    if (st != NVFP4_OK) return st;
+    // a1 on the intermediate rows (row amax from the up epilogue)
+    if (w4a4) {
+        k_prep_rows<true><<<P, kGThreads, (size_t)I * 2, stream>>>(b16(o.act), I, P, 0.0f, u32(o.amax), h16(o.aq),
+                                                                    f32(o.ga));
+        k_prep_rows<true><<<T, kGThreads, (size_t)S * 2, stream>>>(b16(o.act_sh), S, T, 0.0f, u32(o.amax_sh),
+                                                                    h16(o.aq_sh), f32(o.gsh));
+    } else {
+        k_prep_rows<false><<<P, kGThreads, (size_t)I * 2, stream>>>(b16(o.act), I, P, 0.0f, nullptr, h16(o.aq),
+                                                                     f32(o.ga));
+        k_prep_rows<false><<<T, kGThreads, (size_t)S * 2, stream>>>(b16(o.act_sh), S, T, 0.0f, nullptr,
+                                                                     h16(o.aq_sh), f32(o.gsh));
+    }
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    // a4 + a5 (down): gate-weighted partial rows per position, shared rows per token
+    ga.codes = w->down_codes;
+    ga.scales = w->down_scales;
+    ga.global = w->down_global;
+    ga.sh_codes = w->shared_down.codes;
+    ga.sh_scales = w->shared_down.scales;
+    ga.sh_global = w->shared_down.global_scale;
+    ga.M = H;
+    ga.K = I;
+    ga.MS = H;
+    ga.KS = S;
+    ga.b_routed = h16(o.aq);
+    ga.g_routed = f32(o.ga);
+    ga.b_shared = h16(o.aq_sh);
+    ga.g_shared = f32(o.gsh);
+    ga.ypart = f32(o.ypart);
+    ga.ysh = f32(o.ysh);
+    if (w4a4) {
+        if (dyn_smem_limit(k_grouped<true, kGroupedDown>) < (int)gsmem) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        st = launch_plain(k_grouped<true, kGroupedDown>, ggrid, kGThreads, gsmem, stream, ga);
+    } else {
+        if (dyn_smem_limit(k_grouped<false, kGroupedDown>) < (int)gsmem) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        st = launch_plain(k_grouped<false, kGroupedDown>, ggrid, kGThreads, gsmem, stream, ga);
+    }
+    if (st != NVFP4_OK) return st;
+    // a6: combine + residual
+    const int n4 = T * (H / 4);
+    const int cgrid = std::min((n4 + 255) / 256, num_sms() * 8);
+    k_combine<<<cgrid, 256, 0, stream>>>(f32(o.ysh), f32(o.ypart), i32(o.inv), static_cast<const uint16_t*>(residual),
+                                         static_cast<uint16_t*>(out), T, H, k);
+    return launch_status();
+}
+
+}  // namespace
+
+extern "C" nvfp4_status moe_permute(const int32_t* topk_idx, int32_t T, int32_t k, int32_t E, int32_t* offsets,
+                                    int32_t* perm, int32_t* inv, int32_t* tile_offsets, cudaStream_t stream) {
+    if (!topk_idx || !offsets || !perm || !inv) return NVFP4_ERR_INVALID_ARG;
+    if (T < 1 || k < 1 || E < 1 || k > E) return NVFP4_ERR_INVALID_ARG;
+    if (E > 256 || (int64_t)T * k > (int64_t)1 << 28) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    k_permute<<<1, kPermThreads, 0, stream>>>(topk_idx, T * k, E, offsets, tile_offsets, perm, inv);
+    return launch_status();
+}
 
 // ------------------------------------------------------------ fused layer
 namespace {
