@@ -224,6 +224,19 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def launches_per_step(st, T, L, lm_head):
+    """Kernels of the library one step launches (memsets not counted)."""
+    if st.path == "stack":
+        n = 1
+    elif T <= 4:
+        n = 3 * L  # router, up, down
+    else:
+        n = 8 * L  # router, permute, token rows, up, 2 x intermediate rows, down, combine
+    if lm_head:
+        n += (T + 7) // 8 if T <= 8 else 2
+    return n
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args, ws, rank, local):
     import torch
@@ -293,7 +306,7 @@ def run_ours(args, ws, rank, local):
                 evs[2 * l + 1].record(stream)
         if c["lm_head"]:
             evs[2 * L].record(stream)
-            nm.lm_head_gemv(st.lm, st.h[L], st.logits, rms_eps=st.rms_eps)
+            nm.lm_head_forward(st.lm, st.h[L], st.logits, workspace=st.lm_ws, rms_eps=st.rms_eps)
             evs[2 * L + 1].record(stream)
         torch.cuda.synchronize()
         if rep > 0:
@@ -374,7 +387,7 @@ def run_ours(args, ws, rank, local):
                 "step_frac_of_8tbs": gbs_step / NOMINAL_HBM_GBS, "step_bytes": step_b,
                 "unique_experts_per_layer": uniques,
                 "roofline": roof, "cpu_baseline": cpu, "clocks": clk.summary(), "e2e": e2e,
-                "gpu_launches": args.steps * ((1 if st.path == "stack" else 3 * L) + (1 if c["lm_head"] else 0)),
+                "gpu_launches": args.steps * launches_per_step(st, T, L, c["lm_head"]),
                 **extra}
         print(json.dumps(line), flush=True)
 

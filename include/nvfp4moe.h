@@ -342,6 +342,22 @@ nvfp4_status moe_expert_forward_noalloc(const moe_layer_weights* w, const void* 
 nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, float rms_eps,
                           float* logits, cudaStream_t stream);
 
+/*
+ * lm_head_forward - lm_head_gemv's computation for any token count, with a
+ * workspace: up to 8 tokens it is lm_head_gemv; above, the hidden rows are
+ * prepared once (RMS norm when rms_eps > 0, exact f16) and the head runs as
+ * a dense GEMM over 64-token tiles (the 256-sequence concurrent decode of
+ * the [card-w4a4] serving numbers), reading each weight tile once per 64
+ * tokens instead of once per 8.
+ *   w, hidden, T, rms_eps, logits: as lm_head_gemv; for T > 8 also
+ *              V % 64 == 0 and logits 16-byte aligned
+ *   workspace  device, >= lm_head_forward_workspace_size(w, T) bytes,
+ *              256-byte aligned (unused for T <= 8)
+ */
+size_t lm_head_forward_workspace_size(const nvfp4_matrix* w, int32_t T);
+nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidden, int32_t T, float rms_eps, float* logits,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* nvfp4_status_string(nvfp4_status status);
 

@@ -17,7 +17,8 @@ __all__ = ["NVFP4Matrix", "MoELayer", "NVFP4Error", "nvfp4_quantize", "moe_route
            "moe_expert_forward_workspace_size", "moe_expert_forward_workspace_init",
            "moe_expert_forward", "moe_expert_forward_noalloc", "moe_layer_forward",
            "moe_layer_forward_workspace_size", "moe_stack_forward", "moe_stack_forward_workspace_size",
-           "make_stack_workspace", "moe_permute", "lm_head_gemv",
+           "make_stack_workspace", "moe_permute", "lm_head_gemv", "lm_head_forward",
+           "make_lm_head_workspace",
            "nvfp4_status_string", "nvfp4_last_device_error",
            "W4A16", "W4A4", "PER_TENSOR", "PER_ROW", "GIVEN", "lib"]
 
@@ -299,4 +300,23 @@ def lm_head_gemv(w: NVFP4Matrix, hidden, logits=None, rms_eps=0.0, stream=None):
     m = w.c()
     st = _L.lm_head_gemv(ctypes.byref(m), _ptr(hidden), T, float(rms_eps), _ptr(logits), _stream(stream))
     _check(st, "lm_head_gemv")
+    return logits
+
+
+def make_lm_head_workspace(w: NVFP4Matrix, T):
+    n = int(_L.lm_head_forward_workspace_size(ctypes.byref(w.c()), T))
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=w.codes.device)
+
+
+def lm_head_forward(w: NVFP4Matrix, hidden, logits=None, workspace=None, rms_eps=0.0, stream=None):
+    """lm_head_gemv for any token count (dense GEMM above 8 tokens)."""
+    T = hidden.shape[0]
+    if logits is None:
+        logits = torch.empty((T, w.n), dtype=torch.float32, device=hidden.device)
+    if workspace is None:
+        workspace = make_lm_head_workspace(w, T)
+    m = w.c()
+    st = _L.lm_head_forward(ctypes.byref(m), _ptr(hidden), T, float(rms_eps), _ptr(logits), _ptr(workspace),
+                            workspace.numel(), _stream(stream))
+    _check(st, "lm_head_forward")
     return logits

@@ -13,7 +13,7 @@ EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_siz
            "moe_expert_forward_workspace_init", "moe_expert_forward", "moe_expert_forward_noalloc",
            "moe_layer_forward", "moe_layer_forward_workspace_size",
            "moe_stack_forward", "moe_stack_forward_workspace_size", "moe_permute",
-           "lm_head_gemv",
+           "lm_head_gemv", "lm_head_forward", "lm_head_forward_workspace_size",
            "nvfp4_status_string", "nvfp4_last_device_error"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20  # NVFP4MOE_NOALLOC_SCRATCH_BYTES
@@ -79,6 +79,10 @@ def load(path: str = LIB_PATH):
     L.moe_expert_forward_noalloc.restype = ctypes.c_int
     L.lm_head_gemv.argtypes = [ctypes.POINTER(NVFP4Matrix), P, I32, ctypes.c_float, P, P]
     L.lm_head_gemv.restype = ctypes.c_int
+    L.lm_head_forward_workspace_size.argtypes = [ctypes.POINTER(NVFP4Matrix), I32]
+    L.lm_head_forward_workspace_size.restype = ctypes.c_size_t
+    L.lm_head_forward.argtypes = [ctypes.POINTER(NVFP4Matrix), P, I32, ctypes.c_float, P, P, ctypes.c_size_t, P]
+    L.lm_head_forward.restype = ctypes.c_int
     L.nvfp4_status_string.argtypes = [ctypes.c_int]
     L.nvfp4_status_string.restype = ctypes.c_char_p
     L.nvfp4_last_device_error.argtypes = [P]

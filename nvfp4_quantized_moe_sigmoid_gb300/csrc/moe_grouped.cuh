@@ -239,24 +239,29 @@ __global__ void __launch_bounds__(kGThreads) k_grouped(const GroupedArgs a) {
 
     for (int item = blockIdx.x; item < total; item += gridDim.x) {
         // ---- what this tile is
+        // Items are m-major inside each group (an expert's tiles, then the
+        // shared expert's): the n-tiles that share a weight tile run on
+        // neighbouring CTAs at about the same time and meet it in L2.
         bool routed = item < routed_items;
         int e = 0, m0, pos0, npos;
         if (routed) {
-            const int nt = item / MT;
-            m0 = (item % MT) * kGTile;
-            int lo = 0, hi = a.E;  // largest e with tiles[e] <= nt
+            int lo = 0, hi = a.E;  // largest e with tiles[e] * MT <= item
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
-                if (__ldg(a.tiles + mid) <= nt) lo = mid;
+                if (__ldg(a.tiles + mid) * MT <= item) lo = mid;
                 else hi = mid;
             }
             e = lo;
-            pos0 = __ldg(a.offsets + e) + (nt - __ldg(a.tiles + e)) * kGTile;
+            const int t0 = __ldg(a.tiles + e), nte = __ldg(a.tiles + e + 1) - t0;
+            const int local = item - t0 * MT;
+            m0 = (local / nte) * kGTile;
+            pos0 = __ldg(a.offsets + e) + (local % nte) * kGTile;
             npos = min(kGTile, __ldg(a.offsets + e + 1) - pos0);
         } else {
             const int i = item - routed_items;
-            m0 = (i % MTS) * kGTile;
-            pos0 = (i / MTS) * kGTile;
+            const int nts = (a.T + kGTile - 1) / kGTile;
+            m0 = (i / nts) * kGTile;
+            pos0 = (i % nts) * kGTile;
             npos = min(kGTile, a.T - pos0);
         }
         __syncthreads();  // previous tile's users of brow / posv are done

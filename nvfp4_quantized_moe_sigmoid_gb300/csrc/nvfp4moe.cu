@@ -936,3 +936,73 @@ extern "C" nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     return launch_status();
 }
+
+// ------------------------------------------------ lm_head with a workspace
+// Up to kLmMaxT tokens the GEMV kernel; above, the grouped GEMM kernel as one
+// dense group (all tokens, 64-token tiles, each weight tile read once per
+// 64 tokens and shared through L2 by the CTAs of one row tile).
+namespace {
+
+struct LmWsOffsets {
+    size_t zero, xq, total;
+};
+
+LmWsOffsets lm_ws(int T, int H) {
+    LmWsOffsets o{};
+    size_t off = 0;
+    o.zero = off;
+    off += 256;
+    o.xq = off;
+    off += align256((size_t)T * H * 2);
+    o.total = off;
+    return o;
+}
+
+}  // namespace
+
+extern "C" size_t lm_head_forward_workspace_size(const nvfp4_matrix* w, int32_t T) {
+    if (!w || T < 1 || w->k < 64) return 0;
+    if (T <= kLmMaxT) return 256;
+    return lm_ws(T, static_cast<int>(w->k)).total;
+}
+
+extern "C" nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidden, int32_t T, float rms_eps,
+                                        float* logits, void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream) {
+    if (!w || !hidden || !logits || T < 1) return NVFP4_ERR_INVALID_ARG;
+    if (T <= kLmMaxT) return lm_head_gemv(w, hidden, T, rms_eps, logits, stream);
+    if (!workspace) return NVFP4_ERR_INVALID_ARG;
+    if (!w->codes || !w->scales || !w->global_scale || w->n < 64 || w->k < 64) return NVFP4_ERR_INVALID_ARG;
+    if (w->n % 64 || w->k % 64 || w->k > (1 << 20) || w->n > (1 << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(w->codes, 16) || !aligned(w->scales, 16) || !aligned(hidden, 16) || !aligned(logits, 16) ||
+        !aligned(workspace, 256))
+        return NVFP4_ERR_MISALIGNED;
+    const int H = static_cast<int>(w->k);
+    const LmWsOffsets o = lm_ws(T, H);
+    if (workspace_bytes < o.total) return NVFP4_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    // no routed group: its tile count reads as 0
+    if (cudaMemsetAsync(ws + o.zero, 0, 4, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    __half* xq = reinterpret_cast<__half*>(ws + o.xq);
+    k_prep_rows<false><<<T, kGThreads, (size_t)H * 2, stream>>>(static_cast<const uint16_t*>(hidden), H, T, rms_eps,
+                                                                 nullptr, xq, nullptr);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    GroupedArgs ga{};
+    ga.E = 0;
+    ga.M = 0;
+    ga.K = H;
+    ga.tiles = reinterpret_cast<const int32_t*>(ws + o.zero);
+    ga.sh_codes = w->codes;
+    ga.sh_scales = w->scales;
+    ga.sh_global = w->global_scale;
+    ga.MS = static_cast<int>(w->n);
+    ga.KS = H;
+    ga.T = T;
+    ga.k = 1;
+    ga.b_shared = xq;
+    ga.ysh = logits;
+    const size_t gsmem = (size_t)kGStages * kGStageBytes;
+    if (dyn_smem_limit(k_grouped<false, kGroupedDown>) < (int)gsmem) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    k_grouped<false, kGroupedDown><<<num_sms() * 3, kGThreads, gsmem, stream>>>(ga);
+    return launch_status();
+}

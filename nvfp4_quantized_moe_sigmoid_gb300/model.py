@@ -3,7 +3,7 @@ decode step that runs them through the C ABI:
 
     for each layer l:  idx, w = moe_route_topk(norm(h_l))
                        h_{l+1} = h_l + moe_expert_forward(norm(h_l), idx, w)
-    logits = lm_head_gemv(norm(h_L))
+    logits = lm_head_forward(norm(h_L))   (lm_head_gemv up to 8 tokens)
 
 where norm is the unit-weight RMS norm each block of the pre-norm model
 applies to its input (fused into the kernels; rms_eps = 0 disables it).
@@ -18,9 +18,9 @@ nvfp4_quantize from bf16 masters supplied by the caller.
 """
 import torch
 
-from . import (MoELayer, NVFP4Matrix, PER_TENSOR, W4A4, W4A16, _stack_layers, lm_head_gemv,
-               make_layer_workspace, make_stack_workspace, moe_expert_forward, moe_layer_forward,
-               moe_route_topk, moe_stack_forward, nvfp4_quantize)
+from . import (MoELayer, NVFP4Matrix, PER_TENSOR, W4A4, W4A16, _stack_layers, lm_head_forward,
+               make_layer_workspace, make_lm_head_workspace, make_stack_workspace, moe_expert_forward,
+               moe_layer_forward, moe_route_topk, moe_stack_forward, nvfp4_quantize)
 
 
 class MoEDecodeStack:
@@ -79,6 +79,8 @@ class MoEDecodeStack:
 
     def make_workspace(self):
         self.ws = make_layer_workspace(self.layers[0], self.T, self.k, self.mode)
+        if self.lm is not None:
+            self.lm_ws = make_lm_head_workspace(self.lm, self.T)
         if self.T <= 4:
             self.stack_ws = make_stack_workspace(self.layers, self.T, self.k, self.mode)
             self.c_layers = _stack_layers(self.layers)
@@ -102,7 +104,8 @@ class MoEDecodeStack:
                                residual=self.h[l], out=self.h[l + 1], workspace=self.ws,
                                rms_eps=self.rms_eps, stream=stream)
         if self.lm is not None:
-            lm_head_gemv(self.lm, self.h[self.L], self.logits, rms_eps=self.rms_eps, stream=stream)
+            lm_head_forward(self.lm, self.h[self.L], self.logits, workspace=self.lm_ws, rms_eps=self.rms_eps,
+                            stream=stream)
 
     def capture(self):
         """Capture one step in a CUDA graph (after one eager step)."""
