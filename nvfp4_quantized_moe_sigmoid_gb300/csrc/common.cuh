@@ -74,13 +74,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase
+// completes (or the hint, in ns, runs out) instead of spinning, so waiting
+// warps leave the issue slots to the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity), "r"(100000u)
+        : "memory");
+    return ok != 0;
+}
 // Wait until phase `parity` of the barrier has completed; false after 1 s.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity) {
     if (mbar_try_wait(b, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(b, parity)) return true;
+        if (mbar_try_wait_sleep(b, parity)) return true;
         if (globaltimer() - t0 > kWaitTimeoutNs) return false;
     }
 }

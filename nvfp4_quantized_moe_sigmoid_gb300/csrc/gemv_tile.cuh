@@ -118,7 +118,7 @@ __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes
 // wait names the current or the immediately preceding phase; a waiter for use
 // u must not start while the barrier is still in phase u - 2, which fixed
 // ownership guarantees).
-constexpr int kConsumerWarps = 16;
+constexpr int kConsumerWarps = 12;
 constexpr int kMaxStages = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kConsumerThreads = kConsumerWarps * 32;

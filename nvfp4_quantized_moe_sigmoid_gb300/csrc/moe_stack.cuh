@@ -13,10 +13,12 @@
 //     2. x = RMSNorm(h_l); B operand of the up tiles (NVFP4 in W4A4);
 //     3. router logits of this CTA's experts (gate rows staged in shared
 //        memory during the previous layer) -> workspace, count them;
-//     4. its share of the shared expert's up tiles (staged during the
-//        previous layer): relu^2 -> bf16 rows + row amax (W4A4);
-//     5. wait for all E logits; sigmoid + bias top-k (rank per expert, every
+//     4. wait for all E logits; sigmoid + bias top-k (rank per expert, every
 //        CTA computes the same selection), the step plan (unique experts);
+//        from here the producer streams the routed tiles;
+//     5. its share of the shared expert's up tiles (staged during the
+//        previous layer, computed while the routed tiles are in flight):
+//        relu^2 -> bf16 rows + row amax (W4A4);
 //     6. its share of the routed up tiles (per-expert done counters);
 //     7. wait for the experts whose down tiles it owns; quantise their
 //        intermediate rows with the now final row amax (W4A4) as its B operand;
@@ -105,6 +107,7 @@ __device__ __noinline__ bool wait_geq(const int* p, int target, int* abort_g) {
     const unsigned long long t0 = globaltimer();
     for (int it = 0;; ++it) {
         if (ld_acquire_gpu(p) >= target) return true;
+        __nanosleep(64);  // leave the issue slots to the computing warps
         if ((it & 15) == 15) {
             if (ld_acquire_gpu(abort_g)) return false;
             if (globaltimer() - t0 > kWaitTimeoutNs) {
@@ -119,8 +122,7 @@ __device__ __noinline__ bool wait_geq(const int* p, int target, int* abort_g) {
 __device__ __noinline__ bool mbar_wait_abortable(uint64_t* b, uint32_t parity, volatile int* abort_s) {
     const unsigned long long t0 = globaltimer();
     for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(b, parity)) return true;
+        if (mbar_try_wait_sleep(b, parity)) return true;
         if (*abort_s) return false;
         if (globaltimer() - t0 > kWaitTimeoutNs) {
             set_dev_error(kErrWaitFull);
@@ -323,7 +325,7 @@ __device__ __noinline__ bool st_router(const StackArgs& a, StackCta& c, int l) {
     return true;
 }
 
-// ---------------------------------------------------------------- step 5
+// ---------------------------------------------------------------- step 4
 // Top-k by (sigma + bias desc, index asc) for every token, its gates
 // sigma / sum(sigma), and the step plan. Every CTA computes the same result.
 __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l) {
@@ -346,25 +348,25 @@ __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l
         (&c.plan.gate[0][0])[i] = 0.0f;
     }
     consumer_bar();
+    // rank of (t, e) = #{e2 : s2 > s or (s2 == s and e2 < e)}; four threads
+    // per (t, e), each over a quarter of the experts (E % 8 == 0), 16-byte
+    // loads, counts added with shuffles inside the group of four lanes
 #pragma unroll 1
-    for (int i = ctid; i < T * E; i += kConsumerThreads) {
+    for (int i4 = ctid; i4 < 4 * T * E; i4 += kConsumerThreads) {
+        const int i = i4 >> 2, part = i4 & 3;
         const int t = i / E, e = i % E;
         const float* ct = c.tk_c + (size_t)t * E;
         const float s = ct[e];
-        // rank = #{e2 : s2 > s or (s2 == s and e2 < e)}; four scores per
-        // 16-byte load (E % 4 == 0), two independent counts
-        int r0 = 0, r1 = 0;
-#pragma unroll 4
-        for (int e2 = 0; e2 < E; e2 += 8) {
-            const float4 p = *reinterpret_cast<const float4*>(ct + e2);
-            const float4 q = *reinterpret_cast<const float4*>(ct + e2 + 4);
-            r0 += (p.x > s || (p.x == s && e2 < e)) + (p.y > s || (p.y == s && e2 + 1 < e)) +
-                  (p.z > s || (p.z == s && e2 + 2 < e)) + (p.w > s || (p.w == s && e2 + 3 < e));
-            r1 += (q.x > s || (q.x == s && e2 + 4 < e)) + (q.y > s || (q.y == s && e2 + 5 < e)) +
-                  (q.z > s || (q.z == s && e2 + 6 < e)) + (q.w > s || (q.w == s && e2 + 7 < e));
+        const int q4 = E >> 2;
+        int rank = 0;
+#pragma unroll 2
+        for (int e2 = part * q4; e2 < (part + 1) * q4; e2 += 2) {
+            const float2 p = *reinterpret_cast<const float2*>(ct + e2);
+            rank += (p.x > s || (p.x == s && e2 < e)) + (p.y > s || (p.y == s && e2 + 1 < e));
         }
-        const int rank = r0 + r1;
-        if (rank < k) {
+        rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+        rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+        if (part == 0 && rank < k) {
             c.sel_idx[t][rank] = e;
             c.sel_sig[t][rank] = c.tk_s[i];
         }
@@ -408,7 +410,7 @@ __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l
     consumer_bar();
 }
 
-// ---------------------------------------------------------------- steps 4, 6
+// ---------------------------------------------------------------- steps 5, 6
 // Up tiles [base, base + n): shared (routed == false, tiles su_b + i) or
 // routed (tiles i of the U x I/16 list from ru_b). relu^2 -> bf16 rows, row
 // amax (W4A4), one count per finished tile. Returns false on a timeout.
@@ -726,11 +728,9 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
             bad = true;
             break;
         }
-        // 4. shared-expert up tiles
-        const int n_su = c.su_e - c.su_b;
-        if (!st_up_tiles<W4A4>(a, c, l, base, n_su, false, 0)) set_cta_abort(c);
-        base += n_su;
-        // 5. top-k and plan (once the producer has stopped reading the previous plan)
+        // 4. top-k and plan as soon as every logit is posted (and the producer
+        // has stopped reading the previous plan), so that the routed weights
+        // start streaming while this CTA still works on the shared tiles
         {
             bool ok = true;
             if (ctid == 0) ok = wait_geq(cnt + kCntLogits, E, abort_flag(a));
@@ -742,6 +742,10 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
         }
         st_topk_plan(a, c, l);
         if (ctid == 0) mbar_arrive(&c.pbar);  // the producer may stream the routed tiles now
+        // 5. shared-expert up tiles (staged during the previous layer)
+        const int n_su = c.su_e - c.su_b;
+        if (!st_up_tiles<W4A4>(a, c, l, base, n_su, false, 0)) set_cta_abort(c);
+        base += n_su;
         // 6. routed up tiles
         const int U = c.plan.U;
         const int NU = U * RI, ND = U * RH;

@@ -23,7 +23,7 @@ namespace nvfp4moe {
 namespace cg = cooperative_groups;
 
 constexpr int kRouteCluster = 8;
-constexpr int kRouteWarps = 16;
+constexpr int kRouteWarps = kConsumerWarps;
 constexpr int kRouteMaxExpertsPerCta = 32;  // E <= 256
 constexpr int kRouteTile = 8;               // tokens per cluster
 
