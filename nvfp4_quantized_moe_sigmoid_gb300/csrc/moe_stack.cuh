@@ -95,6 +95,18 @@ struct StackArgs {
     int off_gate, off_uni, off_tk;  // dynamic shared-memory regions after the ring
 };
 
+// Counter updates that publish data: the warp's (or CTA's) earlier writes,
+// ordered before the executing thread by a warp or CTA barrier, are visible
+// to whoever acquires the counter (no separate full fence).
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int atom_acq_rel_add(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -165,6 +177,9 @@ struct StackCta {
     float sel_w[kDecodeMaxT][kDecodeMaxK];
     float zred[kConsumerWarps][kDecodeMaxT];
     int slot_u[2];
+    // per-tensor globals of this layer's unique experts and shared expert
+    float up_g[kDecodeMaxU], down_g[kDecodeMaxU];
+    float shu_g, shd_g;
 };
 
 __device__ __forceinline__ bool cta_abort(StackCta& c) { return *static_cast<volatile int*>(&c.abort_s) != 0; }
@@ -317,11 +332,10 @@ __device__ __noinline__ bool st_router(const StackArgs& a, StackCta& c, int l) {
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) s = __fadd_rn(s, c.zred[w][ctid]);
             z[(size_t)ctid * E + c.b + j * c.G] = s;
-            __threadfence();
         }
         consumer_bar();
     }
-    if (ctid == 0 && c.ng > 0) atomicAdd(layer_cnt(a, l) + kCntLogits, c.ng);
+    if (ctid == 0 && c.ng > 0) red_release_add(layer_cnt(a, l) + kCntLogits, c.ng);
     return true;
 }
 
@@ -410,6 +424,21 @@ __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l
     consumer_bar();
 }
 
+// The per-tensor globals the epilogues of layer l need, read once (after the
+// plan is handed to the producer, off its path).
+__device__ __noinline__ void st_layer_globals(const StackArgs& a, StackCta& c, int l) {
+    const int ctid = threadIdx.x;
+    const StackLayer& P = a.layer[l];
+    if (ctid < c.plan.U) {
+        c.up_g[ctid] = __ldg(P.up_global + c.plan.expert[ctid]);
+        c.down_g[ctid] = __ldg(P.down_global + c.plan.expert[ctid]);
+    } else if (ctid == 64) {
+        c.shu_g = __ldg(P.shu_global);
+        c.shd_g = __ldg(P.shd_global);
+    }
+    consumer_bar();
+}
+
 // ---------------------------------------------------------------- steps 5, 6
 // Up tiles [base, base + n): shared (routed == false, tiles su_b + i) or
 // routed (tiles i of the U x I/16 list from ru_b). relu^2 -> bf16 rows, row
@@ -421,7 +450,6 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
     const int g = lane >> 2, q = lane & 3;
     const int T = a.T, k = a.k, H = a.H, I = a.I, S = a.S, RI = I >> 4;
     const int nst = c.nst;
-    const StackLayer& P = a.layer[l];
     unsigned int* const amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
     int* const cnt = layer_cnt(a, l);
     const __half* bcol = g < T ? c.xq + (size_t)g * H : nullptr;
@@ -442,7 +470,7 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
         } else {
             r = c.su_b + (li - base);
         }
-        const float gw = routed ? __ldg(P.up_global + c.plan.expert[u]) : __ldg(P.shu_global);
+        const float gw = routed ? c.up_g[u] : c.shu_g;
         float m[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
@@ -478,9 +506,8 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
                 }
             }
         }
-        __threadfence();
         __syncwarp();
-        if (lane == 0) atomicAdd(cnt + (routed ? kCntUp + u : kCntShUp), 1);
+        if (lane == 0) red_release_add(cnt + (routed ? kCntUp + u : kCntShUp), 1);
     }
     return true;
 }
@@ -564,9 +591,8 @@ __device__ __noinline__ void combine_tile(const StackArgs& a, StackCta& c, int l
         const __nv_bfloat16 ob = __float2bfloat16_rn(acc);
         out[(size_t)t * H + row] = *reinterpret_cast<const uint16_t*>(&ob);
     }
-    __threadfence();
     __syncwarp();
-    if (lane == 0) atomicAdd(layer_cnt(a, l) + kCntHDone, 1);
+    if (lane == 0) red_release_add(layer_cnt(a, l) + kCntHDone, 1);
 }
 
 // ---------------------------------------------------------------- step 8
@@ -577,7 +603,6 @@ __device__ __noinline__ bool st_down_tiles(const StackArgs& a, StackCta& c, int 
     const int T = a.T, k = a.k, H = a.H, I = a.I, S = a.S, RH = H >> 4;
     const int nst = c.nst;
     const int n_sd = c.sd_e - c.sd_b;
-    const StackLayer& P = a.layer[l];
     int* const cnt = layer_cnt(a, l);
     const int U = c.plan.U;
     const __half* bslot2 = c.bslot + (size_t)2 * T * I;
@@ -607,7 +632,7 @@ __device__ __noinline__ bool st_down_tiles(const StackArgs& a, StackCta& c, int 
         const bool lead = group_tile(c.ring, nst, li, st, K, bcol, acc, ok);
         if (!ok) return false;
         if (!lead) continue;
-        const float gw = routed ? __ldg(P.down_global + c.plan.expert[u]) : __ldg(P.shd_global);
+        const float gw = routed ? c.down_g[u] : c.shd_g;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const int t = 2 * q + (v & 1);
@@ -623,13 +648,12 @@ __device__ __noinline__ bool st_down_tiles(const StackArgs& a, StackCta& c, int 
             }
         }
         // count this contribution to output tile r; the last one combines it
-        __threadfence();
         __syncwarp();
         int prev = 0;
-        if (lane == 0) prev = atomicAdd(cnt + kCntTile + r, 1);
+        if (lane == 0) prev = atom_acq_rel_add(cnt + kCntTile + r, 1);
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == U) {
-            __threadfence();
+            __syncwarp();  // lane 0's acquire orders the other lanes' loads too
             combine_tile(a, c, l, r);
         }
     }
@@ -742,6 +766,7 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
         }
         st_topk_plan(a, c, l);
         if (ctid == 0) mbar_arrive(&c.pbar);  // the producer may stream the routed tiles now
+        st_layer_globals(a, c, l);
         // 5. shared-expert up tiles (staged during the previous layer)
         const int n_su = c.su_e - c.su_b;
         if (!st_up_tiles<W4A4>(a, c, l, base, n_su, false, 0)) set_cta_abort(c);
