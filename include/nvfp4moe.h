@@ -284,8 +284,8 @@ nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w
 #define NVFP4MOE_STACK_MAX_LAYERS 32
 typedef struct {
     moe_layer_weights moe;
-    const float* router_w;    /* [E][H] */
-    const float* router_bias; /* [E] */
+    const float* router_w;    /* [E][H], 16-byte aligned */
+    const float* router_bias; /* [E], 16-byte aligned */
 } moe_stack_layer;
 
 size_t moe_stack_forward_workspace_size(const moe_stack_layer* layers, int32_t L, int32_t T, int32_t k,

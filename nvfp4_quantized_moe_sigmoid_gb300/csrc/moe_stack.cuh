@@ -180,6 +180,8 @@ struct StackCta {
     // per-tensor globals of this layer's unique experts and shared expert
     float up_g[kDecodeMaxU], down_g[kDecodeMaxU];
     float shu_g, shd_g;
+    // router correction bias of the current layer, staged with its router rows
+    __align__(16) float bias_s[256];
 };
 
 __device__ __forceinline__ bool cta_abort(StackCta& c) { return *static_cast<volatile int*>(&c.abort_s) != 0; }
@@ -342,64 +344,82 @@ __device__ __noinline__ bool st_router(const StackArgs& a, StackCta& c, int l) {
 // ---------------------------------------------------------------- step 4
 // Top-k by (sigma + bias desc, index asc) for every token, its gates
 // sigma / sum(sigma), and the step plan. Every CTA computes the same result.
+// One warp per token: lane l holds experts l, l + 32, ... as order-preserving
+// 32-bit keys of sigma + bias; each of the k picks is a warp max of the key
+// followed by a warp min of the index among the lanes that hold that key.
+constexpr int kTopkPerLane = 8;  // E <= 256
+
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // > 0 for every non-NaN value
+}
+
 __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l) {
-    const int ctid = threadIdx.x;
+    const int ctid = threadIdx.x, warp = ctid >> 5, lane = ctid & 31;
     const int T = a.T, E = a.E, k = a.k;
-    const float* z = a.ws.z + (size_t)l * T * E;
-    const float* bias = a.layer[l].router_b;
-#pragma unroll 1
-    for (int i = ctid; i < T * E; i += kConsumerThreads) {
-        const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-__ldcg(z + i))));
-        float s = __fadd_rn(sg, __ldg(bias + i % E));
-        if (s != s) s = -INFINITY;
-        c.tk_c[i] = s;
-        c.tk_s[i] = sg;
-    }
     if (ctid < 8) c.plan.bits[ctid] = 0u;
 #pragma unroll 1
     for (int i = ctid; i < kDecodeMaxU * kDecodeMaxT; i += kConsumerThreads) {
         (&c.plan.choice[0][0])[i] = -1;
         (&c.plan.gate[0][0])[i] = 0.0f;
     }
-    consumer_bar();
-    // rank of (t, e) = #{e2 : s2 > s or (s2 == s and e2 < e)}; four threads
-    // per (t, e), each over a quarter of the experts (E % 8 == 0), 16-byte
-    // loads, counts added with shuffles inside the group of four lanes
-#pragma unroll 1
-    for (int i4 = ctid; i4 < 4 * T * E; i4 += kConsumerThreads) {
-        const int i = i4 >> 2, part = i4 & 3;
-        const int t = i / E, e = i % E;
-        const float* ct = c.tk_c + (size_t)t * E;
-        const float s = ct[e];
-        const int q4 = E >> 2;
-        int rank = 0;
-#pragma unroll 2
-        for (int e2 = part * q4; e2 < (part + 1) * q4; e2 += 2) {
-            const float2 p = *reinterpret_cast<const float2*>(ct + e2);
-            rank += (p.x > s || (p.x == s && e2 < e)) + (p.y > s || (p.y == s && e2 + 1 < e));
+    if (warp < T) {
+        const int t = warp;
+        const float* z = a.ws.z + ((size_t)l * T + t) * E;
+        uint32_t key[kTopkPerLane];
+        float sg[kTopkPerLane];
+#pragma unroll
+        for (int q = 0; q < kTopkPerLane; ++q) {
+            const int e = lane + 32 * q;
+            key[q] = 0u;
+            sg[q] = 0.0f;
+            if (e < E) {
+                sg[q] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-__ldcg(z + e))));
+                float v = __fadd_rn(sg[q], c.bias_s[e]);
+                if (v != v) v = -INFINITY;
+                key[q] = order_key(__fadd_rn(v, 0.0f));  // -0 and +0 compare equal
+            }
         }
-        rank += __shfl_xor_sync(0xffffffffu, rank, 1);
-        rank += __shfl_xor_sync(0xffffffffu, rank, 2);
-        if (part == 0 && rank < k) {
-            c.sel_idx[t][rank] = e;
-            c.sel_sig[t][rank] = c.tk_s[i];
-        }
-    }
-    consumer_bar();
-    if (ctid < T) {
         float ssum = 0.0f;
-#pragma unroll 1
-        for (int j = 0; j < k; ++j) ssum = __fadd_rn(ssum, c.sel_sig[ctid][j]);
-#pragma unroll 1
         for (int j = 0; j < k; ++j) {
-            const float w = __fdiv_rn(c.sel_sig[ctid][j], ssum);
-            c.sel_w[ctid][j] = w;
+            // this lane's best: largest key, then smallest index (smaller q)
+            uint32_t bk = 0u;
+            int bq = 0;
+#pragma unroll
+            for (int q = 0; q < kTopkPerLane; ++q)
+                if (key[q] > bk) {
+                    bk = key[q];
+                    bq = q;
+                }
+            const uint32_t km = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t cand = (bk == km && bk != 0u) ? static_cast<uint32_t>(lane + 32 * bq) : 0xFFFFFFFFu;
+            const int es = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+            const int qs = es >> 5;
+            float mine = 0.0f;
+#pragma unroll
+            for (int q = 0; q < kTopkPerLane; ++q)
+                if (q == qs) {
+                    mine = sg[q];
+                    if (lane == (es & 31)) key[q] = 0u;  // taken
+                }
+            const float sj = __shfl_sync(0xffffffffu, mine, es & 31);
+            ssum = __fadd_rn(ssum, sj);
+            if (lane == 0) {
+                c.sel_idx[t][j] = es;
+                c.sel_sig[t][j] = sj;
+            }
+        }
+        __syncwarp();
+        if (lane < k) {
+            const float w = __fdiv_rn(c.sel_sig[t][lane], ssum);
+            c.sel_w[t][lane] = w;
             if (c.b == 0) {
-                a.topk_idx[((size_t)l * T + ctid) * k + j] = c.sel_idx[ctid][j];
-                a.topk_w[((size_t)l * T + ctid) * k + j] = w;
+                a.topk_idx[((size_t)l * T + t) * k + lane] = c.sel_idx[t][lane];
+                a.topk_w[((size_t)l * T + t) * k + lane] = w;
             }
         }
     }
+    consumer_bar();
     if (ctid < T * k) {
         const int e = c.sel_idx[ctid / k][ctid % k];
         atomicOr(&c.plan.bits[e >> 5], 1u << (e & 31));
@@ -681,13 +701,15 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
         }
         ++pli;
     };
+    // router rows of this CTA's experts and the layer's bias (E * 4 bytes,
+    // E % 8 == 0: a multiple of 16 bytes), on one barrier phase per layer
     auto issue_gate = [&](int l) {
-        if (c.ng == 0) return;
-        mbar_arrive_expect_tx(&c.gbar, (uint32_t)(c.ng * H * 4));
+        mbar_arrive_expect_tx(&c.gbar, (uint32_t)(c.ng * H * 4 + a.E * 4));
 #pragma unroll 1
         for (int j = 0; j < c.ng; ++j)
             bulk_g2s(c.gsm + (size_t)j * H, a.layer[l].router_w + (size_t)(b + j * G) * H, (uint32_t)(H * 4),
                      &c.gbar);
+        bulk_g2s(c.bias_s, a.layer[l].router_b, (uint32_t)(a.E * 4), &c.gbar);
         c.gate_issued += 1;
     };
     auto issue_shared_up = [&](int l) {
@@ -747,8 +769,8 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
             }
         }
         st_input<W4A4>(a, c, l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H);
-        // 3. router logits
-        if (c.ng > 0 && !st_router(a, c, l)) {
+        // 3. router logits (the wait also covers the staged bias)
+        if (!st_router(a, c, l)) {
             bad = true;
             break;
         }
