@@ -263,7 +263,8 @@ nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w
  * the current layer still waits on its routing.
  *   layers     host array [L] of per-layer device pointers (copied into the
  *              launch; not read after the call returns); every layer has the
- *              same E, H, I, S with H, I, S % 64 == 0, E % 8 == 0 and E <= 256
+ *              same E, H, I, S with H, I, S % 64 == 0, E % 8 == 0 and E <= 256;
+ *              router_w, router_bias, up_global and down_global 16-byte aligned
  *   L          1 .. NVFP4MOE_STACK_MAX_LAYERS
  *   hidden_in  device bf16 [T][H] h_0, 16-byte aligned
  *   T, k       1 <= T <= 4, 1 <= k <= min(E, 16)

@@ -180,8 +180,11 @@ struct StackCta {
     // per-tensor globals of this layer's unique experts and shared expert
     float up_g[kDecodeMaxU], down_g[kDecodeMaxU];
     float shu_g, shd_g;
-    // router correction bias of the current layer, staged with its router rows
+    // router correction bias and the routed experts' per-tensor globals of
+    // the current layer, staged with its router rows
     __align__(16) float bias_s[256];
+    __align__(16) float upg_s[256];
+    __align__(16) float dng_s[256];
 };
 
 __device__ __forceinline__ bool cta_abort(StackCta& c) { return *static_cast<volatile int*>(&c.abort_s) != 0; }
@@ -210,10 +213,14 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 // eight elements 256c + 8l .. + 7 in order (fused multiply-add), an
 // xor-shuffle tree gives the chunk sum, chunk sums are added in chunk order.
 template <bool W4A4>
-__device__ __noinline__ void st_input(const StackArgs& a, StackCta& c, const uint16_t* h) {
+__device__ __noinline__ void st_input(const StackArgs& a, StackCta& c, const uint16_t* h, int l) {
     const int ctid = threadIdx.x, warp = ctid >> 5, lane = ctid & 31;
     const int T = a.T, H = a.H;
     uint16_t* X = c.X;
+    if (ctid == kConsumerThreads - 1) {  // used by the epilogues later in the layer
+        c.shu_g = __ldg(a.layer[l].shu_global);
+        c.shd_g = __ldg(a.layer[l].shd_global);
+    }
 #pragma unroll 1
     for (int i = 8 * ctid; i < T * H; i += 8 * kConsumerThreads)
         *reinterpret_cast<uint4*>(X + i) = __ldcg(reinterpret_cast<const uint4*>(h + i));
@@ -444,17 +451,13 @@ __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l
     consumer_bar();
 }
 
-// The per-tensor globals the epilogues of layer l need, read once (after the
-// plan is handed to the producer, off its path).
-__device__ __noinline__ void st_layer_globals(const StackArgs& a, StackCta& c, int l) {
+// The per-tensor globals of the layer's unique experts, from the staged
+// arrays (before the producer may restage them for the next layer).
+__device__ __noinline__ void st_layer_globals(StackCta& c) {
     const int ctid = threadIdx.x;
-    const StackLayer& P = a.layer[l];
     if (ctid < c.plan.U) {
-        c.up_g[ctid] = __ldg(P.up_global + c.plan.expert[ctid]);
-        c.down_g[ctid] = __ldg(P.down_global + c.plan.expert[ctid]);
-    } else if (ctid == 64) {
-        c.shu_g = __ldg(P.shu_global);
-        c.shd_g = __ldg(P.shd_global);
+        c.up_g[ctid] = c.upg_s[c.plan.expert[ctid]];
+        c.down_g[ctid] = c.dng_s[c.plan.expert[ctid]];
     }
     consumer_bar();
 }
@@ -704,12 +707,14 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
     // router rows of this CTA's experts and the layer's bias (E * 4 bytes,
     // E % 8 == 0: a multiple of 16 bytes), on one barrier phase per layer
     auto issue_gate = [&](int l) {
-        mbar_arrive_expect_tx(&c.gbar, (uint32_t)(c.ng * H * 4 + a.E * 4));
+        mbar_arrive_expect_tx(&c.gbar, (uint32_t)(c.ng * H * 4 + 3 * a.E * 4));
 #pragma unroll 1
         for (int j = 0; j < c.ng; ++j)
             bulk_g2s(c.gsm + (size_t)j * H, a.layer[l].router_w + (size_t)(b + j * G) * H, (uint32_t)(H * 4),
                      &c.gbar);
         bulk_g2s(c.bias_s, a.layer[l].router_b, (uint32_t)(a.E * 4), &c.gbar);
+        bulk_g2s(c.upg_s, a.layer[l].up_global, (uint32_t)(a.E * 4), &c.gbar);
+        bulk_g2s(c.dng_s, a.layer[l].down_global, (uint32_t)(a.E * 4), &c.gbar);
         c.gate_issued += 1;
     };
     auto issue_shared_up = [&](int l) {
@@ -768,7 +773,7 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
                 break;
             }
         }
-        st_input<W4A4>(a, c, l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H);
+        st_input<W4A4>(a, c, l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H, l);
         // 3. router logits (the wait also covers the staged bias)
         if (!st_router(a, c, l)) {
             bad = true;
@@ -787,8 +792,8 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
             }
         }
         st_topk_plan(a, c, l);
+        st_layer_globals(c);
         if (ctid == 0) mbar_arrive(&c.pbar);  // the producer may stream the routed tiles now
-        st_layer_globals(a, c, l);
         // 5. shared-expert up tiles (staged during the previous layer)
         const int n_su = c.su_e - c.su_b;
         if (!st_up_tiles<W4A4>(a, c, l, base, n_su, false, 0)) set_cta_abort(c);

@@ -827,7 +827,9 @@ nvfp4_status check_stack(const moe_stack_layer* layers, int32_t L, int32_t T, in
             ly.moe.shared_inter != w0.shared_inter)
             return NVFP4_ERR_INVALID_ARG;
         if (!ly.router_w || !ly.router_bias) return NVFP4_ERR_INVALID_ARG;
-        if (!aligned(ly.router_w, 16) || !aligned(ly.router_bias, 16)) return NVFP4_ERR_MISALIGNED;
+        if (!aligned(ly.router_w, 16) || !aligned(ly.router_bias, 16) || !aligned(ly.moe.up_global, 16) ||
+            !aligned(ly.moe.down_global, 16))
+            return NVFP4_ERR_MISALIGNED;
     }
     if (k > w0.num_experts) return NVFP4_ERR_INVALID_ARG;
     if (T > kDecodeMaxT || k > kDecodeMaxK || w0.num_experts > 256 || w0.num_experts % 8) return NVFP4_ERR_UNSUPPORTED_SHAPE;
