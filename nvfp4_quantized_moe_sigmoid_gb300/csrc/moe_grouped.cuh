@@ -205,7 +205,7 @@ constexpr int kGScaleBytes = kGTile * 8;
 constexpr int kGBRowHalves = 128 + 8;  // padded row: fewer bank conflicts
 constexpr int kGBBytes = kGTile * kGBRowHalves * 2;
 constexpr int kGStageBytes = kGCodeBytes + kGScaleBytes + kGBBytes;
-constexpr int kGStages = 3;
+constexpr int kGStages = 5;
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)

@@ -500,7 +500,7 @@ nvfp4_status grouped_forward(const moe_layer_weights* w, const void* hidden, con
     ga.act_sh = b16(o.act_sh);
     ga.amax = u32(o.amax);
     ga.amax_sh = u32(o.amax_sh);
-    const int ggrid = num_sms() * 3;
+    const int ggrid = num_sms() * 2;
     nvfp4_status st;
     if (w4a4) {
         if (dyn_smem_limit(k_grouped<true, kGroupedUp>) < (int)gsmem) return NVFP4_ERR_UNSUPPORTED_SHAPE;
@@ -1005,6 +1005,6 @@ extern "C" nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidde
     ga.ysh = logits;
     const size_t gsmem = (size_t)kGStages * kGStageBytes;
     if (dyn_smem_limit(k_grouped<false, kGroupedDown>) < (int)gsmem) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    k_grouped<false, kGroupedDown><<<num_sms() * 3, kGThreads, gsmem, stream>>>(ga);
+    k_grouped<false, kGroupedDown><<<num_sms() * 2, kGThreads, gsmem, stream>>>(ga);
     return launch_status();
 }
