@@ -195,6 +195,25 @@ struct QBlock {
 // is that same signed zero), which keeps it off the division's slow path.
 __device__ __forceinline__ float div_rn_or_zero(float x, float d) { return x == 0.0f ? x : __fdiv_rn(x, d); }
 
+// x / d rounded to nearest even from y = RN(1/d), by Markstein's correction
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with y the correctly
+// rounded reciprocal and q within one ulp of x / d, the residual x - q d is
+// exact under a fused multiply-add and RN(q + (x - q d) y) is the correctly
+// rounded quotient. The product estimate x y can be 1.5 ulp off, so one
+// correction first makes it faithful, the second rounds it. Exact for finite x
+// and 2^-100 <= d <= 2^100 whenever |x / d| >= 2^-3 (the residuals are then
+// representable); a smaller quotient may be an ulp off, keeps its sign and
+// stays below every E2M1 rounding boundary, the only use made of it here. A
+// zero x is returned as it is (the sum of signed zeros in the corrections
+// would turn -0 into +0).
+__device__ __forceinline__ float div_by_recip(float x, float d, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, d, x), y, q0);
+    const float q2 = __fmaf_rn(__fmaf_rn(-q1, d, x), y, q1);
+    return x == 0.0f ? x : q2;
+}
+
 __device__ __forceinline__ QBlock quantize_block16(const float (&x)[16], float g) {
     float bamax = 0.0f;
 #pragma unroll
@@ -203,7 +222,15 @@ __device__ __forceinline__ QBlock quantize_block16(const float (&x)[16], float g
     if (g > 0.0f && bamax > 0.0f) s = float_to_e4m3_pos(__fdiv_rn(__fdiv_rn(bamax, 6.0f), g));
     const float d = __fmul_rn(e4m3_to_float(s), g);
     QBlock q{0u, 0u, s};
-    if (d != 0.0f) {
+    if (d >= 0x1p-100f && d <= 0x1p100f) {
+        const float y = __frcp_rn(d);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t byte = float2_to_e2m1x2(div_by_recip(x[2 * i], d, y), div_by_recip(x[2 * i + 1], d, y));
+            if (i < 4) q.lo |= byte << (8 * i);
+            else q.hi |= byte << (8 * (i - 4));
+        }
+    } else if (d != 0.0f) {  // extreme per-tensor globals: the plain division
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t byte = float2_to_e2m1x2(div_rn_or_zero(x[2 * i], d), div_rn_or_zero(x[2 * i + 1], d));

@@ -91,7 +91,7 @@ struct StackArgs {
     int32_t* topk_idx;          // [L][T][k]
     float* topk_w;              // [L][T][k]
     StackWs ws;
-    int nst, stage_bytes;
+    int ring_cap;                   // staging ring bytes at the start of dynamic shared memory
     int off_gate, off_uni, off_tk;  // dynamic shared-memory regions after the ring
 };
 
@@ -131,31 +131,65 @@ __device__ __noinline__ bool wait_geq(const int* p, int target, int* abort_g) {
     }
 }
 
-__device__ __noinline__ bool mbar_wait_abortable(uint64_t* b, uint32_t parity, volatile int* abort_s) {
+__device__ __noinline__ bool mbar_wait_abortable(uint64_t* b, uint32_t parity, volatile int* abort_s,
+                                                unsigned int err = kErrWaitFull) {
     const unsigned long long t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait_sleep(b, parity)) return true;
         if (*abort_s) return false;
         if (globaltimer() - t0 > kWaitTimeoutNs) {
-            set_dev_error(kErrWaitFull);
+            set_dev_error(err);
             return false;
         }
     }
 }
 
+// ---------------------------------------------------------------- staging ring
+// A byte ring over the CTA's free shared memory. 16-row tiles of any K
+// (9 K bytes: codes [16][K/2], then scales [16][K/16]) are placed one after
+// another in issue order (an item that would cross the end starts again at
+// offset 0), so that as many tiles are in flight as fit, whatever their K.
+// Item li completes on full[li % kSlots] and is computed by warp group
+// li % kGroups (the consumer warps w with w % kGroups == li % kGroups), whose
+// kGroupWarps warps each take a contiguous share of its 128-k chunks and
+// release it on empty[li % kSlots]. kSlots is a multiple of kGroups, so the
+// same warps wait on every use of a slot, in order (a parity wait can only
+// tell the current phase of an mbarrier from the one before it). The
+// producer reclaims space in issue order: before placing an item it waits
+// until the item that last used the slot, and every older item whose bytes
+// the new one would overwrite, have been released.
+constexpr int kGroups = 4;
+constexpr int kGroupWarps = kConsumerWarps / kGroups;
+constexpr int kSlots = 16;
+static_assert(kConsumerWarps % kGroups == 0 && kSlots % kGroups == 0, "ring groups");
+
+struct BRing {
+    uint64_t full[kSlots];
+    uint64_t empty[kSlots];
+    uint32_t off[kSlots];  // byte offset of the slot's current item
+    int vs[kSlots];        // its virtual start (producer side)
+    int uses[kSlots];      // fills of the slot (producer side)
+    int vhead;             // virtual end of the last item placed
+    int tail;              // oldest item not yet seen released
+    // partial tiles handed from ranks 1.. of a group to its rank 0, double
+    // buffered by the group's item parity; warp w >= kGroups uses w - kGroups
+    float4 xred[kConsumerWarps - kGroups][2][32];
+};
+
 constexpr int kNormMaxChunks = 64;  // H <= 16384
 
 // Per-CTA state of the stack kernel, in shared memory.
 struct StackCta {
-    Ring ring;
+    BRing br;
     DecodePlan plan;
     uint64_t gbar;  // router rows landed (one phase per layer)
     uint64_t pbar;  // plan ready for the producer (one phase per layer)
     uint64_t qbar;  // producer done reading the plan (one phase per layer)
     int gate_issued;
     int abort_s;
+    int last_cta;  // this CTA is the last to leave (resets the workspace)
     // geometry
-    int G, b, nst, stage_bytes, ng, amax_stride;
+    int G, b, ring_cap, ng, amax_stride;
     int su_b, su_e, sd_b, sd_e;  // shared-expert up / down tile ranges of this CTA
     uint8_t* ring_base;
     float* gsm;      // [ng][H] router rows
@@ -169,8 +203,6 @@ struct StackCta {
     float norm_inv[kDecodeMaxT];
     float gx[kDecodeMaxT];
     unsigned int red[kDecodeMaxT];
-    const uint16_t* srcs[3 * kDecodeMaxT];
-    unsigned int amx[3 * kDecodeMaxT];
     float gbf[3 * kDecodeMaxT];
     int sel_idx[kDecodeMaxT][kDecodeMaxK];
     float sel_sig[kDecodeMaxT][kDecodeMaxK];
@@ -189,6 +221,83 @@ struct StackCta {
 
 __device__ __forceinline__ bool cta_abort(StackCta& c) { return *static_cast<volatile int*>(&c.abort_s) != 0; }
 __device__ __forceinline__ void set_cta_abort(StackCta& c) { *static_cast<volatile int*>(&c.abort_s) = 1; }
+
+// Producer: place and issue local item li. False if it gave up waiting.
+__device__ __noinline__ bool bring_fill(StackCta& c, int li, const uint8_t* codes, const uint8_t* scales, int K) {
+    BRing& r = c.br;
+    const int cap = c.ring_cap;
+    const int cb = 8 * K, size = 9 * K;
+    int v = r.vhead;
+    if (v % cap + size > cap) v += cap - v % cap;
+    const int lim = v + size - cap;  // older items starting below this must be released
+#pragma unroll 1
+    while (r.tail < li && (r.tail <= li - kSlots || r.vs[r.tail % kSlots] < lim)) {
+        const int t = r.tail;
+        if (!mbar_wait_abortable(&r.empty[t % kSlots], static_cast<uint32_t>((t / kSlots) & 1), &c.abort_s,
+                                 kErrWaitEmpty))
+            return false;
+        r.tail = t + 1;
+    }
+    const int s = li % kSlots;
+    r.vs[s] = v;
+    r.off[s] = static_cast<uint32_t>(v % cap);
+    r.vhead = v + size;
+    uint8_t* dst = c.ring_base + v % cap;
+    mbar_arrive_expect_tx(&r.full[s], static_cast<uint32_t>(size));
+    bulk_g2s(dst, codes, static_cast<uint32_t>(cb), &r.full[s]);
+    bulk_g2s(dst + cb, scales, static_cast<uint32_t>(K), &r.full[s]);
+    r.uses[s] += 1;
+    return true;
+}
+
+// Consumers: item li by its warp group (see the ring above); the group's
+// rank-0 warp gets lead = 1 and the finished 16 x 8 tile, ok = 0 in every
+// warp of the group if any of them timed out.
+__device__ __noinline__ TileOut bgroup_tile_core(StackCta* cp, int li, int K, const __half* bcol) {
+    BRing& r = cp->br;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = warp % kGroups, rank = warp / kGroups;
+    const int s = li % kSlots;
+    const bool waited = mbar_wait_bounded(&r.full[s], static_cast<uint32_t>((li / kSlots) & 1));
+    const bool got = __all_sync(0xffffffffu, waited);
+    if (!got && lane == 0) set_dev_error(kErrWaitFull);
+    const int nc = (K + 127) >> 7;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (got) {
+        const uint8_t* st = cp->ring_base + r.off[s];
+        tile_mma_16x8(st, st + 8 * K, K, bcol, nc * rank / kGroupWarps, nc * (rank + 1) / kGroupWarps, acc);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&r.empty[s]);
+    TileOut o;
+    o.acc = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    const int u = (li / kGroups) & 1;
+    if (rank) r.xred[warp - kGroups][u][lane] = o.acc;
+    o.ok = group_bar_and(g, kGroupWarps, got);
+    o.lead = 0;
+    if (rank || !o.ok) return o;
+#pragma unroll
+    for (int p = 1; p < kGroupWarps; ++p) {
+        const float4 x = r.xred[g + (p - 1) * kGroups][u][lane];
+        o.acc.x += x.x;
+        o.acc.y += x.y;
+        o.acc.z += x.z;
+        o.acc.w += x.w;
+    }
+    o.lead = 1;
+    return o;
+}
+
+__device__ __forceinline__ bool bgroup_tile(StackCta& c, int li, int K, const __half* bcol, float (&acc)[4],
+                                            bool& ok) {
+    const TileOut o = bgroup_tile_core(&c, li, K, bcol);
+    acc[0] = o.acc.x;
+    acc[1] = o.acc.y;
+    acc[2] = o.acc.z;
+    acc[3] = o.acc.w;
+    ok = o.ok != 0;
+    return o.lead != 0;
+}
 
 __device__ __forceinline__ int* layer_cnt(const StackArgs& a, int l) {
     return a.ws.cnt + (size_t)l * stack_cnt_per_layer(a.H);
@@ -250,7 +359,14 @@ __device__ __noinline__ void st_input(const StackArgs& a, StackCta& c, const uin
         if (ctid < T) {
             float sum = 0.0f;
 #pragma unroll 1
-            for (int ch = 0; ch < nch; ++ch) sum = __fadd_rn(sum, c.norm_part[ctid][ch]);
+            for (int ch0 = 0; ch0 < nch; ch0 += 8) {
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = ch0 + j < nch ? c.norm_part[ctid][ch0 + j] : 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (ch0 + j < nch) sum = __fadd_rn(sum, v[j]);
+            }
             c.norm_inv[ctid] =
                 __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, static_cast<float>(H)), a.rms_eps)));
         }
@@ -370,22 +486,28 @@ __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l
         (&c.plan.choice[0][0])[i] = -1;
         (&c.plan.gate[0][0])[i] = 0.0f;
     }
+    // sigma = 1 / (1 + exp(-z)) and the order key of sigma + bias, one
+    // (token, expert) per thread
+    uint32_t* const keys = reinterpret_cast<uint32_t*>(c.tk_c);
+    const float* const z = a.ws.z + (size_t)l * T * E;
+#pragma unroll 1
+    for (int i = ctid; i < T * E; i += kConsumerThreads) {
+        const float s = __frcp_rn(__fadd_rn(1.0f, expf(-__ldcg(z + i))));
+        float v = __fadd_rn(s, c.bias_s[i % E]);
+        if (v != v) v = -INFINITY;
+        c.tk_s[i] = s;
+        keys[i] = order_key(__fadd_rn(v, 0.0f));  // -0 and +0 compare equal
+    }
+    consumer_bar();
     if (warp < T) {
         const int t = warp;
-        const float* z = a.ws.z + ((size_t)l * T + t) * E;
         uint32_t key[kTopkPerLane];
         float sg[kTopkPerLane];
 #pragma unroll
         for (int q = 0; q < kTopkPerLane; ++q) {
             const int e = lane + 32 * q;
-            key[q] = 0u;
-            sg[q] = 0.0f;
-            if (e < E) {
-                sg[q] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-__ldcg(z + e))));
-                float v = __fadd_rn(sg[q], c.bias_s[e]);
-                if (v != v) v = -INFINITY;
-                key[q] = order_key(__fadd_rn(v, 0.0f));  // -0 and +0 compare equal
-            }
+            key[q] = e < E ? keys[t * E + e] : 0u;
+            sg[q] = e < E ? c.tk_s[t * E + e] : 0.0f;
         }
         float ssum = 0.0f;
         for (int j = 0; j < k; ++j) {
@@ -472,17 +594,15 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     const int T = a.T, k = a.k, H = a.H, I = a.I, S = a.S, RI = I >> 4;
-    const int nst = c.nst;
     unsigned int* const amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
     int* const cnt = layer_cnt(a, l);
     const __half* bcol = g < T ? c.xq + (size_t)g * H : nullptr;
     const int end = base + n;
 #pragma unroll 1
-    for (int li = first_item(base, warp % nst, nst); li < end; li += nst) {
-        const uint8_t* st = c.ring_base + (size_t)(li % nst) * c.stage_bytes;
+    for (int li = first_item(base, warp % kGroups, kGroups); li < end; li += kGroups) {
         float acc[4];
         bool ok;
-        const bool lead = group_tile(c.ring, nst, li, st, H, bcol, acc, ok);
+        const bool lead = bgroup_tile(c, li, H, bcol, acc, ok);
         if (!ok) return false;
         if (!lead) continue;
         int u = 0, r;
@@ -560,29 +680,72 @@ __device__ __noinline__ bool st_down_operands(const StackArgs& a, StackCta& c, i
     if (ctid == 32 && c.slot_u[0] >= 0) ok = wait_geq(cnt + kCntUp + c.slot_u[0], RI, abort_flag(a));
     if (ctid == 64 && c.slot_u[1] >= 0) ok = wait_geq(cnt + kCntUp + c.slot_u[1], RI, abort_flag(a));
     if (consumer_bar_or(!ok || cta_abort(c))) return false;
-    if (ctid < 2 * T) {
-        const int sl = ctid / T, t = ctid % T;
-        const uint16_t* p = nullptr;
-        unsigned int mx = 0u;
-        if (c.slot_u[sl] >= 0) {
-            const int j = c.plan.choice[c.slot_u[sl]][t];
+    // one pass over the blocks of all rows: routed rows r = sl * T + t (slot
+    // sl of this CTA, token t; [I] each), then the shared rows ([S] each).
+    // Every thread reads its row's amax itself (no staging barrier) and keeps
+    // up to kBRegBlocks blocks' loads in flight before quantising any.
+    const int nbr = I >> 4, nbs = S >> 4;
+    const int nr = 2 * T * nbr, total = nr + (has_sd ? T * nbs : 0);
+    auto locate = [&](int i, const uint16_t*& src, const unsigned int*& am, __half*& dst, int& r, int& bb) {
+        src = nullptr;
+        am = nullptr;
+        if (i < nr) {
+            r = i / nbr;
+            bb = i - r * nbr;
+            const int sl = r / T, t = r - sl * T;
+            dst = c.bslot + (size_t)r * I + 16 * bb;
+            const int u = c.slot_u[sl];
+            const int j = u >= 0 ? c.plan.choice[u][t] : -1;
             if (j >= 0) {
-                p = a.ws.act + ((size_t)t * k + j) * I;
-                if (W4A4) mx = __ldcg(amax + t * k + j);
+                src = a.ws.act + ((size_t)t * k + j) * I + 16 * bb;
+                am = amax + t * k + j;
+            }
+        } else {
+            const int i2 = i - nr, t = i2 / nbs;
+            bb = i2 - t * nbs;
+            r = 2 * T + t;
+            dst = c.bslot + (size_t)2 * T * I + (size_t)t * S + 16 * bb;
+            src = a.ws.act_sh + (size_t)t * S + 16 * bb;
+            am = amax + T * k + t;
+        }
+    };
+#pragma unroll 1
+    for (int i0 = ctid; i0 < total; i0 += kBRegBlocks * kConsumerThreads) {
+        uint4 u[kBRegBlocks][2];
+        unsigned int mb[kBRegBlocks];
+#pragma unroll
+        for (int q = 0; q < kBRegBlocks; ++q) {
+            const int i = i0 + q * kConsumerThreads;
+            u[q][0] = u[q][1] = make_uint4(0, 0, 0, 0);
+            mb[q] = 0u;
+            if (i < total) {
+                const uint16_t* src;
+                const unsigned int* am;
+                __half* dst;
+                int r, bb;
+                locate(i, src, am, dst, r, bb);
+                if (src) {
+                    u[q][0] = __ldcg(reinterpret_cast<const uint4*>(src));
+                    u[q][1] = __ldcg(reinterpret_cast<const uint4*>(src) + 1);
+                    if (W4A4) mb[q] = __ldcg(am);
+                }
             }
         }
-        c.srcs[ctid] = p;
-        c.amx[ctid] = mx;
-    } else if (ctid >= 64 && ctid < 64 + T) {
-        const int t = ctid - 64;
-        c.srcs[2 * T + t] = a.ws.act_sh + (size_t)t * S;
-        c.amx[2 * T + t] = W4A4 ? __ldcg(amax + T * k + t) : 0u;
+#pragma unroll
+        for (int q = 0; q < kBRegBlocks; ++q) {
+            const int i = i0 + q * kConsumerThreads;
+            if (i >= total) break;
+            const uint16_t* src;
+            const unsigned int* am;
+            __half* dst;
+            int r, bb;
+            locate(i, src, am, dst, r, bb);
+            const float g = W4A4 ? __fdiv_rn(__uint_as_float(mb[q]), 2688.0f) : 0.0f;
+            b_block_store<W4A4>(u[q][0], u[q][1], g, reinterpret_cast<uint4*>(dst));
+            if (bb == 0) c.gbf[r] = g;  // the row's first block records its global
+        }
     }
     consumer_bar();
-    prepare_b_rows_known_amax<W4A4>(c.srcs, 2 * T, I, c.bslot, c.amx, c.gbf);
-    if (has_sd)
-        prepare_b_rows_known_amax<W4A4>(c.srcs + 2 * T, T, S, c.bslot + (size_t)2 * T * I, c.amx + 2 * T,
-                                        c.gbf + 2 * T);
     return true;
 }
 
@@ -624,14 +787,13 @@ __device__ __noinline__ bool st_down_tiles(const StackArgs& a, StackCta& c, int 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     const int T = a.T, k = a.k, H = a.H, I = a.I, S = a.S, RH = H >> 4;
-    const int nst = c.nst;
     const int n_sd = c.sd_e - c.sd_b;
     int* const cnt = layer_cnt(a, l);
     const int U = c.plan.U;
     const __half* bslot2 = c.bslot + (size_t)2 * T * I;
     const int end = base + n_sd + n_rd;
 #pragma unroll 1
-    for (int li = first_item(base, warp % nst, nst); li < end; li += nst) {
+    for (int li = first_item(base, warp % kGroups, kGroups); li < end; li += kGroups) {
         const bool routed = li >= base + n_sd;
         int u = -1, r, sl, K;
         if (routed) {
@@ -649,10 +811,9 @@ __device__ __noinline__ bool st_down_tiles(const StackArgs& a, StackCta& c, int 
         const __half* bs = sl == 2 ? bslot2 : c.bslot + (size_t)(sl < 0 ? 0 : sl) * T * I;
         const __half* bcol = nullptr;
         if (sl >= 0 && g < T && (!routed || c.plan.choice[u][g] >= 0)) bcol = bs + (size_t)g * K;
-        const uint8_t* st = c.ring_base + (size_t)(li % nst) * c.stage_bytes;
         float acc[4];
         bool ok;
-        const bool lead = group_tile(c.ring, nst, li, st, K, bcol, acc, ok);
+        const bool lead = bgroup_tile(c, li, K, bcol, acc, ok);
         if (!ok) return false;
         if (!lead) continue;
         const float gw = routed ? c.down_g[u] : c.shd_g;
@@ -684,11 +845,6 @@ __device__ __noinline__ bool st_down_tiles(const StackArgs& a, StackCta& c, int 
 }
 
 // ---------------------------------------------------------------- producer
-// One out-of-line fill (the producer streams four kinds of tile from one loop
-// each; a shared copy keeps its code small).
-__device__ __noinline__ bool fill_stage(StackCta& c, int li, const uint8_t* codes, const uint8_t* scales, int K) {
-    return ring_fill(c.ring, c.ring_base, c.stage_bytes, c.nst, li, codes, scales, K);
-}
 
 __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
     const int H = a.H, I = a.I, S = a.S, RI = I >> 4, RH = H >> 4;
@@ -697,7 +853,7 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
     bool alive = true;
     auto fill = [&](const uint8_t* codes, const uint8_t* scales, int K) {
         if (!alive) return;
-        if (cta_abort(c) || !fill_stage(c, pli, codes, scales, K)) {
+        if (cta_abort(c) || !bring_fill(c, pli, codes, scales, K)) {
             alive = false;
             set_cta_abort(c);
             return;
@@ -825,14 +981,28 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
 }
 
 template <bool W4A4>
-__global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant__ StackArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant__ StackArgs args) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ StackCta c;
+    // the steps read the arguments from a shared-memory copy: a kernel
+    // parameter read through a reference in an out-of-line function is a
+    // generic load several hundred cycles long, on every step's critical path
+    __shared__ __align__(16) StackArgs a;
+    static_assert(sizeof(StackArgs) % 4 == 0, "StackArgs copy");
+    for (int i = threadIdx.x; i < (int)(sizeof(StackArgs) / 4); i += blockDim.x)
+        reinterpret_cast<uint32_t*>(&a)[i] = reinterpret_cast<const uint32_t*>(&args)[i];
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, b = blockIdx.x;
 
-    ring_init(c.ring, a.nst);
     if (threadIdx.x == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&c.br.full[s], 1);
+            mbar_init(&c.br.empty[s], kGroupWarps);
+            c.br.uses[s] = 0;
+        }
+        c.br.vhead = 0;
+        c.br.tail = 0;
         mbar_init(&c.gbar, 1);
         mbar_init(&c.pbar, 1);
         mbar_init(&c.qbar, 1);
@@ -841,8 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant
         c.gate_issued = 0;
         c.G = G;
         c.b = b;
-        c.nst = a.nst;
-        c.stage_bytes = a.stage_bytes;
+        c.ring_cap = a.ring_cap;
         c.ng = b < a.E ? (a.E - b + G - 1) / G : 0;
         c.amax_stride = a.T * a.k + a.T;
         const int RS = a.S >> 4, RH = a.H >> 4;
@@ -867,16 +1036,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant
     }
 
     __syncthreads();
-    ring_drain(c.ring, c.nst);
+    // no bulk copy may still be landing in shared memory when the CTA exits
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSlots; ++s)
+            if (c.br.uses[s] > 0 && !mbar_wait_bounded(&c.br.full[s], (c.br.uses[s] - 1) & 1))
+                set_dev_error(kErrWaitDrain);
+    }
     if (threadIdx.x == 0 && c.gate_issued > 0 && !mbar_wait_bounded(&c.gbar, (c.gate_issued - 1) & 1))
         set_dev_error(kErrWaitDrain);
-    // the last CTA to leave resets the counters and the row amax for the next call
+    // the last CTA to leave resets the counters and the row amax for the next
+    // call (from the kernel parameters: stores through the workspace pointers
+    // would make every read of the shared copy a reload)
+    const int ncnt = args.L * stack_cnt_per_layer(args.H);
+    int* const cnt_exit = args.ws.cnt + ncnt;
     if (threadIdx.x == 0) {
-        int* const cnt_exit = a.ws.cnt + (size_t)a.L * stack_cnt_per_layer(a.H);
         __threadfence();
-        if (atomicAdd(cnt_exit, 1) == G - 1) {
-            for (int i = 0; i < a.L * stack_cnt_per_layer(a.H); ++i) a.ws.cnt[i] = 0;
-            for (int i = 0; i < 2 * (a.T * a.k + a.T); ++i) a.ws.amax[i] = 0u;
+        c.last_cta = atomicAdd(cnt_exit, 1) == G - 1;
+    }
+    __syncthreads();
+    if (c.last_cta) {
+        for (int i = threadIdx.x; i < ncnt; i += blockDim.x) args.ws.cnt[i] = 0;
+        for (int i = threadIdx.x; i < 2 * (args.T * args.k + args.T); i += blockDim.x) args.ws.amax[i] = 0u;
+        __syncthreads();
+        if (threadIdx.x == 0) {
             cnt_exit[1] = 0;
             __threadfence();
             *cnt_exit = 0;

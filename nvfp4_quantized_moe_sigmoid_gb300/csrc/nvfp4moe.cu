@@ -793,22 +793,24 @@ StackWsOffsets stack_ws(int L, int T, int k, int E, int H, int I, int S) {
 // Dynamic shared memory of the stack kernel: the ring, then the router rows,
 // the operand union (layer input + up B / down B slots), the top-k scores.
 struct StackSmem {
-    int nst, stage_bytes, off_gate, off_uni, off_tk, total;
+    int ring_cap, off_gate, off_uni, off_tk, total;
 };
 
+// Dynamic shared memory of the stack kernel: the staging ring takes whatever
+// the router rows, the B operands and the top-k scratch leave, and must hold
+// at least two of the largest tiles (9 K bytes for 16 rows of K).
 bool stack_smem(int lim, int E, int G, int T, int H, int I, int S, StackSmem* out) {
     auto a128 = [](size_t x) { return static_cast<int>((x + 127) & ~size_t(127)); };
-    const int stage = 9 * std::max(std::max(H, I), S);
+    const int item = 9 * std::max(std::max(H, I), S);
     const int ng = (E + G - 1) / G;
     const int gate = a128((size_t)ng * H * 4);
     const int uni = a128(std::max((size_t)T * H * 4, ((size_t)2 * T * I + (size_t)T * S) * 2));
     const int tk = a128((size_t)T * E * 8);
     const int rest = gate + uni + tk;
-    const int nst = std::min(kMaxStages, (lim - rest) / stage);
-    if (nst < 2) return false;
-    out->nst = nst;
-    out->stage_bytes = stage;
-    out->off_gate = nst * stage;
+    const int ring = ((lim - rest) / 128) * 128;
+    if (ring < 2 * item) return false;
+    out->ring_cap = ring;
+    out->off_gate = ring;
     out->off_uni = out->off_gate + gate;
     out->off_tk = out->off_uni + uni;
     out->total = out->off_tk + tk;
@@ -917,8 +919,7 @@ extern "C" nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t
     a.ws.amax = reinterpret_cast<unsigned int*>(base + o.amax);
     a.ws.ypart = reinterpret_cast<float*>(base + o.ypart);
     a.ws.ysh = reinterpret_cast<float*>(base + o.ysh);
-    a.nst = sm.nst;
-    a.stage_bytes = sm.stage_bytes;
+    a.ring_cap = sm.ring_cap;
     a.off_gate = sm.off_gate;
     a.off_uni = sm.off_uni;
     a.off_tk = sm.off_tk;
