@@ -31,11 +31,13 @@ constexpr int kGThreads = 256;
 // ---------------------------------------------------------------- permute
 // offsets[e] = first position of expert e; positions of one expert keep the
 // pairs' order (t * k + j ascending). tiles[e] = first 64-position n-tile of
-// expert e (tiles[E] = their total; not written if tiles is null). Expert
-// ids outside [0, E) are counted as expert 0 and flagged in the error word.
+// expert e and chunks[e] the first 128-position chunk (tiles[E], chunks[E] =
+// their totals; either is skipped when null). Expert ids outside [0, E) are
+// counted as expert 0 and flagged in the error word.
 __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restrict__ idx, int P, int E,
                                                           int32_t* __restrict__ offsets, int32_t* __restrict__ tiles,
-                                                          int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+                                                          int32_t* __restrict__ chunks, int32_t* __restrict__ perm,
+                                                          int32_t* __restrict__ inv) {
     __shared__ int cnt[256];
     __shared__ int running[256];
     __shared__ int wcnt[kPermWarps][256];
@@ -53,16 +55,19 @@ __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restr
     for (int p = tid; p < P; p += kPermThreads) atomicAdd(&cnt[expert_of(p)], 1);
     __syncthreads();
     if (tid == 0) {
-        int off = 0, toff = 0;
+        int off = 0, toff = 0, coff = 0;
         for (int e = 0; e < E; ++e) {
             offsets[e] = off;
             if (tiles) tiles[e] = toff;
+            if (chunks) chunks[e] = coff;
             running[e] = off;
             off += cnt[e];
             toff += (cnt[e] + kGTile - 1) / kGTile;
+            coff += (cnt[e] + 127) / 128;
         }
         offsets[E] = off;
         if (tiles) tiles[E] = toff;
+        if (chunks) chunks[E] = coff;
     }
     for (int p0 = 0; p0 < P; p0 += kPermThreads) {
         for (int i = tid; i < kPermWarps * E; i += kPermThreads) (&wcnt[0][0])[(i / E) * 256 + i % E] = 0;

@@ -1,0 +1,518 @@
+// moe_grouped_tc.cuh - the grouped expert GEMMs of moe_expert_forward in W4A4
+// for more than 4 tokens (prefill and high-concurrency decode: "Let's
+// optimize Nemotron 3.5 Lightning - a worklog", Step 3) on the 5th-generation
+// tensor cores: tcgen05.mma kind::mxf4nvf4 multiplies the NVFP4 weights by the
+// NVFP4-quantised activations directly (E2M1 x E2M1 products, one E4M3 scale
+// per 16 elements on each side, FP32 accumulation in tensor memory), so no
+// operand is ever decoded on the CUDA cores.
+//
+//   D[m][n] = sum_k W[m][k] X[n][k]   (m: 128 weight rows of one expert,
+//                                      n: up to 128 positions of that expert)
+//   up:   act[n][m] = bf16(relu(D gw gx[n])^2), row amax of act[n] (atomic)
+//   down: y[n][m]   = gate[n] (D gw gx[n])
+//
+// Operand layout in shared memory (K-major, no swizzle): 8-row x 16-byte core
+// matrices, core matrices of one 8-row group adjacent along K at the
+// "leading" byte offset (LBO = rows x 16), 8-row groups at the "stride" byte
+// offset (SBO = 128). A 3-D TMA box {16 bytes, rows, 8 cores} of the row-major
+// [rows][K/2] code matrix lands exactly in that layout (one box = 256 k).
+//
+// Scale factors live in tensor memory. For M = 128 the MMA reads the scales of
+// row m from TMEM lane m, column sfa + m / 32 (byte b = 16-element block b of
+// the 64-k step), and those of output column n from lane 32 q + n % 32 of each
+// lane quarter q, column sfb + n / 32. Both are written with tcgen05.st by four
+// warps, one per lane quarter, from the row-major scale bytes staged in shared
+// memory.
+//
+// Warp roles (one CTA per SM, persistent over the work items):
+//   warp 0      producer: TMA for the codes, cp.async for the scale bytes
+//   warp 1      tensor memory allocation; lane 0 issues the MMAs
+//   warps 2-5   scale warps (lane quarter = warp % 4)
+//   warps 6-9   epilogue warps (lane quarter = warp % 4), accumulator in TMEM
+//               double-buffered so that an item's epilogue overlaps the next
+//               item's MMAs
+// Every wait is bounded (1 s); a role that gives up flags the error word and
+// the CTA abort flag, and the others stop at their next wait.
+#pragma once
+
+#include <cuda.h>
+
+#include "moe_decode.cuh"
+#include "moe_grouped.cuh"
+
+namespace nvfp4moe {
+
+constexpr int kTcThreads = 320;
+constexpr int kTcStages = 5;
+constexpr int kTcRows = 128;                     // weight rows per item (MMA M)
+constexpr int kTcPos = 128;                      // positions per item (MMA N <= 128)
+constexpr int kTcKStage = 256;                   // k per pipeline stage (4 MMAs of 64)
+constexpr int kTcCodeA = kTcRows * kTcKStage / 2;  // 16 KB
+constexpr int kTcCodeB = kTcPos * kTcKStage / 2;   // 16 KB (32 positions per 4 KB)
+constexpr int kTcScaleA = kTcRows * 16;            // 2 KB: 16 scale bytes per row
+constexpr int kTcScaleB = kTcPos * 16;
+constexpr int kTcOffB = kTcCodeA;
+constexpr int kTcOffSA = kTcOffB + kTcCodeB;
+constexpr int kTcOffSB = kTcOffSA + kTcScaleA;
+constexpr int kTcStageBytes = kTcOffSB + kTcScaleB;  // 36 KB
+constexpr int kTcSmem = kTcStages * kTcStageBytes;
+// tensor memory columns: two 128-column accumulators, then per stage 16
+// columns of A scales (4 steps x 4 lane quarters) and 16 of B scales
+// (4 steps x 4 column groups of 32)
+constexpr uint32_t kTcCols = 512;
+constexpr uint32_t kTcColSFA = 256;
+constexpr uint32_t kTcColSFB = kTcColSFA + 16 * kTcStages;
+static_assert(kTcColSFB + 16 * kTcStages <= kTcCols, "tensor memory columns");
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+// the mbarrier counts one arrival when every earlier cp.async of this thread has landed
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_alloc(uint32_t* dst, uint32_t ncols) {  // whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+// arrives once on the mbarrier when every earlier MMA of this thread is complete
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_st_x1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tc_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+                 "r"(v2), "r"(v3)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+        "[%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of tcgen05.mma: start address, leading and
+// stride byte offsets (all in 16-byte units), descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), both
+// K-major, E4M3 scales, M = 128, N = n.
+__device__ __forceinline__ uint32_t umma_idesc_mxf4(int n) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcRows >> 4) << 24);
+}
+
+// Bounded mbarrier wait that also gives up when the CTA abort flag is raised.
+__device__ __noinline__ bool tc_wait(uint64_t* b, uint32_t parity, volatile int* abort_s) {
+    if (mbar_try_wait(b, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_sleep(b, parity)) return true;
+        if (*abort_s) return false;
+        if (globaltimer() - t0 > kWaitTimeoutNs) {
+            set_dev_error(kErrWaitFull);
+            *abort_s = 1;
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- arguments
+// A segment is one weight tensor over its positions: the routed experts
+// (positions grouped by expert) or the shared expert (all tokens in order).
+struct TcSeg {
+    int nexp, M, K;          // experts, weight rows per expert, reduction length (K % 64 == 0)
+    const int32_t* offsets;  // [nexp + 1] position range of each expert; null: one range [0, npos)
+    const int32_t* chunks;   // [nexp + 1] prefix sums of ceil(n_e / 128) (with offsets)
+    int npos;
+    const uint8_t* a_scales;  // [nexp * M][K / 16] E4M3
+    const float* a_global;    // [nexp]
+    const uint8_t* b_scales;  // [b_rows][b_spitch] E4M3 (b_spitch % 16 == 0)
+    int b_spitch, b_rows;
+    const float* b_global;  // [b_rows] row globals of the quantised B rows
+    uint16_t* act;          // up: [positions][M] bf16
+    unsigned int* amax;     // up: [positions] row amax bits
+    float* y;               // down: [positions][M] FP32
+    const float* gate;      // down: topk_w of each pair (null: 1)
+    const int32_t* perm;    // position -> pair
+};
+
+struct TcArgs {
+    CUtensorMap a_map[2];     // weight codes: 3-D {16, nexp * M, K / 32}, box {16, 128, 8}
+    CUtensorMap b_map[2][4];  // B codes: 3-D {16, b_rows, K / 32}, box {16, 32 (g + 1), 8}
+    TcSeg seg[2];
+    int nseg;
+};
+
+struct TcItem {
+    int seg, e, row0, n, mt;
+};
+
+__device__ __forceinline__ int tc_seg_items(const TcSeg& s) {
+    const int MT = (s.M + kTcRows - 1) / kTcRows;
+    const int nch = s.offsets ? __ldg(s.chunks + s.nexp) : (s.npos + kTcPos - 1) / kTcPos;
+    return nch * MT;
+}
+
+// Item i: m-major inside a chunk of positions, so that consecutive items (on
+// neighbouring CTAs at about the same time) share their B rows in L2.
+__device__ __forceinline__ TcItem tc_item(const TcArgs& a, int i, int items0) {
+    TcItem it;
+    it.seg = i < items0 ? 0 : 1;
+    if (it.seg) i -= items0;
+    const TcSeg& s = a.seg[it.seg];
+    const int MT = (s.M + kTcRows - 1) / kTcRows;
+    const int ch = i / MT;
+    it.mt = i - ch * MT;
+    if (s.offsets) {
+        int lo = 0, hi = s.nexp;  // chunks[lo] <= ch < chunks[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(s.chunks + mid) <= ch) lo = mid;
+            else hi = mid;
+        }
+        it.e = lo;
+        it.row0 = __ldg(s.offsets + lo) + (ch - __ldg(s.chunks + lo)) * kTcPos;
+        it.n = min(kTcPos, __ldg(s.offsets + lo + 1) - it.row0);
+    } else {
+        it.e = 0;
+        it.row0 = ch * kTcPos;
+        it.n = min(kTcPos, s.npos - it.row0);
+    }
+    return it;
+}
+
+// ---------------------------------------------------------------- the GEMM
+template <int KIND>
+__global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_constant__ TcArgs a) {
+    extern __shared__ __align__(128) uint8_t tc_smem[];
+    uint8_t* const smem = tc_smem;
+    __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], sfready[kTcStages];
+    __shared__ __align__(8) uint64_t dfull[2], dempty[2], drain;
+    __shared__ uint32_t tmem_s;
+    __shared__ int abort_s;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&full[s], 33);  // the producer's expect_tx + one cp.async arrival per lane
+            mbar_init(&empty[s], 1);
+            mbar_init(&sfready[s], 4);
+        }
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(&dfull[d], 1);
+            mbar_init(&dempty[d], 4);
+        }
+        mbar_init(&drain, 1);
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tc_alloc(&tmem_s, kTcCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_s;
+    volatile int* ab = &abort_s;
+    const int items0 = tc_seg_items(a.seg[0]);
+    const int total = items0 + (a.nseg > 1 ? tc_seg_items(a.seg[1]) : 0);
+
+    if (warp == 0) {
+        // ---- producer
+        int g = 0;
+        int uses[kTcStages];
+#pragma unroll
+        for (int s = 0; s < kTcStages; ++s) uses[s] = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+            const TcItem it = tc_item(a, i, items0);
+            const TcSeg& s = a.seg[it.seg];
+            const int nstage = ((s.K >> 6) + 3) >> 2, ng = (it.n + 31) >> 5;
+            const int arow0 = it.e * s.M + it.mt * kTcRows;
+            const int arows = s.nexp * s.M, sp = s.K >> 4;
+            for (int ks = 0; ks < nstage; ++ks, ++g) {
+                const int st = g % kTcStages;
+                bool w = true;
+                if (lane == 0 && g >= kTcStages) w = tc_wait(&empty[st], ((g / kTcStages) - 1) & 1, ab);
+                if (!__shfl_sync(0xffffffffu, w, 0)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* base = smem + (size_t)st * kTcStageBytes;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)(kTcCodeA + ng * 4096));
+                    tma_load_3d(base, &a.a_map[it.seg], 0, arow0, ks * 8, &full[st]);
+                    tma_load_3d(base + kTcOffB, &a.b_map[it.seg][ng - 1], 0, it.row0, ks * 8, &full[st]);
+                }
+                // A scales: 128 rows x 16 bytes in 4-byte pieces (the rows of
+                // the caller's scale matrix are only 4-byte aligned)
+                for (int q = lane; q < kTcRows * 4; q += 32) {
+                    const int r = q >> 2, byte = ks * 16 + 4 * (q & 3), row = arow0 + r;
+                    const bool in = row < arows && byte < sp;
+                    cp_async4(base + kTcOffSA + 4 * q, in ? s.a_scales + (size_t)row * sp + byte : s.a_scales,
+                              in ? 4 : 0);
+                }
+                // B scales: 32 ng rows x 16 bytes
+                for (int r = lane; r < 32 * ng; r += 32) {
+                    const int row = it.row0 + r;
+                    const bool in = row < s.b_rows;
+                    cp_async16(base + kTcOffSB + 16 * r,
+                               in ? s.b_scales + (size_t)row * s.b_spitch + ks * 16 : s.b_scales, in ? 16 : 0);
+                }
+                cp_async_mbar_arrive(&full[st]);
+                uses[st] += 1;
+            }
+        }
+        // nothing may still be landing in shared memory when the CTA exits
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < kTcStages; ++s)
+                if (uses[s] > 0 && !mbar_wait_bounded(&full[s], (uses[s] - 1) & 1)) set_dev_error(kErrWaitDrain);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issue
+        if (lane == 0) {
+            int g = 0, n_it = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
+                const TcItem it = tc_item(a, i, items0);
+                const TcSeg& s = a.seg[it.seg];
+                const int nks = s.K >> 6, nstage = (nks + 3) >> 2, ng = (it.n + 31) >> 5;
+                const int db = n_it & 1;
+                if (n_it >= 2 && !tc_wait(&dempty[db], ((n_it >> 1) - 1) & 1, ab)) break;
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_mxf4(32 * ng);
+                const uint32_t dcol = tmem + 128u * db;
+                for (int ks = 0; ks < nstage; ++ks, ++g) {
+                    const int st = g % kTcStages;
+                    const uint32_t par = (g / kTcStages) & 1;
+                    if (!tc_wait(&full[st], par, ab) || !tc_wait(&sfready[st], par, ab)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sbase = smem_u32(smem + (size_t)st * kTcStageBytes);
+                    const int nk = min(4, nks - 4 * ks);
+                    for (int kk = 0; kk < nk; ++kk) {
+                        const uint64_t ad = umma_desc(sbase + 4096u * kk, 2048u, 128u);
+                        const uint64_t bd = umma_desc(sbase + kTcOffB + 1024u * ng * kk, 512u * ng, 128u);
+                        tc_mma_mxf4(dcol, ad, bd, idesc, tmem + kTcColSFA + 16u * st + 4u * kk,
+                                    tmem + kTcColSFB + 16u * st + 4u * kk, ks > 0 || kk > 0);
+                    }
+                    tc_commit(&empty[st]);  // stage (and its scale columns) free once these MMAs are done
+                }
+                if (!ok) break;
+                tc_commit(&dfull[db]);
+            }
+            // every MMA of this CTA is complete before the tensor memory is released
+            tc_commit(&drain);
+            if (!mbar_wait_bounded(&drain, 0)) set_dev_error(kErrWaitDrain);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ---- scale factors -> tensor memory (lane quarter q)
+        const int q = warp & 3;
+        const uint32_t lb = (uint32_t)(32 * q) << 16;
+        int g = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+            const TcItem it = tc_item(a, i, items0);
+            const TcSeg& s = a.seg[it.seg];
+            const int nstage = ((s.K >> 6) + 3) >> 2, ng = (it.n + 31) >> 5;
+            for (int ks = 0; ks < nstage; ++ks, ++g) {
+                const int st = g % kTcStages;
+                bool w = true;
+                if (lane == 0) w = tc_wait(&full[st], (g / kTcStages) & 1, ab);
+                if (!__shfl_sync(0xffffffffu, w, 0)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* base = smem + (size_t)st * kTcStageBytes;
+                // A: row 32 q + lane, step kk -> column sfa(kk) + q
+                const uint4 sa = *reinterpret_cast<const uint4*>(base + kTcOffSA + 16 * (32 * q + lane));
+                const uint32_t ca = tmem + lb + kTcColSFA + 16u * st + q;
+                tc_st_x1(ca, sa.x);
+                tc_st_x1(ca + 4, sa.y);
+                tc_st_x1(ca + 8, sa.z);
+                tc_st_x1(ca + 12, sa.w);
+                // B: position 32 j + lane, step kk -> column sfb(kk) + j (every quarter)
+                uint4 sb[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    sb[j] = j < ng ? *reinterpret_cast<const uint4*>(base + kTcOffSB + 16 * (32 * j + lane))
+                                   : make_uint4(0, 0, 0, 0);
+                const uint32_t cb = tmem + lb + kTcColSFB + 16u * st;
+                tc_st_x4(cb, sb[0].x, sb[1].x, sb[2].x, sb[3].x);
+                tc_st_x4(cb + 4, sb[0].y, sb[1].y, sb[2].y, sb[3].y);
+                tc_st_x4(cb + 8, sb[0].z, sb[1].z, sb[2].z, sb[3].z);
+                tc_st_x4(cb + 12, sb[0].w, sb[1].w, sb[2].w, sb[3].w);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfready[st]);
+            }
+        }
+    } else {
+        // ---- epilogue (lane quarter q: weight rows 32 q .. 32 q + 31 of the item)
+        const int q = warp & 3;
+        const uint32_t lb = (uint32_t)(32 * q) << 16;
+        int n_it = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, ++n_it) {
+            const TcItem it = tc_item(a, i, items0);
+            const TcSeg& s = a.seg[it.seg];
+            const int db = n_it & 1;
+            bool w = true;
+            if (lane == 0) w = tc_wait(&dfull[db], (n_it >> 1) & 1, ab);
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            tc_fence_after();
+            const float gw = __ldg(s.a_global + it.e);
+            const int m = it.mt * kTcRows + 32 * q + lane;
+            const bool mv = m < s.M;
+            for (int c0 = 0; c0 < it.n; c0 += 16) {
+                uint32_t r[16];
+                tc_ld_x16(tmem + lb + 128u * db + c0, r);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int p = it.row0 + c0 + j;
+                    if (c0 + j >= it.n) break;
+                    const float v = __fmul_rn(__uint_as_float(r[j]), __fmul_rn(gw, __ldg(s.b_global + p)));
+                    if (KIND == kGroupedUp) {
+                        const float rl = fmaxf(v, 0.0f);
+                        const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
+                        if (mv) s.act[(size_t)p * s.M + m] = *reinterpret_cast<const uint16_t*>(&bv);
+                        const unsigned int mx =
+                            __reduce_max_sync(0xffffffffu, mv ? __float_as_uint(__bfloat162float(bv)) : 0u);
+                        if (lane == 0 && mx != 0u) atomicMax(s.amax + p, mx);
+                    } else {
+                        const float gt = s.gate ? __ldg(s.gate + __ldg(s.perm + p)) : 1.0f;
+                        if (mv) s.y[(size_t)p * s.M + m] = s.gate ? __fmul_rn(gt, v) : v;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[db]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tc_dealloc(tmem, kTcCols);
+    }
+}
+
+// ---------------------------------------------------------------- B operand rows
+// Row r of src (bf16 [K]) -> NVFP4 codes [K/2] (low nibble = even element) and
+// E4M3 scales [spitch] with the row's global g = amax / 2688 (amax given in
+// amax_bits[r], else of the row); rms_eps > 0 normalises the row first (the
+// same unit-weight RMS norm as the other paths). The row goes to row r of
+// codes / scales / gout and, when inv is given, also to rows inv[r k + j]
+// (j < k) of the position-order copy pcodes / pscales / pgout.
+__global__ void __launch_bounds__(kGThreads) k_quant_rows_tc(const uint16_t* __restrict__ src, int K, int nrows,
+                                                             float rms_eps, const unsigned int* __restrict__ amax_bits,
+                                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                             int spitch, float* __restrict__ gout,
+                                                             const int32_t* __restrict__ inv, int k,
+                                                             uint8_t* __restrict__ pcodes,
+                                                             uint8_t* __restrict__ pscales, float* __restrict__ pgout) {
+    extern __shared__ __align__(16) uint16_t row[];  // [K] bf16
+    __shared__ float red[kGThreads / 32];
+    __shared__ unsigned int amax_s;
+    __shared__ int dst_rows[kDecodeMaxK + 1];
+    const int r = blockIdx.x;
+    if (r >= nrows) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint16_t* s = src + (size_t)r * K;
+    for (int i = 8 * tid; i < K; i += 8 * kGThreads)
+        *reinterpret_cast<uint4*>(row + i) = __ldcg(reinterpret_cast<const uint4*>(s + i));
+    if (tid == 0) amax_s = 0u;
+    const int ncopy = inv ? k : 0;
+    if (tid <= ncopy) dst_rows[tid] = tid == 0 ? r : __ldg(inv + (size_t)r * k + tid - 1);
+    __syncthreads();
+    if (rms_eps > 0.0f) {
+        float ss = 0.0f;
+        for (int i = tid; i < K; i += kGThreads) {
+            const float x = __uint_as_float(static_cast<uint32_t>(row[i]) << 16);
+            ss = __fmaf_rn(x, x, ss);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kGThreads / 32; ++w) sum = __fadd_rn(sum, red[w]);
+        const float inv_rms = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, static_cast<float>(K)), rms_eps)));
+        __syncthreads();
+        for (int i = tid; i < K; i += kGThreads) {
+            const __nv_bfloat16 b =
+                __float2bfloat16_rn(__fmul_rn(__uint_as_float(static_cast<uint32_t>(row[i]) << 16), inv_rms));
+            row[i] = *reinterpret_cast<const uint16_t*>(&b);
+        }
+        __syncthreads();
+    }
+    float g;
+    if (amax_bits) {
+        g = __fdiv_rn(__uint_as_float(__ldcg(amax_bits + r)), 2688.0f);
+    } else {
+        float mx = 0.0f;
+        for (int i = tid; i < K; i += kGThreads)
+            mx = fmaxf(mx, fabsf(__uint_as_float(static_cast<uint32_t>(row[i]) << 16)));
+        mx = warp_max(mx);
+        if (lane == 0) atomicMax(&amax_s, __float_as_uint(mx));
+        __syncthreads();
+        g = __fdiv_rn(__uint_as_float(amax_s), 2688.0f);
+    }
+    if (tid <= ncopy) (tid == 0 ? gout : pgout)[dst_rows[tid]] = g;
+    for (int b = tid; b < (K >> 4); b += kGThreads) {
+        const uint4 u0 = *reinterpret_cast<const uint4*>(row + 16 * b);
+        const uint4 u1 = *reinterpret_cast<const uint4*>(row + 16 * b + 8);
+        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            v[2 * j] = __uint_as_float(w[j] << 16);
+            v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+        const QBlock qb = quantize_block16(v, g);
+        for (int c = 0; c <= ncopy; ++c) {
+            const size_t dr = static_cast<size_t>(dst_rows[c]);
+            uint8_t* cd = (c == 0 ? codes : pcodes) + dr * (K >> 1) + 8 * b;
+            *reinterpret_cast<uint2*>(cd) = make_uint2(qb.lo, qb.hi);
+            (c == 0 ? scales : pscales)[dr * spitch + b] = static_cast<uint8_t>(qb.scale);
+        }
+    }
+}
+
+}  // namespace nvfp4moe

@@ -13,6 +13,7 @@
 #include "lm_head.cuh"
 #include "moe_decode.cuh"
 #include "moe_grouped.cuh"
+#include "moe_grouped_tc.cuh"
 #include "moe_layer.cuh"
 #include "moe_stack.cuh"
 #include "quantize.cuh"
@@ -406,8 +407,13 @@ nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, 
 namespace {
 
 struct GroupedWsOffsets {
-    size_t offsets, tiles, perm, inv, xq, gx, act, amax, act_sh, amax_sh, aq, ga, aq_sh, gsh, ypart, ysh, total;
+    size_t offsets, tiles, perm, inv, xq, gx, act, amax, act_sh, amax_sh, aq, ga, aq_sh, gsh, ypart, ysh;
+    // tensor-core path (W4A4): 128-position chunk prefix, NVFP4 B rows
+    // (codes, then scales with a 16-byte pitch) in token and position order
+    size_t chunks, tq_c, tq_s, xp_c, xp_s, gxp, aq_c, aq_s, as_c, as_s;
+    size_t total;
 };
+inline int spitch16(int K) { return ((K / 16) + 15) & ~15; }
 
 GroupedWsOffsets grouped_ws(int T, int k, int E, int H, int I, int S) {
     GroupedWsOffsets o{};
@@ -434,6 +440,16 @@ GroupedWsOffsets grouped_ws(int T, int k, int E, int H, int I, int S) {
     o.gsh = take(4 * (size_t)T);
     o.ypart = take(4 * P * H);
     o.ysh = take(4 * (size_t)T * H);
+    o.chunks = take(4 * (size_t)(E + 1));
+    o.tq_c = take((size_t)T * H / 2);
+    o.tq_s = take((size_t)T * spitch16(H));
+    o.xp_c = take(P * H / 2);
+    o.xp_s = take(P * spitch16(H));
+    o.gxp = take(4 * P);
+    o.aq_c = take(P * I / 2);
+    o.aq_s = take(P * spitch16(I));
+    o.as_c = take((size_t)T * S / 2);
+    o.as_s = take((size_t)T * spitch16(S));
     o.total = off;
     return o;
 }
@@ -447,10 +463,176 @@ nvfp4_status launch_plain(Kernel kernel, int grid, int block, size_t smem, cudaS
     return launch_status();
 }
 
+// cuTensorMapEncodeTiled from the driver (no link-time dependency on libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 3-D view {16 bytes, rows, K / 32 core columns} of a row-major [rows][K/2]
+// NVFP4 code matrix; a box {16, box_rows, 8} lands as 8 core columns of
+// box_rows x 16 bytes each (the canonical K-major layout of tcgen05.mma).
+bool code_map(CUtensorMap* m, const void* codes, int64_t rows, int K, int box_rows) {
+    const EncodeTiledFn enc = encode_tiled();
+    if (!enc || !aligned(codes, 16) || (K % 64) != 0 || rows < 1) return false;
+    const cuuint64_t dims[3] = {16, (cuuint64_t)rows, (cuuint64_t)(K / 32)};
+    const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), 16};
+    const cuuint32_t box[3] = {16, (cuuint32_t)box_rows, 8};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(codes), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool seg_maps(TcArgs& ta, int s, const void* a_codes, int64_t a_rows, const void* b_codes, int64_t b_rows, int K) {
+    if (!code_map(&ta.a_map[s], a_codes, a_rows, K, kTcRows)) return false;
+    for (int g = 0; g < 4; ++g)
+        if (!code_map(&ta.b_map[s][g], b_codes, b_rows, K, 32 * (g + 1))) return false;
+    return true;
+}
+
+// W4A4 grouped path on the tensor cores (tcgen05 kind::mxf4nvf4).
+bool tc_path_ok(const moe_layer_weights* w) {
+    const int H = w->hidden, I = w->inter, S = w->shared_inter;
+    if (H % 64 || I % 64 || S % 64) return false;
+    const void* p[] = {w->up_codes, w->down_codes, w->shared_up.codes, w->shared_down.codes};
+    for (const void* q : p)
+        if (!aligned(q, 16)) return false;
+    const void* sc[] = {w->up_scales, w->down_scales, w->shared_up.scales, w->shared_down.scales};
+    for (const void* q : sc)
+        if (!aligned(q, 4)) return false;
+    return encode_tiled() != nullptr && dyn_smem_limit(k_grouped_tc<kGroupedUp>) >= kTcSmem &&
+           dyn_smem_limit(k_grouped_tc<kGroupedDown>) >= kTcSmem;
+}
+
+nvfp4_status grouped_forward_tc(const moe_layer_weights* w, const void* hidden, const int32_t* topk_idx,
+                                const float* topk_w, int T, int k, float rms_eps, const void* residual, void* out,
+                                uint8_t* ws, cudaStream_t stream) {
+    const int E = w->num_experts, H = w->hidden, I = w->inter, S = w->shared_inter;
+    const int P = T * k;
+    const GroupedWsOffsets o = grouped_ws(T, k, E, H, I, S);
+    auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+    auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    auto b16 = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
+    auto u32 = [&](size_t off) { return reinterpret_cast<unsigned int*>(ws + off); };
+    auto u8 = [&](size_t off) { return ws + off; };
+
+    k_permute<<<1, kPermThreads, 0, stream>>>(topk_idx, P, E, i32(o.offsets), nullptr, i32(o.chunks), i32(o.perm),
+                                              i32(o.inv));
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaMemsetAsync(ws + o.amax, 0, o.xq - o.amax, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    // a1: token rows -> NVFP4 B rows, in token order and once per (token, choice) in position order
+    k_quant_rows_tc<<<T, kGThreads, (size_t)H * 2, stream>>>(static_cast<const uint16_t*>(hidden), H, T, rms_eps,
+                                                             nullptr, u8(o.tq_c), u8(o.tq_s), spitch16(H), f32(o.gx),
+                                                             i32(o.inv), k, u8(o.xp_c), u8(o.xp_s), f32(o.gxp));
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+
+    const int grid = num_sms();
+    // a3 + a5 (up): routed experts over their positions, the shared expert over all tokens
+    TcArgs ta{};
+    ta.nseg = 2;
+    TcSeg& ru = ta.seg[0];
+    ru.nexp = E;
+    ru.M = I;
+    ru.K = H;
+    ru.offsets = i32(o.offsets);
+    ru.chunks = i32(o.chunks);
+    ru.a_scales = w->up_scales;
+    ru.a_global = w->up_global;
+    ru.b_scales = u8(o.xp_s);
+    ru.b_spitch = spitch16(H);
+    ru.b_rows = P;
+    ru.b_global = f32(o.gxp);
+    ru.act = b16(o.act);
+    ru.amax = u32(o.amax);
+    TcSeg& su = ta.seg[1];
+    su.nexp = 1;
+    su.M = S;
+    su.K = H;
+    su.npos = T;
+    su.a_scales = w->shared_up.scales;
+    su.a_global = w->shared_up.global_scale;
+    su.b_scales = u8(o.tq_s);
+    su.b_spitch = spitch16(H);
+    su.b_rows = T;
+    su.b_global = f32(o.gx);
+    su.act = b16(o.act_sh);
+    su.amax = u32(o.amax_sh);
+    if (!seg_maps(ta, 0, w->up_codes, (int64_t)E * I, u8(o.xp_c), P, H) ||
+        !seg_maps(ta, 1, w->shared_up.codes, S, u8(o.tq_c), T, H))
+        return NVFP4_ERR_CUDA;
+    k_grouped_tc<kGroupedUp><<<grid, kTcThreads, kTcSmem, stream>>>(ta);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    // a1 on the intermediate rows (row amax from the up epilogue)
+    k_quant_rows_tc<<<P, kGThreads, (size_t)I * 2, stream>>>(b16(o.act), I, P, 0.0f, u32(o.amax), u8(o.aq_c),
+                                                             u8(o.aq_s), spitch16(I), f32(o.ga), nullptr, 0, nullptr,
+                                                             nullptr, nullptr);
+    k_quant_rows_tc<<<T, kGThreads, (size_t)S * 2, stream>>>(b16(o.act_sh), S, T, 0.0f, u32(o.amax_sh),
+                                                             u8(o.as_c), u8(o.as_s), spitch16(S), f32(o.gsh), nullptr,
+                                                             0, nullptr, nullptr, nullptr);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    // a4 + a5 (down): gate-weighted rows per position, shared rows per token
+    TcArgs td{};
+    td.nseg = 2;
+    TcSeg& rd = td.seg[0];
+    rd.nexp = E;
+    rd.M = H;
+    rd.K = I;
+    rd.offsets = i32(o.offsets);
+    rd.chunks = i32(o.chunks);
+    rd.a_scales = w->down_scales;
+    rd.a_global = w->down_global;
+    rd.b_scales = u8(o.aq_s);
+    rd.b_spitch = spitch16(I);
+    rd.b_rows = P;
+    rd.b_global = f32(o.ga);
+    rd.y = f32(o.ypart);
+    rd.gate = topk_w;
+    rd.perm = i32(o.perm);
+    TcSeg& sd = td.seg[1];
+    sd.nexp = 1;
+    sd.M = H;
+    sd.K = S;
+    sd.npos = T;
+    sd.a_scales = w->shared_down.scales;
+    sd.a_global = w->shared_down.global_scale;
+    sd.b_scales = u8(o.as_s);
+    sd.b_spitch = spitch16(S);
+    sd.b_rows = T;
+    sd.b_global = f32(o.gsh);
+    sd.y = f32(o.ysh);
+    if (!seg_maps(td, 0, w->down_codes, (int64_t)E * H, u8(o.aq_c), P, I) ||
+        !seg_maps(td, 1, w->shared_down.codes, H, u8(o.as_c), T, S))
+        return NVFP4_ERR_CUDA;
+    k_grouped_tc<kGroupedDown><<<grid, kTcThreads, kTcSmem, stream>>>(td);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    // a6: combine + residual
+    const int n4 = T * (H / 4);
+    const int cgrid = std::min((n4 + 255) / 256, num_sms() * 8);
+    k_combine<<<cgrid, 256, 0, stream>>>(f32(o.ysh), f32(o.ypart), i32(o.inv), static_cast<const uint16_t*>(residual),
+                                         static_cast<uint16_t*>(out), T, H, k);
+    return launch_status();
+}
+
 nvfp4_status grouped_forward(const moe_layer_weights* w, const void* hidden, const int32_t* topk_idx,
                              const float* topk_w, int T, int k, bool w4a4, float rms_eps, const void* residual,
                              void* out, uint8_t* ws, cudaStream_t stream) {
     const int E = w->num_experts, H = w->hidden, I = w->inter, S = w->shared_inter;
+    if (w4a4 && k <= kDecodeMaxK && tc_path_ok(w)) return grouped_forward_tc(w, hidden, topk_idx, topk_w, T, k, rms_eps, residual, out, ws,
+                                                         stream);
     const int P = T * k;
     const GroupedWsOffsets o = grouped_ws(T, k, E, H, I, S);
     auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
@@ -460,7 +642,7 @@ nvfp4_status grouped_forward(const moe_layer_weights* w, const void* hidden, con
     auto u32 = [&](size_t off) { return reinterpret_cast<unsigned int*>(ws + off); };
 
     // a7: pairs grouped by expert
-    k_permute<<<1, kPermThreads, 0, stream>>>(topk_idx, P, E, i32(o.offsets), i32(o.tiles), i32(o.perm),
+    k_permute<<<1, kPermThreads, 0, stream>>>(topk_idx, P, E, i32(o.offsets), i32(o.tiles), nullptr, i32(o.perm),
                                               i32(o.inv));
     if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
     // amax words start at zero (amax and amax_sh are adjacent)
@@ -563,7 +745,7 @@ extern "C" nvfp4_status moe_permute(const int32_t* topk_idx, int32_t T, int32_t 
     if (!topk_idx || !offsets || !perm || !inv) return NVFP4_ERR_INVALID_ARG;
     if (T < 1 || k < 1 || E < 1 || k > E) return NVFP4_ERR_INVALID_ARG;
     if (E > 256 || (int64_t)T * k > (int64_t)1 << 28) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    k_permute<<<1, kPermThreads, 0, stream>>>(topk_idx, T * k, E, offsets, tile_offsets, perm, inv);
+    k_permute<<<1, kPermThreads, 0, stream>>>(topk_idx, T * k, E, offsets, tile_offsets, nullptr, perm, inv);
     return launch_status();
 }
 
