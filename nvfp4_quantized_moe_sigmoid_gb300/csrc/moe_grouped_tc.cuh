@@ -11,21 +11,25 @@
 //   up:   act[n][m] = bf16(relu(D gw gx[n])^2), row amax of act[n] (atomic)
 //   down: y[n][m]   = gate[n] (D gw gx[n])
 //
-// Operand layout in shared memory (K-major, no swizzle): 8-row x 16-byte core
-// matrices, core matrices of one 8-row group adjacent along K at the
-// "leading" byte offset (LBO = rows x 16), 8-row groups at the "stride" byte
-// offset (SBO = 128). A 3-D TMA box {16 bytes, rows, 8 cores} of the row-major
-// [rows][K/2] code matrix lands exactly in that layout (one box = 256 k).
+// Operand layout in shared memory: K-major with the 128-byte swizzle. Each
+// row holds 256 k (128 bytes), rows in 1024-byte atoms of 8, and 16-byte chunk
+// c of row r stored at chunk c ^ (r % 8); descriptor: stride between 8-row
+// groups 1024 bytes, and the 64-k step s starts 32 s bytes into the row. A 2-D
+// TMA box {128 bytes, rows} of the row-major [rows][K/2] code matrix with the
+// 128-byte swizzle lands exactly in that layout (whole 128-byte rows per
+// request; a 16-byte-wide box of the unswizzled layout limits the copy engine
+// to 16-byte requests).
 //
 // Scale factors live in tensor memory. For M = 128 the MMA reads the scales of
 // row m from TMEM lane m, column sfa + m / 32 (byte b = 16-element block b of
 // the 64-k step), and those of output column n from lane 32 q + n % 32 of each
 // lane quarter q, column sfb + n / 32. Both are written with tcgen05.st by four
-// warps, one per lane quarter, from the row-major scale bytes staged in shared
-// memory.
+// warps, one per lane quarter, from row-major scale bytes in shared memory
+// (the weights' per item, the activations' per stage).
 //
 // Warp roles (one CTA per SM, persistent over the work items):
-//   warp 0      producer: TMA for the codes, cp.async for the scale bytes
+//   warp 0      producer: TMA for the codes, a bulk copy per item for the
+//               weight scales, cp.async for the activation scales
 //   warp 1      tensor memory allocation; lane 0 issues the MMAs
 //   warps 2-5   scale warps (lane quarter = warp % 4)
 //   warps 6-9   epilogue warps (lane quarter = warp % 4), accumulator in TMEM
@@ -43,33 +47,43 @@
 namespace nvfp4moe {
 
 constexpr int kTcThreads = 320;
-constexpr int kTcStages = 5;
+constexpr int kTcSlots = 8;  // pipeline stages in flight (mbarrier slots)
 constexpr int kTcRows = 128;                     // weight rows per item (MMA M)
 constexpr int kTcPos = 128;                      // positions per item (MMA N <= 128)
 constexpr int kTcKStage = 256;                   // k per pipeline stage (4 MMAs of 64)
 constexpr int kTcCodeA = kTcRows * kTcKStage / 2;  // 16 KB
 constexpr int kTcCodeB = kTcPos * kTcKStage / 2;   // 16 KB (32 positions per 4 KB)
-constexpr int kTcScaleA = kTcRows * 16;            // 2 KB: 16 scale bytes per row
-constexpr int kTcScaleB = kTcPos * 16;
+// A pipeline stage: [A codes 16 KB][B codes ng x 4 KB][B scales ng x 512 B]
+// for an item with ng groups of 32 positions, rounded up to the 1024-byte
+// swizzle atom; stages of any size are packed in issue order into a byte ring
+// over the rest of shared memory (one that would cross the end starts again
+// at its beginning), so that items with few positions keep more stages in
+// flight.
 constexpr int kTcOffB = kTcCodeA;
-constexpr int kTcOffSA = kTcOffB + kTcCodeB;
-constexpr int kTcOffSB = kTcOffSA + kTcScaleA;
-constexpr int kTcStageBytes = kTcOffSB + kTcScaleB;  // 36 KB
-constexpr int kTcSmem = kTcStages * kTcStageBytes;
-// tensor memory columns: two 128-column accumulators, then per stage 16
+__host__ __device__ constexpr int tc_stage_bytes(int ng) { return (kTcCodeA + ng * (4096 + 512) + 1023) & ~1023; }
+// The weight scales of an item (128 rows x K/16 bytes, contiguous in the
+// caller's matrix) arrive in one bulk copy into one of two per-item blocks:
+// the rows are only 4-byte aligned, so a per-stage copy would take 512
+// separate 4-byte requests. 16 bytes of slack after the block (the last row's
+// final step may read past it; those words are never used).
+constexpr int kTcScBlk = 30720;
+constexpr int kTcOffScBlk = 0;
+constexpr int kTcOffRing = 2 * kTcScBlk;  // a multiple of 1024
+constexpr int kTcSmemSlack = 1024;        // the kernel aligns its dynamic shared memory to 1024 bytes
+// tensor memory columns: two 128-column accumulators, then per slot 16
 // columns of A scales (4 steps x 4 lane quarters) and 16 of B scales
 // (4 steps x 4 column groups of 32)
 constexpr uint32_t kTcCols = 512;
 constexpr uint32_t kTcColSFA = 256;
-constexpr uint32_t kTcColSFB = kTcColSFA + 16 * kTcStages;
-static_assert(kTcColSFB + 16 * kTcStages <= kTcCols, "tensor memory columns");
+constexpr uint32_t kTcColSFB = kTcColSFA + 16 * kTcSlots;
+static_assert(kTcColSFB + 16 * kTcSlots <= kTcCols, "tensor memory columns");
 
 // ---------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
 // the mbarrier counts one arrival when every earlier cp.async of this thread has landed
@@ -120,11 +134,13 @@ __device__ __forceinline__ void tc_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor of tcgen05.mma: start address, leading and
-// stride byte offsets (all in 16-byte units), descriptor version 1, no swizzle.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+// Shared-memory matrix descriptor of tcgen05.mma for the K-major 128-byte
+// swizzled layout: start address (16-byte units), leading byte offset 16
+// (unused by this layout), stride byte offset 1024 (8-row groups),
+// descriptor version 1, layout type 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
 }
 // Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), both
 // K-major, E4M3 scales, M = 128, N = n.
@@ -133,16 +149,33 @@ __device__ __forceinline__ uint32_t umma_idesc_mxf4(int n) {
 }
 
 // Bounded mbarrier wait that also gives up when the CTA abort flag is raised.
+// It spins on the non-blocking test: each pipeline hand-off here is on the
+// critical path, and a suspended waiter resumes only some hundreds of
+// nanoseconds after the phase completes; the few waiting warps cost no issue
+// slots the tensor cores need.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __noinline__ bool tc_wait(uint64_t* b, uint32_t parity, volatile int* abort_s) {
-    if (mbar_try_wait(b, parity)) return true;
+    if (mbar_test_wait(b, parity)) return true;
     const unsigned long long t0 = globaltimer();
-    for (;;) {
-        if (mbar_try_wait_sleep(b, parity)) return true;
-        if (*abort_s) return false;
-        if (globaltimer() - t0 > kWaitTimeoutNs) {
-            set_dev_error(kErrWaitFull);
-            *abort_s = 1;
-            return false;
+    for (int it = 1;; ++it) {
+        if (mbar_test_wait(b, parity)) return true;
+        if ((it & 255) == 0) {
+            if (*abort_s) return false;
+            if (globaltimer() - t0 > kWaitTimeoutNs) {
+                set_dev_error(kErrWaitFull);
+                *abort_s = 1;
+                return false;
+            }
         }
     }
 }
@@ -168,15 +201,23 @@ struct TcSeg {
 };
 
 struct TcArgs {
-    CUtensorMap a_map[2];     // weight codes: 3-D {16, nexp * M, K / 32}, box {16, 128, 8}
-    CUtensorMap b_map[2][4];  // B codes: 3-D {16, b_rows, K / 32}, box {16, 32 (g + 1), 8}
+    CUtensorMap a_map[2];     // weight codes: 2-D {K / 2, nexp * M}, box {128, 128}, 128-byte swizzle
+    CUtensorMap b_map[2][4];  // B codes: 2-D {K / 2, b_rows}, box {128, 32 (g + 1)}, 128-byte swizzle
     TcSeg seg[2];
     int nseg;
+    int ring_cap;  // bytes of the stage ring (a multiple of 1024, >= 2 stages of 4 groups)
 };
 
 struct TcItem {
     int seg, e, row0, n, mt;
 };
+
+// Independent accumulators of an item: its 64-k steps go round-robin to nc
+// accumulators of 32 ng columns in the item's 128 (steps that accumulate
+// into one accumulator form a dependent chain, and at small N each MMA is
+// short enough for that chain's latency to set the pace); the epilogue adds
+// them in order.
+__device__ __forceinline__ int tc_chains(int ng, int nks) { return min(min(4 / ng, 4), nks); }
 
 __device__ __forceinline__ int tc_seg_items(const TcSeg& s) {
     const int MT = (s.M + kTcRows - 1) / kTcRows;
@@ -186,11 +227,11 @@ __device__ __forceinline__ int tc_seg_items(const TcSeg& s) {
 
 // Item i: m-major inside a chunk of positions, so that consecutive items (on
 // neighbouring CTAs at about the same time) share their B rows in L2.
-__device__ __forceinline__ TcItem tc_item(const TcArgs& a, int i, int items0) {
+__device__ __forceinline__ TcItem tc_item(const TcSeg* segs, int i, int items0) {
     TcItem it;
     it.seg = i < items0 ? 0 : 1;
     if (it.seg) i -= items0;
-    const TcSeg& s = a.seg[it.seg];
+    const TcSeg& s = segs[it.seg];
     const int MT = (s.M + kTcRows - 1) / kTcRows;
     const int ch = i / MT;
     it.mt = i - ch * MT;
@@ -215,15 +256,29 @@ __device__ __forceinline__ TcItem tc_item(const TcArgs& a, int i, int items0) {
 // ---------------------------------------------------------------- the GEMM
 template <int KIND>
 __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_constant__ TcArgs a) {
-    extern __shared__ __align__(128) uint8_t tc_smem[];
-    uint8_t* const smem = tc_smem;
-    __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], sfready[kTcStages];
+    extern __shared__ __align__(1024) uint8_t tc_smem[];
+    // the swizzled stages need 1024-byte aligned addresses
+    uint8_t* const smem = tc_smem + ((1024u - (smem_u32(tc_smem) & 1023u)) & 1023u);
+    __shared__ __align__(8) uint64_t full[kTcSlots], empty[kTcSlots], sfready[kTcSlots];
+    __shared__ uint32_t stage_off[kTcSlots];  // shared-memory offset of the slot's current stage
+    // producer bookkeeping (in shared memory: a run-time indexed local array
+    // lives in local memory, whose lines the streaming traffic evicts from L1)
+    __shared__ int p_uses[kTcSlots], p_vs[kTcSlots], p_scuses[2];
+    // the segment descriptors, read in every step of every role: from shared
+    // memory (a run-time indexed kernel parameter is a slow generic load)
+    __shared__ TcSeg segs[2];
+    // per epilogue warp: the item's column factors gw gx[p] and gates
+    __shared__ float ep_scale[4][kTcPos], ep_gate[4][kTcPos];
+    static_assert(sizeof(TcSeg) % 8 == 0, "TcSeg copy");
+    for (int i = threadIdx.x; i < (int)(2 * sizeof(TcSeg) / 8); i += blockDim.x)
+        reinterpret_cast<uint64_t*>(segs)[i] = reinterpret_cast<const uint64_t*>(a.seg)[i];
     __shared__ __align__(8) uint64_t dfull[2], dempty[2], drain;
+    __shared__ __align__(8) uint64_t scfull[2], scempty[2];  // per-item weight scale blocks
     __shared__ uint32_t tmem_s;
     __shared__ int abort_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < kTcSlots; ++s) {
             mbar_init(&full[s], 33);  // the producer's expect_tx + one cp.async arrival per lane
             mbar_init(&empty[s], 1);
             mbar_init(&sfready[s], 4);
@@ -231,6 +286,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
         for (int d = 0; d < 2; ++d) {
             mbar_init(&dfull[d], 1);
             mbar_init(&dempty[d], 4);
+            mbar_init(&scfull[d], 1);
+            mbar_init(&scempty[d], 4);
         }
         mbar_init(&drain, 1);
         abort_s = 0;
@@ -242,61 +299,98 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
     tc_fence_after();
     const uint32_t tmem = tmem_s;
     volatile int* ab = &abort_s;
-    const int items0 = tc_seg_items(a.seg[0]);
-    const int total = items0 + (a.nseg > 1 ? tc_seg_items(a.seg[1]) : 0);
+    const int items0 = tc_seg_items(segs[0]);
+    const int total = items0 + (a.nseg > 1 ? tc_seg_items(segs[1]) : 0);
 
     if (warp == 0) {
         // ---- producer
-        int g = 0;
-        int uses[kTcStages];
-#pragma unroll
-        for (int s = 0; s < kTcStages; ++s) uses[s] = 0;
+        // tensor maps into the copy engine's descriptor cache up front
+        if (lane < 5 * a.nseg) {
+            const CUtensorMap* tm = lane % 5 == 0 ? &a.a_map[lane / 5] : &a.b_map[lane / 5][lane % 5 - 1];
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+        }
+        int g = 0, n_it = 0, tail = 0, vhead = 0;
+        const int cap = a.ring_cap;
+        int* const uses = p_uses;
+        int* const vs = p_vs;
+        int* const scuses = p_scuses;
+        if (lane < kTcSlots) uses[lane] = vs[lane] = 0;
+        if (lane < 2) scuses[lane] = 0;
+        __syncwarp();
         bool ok = true;
-        for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-            const TcItem it = tc_item(a, i, items0);
-            const TcSeg& s = a.seg[it.seg];
+        for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
+            const TcItem it = tc_item(segs, i, items0);
+            const TcSeg& s = segs[it.seg];
             const int nstage = ((s.K >> 6) + 3) >> 2, ng = (it.n + 31) >> 5;
             const int arow0 = it.e * s.M + it.mt * kTcRows;
             const int arows = s.nexp * s.M, sp = s.K >> 4;
-            for (int ks = 0; ks < nstage; ++ks, ++g) {
-                const int st = g % kTcStages;
+            const uint8_t* const b_scales = s.b_scales;
+            const int b_rows = s.b_rows, b_spitch = s.b_spitch;
+            const CUtensorMap* const amap = &a.a_map[it.seg];
+            const CUtensorMap* const bmap = &a.b_map[it.seg][ng - 1];
+            // the item's weight scales: min(128, rows left) x K/16 bytes
+            {
+                const int b = n_it & 1;
                 bool w = true;
-                if (lane == 0 && g >= kTcStages) w = tc_wait(&empty[st], ((g / kTcStages) - 1) & 1, ab);
+                if (lane == 0 && n_it >= 2) w = tc_wait(&scempty[b], ((n_it >> 1) - 1) & 1, ab);
+                if (!__shfl_sync(0xffffffffu, w, 0)) break;
+                if (lane == 0) {
+                    const uint32_t bytes = (uint32_t)(min(kTcRows, arows - arow0) * sp);
+                    mbar_arrive_expect_tx(&scfull[b], bytes);
+                    bulk_g2s(smem + kTcOffScBlk + b * kTcScBlk, s.a_scales + (size_t)arow0 * sp, bytes, &scfull[b]);
+                }
+                if (lane == 0) scuses[b] += 1;
+            }
+            for (int ks = 0; ks < nstage; ++ks, ++g) {
+                const int st = g % kTcSlots;
+                const int size = tc_stage_bytes(ng);
+                int v = vhead;
+                if (v % cap + size > cap) v += cap - v % cap;
+                // release in issue order: the slot's previous stage and every
+                // older stage whose bytes this one overwrites
+                const int lim = v + size - cap;
+                bool w = true;
+                if (lane == 0) {
+                    while (tail < g && (tail <= g - kTcSlots || vs[tail % kTcSlots] < lim)) {
+                        w = tc_wait(&empty[tail % kTcSlots], (tail / kTcSlots) & 1, ab);
+                        if (!w) break;
+                        ++tail;
+                    }
+                }
                 if (!__shfl_sync(0xffffffffu, w, 0)) {
                     ok = false;
                     break;
                 }
-                uint8_t* base = smem + (size_t)st * kTcStageBytes;
+                tail = __shfl_sync(0xffffffffu, tail, 0);
+                if (lane == 0) vs[st] = v;  // read by lane 0 only
+                vhead = v + size;
+                const uint32_t off = (uint32_t)(kTcOffRing + v % cap);
+                uint8_t* base = smem + off;
                 if (lane == 0) {
+                    stage_off[st] = off;
                     mbar_arrive_expect_tx(&full[st], (uint32_t)(kTcCodeA + ng * 4096));
-                    tma_load_3d(base, &a.a_map[it.seg], 0, arow0, ks * 8, &full[st]);
-                    tma_load_3d(base + kTcOffB, &a.b_map[it.seg][ng - 1], 0, it.row0, ks * 8, &full[st]);
-                }
-                // A scales: 128 rows x 16 bytes in 4-byte pieces (the rows of
-                // the caller's scale matrix are only 4-byte aligned)
-                for (int q = lane; q < kTcRows * 4; q += 32) {
-                    const int r = q >> 2, byte = ks * 16 + 4 * (q & 3), row = arow0 + r;
-                    const bool in = row < arows && byte < sp;
-                    cp_async4(base + kTcOffSA + 4 * q, in ? s.a_scales + (size_t)row * sp + byte : s.a_scales,
-                              in ? 4 : 0);
+                    tma_load_2d(base, amap, ks * 128, arow0, &full[st]);
+                    tma_load_2d(base + kTcOffB, bmap, ks * 128, it.row0, &full[st]);
                 }
                 // B scales: 32 ng rows x 16 bytes
                 for (int r = lane; r < 32 * ng; r += 32) {
                     const int row = it.row0 + r;
-                    const bool in = row < s.b_rows;
-                    cp_async16(base + kTcOffSB + 16 * r,
-                               in ? s.b_scales + (size_t)row * s.b_spitch + ks * 16 : s.b_scales, in ? 16 : 0);
+                    const bool in = row < b_rows;
+                    cp_async16(base + kTcOffB + 4096 * ng + 16 * r,
+                               in ? b_scales + (size_t)row * b_spitch + ks * 16 : b_scales, in ? 16 : 0);
                 }
                 cp_async_mbar_arrive(&full[st]);
-                uses[st] += 1;
+                if (lane == 0) uses[st] += 1;
             }
         }
         // nothing may still be landing in shared memory when the CTA exits
         asm volatile("cp.async.wait_all;" ::: "memory");
         if (lane == 0) {
 #pragma unroll
-            for (int s = 0; s < kTcStages; ++s)
+            for (int s = 0; s < kTcSlots; ++s)
                 if (uses[s] > 0 && !mbar_wait_bounded(&full[s], (uses[s] - 1) & 1)) set_dev_error(kErrWaitDrain);
+            for (int b = 0; b < 2; ++b)  // the last scale block issued into each buffer
+                if (scuses[b] > 0 && !mbar_wait_bounded(&scfull[b], (scuses[b] - 1) & 1)) set_dev_error(kErrWaitDrain);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -305,29 +399,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
             int g = 0, n_it = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
-                const TcItem it = tc_item(a, i, items0);
-                const TcSeg& s = a.seg[it.seg];
+                const TcItem it = tc_item(segs, i, items0);
+                const TcSeg& s = segs[it.seg];
                 const int nks = s.K >> 6, nstage = (nks + 3) >> 2, ng = (it.n + 31) >> 5;
                 const int db = n_it & 1;
                 if (n_it >= 2 && !tc_wait(&dempty[db], ((n_it >> 1) - 1) & 1, ab)) break;
                 tc_fence_after();
                 const uint32_t idesc = umma_idesc_mxf4(32 * ng);
                 const uint32_t dcol = tmem + 128u * db;
+                const int nc = tc_chains(ng, nks);
                 for (int ks = 0; ks < nstage; ++ks, ++g) {
-                    const int st = g % kTcStages;
-                    const uint32_t par = (g / kTcStages) & 1;
+                    const int st = g % kTcSlots;
+                    const uint32_t par = (g / kTcSlots) & 1;
                     if (!tc_wait(&full[st], par, ab) || !tc_wait(&sfready[st], par, ab)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sbase = smem_u32(smem + (size_t)st * kTcStageBytes);
+                    const uint32_t sbase = smem_u32(smem + stage_off[st]);
                     const int nk = min(4, nks - 4 * ks);
                     for (int kk = 0; kk < nk; ++kk) {
-                        const uint64_t ad = umma_desc(sbase + 4096u * kk, 2048u, 128u);
-                        const uint64_t bd = umma_desc(sbase + kTcOffB + 1024u * ng * kk, 512u * ng, 128u);
-                        tc_mma_mxf4(dcol, ad, bd, idesc, tmem + kTcColSFA + 16u * st + 4u * kk,
-                                    tmem + kTcColSFB + 16u * st + 4u * kk, ks > 0 || kk > 0);
+                        const uint64_t ad = umma_desc_sw128(sbase + 32u * kk);
+                        const uint64_t bd = umma_desc_sw128(sbase + kTcOffB + 32u * kk);
+                        const int q = 4 * ks + kk;  // 64-k step of the item
+                        tc_mma_mxf4(dcol + 32u * ng * (q % nc), ad, bd, idesc, tmem + kTcColSFA + 16u * st + 4u * kk,
+                                    tmem + kTcColSFB + 16u * st + 4u * kk, q >= nc);
                     }
                     tc_commit(&empty[st]);  // stage (and its scale columns) free once these MMAs are done
                 }
@@ -343,33 +439,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
         // ---- scale factors -> tensor memory (lane quarter q)
         const int q = warp & 3;
         const uint32_t lb = (uint32_t)(32 * q) << 16;
-        int g = 0;
+        int g = 0, n_it = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-            const TcItem it = tc_item(a, i, items0);
-            const TcSeg& s = a.seg[it.seg];
+        for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
+            const TcItem it = tc_item(segs, i, items0);
+            const TcSeg& s = segs[it.seg];
             const int nstage = ((s.K >> 6) + 3) >> 2, ng = (it.n + 31) >> 5;
-            for (int ks = 0; ks < nstage; ++ks, ++g) {
-                const int st = g % kTcStages;
+            const int sp = s.K >> 4;
+            const int b = n_it & 1;
+            {
                 bool w = true;
-                if (lane == 0) w = tc_wait(&full[st], (g / kTcStages) & 1, ab);
+                if (lane == 0) w = tc_wait(&scfull[b], (n_it >> 1) & 1, ab);
+                if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            }
+            const uint8_t* scrow = smem + kTcOffScBlk + b * kTcScBlk + (size_t)(32 * q + lane) * sp;
+            for (int ks = 0; ks < nstage; ++ks, ++g) {
+                const int st = g % kTcSlots;
+                bool w = true;
+                if (lane == 0) w = tc_wait(&full[st], (g / kTcSlots) & 1, ab);
                 if (!__shfl_sync(0xffffffffu, w, 0)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* base = smem + (size_t)st * kTcStageBytes;
+                const uint8_t* base = smem + stage_off[st];
                 // A: row 32 q + lane, step kk -> column sfa(kk) + q
-                const uint4 sa = *reinterpret_cast<const uint4*>(base + kTcOffSA + 16 * (32 * q + lane));
+                const uint32_t* sw = reinterpret_cast<const uint32_t*>(scrow + 16 * ks);
                 const uint32_t ca = tmem + lb + kTcColSFA + 16u * st + q;
-                tc_st_x1(ca, sa.x);
-                tc_st_x1(ca + 4, sa.y);
-                tc_st_x1(ca + 8, sa.z);
-                tc_st_x1(ca + 12, sa.w);
+                tc_st_x1(ca, sw[0]);
+                tc_st_x1(ca + 4, sw[1]);
+                tc_st_x1(ca + 8, sw[2]);
+                tc_st_x1(ca + 12, sw[3]);
                 // B: position 32 j + lane, step kk -> column sfb(kk) + j (every quarter)
                 uint4 sb[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    sb[j] = j < ng ? *reinterpret_cast<const uint4*>(base + kTcOffSB + 16 * (32 * j + lane))
+                    sb[j] = j < ng ? *reinterpret_cast<const uint4*>(base + kTcOffB + 4096 * ng + 16 * (32 * j + lane))
                                    : make_uint4(0, 0, 0, 0);
                 const uint32_t cb = tmem + lb + kTcColSFB + 16u * st;
                 tc_st_x4(cb, sb[0].x, sb[1].x, sb[2].x, sb[3].x);
@@ -381,6 +485,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sfready[st]);
             }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(&scempty[b]);  // done with this item's scale block
         }
     } else {
         // ---- epilogue (lane quarter q: weight rows 32 q .. 32 q + 31 of the item)
@@ -388,8 +494,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
         const uint32_t lb = (uint32_t)(32 * q) << 16;
         int n_it = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ++n_it) {
-            const TcItem it = tc_item(a, i, items0);
-            const TcSeg& s = a.seg[it.seg];
+            const TcItem it = tc_item(segs, i, items0);
+            const TcSeg& s = segs[it.seg];
             const int db = n_it & 1;
             bool w = true;
             if (lane == 0) w = tc_wait(&dfull[db], (n_it >> 1) & 1, ab);
@@ -397,30 +503,61 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
             tc_fence_after();
             const float gw = __ldg(s.a_global + it.e);
             const int m = it.mt * kTcRows + 32 * q + lane;
+            // the item's column factors, every load in flight at once (one
+            // round trip per item instead of dependent loads per column)
+            {
+                float f[kTcPos / 32], gt[kTcPos / 32];
+#pragma unroll
+                for (int u = 0; u < kTcPos / 32; ++u) {
+                    const int c = lane + 32 * u;
+                    f[u] = c < it.n ? __ldg(s.b_global + it.row0 + c) : 0.0f;
+                    gt[u] = 1.0f;
+                    if (KIND == kGroupedDown && s.gate && c < it.n) gt[u] = __ldg(s.gate + __ldg(s.perm + it.row0 + c));
+                }
+#pragma unroll
+                for (int u = 0; u < kTcPos / 32; ++u) {
+                    ep_scale[q][lane + 32 * u] = __fmul_rn(gw, f[u]);
+                    ep_gate[q][lane + 32 * u] = gt[u];
+                }
+                __syncwarp();
+            }
             const bool mv = m < s.M;
+            const int ng = (it.n + 31) >> 5, nc = tc_chains(ng, s.K >> 6);
+            // this item's output pointers in registers (stores would otherwise
+            // make every read of the shared descriptor a reload)
+            const int M = s.M;
+            uint16_t* const act = s.act;
+            unsigned int* const amax = s.amax;
+            float* const yout = s.y;
+            const bool gated = s.gate != nullptr;
             for (int c0 = 0; c0 < it.n; c0 += 16) {
                 uint32_t r[16];
                 tc_ld_x16(tmem + lb + 128u * db + c0, r);
+                for (int c = 1; c < nc; ++c) {  // the other accumulators, added in order
+                    uint32_t r2[16];
+                    tc_ld_x16(tmem + lb + 128u * db + 32u * ng * c + c0, r2);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), __uint_as_float(r2[j])));
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int p = it.row0 + c0 + j;
                     if (c0 + j >= it.n) break;
-                    const float v = __fmul_rn(__uint_as_float(r[j]), __fmul_rn(gw, __ldg(s.b_global + p)));
+                    const float v = __fmul_rn(__uint_as_float(r[j]), ep_scale[q][c0 + j]);
                     if (KIND == kGroupedUp) {
                         const float rl = fmaxf(v, 0.0f);
                         const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
-                        if (mv) s.act[(size_t)p * s.M + m] = *reinterpret_cast<const uint16_t*>(&bv);
+                        if (mv) act[(size_t)p * M + m] = *reinterpret_cast<const uint16_t*>(&bv);
                         const unsigned int mx =
                             __reduce_max_sync(0xffffffffu, mv ? __float_as_uint(__bfloat162float(bv)) : 0u);
-                        if (lane == 0 && mx != 0u) atomicMax(s.amax + p, mx);
+                        if (lane == 0 && mx != 0u) atomicMax(amax + p, mx);
                     } else {
-                        const float gt = s.gate ? __ldg(s.gate + __ldg(s.perm + p)) : 1.0f;
-                        if (mv) s.y[(size_t)p * s.M + m] = s.gate ? __fmul_rn(gt, v) : v;
+                        if (mv) yout[(size_t)p * M + m] = gated ? __fmul_rn(ep_gate[q][c0 + j], v) : v;
                     }
                 }
             }
             tc_fence_before();
-            __syncwarp();
+            __syncwarp();  // also: this warp's column factors may be rewritten
             if (lane == 0) mbar_arrive(&dempty[db]);
         }
     }

@@ -241,18 +241,23 @@ nvfp4_status moe_route_topk(const void* hidden, const float* router_w, const flo
     if (T < 1 || H < 16 || E < 1 || k < 1 || k > E) return NVFP4_ERR_INVALID_ARG;
     if (H % 16 || E > 256 || k > 32) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(hidden, 16) || !aligned(router_w, 16)) return NVFP4_ERR_MISALIGNED;
-    constexpr int TT = 8;
-    const int lim = dyn_smem_limit(k_route<TT>);
-    const int hbytes = TT * H * 2;
-    const int nj = (E + kRouteCluster - 1) / kRouteCluster;  // gate rows of CTA rank 0
-    const int stage_w = hbytes + nj * H * 4 <= lim ? 1 : 0;
-    const int smem = hbytes + (stage_w ? nj * H * 4 : 0);
-    if (smem > lim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    const int tiles = (T + TT - 1) / TT;
-    return launch_pdl(k_route<TT>, tiles * kRouteCluster, kRouteWarps * 32, smem, stream,
-                      static_cast<const uint16_t*>(hidden), router_w, bias, T, H, E, k, rms_eps, stage_w,
-                      topk_idx, topk_w, static_cast<DecodePlan*>(nullptr), static_cast<__half*>(nullptr),
-                      static_cast<float*>(nullptr), 0);
+    // Small batches: the cluster's gate rows staged in shared memory. Large
+    // batches: gate rows read from L2 (where the 1.4 MB matrix stays), so that
+    // a CTA needs shared memory only for its token rows and many fit per SM.
+    auto launch = [&](auto kernel, int TT) {
+        const int lim = dyn_smem_limit(kernel);
+        const int hbytes = TT * H * 2;
+        const int nj = (E + kRouteCluster - 1) / kRouteCluster;  // gate rows of CTA rank 0
+        const int stage_w = T < 64 && hbytes + nj * H * 4 <= lim ? 1 : 0;
+        const int smem = hbytes + (stage_w ? nj * H * 4 : 0);
+        if (smem > lim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        const int tiles = (T + TT - 1) / TT;
+        return launch_pdl(kernel, tiles * kRouteCluster, kRouteWarps * 32, smem, stream,
+                          static_cast<const uint16_t*>(hidden), router_w, bias, T, H, E, k, rms_eps, stage_w,
+                          topk_idx, topk_w, static_cast<DecodePlan*>(nullptr), static_cast<__half*>(nullptr),
+                          static_cast<float*>(nullptr), 0);
+    };
+    return launch(k_route<8>, 8);
 }
 
 size_t moe_expert_forward_workspace_size(const moe_layer_weights* w, int32_t T, int32_t k,
@@ -482,18 +487,18 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// 3-D view {16 bytes, rows, K / 32 core columns} of a row-major [rows][K/2]
-// NVFP4 code matrix; a box {16, box_rows, 8} lands as 8 core columns of
-// box_rows x 16 bytes each (the canonical K-major layout of tcgen05.mma).
+// Row-major [rows][K/2] NVFP4 code matrix as a 2-D byte tensor; a box
+// {128 bytes, box_rows} with the 128-byte swizzle lands in the K-major
+// swizzled layout tcgen05.mma reads (256 k per box).
 bool code_map(CUtensorMap* m, const void* codes, int64_t rows, int K, int box_rows) {
     const EncodeTiledFn enc = encode_tiled();
     if (!enc || !aligned(codes, 16) || (K % 64) != 0 || rows < 1) return false;
-    const cuuint64_t dims[3] = {16, (cuuint64_t)rows, (cuuint64_t)(K / 32)};
-    const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), 16};
-    const cuuint32_t box[3] = {16, (cuuint32_t)box_rows, 8};
-    const cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(codes), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+    const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -502,6 +507,12 @@ bool seg_maps(TcArgs& ta, int s, const void* a_codes, int64_t a_rows, const void
     for (int g = 0; g < 4; ++g)
         if (!code_map(&ta.b_map[s][g], b_codes, b_rows, K, 32 * (g + 1))) return false;
     return true;
+}
+
+// Stage-ring bytes of k_grouped_tc: the shared memory the two scale blocks leave.
+int tc_ring_cap() {
+    const int lim = std::min(dyn_smem_limit(k_grouped_tc<kGroupedUp>), dyn_smem_limit(k_grouped_tc<kGroupedDown>));
+    return ((lim - kTcOffRing - kTcSmemSlack) / 1024) * 1024;
 }
 
 // W4A4 grouped path on the tensor cores (tcgen05 kind::mxf4nvf4).
@@ -513,9 +524,11 @@ bool tc_path_ok(const moe_layer_weights* w) {
         if (!aligned(q, 16)) return false;
     const void* sc[] = {w->up_scales, w->down_scales, w->shared_up.scales, w->shared_down.scales};
     for (const void* q : sc)
-        if (!aligned(q, 4)) return false;
-    return encode_tiled() != nullptr && dyn_smem_limit(k_grouped_tc<kGroupedUp>) >= kTcSmem &&
-           dyn_smem_limit(k_grouped_tc<kGroupedDown>) >= kTcSmem;
+        if (!aligned(q, 16)) return false;
+    // one item's weight scales (128 rows x K/16 bytes) plus slack fit a block
+    for (int K : {H, I, S})
+        if (kTcRows * (K / 16) + 16 > kTcScBlk) return false;
+    return encode_tiled() != nullptr && tc_ring_cap() >= 2 * tc_stage_bytes(4);
 }
 
 nvfp4_status grouped_forward_tc(const moe_layer_weights* w, const void* hidden, const int32_t* topk_idx,
@@ -574,7 +587,8 @@ nvfp4_status grouped_forward_tc(const moe_layer_weights* w, const void* hidden, 
     if (!seg_maps(ta, 0, w->up_codes, (int64_t)E * I, u8(o.xp_c), P, H) ||
         !seg_maps(ta, 1, w->shared_up.codes, S, u8(o.tq_c), T, H))
         return NVFP4_ERR_CUDA;
-    k_grouped_tc<kGroupedUp><<<grid, kTcThreads, kTcSmem, stream>>>(ta);
+    ta.ring_cap = tc_ring_cap();
+    k_grouped_tc<kGroupedUp><<<grid, kTcThreads, kTcSmemSlack + kTcOffRing + ta.ring_cap, stream>>>(ta);
     if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
     // a1 on the intermediate rows (row amax from the up epilogue)
     k_quant_rows_tc<<<P, kGThreads, (size_t)I * 2, stream>>>(b16(o.act), I, P, 0.0f, u32(o.amax), u8(o.aq_c),
@@ -617,7 +631,8 @@ nvfp4_status grouped_forward_tc(const moe_layer_weights* w, const void* hidden, 
     if (!seg_maps(td, 0, w->down_codes, (int64_t)E * H, u8(o.aq_c), P, I) ||
         !seg_maps(td, 1, w->shared_down.codes, H, u8(o.as_c), T, S))
         return NVFP4_ERR_CUDA;
-    k_grouped_tc<kGroupedDown><<<grid, kTcThreads, kTcSmem, stream>>>(td);
+    td.ring_cap = tc_ring_cap();
+    k_grouped_tc<kGroupedDown><<<grid, kTcThreads, kTcSmemSlack + kTcOffRing + td.ring_cap, stream>>>(td);
     if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
     // a6: combine + residual
     const int n4 = T * (H / 4);
