@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only this many MoE layers of the config (small cases for ncu captures); 0 = all")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -237,6 +239,14 @@ def launches_per_step(st, T, L, lm_head):
     return n
 
 
+# DRAM bytes (read + write) per W4A4 layer of k_moe_stack at one token, from
+# one ncu capture of the current kernel (profiles/k_moe_stack_w4a4_t1_2layer_
+# ncu_full.md: 92.72 MB read + 3.25 MB written over two layers; traffic grows
+# with the layers, one weight stream each). Reset to None when the kernel
+# changes and re-measure.
+STACK_T1_W4A4_DRAM_BYTES_PER_LAYER = (92720384 + 3246848) / 2
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args, ws, rank, local):
     import torch
@@ -249,7 +259,10 @@ def run_ours(args, ws, rank, local):
     from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
     from gen import configs, fill
 
-    c = configs.shape(args.config)
+    c = dict(configs.shape(args.config))
+    if args.layers > 0 and args.layers < c["layers"]:
+        c["layers"] = args.layers
+        c["name"] = "%s_first%dlayers" % (c["name"], args.layers)  # a profiling case, not the benchmark
     T, L, E, H, I, S, K, V = c["T"], c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], c["V"]
     st = MoEDecodeStack(L, E, H, I, S, K, T, w4a4=c["w4a4"], V=V if c["lm_head"] else None,
                         rms_eps=c["rms_eps"])
@@ -323,9 +336,12 @@ def run_ours(args, ws, rank, local):
     else:
         call_b = statistics.mean(rf.expert_call_bytes(T, u, H, I, S, K) for u in uniques)
         kname = "moe_expert_forward (up + down kernels, per layer)"
+    traffic = None
+    if st.path == "stack" and T == 1 and c["w4a4"]:
+        traffic = STACK_T1_W4A4_DRAM_BYTES_PER_LAYER * L
     roof = {"bound": "hbm", "kernel": kname,
             "achieved": call_b / (call_avg_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
-            "frac": None, "traffic": None, "algorithmic_bytes": call_b,
+            "frac": None, "traffic": traffic, "algorithmic_bytes": call_b,
             "avg_launch_us": call_avg_ms * 1e3, "peak_kind": peak_kind}
     roof["frac"] = roof["achieved"] / peak
     extra = {}
