@@ -244,7 +244,7 @@ def launches_per_step(st, T, L, lm_head):
 # ncu_full.md: 92.72 MB read + 3.25 MB written over two layers; traffic grows
 # with the layers, one weight stream each). Reset to None when the kernel
 # changes and re-measure.
-STACK_T1_W4A4_DRAM_BYTES_PER_LAYER = (92720384 + 3246848) / 2
+STACK_T1_W4A4_DRAM_BYTES_PER_LAYER = None  # kernel changed since the last capture
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -337,7 +337,7 @@ def run_ours(args, ws, rank, local):
         call_b = statistics.mean(rf.expert_call_bytes(T, u, H, I, S, K) for u in uniques)
         kname = "moe_expert_forward (up + down kernels, per layer)"
     traffic = None
-    if st.path == "stack" and T == 1 and c["w4a4"]:
+    if st.path == "stack" and T == 1 and c["w4a4"] and STACK_T1_W4A4_DRAM_BYTES_PER_LAYER is not None:
         traffic = STACK_T1_W4A4_DRAM_BYTES_PER_LAYER * L
     roof = {"bound": "hbm", "kernel": kname,
             "achieved": call_b / (call_avg_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",

@@ -116,6 +116,7 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 // Wait until *p >= target. False if the wait expired (flags the error word and
 // the abort flag) or another CTA raised the abort flag.
 __device__ __noinline__ bool wait_geq(const int* p, int target, int* abort_g) {
+    if (ld_acquire_gpu(p) >= target) return true;  // no timer read when nothing to wait for
     const unsigned long long t0 = globaltimer();
     for (int it = 0;; ++it) {
         if (ld_acquire_gpu(p) >= target) return true;
@@ -133,6 +134,7 @@ __device__ __noinline__ bool wait_geq(const int* p, int target, int* abort_g) {
 
 __device__ __noinline__ bool mbar_wait_abortable(uint64_t* b, uint32_t parity, volatile int* abort_s,
                                                 unsigned int err = kErrWaitFull) {
+    if (mbar_try_wait(b, parity)) return true;  // no timer read and no suspension when the phase is done
     const unsigned long long t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait_sleep(b, parity)) return true;
@@ -162,6 +164,7 @@ constexpr int kGroups = 4;
 constexpr int kGroupWarps = kConsumerWarps / kGroups;
 constexpr int kSlots = 16;
 static_assert(kConsumerWarps % kGroups == 0 && kSlots % kGroups == 0, "ring groups");
+static_assert((kSlots & (kSlots - 1)) == 0, "slot index by mask");
 
 struct BRing {
     uint64_t full[kSlots];
@@ -169,8 +172,6 @@ struct BRing {
     uint32_t off[kSlots];  // byte offset of the slot's current item
     int vs[kSlots];        // its virtual start (producer side)
     int uses[kSlots];      // fills of the slot (producer side)
-    int vhead;             // virtual end of the last item placed
-    int tail;              // oldest item not yet seen released
     // partial tiles handed from ranks 1.. of a group to its rank 0, double
     // buffered by the group's item parity; warp w >= kGroups uses w - kGroups
     float4 xred[kConsumerWarps - kGroups][2][32];
@@ -221,34 +222,6 @@ struct StackCta {
 
 __device__ __forceinline__ bool cta_abort(StackCta& c) { return *static_cast<volatile int*>(&c.abort_s) != 0; }
 __device__ __forceinline__ void set_cta_abort(StackCta& c) { *static_cast<volatile int*>(&c.abort_s) = 1; }
-
-// Producer: place and issue local item li. False if it gave up waiting.
-__device__ __noinline__ bool bring_fill(StackCta& c, int li, const uint8_t* codes, const uint8_t* scales, int K) {
-    BRing& r = c.br;
-    const int cap = c.ring_cap;
-    const int cb = 8 * K, size = 9 * K;
-    int v = r.vhead;
-    if (v % cap + size > cap) v += cap - v % cap;
-    const int lim = v + size - cap;  // older items starting below this must be released
-#pragma unroll 1
-    while (r.tail < li && (r.tail <= li - kSlots || r.vs[r.tail % kSlots] < lim)) {
-        const int t = r.tail;
-        if (!mbar_wait_abortable(&r.empty[t % kSlots], static_cast<uint32_t>((t / kSlots) & 1), &c.abort_s,
-                                 kErrWaitEmpty))
-            return false;
-        r.tail = t + 1;
-    }
-    const int s = li % kSlots;
-    r.vs[s] = v;
-    r.off[s] = static_cast<uint32_t>(v % cap);
-    r.vhead = v + size;
-    uint8_t* dst = c.ring_base + v % cap;
-    mbar_arrive_expect_tx(&r.full[s], static_cast<uint32_t>(size));
-    bulk_g2s(dst, codes, static_cast<uint32_t>(cb), &r.full[s]);
-    bulk_g2s(dst + cb, scales, static_cast<uint32_t>(K), &r.full[s]);
-    r.uses[s] += 1;
-    return true;
-}
 
 // Consumers: item li by its warp group (see the ring above); the group's
 // rank-0 warp gets lead = 1 and the finished 16 x 8 tile, ok = 0 in every
@@ -846,18 +819,54 @@ __device__ __noinline__ bool st_down_tiles(const StackArgs& a, StackCta& c, int 
 
 // ---------------------------------------------------------------- producer
 
+// The producer is one thread among twelve busy warps, so its per-tile work is
+// kept short: the ring position lives in registers (phys = vhead mod cap,
+// advanced without divisions), the fill is inlined, and the routed tiles'
+// addresses advance without divisions.
 __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
     const int H = a.H, I = a.I, S = a.S, RI = I >> 4, RH = H >> 4;
     const int G = c.G, b = c.b;
-    int pli = 0;
+    BRing& r = c.br;
+    const int cap = c.ring_cap;
+    uint8_t* const rbase = c.ring_base;
+    int pli = 0, tail = 0, vhead = 0, phys = 0;
     bool alive = true;
+    // item pli: a 16-row tile of K columns (9 K bytes), placed after the
+    // previous one (or at offset 0 if it would cross the end), once the item
+    // that last used its slot and every older item whose bytes it overwrites
+    // are released (waited for in issue order)
     auto fill = [&](const uint8_t* codes, const uint8_t* scales, int K) {
         if (!alive) return;
-        if (cta_abort(c) || !bring_fill(c, pli, codes, scales, K)) {
+        if (cta_abort(c)) {
             alive = false;
-            set_cta_abort(c);
             return;
         }
+        const int size = 9 * K;
+        if (phys + size > cap) {
+            vhead += cap - phys;
+            phys = 0;
+        }
+        const int lim = vhead + size - cap;
+#pragma unroll 1
+        while (tail < pli && (tail <= pli - kSlots || r.vs[tail & (kSlots - 1)] < lim)) {
+            if (!mbar_wait_abortable(&r.empty[tail & (kSlots - 1)], static_cast<uint32_t>((tail / kSlots) & 1),
+                                     &c.abort_s, kErrWaitEmpty)) {
+                alive = false;
+                set_cta_abort(c);
+                return;
+            }
+            ++tail;
+        }
+        const int s = pli & (kSlots - 1);
+        r.vs[s] = vhead;
+        r.off[s] = static_cast<uint32_t>(phys);
+        uint8_t* dst = rbase + phys;
+        mbar_arrive_expect_tx(&r.full[s], static_cast<uint32_t>(size));
+        bulk_g2s(dst, codes, static_cast<uint32_t>(8 * K), &r.full[s]);
+        bulk_g2s(dst + 8 * K, scales, static_cast<uint32_t>(K), &r.full[s]);
+        r.uses[s] += 1;
+        vhead += size;
+        phys += size;
         ++pli;
     };
     // router rows of this CTA's experts and the layer's bias (E * 4 bytes,
@@ -876,8 +885,8 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
     auto issue_shared_up = [&](int l) {
         const StackLayer& P = a.layer[l];
 #pragma unroll 1
-        for (int r = c.su_b; r < c.su_e; ++r)
-            fill(P.shu_codes + (size_t)16 * r * (H >> 1), P.shu_scales + (size_t)16 * r * (H >> 4), H);
+        for (int sr = c.su_b; sr < c.su_e; ++sr)
+            fill(P.shu_codes + (size_t)16 * sr * (H >> 1), P.shu_scales + (size_t)16 * sr * (H >> 4), H);
     };
     issue_gate(0);
     issue_shared_up(0);
@@ -890,18 +899,38 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
         if (l + 1 < a.L) issue_gate(l + 1);
         const StackLayer& P = a.layer[l];
         const int NU = c.plan.U * RI, ND = c.plan.U * RH;
+        {  // routed up tiles: tile rr of unique expert u
+            const uint8_t* const uc = P.up_codes;
+            const uint8_t* const us = P.up_scales;
+            const int i0 = share_begin32(NU, b, G), n = share_begin32(NU, b + 1, G) - i0;
+            int u = i0 / RI, rr = i0 - u * RI;
 #pragma unroll 1
-        for (int i = share_begin32(NU, b, G), e = share_begin32(NU, b + 1, G); i < e; ++i) {
-            const int64_t row = (int64_t)c.plan.expert[i / RI] * I + 16 * (i % RI);
-            fill(P.up_codes + row * (H >> 1), P.up_scales + row * (H >> 4), H);
+            for (int j = 0; j < n; ++j) {
+                const int64_t row = (int64_t)c.plan.expert[u] * I + 16 * rr;
+                fill(uc + row * (H >> 1), us + row * (H >> 4), H);
+                if (++rr == RI) {
+                    rr = 0;
+                    ++u;
+                }
+            }
         }
 #pragma unroll 1
-        for (int r = c.sd_b; r < c.sd_e; ++r)
-            fill(P.shd_codes + (size_t)16 * r * (S >> 1), P.shd_scales + (size_t)16 * r * (S >> 4), S);
+        for (int sr = c.sd_b; sr < c.sd_e; ++sr)
+            fill(P.shd_codes + (size_t)16 * sr * (S >> 1), P.shd_scales + (size_t)16 * sr * (S >> 4), S);
+        {  // routed down tiles
+            const uint8_t* const dc = P.down_codes;
+            const uint8_t* const ds = P.down_scales;
+            const int i0 = share_begin32(ND, b, G), n = share_begin32(ND, b + 1, G) - i0;
+            int u = i0 / RH, rr = i0 - u * RH;
 #pragma unroll 1
-        for (int i = share_begin32(ND, b, G), e = share_begin32(ND, b + 1, G); i < e; ++i) {
-            const int64_t row = (int64_t)c.plan.expert[i / RH] * H + 16 * (i % RH);
-            fill(P.down_codes + row * (I >> 1), P.down_scales + row * (I >> 4), I);
+            for (int j = 0; j < n; ++j) {
+                const int64_t row = (int64_t)c.plan.expert[u] * H + 16 * rr;
+                fill(dc + row * (I >> 1), ds + row * (I >> 4), I);
+                if (++rr == RH) {
+                    rr = 0;
+                    ++u;
+                }
+            }
         }
         mbar_arrive(&c.qbar);  // the plan of layer l is no longer read here
         if (l + 1 < a.L) issue_shared_up(l + 1);
@@ -1001,8 +1030,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant
             mbar_init(&c.br.empty[s], kGroupWarps);
             c.br.uses[s] = 0;
         }
-        c.br.vhead = 0;
-        c.br.tail = 0;
         mbar_init(&c.gbar, 1);
         mbar_init(&c.pbar, 1);
         mbar_init(&c.qbar, 1);
