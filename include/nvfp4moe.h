@@ -18,7 +18,9 @@
  *               FP32; MoE and shared-expert GEMMs NVFP4) and Deployment
  *               (Blackwell runs W4A4).
  *
- * NVFP4 tensor (the canonical layout every call takes), for a matrix of n rows
+ * NVFP4 tensor (the canonical layout every call takes; moe_stack_forward also
+ * reads a column-block copy of its down weights, nvfp4_colblock_layout), for
+ * a matrix of n rows
  * and k columns (k % 16 == 0, element (r, c) = row r, reduction index c):
  *   codes  uint8 [n][k/2]   E2M1 codes, element 2j in the low nibble of byte j
  *   scales uint8 [n][k/16]  E4M3 (OCP "FN") scale of each 16-element block
@@ -260,11 +262,21 @@ nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w
  * runs as one persistent cooperative kernel with one CTA per SM: the layers'
  * steps meet through counters in the workspace instead of kernel boundaries,
  * and the next layer's router rows and shared-expert tiles are staged while
- * the current layer still waits on its routing.
+ * the current layer still waits on its routing. Each CTA takes an even share
+ * of the layer's 16-row units of the experts' intermediate dimension and
+ * computes, per unit, 16 rows of W_up and then the matching 16 columns of
+ * W_down (a split-K partial of the expert's output); so the down weights are
+ * read from a column-block copy (nvfp4_colblock_layout), and the per-CTA
+ * partials are added in a fixed order.
  *   layers     host array [L] of per-layer device pointers (copied into the
  *              launch; not read after the call returns); every layer has the
- *              same E, H, I, S with H, I, S % 64 == 0, E % 8 == 0 and E <= 256;
- *              router_w, router_bias, up_global and down_global 16-byte aligned
+ *              same E, H, I, S with H, I, S % 64 == 0, H <= 3072, E % 8 == 0
+ *              and E <= 256; router_w, router_bias, up_global, down_global and
+ *              the two column-block copies 16-byte aligned. The row-major
+ *              down weights in moe are not read: down_colblock must hold
+ *              nvfp4_colblock_layout of down_codes / down_scales (batch E,
+ *              rows H, cols I) and shared_down_colblock that of shared_down
+ *              (batch 1, rows H, cols S).
  *   L          1 .. NVFP4MOE_STACK_MAX_LAYERS
  *   hidden_in  device bf16 [T][H] h_0, 16-byte aligned
  *   T, k       1 <= T <= 4, 1 <= k <= min(E, 16)
@@ -276,9 +288,11 @@ nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w
  *              left zeroed by every completed call; calls that share it must
  *              not overlap.
  * Summation orders differ from moe_layer_forward's (router dot products, the
- * split of tile reductions), so results agree with it to FP32 rounding, not
- * bit for bit. Returns NVFP4_ERR_UNSUPPORTED_SHAPE for shapes outside the
- * limits above or when one CTA per SM does not fit, NVFP4_ERR_CUDA if the
+ * split of tile reductions, the down projection split over 16-column blocks),
+ * so results agree with it to FP32 rounding, not bit for bit; repeated calls
+ * give identical bits. Returns NVFP4_ERR_UNSUPPORTED_SHAPE for shapes outside
+ * the limits above, when one CTA per SM does not fit or when a CTA's share of
+ * a layer exceeds 32 units, NVFP4_ERR_CUDA if the
  * cooperative launch fails; a device wait that expires ends every CTA of the
  * call early and is reported by nvfp4_last_device_error (NVFP4_ERR_TIMEOUT).
  */
@@ -287,7 +301,33 @@ typedef struct {
     moe_layer_weights moe;
     const float* router_w;    /* [E][H], 16-byte aligned */
     const float* router_bias; /* [E], 16-byte aligned */
+    const uint8_t* down_colblock;        /* [E][I/16][9 H] (nvfp4_colblock_layout) */
+    const uint8_t* shared_down_colblock; /* [S/16][9 H] */
 } moe_stack_layer;
+
+/*
+ * nvfp4_colblock_layout - the column-block copy of a batch of NVFP4 matrices
+ * that moe_stack_forward reads its down weights from. Not an operation of
+ * the pages: a storage order of the same codes and scales (the NVFP4 tensor
+ * above, [worklog] Step 1: group size 16), so that one scale block of every
+ * row (16 consecutive columns) sits together with the next rows' blocks.
+ *   codes   device [batch][rows][cols/2] (two E2M1 codes a byte, low nibble
+ *           first), scales device [batch][rows][cols/16] (E4M3), as every
+ *           NVFP4 matrix here
+ *   out     device [batch][cols/16][9 rows] bytes, 16-byte aligned: block c
+ *           of matrix b holds columns 16c .. 16c + 15 of every row, codes
+ *           [rows/32][32][8], then scales [rows/32][8][4]. Pair p covers rows
+ *           32p .. 32p + 31 as two 16-row tiles m = 0, 1; byte 8L + 4m + i of
+ *           its codes, L = 4g + q, holds row 32p + 16m + g (i = 0, 1) or that
+ *           row + 8 (i = 2, 3), columns 16c + 4q + 2 (i & 1) and the next one;
+ *           byte 4g + 2m + j of its scales holds the block scale of row
+ *           32p + 16m + g + 8 j.
+ *   rows % 32 == 0, cols % 16 == 0, batch >= 1; out must not overlap the
+ *   inputs. NVFP4_ERR_INVALID_ARG / NVFP4_ERR_UNSUPPORTED_SHAPE /
+ *   NVFP4_ERR_MISALIGNED (out) before anything is launched.
+ */
+nvfp4_status nvfp4_colblock_layout(const uint8_t* codes, const uint8_t* scales, int64_t batch, int64_t rows,
+                                   int64_t cols, uint8_t* out, cudaStream_t stream);
 
 size_t moe_stack_forward_workspace_size(const moe_stack_layer* layers, int32_t L, int32_t T, int32_t k,
                                         nvfp4_act_mode mode);

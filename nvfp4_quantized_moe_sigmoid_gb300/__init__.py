@@ -17,7 +17,7 @@ __all__ = ["NVFP4Matrix", "MoELayer", "NVFP4Error", "nvfp4_quantize", "moe_route
            "moe_expert_forward_workspace_size", "moe_expert_forward_workspace_init",
            "moe_expert_forward", "moe_expert_forward_noalloc", "moe_layer_forward",
            "moe_layer_forward_workspace_size", "moe_stack_forward", "moe_stack_forward_workspace_size",
-           "make_stack_workspace", "moe_permute", "lm_head_gemv", "lm_head_forward",
+           "make_stack_workspace", "nvfp4_colblock_layout", "moe_permute", "lm_head_gemv", "lm_head_forward",
            "make_lm_head_workspace",
            "nvfp4_status_string", "nvfp4_last_device_error",
            "W4A16", "W4A4", "PER_TENSOR", "PER_ROW", "GIVEN", "lib"]
@@ -99,6 +99,10 @@ class MoELayer:
         self.down_global = torch.empty(E, dtype=torch.float32, device=device)
         self.shared_up = NVFP4Matrix.empty(S, H, device)
         self.shared_down = NVFP4Matrix.empty(H, S, device)
+        # column-block copies of the down weights for moe_stack_forward,
+        # made on first use from the weights at that time (stack_layout)
+        self.down_cb = None
+        self.shared_down_cb = None
         self._c = None
 
     def expert_up(self, e):
@@ -106,6 +110,17 @@ class MoELayer:
 
     def expert_down(self, e):
         return NVFP4Matrix(self.down_codes[e], self.down_scales[e], self.down_global[e:e + 1])
+
+    def stack_layout(self, stream=None):
+        """(Re)writes the column-block copies of the down weights that
+        moe_stack_forward reads; call again after changing the down weights."""
+        E, H, I, S = self.E, self.H, self.I, self.S
+        if self.down_cb is None:
+            self.down_cb = torch.empty((E, I // 16, 9 * H), dtype=torch.uint8, device=self.down_codes.device)
+            self.shared_down_cb = torch.empty((S // 16, 9 * H), dtype=torch.uint8, device=self.down_codes.device)
+        nvfp4_colblock_layout(self.down_codes, self.down_scales, out=self.down_cb, stream=stream)
+        nvfp4_colblock_layout(self.shared_down.codes, self.shared_down.scales, out=self.shared_down_cb,
+                              stream=stream)
 
     def c(self):
         if self._c is None:
@@ -215,11 +230,29 @@ def moe_layer_forward(layer: MoELayer, hidden, k, mode=W4A4, residual=None, out=
     return out, topk_idx, topk_w
 
 
+def nvfp4_colblock_layout(codes, scales, out=None, stream=None):
+    """Column-block copy of NVFP4 matrices codes [..][rows][cols/2], scales
+    [..][rows][cols/16] (uint8, CUDA): out [batch][cols/16][9 rows] uint8."""
+    rows, half = codes.shape[-2], codes.shape[-1]
+    cols = 2 * half
+    batch = codes.numel() // (rows * half)
+    if out is None:
+        out = torch.empty((batch, cols // 16, 9 * rows), dtype=torch.uint8, device=codes.device)
+    st = _L.nvfp4_colblock_layout(_ptr(codes.contiguous()), _ptr(scales.contiguous()), batch, rows, cols,
+                                  _ptr(out), _stream(stream))
+    _check(st, "nvfp4_colblock_layout")
+    return out
+
+
 def _stack_layers(layers):
-    """ctypes array of moe_stack_layer for a list of MoELayer (cached on the list's layers)."""
+    """ctypes array of moe_stack_layer for a list of MoELayer; makes each
+    layer's column-block down weights on first use."""
     arr = (_abi.MoeStackLayer * len(layers))()
     for i, Lw in enumerate(layers):
-        arr[i] = _abi.MoeStackLayer(Lw.c(), Lw.router_w.data_ptr(), Lw.router_b.data_ptr())
+        if Lw.down_cb is None:
+            Lw.stack_layout()
+        arr[i] = _abi.MoeStackLayer(Lw.c(), Lw.router_w.data_ptr(), Lw.router_b.data_ptr(), Lw.down_cb.data_ptr(),
+                                    Lw.shared_down_cb.data_ptr())
     return arr
 
 

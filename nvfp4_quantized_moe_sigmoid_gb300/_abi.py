@@ -14,7 +14,7 @@ EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_siz
            "moe_layer_forward", "moe_layer_forward_workspace_size",
            "moe_stack_forward", "moe_stack_forward_workspace_size", "moe_permute",
            "lm_head_gemv", "lm_head_forward", "lm_head_forward_workspace_size",
-           "nvfp4_status_string", "nvfp4_last_device_error"]
+           "nvfp4_colblock_layout", "nvfp4_status_string", "nvfp4_last_device_error"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20  # NVFP4MOE_NOALLOC_SCRATCH_BYTES
 STACK_MAX_LAYERS = 32  # NVFP4MOE_STACK_MAX_LAYERS
@@ -36,7 +36,8 @@ class MoeLayerWeights(ctypes.Structure):
 
 
 class MoeStackLayer(ctypes.Structure):
-    _fields_ = [("moe", MoeLayerWeights), ("router_w", P), ("router_bias", P)]
+    _fields_ = [("moe", MoeLayerWeights), ("router_w", P), ("router_bias", P),
+                ("down_colblock", P), ("shared_down_colblock", P)]
 
 
 _lib = None
@@ -72,6 +73,8 @@ def load(path: str = LIB_PATH):
     L.moe_stack_forward.argtypes = [ctypes.POINTER(MoeStackLayer), I32, P, I32, I32, ctypes.c_int, ctypes.c_float,
                                     P, P, P, P, ctypes.c_size_t, P]
     L.moe_stack_forward.restype = ctypes.c_int
+    L.nvfp4_colblock_layout.argtypes = [P, P, I64, I64, I64, P, P]
+    L.nvfp4_colblock_layout.restype = ctypes.c_int
     L.moe_permute.argtypes = [P, I32, I32, I32, P, P, P, P, P]
     L.moe_permute.restype = ctypes.c_int
     L.moe_expert_forward_noalloc.argtypes = [ctypes.POINTER(MoeLayerWeights), P, P, P, I32, I32,

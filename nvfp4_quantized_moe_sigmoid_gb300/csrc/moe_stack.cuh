@@ -9,23 +9,34 @@
 // and the steps meet through per-layer counters in the workspace:
 //
 //   per layer l, every CTA:
-//     1. wait until every 16-row tile of h_l is final (counter); load h_l;
+//     1. wait until every CTA has written its share of h_l (counter); load h_l;
 //     2. x = RMSNorm(h_l); B operand of the up tiles (NVFP4 in W4A4);
 //     3. router logits of this CTA's experts (gate rows staged in shared
 //        memory during the previous layer) -> workspace, count them;
 //     4. wait for all E logits; sigmoid + bias top-k (rank per expert, every
 //        CTA computes the same selection), the step plan (unique experts);
-//        from here the producer streams the routed tiles;
-//     5. its share of the shared expert's up tiles (staged during the
-//        previous layer, computed while the routed tiles are in flight):
-//        relu^2 -> bf16 rows + row amax (W4A4);
-//     6. its share of the routed up tiles (per-expert done counters);
-//     7. wait for the experts whose down tiles it owns; quantise their
-//        intermediate rows with the now final row amax (W4A4) as its B operand;
-//     8. its share of the shared and routed down tiles -> gate-weighted FP32
-//        partial rows; each tile counts its contribution to its 16 output
-//        rows, and the warp that brings the last one (U routed + 1 shared)
-//        combines them: h_{l+1} = bf16(shared + sum_j gate_j y_j + h_l).
+//        from here the producer streams the routed weights;
+//     5. its units: a unit is 16 rows of one expert's intermediate dimension
+//        (the shared expert's S/16 units, then the routed experts' I/16 each,
+//        split evenly over the CTAs). Per unit, the up tile (16 rows of W_up)
+//        gives 16 intermediate values relu^2 -> bf16, kept in shared memory,
+//        and their amax is posted per (expert, token) (W4A4);
+//     6. wait until every up tile of the experts it holds units of is done
+//        (per-expert counters): the row amax, and with it the per-tensor
+//        global of the intermediate row, is final. Quantise each unit's 16
+//        values (one NVFP4 block) as a down B operand;
+//     7. per unit, the matching 16 columns of W_down (all H rows; a
+//        column-block copy of W_down keeps them contiguous) times the unit's
+//        block: a split-K partial of the expert's output. Partials of one
+//        expert add up raw and are scaled once (gate x globals) into the CTA's
+//        FP32 partial of the layer output, written to the workspace; count it;
+//     8. wait for every CTA's partial; add, for its share of the H rows, the
+//        G partials in CTA order and the residual: h_{l+1} = bf16(sum + h_l).
+//
+// The down weights of a unit depend only on the plan, so they stream while
+// the up tiles are still computing, and no intermediate row leaves the CTA
+// that computed it: across CTAs only the per-row amax and the H-wide partial
+// sums meet.
 //
 // One producer thread streams every tile the CTA owns through the staging
 // ring in consumption order, and fills the next layer's constant tiles
@@ -50,36 +61,43 @@ struct StackLayer {
     const uint8_t* up_codes;  // [E][I][H/2]
     const uint8_t* up_scales;
     const float* up_global;   // [E]
-    const uint8_t* down_codes;  // [E][H][I/2]
-    const uint8_t* down_scales;
+    const uint8_t* down_cb;  // [E][I/16][9 H] column blocks of W_down (layout below)
     const float* down_global;
     const uint8_t* shu_codes;  // [S][H/2]
     const uint8_t* shu_scales;
     const float* shu_global;
-    const uint8_t* shd_codes;  // [H][S/2]
-    const uint8_t* shd_scales;
+    const uint8_t* shd_cb;  // [S/16][9 H] column blocks of the shared W_down
     const float* shd_global;
     const float* router_w;  // [E][H]
     const float* router_b;  // [E]
 };
 
-// Per-layer counters: fixed slots, then one per unique expert, then one per
-// 16-row output tile.
+// Per-layer counters: fixed slots, then one per unique expert.
 constexpr int kCntLogits = 0;  // router logits written (target E)
 constexpr int kCntShUp = 1;    // shared-expert up tiles done (target S/16)
-constexpr int kCntHDone = 2;   // output tiles of h_{l+1} final (target H/16)
-constexpr int kCntUp = 3;      // + u: up tiles of unique expert u done (target I/16)
-constexpr int kCntTile = kCntUp + kDecodeMaxU;  // + r: contributions to output tile r (target U + 1)
-__host__ __device__ constexpr int stack_cnt_per_layer(int H) { return kCntTile + H / 16; }
+constexpr int kCntPart = 2;    // CTAs whose partial of h_{l+1} is written (target G)
+constexpr int kCntHDone = 3;   // CTAs whose rows of h_{l+1} are final (target G)
+constexpr int kCntUp = 4;      // + u: up tiles of unique expert u done (target I/16)
+__host__ __device__ constexpr int stack_cnt_per_layer(int /*H*/) { return kCntUp + kDecodeMaxU; }
+
+// Column-block layout of a down matrix W [H][C] (NVFP4, C the reduction
+// dimension): block c holds columns [16 c, 16 c + 16) of every row, 9 H bytes:
+// codes [H/32][32 lanes][8 B], then scales [H/32][8][4 B]. Within pair p (rows
+// 32 p .. 32 p + 31, two 16-row MMA tiles m = 0, 1), lane 4 g + q holds, for
+// tile m, bytes 4m .. 4m + 3: row 32p + 16m + g, columns 4q, 4q + 1 and 4q + 2,
+// 4q + 3 (one E2M1 pair each, low nibble first), then the same for row
+// 32p + 16m + g + 8; scale group g holds, for tile m, bytes 2m, 2m + 1: the
+// block scales of rows 32p + 16m + g and 32p + 16m + g + 8. So each lane loads
+// the A fragment of an m16n8k16 MMA with one 8-byte load per pair of tiles.
+constexpr int kUnitRows = 16;
+constexpr int kMaxUnits = 32;      // units per CTA and layer
+constexpr int kDownMaxPairs = 8;   // 32-row pairs per consumer warp: H <= 12 x 8 x 32 = 3072
 
 struct StackWs {
     int* cnt;            // [L][stack_cnt_per_layer], then the exit count and the abort flag
     float* z;            // [L][T][E] router logits
-    uint16_t* act;       // [T*k][I] bf16 relu^2 rows of the routed experts
-    uint16_t* act_sh;    // [T][S] of the shared expert
-    unsigned int* amax;  // [2][T*k + T] row amax bits of act, then act_sh, by layer parity
-    float* ypart;        // [T*k][H] gate-weighted down rows
-    float* ysh;          // [T][H] shared-expert down rows
+    unsigned int* amax;  // [2][T*k + T] intermediate row amax bits (routed, then shared), by layer parity
+    float* part;         // [G][T][H] per-CTA partials of the layer output
 };
 
 struct StackArgs {
@@ -93,6 +111,7 @@ struct StackArgs {
     StackWs ws;
     int ring_cap;                   // staging ring bytes at the start of dynamic shared memory
     int off_gate, off_uni, off_tk;  // dynamic shared-memory regions after the ring
+    int off_uact, off_ubq;          // per-unit intermediate values, per-unit down B operands
 };
 
 // Counter updates that publish data: the warp's (or CTA's) earlier writes,
@@ -147,19 +166,23 @@ __device__ __noinline__ bool mbar_wait_abortable(uint64_t* b, uint32_t parity, v
 }
 
 // ---------------------------------------------------------------- staging ring
-// A byte ring over the CTA's free shared memory. 16-row tiles of any K
-// (9 K bytes: codes [16][K/2], then scales [16][K/16]) are placed one after
-// another in issue order (an item that would cross the end starts again at
-// offset 0), so that as many tiles are in flight as fit, whatever their K.
-// Item li completes on full[li % kSlots] and is computed by warp group
+// A byte ring over the CTA's free shared memory. Items of 9 H bytes (an up
+// tile: codes [16][H/2], then scales [16][H/16]; or a down column block) are
+// placed one after another in issue order (an item that would cross the end
+// starts again at offset 0), so that as many items are in flight as fit.
+// Item li completes on full[li % kSlots]. Up items are computed by warp group
 // li % kGroups (the consumer warps w with w % kGroups == li % kGroups), whose
-// kGroupWarps warps each take a contiguous share of its 128-k chunks and
-// release it on empty[li % kSlots]. kSlots is a multiple of kGroups, so the
-// same warps wait on every use of a slot, in order (a parity wait can only
-// tell the current phase of an mbarrier from the one before it). The
-// producer reclaims space in issue order: before placing an item it waits
-// until the item that last used the slot, and every older item whose bytes
-// the new one would overwrite, have been released.
+// kGroupWarps warps each take a contiguous share of its 128-k chunks; down
+// items by all consumer warps, each taking its own rows. Either way the
+// consumers release an item on empty[li % kSlots] with kConsumerWarps arrivals
+// in all (an up item's three warps arrive kGroups each). kSlots is a multiple
+// of kGroups, so the same warps wait on every up use of a slot, in order, and
+// every warp waits on a down item only once all of the layer's up items are
+// consumed (a parity wait can only tell the current phase of an mbarrier from
+// the one before it, so no warp may wait on use u of a slot before use u - 1
+// has completed). The producer reclaims space in issue order: before placing
+// an item it waits until the item that last used the slot, and every older
+// item whose bytes the new one would overwrite, have been released.
 constexpr int kGroups = 4;
 constexpr int kGroupWarps = kConsumerWarps / kGroups;
 constexpr int kSlots = 16;
@@ -191,12 +214,15 @@ struct StackCta {
     int last_cta;  // this CTA is the last to leave (resets the workspace)
     // geometry
     int G, b, ring_cap, ng, amax_stride;
-    int su_b, su_e, sd_b, sd_e;  // shared-expert up / down tile ranges of this CTA
+    int su_b, su_e;  // shared-expert units of this CTA
+    int ru_b, ru_e;  // routed units of this CTA (of U x I/16, this layer)
     uint8_t* ring_base;
     float* gsm;      // [ng][H] router rows
     uint16_t* X;     // [T][H] h_l, then x_l
     __half* xq;      // [T][H] up B operand
-    __half* bslot;   // down B: routed [T][I], [T][I], shared [T][S] (aliases X, xq)
+    float* ysm;      // [T][H] FP32 partial of the layer output (aliases X, xq)
+    uint16_t* uact;  // [units][T][16] bf16 relu^2 values of this CTA's units
+    __half* ubq;     // [units][T][16] their down B operands
     float* tk_c;     // [T][E] biased scores
     float* tk_s;     // [T][E] sigmoids
     // step scratch
@@ -204,12 +230,11 @@ struct StackCta {
     float norm_inv[kDecodeMaxT];
     float gx[kDecodeMaxT];
     unsigned int red[kDecodeMaxT];
-    float gbf[3 * kDecodeMaxT];
+    float fct[kMaxUnits][kDecodeMaxT];  // per unit and token: gate x down global x B global
     int sel_idx[kDecodeMaxT][kDecodeMaxK];
     float sel_sig[kDecodeMaxT][kDecodeMaxK];
     float sel_w[kDecodeMaxT][kDecodeMaxK];
     float zred[kConsumerWarps][kDecodeMaxT];
-    int slot_u[2];
     // per-tensor globals of this layer's unique experts and shared expert
     float up_g[kDecodeMaxU], down_g[kDecodeMaxU];
     float shu_g, shd_g;
@@ -241,7 +266,7 @@ __device__ __noinline__ TileOut bgroup_tile_core(StackCta* cp, int li, int K, co
         tile_mma_16x8(st, st + 8 * K, K, bcol, nc * rank / kGroupWarps, nc * (rank + 1) / kGroupWarps, acc);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&r.empty[s]);
+    if (lane == 0) mbar_arrive_cnt(&r.empty[s], kGroups);
     TileOut o;
     o.acc = make_float4(acc[0], acc[1], acc[2], acc[3]);
     const int u = (li / kGroups) & 1;
@@ -558,17 +583,18 @@ __device__ __noinline__ void st_layer_globals(StackCta& c) {
 }
 
 // ---------------------------------------------------------------- steps 5, 6
-// Up tiles [base, base + n): shared (routed == false, tiles su_b + i) or
-// routed (tiles i of the U x I/16 list from ru_b). relu^2 -> bf16 rows, row
-// amax (W4A4), one count per finished tile. Returns false on a timeout.
+// Up tiles [base, base + n), the CTA's units j0 .. j0 + n - 1: shared
+// (routed == false, tiles su_b + i) or routed (tiles i of the U x I/16 list
+// from ru_b). relu^2 -> bf16 values of the unit (shared memory), their amax
+// per (expert, token) (W4A4; counted once per CTA in step 6). Returns false on
+// a timeout.
 template <bool W4A4>
 __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l, int base, int n, bool routed,
-                                         int ru_b) {
+                                         int ru_b, int j0) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
-    const int T = a.T, k = a.k, H = a.H, I = a.I, S = a.S, RI = I >> 4;
+    const int T = a.T, k = a.k, H = a.H, I = a.I, RI = I >> 4;
     unsigned int* const amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
-    int* const cnt = layer_cnt(a, l);
     const __half* bcol = g < T ? c.xq + (size_t)g * H : nullptr;
     const int end = base + n;
 #pragma unroll 1
@@ -578,14 +604,7 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
         const bool lead = bgroup_tile(c, li, H, bcol, acc, ok);
         if (!ok) return false;
         if (!lead) continue;
-        int u = 0, r;
-        if (routed) {
-            const int i = ru_b + (li - base);
-            u = i / RI;
-            r = i % RI;
-        } else {
-            r = c.su_b + (li - base);
-        }
+        const int u = routed ? (ru_b + (li - base)) / RI : 0;
         const float gw = routed ? c.up_g[u] : c.shu_g;
         float m[2] = {0.0f, 0.0f};
 #pragma unroll
@@ -597,9 +616,8 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
             const float gs = W4A4 ? __fmul_rn(gw, c.gx[t]) : gw;
             const float rl = fmaxf(__fmul_rn(acc[v], gs), 0.0f);
             const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
-            const int row = 16 * r + g + 8 * (v >> 1);
-            uint16_t* dst = routed ? a.ws.act + ((size_t)t * k + j) * I : a.ws.act_sh + (size_t)t * S;
-            dst[row] = *reinterpret_cast<const uint16_t*>(&bv);
+            c.uact[((size_t)(j0 + li - base) * T + t) * kUnitRows + g + 8 * (v >> 1)] =
+                *reinterpret_cast<const uint16_t*>(&bv);
             m[v & 1] = fmaxf(m[v & 1], __bfloat162float(bv));
         }
         if (W4A4) {
@@ -622,253 +640,275 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) red_release_add(cnt + (routed ? kCntUp + u : kCntShUp), 1);
     }
     return true;
 }
 
-// ---------------------------------------------------------------- step 7
-// B operands of this CTA's down tiles: routed experts slot_u[0..1] ([T][I]
-// each) and the shared expert ([T][S]), from the finished bf16 rows and their
-// final row amax. Returns false if a wait failed.
+// ---------------------------------------------------------------- step 6
+// The down B operands of this CTA's units. In W4A4 it first waits until every
+// up tile of each expert it holds units of is done, so that the intermediate
+// row amax is final; then each (unit, token) block of 16 values is quantised
+// under the row global amax / 2688 (W4A4) or converted to f16 (W4A16), and
+// its factor gate x down global (x B global in W4A4) recorded; a token that
+// does not route to the unit's expert gets a zero block and factor. Also
+// zeroes the FP32 partial, which aliases the up tiles' operands (all of this
+// CTA's up tiles are done). Returns false if a wait failed.
 template <bool W4A4>
-__device__ __noinline__ bool st_down_operands(const StackArgs& a, StackCta& c, int l, int rd_b, int rd_e) {
+__device__ __noinline__ bool st_down_prep(const StackArgs& a, StackCta& c, int l) {
     const int ctid = threadIdx.x;
-    const int T = a.T, k = a.k, I = a.I, S = a.S, RI = I >> 4, RS = S >> 4, RH = a.H >> 4;
-    const bool has_sd = c.sd_e > c.sd_b;
+    const int T = a.T, k = a.k, H = a.H, RI = a.I >> 4, RS = a.S >> 4;
     int* const cnt = layer_cnt(a, l);
-    const unsigned int* amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
-    if (ctid == 0) {
-        c.slot_u[0] = c.slot_u[1] = -1;
-        if (rd_e > rd_b) {
-            c.slot_u[0] = rd_b / RH;
-            const int u1 = (rd_e - 1) / RH;
-            if (u1 != c.slot_u[0]) c.slot_u[1] = u1;
+    const int n_su = c.su_e - c.su_b, n_ru = c.ru_e - c.ru_b, nu = n_su + n_ru;
+    consumer_bar();
+    // this CTA's up tiles are done: count them, per expert, in one release
+    // each (the CTA barrier orders every warp's amax updates before it)
+    if (ctid == 0 && n_su > 0) red_release_add(cnt + kCntShUp, n_su);
+    if (ctid == 32 && n_ru > 0) {
+#pragma unroll 1
+        for (int u = c.ru_b / RI; u <= (c.ru_e - 1) / RI; ++u)
+            red_release_add(cnt + kCntUp + u, min(c.ru_e, (u + 1) * RI) - max(c.ru_b, u * RI));
+    }
+#pragma unroll 1
+    for (int i = ctid; i < T * H / 4; i += kConsumerThreads)
+        reinterpret_cast<float4*>(c.ysm)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    bool ok = true;
+    if (W4A4) {
+        if (ctid == 0 && n_su > 0) ok = wait_geq(cnt + kCntShUp, RS, abort_flag(a));
+        if (ctid == 32 && n_ru > 0) {
+#pragma unroll 1
+            for (int u = c.ru_b / RI; u <= (c.ru_e - 1) / RI && ok; ++u)
+                ok = wait_geq(cnt + kCntUp + u, RI, abort_flag(a));
         }
     }
-    consumer_bar();  // also: every up tile of this CTA is done, X / xq may be overwritten
-    bool ok = true;
-    if (ctid == 0 && has_sd) ok = wait_geq(cnt + kCntShUp, RS, abort_flag(a));
-    if (ctid == 32 && c.slot_u[0] >= 0) ok = wait_geq(cnt + kCntUp + c.slot_u[0], RI, abort_flag(a));
-    if (ctid == 64 && c.slot_u[1] >= 0) ok = wait_geq(cnt + kCntUp + c.slot_u[1], RI, abort_flag(a));
     if (consumer_bar_or(!ok || cta_abort(c))) return false;
-    // one pass over the blocks of all rows: routed rows r = sl * T + t (slot
-    // sl of this CTA, token t; [I] each), then the shared rows ([S] each).
-    // Every thread reads its row's amax itself (no staging barrier) and keeps
-    // up to kBRegBlocks blocks' loads in flight before quantising any.
-    const int nbr = I >> 4, nbs = S >> 4;
-    const int nr = 2 * T * nbr, total = nr + (has_sd ? T * nbs : 0);
-    auto locate = [&](int i, const uint16_t*& src, const unsigned int*& am, __half*& dst, int& r, int& bb) {
-        src = nullptr;
-        am = nullptr;
-        if (i < nr) {
-            r = i / nbr;
-            bb = i - r * nbr;
-            const int sl = r / T, t = r - sl * T;
-            dst = c.bslot + (size_t)r * I + 16 * bb;
-            const int u = c.slot_u[sl];
-            const int j = u >= 0 ? c.plan.choice[u][t] : -1;
-            if (j >= 0) {
-                src = a.ws.act + ((size_t)t * k + j) * I + 16 * bb;
-                am = amax + t * k + j;
-            }
-        } else {
-            const int i2 = i - nr, t = i2 / nbs;
-            bb = i2 - t * nbs;
-            r = 2 * T + t;
-            dst = c.bslot + (size_t)2 * T * I + (size_t)t * S + 16 * bb;
-            src = a.ws.act_sh + (size_t)t * S + 16 * bb;
-            am = amax + T * k + t;
-        }
-    };
+    const unsigned int* amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
 #pragma unroll 1
-    for (int i0 = ctid; i0 < total; i0 += kBRegBlocks * kConsumerThreads) {
-        uint4 u[kBRegBlocks][2];
-        unsigned int mb[kBRegBlocks];
-#pragma unroll
-        for (int q = 0; q < kBRegBlocks; ++q) {
-            const int i = i0 + q * kConsumerThreads;
-            u[q][0] = u[q][1] = make_uint4(0, 0, 0, 0);
-            mb[q] = 0u;
-            if (i < total) {
-                const uint16_t* src;
-                const unsigned int* am;
-                __half* dst;
-                int r, bb;
-                locate(i, src, am, dst, r, bb);
-                if (src) {
-                    u[q][0] = __ldcg(reinterpret_cast<const uint4*>(src));
-                    u[q][1] = __ldcg(reinterpret_cast<const uint4*>(src) + 1);
-                    if (W4A4) mb[q] = __ldcg(am);
-                }
-            }
+    for (int i = ctid; i < nu * T; i += kConsumerThreads) {
+        const int j = i / T, t = i - j * T;
+        bool used = true;
+        float gate = 1.0f, dg = c.shd_g;
+        const unsigned int* am = amax + T * k + t;
+        if (j >= n_su) {
+            const int u = (c.ru_b + j - n_su) / RI;
+            const int jj = c.plan.choice[u][t];
+            used = jj >= 0;
+            gate = c.plan.gate[u][t];
+            dg = c.down_g[u];
+            am = amax + t * k + (used ? jj : 0);
         }
-#pragma unroll
-        for (int q = 0; q < kBRegBlocks; ++q) {
-            const int i = i0 + q * kConsumerThreads;
-            if (i >= total) break;
-            const uint16_t* src;
-            const unsigned int* am;
-            __half* dst;
-            int r, bb;
-            locate(i, src, am, dst, r, bb);
-            const float g = W4A4 ? __fdiv_rn(__uint_as_float(mb[q]), 2688.0f) : 0.0f;
-            b_block_store<W4A4>(u[q][0], u[q][1], g, reinterpret_cast<uint4*>(dst));
-            if (bb == 0) c.gbf[r] = g;  // the row's first block records its global
+        uint4 u0 = make_uint4(0, 0, 0, 0), u1 = make_uint4(0, 0, 0, 0);
+        if (used) {
+            const uint4* src = reinterpret_cast<const uint4*>(c.uact + ((size_t)j * T + t) * kUnitRows);
+            u0 = src[0];
+            u1 = src[1];
         }
+        const float g = W4A4 && used ? __fdiv_rn(__uint_as_float(__ldcg(am)), 2688.0f) : 0.0f;
+        b_block_store<W4A4>(u0, u1, g, reinterpret_cast<uint4*>(c.ubq + ((size_t)j * T + t) * kUnitRows));
+        c.fct[j][t] = used ? __fmul_rn(gate, W4A4 ? __fmul_rn(dg, g) : dg) : 0.0f;
     }
     consumer_bar();
     return true;
 }
 
-// The warp that completes output tile r of layer l: its 16 rows of
-// h_{l+1} = bf16(((ysh + y_0) + y_1) + ... + y_{k-1} + h_l), FP32 in this order.
-__device__ __noinline__ void combine_tile(const StackArgs& a, StackCta& c, int l, int r) {
-    const int lane = threadIdx.x & 31;
-    const int T = a.T, k = a.k, H = a.H;
-    const uint16_t* res = l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H;
-    uint16_t* out = a.hidden_out + (size_t)l * T * H;
-    // the next layer's row amax buffer starts at zero: its last readers (layer
-    // l - 1) are done, and its first writers wait until every tile is final
-    unsigned int* am = a.ws.amax + (size_t)((l + 1) & 1) * c.amax_stride;
-#pragma unroll 1
-    for (int i = lane; i < c.amax_stride; i += 32) am[i] = 0u;
-#pragma unroll 1
-    for (int o = lane; o < 16 * T; o += 32) {
-        const int t = o >> 4, row = 16 * r + (o & 15);
-        float y[kDecodeMaxK];
+// ---------------------------------------------------------------- step 7
+// The down column blocks of this CTA's units (ring items base .. base + nu - 1),
+// by every consumer warp: warp w takes the 32-row pairs [P w / 12,
+// P (w + 1) / 12) of the H rows (P = H / 32) of every block. The raw products
+// of one expert's units add up in registers (FP32); when the expert changes,
+// and after the last unit, they are added, times the unit's factor per token,
+// into the FP32 partial ysm (rows of this warp only). Returns false on a
+// timeout.
+__device__ __noinline__ bool st_down_units(const StackArgs& a, StackCta& c, int base) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int T = a.T, H = a.H, RI = a.I >> 4, P = H >> 5;
+    const int p0 = P * warp / kConsumerWarps, np = P * (warp + 1) / kConsumerWarps - p0;
+    const int n_su = c.su_e - c.su_b, nu = n_su + (c.ru_e - c.ru_b);
+    BRing& r = c.br;
+    float acc[kDownMaxPairs][2][4];
 #pragma unroll
-        for (int j = 0; j < kDecodeMaxK; ++j)
-            if (j < k) y[j] = __ldcg(a.ws.ypart + ((size_t)t * k + j) * H + row);
-        float acc = __ldcg(a.ws.ysh + (size_t)t * H + row);
-        const float rv = bf16_bits_to_float(__ldcg(res + (size_t)t * H + row));
+    for (int p = 0; p < kDownMaxPairs; ++p)
 #pragma unroll
-        for (int j = 0; j < kDecodeMaxK; ++j)
-            if (j < k) acc = __fadd_rn(acc, y[j]);
-        acc = __fadd_rn(acc, rv);
-        const __nv_bfloat16 ob = __float2bfloat16_rn(acc);
-        out[(size_t)t * H + row] = *reinterpret_cast<const uint16_t*>(&ob);
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) acc[p][mt][v] = 0.0f;
+    // acc x fct[j] into ysm; acc = 0. The factors are read first and each
+    // pair's eight partial values are all loaded before any is stored (the
+    // stores could alias the factor table for all the compiler knows, which
+    // would otherwise serialise every load behind the previous store).
+    auto flush = [&](int j) {
+        const bool t0 = 2 * q < T, t1 = 2 * q + 1 < T;
+        const float f0 = t0 ? c.fct[j][2 * q] : 0.0f, f1 = t1 ? c.fct[j][2 * q + 1] : 0.0f;
+        float* const y0 = c.ysm + (size_t)(2 * q) * H + 32 * p0 + g;
+        float* const y1 = y0 + H;
+#pragma unroll
+        for (int p = 0; p < kDownMaxPairs; ++p) {
+            if (p >= np) break;
+            float y[2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int o = 32 * p + 16 * mt + 8 * (v >> 1);
+                    y[mt][v] = (v & 1) ? (t1 ? y1[o] : 0.0f) : (t0 ? y0[o] : 0.0f);
+                }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int o = 32 * p + 16 * mt + 8 * (v >> 1);
+                    if (v & 1) {
+                        if (t1) y1[o] = __fmaf_rn(f1, acc[p][mt][v], y[mt][v]);
+                    } else if (t0) {
+                        y0[o] = __fmaf_rn(f0, acc[p][mt][v], y[mt][v]);
+                    }
+                    acc[p][mt][v] = 0.0f;
+                }
+        }
+    };
+    bool ok = true;
+    int seg = -2;  // expert of the units in acc (-1: the shared expert)
+#pragma unroll 1
+    for (int j = 0; j < nu; ++j) {
+        const int ex = j < n_su ? -1 : (c.ru_b + j - n_su) / RI;
+        if (j > 0 && ex != seg) flush(j - 1);
+        seg = ex;
+        const int li = base + j, s = li % kSlots;
+        const bool waited = mbar_wait_bounded(&r.full[s], static_cast<uint32_t>((li / kSlots) & 1));
+        const bool got = __all_sync(0xffffffffu, waited);
+        if (got) {
+            // B: token g's block of unit j, elements 4q .. 4q + 3 (the MMA's
+            // k-slots 2q, 2q + 1, 2q + 8, 2q + 9, in the order the block's
+            // layout gives the weights)
+            uint2 bv = make_uint2(0u, 0u);
+            if (g < T) bv = *reinterpret_cast<const uint2*>(c.ubq + ((size_t)j * T + g) * kUnitRows + 4 * q);
+            const uint8_t* blk = c.ring_base + r.off[s];
+            const uint8_t* cw = blk + (size_t)p0 * 256 + lane * 8;
+            const uint8_t* sw = blk + (size_t)8 * H + (size_t)p0 * 32 + g * 4;
+#pragma unroll
+            for (int p = 0; p < kDownMaxPairs; ++p) {
+                if (p >= np) break;
+                const uint2 w = *reinterpret_cast<const uint2*>(cw + p * 256);
+                const uint32_t sc = *reinterpret_cast<const uint32_t*>(sw + p * 32);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const uint32_t s2 = e4m3x2_to_f16x2(mt ? sc >> 16 : sc);  // rows g (low), g + 8
+                    const uint32_t sa = bcast_lo(s2), sb = bcast_hi(s2);
+                    uint32_t f[4];
+                    e2m1x8_to_f16x8(mt ? w.y : w.x, f);
+                    mma_16816(acc[p][mt], hmul2(f[0], sa), hmul2(f[2], sb), hmul2(f[1], sa), hmul2(f[3], sb), bv.x,
+                              bv.y);
+                }
+            }
+        } else if (lane == 0) {
+            set_dev_error(kErrWaitFull);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r.empty[s]);
+        if (!got) {
+            ok = false;
+            break;
+        }
     }
+    if (ok && nu > 0) flush(nu - 1);
+    return ok;
+}
+
+// The CTA's FP32 partial to the workspace (each warp its own rows), counted
+// once the whole CTA has written it.
+__device__ __noinline__ void st_part_write(const StackArgs& a, StackCta& c, int l) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = a.T, H = a.H, P = H >> 5;
+    const int r0 = 32 * (P * warp / kConsumerWarps), r1 = 32 * (P * (warp + 1) / kConsumerWarps);
     __syncwarp();
-    if (lane == 0) red_release_add(layer_cnt(a, l) + kCntHDone, 1);
+    float* const dst = a.ws.part + (size_t)c.b * T * H;
+#pragma unroll 1
+    for (int t = 0; t < T; ++t)
+#pragma unroll 1
+        for (int i = r0 + 4 * lane; i < r1; i += 128)
+            __stcg(reinterpret_cast<float4*>(dst + (size_t)t * H + i),
+                   *reinterpret_cast<const float4*>(c.ysm + (size_t)t * H + i));
+    consumer_bar();
+    if (threadIdx.x == 0) red_release_add(layer_cnt(a, l) + kCntPart, 1);
 }
 
 // ---------------------------------------------------------------- step 8
-template <bool W4A4>
-__device__ __noinline__ bool st_down_tiles(const StackArgs& a, StackCta& c, int l, int base, int rd_b, int n_rd) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, q = lane & 3;
-    const int T = a.T, k = a.k, H = a.H, I = a.I, S = a.S, RH = H >> 4;
-    const int n_sd = c.sd_e - c.sd_b;
-    int* const cnt = layer_cnt(a, l);
-    const int U = c.plan.U;
-    const __half* bslot2 = c.bslot + (size_t)2 * T * I;
-    const int end = base + n_sd + n_rd;
+// This CTA's rows [h0, h1) of h_{l+1}, once every CTA's partial is written:
+// the G partials of a (token, row) are split into chunks of kPartChunk
+// consecutive CTAs; thread i takes chunk i / (T nr) of item i % (T nr), adds
+// its partials in CTA order (all its loads in flight at once), and the chunk
+// sums are added in chunk order; then the residual h_l; then bf16. CTA 0 also
+// clears the row amax buffer of layer l + 1 (its last readers, the down steps
+// of layer l - 1, are done; its first writers wait for this layer's rows).
+// Returns false if the wait failed.
+constexpr int kPartChunk = 8;
+
+__device__ __noinline__ bool st_reduce(const StackArgs& a, StackCta& c, int l) {
+    const int ctid = threadIdx.x;
+    const int T = a.T, H = a.H, G = c.G;
+    bool ok = true;
+    if (ctid == 0) ok = wait_geq(layer_cnt(a, l) + kCntPart, G, abort_flag(a));
+    if (consumer_bar_or(!ok || cta_abort(c))) return false;
+    if (c.b == 0) {
+        unsigned int* am = a.ws.amax + (size_t)((l + 1) & 1) * c.amax_stride;
 #pragma unroll 1
-    for (int li = first_item(base, warp % kGroups, kGroups); li < end; li += kGroups) {
-        const bool routed = li >= base + n_sd;
-        int u = -1, r, sl, K;
-        if (routed) {
-            const int i = rd_b + (li - base - n_sd);
-            u = i / RH;
-            r = i % RH;
-            sl = u == c.slot_u[0] ? 0 : (u == c.slot_u[1] ? 1 : -1);
-            K = I;
-        } else {
-            r = c.sd_b + (li - base);
-            sl = 2;
-            K = S;
-        }
-        if (sl < 0 && lane == 0) set_dev_error(kErrBadInput);
-        const __half* bs = sl == 2 ? bslot2 : c.bslot + (size_t)(sl < 0 ? 0 : sl) * T * I;
-        const __half* bcol = nullptr;
-        if (sl >= 0 && g < T && (!routed || c.plan.choice[u][g] >= 0)) bcol = bs + (size_t)g * K;
-        float acc[4];
-        bool ok;
-        const bool lead = bgroup_tile(c, li, K, bcol, acc, ok);
-        if (!ok) return false;
-        if (!lead) continue;
-        const float gw = routed ? c.down_g[u] : c.shd_g;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const int t = 2 * q + (v & 1);
-            const int row = 16 * r + g + 8 * (v >> 1);
-            if (t >= T || sl < 0) continue;
-            const float gs = W4A4 ? __fmul_rn(gw, c.gbf[sl * T + t]) : gw;
-            const float y = __fmul_rn(acc[v], gs);
-            if (routed) {
-                const int j = c.plan.choice[u][t];
-                if (j >= 0) a.ws.ypart[((size_t)t * k + j) * H + row] = __fmul_rn(c.plan.gate[u][t], y);
-            } else {
-                a.ws.ysh[(size_t)t * H + row] = y;
-            }
-        }
-        // count this contribution to output tile r; the last one combines it
-        __syncwarp();
-        int prev = 0;
-        if (lane == 0) prev = atom_acq_rel_add(cnt + kCntTile + r, 1);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == U) {
-            __syncwarp();  // lane 0's acquire orders the other lanes' loads too
-            combine_tile(a, c, l, r);
-        }
+        for (int i = ctid; i < c.amax_stride; i += kConsumerThreads) am[i] = 0u;
     }
+    const uint16_t* res = l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H;
+    uint16_t* out = a.hidden_out + (size_t)l * T * H;
+    const int h0 = share_begin32(H, c.b, G), nr = share_begin32(H, c.b + 1, G) - h0;
+    const int items = T * nr, nch = (G + kPartChunk - 1) / kPartChunk;
+    // the chunk sums, [chunk][item], in ysm (its rows are in the workspace
+    // now): T nr nch <= T (H/G + 1)(G/8 + 1) floats, within its T H
+    float* const csum = c.ysm;
+#pragma unroll 1
+    for (int i = ctid; i < items * nch; i += kConsumerThreads) {
+        const int ch = i / items, it = i - ch * items;
+        const int t = it / nr, row = h0 + it - t * nr;
+        const float* src = a.ws.part + (size_t)t * H + row;
+        float v[kPartChunk];
+#pragma unroll
+        for (int j = 0; j < kPartChunk; ++j) {
+            const int b2 = kPartChunk * ch + j;
+            v[j] = b2 < G ? __ldcg(src + (size_t)b2 * T * H) : 0.0f;
+        }
+        float s = v[0];
+#pragma unroll
+        for (int j = 1; j < kPartChunk; ++j) s = __fadd_rn(s, v[j]);
+        csum[ch * items + it] = s;
+    }
+    consumer_bar();
+    if (ctid < items) {
+        const int t = ctid / nr, row = h0 + ctid - t * nr;
+        float s = csum[ctid];
+#pragma unroll 1
+        for (int ch = 1; ch < nch; ++ch) s = __fadd_rn(s, csum[ch * items + ctid]);
+        const float h = __fadd_rn(s, bf16_bits_to_float(__ldcg(res + (size_t)t * H + row)));
+        const __nv_bfloat16 ob = __float2bfloat16_rn(h);
+        out[(size_t)t * H + row] = *reinterpret_cast<const uint16_t*>(&ob);
+    }
+    consumer_bar();
+    if (ctid == 0) red_release_add(layer_cnt(a, l) + kCntHDone, 1);
     return true;
 }
 
 // ---------------------------------------------------------------- producer
-
-// The producer is one thread among twelve busy warps, so its per-tile work is
-// kept short: the ring position lives in registers (phys = vhead mod cap,
-// advanced without divisions), the fill is inlined, and the routed tiles'
-// addresses advance without divisions.
+// Per layer l the items go out in the order the consumers take them: the
+// up tiles of the CTA's shared-expert units (before the plan exists, while
+// the previous layer finishes), then, once the plan is posted, the up tiles
+// of its routed units, and the down column blocks of its shared, then routed
+// units. All items are 9 H bytes. The producer is one thread among twelve
+// busy warps, so its per-item work is kept short: the ring position lives in
+// registers (phys = vhead mod cap, advanced without divisions), the routed
+// addresses advance without divisions, and all items go through one fill site.
 __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
-    const int H = a.H, I = a.I, S = a.S, RI = I >> 4, RH = H >> 4;
+    const int H = a.H, I = a.I, RI = I >> 4;
     const int G = c.G, b = c.b;
     BRing& r = c.br;
-    const int cap = c.ring_cap;
+    const int cap = c.ring_cap, size = 9 * H;
     uint8_t* const rbase = c.ring_base;
     int pli = 0, tail = 0, vhead = 0, phys = 0;
     bool alive = true;
-    // item pli: a 16-row tile of K columns (9 K bytes), placed after the
-    // previous one (or at offset 0 if it would cross the end), once the item
-    // that last used its slot and every older item whose bytes it overwrites
-    // are released (waited for in issue order)
-    auto fill = [&](const uint8_t* codes, const uint8_t* scales, int K) {
-        if (!alive) return;
-        if (cta_abort(c)) {
-            alive = false;
-            return;
-        }
-        const int size = 9 * K;
-        if (phys + size > cap) {
-            vhead += cap - phys;
-            phys = 0;
-        }
-        const int lim = vhead + size - cap;
-#pragma unroll 1
-        while (tail < pli && (tail <= pli - kSlots || r.vs[tail & (kSlots - 1)] < lim)) {
-            if (!mbar_wait_abortable(&r.empty[tail & (kSlots - 1)], static_cast<uint32_t>((tail / kSlots) & 1),
-                                     &c.abort_s, kErrWaitEmpty)) {
-                alive = false;
-                set_cta_abort(c);
-                return;
-            }
-            ++tail;
-        }
-        const int s = pli & (kSlots - 1);
-        r.vs[s] = vhead;
-        r.off[s] = static_cast<uint32_t>(phys);
-        uint8_t* dst = rbase + phys;
-        mbar_arrive_expect_tx(&r.full[s], static_cast<uint32_t>(size));
-        bulk_g2s(dst, codes, static_cast<uint32_t>(8 * K), &r.full[s]);
-        bulk_g2s(dst + 8 * K, scales, static_cast<uint32_t>(K), &r.full[s]);
-        r.uses[s] += 1;
-        vhead += size;
-        phys += size;
-        ++pli;
-    };
     // router rows of this CTA's experts and the layer's bias (E * 4 bytes,
     // E % 8 == 0: a multiple of 16 bytes), on one barrier phase per layer
     auto issue_gate = [&](int l) {
@@ -882,58 +922,84 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
         bulk_g2s(c.dng_s, a.layer[l].down_global, (uint32_t)(a.E * 4), &c.gbar);
         c.gate_issued += 1;
     };
-    auto issue_shared_up = [&](int l) {
-        const StackLayer& P = a.layer[l];
-#pragma unroll 1
-        for (int sr = c.su_b; sr < c.su_e; ++sr)
-            fill(P.shu_codes + (size_t)16 * sr * (H >> 1), P.shu_scales + (size_t)16 * sr * (H >> 4), H);
-    };
     issue_gate(0);
-    issue_shared_up(0);
 #pragma unroll 1
     for (int l = 0; l < a.L && alive; ++l) {
-        if (!mbar_wait_abortable(&c.pbar, l & 1, &c.abort_s)) {
-            set_cta_abort(c);
-            break;
-        }
-        if (l + 1 < a.L) issue_gate(l + 1);
         const StackLayer& P = a.layer[l];
-        const int NU = c.plan.U * RI, ND = c.plan.U * RH;
-        {  // routed up tiles: tile rr of unique expert u
-            const uint8_t* const uc = P.up_codes;
-            const uint8_t* const us = P.up_scales;
-            const int i0 = share_begin32(NU, b, G), n = share_begin32(NU, b + 1, G) - i0;
-            int u = i0 / RI, rr = i0 - u * RI;
+        int ru_b = 0, ru_e = 0;
+#pragma unroll 1
+        for (int sg = 0; sg < 4 && alive; ++sg) {
+            if (sg == 1) {  // the plan of layer l
+                if (!mbar_wait_abortable(&c.pbar, l & 1, &c.abort_s)) {
+                    set_cta_abort(c);
+                    alive = false;
+                    break;
+                }
+                if (l + 1 < a.L) issue_gate(l + 1);
+                const int NU = c.plan.U * RI;
+                ru_b = share_begin32(NU, b, G);
+                ru_e = share_begin32(NU, b + 1, G);
+            }
+            // segment sg: units [i0, i0 + n); an up unit is 16 rows of W_up
+            // (codes, then scales, from two arrays), a down unit one column
+            // block (codes, then scales, contiguous)
+            const bool routed = sg & 1, up = sg < 2;
+            const int i0 = routed ? ru_b : c.su_b, n = routed ? ru_e - ru_b : c.su_e - c.su_b;
+            int u = routed ? i0 / RI : 0, rr = routed ? i0 - u * RI : i0;
 #pragma unroll 1
             for (int j = 0; j < n; ++j) {
-                const int64_t row = (int64_t)c.plan.expert[u] * I + 16 * rr;
-                fill(uc + row * (H >> 1), us + row * (H >> 4), H);
-                if (++rr == RI) {
+                const uint8_t *src_c, *src_s;
+                if (up) {
+                    const int64_t row = (routed ? (int64_t)c.plan.expert[u] * I : 0) + 16 * rr;
+                    src_c = (routed ? P.up_codes : P.shu_codes) + row * (H >> 1);
+                    src_s = (routed ? P.up_scales : P.shu_scales) + row * (H >> 4);
+                } else {
+                    const int64_t blk = (routed ? (int64_t)c.plan.expert[u] * RI : 0) + rr;
+                    src_c = (routed ? P.down_cb : P.shd_cb) + blk * size;
+                    src_s = src_c + 8 * H;
+                }
+                if (++rr == RI && routed) {
                     rr = 0;
                     ++u;
                 }
-            }
-        }
-#pragma unroll 1
-        for (int sr = c.sd_b; sr < c.sd_e; ++sr)
-            fill(P.shd_codes + (size_t)16 * sr * (S >> 1), P.shd_scales + (size_t)16 * sr * (S >> 4), S);
-        {  // routed down tiles
-            const uint8_t* const dc = P.down_codes;
-            const uint8_t* const ds = P.down_scales;
-            const int i0 = share_begin32(ND, b, G), n = share_begin32(ND, b + 1, G) - i0;
-            int u = i0 / RH, rr = i0 - u * RH;
-#pragma unroll 1
-            for (int j = 0; j < n; ++j) {
-                const int64_t row = (int64_t)c.plan.expert[u] * H + 16 * rr;
-                fill(dc + row * (I >> 1), ds + row * (I >> 4), I);
-                if (++rr == RH) {
-                    rr = 0;
-                    ++u;
+                // item pli goes after the previous one, or at offset 0 if it
+                // would cross the end, once the item that last used its slot
+                // and every older item whose bytes it overwrites are released
+                // (waited for in issue order)
+                if (cta_abort(c)) {
+                    alive = false;
+                    break;
                 }
+                if (phys + size > cap) {
+                    vhead += cap - phys;
+                    phys = 0;
+                }
+                const int lim = vhead + size - cap;
+#pragma unroll 1
+                while (tail < pli && (tail <= pli - kSlots || r.vs[tail & (kSlots - 1)] < lim)) {
+                    if (!mbar_wait_abortable(&r.empty[tail & (kSlots - 1)],
+                                             static_cast<uint32_t>((tail / kSlots) & 1), &c.abort_s, kErrWaitEmpty)) {
+                        alive = false;
+                        set_cta_abort(c);
+                        break;
+                    }
+                    ++tail;
+                }
+                if (!alive) break;
+                const int s = pli & (kSlots - 1);
+                r.vs[s] = vhead;
+                r.off[s] = static_cast<uint32_t>(phys);
+                uint8_t* dst = rbase + phys;
+                mbar_arrive_expect_tx(&r.full[s], static_cast<uint32_t>(size));
+                bulk_g2s(dst, src_c, static_cast<uint32_t>(8 * H), &r.full[s]);
+                bulk_g2s(dst + 8 * H, src_s, static_cast<uint32_t>(H), &r.full[s]);
+                r.uses[s] += 1;
+                vhead += size;
+                phys += size;
+                ++pli;
             }
         }
-        mbar_arrive(&c.qbar);  // the plan of layer l is no longer read here
-        if (l + 1 < a.L) issue_shared_up(l + 1);
+        if (alive) mbar_arrive(&c.qbar);  // the plan of layer l is no longer read here
     }
     if (!alive) atomicExch(abort_flag(a), 1);
 }
@@ -942,17 +1008,17 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
 template <bool W4A4>
 __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
     const int ctid = threadIdx.x;
-    const int T = a.T, E = a.E, H = a.H, I = a.I, RI = I >> 4, RH = H >> 4;
+    const int T = a.T, E = a.E, H = a.H, I = a.I, RI = I >> 4;
     const int G = c.G, b = c.b;
     int base = 0;  // first ring item of the current step
     bool bad = false;
 #pragma unroll 1
     for (int l = 0; l < a.L; ++l) {
         int* const cnt = layer_cnt(a, l);
-        // 1-2. the layer input, once every tile of it is final
+        // 1-2. the layer input, once every CTA's rows of it are final
         if (l > 0) {
             bool ok = true;
-            if (ctid == 0) ok = wait_geq(layer_cnt(a, l - 1) + kCntHDone, RH, abort_flag(a));
+            if (ctid == 0) ok = wait_geq(layer_cnt(a, l - 1) + kCntHDone, G, abort_flag(a));
             if (consumer_bar_or(!ok || cta_abort(c))) {
                 bad = true;
                 break;
@@ -978,27 +1044,34 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
         }
         st_topk_plan(a, c, l);
         st_layer_globals(c);
-        if (ctid == 0) mbar_arrive(&c.pbar);  // the producer may stream the routed tiles now
-        // 5. shared-expert up tiles (staged during the previous layer)
-        const int n_su = c.su_e - c.su_b;
-        if (!st_up_tiles<W4A4>(a, c, l, base, n_su, false, 0)) set_cta_abort(c);
-        base += n_su;
-        // 6. routed up tiles
-        const int U = c.plan.U;
-        const int NU = U * RI, ND = U * RH;
+        if (ctid == 0) mbar_arrive(&c.pbar);  // the producer may stream the routed weights now
+        // 5. up tiles of the shared-expert units (staged during the previous
+        // layer), then of the routed units
+        const int NU = c.plan.U * RI;
         const int ru_b = share_begin32(NU, b, G), ru_e = share_begin32(NU, b + 1, G);
-        const int rd_b = share_begin32(ND, b, G), rd_e = share_begin32(ND, b + 1, G);
-        if (!st_up_tiles<W4A4>(a, c, l, base, ru_e - ru_b, true, ru_b)) set_cta_abort(c);
-        base += ru_e - ru_b;
-        // 7. down operands
-        if (!st_down_operands<W4A4>(a, c, l, rd_b, rd_e)) {
+        const int n_su = c.su_e - c.su_b, n_ru = ru_e - ru_b;
+        if (ctid == 0) {  // read after the barrier that opens step 6
+            c.ru_b = ru_b;
+            c.ru_e = ru_e;
+        }
+        if (!st_up_tiles<W4A4>(a, c, l, base, n_su, false, 0, 0)) set_cta_abort(c);
+        if (!st_up_tiles<W4A4>(a, c, l, base + n_su, n_ru, true, ru_b, n_su)) set_cta_abort(c);
+        base += n_su + n_ru;
+        // 6. the units' down B operands
+        if (!st_down_prep<W4A4>(a, c, l)) {
             bad = true;
             break;
         }
-        // 8. down tiles, counted per output tile; the last contribution combines it
-        if (!st_down_tiles<W4A4>(a, c, l, base, rd_b, rd_e - rd_b)) set_cta_abort(c);
-        base += (c.sd_e - c.sd_b) + (rd_e - rd_b);
+        // 7. the units' down column blocks -> this CTA's partial
+        if (!st_down_units(a, c, base)) set_cta_abort(c);
+        base += n_su + n_ru;
         if (consumer_bar_or(cta_abort(c))) {
+            bad = true;
+            break;
+        }
+        st_part_write(a, c, l);
+        // 8. this CTA's rows of h_{l+1}
+        if (!st_reduce(a, c, l)) {
             bad = true;
             break;
         }
@@ -1027,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(&c.br.full[s], 1);
-            mbar_init(&c.br.empty[s], kGroupWarps);
+            mbar_init(&c.br.empty[s], kConsumerWarps);
             c.br.uses[s] = 0;
         }
         mbar_init(&c.gbar, 1);
@@ -1041,16 +1114,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant
         c.ring_cap = a.ring_cap;
         c.ng = b < a.E ? (a.E - b + G - 1) / G : 0;
         c.amax_stride = a.T * a.k + a.T;
-        const int RS = a.S >> 4, RH = a.H >> 4;
+        const int RS = a.S >> 4;
         c.su_b = share_begin32(RS, b, G);
         c.su_e = share_begin32(RS, b + 1, G);
-        c.sd_b = share_begin32(RH, b, G);
-        c.sd_e = share_begin32(RH, b + 1, G);
+        c.ru_b = c.ru_e = 0;
         c.ring_base = smem;
         c.gsm = reinterpret_cast<float*>(smem + a.off_gate);
         c.X = reinterpret_cast<uint16_t*>(smem + a.off_uni);
         c.xq = reinterpret_cast<__half*>(smem + a.off_uni + (size_t)a.T * a.H * 2);
-        c.bslot = reinterpret_cast<__half*>(smem + a.off_uni);
+        c.ysm = reinterpret_cast<float*>(smem + a.off_uni);
+        c.uact = reinterpret_cast<uint16_t*>(smem + a.off_uact);
+        c.ubq = reinterpret_cast<__half*>(smem + a.off_ubq);
         c.tk_c = reinterpret_cast<float*>(smem + a.off_tk);
         c.tk_s = c.tk_c + (size_t)a.T * a.E;
     }

@@ -961,14 +961,73 @@ extern "C" nvfp4_status moe_expert_forward_noalloc(const moe_layer_weights* w, c
                               need, stream);
 }
 
+// ------------------------------------------------ column-block copy
+namespace {
+
+// One warp per (matrix, 16-column block, 32-row pair): lane L = 4g + q writes
+// its 8 code bytes, lanes 0..7 the 4 scale bytes of group g = L (the layout
+// in the header).
+__global__ void k_colblock_layout(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                  int64_t pairs_total, int rows, int cols, uint8_t* __restrict__ out) {
+    const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (w >= pairs_total) return;
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int P = rows >> 5, C = cols >> 4;
+    const int p = static_cast<int>(w % P);
+    const int64_t bc = w / P;  // matrix * C + block
+    const int c = static_cast<int>(bc % C);
+    const int64_t mat = bc / C;
+    const uint8_t* mc = codes + mat * rows * (int64_t)(cols >> 1);
+    const uint8_t* ms = scales + mat * rows * (int64_t)C;
+    uint8_t* blk = out + bc * 9 * (int64_t)rows;
+    uint8_t v[8];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = 32 * p + 16 * mt + g + 8 * (i >> 1);
+            v[4 * mt + i] = mc[(int64_t)row * (cols >> 1) + 8 * c + 2 * q + (i & 1)];
+        }
+    uint2 o;
+    o.x = v[0] | (v[1] << 8) | (v[2] << 16) | ((uint32_t)v[3] << 24);
+    o.y = v[4] | (v[5] << 8) | (v[6] << 16) | ((uint32_t)v[7] << 24);
+    *reinterpret_cast<uint2*>(blk + (int64_t)p * 256 + lane * 8) = o;
+    if (lane < 8) {
+        uint32_t s = 0;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                s |= (uint32_t)ms[(int64_t)(32 * p + 16 * mt + lane + 8 * j) * C + c] << (8 * (2 * mt + j));
+        *reinterpret_cast<uint32_t*>(blk + 8 * (int64_t)rows + (int64_t)p * 32 + lane * 4) = s;
+    }
+}
+
+}  // namespace
+
+extern "C" nvfp4_status nvfp4_colblock_layout(const uint8_t* codes, const uint8_t* scales, int64_t batch,
+                                              int64_t rows, int64_t cols, uint8_t* out, cudaStream_t stream) {
+    if (!codes || !scales || !out || batch < 1 || rows < 1 || cols < 1) return NVFP4_ERR_INVALID_ARG;
+    if (rows % 32 || cols % 16 || rows > (1 << 24) || cols > (1 << 24)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(out, 16)) return NVFP4_ERR_MISALIGNED;
+    const int64_t pairs = batch * (cols / 16) * (rows / 32);
+    const int wpb = 8;  // warps per block
+    k_colblock_layout<<<(unsigned)((pairs + wpb - 1) / wpb), 32 * wpb, 0, stream>>>(
+        codes, scales, pairs, static_cast<int>(rows), static_cast<int>(cols), out);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    return NVFP4_OK;
+}
+
 // ------------------------------------------------ persistent layer stack
 namespace {
 
 struct StackWsOffsets {
-    size_t cnt, z, act, act_sh, amax, ypart, ysh, total;
+    size_t cnt, z, amax, part, total;
 };
 
-StackWsOffsets stack_ws(int L, int T, int k, int E, int H, int I, int S) {
+// G: the grid (one CTA per SM), whose partials of each layer output meet in
+// the workspace.
+StackWsOffsets stack_ws(int L, int T, int k, int E, int H, int G) {
     StackWsOffsets o{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -979,38 +1038,47 @@ StackWsOffsets stack_ws(int L, int T, int k, int E, int H, int I, int S) {
     o.cnt = take(sizeof(int) * ((size_t)L * stack_cnt_per_layer(H) + 2));
     o.amax = take(sizeof(unsigned int) * 2 * (size_t)(T * k + T));
     o.z = take(sizeof(float) * (size_t)L * T * E);
-    o.act = take((size_t)T * k * I * 2);
-    o.act_sh = take((size_t)T * S * 2);
-    o.ypart = take((size_t)T * k * H * 4);
-    o.ysh = take((size_t)T * H * 4);
+    o.part = take(sizeof(float) * (size_t)G * T * H);
     o.total = off;
     return o;
 }
 
+// Units (16 intermediate rows of one expert) a CTA holds in one layer at
+// most: its share of the shared expert's S/16 and of the routed U x I/16,
+// U <= min(T k, E).
+int stack_max_units(int T, int k, int E, int I, int S, int G) {
+    const int U = std::min(T * k, E);
+    return (S / 16 + G - 1) / G + (U * (I / 16) + G - 1) / G;
+}
+
 // Dynamic shared memory of the stack kernel: the ring, then the router rows,
-// the operand union (layer input + up B / down B slots), the top-k scores.
+// the operand union (layer input and up B operand; later the layer output
+// partial), the top-k scores, the units' intermediate values and down B
+// operands.
 struct StackSmem {
-    int ring_cap, off_gate, off_uni, off_tk, total;
+    int ring_cap, off_gate, off_uni, off_tk, off_uact, off_ubq, total;
 };
 
-// Dynamic shared memory of the stack kernel: the staging ring takes whatever
-// the router rows, the B operands and the top-k scratch leave, and must hold
-// at least two of the largest tiles (9 K bytes for 16 rows of K).
-bool stack_smem(int lim, int E, int G, int T, int H, int I, int S, StackSmem* out) {
+// The staging ring takes whatever the rest leaves, and must hold at least two
+// items (9 H bytes each).
+bool stack_smem(int lim, int E, int G, int T, int H, int units, StackSmem* out) {
     auto a128 = [](size_t x) { return static_cast<int>((x + 127) & ~size_t(127)); };
-    const int item = 9 * std::max(std::max(H, I), S);
+    const int item = 9 * H;
     const int ng = (E + G - 1) / G;
     const int gate = a128((size_t)ng * H * 4);
-    const int uni = a128(std::max((size_t)T * H * 4, ((size_t)2 * T * I + (size_t)T * S) * 2));
+    const int uni = a128((size_t)T * H * 4);
     const int tk = a128((size_t)T * E * 8);
-    const int rest = gate + uni + tk;
+    const int ua = a128((size_t)units * T * kUnitRows * 2);
+    const int rest = gate + uni + tk + 2 * ua;
     const int ring = ((lim - rest) / 128) * 128;
     if (ring < 2 * item) return false;
     out->ring_cap = ring;
     out->off_gate = ring;
     out->off_uni = out->off_gate + gate;
     out->off_tk = out->off_uni + uni;
-    out->total = out->off_tk + tk;
+    out->off_uact = out->off_tk + tk;
+    out->off_ubq = out->off_uact + ua;
+    out->total = out->off_ubq + ua;
     return true;
 }
 
@@ -1025,13 +1093,19 @@ nvfp4_status check_stack(const moe_stack_layer* layers, int32_t L, int32_t T, in
         if (ly.moe.num_experts != w0.num_experts || ly.moe.hidden != w0.hidden || ly.moe.inter != w0.inter ||
             ly.moe.shared_inter != w0.shared_inter)
             return NVFP4_ERR_INVALID_ARG;
-        if (!ly.router_w || !ly.router_bias) return NVFP4_ERR_INVALID_ARG;
+        if (!ly.router_w || !ly.router_bias || !ly.down_colblock || !ly.shared_down_colblock)
+            return NVFP4_ERR_INVALID_ARG;
         if (!aligned(ly.router_w, 16) || !aligned(ly.router_bias, 16) || !aligned(ly.moe.up_global, 16) ||
-            !aligned(ly.moe.down_global, 16))
+            !aligned(ly.moe.down_global, 16) || !aligned(ly.down_colblock, 16) ||
+            !aligned(ly.shared_down_colblock, 16))
             return NVFP4_ERR_MISALIGNED;
     }
     if (k > w0.num_experts) return NVFP4_ERR_INVALID_ARG;
     if (T > kDecodeMaxT || k > kDecodeMaxK || w0.num_experts > 256 || w0.num_experts % 8) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    // the down step's warps hold at most kDownMaxPairs 32-row pairs each
+    if (w0.hidden > 32 * kDownMaxPairs * kConsumerWarps) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (stack_max_units(T, k, w0.num_experts, w0.inter, w0.shared_inter, num_sms()) > kMaxUnits)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
     return NVFP4_OK;
 }
 
@@ -1042,7 +1116,7 @@ extern "C" size_t moe_stack_forward_workspace_size(const moe_stack_layer* layers
     (void)mode;
     if (check_stack(layers, L, T, k) != NVFP4_OK) return 0;
     const moe_layer_weights& w = layers[0].moe;
-    return stack_ws(L, T, k, w.num_experts, w.hidden, w.inter, w.shared_inter).total;
+    return stack_ws(L, T, k, w.num_experts, w.hidden, num_sms()).total;
 }
 
 extern "C" nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t L, const void* hidden_in, int32_t T,
@@ -1063,15 +1137,16 @@ extern "C" nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t
         const uintptr_t b0 = reinterpret_cast<uintptr_t>(hidden_out), b1 = b0 + (size_t)L * T * H * 2;
         if (a0 < b1 && b0 < a1) return NVFP4_ERR_INVALID_ARG;
     }
-    const StackWsOffsets o = stack_ws(L, T, k, E, H, I, S);
+    const int G = num_sms();
+    const StackWsOffsets o = stack_ws(L, T, k, E, H, G);
     if (workspace_bytes < o.total) return NVFP4_ERR_WORKSPACE;
     const bool w4a4 = mode == NVFP4_W4A4;
     const void* kfn = w4a4 ? reinterpret_cast<const void*>(k_moe_stack<true>)
                            : reinterpret_cast<const void*>(k_moe_stack<false>);
-    const int G = num_sms();
     const int lim = dyn_smem_limit(kfn);
     StackSmem sm{};
-    if (lim <= 0 || !stack_smem(lim, E, G, T, H, I, S, &sm)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (lim <= 0 || !stack_smem(lim, E, G, T, H, stack_max_units(T, k, E, I, S, G), &sm))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kThreads, sm.total) != cudaSuccess)
         return NVFP4_ERR_CUDA;
@@ -1084,14 +1159,12 @@ extern "C" nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t
         d.up_codes = ly.moe.up_codes;
         d.up_scales = ly.moe.up_scales;
         d.up_global = ly.moe.up_global;
-        d.down_codes = ly.moe.down_codes;
-        d.down_scales = ly.moe.down_scales;
+        d.down_cb = ly.down_colblock;
         d.down_global = ly.moe.down_global;
         d.shu_codes = ly.moe.shared_up.codes;
         d.shu_scales = ly.moe.shared_up.scales;
         d.shu_global = ly.moe.shared_up.global_scale;
-        d.shd_codes = ly.moe.shared_down.codes;
-        d.shd_scales = ly.moe.shared_down.scales;
+        d.shd_cb = ly.shared_down_colblock;
         d.shd_global = ly.moe.shared_down.global_scale;
         d.router_w = ly.router_w;
         d.router_b = ly.router_bias;
@@ -1111,15 +1184,14 @@ extern "C" nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t
     uint8_t* base = static_cast<uint8_t*>(workspace);
     a.ws.cnt = reinterpret_cast<int*>(base + o.cnt);
     a.ws.z = reinterpret_cast<float*>(base + o.z);
-    a.ws.act = reinterpret_cast<uint16_t*>(base + o.act);
-    a.ws.act_sh = reinterpret_cast<uint16_t*>(base + o.act_sh);
     a.ws.amax = reinterpret_cast<unsigned int*>(base + o.amax);
-    a.ws.ypart = reinterpret_cast<float*>(base + o.ypart);
-    a.ws.ysh = reinterpret_cast<float*>(base + o.ysh);
+    a.ws.part = reinterpret_cast<float*>(base + o.part);
     a.ring_cap = sm.ring_cap;
     a.off_gate = sm.off_gate;
     a.off_uni = sm.off_uni;
     a.off_tk = sm.off_tk;
+    a.off_uact = sm.off_uact;
+    a.off_ubq = sm.off_ubq;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);

@@ -82,6 +82,8 @@ class MoEDecodeStack:
         if self.lm is not None:
             self.lm_ws = make_lm_head_workspace(self.lm, self.T)
         if self.T <= 4:
+            for Lw in self.layers:  # the column-block down weights, from the weights just registered
+                Lw.stack_layout()
             self.stack_ws = make_stack_workspace(self.layers, self.T, self.k, self.mode)
             self.c_layers = _stack_layers(self.layers)
 

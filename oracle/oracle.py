@@ -174,6 +174,33 @@ def route(h_bf16: np.ndarray, Wg: np.ndarray, bias: np.ndarray, k: int):
     return dict(idx=idx, w=w, z=z, c=c, tau=tau)
 
 
+def rms_norm_slack(h_bf16, eps, Wg, window=2.0 ** -18):
+    """Logit slack [T][E] of routing on an RMS norm evaluated in binary32
+    instead of this oracle's binary64 (the pages fix the norm's bf16 output,
+    card-int4 "Left at bfloat16", not the precision it is computed in). An
+    element whose exact normalised value lies within `window` (relative) of a
+    bf16 rounding midpoint may round to the other neighbour in binary32 (the
+    binary32 sum of squares and reciprocal square root are good to a few
+    2^-24), moving logit e by up to |Wg[e][i]| times the gap between the two
+    neighbours; the slack adds this up over such elements. Zero for eps <= 0
+    (no norm, the input is used as it is)."""
+    h = np.ascontiguousarray(h_bf16, np.uint16)
+    if h.ndim == 1:
+        h = h[None, :]
+    Wg = np.asarray(Wg, np.float64)
+    if eps <= 0:
+        return np.zeros((h.shape[0], Wg.shape[0]))
+    hv = (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    inv = 1.0 / np.sqrt((hv * hv).sum(axis=1) / hv.shape[1] + eps)
+    x = hv * inv[:, None]
+    lo_bits = x.astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+    lo = lo_bits.view(np.float32).astype(np.float64)
+    hi = (lo_bits + np.uint32(0x10000)).view(np.float32).astype(np.float64)
+    gap = np.abs(hi - lo)
+    near = (np.abs(x - 0.5 * (lo + hi)) <= window * np.abs(x)) & (x != 0)
+    return (near * gap) @ np.abs(Wg).T
+
+
 # ---- MoE layer / lm_head --------------------------------------------------
 def rms_norm(h_bf16, eps):
     """Unit-weight RMS norm of each bf16 row -> bf16 (uint16 bits)."""

@@ -25,13 +25,21 @@ class OracleLayer:
 
     def route(self, h, k, rms_eps=0.0):
         x = orc.rms_norm(h, rms_eps) if rms_eps > 0 else h
-        return orc.route(x, self.Wg, self.bias, k)
+        r = orc.route(x, self.Wg, self.bias, k)
+        if rms_eps > 0:
+            r["zslack"] = orc.rms_norm_slack(h, rms_eps, self.Wg)
+        return r
 
     def forward(self, h, k, w4a4, residual, routing=None, rms_eps=0.0):
         """One MoE block: x = RMSNorm(h) when rms_eps > 0 (else x = h), route(x),
         experts(x), plus h when residual."""
         x = orc.rms_norm(h, rms_eps) if rms_eps > 0 else h
-        r = orc.route(x, self.Wg, self.bias, k) if routing is None else routing
+        if routing is None:
+            r = orc.route(x, self.Wg, self.bias, k)
+            if rms_eps > 0:
+                r["zslack"] = orc.rms_norm_slack(h, rms_eps, self.Wg)
+        else:
+            r = routing
         self.ensure(r["idx"])
         out, outf = orc.moe_layer(x, r["idx"], r["w"], self.up, self.down, self.sh_up,
                                   self.sh_down, w4a4, h if residual else None, self.E)

@@ -47,14 +47,27 @@ def assert_close(got, ref, what=""):
 def check_routing(gpu_idx, gpu_w, orc, k):
     """Routing parity: indices must equal the oracle's; a difference is allowed
     only where the oracle's biased scores of the swapped experts are within
-    their binary32 error bounds (tau). Returns the number of exempted tokens."""
+    their binary32 error bounds (tau). Weights agree to 1e-5 relative, plus,
+    when the oracle routed a normalised input, what the input's bf16 rounding
+    decisions may move them by (zslack). Returns the number of exempted tokens."""
     gpu_idx = np.asarray(gpu_idx)
     T, E = orc["c"].shape
     exempt = 0
     for t in range(T):
         gi = list(gpu_idx[t])
         if gi == list(orc["idx"][t]):
-            np.testing.assert_allclose(gpu_w[t], orc["w"][t], rtol=1e-5, atol=1e-7)
+            bound = 0.0
+            if orc.get("zslack") is not None:
+                # the input's own bf16 rounding may differ (rms_norm_slack):
+                # sigma moves by at most slack / 4, w_j = sigma_j / S by at
+                # most (dsigma_j + w_j sum_l dsigma_l) / S
+                sel = orc["idx"][t]
+                sig = 1.0 / (1.0 + np.exp(-orc["z"][t][sel]))
+                ds = 0.25 * orc["zslack"][t][sel]
+                bound = (ds + orc["w"][t] * ds.sum()) / sig.sum()
+            err = np.abs(np.asarray(gpu_w[t], np.float64) - orc["w"][t])
+            assert (err <= 1e-7 + 1e-5 * np.abs(orc["w"][t]) + bound).all(), \
+                f"token {t}: weights {gpu_w[t]} vs {orc['w'][t]} (slack {bound})"
             continue
         c, tau = orc["c"][t], orc["tau"][t]
         assert len(set(gi)) == k and all(0 <= e < E for e in gi), f"token {t}: invalid {gi}"

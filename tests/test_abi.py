@@ -82,6 +82,12 @@ def test_host_validation_rejects_bad_arguments(abi):
                               sh_up, sh_dn)
     assert L.moe_expert_forward(ctypes.byref(nul), fake, fake, fake, 1, 6, 1, 0.0, null, fake, fake, need,
                                 null) == 1
+    # nvfp4_colblock_layout: null input, rows % 32, cols % 16, misaligned out
+    assert L.nvfp4_colblock_layout(null, fake, 1, 64, 32, fake, null) == 1
+    assert L.nvfp4_colblock_layout(fake, fake, 1, 48, 32, fake, null) == 2
+    assert L.nvfp4_colblock_layout(fake, fake, 1, 64, 24, fake, null) == 2
+    assert L.nvfp4_colblock_layout(fake, fake, 1, 64, 32, odd, null) == 3
+    assert L.nvfp4_colblock_layout(fake, fake, 0, 64, 32, fake, null) == 1
 
 
 def test_workspace_size_grows_with_tokens(abi):

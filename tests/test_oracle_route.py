@@ -77,3 +77,23 @@ def test_rms_norm_matches_numpy_and_torch_rounding():
     near = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).float().numpy()
     assert np.mean(near == got) > 0.999
     assert np.allclose(np.sqrt((got[:2] ** 2).mean(axis=1)), 1.0, atol=5e-3)  # row 3: eps dominates
+
+
+def test_rms_norm_slack_counts_only_elements_at_a_rounding_midpoint():
+    """rms_norm_slack: an all-ones row normalised to exactly the midpoint
+    between the bf16 neighbours 0.99609375 and 1.0 (eps = 1/m^2 - 1 with
+    m = 0.998046875) may round either way in every element: the slack of a
+    router row is then sum_i |Wg_i| * 2^-8. Away from a midpoint, for a zero
+    row, and without a norm, the slack is zero."""
+    ones = np.full((1, 4), 0x3F80, np.uint16)  # bf16 1.0
+    Wg = np.array([[1.0, -2.0, 0.5, 0.25], [0.0, 0.0, 0.0, 0.0]])
+    m = 0.998046875
+    s = orc.rms_norm_slack(ones, 1.0 / m ** 2 - 1.0, Wg)
+    np.testing.assert_allclose(s, [[3.75 * 2.0 ** -8, 0.0]], rtol=1e-12)
+    assert not orc.rms_norm_slack(ones, 1e-5, Wg).any()            # x = 0.999995: far from a midpoint
+    assert not orc.rms_norm_slack(np.zeros((1, 4), np.uint16), 1e-5, Wg).any()
+    assert not orc.rms_norm_slack(ones, 0.0, Wg).any()             # no norm
+    # real rows: a handful of near-midpoint elements at most
+    h, Wg2, _ = _setup(T=4, H=2688, E=8)
+    s2 = orc.rms_norm_slack(h, 1e-5, Wg2)
+    assert s2.shape == (4, 8) and (s2 >= 0).all() and s2.max() < 1e-2
