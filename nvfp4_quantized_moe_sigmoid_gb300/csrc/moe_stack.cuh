@@ -16,20 +16,21 @@
 //     4. wait for all E logits; sigmoid + bias top-k (rank per expert, every
 //        CTA computes the same selection), the step plan (unique experts);
 //        from here the producer streams the routed weights;
-//     5. its units: a unit is 16 rows of one expert's intermediate dimension
-//        (the shared expert's S/16 units, then the routed experts' I/16 each,
-//        split evenly over the CTAs). Per unit, the up tile (16 rows of W_up)
-//        gives 16 intermediate values relu^2 -> bf16, kept in shared memory,
-//        and their amax is posted per (expert, token) (W4A4);
-//     6. wait until every up tile of the experts it holds units of is done
-//        (per-expert counters): the row amax, and with it the per-tensor
+//     5. its units: a unit is 16 rows of one expert's intermediate dimension;
+//        each CTA takes units of one expert (the shared expert's S/16 are
+//        split over a fixed set of CTAs, each routed expert's I/16 over its
+//        share of the others). Per unit, the up tile (16 rows of W_up) gives
+//        16 intermediate values relu^2 -> bf16, kept in shared memory, and
+//        their amax is posted per (expert, token) (W4A4);
+//     6. count its up tiles on the expert's counter and wait (W4A4) until
+//        all of them are done: the row amax, and with it the per-tensor
 //        global of the intermediate row, is final. Quantise each unit's 16
 //        values (one NVFP4 block) as a down B operand;
 //     7. per unit, the matching 16 columns of W_down (all H rows; a
 //        column-block copy of W_down keeps them contiguous) times the unit's
-//        block: a split-K partial of the expert's output. Partials of one
-//        expert add up raw and are scaled once (gate x globals) into the CTA's
-//        FP32 partial of the layer output, written to the workspace; count it;
+//        block: a split-K partial of the expert's output, accumulated raw in
+//        registers and scaled once (gate x globals) into the CTA's FP32
+//        partial of the layer output in the workspace; count it;
 //     8. wait for every CTA's partial; add, for its share of the H rows, the
 //        G partials in CTA order and the residual: h_{l+1} = bf16(sum + h_l).
 //
@@ -214,13 +215,12 @@ struct StackCta {
     int last_cta;  // this CTA is the last to leave (resets the workspace)
     // geometry
     int G, b, ring_cap, ng, amax_stride;
-    int su_b, su_e;  // shared-expert units of this CTA
-    int ru_b, ru_e;  // routed units of this CTA (of U x I/16, this layer)
+    int cs;          // CTAs [0, cs) take the shared expert's units
+    int ex, ub, ue;  // this layer's units of this CTA: expert (-1 shared, else slot), [ub, ue) of its units
     uint8_t* ring_base;
     float* gsm;      // [ng][H] router rows
     uint16_t* X;     // [T][H] h_l, then x_l
     __half* xq;      // [T][H] up B operand
-    float* ysm;      // [T][H] FP32 partial of the layer output (aliases X, xq)
     uint16_t* uact;  // [units][T][16] bf16 relu^2 values of this CTA's units
     __half* ubq;     // [units][T][16] their down B operands
     float* tk_c;     // [T][E] biased scores
@@ -230,7 +230,8 @@ struct StackCta {
     float norm_inv[kDecodeMaxT];
     float gx[kDecodeMaxT];
     unsigned int red[kDecodeMaxT];
-    float fct[kMaxUnits][kDecodeMaxT];  // per unit and token: gate x down global x B global
+    float fct[kDecodeMaxT];             // per token: gate x down global (x B global)
+    float gb[kDecodeMaxT];              // per token: the down B global (W4A4)
     int sel_idx[kDecodeMaxT][kDecodeMaxK];
     float sel_sig[kDecodeMaxT][kDecodeMaxK];
     float sel_w[kDecodeMaxT][kDecodeMaxK];
@@ -582,18 +583,54 @@ __device__ __noinline__ void st_layer_globals(StackCta& c) {
     consumer_bar();
 }
 
-// ---------------------------------------------------------------- steps 5, 6
-// Up tiles [base, base + n), the CTA's units j0 .. j0 + n - 1: shared
-// (routed == false, tiles su_b + i) or routed (tiles i of the U x I/16 list
-// from ru_b). relu^2 -> bf16 values of the unit (shared memory), their amax
-// per (expert, token) (W4A4; counted once per CTA in step 6). Returns false on
-// a timeout.
+// ---------------------------------------------------------------- units
+// Every CTA works on units of one expert per layer: the shared expert's RS
+// units go evenly to CTAs [0, cs), cs = G RS / (RS + Umax RI) (at least 1, at
+// most G - Umax, Umax = min(T k, E)); the U routed experts' RI units each to
+// the other Gr = G - cs CTAs, expert slot u to CTAs [cs + Gr u / U,
+// cs + Gr (u + 1) / U), evenly. The shared CTAs' share does not depend on the
+// routing, so their weights stream before the plan exists. Every CTA and its
+// producer compute the same ranges.
+struct UnitRange {
+    int ex, ub, ue;  // expert (-1 shared, else routed slot), units [ub, ue) of it
+};
+
+__host__ __device__ inline int stack_shared_ctas(int G, int RS, int RI, int Umax) {
+    const int cs = static_cast<int>((long long)G * RS / (RS + (long long)Umax * RI));
+    return cs < 1 ? 1 : (cs > G - Umax ? G - Umax : cs);
+}
+
+__device__ __forceinline__ UnitRange stack_units(int b, int G, int cs, int RS, int RI, int U) {
+    UnitRange r;
+    if (b < cs) {
+        r.ex = -1;
+        r.ub = RS * b / cs;
+        r.ue = RS * (b + 1) / cs;
+        return r;
+    }
+    const int Gr = G - cs, bb = b - cs;
+    int u = bb * U / Gr;
+    while (u > 0 && Gr * u / U > bb) --u;
+    while (u + 1 < U && Gr * (u + 1) / U <= bb) ++u;
+    const int c0 = Gr * u / U, nc = Gr * (u + 1) / U - c0;
+    r.ex = u;
+    r.ub = RI * (bb - c0) / nc;
+    r.ue = RI * (bb - c0 + 1) / nc;
+    return r;
+}
+
+// ---------------------------------------------------------------- step 5
+// Up tiles [base, base + n): the CTA's units (of expert ex: -1 shared, else
+// routed slot). relu^2 -> bf16 values of each unit (shared memory), their
+// amax per (expert, token) (W4A4; counted once per CTA in step 6). Returns
+// false on a timeout.
 template <bool W4A4>
-__device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l, int base, int n, bool routed,
-                                         int ru_b, int j0) {
+__device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l, int base, int n, int ex) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
-    const int T = a.T, k = a.k, H = a.H, I = a.I, RI = I >> 4;
+    const int T = a.T, k = a.k, H = a.H;
+    const bool routed = ex >= 0;
+    const int u = routed ? ex : 0;
     unsigned int* const amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
     const __half* bcol = g < T ? c.xq + (size_t)g * H : nullptr;
     const int end = base + n;
@@ -604,7 +641,6 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
         const bool lead = bgroup_tile(c, li, H, bcol, acc, ok);
         if (!ok) return false;
         if (!lead) continue;
-        const int u = routed ? (ru_b + (li - base)) / RI : 0;
         const float gw = routed ? c.up_g[u] : c.shu_g;
         float m[2] = {0.0f, 0.0f};
 #pragma unroll
@@ -616,7 +652,7 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
             const float gs = W4A4 ? __fmul_rn(gw, c.gx[t]) : gw;
             const float rl = fmaxf(__fmul_rn(acc[v], gs), 0.0f);
             const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
-            c.uact[((size_t)(j0 + li - base) * T + t) * kUnitRows + g + 8 * (v >> 1)] =
+            c.uact[((size_t)(li - base) * T + t) * kUnitRows + g + 8 * (v >> 1)] =
                 *reinterpret_cast<const uint16_t*>(&bv);
             m[v & 1] = fmaxf(m[v & 1], __bfloat162float(bv));
         }
@@ -645,66 +681,61 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
 }
 
 // ---------------------------------------------------------------- step 6
-// The down B operands of this CTA's units. In W4A4 it first waits until every
-// up tile of each expert it holds units of is done, so that the intermediate
-// row amax is final; then each (unit, token) block of 16 values is quantised
-// under the row global amax / 2688 (W4A4) or converted to f16 (W4A16), and
-// its factor gate x down global (x B global in W4A4) recorded; a token that
-// does not route to the unit's expert gets a zero block and factor. Also
-// zeroes the FP32 partial, which aliases the up tiles' operands (all of this
-// CTA's up tiles are done). Returns false if a wait failed.
+// The down B operands of this CTA's units. It counts its up tiles on its
+// expert's counter (one release, after the CTA barrier that orders every
+// warp's amax updates before it); in W4A4 it then waits until every up tile
+// of the expert is done, so that the intermediate row amax is final. Each
+// (unit, token) block of 16 values is quantised under the row global
+// amax / 2688 (W4A4) or converted to f16 (W4A16), and the factor per token
+// gate x down global (x B global in W4A4) recorded; a token that does not
+// route to the expert gets a zero block and factor. Returns false if a wait
+// failed.
 template <bool W4A4>
 __device__ __noinline__ bool st_down_prep(const StackArgs& a, StackCta& c, int l) {
     const int ctid = threadIdx.x;
-    const int T = a.T, k = a.k, H = a.H, RI = a.I >> 4, RS = a.S >> 4;
+    const int T = a.T, k = a.k, RI = a.I >> 4, RS = a.S >> 4;
     int* const cnt = layer_cnt(a, l);
-    const int n_su = c.su_e - c.su_b, n_ru = c.ru_e - c.ru_b, nu = n_su + n_ru;
-    consumer_bar();
-    // this CTA's up tiles are done: count them, per expert, in one release
-    // each (the CTA barrier orders every warp's amax updates before it)
-    if (ctid == 0 && n_su > 0) red_release_add(cnt + kCntShUp, n_su);
-    if (ctid == 32 && n_ru > 0) {
-#pragma unroll 1
-        for (int u = c.ru_b / RI; u <= (c.ru_e - 1) / RI; ++u)
-            red_release_add(cnt + kCntUp + u, min(c.ru_e, (u + 1) * RI) - max(c.ru_b, u * RI));
-    }
-#pragma unroll 1
-    for (int i = ctid; i < T * H / 4; i += kConsumerThreads)
-        reinterpret_cast<float4*>(c.ysm)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const int ex = c.ex, nu = c.ue - c.ub;
+    int* const ecnt = cnt + (ex < 0 ? kCntShUp : kCntUp + ex);
+    consumer_bar();  // every up tile of this CTA is done
     bool ok = true;
-    if (W4A4) {
-        if (ctid == 0 && n_su > 0) ok = wait_geq(cnt + kCntShUp, RS, abort_flag(a));
-        if (ctid == 32 && n_ru > 0) {
-#pragma unroll 1
-            for (int u = c.ru_b / RI; u <= (c.ru_e - 1) / RI && ok; ++u)
-                ok = wait_geq(cnt + kCntUp + u, RI, abort_flag(a));
-        }
+    if (ctid == 0 && nu > 0) {
+        red_release_add(ecnt, nu);
+        if (W4A4) ok = wait_geq(ecnt, ex < 0 ? RS : RI, abort_flag(a));
     }
     if (consumer_bar_or(!ok || cta_abort(c))) return false;
     const unsigned int* amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
+    if (ctid < T) {  // the factor per token
+        const int t = ctid;
+        int jj = 0;
+        float gate = 1.0f, dg = c.shd_g;
+        if (ex >= 0) {
+            jj = c.plan.choice[ex][t];
+            gate = c.plan.gate[ex][t];
+            dg = c.down_g[ex];
+        }
+        float f = 0.0f;
+        if (jj >= 0 && nu > 0) {
+            const float gB = W4A4 ? __fdiv_rn(__uint_as_float(__ldcg(ex < 0 ? amax + T * k + t : amax + t * k + jj)),
+                                              2688.0f)
+                                  : 0.0f;
+            f = __fmul_rn(gate, W4A4 ? __fmul_rn(dg, gB) : dg);
+            c.gb[t] = gB;
+        }
+        c.fct[t] = f;
+    }
+    consumer_bar();
 #pragma unroll 1
     for (int i = ctid; i < nu * T; i += kConsumerThreads) {
         const int j = i / T, t = i - j * T;
-        bool used = true;
-        float gate = 1.0f, dg = c.shd_g;
-        const unsigned int* am = amax + T * k + t;
-        if (j >= n_su) {
-            const int u = (c.ru_b + j - n_su) / RI;
-            const int jj = c.plan.choice[u][t];
-            used = jj >= 0;
-            gate = c.plan.gate[u][t];
-            dg = c.down_g[u];
-            am = amax + t * k + (used ? jj : 0);
-        }
         uint4 u0 = make_uint4(0, 0, 0, 0), u1 = make_uint4(0, 0, 0, 0);
-        if (used) {
+        if (ex < 0 || c.plan.choice[ex][t] >= 0) {  // else the token's values were never written
             const uint4* src = reinterpret_cast<const uint4*>(c.uact + ((size_t)j * T + t) * kUnitRows);
             u0 = src[0];
             u1 = src[1];
         }
-        const float g = W4A4 && used ? __fdiv_rn(__uint_as_float(__ldcg(am)), 2688.0f) : 0.0f;
-        b_block_store<W4A4>(u0, u1, g, reinterpret_cast<uint4*>(c.ubq + ((size_t)j * T + t) * kUnitRows));
-        c.fct[j][t] = used ? __fmul_rn(gate, W4A4 ? __fmul_rn(dg, g) : dg) : 0.0f;
+        b_block_store<W4A4>(u0, u1, W4A4 ? c.gb[t] : 0.0f,
+                            reinterpret_cast<uint4*>(c.ubq + ((size_t)j * T + t) * kUnitRows));
     }
     consumer_bar();
     return true;
@@ -714,16 +745,16 @@ __device__ __noinline__ bool st_down_prep(const StackArgs& a, StackCta& c, int l
 // The down column blocks of this CTA's units (ring items base .. base + nu - 1),
 // by every consumer warp: warp w takes the 32-row pairs [P w / 12,
 // P (w + 1) / 12) of the H rows (P = H / 32) of every block. The raw products
-// of one expert's units add up in registers (FP32); when the expert changes,
-// and after the last unit, they are added, times the unit's factor per token,
-// into the FP32 partial ysm (rows of this warp only). Returns false on a
+// add up in registers (FP32; one expert, so one factor per token); the warp
+// then writes factor x sum for its rows to the CTA's partial in the
+// workspace, and the CTA counts it once every warp has. Returns false on a
 // timeout.
-__device__ __noinline__ bool st_down_units(const StackArgs& a, StackCta& c, int base) {
+__device__ __noinline__ bool st_down_units(const StackArgs& a, StackCta& c, int l, int base) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
-    const int T = a.T, H = a.H, RI = a.I >> 4, P = H >> 5;
+    const int T = a.T, H = a.H, P = H >> 5;
     const int p0 = P * warp / kConsumerWarps, np = P * (warp + 1) / kConsumerWarps - p0;
-    const int n_su = c.su_e - c.su_b, nu = n_su + (c.ru_e - c.ru_b);
+    const int nu = c.ue - c.ub;
     BRing& r = c.br;
     float acc[kDownMaxPairs][2][4];
 #pragma unroll
@@ -732,47 +763,9 @@ __device__ __noinline__ bool st_down_units(const StackArgs& a, StackCta& c, int 
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int v = 0; v < 4; ++v) acc[p][mt][v] = 0.0f;
-    // acc x fct[j] into ysm; acc = 0. The factors are read first and each
-    // pair's eight partial values are all loaded before any is stored (the
-    // stores could alias the factor table for all the compiler knows, which
-    // would otherwise serialise every load behind the previous store).
-    auto flush = [&](int j) {
-        const bool t0 = 2 * q < T, t1 = 2 * q + 1 < T;
-        const float f0 = t0 ? c.fct[j][2 * q] : 0.0f, f1 = t1 ? c.fct[j][2 * q + 1] : 0.0f;
-        float* const y0 = c.ysm + (size_t)(2 * q) * H + 32 * p0 + g;
-        float* const y1 = y0 + H;
-#pragma unroll
-        for (int p = 0; p < kDownMaxPairs; ++p) {
-            if (p >= np) break;
-            float y[2][4];
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const int o = 32 * p + 16 * mt + 8 * (v >> 1);
-                    y[mt][v] = (v & 1) ? (t1 ? y1[o] : 0.0f) : (t0 ? y0[o] : 0.0f);
-                }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const int o = 32 * p + 16 * mt + 8 * (v >> 1);
-                    if (v & 1) {
-                        if (t1) y1[o] = __fmaf_rn(f1, acc[p][mt][v], y[mt][v]);
-                    } else if (t0) {
-                        y0[o] = __fmaf_rn(f0, acc[p][mt][v], y[mt][v]);
-                    }
-                    acc[p][mt][v] = 0.0f;
-                }
-        }
-    };
     bool ok = true;
-    int seg = -2;  // expert of the units in acc (-1: the shared expert)
 #pragma unroll 1
     for (int j = 0; j < nu; ++j) {
-        const int ex = j < n_su ? -1 : (c.ru_b + j - n_su) / RI;
-        if (j > 0 && ex != seg) flush(j - 1);
-        seg = ex;
         const int li = base + j, s = li % kSlots;
         const bool waited = mbar_wait_bounded(&r.full[s], static_cast<uint32_t>((li / kSlots) & 1));
         const bool got = __all_sync(0xffffffffu, waited);
@@ -810,26 +803,30 @@ __device__ __noinline__ bool st_down_units(const StackArgs& a, StackCta& c, int 
             break;
         }
     }
-    if (ok && nu > 0) flush(nu - 1);
-    return ok;
-}
-
-// The CTA's FP32 partial to the workspace (each warp its own rows), counted
-// once the whole CTA has written it.
-__device__ __noinline__ void st_part_write(const StackArgs& a, StackCta& c, int l) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int T = a.T, H = a.H, P = H >> 5;
-    const int r0 = 32 * (P * warp / kConsumerWarps), r1 = 32 * (P * (warp + 1) / kConsumerWarps);
-    __syncwarp();
-    float* const dst = a.ws.part + (size_t)c.b * T * H;
-#pragma unroll 1
-    for (int t = 0; t < T; ++t)
-#pragma unroll 1
-        for (int i = r0 + 4 * lane; i < r1; i += 128)
-            __stcg(reinterpret_cast<float4*>(dst + (size_t)t * H + i),
-                   *reinterpret_cast<const float4*>(c.ysm + (size_t)t * H + i));
-    consumer_bar();
+    // factor x sum -> this CTA's partial: lane (g, q) holds rows g, g + 8 of
+    // each 16-row tile for tokens 2q, 2q + 1
+    const bool t0 = 2 * q < T, t1 = 2 * q + 1 < T;
+    const float f0 = t0 ? c.fct[2 * q] : 0.0f, f1 = t1 ? c.fct[2 * q + 1] : 0.0f;
+    float* const d0 = a.ws.part + ((size_t)c.b * T + 2 * q) * H + 32 * p0 + g;
+    float* const d1 = d0 + H;
+#pragma unroll
+    for (int p = 0; p < kDownMaxPairs; ++p) {
+        if (p >= np) break;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int o = 32 * p + 16 * mt + 8 * (v >> 1);
+                if (v & 1) {
+                    if (t1) __stcg(d1 + o, __fmul_rn(f1, acc[p][mt][v]));
+                } else if (t0) {
+                    __stcg(d0 + o, __fmul_rn(f0, acc[p][mt][v]));
+                }
+            }
+    }
+    if (consumer_bar_or(!ok || cta_abort(c))) return false;
     if (threadIdx.x == 0) red_release_add(layer_cnt(a, l) + kCntPart, 1);
+    return true;
 }
 
 // ---------------------------------------------------------------- step 8
@@ -858,9 +855,9 @@ __device__ __noinline__ bool st_reduce(const StackArgs& a, StackCta& c, int l) {
     uint16_t* out = a.hidden_out + (size_t)l * T * H;
     const int h0 = share_begin32(H, c.b, G), nr = share_begin32(H, c.b + 1, G) - h0;
     const int items = T * nr, nch = (G + kPartChunk - 1) / kPartChunk;
-    // the chunk sums, [chunk][item], in ysm (its rows are in the workspace
-    // now): T nr nch <= T (H/G + 1)(G/8 + 1) floats, within its T H
-    float* const csum = c.ysm;
+    // the chunk sums, [chunk][item], over the (dead) layer input and up B
+    // operand: T nr nch <= T (H/G + 1)(G/8 + 1) floats, within their T H
+    float* const csum = reinterpret_cast<float*>(c.X);
 #pragma unroll 1
     for (int i = ctid; i < items * nch; i += kConsumerThreads) {
         const int ch = i / items, it = i - ch * items;
@@ -893,14 +890,14 @@ __device__ __noinline__ bool st_reduce(const StackArgs& a, StackCta& c, int l) {
 }
 
 // ---------------------------------------------------------------- producer
-// Per layer l the items go out in the order the consumers take them: the
-// up tiles of the CTA's shared-expert units (before the plan exists, while
-// the previous layer finishes), then, once the plan is posted, the up tiles
-// of its routed units, and the down column blocks of its shared, then routed
-// units. All items are 9 H bytes. The producer is one thread among twelve
-// busy warps, so its per-item work is kept short: the ring position lives in
-// registers (phys = vhead mod cap, advanced without divisions), the routed
-// addresses advance without divisions, and all items go through one fill site.
+// Per layer l the items go out in the order the consumers take them: the up
+// tiles of the CTA's units, then their down column blocks; a shared-expert
+// CTA issues them before the plan of layer l exists (right after the plan of
+// layer l - 1, so they stream while that layer finishes), a routed CTA once
+// the plan is posted. All items are 9 H bytes. The producer is one thread
+// among twelve busy warps, so its per-item work is kept short: the ring
+// position lives in registers (phys = vhead mod cap, advanced without
+// divisions) and all items go through one fill site.
 __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
     const int H = a.H, I = a.I, RI = I >> 4;
     const int G = c.G, b = c.b;
@@ -923,44 +920,40 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
         c.gate_issued += 1;
     };
     issue_gate(0);
+    const int RS = a.S >> 4;
+    const bool sh = b < c.cs;  // a shared-expert CTA: its units do not depend on the plan
 #pragma unroll 1
     for (int l = 0; l < a.L && alive; ++l) {
         const StackLayer& P = a.layer[l];
-        int ru_b = 0, ru_e = 0;
 #pragma unroll 1
-        for (int sg = 0; sg < 4 && alive; ++sg) {
-            if (sg == 1) {  // the plan of layer l
+        for (int ph = 0; ph < 2 && alive; ++ph) {
+            if (ph == 1) {  // the plan of layer l
                 if (!mbar_wait_abortable(&c.pbar, l & 1, &c.abort_s)) {
                     set_cta_abort(c);
                     alive = false;
                     break;
                 }
                 if (l + 1 < a.L) issue_gate(l + 1);
-                const int NU = c.plan.U * RI;
-                ru_b = share_begin32(NU, b, G);
-                ru_e = share_begin32(NU, b + 1, G);
             }
-            // segment sg: units [i0, i0 + n); an up unit is 16 rows of W_up
-            // (codes, then scales, from two arrays), a down unit one column
-            // block (codes, then scales, contiguous)
-            const bool routed = sg & 1, up = sg < 2;
-            const int i0 = routed ? ru_b : c.su_b, n = routed ? ru_e - ru_b : c.su_e - c.su_b;
-            int u = routed ? i0 / RI : 0, rr = routed ? i0 - u * RI : i0;
+            if ((ph == 0) != sh) continue;
+            // the units' up tiles (16 rows of W_up: codes, then scales, from
+            // two arrays), then their down column blocks (codes, then scales,
+            // contiguous)
+            const UnitRange ur = stack_units(b, G, c.cs, RS, RI, sh ? 1 : c.plan.U);
+            const int n = ur.ue - ur.ub;
+            const int64_t e = sh ? 0 : c.plan.expert[ur.ex];
 #pragma unroll 1
-            for (int j = 0; j < n; ++j) {
+            for (int it = 0; it < 2 * n; ++it) {
+                const bool up = it < n;
+                const int rr = ur.ub + (up ? it : it - n);
                 const uint8_t *src_c, *src_s;
                 if (up) {
-                    const int64_t row = (routed ? (int64_t)c.plan.expert[u] * I : 0) + 16 * rr;
-                    src_c = (routed ? P.up_codes : P.shu_codes) + row * (H >> 1);
-                    src_s = (routed ? P.up_scales : P.shu_scales) + row * (H >> 4);
+                    const int64_t row = e * I + 16 * rr;
+                    src_c = (sh ? P.shu_codes : P.up_codes) + row * (H >> 1);
+                    src_s = (sh ? P.shu_scales : P.up_scales) + row * (H >> 4);
                 } else {
-                    const int64_t blk = (routed ? (int64_t)c.plan.expert[u] * RI : 0) + rr;
-                    src_c = (routed ? P.down_cb : P.shd_cb) + blk * size;
+                    src_c = (sh ? P.shd_cb : P.down_cb) + (e * RI + rr) * size;
                     src_s = src_c + 8 * H;
-                }
-                if (++rr == RI && routed) {
-                    rr = 0;
-                    ++u;
                 }
                 // item pli goes after the previous one, or at offset 0 if it
                 // would cross the end, once the item that last used its slot
@@ -1045,31 +1038,27 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
         st_topk_plan(a, c, l);
         st_layer_globals(c);
         if (ctid == 0) mbar_arrive(&c.pbar);  // the producer may stream the routed weights now
-        // 5. up tiles of the shared-expert units (staged during the previous
-        // layer), then of the routed units
-        const int NU = c.plan.U * RI;
-        const int ru_b = share_begin32(NU, b, G), ru_e = share_begin32(NU, b + 1, G);
-        const int n_su = c.su_e - c.su_b, n_ru = ru_e - ru_b;
+        // 5. up tiles of this CTA's units (one expert)
+        const UnitRange ur = stack_units(b, G, c.cs, a.S >> 4, RI, c.plan.U);
+        const int nu = ur.ue - ur.ub;
         if (ctid == 0) {  // read after the barrier that opens step 6
-            c.ru_b = ru_b;
-            c.ru_e = ru_e;
+            c.ex = ur.ex;
+            c.ub = ur.ub;
+            c.ue = ur.ue;
         }
-        if (!st_up_tiles<W4A4>(a, c, l, base, n_su, false, 0, 0)) set_cta_abort(c);
-        if (!st_up_tiles<W4A4>(a, c, l, base + n_su, n_ru, true, ru_b, n_su)) set_cta_abort(c);
-        base += n_su + n_ru;
+        if (!st_up_tiles<W4A4>(a, c, l, base, nu, ur.ex)) set_cta_abort(c);
+        base += nu;
         // 6. the units' down B operands
         if (!st_down_prep<W4A4>(a, c, l)) {
             bad = true;
             break;
         }
         // 7. the units' down column blocks -> this CTA's partial
-        if (!st_down_units(a, c, base)) set_cta_abort(c);
-        base += n_su + n_ru;
-        if (consumer_bar_or(cta_abort(c))) {
+        if (!st_down_units(a, c, l, base)) {
             bad = true;
             break;
         }
-        st_part_write(a, c, l);
+        base += nu;
         // 8. this CTA's rows of h_{l+1}
         if (!st_reduce(a, c, l)) {
             bad = true;
@@ -1115,14 +1104,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant
         c.ng = b < a.E ? (a.E - b + G - 1) / G : 0;
         c.amax_stride = a.T * a.k + a.T;
         const int RS = a.S >> 4;
-        c.su_b = share_begin32(RS, b, G);
-        c.su_e = share_begin32(RS, b + 1, G);
-        c.ru_b = c.ru_e = 0;
+        c.cs = stack_shared_ctas(G, RS, a.I >> 4, min(a.T * a.k, a.E));
+        c.ex = c.ub = c.ue = 0;
         c.ring_base = smem;
         c.gsm = reinterpret_cast<float*>(smem + a.off_gate);
         c.X = reinterpret_cast<uint16_t*>(smem + a.off_uni);
         c.xq = reinterpret_cast<__half*>(smem + a.off_uni + (size_t)a.T * a.H * 2);
-        c.ysm = reinterpret_cast<float*>(smem + a.off_uni);
         c.uact = reinterpret_cast<uint16_t*>(smem + a.off_uact);
         c.ubq = reinterpret_cast<__half*>(smem + a.off_ubq);
         c.tk_c = reinterpret_cast<float*>(smem + a.off_tk);

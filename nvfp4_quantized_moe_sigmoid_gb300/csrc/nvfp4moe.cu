@@ -1044,11 +1044,16 @@ StackWsOffsets stack_ws(int L, int T, int k, int E, int H, int G) {
 }
 
 // Units (16 intermediate rows of one expert) a CTA holds in one layer at
-// most: its share of the shared expert's S/16 and of the routed U x I/16,
-// U <= min(T k, E).
+// most, under the kernel's split (stack_units): the shared expert's S/16 over
+// cs CTAs, each routed expert's I/16 over at least (G - cs) / Umax CTAs,
+// Umax = min(T k, E); 0 if some expert would get no CTA (G <= Umax).
 int stack_max_units(int T, int k, int E, int I, int S, int G) {
-    const int U = std::min(T * k, E);
-    return (S / 16 + G - 1) / G + (U * (I / 16) + G - 1) / G;
+    const int Umax = std::min(T * k, E), RS = S / 16, RI = I / 16;
+    if (G <= Umax) return 0;
+    const int cs = stack_shared_ctas(G, RS, RI, Umax);
+    const int per_routed = (G - cs) / Umax;
+    if (per_routed < 1) return 0;
+    return std::max((RS + cs - 1) / cs, (RI + per_routed - 1) / per_routed);
 }
 
 // Dynamic shared memory of the stack kernel: the ring, then the router rows,
@@ -1104,8 +1109,8 @@ nvfp4_status check_stack(const moe_stack_layer* layers, int32_t L, int32_t T, in
     if (T > kDecodeMaxT || k > kDecodeMaxK || w0.num_experts > 256 || w0.num_experts % 8) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     // the down step's warps hold at most kDownMaxPairs 32-row pairs each
     if (w0.hidden > 32 * kDownMaxPairs * kConsumerWarps) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (stack_max_units(T, k, w0.num_experts, w0.inter, w0.shared_inter, num_sms()) > kMaxUnits)
-        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const int mu = stack_max_units(T, k, w0.num_experts, w0.inter, w0.shared_inter, num_sms());
+    if (mu < 1 || mu > kMaxUnits) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     return NVFP4_OK;
 }
 
