@@ -236,6 +236,7 @@ struct StackCta {
     float sel_sig[kDecodeMaxT][kDecodeMaxK];
     float sel_w[kDecodeMaxT][kDecodeMaxK];
     float zred[kConsumerWarps][kDecodeMaxT];
+    float wmax[kConsumerWarps];
     // per-tensor globals of this layer's unique experts and shared expert
     float up_g[kDecodeMaxU], down_g[kDecodeMaxU];
     float shu_g, shd_g;
@@ -463,6 +464,115 @@ __device__ __noinline__ bool st_router(const StackArgs& a, StackCta& c, int l) {
     return true;
 }
 
+constexpr int kT1MaxNg = 2;  // router rows per CTA on the one-token path
+
+template <bool W4A4>
+__device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c, const uint16_t* h, int l) {
+    const int ctid = threadIdx.x, warp = ctid >> 5, lane = ctid & 31;
+    const int H = a.H, E = a.E;
+    if (ctid == kConsumerThreads - 1) {  // used by the epilogues later in the layer
+        c.shu_g = __ldg(a.layer[l].shu_global);
+        c.shd_g = __ldg(a.layer[l].shd_global);
+    }
+    const int i = 8 * ctid;
+    const bool mine = i < H;
+    uint4 hv = make_uint4(0, 0, 0, 0);
+    if (mine) hv = __ldcg(reinterpret_cast<const uint4*>(h + i));
+    uint32_t w[4] = {hv.x, hv.y, hv.z, hv.w};
+    if (a.rms_eps > 0.0f) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float x0 = __uint_as_float(w[j] << 16), x1 = __uint_as_float(w[j] & 0xFFFF0000u);
+            ss = __fmaf_rn(x0, x0, ss);
+            ss = __fmaf_rn(x1, x1, ss);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        if (lane == 0) c.norm_part[0][warp] = ss;
+        consumer_bar();
+        const int nch = (H + 255) >> 8;
+        float sum = 0.0f;
+#pragma unroll 1
+        for (int ch = 0; ch < nch; ++ch) sum = __fadd_rn(sum, c.norm_part[0][ch]);
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, static_cast<float>(H)), a.rms_eps)));
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = bf16x2_rn(__fmul_rn(__uint_as_float(w[j] << 16), inv),
+                             __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), inv));
+    }
+    // router partials of this thread's eight elements, the row amax
+    const bool ok = mbar_wait_bounded(&c.gbar, static_cast<uint32_t>(l & 1));
+    float zp[kT1MaxNg] = {0.0f, 0.0f};
+    float mx = 0.0f;
+    if (mine) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+        if (ok) {
+#pragma unroll
+            for (int r = 0; r < kT1MaxNg; ++r) {
+                if (r < c.ng) {
+                    const float4* g4 = reinterpret_cast<const float4*>(c.gsm + (size_t)r * H + i);
+                    const float4 ga = g4[0], gb = g4[1];
+                    const float gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        zp[r] = fmaf(gw[2 * j], __uint_as_float(w[j] << 16), zp[r]);
+                        zp[r] = fmaf(gw[2 * j + 1], __uint_as_float(w[j] & 0xFFFF0000u), zp[r]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+        for (int r = 0; r < kT1MaxNg; ++r) zp[r] = __fadd_rn(zp[r], __shfl_xor_sync(0xffffffffu, zp[r], o));
+    }
+    if (lane == 0) {
+        c.wmax[warp] = mx;
+#pragma unroll
+        for (int r = 0; r < kT1MaxNg; ++r) c.zred[warp][r] = zp[r];
+    }
+    if (consumer_bar_or(!ok || cta_abort(c))) {
+        if (ctid == 0 && !ok) set_dev_error(kErrWaitFull);
+        return false;
+    }
+    // the logits of this CTA's experts, warps added in order (first: every
+    // CTA waits for them), by the last thread: its warp holds no input
+    // elements when H <= 8 x 352, and warp 0 waits for the logits next
+    if (ctid == kConsumerThreads - 1 && c.ng > 0) {
+        float* z = a.ws.z + (size_t)l * E;
+#pragma unroll 1
+        for (int r = 0; r < c.ng; ++r) {
+            float s = 0.0f;
+#pragma unroll
+            for (int ww = 0; ww < kConsumerWarps; ++ww) s = __fadd_rn(s, c.zred[ww][r]);
+            z[c.b + r * c.G] = s;
+        }
+        red_release_add(layer_cnt(a, l) + kCntLogits, c.ng);
+    }
+    // the B operand: each even lane quantises the 16-block it shares with the
+    // next lane, under the row global amax / 2688 (W4A4)
+    float g = 0.0f;
+    if (W4A4) {
+        float rm = 0.0f;
+#pragma unroll
+        for (int ww = 0; ww < kConsumerWarps; ++ww) rm = fmaxf(rm, c.wmax[ww]);
+        g = __fdiv_rn(rm, 2688.0f);
+        if (ctid == 0) c.gx[0] = g;
+    }
+    uint32_t p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) p[j] = __shfl_down_sync(0xffffffffu, w[j], 1);
+    if (mine && (lane & 1) == 0)
+        b_block_store<W4A4>(make_uint4(w[0], w[1], w[2], w[3]), make_uint4(p[0], p[1], p[2], p[3]), g,
+                            reinterpret_cast<uint4*>(c.xq + i));
+    return true;
+}
+
 // ---------------------------------------------------------------- step 4
 // Top-k by (sigma + bias desc, index asc) for every token, its gates
 // sigma / sum(sigma), and the step plan. Every CTA computes the same result.
@@ -568,6 +678,89 @@ __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l
 #pragma unroll
         for (int w = 0; w < 8; ++w) u += __popc(c.plan.bits[w]);
         c.plan.U = u;
+    }
+    consumer_bar();
+}
+
+// Step 4 for one token: the sigmoids and keys as in st_topk_plan (one expert
+// per thread), then warp 0 alone picks the top k, writes the plan (with one
+// token the k picks are the unique experts; slot u holds the u-th smallest
+// id, as in the general plan) and the unique experts' per-tensor globals; one
+// CTA barrier publishes it (three fewer than the general plan and
+// st_layer_globals).
+__device__ __noinline__ void st_topk_plan_t1(const StackArgs& a, StackCta& c, int l) {
+    const int ctid = threadIdx.x, lane = ctid & 31;
+    const int E = a.E, k = a.k;
+    uint32_t* const keys = reinterpret_cast<uint32_t*>(c.tk_c);
+    const float* const z = a.ws.z + (size_t)l * E;
+    if (ctid < E) {
+        const float s = __frcp_rn(__fadd_rn(1.0f, expf(-__ldcg(z + ctid))));
+        float v = __fadd_rn(s, c.bias_s[ctid]);
+        if (v != v) v = -INFINITY;
+        c.tk_s[ctid] = s;
+        keys[ctid] = order_key(__fadd_rn(v, 0.0f));  // -0 and +0 compare equal
+    }
+    consumer_bar();
+    if (ctid < 32) {
+        uint32_t key[kTopkPerLane];
+        float sg[kTopkPerLane];
+#pragma unroll
+        for (int q = 0; q < kTopkPerLane; ++q) {
+            const int e = lane + 32 * q;
+            key[q] = e < E ? keys[e] : 0u;
+            sg[q] = e < E ? c.tk_s[e] : 0.0f;
+        }
+        float ssum = 0.0f, my_s = 0.0f;
+        int my_e = 0x7FFFFFFF;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            // this lane's best: largest key, then smallest index (smaller q)
+            uint32_t bk = 0u;
+            int bq = 0;
+#pragma unroll
+            for (int q = 0; q < kTopkPerLane; ++q)
+                if (key[q] > bk) {
+                    bk = key[q];
+                    bq = q;
+                }
+            const uint32_t km = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t cand = (bk == km && bk != 0u) ? static_cast<uint32_t>(lane + 32 * bq) : 0xFFFFFFFFu;
+            const int es = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+            const int qs = es >> 5;
+            float pick = 0.0f;
+#pragma unroll
+            for (int q = 0; q < kTopkPerLane; ++q)
+                if (q == qs) {
+                    pick = sg[q];
+                    if (lane == (es & 31)) key[q] = 0u;  // taken
+                }
+            const float sj = __shfl_sync(0xffffffffu, pick, es & 31);
+            ssum = __fadd_rn(ssum, sj);
+            if (lane == j) {
+                my_e = es;
+                my_s = sj;
+            }
+        }
+        int slot = 0;
+#pragma unroll 1
+        for (int jj = 0; jj < k; ++jj)
+            if (__shfl_sync(0xffffffffu, my_e, jj) < my_e) ++slot;
+        if (lane < k) {
+            const float wj = __fdiv_rn(my_s, ssum);
+            if (c.b == 0) {
+                a.topk_idx[(size_t)l * k + lane] = my_e;
+                a.topk_w[(size_t)l * k + lane] = wj;
+            }
+            c.plan.expert[slot] = my_e;
+#pragma unroll
+            for (int t = 0; t < kDecodeMaxT; ++t) {
+                c.plan.choice[slot][t] = static_cast<int8_t>(t == 0 ? lane : -1);
+                c.plan.gate[slot][t] = t == 0 ? wj : 0.0f;
+            }
+            c.up_g[slot] = c.upg_s[my_e];
+            c.down_g[slot] = c.dng_s[my_e];
+        }
+        if (lane == 0) c.plan.U = k;
     }
     consumer_bar();
 }
@@ -1005,6 +1198,7 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
     const int G = c.G, b = c.b;
     int base = 0;  // first ring item of the current step
     bool bad = false;
+    const bool one_token = T == 1 && H <= 8 * kConsumerThreads && c.ng <= kT1MaxNg;
 #pragma unroll 1
     for (int l = 0; l < a.L; ++l) {
         int* const cnt = layer_cnt(a, l);
@@ -1017,11 +1211,19 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
                 break;
             }
         }
-        st_input<W4A4>(a, c, l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H, l);
-        // 3. router logits (the wait also covers the staged bias)
-        if (!st_router(a, c, l)) {
-            bad = true;
-            break;
+        const uint16_t* const hin = l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H;
+        if (one_token) {  // 1-3 for one token from registers
+            if (!st_input_router_t1<W4A4>(a, c, hin, l)) {
+                bad = true;
+                break;
+            }
+        } else {
+            st_input<W4A4>(a, c, hin, l);
+            // 3. router logits (the wait also covers the staged bias)
+            if (!st_router(a, c, l)) {
+                bad = true;
+                break;
+            }
         }
         // 4. top-k and plan as soon as every logit is posted (and the producer
         // has stopped reading the previous plan), so that the routed weights
@@ -1035,8 +1237,12 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
                 break;
             }
         }
-        st_topk_plan(a, c, l);
-        st_layer_globals(c);
+        if (one_token) {
+            st_topk_plan_t1(a, c, l);
+        } else {
+            st_topk_plan(a, c, l);
+            st_layer_globals(c);
+        }
         if (ctid == 0) mbar_arrive(&c.pbar);  // the producer may stream the routed weights now
         // 5. up tiles of this CTA's units (one expert)
         const UnitRange ur = stack_units(b, G, c.cs, a.S >> 4, RI, c.plan.U);
