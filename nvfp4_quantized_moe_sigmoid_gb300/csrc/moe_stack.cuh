@@ -892,32 +892,34 @@ __device__ __noinline__ bool st_down_prep(const StackArgs& a, StackCta& c, int l
     int* const ecnt = cnt + (ex < 0 ? kCntShUp : kCntUp + ex);
     consumer_bar();  // every up tile of this CTA is done
     bool ok = true;
-    if (ctid == 0 && nu > 0) {
-        red_release_add(ecnt, nu);
-        if (W4A4) ok = wait_geq(ecnt, ex < 0 ? RS : RI, abort_flag(a));
+    if (ctid == 0) {
+        if (nu > 0) {
+            red_release_add(ecnt, nu);
+            if (W4A4) ok = wait_geq(ecnt, ex < 0 ? RS : RI, abort_flag(a));
+        }
+        // the factor per token (the amax is final once the count is)
+        const unsigned int* amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            int jj = 0;
+            float gate = 1.0f, dg = c.shd_g;
+            if (ex >= 0) {
+                jj = c.plan.choice[ex][t];
+                gate = c.plan.gate[ex][t];
+                dg = c.down_g[ex];
+            }
+            float f = 0.0f;
+            if (ok && jj >= 0 && nu > 0) {
+                const float gB =
+                    W4A4 ? __fdiv_rn(__uint_as_float(__ldcg(ex < 0 ? amax + T * k + t : amax + t * k + jj)), 2688.0f)
+                         : 0.0f;
+                f = __fmul_rn(gate, W4A4 ? __fmul_rn(dg, gB) : dg);
+                c.gb[t] = gB;
+            }
+            c.fct[t] = f;
+        }
     }
     if (consumer_bar_or(!ok || cta_abort(c))) return false;
-    const unsigned int* amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
-    if (ctid < T) {  // the factor per token
-        const int t = ctid;
-        int jj = 0;
-        float gate = 1.0f, dg = c.shd_g;
-        if (ex >= 0) {
-            jj = c.plan.choice[ex][t];
-            gate = c.plan.gate[ex][t];
-            dg = c.down_g[ex];
-        }
-        float f = 0.0f;
-        if (jj >= 0 && nu > 0) {
-            const float gB = W4A4 ? __fdiv_rn(__uint_as_float(__ldcg(ex < 0 ? amax + T * k + t : amax + t * k + jj)),
-                                              2688.0f)
-                                  : 0.0f;
-            f = __fmul_rn(gate, W4A4 ? __fmul_rn(dg, gB) : dg);
-            c.gb[t] = gB;
-        }
-        c.fct[t] = f;
-    }
-    consumer_bar();
 #pragma unroll 1
     for (int i = ctid; i < nu * T; i += kConsumerThreads) {
         const int j = i / T, t = i - j * T;
@@ -956,41 +958,53 @@ __device__ __noinline__ bool st_down_units(const StackArgs& a, StackCta& c, int 
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int v = 0; v < 4; ++v) acc[p][mt][v] = 0.0f;
+    // one unit's products into acc: B (token g's block, elements 4q .. 4q + 3,
+    // the MMA's k-slots 2q, 2q + 1, 2q + 8, 2q + 9 in the order the block's
+    // layout gives the weights) times this warp's rows of block blk
+    auto unit_mma = [&](const uint8_t* blk, uint2 bv) {
+        const uint8_t* cw = blk + (size_t)p0 * 256 + lane * 8;
+        const uint8_t* sw = blk + (size_t)8 * H + (size_t)p0 * 32 + g * 4;
+#pragma unroll
+        for (int p = 0; p < kDownMaxPairs; ++p) {
+            if (p >= np) break;
+            const uint2 w = *reinterpret_cast<const uint2*>(cw + p * 256);
+            const uint32_t sc = *reinterpret_cast<const uint32_t*>(sw + p * 32);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const uint32_t s2 = e4m3x2_to_f16x2(mt ? sc >> 16 : sc);  // rows g (low), g + 8
+                const uint32_t sa = bcast_lo(s2), sb = bcast_hi(s2);
+                uint32_t f[4];
+                e2m1x8_to_f16x8(mt ? w.y : w.x, f);
+                mma_16816(acc[p][mt], hmul2(f[0], sa), hmul2(f[2], sb), hmul2(f[1], sa), hmul2(f[3], sb), bv.x,
+                          bv.y);
+            }
+        }
+    };
+    auto b_of = [&](int j) {
+        return g < T ? *reinterpret_cast<const uint2*>(c.ubq + ((size_t)j * T + g) * kUnitRows + 4 * q)
+                     : make_uint2(0u, 0u);
+    };
+    // two units per round: their waits, loads and MMAs overlap
     bool ok = true;
 #pragma unroll 1
-    for (int j = 0; j < nu; ++j) {
-        const int li = base + j, s = li % kSlots;
-        const bool waited = mbar_wait_bounded(&r.full[s], static_cast<uint32_t>((li / kSlots) & 1));
+    for (int j = 0; j < nu; j += 2) {
+        const bool two = j + 1 < nu;
+        const int li0 = base + j, s0 = li0 % kSlots, s1 = (li0 + 1) % kSlots;
+        bool waited = mbar_wait_bounded(&r.full[s0], static_cast<uint32_t>((li0 / kSlots) & 1));
+        if (two && waited) waited = mbar_wait_bounded(&r.full[s1], static_cast<uint32_t>(((li0 + 1) / kSlots) & 1));
         const bool got = __all_sync(0xffffffffu, waited);
         if (got) {
-            // B: token g's block of unit j, elements 4q .. 4q + 3 (the MMA's
-            // k-slots 2q, 2q + 1, 2q + 8, 2q + 9, in the order the block's
-            // layout gives the weights)
-            uint2 bv = make_uint2(0u, 0u);
-            if (g < T) bv = *reinterpret_cast<const uint2*>(c.ubq + ((size_t)j * T + g) * kUnitRows + 4 * q);
-            const uint8_t* blk = c.ring_base + r.off[s];
-            const uint8_t* cw = blk + (size_t)p0 * 256 + lane * 8;
-            const uint8_t* sw = blk + (size_t)8 * H + (size_t)p0 * 32 + g * 4;
-#pragma unroll
-            for (int p = 0; p < kDownMaxPairs; ++p) {
-                if (p >= np) break;
-                const uint2 w = *reinterpret_cast<const uint2*>(cw + p * 256);
-                const uint32_t sc = *reinterpret_cast<const uint32_t*>(sw + p * 32);
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    const uint32_t s2 = e4m3x2_to_f16x2(mt ? sc >> 16 : sc);  // rows g (low), g + 8
-                    const uint32_t sa = bcast_lo(s2), sb = bcast_hi(s2);
-                    uint32_t f[4];
-                    e2m1x8_to_f16x8(mt ? w.y : w.x, f);
-                    mma_16816(acc[p][mt], hmul2(f[0], sa), hmul2(f[2], sb), hmul2(f[1], sa), hmul2(f[3], sb), bv.x,
-                              bv.y);
-                }
-            }
+            const uint2 b0 = b_of(j);
+            unit_mma(c.ring_base + r.off[s0], b0);
+            if (two) unit_mma(c.ring_base + r.off[s1], b_of(j + 1));
         } else if (lane == 0) {
             set_dev_error(kErrWaitFull);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&r.empty[s]);
+        if (lane == 0) {
+            mbar_arrive(&r.empty[s0]);
+            if (two) mbar_arrive(&r.empty[s1]);
+        }
         if (!got) {
             ok = false;
             break;
@@ -1036,6 +1050,15 @@ constexpr int kPartChunk = 8;
 __device__ __noinline__ bool st_reduce(const StackArgs& a, StackCta& c, int l) {
     const int ctid = threadIdx.x;
     const int T = a.T, H = a.H, G = c.G;
+    const uint16_t* res = l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H;
+    uint16_t* out = a.hidden_out + (size_t)l * T * H;
+    const int h0 = share_begin32(H, c.b, G), nr = share_begin32(H, c.b + 1, G) - h0;
+    const int items = T * nr, nch = (G + kPartChunk - 1) / kPartChunk;
+    float resv = 0.0f;  // the residual of item ctid (final since the layer began), loaded early
+    if (ctid < items) {
+        const int t = ctid / nr, row = h0 + ctid - t * nr;
+        resv = bf16_bits_to_float(__ldcg(res + (size_t)t * H + row));
+    }
     bool ok = true;
     if (ctid == 0) ok = wait_geq(layer_cnt(a, l) + kCntPart, G, abort_flag(a));
     if (consumer_bar_or(!ok || cta_abort(c))) return false;
@@ -1044,10 +1067,6 @@ __device__ __noinline__ bool st_reduce(const StackArgs& a, StackCta& c, int l) {
 #pragma unroll 1
         for (int i = ctid; i < c.amax_stride; i += kConsumerThreads) am[i] = 0u;
     }
-    const uint16_t* res = l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H;
-    uint16_t* out = a.hidden_out + (size_t)l * T * H;
-    const int h0 = share_begin32(H, c.b, G), nr = share_begin32(H, c.b + 1, G) - h0;
-    const int items = T * nr, nch = (G + kPartChunk - 1) / kPartChunk;
     // the chunk sums, [chunk][item], over the (dead) layer input and up B
     // operand: T nr nch <= T (H/G + 1)(G/8 + 1) floats, within their T H
     float* const csum = reinterpret_cast<float*>(c.X);
@@ -1073,7 +1092,7 @@ __device__ __noinline__ bool st_reduce(const StackArgs& a, StackCta& c, int l) {
         float s = csum[ctid];
 #pragma unroll 1
         for (int ch = 1; ch < nch; ++ch) s = __fadd_rn(s, csum[ch * items + ctid]);
-        const float h = __fadd_rn(s, bf16_bits_to_float(__ldcg(res + (size_t)t * H + row)));
+        const float h = __fadd_rn(s, resv);
         const __nv_bfloat16 ob = __float2bfloat16_rn(h);
         out[(size_t)t * H + row] = *reinterpret_cast<const uint16_t*>(&ob);
     }
