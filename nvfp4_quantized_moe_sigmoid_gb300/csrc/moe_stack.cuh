@@ -778,19 +778,25 @@ __device__ __noinline__ void st_layer_globals(StackCta& c) {
 
 // ---------------------------------------------------------------- units
 // Every CTA works on units of one expert per layer: the shared expert's RS
-// units go evenly to CTAs [0, cs), cs = G RS / (RS + Umax RI) (at least 1, at
-// most G - Umax, Umax = min(T k, E)); the U routed experts' RI units each to
-// the other Gr = G - cs CTAs, expert slot u to CTAs [cs + Gr u / U,
+// units go evenly to CTAs [0, cs), the U routed experts' RI units each to the
+// other Gr = G - cs CTAs, expert slot u to CTAs [cs + Gr u / U,
 // cs + Gr (u + 1) / U), evenly. The shared CTAs' share does not depend on the
-// routing, so their weights stream before the plan exists. Every CTA and its
-// producer compute the same ranges.
+// routing, so their weights stream before the plan exists: cs is the fewest
+// CTAs (from the even split G RS / (RS + Umax RI) down, Umax = min(T k, E))
+// with which a shared CTA holds at most 1.5 units more than a routed CTA,
+// RS / cs <= Umax RI / (G - cs) + 1.5 (at one token 32 of 152 CTAs, measured
+// better than the even 38 and than 28; at four tokens the even 11). Every
+// CTA and its producer compute the same ranges.
 struct UnitRange {
     int ex, ub, ue;  // expert (-1 shared, else routed slot), units [ub, ue) of it
 };
 
 __host__ __device__ inline int stack_shared_ctas(int G, int RS, int RI, int Umax) {
-    const int cs = static_cast<int>((long long)G * RS / (RS + (long long)Umax * RI));
-    return cs < 1 ? 1 : (cs > G - Umax ? G - Umax : cs);
+    int cs = static_cast<int>((long long)G * RS / (RS + (long long)Umax * RI));
+    cs = cs < 1 ? 1 : (cs > G - Umax ? G - Umax : cs);
+    // 2 RS (G - c) <= c (2 Umax RI + 3 (G - c)): RS / c <= Umax RI / (G - c) + 1.5
+    while (cs > 1 && 2LL * RS * (G - cs + 1) <= (long long)(cs - 1) * (2LL * Umax * RI + 3LL * (G - cs + 1))) --cs;
+    return cs;
 }
 
 __device__ __forceinline__ UnitRange stack_units(int b, int G, int cs, int RS, int RI, int U) {
