@@ -759,7 +759,11 @@ __device__ __noinline__ void st_topk_plan_t1(const StackArgs& a, StackCta& c, in
             c.up_g[slot] = c.upg_s[my_e];
             c.down_g[slot] = c.dng_s[my_e];
         }
-        if (lane == 0) c.plan.U = k;
+        __syncwarp();
+        if (lane == 0) {
+            c.plan.U = k;
+            mbar_arrive(&c.pbar);  // the producer may stream the routed weights now (release: the plan is visible)
+        }
     }
     consumer_bar();
 }
@@ -1144,13 +1148,10 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
         const StackLayer& P = a.layer[l];
 #pragma unroll 1
         for (int ph = 0; ph < 2 && alive; ++ph) {
-            if (ph == 1) {  // the plan of layer l
-                if (!mbar_wait_abortable(&c.pbar, l & 1, &c.abort_s)) {
-                    set_cta_abort(c);
-                    alive = false;
-                    break;
-                }
-                if (l + 1 < a.L) issue_gate(l + 1);
+            if (ph == 1 && !mbar_wait_abortable(&c.pbar, l & 1, &c.abort_s)) {  // the plan of layer l
+                set_cta_abort(c);
+                alive = false;
+                break;
             }
             if ((ph == 0) != sh) continue;
             // the units' up tiles (16 rows of W_up: codes, then scales, from
@@ -1209,6 +1210,9 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
                 ++pli;
             }
         }
+        // the next layer's router rows, once this layer's weights are on their
+        // way (they are needed a layer later)
+        if (alive && l + 1 < a.L) issue_gate(l + 1);
         if (alive) mbar_arrive(&c.qbar);  // the plan of layer l is no longer read here
     }
     if (!alive) atomicExch(abort_flag(a), 1);
@@ -1267,7 +1271,7 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
             st_topk_plan(a, c, l);
             st_layer_globals(c);
         }
-        if (ctid == 0) mbar_arrive(&c.pbar);  // the producer may stream the routed weights now
+        if (ctid == 0 && !one_token) mbar_arrive(&c.pbar);  // the producer may stream the routed weights now
         // 5. up tiles of this CTA's units (one expert)
         const UnitRange ur = stack_units(b, G, c.cs, a.S >> 4, RI, c.plan.U);
         const int nu = ur.ue - ur.ub;
