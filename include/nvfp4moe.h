@@ -262,8 +262,9 @@ nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w
  * runs as one persistent cooperative kernel with one CTA per SM: the layers'
  * steps meet through counters in the workspace instead of kernel boundaries,
  * and the next layer's router rows and shared-expert tiles are staged while
- * the current layer still waits on its routing. Each CTA takes an even share
- * of the layer's 16-row units of the experts' intermediate dimension and
+ * the current layer still waits on its routing. Each CTA takes 16-row units
+ * of one expert's intermediate dimension (the shared expert's units go to a
+ * fixed set of CTAs, each routed expert's to its share of the others) and
  * computes, per unit, 16 rows of W_up and then the matching 16 columns of
  * W_down (a split-K partial of the expert's output); so the down weights are
  * read from a column-block copy (nvfp4_colblock_layout), and the per-CTA
@@ -291,8 +292,9 @@ nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w
  * split of tile reductions, the down projection split over 16-column blocks),
  * so results agree with it to FP32 rounding, not bit for bit; repeated calls
  * give identical bits. Returns NVFP4_ERR_UNSUPPORTED_SHAPE for shapes outside
- * the limits above, when one CTA per SM does not fit or when a CTA's share of
- * a layer exceeds 32 units, NVFP4_ERR_CUDA if the
+ * the limits above, when one CTA per SM does not fit, when the GPU has fewer
+ * SMs than min(T k, E) + 1 or when a CTA's share of a layer exceeds 32 units,
+ * NVFP4_ERR_CUDA if the
  * cooperative launch fails; a device wait that expires ends every CTA of the
  * call early and is reported by nvfp4_last_device_error (NVFP4_ERR_TIMEOUT).
  */
