@@ -490,10 +490,15 @@ __device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c,
         for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
         if (lane == 0) c.norm_part[0][warp] = ss;
         consumer_bar();
+        // chunk sums in chunk order (all loaded first: nch <= 12 here)
         const int nch = (H + 255) >> 8;
+        float part[kConsumerWarps];
+#pragma unroll
+        for (int ch = 0; ch < kConsumerWarps; ++ch) part[ch] = ch < nch ? c.norm_part[0][ch] : 0.0f;
         float sum = 0.0f;
-#pragma unroll 1
-        for (int ch = 0; ch < nch; ++ch) sum = __fadd_rn(sum, c.norm_part[0][ch]);
+#pragma unroll
+        for (int ch = 0; ch < kConsumerWarps; ++ch)
+            if (ch < nch) sum = __fadd_rn(sum, part[ch]);
         const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, static_cast<float>(H)), a.rms_eps)));
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -546,9 +551,12 @@ __device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c,
         float* z = a.ws.z + (size_t)l * E;
 #pragma unroll 1
         for (int r = 0; r < c.ng; ++r) {
+            float zw[kConsumerWarps];  // all loaded first, then added in warp order
+#pragma unroll
+            for (int ww = 0; ww < kConsumerWarps; ++ww) zw[ww] = c.zred[ww][r];
             float s = 0.0f;
 #pragma unroll
-            for (int ww = 0; ww < kConsumerWarps; ++ww) s = __fadd_rn(s, c.zred[ww][r]);
+            for (int ww = 0; ww < kConsumerWarps; ++ww) s = __fadd_rn(s, zw[ww]);
             z[c.b + r * c.G] = s;
         }
         red_release_add(layer_cnt(a, l) + kCntLogits, c.ng);
