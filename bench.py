@@ -241,10 +241,10 @@ def launches_per_step(st, T, L, lm_head):
 
 # DRAM bytes (read + write) per W4A4 layer of k_moe_stack at one token, from
 # one ncu capture of the current kernel (profiles/k_moe_stack_w4a4_t1_2layer_
-# ncu_full.md: 92.68 MB read + 2.68 MB written over two layers; traffic grows
+# ncu_full.md: 92.70 MB read + 2.70 MB written over two layers; traffic grows
 # with the layers, one weight stream each). Reset to None when the kernel
 # changes and re-measure.
-STACK_T1_W4A4_DRAM_BYTES_PER_LAYER = (92684544 + 2684160) / 2
+STACK_T1_W4A4_DRAM_BYTES_PER_LAYER = (92697344 + 2700800) / 2
 
 
 # ------------------------------------------------------------------ GPU arm
