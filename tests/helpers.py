@@ -80,3 +80,43 @@ def check_routing(gpu_idx, gpu_w, orc, k):
             assert c[a] + tau[a] >= c[b] - tau[b], f"token {t}: order {gi}"
         exempt += 1
     return exempt
+
+
+def colblock_loops(codes, scales):
+    """The column-block order of nvfp4_colblock_layout as include/nvfp4moe.h
+    states it, byte by byte."""
+    B, R, C2 = codes.shape
+    out = np.zeros((B, 2 * C2 // 16, 9 * R), np.uint8)
+    for b in range(B):
+        for c in range(2 * C2 // 16):
+            for p in range(R // 32):
+                for L in range(32):
+                    g, q = L // 4, L % 4
+                    for mt in range(2):
+                        for i in range(4):
+                            row = 32 * p + 16 * mt + g + 8 * (i >> 1)
+                            col = 16 * c + 4 * q + 2 * (i & 1)
+                            out[b, c, 256 * p + 8 * L + 4 * mt + i] = codes[b, row, col // 2]
+                for g in range(8):
+                    for mt in range(2):
+                        for j in range(2):
+                            out[b, c, 8 * R + 32 * p + 4 * g + 2 * mt + j] = scales[b, 32 * p + 16 * mt + g + 8 * j, c]
+    return out
+
+
+def colblock_vectorised(codes, scales):
+    """colblock_loops with numpy indexing, for the large cases."""
+    B, R, C2 = codes.shape
+    P, NB = R // 32, 2 * C2 // 16
+    L = np.arange(32)
+    g, q = L // 4, L % 4
+    mt, i = np.arange(2), np.arange(4)
+    rows = (32 * np.arange(P)[:, None, None, None] + 16 * mt[None, None, :, None] + g[None, :, None, None]
+            + 8 * (i[None, None, None, :] >> 1))                                       # [P, 32, 2, 4]
+    cbyte = 8 * np.arange(NB)[:, None, None] + 2 * q[None, :, None] + (i[None, None, :] & 1)  # [NB, 32, 4]
+    cod = codes[:, rows[None], cbyte[:, None, :, None, :]].reshape(B, NB, 256 * P)
+    gg = np.arange(8)
+    srow = (32 * np.arange(P)[:, None, None, None] + 16 * mt[None, None, :, None] + gg[None, :, None, None]
+            + 8 * np.arange(2)[None, None, None, :])                                     # [P, 8, 2, 2]
+    sc = scales[:, srow[None], np.arange(NB)[:, None, None, None, None]].reshape(B, NB, 32 * P)
+    return np.concatenate([cod, sc], axis=2)

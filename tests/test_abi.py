@@ -110,3 +110,20 @@ def test_package_fails_loudly_without_library(abi, tmp_path):
             a2.load(str(tmp_path / "missing.so"))
         finally:
             a2._lib = saved
+
+
+def test_colblock_references_agree():
+    """The vectorised column-block reference equals the byte-by-byte statement
+    of the layout in include/nvfp4moe.h (the GPU test compares the kernel with
+    the vectorised one at the full shapes)."""
+    import numpy as np
+    from tests.helpers import colblock_loops, colblock_vectorised
+    rng = np.random.default_rng(7)
+    for B, R, C in [(2, 64, 64), (1, 96, 48), (3, 32, 16)]:
+        codes = rng.integers(0, 256, (B, R, C // 2), dtype=np.uint8)
+        scales = rng.integers(0, 256, (B, R, C // 16), dtype=np.uint8)
+        a = colblock_loops(codes, scales)
+        assert a.shape == (B, C // 16, 9 * R)
+        np.testing.assert_array_equal(a, colblock_vectorised(codes, scales))
+        # every input byte lands exactly once
+        assert sorted(a.reshape(-1).tolist()) == sorted(codes.reshape(-1).tolist() + scales.reshape(-1).tolist())
