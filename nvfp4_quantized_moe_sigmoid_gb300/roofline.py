@@ -57,3 +57,31 @@ def step_flops(T, L, E, H, I, S, k, V=None):
     if V:
         f += 2 * T * V * H
     return f
+
+
+# ---- the pages' own byte arithmetic ("Let's optimize Nemotron 3.5 Lightning -
+# a worklog", Step 4; the W4A4 card's precision table), which the model above
+# refines (it also counts the block scales and globals)
+def bf16_weight_bytes(n, k):
+    """Dense bf16 matrix [n][k]."""
+    return n * k * 2
+
+
+def fp4_code_bytes(n, k):
+    """E2M1 codes of an [n][k] NVFP4 matrix alone (the pages' "176 MB")."""
+    return n * k // 2
+
+
+def lm_head_quant_saving(V, H, bw_bytes_per_s):
+    """Reads saved per decode step by storing the lm_head [V][H] as NVFP4
+    codes instead of bf16, and the time they take at bw_bytes_per_s:
+    (bf16 bytes, NVFP4 code bytes, saved bytes, saved seconds)."""
+    b16, b4 = bf16_weight_bytes(V, H), fp4_code_bytes(V, H)
+    return b16, b4, b16 - b4, (b16 - b4) / bw_bytes_per_s
+
+
+def routed_expert_tensors(L, E):
+    """NVFP4 routed-expert weight tensors of L MoE layers: up_proj and
+    down_proj of each of the E experts (no gate_proj)."""
+    return L * E * 2
+

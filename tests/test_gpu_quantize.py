@@ -113,3 +113,24 @@ def test_full_size_lm_head_matrix(nm):
     c0, s0, _ = orc.quantize(host[rows], orc.GIVEN, g=float(g0))
     assert np.array_equal(m.codes[torch.from_numpy(rows).cuda()].cpu().numpy(), c0)
     assert np.array_equal(m.scales[torch.from_numpy(rows).cuda()].cpu().numpy(), s0)
+
+
+def test_offgrid_boundary_cases_exact(nm):
+    """The quantiser cases next to rounding boundaries (tests/golden/nvfp4_offgrid.txt,
+    expected values from exact arithmetic): the kernels' corrected-reciprocal
+    division and scale arithmetic must give the reading's codes bit for bit."""
+    from fractions import Fraction
+    from tests.test_oracle_quant_exact import _cases
+    for c in _cases():
+        if c[0] == "global":
+            _, _, amax, g = c
+            row = np.zeros((1, 16), np.float32)
+            row[0, 5] = np.float32(float(amax))
+            _, _, gq = gpu_quant(nm, row, orc.PER_TENSOR)
+            assert Fraction(float(gq[0])) == g
+        else:
+            _, _, g, x, s, codes = c
+            xa = np.array([[float(v) for v in x]], np.float32)
+            cq, sq, _ = gpu_quant(nm, xa, orc.GIVEN, float(g))
+            assert int(sq[0, 0]) == s
+            assert bytes(cq[0]) == codes
