@@ -53,6 +53,11 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="time only the chosen config (by default the headline run also times configs 0, 2, 3, 4)")
+    ap.add_argument("--trace", action="store_true",
+                    help="per-phase timeline of the stack kernel (1-4 token configs) from the phase-trace build "
+                         "of the library; prints a table instead of the JSON line")
     return ap.parse_args()
 
 
@@ -149,21 +154,21 @@ def physical_gpu_index(local_rank):
 
 
 # ------------------------------------------------------------------ oracle timing
-class OracleSample:
-    """The CPU oracle on a bounded sample of the workload: the first n_layers
-    MoE layers of the chain (route + experts + shared + combine) and
-    1/lm_den of the lm_head rows. Weights are generated and quantised once,
-    outside the timed part; run() returns the time scaled to a full step, in
-    microseconds per token."""
+class OracleRun:
+    """The CPU oracle on the same workload: the first n_layers MoE layers of
+    the chain (route + experts + shared + combine) and 1/lm_den of the
+    lm_head rows. Weights are generated and quantised once, outside the
+    timed part; run() returns the time scaled to a full step (exactly the
+    step when n_layers is all of them and lm_den is 1), in microseconds per
+    token, and the seconds it took."""
 
-    def __init__(self, cfg_id, n_layers, lm_den, threads):
+    def __init__(self, cfg_id, n_layers, lm_den):
         from gen import configs, gen
         from oracle import oracle as orc
         from oracle.workload import OracleLayer
 
         self.orc = orc
         self.c = c = configs.shape(cfg_id)
-        orc.set_threads(threads)
         self.h0 = gen.hidden_bf16(c["T"], c["H"], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
         self.nl = min(n_layers, c["layers"])
         self.layers = []
@@ -178,11 +183,18 @@ class OracleSample:
             master = gen.lm_head_master(c["seed"], c["V"], c["H"], 0, self.rows)
             cc, ss, gg = orc.quantize(master, orc.PER_TENSOR)
             self.W = orc.Mat(cc, ss, gg[0])
-        self.desc = (f"{self.nl} of {c['layers']} MoE layers (route+experts+shared+combine) and "
-                     f"{self.rows} of {c['V']} lm_head rows at T={c['T']}, scaled to a full step")
+        self.full = self.nl == c["layers"] and (not c["lm_head"] or self.rows == c["V"])
+        if self.full:
+            self.desc = (f"the full step: {c['layers']} MoE layers (route+experts+shared+combine)"
+                         + (f" and all {c['V']} lm_head rows" if c["lm_head"] else "") + f" at T={c['T']}")
+        else:
+            self.desc = (f"{self.nl} of {c['layers']} MoE layers (route+experts+shared+combine)"
+                         + (f" and {self.rows} of {c['V']} lm_head rows" if c["lm_head"] else "")
+                         + f" at T={c['T']}, scaled to a full step")
 
-    def run(self):
+    def run(self, threads):
         c, orc = self.c, self.orc
+        orc.set_threads(threads)
         h = self.h0
         t0 = time.perf_counter()
         eps = c["rms_eps"]
@@ -201,27 +213,37 @@ class OracleSample:
         return per_step / c["T"] * 1e6, t_layers + t_lm
 
 
+def config_dict(c, ws):
+    """The workload as both arms name it."""
+    return {"workload": c["name"], "T": c["T"], "layers": c["layers"], "hidden": c["H"], "experts": c["E"],
+            "top_k": c["K"], "inter": c["I"], "shared_inter": c["S"],
+            "vocab": c["V"] if c["lm_head"] else None, "mode": "W4A4" if c["w4a4"] else "W4A16",
+            "parallelism": "replicas" if ws > 1 else "single",
+            "l2": "inputs larger than L2: each step streams the step's weights (>= 46 MB per layer) once; "
+                  "the decode step streams 1.26 GB vs 129 MB of L2"}
+
+
 def run_reference(args, ws, rank):
+    """The reference arm: the CPU oracle (the plain, slow reference of the same
+    computation) on the full workload of the config, on the host cores."""
     if rank != 0:
         return
     threads = len(os.sched_getaffinity(0))
-    sample = OracleSample(args.config, 1, 32, threads)
-    vals = []
+    run = OracleRun(args.config, 10 ** 6, 1)
+    vals, secs = [], []
     for i in range(args.warmup + args.steps):
-        v, _ = sample.run()
+        v, t = run.run(threads)
         if i >= args.warmup:
             vals.append(v)
+            secs.append(t)
     value = statistics.median(vals)
-    c = sample.c
+    c = run.c
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": value * c["T"] / 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(secs) * 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": c["name"], "T": c["T"], "layers": c["layers"], "hidden": c["H"],
-                       "experts": c["E"], "top_k": c["K"], "inter": c["I"], "shared_inter": c["S"],
-                       "vocab": c["V"] if c["lm_head"] else None, "parallelism": "replicas"},
+            "data": "synthetic", "config": config_dict(c, ws),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": sample.desc},
+                             "sample": run.desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -240,11 +262,82 @@ def launches_per_step(st, T, L, lm_head):
 
 
 # DRAM bytes (read + write) per W4A4 layer of k_moe_stack at one token, from
-# one ncu capture of the current kernel (profiles/k_moe_stack_w4a4_t1_2layer_
-# ncu_full.md: 92.70 MB read + 2.70 MB written over two layers; traffic grows
-# with the layers, one weight stream each). Reset to None when the kernel
-# changes and re-measure.
-STACK_T1_W4A4_DRAM_BYTES_PER_LAYER = (92697344 + 2700800) / 2
+# one ncu capture of the current kernel. None until the current kernel has
+# been captured (traffic is then reported as null).
+STACK_T1_W4A4_DRAM_BYTES_PER_LAYER = None
+
+
+def graph_of(fn, reps):
+    """A CUDA graph of `reps` back-to-back calls of fn (captured after one
+    eager call): replaying it times the calls' kernels without launch gaps."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, iters, warm=2):
+    import torch
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(iters):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def measure_other_config(cfg_id, base, nm, rf, peak, iters=10):
+    """One more configuration on the weights already registered for the
+    headline (the configs share seed-0 weights; the prefill config has its
+    own router bias): µs/token, algorithmic GB/s and their fraction of the
+    measured HBM copy peak, from a graph of one step replayed `iters` times."""
+    import copy
+    import torch
+    from gen import configs, fill
+    from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
+
+    c = dict(configs.shape(cfg_id))
+    T, L, E, H, I, S, K, V = c["T"], c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], c["V"]
+    st = MoEDecodeStack(L, E, H, I, S, K, T, w4a4=c["w4a4"], V=V if c["lm_head"] else None,
+                        rms_eps=c["rms_eps"], weights_from=base)
+    st.layers = base.layers[:L]
+    st.lm = base.lm if c["lm_head"] else None
+    if tuple(c["bias"]) != tuple(configs.shape(1)["bias"]):
+        st.layers = [copy.copy(Lw) for Lw in st.layers]
+        _, _, fbias = fill.fillers(c["seed"], c["bias"])
+        for l, Lw in enumerate(st.layers):
+            Lw.router_b = torch.empty_like(Lw.router_b)
+            Lw._c = None
+            fbias(l, Lw.router_b)
+    st.make_workspace()
+    fill.hidden(st.h[0], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+    torch.cuda.synchronize()
+    g = st.capture()
+    ms = time_graph(g, iters, warm=3)
+    uniques = st.unique_experts()
+    assert nm.nvfp4_last_device_error() == 0
+    b = rf.step_bytes(T, uniques, E, H, I, S, K, V if c["lm_head"] else None)
+    gbs = b / (ms * 1e-3) / 1e9
+    out = {"workload": c["name"], "path": st.path, "T": T, "layers": L, "mode": "W4A4" if c["w4a4"] else "W4A16",
+           "ms_per_step": ms, "us_per_token": ms * 1e3 / T, "step_bytes": b, "gbs": gbs, "frac_of_measured_hbm": gbs / peak,
+           "unique_experts_mean": sum(uniques) / len(uniques)}
+    del st, g
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -298,56 +391,45 @@ def run_ours(args, ws, rank, local):
     peak, peak_kind = measured_peaks()
     gbs_step = step_b / (ms_step * 1e-3) / 1e9
 
-    # per-call timing of the dominant call (eager, same stream, same kernels)
-    call_ms, lm_ms = [], []
-    for rep in range(4):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * L + 2)]
-        if st.path == "stack":
-            evs[0].record(stream)
-            nm.moe_stack_forward(st.layers, st.h[0], K, st.mode, hidden_out=st.h[1:], topk_idx=st.topk_idx,
-                                 topk_w=st.topk_w, workspace=st.stack_ws, rms_eps=st.rms_eps,
-                                 c_layers=st.c_layers)
-            evs[1].record(stream)
-        else:
-            for l, Lw in enumerate(st.layers):
-                nm.moe_route_topk(st.h[l], Lw.router_w, Lw.router_b, K, st.topk_idx[l], st.topk_w[l],
-                                  rms_eps=st.rms_eps)
-                evs[2 * l].record(stream)
-                nm.moe_expert_forward(Lw, st.h[l], st.topk_idx[l], st.topk_w[l], st.mode,
-                                      residual=st.h[l], out=st.h[l + 1], workspace=st.ws,
-                                      rms_eps=st.rms_eps)
-                evs[2 * l + 1].record(stream)
-        if c["lm_head"]:
-            evs[2 * L].record(stream)
-            nm.lm_head_forward(st.lm, st.h[L], st.logits, workspace=st.lm_ws, rms_eps=st.rms_eps)
-            evs[2 * L + 1].record(stream)
-        torch.cuda.synchronize()
-        if rep > 0:
-            if st.path == "stack":
-                call_ms.append(evs[0].elapsed_time(evs[1]))
-            else:
-                call_ms += [evs[2 * l].elapsed_time(evs[2 * l + 1]) for l in range(L)]
-            if c["lm_head"]:
-                lm_ms.append(evs[2 * L].elapsed_time(evs[2 * L + 1]))
-    call_avg_ms = statistics.mean(call_ms)
+    # the dominant call timed inside a graph: REPS back-to-back calls on the
+    # launching stream, replayed; its average is the kernel's time per launch
+    # without launch gaps (each call streams its weights from HBM again)
+    REPS = 5
     if st.path == "stack":
+        dom = graph_of(lambda: nm.moe_stack_forward(st.layers, st.h[0], K, st.mode, hidden_out=st.h[1:],
+                                                    topk_idx=st.topk_idx, topk_w=st.topk_w,
+                                                    workspace=st.stack_ws, rms_eps=st.rms_eps,
+                                                    c_layers=st.c_layers), REPS)
         call_b = sum(rf.layer_bytes(T, u, E, H, I, S, K) for u in uniques)
         kname = "k_moe_stack (moe_stack_forward: all %d MoE layers in one launch)" % L
     else:
-        call_b = statistics.mean(rf.expert_call_bytes(T, u, H, I, S, K) for u in uniques)
-        kname = "moe_expert_forward (up + down kernels, per layer)"
+        def split_layers():
+            for l, Lw in enumerate(st.layers):
+                nm.moe_route_topk(st.h[l], Lw.router_w, Lw.router_b, K, st.topk_idx[l], st.topk_w[l],
+                                  rms_eps=st.rms_eps)
+                nm.moe_expert_forward(Lw, st.h[l], st.topk_idx[l], st.topk_w[l], st.mode, residual=st.h[l],
+                                      out=st.h[l + 1], workspace=st.ws, rms_eps=st.rms_eps)
+        dom = graph_of(split_layers, 1)
+        call_b = sum(rf.layer_bytes(T, u, E, H, I, S, K) for u in uniques)
+        kname = "the MoE layers (router + grouped expert kernels, %d layers)" % L
+    dom_ms = time_graph(dom, 6) / (REPS if st.path == "stack" else 1)
+    del dom
     traffic = None
     if st.path == "stack" and T == 1 and c["w4a4"] and STACK_T1_W4A4_DRAM_BYTES_PER_LAYER is not None:
         traffic = STACK_T1_W4A4_DRAM_BYTES_PER_LAYER * L
     roof = {"bound": "hbm", "kernel": kname,
-            "achieved": call_b / (call_avg_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+            "achieved": call_b / (dom_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
             "frac": None, "traffic": traffic, "algorithmic_bytes": call_b,
-            "avg_launch_us": call_avg_ms * 1e3, "peak_kind": peak_kind}
+            "avg_launch_us": dom_ms * 1e3, "peak_kind": peak_kind,
+            "timing": "CUDA events around graph replays of %d back-to-back launches" % REPS}
     roof["frac"] = roof["achieved"] / peak
     extra = {}
-    if lm_ms:
+    if c["lm_head"]:
+        lmg = graph_of(lambda: nm.lm_head_forward(st.lm, st.h[L], st.logits, workspace=st.lm_ws,
+                                                  rms_eps=st.rms_eps), REPS)
+        lmm = time_graph(lmg, 6) / REPS
+        del lmg
         lb = rf.lm_head_bytes(T, V, H)
-        lmm = statistics.mean(lm_ms)
         extra["lm_head"] = {"avg_us": lmm * 1e3, "achieved_gbs": lb / (lmm * 1e-3) / 1e9,
                             "frac": lb / (lmm * 1e-3) / 1e9 / peak}
 
@@ -380,37 +462,127 @@ def run_ours(args, ws, rank, local):
                "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
                "wall_us_per_step": wall / args.steps * 1e6}
 
+    # the other configurations, on the same weights (parity cases elsewhere;
+    # reported here so that every number comes from this run)
+    others = None
+    if rank == 0 and not args.no_other_configs and args.layers == 0 and args.config == 1:
+        others = {}
+        st.graph = None
+        for oc in (0, 2, 3, 4):
+            others[configs.shape(oc)["name"]] = measure_other_config(oc, st, nm, rf, peak)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         threads = len(os.sched_getaffinity(0))
-        sample = OracleSample(args.config, 3, 8, threads)
-        v, secs = sample.run()
-        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample.desc,
-               "seconds": secs}
+        full = OracleRun(args.config, 10 ** 6, 1)
+        v_all, secs_all = full.run(threads)
+        sample = OracleRun(args.config, 2, 16)
+        v_one, secs_one = sample.run(1)
+        cpu = {"value": v_all, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": full.desc,
+               "seconds": secs_all,
+               "single_thread": {"value": v_one, "unit": UNIT, "cores": 1, "sample": sample.desc,
+                                 "seconds": secs_one}}
 
     if rank == 0:
         line = {"metric": METRIC, "value": us_token, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
                 "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4(e2m1,e4m3)->f16 mma, f32 acc",
                 "data": "synthetic",
-                "config": {"workload": c["name"], "T": T, "layers": L, "hidden": H, "experts": E,
-                           "top_k": K, "inter": I, "shared_inter": S,
-                           "vocab": V if c["lm_head"] else None, "mode": "W4A4" if c["w4a4"] else "W4A16",
-                           "parallelism": "replicas" if ws > 1 else "single",
-                           "l2": "inputs larger than L2: each step streams %.2f GB vs 129 MB L2" % (step_b / 1e9),
-                           "graph": "one CUDA graph per step", "path": st.path},
+                "config": dict(config_dict(c, ws), graph="one CUDA graph per step", path=st.path),
                 "step_gbs": gbs_step, "step_frac_of_measured_hbm": gbs_step / peak,
                 "step_frac_of_8tbs": gbs_step / NOMINAL_HBM_GBS, "step_bytes": step_b,
                 "unique_experts_per_layer": uniques,
                 "roofline": roof, "cpu_baseline": cpu, "clocks": clk.summary(), "e2e": e2e,
                 "gpu_launches": args.steps * launches_per_step(st, T, L, c["lm_head"]),
-                **extra}
+                "other_configs": others, **extra}
         print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ phase trace
+TRACE_EVENTS = ["layer start", "h_l final (all CTAs)", "router logits posted", "all logits posted",
+                "plan written", "up tiles done", "row amax final", "down units done", "all partials posted",
+                "rows of h_l+1 written", "producer: first item", "producer: last item"]
+
+
+def run_trace(args, local):
+    """Runs the config's decode step with the phase-trace build of the library
+    and prints, per phase boundary of the stack kernel, the median over layers
+    of the median and the maximum over CTAs of its time after the first CTA
+    saw h_l final, plus the layer period."""
+    import importlib.util
+    import numpy as np
+
+    spec = importlib.util.spec_from_file_location(
+        "_nvfp4moe_build", os.path.join(ROOT, "nvfp4_quantized_moe_sigmoid_gb300", "build.py"))
+    pb = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(pb)
+    os.environ["NVFP4MOE_LIB"] = pb.build_trace()
+    import torch
+
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import ctypes
+    import nvfp4_quantized_moe_sigmoid_gb300 as nm
+    from nvfp4_quantized_moe_sigmoid_gb300 import _abi
+    from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
+    from gen import configs, fill
+
+    assert _abi.LIB_PATH == pb.TRACE_LIB
+    c = dict(configs.shape(args.config))
+    if args.layers > 0:
+        c["layers"] = min(c["layers"], args.layers)
+    T, L = c["T"], c["layers"]
+    if T > 4:
+        raise SystemExit("--trace covers the stack kernel (1-4 tokens)")
+    st = MoEDecodeStack(L, c["E"], c["H"], c["I"], c["S"], c["K"], T, w4a4=c["w4a4"],
+                        V=c["V"] if c["lm_head"] else None, rms_eps=c["rms_eps"])
+    st.register(*fill.fillers(c["seed"], c["bias"]))
+    fill.hidden(st.h[0], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+    for _ in range(max(3, args.warmup)):
+        st.step()
+    torch.cuda.synchronize()
+    st.step()
+    n = 256 * 32 * 16
+    buf = np.zeros(n, dtype=np.uint64)
+    lib = nm._L
+    lib.nvfp4moe_stack_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    lib.nvfp4moe_stack_trace_read.restype = ctypes.c_int
+    assert lib.nvfp4moe_stack_trace_read(buf.ctypes.data, buf.nbytes) == 0
+    assert nm.nvfp4_last_device_error() == 0
+    G = torch.cuda.get_device_properties(local).multi_processor_count
+    tr = buf.reshape(256, 32, 16)[:G, :L, :].astype(np.float64)
+    ref = tr[:, :, 1].min(axis=0)  # first CTA to see h_l final, per layer
+    rows = []
+    first = 1 if L > 1 else 0
+    for ev, name in enumerate(TRACE_EVENTS):
+        med, mx = [], []
+        for l in range(first, L):
+            v = tr[:, l, ev]
+            v = v[v > 0]
+            if v.size == 0:
+                continue
+            d = (v - ref[l]) / 1e3
+            med.append(np.median(d))
+            mx.append(np.max(d))
+        if med:
+            rows.append((name, float(np.median(med)), float(np.median(mx))))
+    period = np.diff(ref) / 1e3
+    print(f"phase trace: {c['name']}, {L} layers, T={T}, {G} CTAs; times in us after the first CTA saw h_l final "
+          f"(median over layers {first}..{L - 1})")
+    print(f"{'event':34s} {'median CTA':>11s} {'last CTA':>10s}")
+    for name, a, b in rows:
+        print(f"{name:34s} {a:11.2f} {b:10.2f}")
+    if period.size:
+        print(f"layer period: median {np.median(period):.2f} us, min {period.min():.2f}, max {period.max():.2f}")
 
 
 def main():
     args = parse()
     ws, rank, local = dist_init()
+    if args.trace:
+        run_trace(args, local)
+        return
     if args.impl == "reference":
         run_reference(args, ws, rank)
     else:

@@ -260,8 +260,10 @@ nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w
  * blocks between them, and the bare chain overflows bf16 within a few
  * layers at the pages' shapes. It
  * runs as one persistent cooperative kernel with one CTA per SM: the layers'
- * steps meet through counters in the workspace instead of kernel boundaries,
- * and the next layer's router rows and shared-expert tiles are staged while
+ * steps meet in the workspace instead of at kernel boundaries (the router
+ * logits and each layer's output as words tagged with their layer, which a
+ * reader polls directly; counters for the rest), and the next layer's router
+ * rows and shared-expert tiles are staged while
  * the current layer still waits on its routing. Each CTA takes 16-row units
  * of one expert's intermediate dimension (the shared expert's units go to a
  * fixed set of CTAs, each routed expert's to its share of the others) and
@@ -285,9 +287,11 @@ nvfp4_status moe_layer_forward(const moe_layer_weights* w, const float* router_w
  *              overlap hidden_in
  *   topk_idx, topk_w: device out [L][T][k], each layer's routing
  *   workspace  device, >= moe_stack_forward_workspace_size() bytes, 256-byte
- *              aligned, zeroed once by moe_expert_forward_workspace_init and
- *              left zeroed by every completed call; calls that share it must
- *              not overlap.
+ *              aligned, zeroed once by moe_expert_forward_workspace_init;
+ *              every completed call leaves it ready for the next (counters
+ *              zeroed, a call count advanced so that no tagged word left by
+ *              one call matches the next); calls that share it must not
+ *              overlap.
  * Summation orders differ from moe_layer_forward's (router dot products, the
  * split of tile reductions, the down projection split over 16-column blocks),
  * so results agree with it to FP32 rounding, not bit for bit; repeated calls
@@ -354,9 +358,14 @@ nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t L, const v
  *     moe_expert_forward_workspace_size exceeds it is rejected with
  *     NVFP4_ERR_WORKSPACE before anything is launched (at the pages' layer
  *     shape this admits 1-4 tokens with top-6).
- *   - The first call on a device looks up the scratch array's device address
- *     (with that device current) and caches it; make that first call before
- *     any stream capture.
+ *   - The first call in each CUDA context (per device: the primary context,
+ *     or one made with cuCtxCreate or after cudaDeviceReset) looks up the
+ *     scratch array's device address in that context, with its device
+ *     current, and caches it under the context's id; make that first call
+ *     before any stream capture. A driver without context ids makes every
+ *     call look the address up again.
+ *   - The arguments are checked exactly as moe_expert_forward checks them,
+ *     before the scratch size is derived from them.
  *   - Each call clears the scratch region it uses on `stream` and leaves its
  *     contents behind; all calls on a device share the one array, so calls
  *     that overlap on the GPU (other streams, other threads) race. Order

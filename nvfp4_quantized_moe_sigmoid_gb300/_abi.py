@@ -4,7 +4,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libnvfp4moe.so")
+# NVFP4MOE_LIB may name another build of the same library (the phase-trace
+# variant, libnvfp4moe_trace.so); by default the in-tree libnvfp4moe.so.
+LIB_PATH = os.environ.get("NVFP4MOE_LIB") or os.path.join(HERE, "libnvfp4moe.so")
 
 P = ctypes.c_void_p
 I32, I64 = ctypes.c_int32, ctypes.c_int64

@@ -91,6 +91,32 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* b, uint32_t parity
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of a phase: never suspends the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until phase `parity` has completed by spinning on the non-blocking
+// test (a thread suspended in try_wait resumes some hundreds of nanoseconds
+// after the phase completes, which on a critical path costs more than the
+// issue slots of the spin); false after 1 s.
+__device__ __noinline__ bool mbar_wait_spin(uint64_t* b, uint32_t parity) {
+    if (mbar_test_wait(b, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (int it = 1;; ++it) {
+        if (mbar_test_wait(b, parity)) return true;
+        if ((it & 255) == 0 && globaltimer() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
 // Wait until phase `parity` of the barrier has completed; false after 1 s.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity) {
     if (mbar_try_wait(b, parity)) return true;
@@ -260,6 +286,24 @@ __device__ __forceinline__ void dequant_block16_f16(const QBlock& q, uint32_t (&
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// W4A16: a bf16 activation row (B operand) enters the f16 MMA as f16, whose
+// largest finite value is 65504. A row whose amax reaches 2^15 is therefore
+// scaled by 2^-e first, e = floor(log2 amax) - 14 (a power of two: exact down
+// to f16's subnormal range), and every GEMV result of the row by 2^e, so that
+// no element overflows; rows below 2^15 (every normalised row) keep e = 0 and
+// convert unscaled. w4a16_row_scale returns 2^e, w4a16_row_inv_scale 2^-e
+// (amax finite and >= 0).
+__device__ __forceinline__ int w4a16_row_exp(float amax) {
+    const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 14;
+    return e > 0 ? e : 0;
+}
+__device__ __forceinline__ float w4a16_row_scale(float amax) {
+    return __uint_as_float(static_cast<uint32_t>(127 + w4a16_row_exp(amax)) << 23);
+}
+__device__ __forceinline__ float w4a16_row_inv_scale(float amax) {
+    return __uint_as_float(static_cast<uint32_t>(127 - w4a16_row_exp(amax)) << 23);
+}
 
 // Unit-weight RMS norm of one bf16 row by one warp (the per-block input norm
 // of the pre-norm model the pages serve; its norms stay in bf16):

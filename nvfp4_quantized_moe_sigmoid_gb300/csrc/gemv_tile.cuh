@@ -301,6 +301,9 @@ __device__ __forceinline__ uint4 ld_row16(const uint16_t* p) {
 
 constexpr int kBRegBlocks = 4;
 
+// One 16-element block of a B row: W4A4 quantises it with the row global g
+// (then stores its exact f16 dequantisation without g); W4A16 stores
+// f16(x * g), g the row's power-of-two prescale 2^-e (w4a16_row_inv_scale).
 template <bool W4A4>
 __device__ __noinline__ void b_block_store(uint4 u0, uint4 u1, float g, uint4* d) {
     const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -316,7 +319,7 @@ __device__ __noinline__ void b_block_store(uint4 u0, uint4 u1, float g, uint4* d
     } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const __half2 h2 = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+            const __half2 h2 = __floats2half2_rn(__fmul_rn(v[2 * j], g), __fmul_rn(v[2 * j + 1], g));
             o[j] = *reinterpret_cast<const uint32_t*>(&h2);
         }
     }
@@ -324,16 +327,17 @@ __device__ __noinline__ void b_block_store(uint4 u0, uint4 u1, float g, uint4* d
     d[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// B rows for the GEMV engine: per row the amax (red[r], scratch), then the
+// row factor gout[r] the epilogue multiplies in: W4A4 the row global
+// amax / 2688, W4A16 the prescale 2^e (1 for rows below 2^15).
 template <bool W4A4, bool GSRC>
 __device__ __noinline__ void prepare_b_rows(const uint16_t* const* src, int nrows, int K,
                                                __half* dst, float* gout, unsigned int* red) {
     const int ctid = threadIdx.x;  // consumer thread index
     const int nb = K >> 4;
     const int total = nrows * nb;
-    if (W4A4) {
-        if (ctid < nrows) red[ctid] = 0u;
-        consumer_bar();
-    }
+    if (ctid < nrows) red[ctid] = 0u;
+    consumer_bar();
     uint4 u[kBRegBlocks][2];
 #pragma unroll
     for (int m = 0; m < kBRegBlocks; ++m) {
@@ -347,7 +351,7 @@ __device__ __noinline__ void prepare_b_rows(const uint16_t* const* src, int nrow
             }
         }
     }
-    if (W4A4) {
+    {
 #pragma unroll
         for (int m = 0; m < kBRegBlocks; ++m) {
             const int i = ctid + m * kConsumerThreads;
@@ -377,14 +381,17 @@ __device__ __noinline__ void prepare_b_rows(const uint16_t* const* src, int nrow
             atomicMax(&red[r], __float_as_uint(mx));
         }
         consumer_bar();
-        if (ctid < nrows) gout[ctid] = __fdiv_rn(__uint_as_float(red[ctid]), 2688.0f);
+        if (gout && ctid < nrows)
+            gout[ctid] = W4A4 ? __fdiv_rn(__uint_as_float(red[ctid]), 2688.0f)
+                              : w4a16_row_scale(__uint_as_float(red[ctid]));
     }
 #pragma unroll
     for (int m = 0; m < kBRegBlocks; ++m) {
         const int i = ctid + m * kConsumerThreads;
         if (i >= total) break;
         const int r = i / nb, b = i % nb;
-        const float g = W4A4 ? __fdiv_rn(__uint_as_float(red[r]), 2688.0f) : 0.0f;
+        const float g = W4A4 ? __fdiv_rn(__uint_as_float(red[r]), 2688.0f)
+                             : w4a16_row_inv_scale(__uint_as_float(red[r]));
         b_block_store<W4A4>(u[m][0], u[m][1], g, reinterpret_cast<uint4*>(dst + (size_t)r * K + 16 * b));
     }
     for (int i = ctid + kBRegBlocks * kConsumerThreads; i < total; i += kConsumerThreads) {
@@ -394,46 +401,12 @@ __device__ __noinline__ void prepare_b_rows(const uint16_t* const* src, int nrow
             a0 = ld_row16<GSRC>(src[r] + 16 * b);
             a1 = ld_row16<GSRC>(src[r] + 16 * b + 8);
         }
-        const float g = W4A4 ? __fdiv_rn(__uint_as_float(red[r]), 2688.0f) : 0.0f;
+        const float g = W4A4 ? __fdiv_rn(__uint_as_float(red[r]), 2688.0f)
+                             : w4a16_row_inv_scale(__uint_as_float(red[r]));
         b_block_store<W4A4>(a0, a1, g, reinterpret_cast<uint4*>(dst + (size_t)r * K + 16 * b));
     }
     consumer_bar();
 }
 
-
-// B rows from global bf16 rows whose globals are already known: gk[r] holds
-// the row amax bits (W4A4; g = amax / 2688), so every block is quantised
-// independently in one pass. Rows with src == null are zero-filled.
-template <bool W4A4>
-__device__ __noinline__ void prepare_b_rows_known_amax(const uint16_t* const* src, int nrows, int K, __half* dst,
-                                                          const unsigned int* amax_bits, float* gout) {
-    const int ctid = threadIdx.x;
-    const int nb = K >> 4;
-    if (W4A4 && ctid < nrows) gout[ctid] = __fdiv_rn(__uint_as_float(amax_bits[ctid]), 2688.0f);
-    for (int i0 = ctid; i0 < nrows * nb; i0 += kBRegBlocks * kConsumerThreads) {
-        uint4 u[kBRegBlocks][2];
-#pragma unroll
-        for (int m = 0; m < kBRegBlocks; ++m) {
-            const int i = i0 + m * kConsumerThreads;
-            u[m][0] = u[m][1] = make_uint4(0, 0, 0, 0);
-            if (i < nrows * nb) {
-                const int r = i / nb, b = i % nb;
-                if (src[r]) {
-                    u[m][0] = __ldcg(reinterpret_cast<const uint4*>(src[r] + 16 * b));
-                    u[m][1] = __ldcg(reinterpret_cast<const uint4*>(src[r] + 16 * b + 8));
-                }
-            }
-        }
-#pragma unroll
-        for (int m = 0; m < kBRegBlocks; ++m) {
-            const int i = i0 + m * kConsumerThreads;
-            if (i >= nrows * nb) break;
-            const int r = i / nb, b = i % nb;
-            const float g = W4A4 ? __fdiv_rn(__uint_as_float(amax_bits[r]), 2688.0f) : 0.0f;
-            b_block_store<W4A4>(u[m][0], u[m][1], g, reinterpret_cast<uint4*>(dst + (size_t)r * K + 16 * b));
-        }
-    }
-    consumer_bar();
-}
 
 }  // namespace nvfp4moe

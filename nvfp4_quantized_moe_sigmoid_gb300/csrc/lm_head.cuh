@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Ring ring;
     __shared__ const uint16_t* srcs[kLmMaxT];
+    __shared__ float gx[kLmMaxT];            // per token: the W4A16 row prescale 2^e
+    __shared__ unsigned int red[kLmMaxT];    // per token: the row amax
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stage_bytes = 9 * a.H;
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
         }
         if (threadIdx.x < a.T) srcs[threadIdx.x] = xn + (size_t)threadIdx.x * a.H;
         consumer_bar();
-        prepare_b_rows<false, false>(srcs, a.T, a.H, xb, nullptr, nullptr);
+        prepare_b_rows<false, false>(srcs, a.T, a.H, xb, gx, red);
         const float gw = __ldg(a.global);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
                 const int t = 2 * q + (v & 1);
-                if (t < a.T) a.logits[(size_t)t * a.ld + row0 + g + 8 * (v >> 1)] = __fmul_rn(acc[v], gw);
+                if (t < a.T) a.logits[(size_t)t * a.ld + row0 + g + 8 * (v >> 1)] = __fmul_rn(acc[v], __fmul_rn(gw, gx[t]));
             }
         }
     }

@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_up_decode(const UpArgs a) {
                 const int t = 2 * q + (v & 1);
                 const int row = 16 * r + g + 8 * (v >> 1);
                 if (t >= a.T) continue;
-                const float gs = W4A4 ? __fmul_rn(gw, gx[t]) : gw;
+                const float gs = __fmul_rn(gw, gx[t]);  // gx: W4A4 row global, W4A16 row prescale
                 const float uval = __fmul_rn(acc[v], gs);
                 const float rl = fmaxf(uval, 0.0f);
                 const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
                 const int t = 2 * q + (v & 1);
                 const int row = 16 * r + g + 8 * (v >> 1);
                 if (t >= a.T || sl < 0) continue;
-                const float gs = W4A4 ? __fmul_rn(gw, gbf[sl * a.T + t]) : gw;
+                const float gs = __fmul_rn(gw, gbf[sl * a.T + t]);
                 const float y = __fmul_rn(acc[v], gs);
                 if (routed) {
                     const int j = plan.choice[u][t];

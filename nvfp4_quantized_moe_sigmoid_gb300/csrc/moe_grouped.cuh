@@ -146,21 +146,22 @@ __global__ void __launch_bounds__(kGThreads) k_prep_rows(const uint16_t* __restr
         }
         __syncthreads();
     }
-    float g = 0.0f;
-    if (W4A4) {
-        if (amax_bits) {
-            g = __fdiv_rn(__uint_as_float(__ldcg(amax_bits + r)), 2688.0f);
-        } else {
-            float mx = 0.0f;
-            for (int i = tid; i < K; i += kGThreads)
-                mx = fmaxf(mx, fabsf(__uint_as_float(static_cast<uint32_t>(row[i]) << 16)));
-            mx = warp_max(mx);
-            if (lane == 0) atomicMax(&amax_s, __float_as_uint(mx));
-            __syncthreads();
-            g = __fdiv_rn(__uint_as_float(amax_s), 2688.0f);
-        }
-        if (tid == 0) gout[r] = g;
+    // the row factor: W4A4 the row global amax / 2688 (g quantises the row);
+    // W4A16 the prescale 2^e of a row whose amax reaches 2^15 (g = 2^-e)
+    float g = 0.0f, amax = 0.0f;
+    if (amax_bits) {
+        amax = __uint_as_float(__ldcg(amax_bits + r));
+    } else {
+        float mx = 0.0f;
+        for (int i = tid; i < K; i += kGThreads)
+            mx = fmaxf(mx, fabsf(__uint_as_float(static_cast<uint32_t>(row[i]) << 16)));
+        mx = warp_max(mx);
+        if (lane == 0) atomicMax(&amax_s, __float_as_uint(mx));
+        __syncthreads();
+        amax = __uint_as_float(amax_s);
     }
+    g = W4A4 ? __fdiv_rn(amax, 2688.0f) : w4a16_row_inv_scale(amax);
+    if (tid == 0 && gout) gout[r] = W4A4 ? g : w4a16_row_scale(amax);
     __half* d = dst + (size_t)r * K;
     for (int b = tid; b < (K >> 4); b += kGThreads) {
         const uint4 u0 = *reinterpret_cast<const uint4*>(row + 16 * b);
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kGThreads) k_grouped(const GroupedArgs a) {
                     br = pos;
                     pv = pos;
                 }
-                if (W4A4) gl = __ldg((routed ? a.g_routed : a.g_shared) + br);
+                gl = __ldg((routed ? a.g_routed : a.g_shared) + br);  // W4A4 global, W4A16 prescale
             }
             brow[tid] = br;
             posv[tid] = pv;
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kGThreads) k_grouped(const GroupedArgs a) {
                 const int row = m0 + rg * 16 + g + 8 * (v >> 1);
                 if (v < 2) m[cb][v] = 0.0f;
                 if (col >= npos) continue;
-                const float gs = W4A4 ? __fmul_rn(gw, bglob[col]) : gw;
+                const float gs = __fmul_rn(gw, bglob[col]);
                 const float y = __fmul_rn(acc[cb][v], gs);
                 const int pv = posv[col];
                 if (KIND == kGroupedUp) {

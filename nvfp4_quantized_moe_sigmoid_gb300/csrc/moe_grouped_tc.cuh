@@ -153,17 +153,6 @@ __device__ __forceinline__ uint32_t umma_idesc_mxf4(int n) {
 // critical path, and a suspended waiter resumes only some hundreds of
 // nanoseconds after the phase completes; the few waiting warps cost no issue
 // slots the tensor cores need.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 __device__ __noinline__ bool tc_wait(uint64_t* b, uint32_t parity, volatile int* abort_s) {
     if (mbar_test_wait(b, parity)) return true;
     const unsigned long long t0 = globaltimer();

@@ -59,7 +59,7 @@ __device__ __forceinline__ void cta_prepare_row_global(const uint16_t* src, int 
         }
     }
     float g = 0.0f;
-    if (W4A4) {
+    {
         if (ctid == 0) *red_slot = 0u;
         consumer_bar();
         float mx = 0.0f;
@@ -76,8 +76,9 @@ __device__ __forceinline__ void cta_prepare_row_global(const uint16_t* src, int 
         mx = warp_max(mx);
         if ((ctid & 31) == 0) atomicMax(red_slot, __float_as_uint(mx));
         consumer_bar();
-        g = __fdiv_rn(__uint_as_float(*red_slot), 2688.0f);
-        if (ctid == 0) *gout = g;
+        const float amax = __uint_as_float(*red_slot);
+        g = W4A4 ? __fdiv_rn(amax, 2688.0f) : w4a16_row_inv_scale(amax);
+        if (ctid == 0) *gout = W4A4 ? g : w4a16_row_scale(amax);  // the epilogue's row factor
     }
 #pragma unroll
     for (int m = 0; m < kBRegBlocks; ++m) {
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_up(const LayerUpArgs a) {
                 const int t = 2 * q + (v & 1);
                 const int row = 16 * r + g + 8 * (v >> 1);
                 if (t >= a.T) continue;
-                const float gs = W4A4 ? __fmul_rn(gw, gx[t]) : gw;
+                const float gs = __fmul_rn(gw, gx[t]);  // gx: W4A4 row global, W4A16 row prescale
                 const float uval = __fmul_rn(acc[v], gs);
                 const float rl = fmaxf(uval, 0.0f);
                 const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_down(const LayerDownArgs 
                 const int t = 2 * q + (v & 1);
                 const int row = 16 * r + g + 8 * (v >> 1);
                 if (t >= a.T || sl < 0) continue;
-                const float gs = W4A4 ? __fmul_rn(gw, gbf[sl * a.T + t]) : gw;
+                const float gs = __fmul_rn(gw, gbf[sl * a.T + t]);
                 const float y = __fmul_rn(acc[v], gs);
                 if (routed) {
                     const int j = plan.choice[u][t];

@@ -44,8 +44,8 @@
 // (router rows, shared-expert up tiles) as soon as stages free up, so they
 // land while the current layer is still waiting on its dependencies.
 // Every wait is bounded; a CTA that gives up sets the workspace abort flag,
-// which ends every other CTA's waits, and the last CTA to leave resets the
-// counters for the next call.
+// which ends every other CTA's waits, and the last CTA to leave clears it
+// for the next call.
 //
 // The steps are out-of-line functions sharing one per-CTA context in shared
 // memory, which keeps the code a layer runs small enough for the SM's
@@ -73,13 +73,9 @@ struct StackLayer {
     const float* router_b;  // [E]
 };
 
-// Per-layer counters: fixed slots, then one per unique expert.
-constexpr int kCntLogits = 0;  // router logits written (target E)
-constexpr int kCntShUp = 1;    // shared-expert up tiles done (target S/16)
-constexpr int kCntPart = 2;    // CTAs whose partial of h_{l+1} is written (target G)
-constexpr int kCntHDone = 3;   // CTAs whose rows of h_{l+1} are final (target G)
-constexpr int kCntUp = 4;      // + u: up tiles of unique expert u done (target I/16)
-__host__ __device__ constexpr int stack_cnt_per_layer(int /*H*/) { return kCntUp + kDecodeMaxU; }
+// Control words of the workspace: the count of CTAs that have left, the
+// abort flag, the epoch (completed calls).
+constexpr int kCtlExit = 0, kCtlAbort = 1, kCtlEpoch = 2, kCtlWords = 3;
 
 // Column-block layout of a down matrix W [H][C] (NVFP4, C the reduction
 // dimension): block c holds columns [16 c, 16 c + 16) of every row, 9 H bytes:
@@ -94,11 +90,21 @@ constexpr int kUnitRows = 16;
 constexpr int kMaxUnits = 32;      // units per CTA and layer
 constexpr int kDownMaxPairs = 8;   // 32-row pairs per consumer warp: H <= 12 x 8 x 32 = 3072
 
+// Values that every CTA waits for carry the layer they belong to: a router
+// logit is one 64-bit word {float bits, tag}, an element of a layer output one
+// 32-bit word {bf16 bits, low 16 bits of the tag}, each written with a single
+// store. A reader polls the words themselves until every tag is the current
+// layer's, so one round trip to L2 both waits and reads (a count that
+// publishes separate data costs a second one). tag = 32 epoch + l + 1, where
+// the epoch word counts completed calls on this workspace: never 0 (the value
+// of a zeroed workspace), and a word left by an earlier layer or call never
+// carries the current tag.
 struct StackWs {
-    int* cnt;            // [L][stack_cnt_per_layer], then the exit count and the abort flag
-    float* z;            // [L][T][E] router logits
-    unsigned int* amax;  // [2][T*k + T] intermediate row amax bits (routed, then shared), by layer parity
-    float* part;         // [G][T][H] per-CTA partials of the layer output
+    int* cnt;                // control words [kCtlWords]
+    unsigned long long* zt;  // [L][T][E] tagged router logits
+    unsigned int* hx;        // [T][H] tagged layer output (the next layer's input)
+    unsigned long long* amx;   // [G][T] tagged amax of each CTA's intermediate values per token (W4A4)
+    unsigned long long* part;  // [G][T][H] tagged per-CTA partials of the layer output
 };
 
 struct StackArgs {
@@ -115,53 +121,172 @@ struct StackArgs {
     int off_uact, off_ubq;          // per-unit intermediate values, per-unit down B operands
 };
 
-// Counter updates that publish data: the warp's (or CTA's) earlier writes,
-// ordered before the executing thread by a warp or CTA barrier, are visible
-// to whoever acquires the counter (no separate full fence).
-__device__ __forceinline__ void red_release_add(int* p, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ int atom_acq_rel_add(int* p, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
-// Wait until *p >= target. False if the wait expired (flags the error word and
-// the abort flag) or another CTA raised the abort flag.
-__device__ __noinline__ bool wait_geq(const int* p, int target, int* abort_g) {
-    if (ld_acquire_gpu(p) >= target) return true;  // no timer read when nothing to wait for
-    const unsigned long long t0 = globaltimer();
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u32(unsigned int* p, unsigned int v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Poll-and-read of tagged words (StackWs): false if the abort flag rose or the
+// wait expired (flags the error word and the abort flag).
+__device__ __forceinline__ bool poll_give_up(unsigned long long& t0, int it, const int* abort_g) {
+    if (it == 0) {
+        t0 = globaltimer();
+        return false;
+    }
+    if (ld_acquire_gpu(abort_g)) return true;
+    if (globaltimer() - t0 > kWaitTimeoutNs) {
+        set_dev_error(kErrWaitPeer);
+        atomicExch(const_cast<int*>(abort_g), 1);
+        return true;
+    }
+    return false;
+}
+// Eight consecutive bf16 elements of a tagged layer output -> out (packed).
+__device__ __noinline__ bool poll_h8(const unsigned int* p, uint32_t tag16, uint4& out, const int* abort_g) {
+    unsigned long long t0 = 0;
     for (int it = 0;; ++it) {
-        if (ld_acquire_gpu(p) >= target) return true;  // (a sleep here cost ~7 us a step)
-        if ((it & 15) == 15) {
-            if (ld_acquire_gpu(abort_g)) return false;
+        const uint4 a = ld_relaxed_v4(p), b = ld_relaxed_v4(p + 4);
+        const uint32_t hi = tag16 << 16;
+        if (((a.x & 0xFFFF0000u) == hi) & ((a.y & 0xFFFF0000u) == hi) & ((a.z & 0xFFFF0000u) == hi) &
+            ((a.w & 0xFFFF0000u) == hi) & ((b.x & 0xFFFF0000u) == hi) & ((b.y & 0xFFFF0000u) == hi) &
+            ((b.z & 0xFFFF0000u) == hi) & ((b.w & 0xFFFF0000u) == hi)) {
+            out = make_uint4((a.x & 0xFFFFu) | (a.y << 16), (a.z & 0xFFFFu) | (a.w << 16), (b.x & 0xFFFFu) | (b.y << 16),
+                             (b.z & 0xFFFFu) | (b.w << 16));
+            return true;
+        }
+        if ((it & 15) == 0 && poll_give_up(t0, it, abort_g)) return false;
+    }
+}
+// One tagged router logit.
+__device__ __noinline__ bool poll_logit(const unsigned long long* p, uint32_t tag, float& out, const int* abort_g) {
+    unsigned long long t0 = 0;
+    for (int it = 0;; ++it) {
+        const unsigned long long w = ld_relaxed_u64(p);
+        if (static_cast<uint32_t>(w >> 32) == tag) {
+            out = __uint_as_float(static_cast<uint32_t>(w));
+            return true;
+        }
+        if ((it & 15) == 0 && poll_give_up(t0, it, abort_g)) return false;
+    }
+}
+__device__ __forceinline__ unsigned long long tagged_logit(float z, uint32_t tag) {
+    return (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(z);
+}
+__device__ __forceinline__ unsigned long long tagged_f32(float v, uint32_t tag) { return tagged_logit(v, tag); }
+
+// Spins on the non-blocking test (the producer's hand-offs are on the
+// critical path of every layer); gives up on the CTA abort flag or after 1 s.
+__device__ __noinline__ bool mbar_wait_abortable(uint64_t* b, uint32_t parity, volatile int* abort_s,
+                                                unsigned int err = kErrWaitFull) {
+    if (mbar_test_wait(b, parity)) return true;  // no timer read when the phase is done
+    const unsigned long long t0 = globaltimer();
+    for (int it = 1;; ++it) {
+        if (mbar_test_wait(b, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_s) return false;
             if (globaltimer() - t0 > kWaitTimeoutNs) {
-                set_dev_error(kErrWaitPeer);
-                atomicExch(abort_g, 1);
+                set_dev_error(err);
                 return false;
             }
         }
     }
 }
 
-__device__ __noinline__ bool mbar_wait_abortable(uint64_t* b, uint32_t parity, volatile int* abort_s,
-                                                unsigned int err = kErrWaitFull) {
-    if (mbar_try_wait(b, parity)) return true;  // no timer read and no suspension when the phase is done
-    const unsigned long long t0 = globaltimer();
-    for (;;) {
-        if (mbar_try_wait_sleep(b, parity)) return true;
-        if (*abort_s) return false;
-        if (globaltimer() - t0 > kWaitTimeoutNs) {
-            set_dev_error(err);
-            return false;
-        }
+// ---------------------------------------------------------------- phase trace
+// Built with -DNVFP4MOE_TRACE, every CTA records the global timer at the
+// phase boundaries of every layer (consumer thread 0 and the producer) into
+// g_stack_trace[CTA][layer][event], read back by nvfp4moe_stack_trace_read.
+// Without the flag the trace points compile to nothing.
+enum StackTraceEvent : int {
+    kTrStart = 0,    // layer begins (consumer)
+    kTrHReady,       // every CTA's rows of h_l are final
+    kTrRouter,       // input, norm and this CTA's router logits posted
+    kTrLogits,       // all E logits posted
+    kTrPlan,         // top-k and the plan of unique experts written
+    kTrUp,           // this CTA's up tiles done
+    kTrAmax,         // (W4A4) the expert's row amax final; down operands ready
+    kTrDown,         // this CTA's down units done, partial posted
+    kTrParts,        // every CTA's partial posted
+    kTrReduce,       // this CTA's rows of h_{l+1} written
+    kTrProdFirst,    // producer: first item of the layer issued
+    kTrProdLast,     // producer: last item of the layer issued
+    kTrEvents = 16
+};
+constexpr int kTraceMaxCtas = 256;
+#if defined(NVFP4MOE_TRACE)
+__device__ unsigned long long g_stack_trace[kTraceMaxCtas * kStackMaxLayers * kTrEvents];
+#define STACK_TRACE(cond, b, l, ev)                                                                        \
+    do {                                                                                                   \
+        if ((cond) && (b) < kTraceMaxCtas) g_stack_trace[((b) * kStackMaxLayers + (l)) * kTrEvents + (ev)] = \
+                                              globaltimer();                                               \
+    } while (0)
+#else
+#define STACK_TRACE(cond, b, l, ev) \
+    do {                            \
+    } while (0)
+#endif
+
+// ---------------------------------------------------------------- L2 prefetch
+// Decode streams each layer's weights once; the experts a layer routes to are
+// known only once its plan is written, and one CTA alone pulls its own units'
+// tiles at a few tens of GB/s. So, as soon as the plan exists, every CTA asks
+// L2 for its 1/G share (by bytes) of everything the layer will still read
+// from HBM: the routed experts' up rows and down column blocks, then the next
+// layer's shared expert and router rows. The whole GPU then streams them at
+// the HBM rate, and each CTA's own staging copies find them in L2.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+struct ByteRange {
+    const uint8_t* p;
+    long long n;  // a multiple of 16 bytes; p 16-byte aligned
+};
+
+constexpr long long kPrefetchChunk = 65536;
+
+// The share of CTA b of G of the concatenation of ranges range(0 .. nr - 1),
+// split over the 32 lanes of the calling warp.
+template <typename F>
+__device__ __forceinline__ void l2_prefetch_share(int nr, F range, int b, int G, int lane) {
+    long long tot = 0;
+#pragma unroll 1
+    for (int i = 0; i < nr; ++i) tot += range(i).n;
+    const long long per = (tot + 16LL * G - 1) / (16LL * G) * 16;
+    const long long s0 = per * b, s1 = min(tot, s0 + per);
+    if (s0 >= s1) return;
+    const long long pl = (s1 - s0 + 16LL * 32 - 1) / (16LL * 32) * 16;
+    const long long l0 = s0 + pl * lane, l1 = min(s1, l0 + pl);
+    long long base = 0;
+#pragma unroll 1
+    for (int i = 0; i < nr && base < l1; ++i) {
+        const ByteRange r = range(i);
+        const long long x0 = max(base, l0), x1 = min(base + r.n, l1);
+#pragma unroll 1
+        for (long long x = x0; x < x1; x += kPrefetchChunk)
+            l2_prefetch(r.p + (x - base), static_cast<uint32_t>(min(kPrefetchChunk, x1 - x)));
+        base += r.n;
     }
 }
 
@@ -211,9 +336,9 @@ struct StackCta {
     uint64_t qbar;  // producer done reading the plan (one phase per layer)
     int gate_issued;
     int abort_s;
-    int last_cta;  // this CTA is the last to leave (resets the workspace)
+    uint32_t tag0;  // tag of layer 0 of this call (StackWs)
     // geometry
-    int G, b, ring_cap, ng, amax_stride;
+    int G, b, ring_cap, ng;
     int cs;          // CTAs [0, cs) take the shared expert's units
     int ex, ub, ue;  // this layer's units of this CTA: expert (-1 shared, else slot), [ub, ue) of its units
     uint8_t* ring_base;
@@ -229,6 +354,7 @@ struct StackCta {
     float norm_inv[kDecodeMaxT];
     float gx[kDecodeMaxT];
     unsigned int red[kDecodeMaxT];
+    unsigned int amax_s[kDecodeMaxT];   // this CTA's intermediate values, max per token (W4A4)
     float fct[kDecodeMaxT];             // per token: gate x down global (x B global)
     float gb[kDecodeMaxT];              // per token: the down B global (W4A4)
     int sel_idx[kDecodeMaxT][kDecodeMaxK];
@@ -298,12 +424,8 @@ __device__ __forceinline__ bool bgroup_tile(StackCta& c, int li, int K, const __
     return o.lead != 0;
 }
 
-__device__ __forceinline__ int* layer_cnt(const StackArgs& a, int l) {
-    return a.ws.cnt + (size_t)l * stack_cnt_per_layer(a.H);
-}
-__device__ __forceinline__ int* abort_flag(const StackArgs& a) {
-    return a.ws.cnt + (size_t)a.L * stack_cnt_per_layer(a.H) + 1;
-}
+__device__ __forceinline__ int* abort_flag(const StackArgs& a) { return a.ws.cnt + kCtlAbort; }
+__device__ __forceinline__ int* epoch_word(const StackArgs& a) { return a.ws.cnt + kCtlEpoch; }
 
 // Even share of n items: CTA b of G takes [n b / G, n (b + 1) / G) (n G < 2^31).
 __device__ __forceinline__ int share_begin32(int n, int b, int G) { return n * b / G; }
@@ -321,7 +443,7 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 // eight elements 256c + 8l .. + 7 in order (fused multiply-add), an
 // xor-shuffle tree gives the chunk sum, chunk sums are added in chunk order.
 template <bool W4A4>
-__device__ __noinline__ void st_input(const StackArgs& a, StackCta& c, const uint16_t* h, int l) {
+__device__ __noinline__ bool st_input(const StackArgs& a, StackCta& c, int l) {
     const int ctid = threadIdx.x, warp = ctid >> 5, lane = ctid & 31;
     const int T = a.T, H = a.H;
     uint16_t* X = c.X;
@@ -329,10 +451,17 @@ __device__ __noinline__ void st_input(const StackArgs& a, StackCta& c, const uin
         c.shu_g = __ldg(a.layer[l].shu_global);
         c.shd_g = __ldg(a.layer[l].shd_global);
     }
+    bool ok = true;
+    const uint32_t tag16 = (c.tag0 + l - 1) & 0xFFFFu;  // h_l is layer l - 1's output
 #pragma unroll 1
-    for (int i = 8 * ctid; i < T * H; i += 8 * kConsumerThreads)
-        *reinterpret_cast<uint4*>(X + i) = __ldcg(reinterpret_cast<const uint4*>(h + i));
-    consumer_bar();
+    for (int i = 8 * ctid; i < T * H && ok; i += 8 * kConsumerThreads) {
+        uint4 v;
+        if (l == 0) v = __ldcg(reinterpret_cast<const uint4*>(a.hidden_in + i));
+        else ok = poll_h8(a.ws.hx + i, tag16, v, abort_flag(a));
+        *reinterpret_cast<uint4*>(X + i) = v;
+    }
+    STACK_TRACE(ctid == 0, c.b, l, kTrHReady);
+    if (consumer_bar_or(!ok || cta_abort(c))) return false;
     if (a.rms_eps > 0.0f) {
         const int nch = (H + 255) >> 8;
 #pragma unroll 1
@@ -383,9 +512,10 @@ __device__ __noinline__ void st_input(const StackArgs& a, StackCta& c, const uin
             *reinterpret_cast<uint4*>(X + i) = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
-    // B operand: per-row global = amax / 2688 (W4A4), then each 16-block
+    // B operand: the row amax gives the row factor (W4A4 the global amax /
+    // 2688, W4A16 the prescale 2^e), then each 16-block
     const int nb = H >> 4;
-    if (W4A4) {
+    {
         if (ctid < T) c.red[ctid] = 0u;
         consumer_bar();
 #pragma unroll 1
@@ -401,16 +531,21 @@ __device__ __noinline__ void st_input(const StackArgs& a, StackCta& c, const uin
         }
     }
     consumer_bar();
-    if (W4A4 && ctid < T) c.gx[ctid] = __fdiv_rn(__uint_as_float(c.red[ctid]), 2688.0f);
+    if (ctid < T) {
+        const float amax = __uint_as_float(c.red[ctid]);
+        c.gx[ctid] = W4A4 ? __fdiv_rn(amax, 2688.0f) : w4a16_row_scale(amax);
+    }
 #pragma unroll 1
     for (int i = ctid; i < T * nb; i += kConsumerThreads) {
         const int r = i / nb;
         const uint16_t* p = X + (size_t)r * H + 16 * (i % nb);
-        const float g = W4A4 ? __fdiv_rn(__uint_as_float(c.red[r]), 2688.0f) : 0.0f;
+        const float amax = __uint_as_float(c.red[r]);
+        const float g = W4A4 ? __fdiv_rn(amax, 2688.0f) : w4a16_row_inv_scale(amax);
         b_block_store<W4A4>(*reinterpret_cast<const uint4*>(p), *reinterpret_cast<const uint4*>(p + 8), g,
                             reinterpret_cast<uint4*>(c.xq + (size_t)r * H + 16 * (i % nb)));
     }
     consumer_bar();
+    return true;
 }
 
 // ---------------------------------------------------------------- step 3
@@ -424,7 +559,8 @@ __device__ __noinline__ bool st_router(const StackArgs& a, StackCta& c, int l) {
         if (ctid == 0 && !ok) set_dev_error(kErrWaitFull);
         return false;
     }
-    float* z = a.ws.z + (size_t)l * T * E;
+    unsigned long long* z = a.ws.zt + (size_t)l * T * E;
+    const uint32_t tag = c.tag0 + l;
 #pragma unroll 1
     for (int j = 0; j < c.ng; ++j) {
         const float4* w4 = reinterpret_cast<const float4*>(c.gsm + (size_t)j * H);
@@ -455,18 +591,17 @@ __device__ __noinline__ bool st_router(const StackArgs& a, StackCta& c, int l) {
             float s = 0.0f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) s = __fadd_rn(s, c.zred[w][ctid]);
-            z[(size_t)ctid * E + c.b + j * c.G] = s;
+            st_relaxed_u64(z + (size_t)ctid * E + c.b + j * c.G, tagged_logit(s, tag));
         }
         consumer_bar();
     }
-    if (ctid == 0 && c.ng > 0) red_release_add(layer_cnt(a, l) + kCntLogits, c.ng);
     return true;
 }
 
 constexpr int kT1MaxNg = 2;  // router rows per CTA on the one-token path
 
 template <bool W4A4>
-__device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c, const uint16_t* h, int l) {
+__device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c, int l) {
     const int ctid = threadIdx.x, warp = ctid >> 5, lane = ctid & 31;
     const int H = a.H, E = a.E;
     if (ctid == kConsumerThreads - 1) {  // used by the epilogues later in the layer
@@ -476,7 +611,12 @@ __device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c,
     const int i = 8 * ctid;
     const bool mine = i < H;
     uint4 hv = make_uint4(0, 0, 0, 0);
-    if (mine) hv = __ldcg(reinterpret_cast<const uint4*>(h + i));
+    bool hok = true;
+    if (mine) {
+        if (l == 0) hv = __ldcg(reinterpret_cast<const uint4*>(a.hidden_in + i));
+        else hok = poll_h8(a.ws.hx + i, (c.tag0 + l - 1) & 0xFFFFu, hv, abort_flag(a));  // layer l - 1's output
+    }
+    STACK_TRACE(ctid == 0, c.b, l, kTrHReady);
     uint32_t w[4] = {hv.x, hv.y, hv.z, hv.w};
     if (a.rms_eps > 0.0f) {
         float ss = 0.0f;
@@ -540,7 +680,7 @@ __device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c,
 #pragma unroll
         for (int r = 0; r < kT1MaxNg; ++r) c.zred[warp][r] = zp[r];
     }
-    if (consumer_bar_or(!ok || cta_abort(c))) {
+    if (consumer_bar_or(!ok || !hok || cta_abort(c))) {
         if (ctid == 0 && !ok) set_dev_error(kErrWaitFull);
         return false;
     }
@@ -548,7 +688,7 @@ __device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c,
     // CTA waits for them), by the last thread: its warp holds no input
     // elements when H <= 8 x 352, and warp 0 waits for the logits next
     if (ctid == kConsumerThreads - 1 && c.ng > 0) {
-        float* z = a.ws.z + (size_t)l * E;
+        unsigned long long* z = a.ws.zt + (size_t)l * E;
 #pragma unroll 1
         for (int r = 0; r < c.ng; ++r) {
             float zw[kConsumerWarps];  // all loaded first, then added in warp order
@@ -557,19 +697,19 @@ __device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c,
             float s = 0.0f;
 #pragma unroll
             for (int ww = 0; ww < kConsumerWarps; ++ww) s = __fadd_rn(s, zw[ww]);
-            z[c.b + r * c.G] = s;
+            st_relaxed_u64(z + c.b + r * c.G, tagged_logit(s, c.tag0 + l));
         }
-        red_release_add(layer_cnt(a, l) + kCntLogits, c.ng);
     }
     // the B operand: each even lane quantises the 16-block it shares with the
-    // next lane, under the row global amax / 2688 (W4A4)
+    // next lane, under the row global amax / 2688 (W4A4), or converts it to
+    // f16 under the row prescale (W4A16)
     float g = 0.0f;
-    if (W4A4) {
+    {
         float rm = 0.0f;
 #pragma unroll
         for (int ww = 0; ww < kConsumerWarps; ++ww) rm = fmaxf(rm, c.wmax[ww]);
-        g = __fdiv_rn(rm, 2688.0f);
-        if (ctid == 0) c.gx[0] = g;
+        g = W4A4 ? __fdiv_rn(rm, 2688.0f) : w4a16_row_inv_scale(rm);
+        if (ctid == 0) c.gx[0] = W4A4 ? g : w4a16_row_scale(rm);
     }
     uint32_t p[4];
 #pragma unroll
@@ -578,6 +718,42 @@ __device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c,
         b_block_store<W4A4>(make_uint4(w[0], w[1], w[2], w[3]), make_uint4(p[0], p[1], p[2], p[3]), g,
                             reinterpret_cast<uint4*>(c.xq + i));
     return true;
+}
+
+// ---------------------------------------------------------------- L2 prefetch of a layer
+// By one warp, once the plan of layer l is in shared memory: this CTA's share
+// of the routed experts' up rows (codes, scales), then of their down column
+// blocks, then of the next layer's shared expert and router rows (each group
+// split over all CTAs on its own, so that the up rows are asked for first).
+__device__ __noinline__ void st_prefetch_layer(const StackArgs& a, const StackCta& c, int l) {
+    const int lane = threadIdx.x & 31;
+    const StackLayer& P = a.layer[l];
+    const int U = c.plan.U, H = a.H, I = a.I, RI = I >> 4;
+    const long long upc = (long long)I * (H >> 1), ups = (long long)I * (H >> 4), dnb = (long long)RI * 9 * H;
+    l2_prefetch_share(
+        2 * U,
+        [&](int i) {
+            const long long e = c.plan.expert[i >> 1];
+            return (i & 1) ? ByteRange{P.up_scales + e * ups, ups} : ByteRange{P.up_codes + e * upc, upc};
+        },
+        c.b, c.G, lane);
+    l2_prefetch_share(
+        U, [&](int i) { return ByteRange{P.down_cb + (long long)c.plan.expert[i] * dnb, dnb}; }, c.b, c.G, lane);
+    if (l + 1 < a.L) {
+        const StackLayer& Q = a.layer[l + 1];
+        const int S = a.S;
+        l2_prefetch_share(
+            4,
+            [&](int i) {
+                switch (i) {
+                    case 0: return ByteRange{Q.shu_codes, (long long)S * (H >> 1)};
+                    case 1: return ByteRange{Q.shu_scales, (long long)S * (H >> 4)};
+                    case 2: return ByteRange{Q.shd_cb, (long long)(S >> 4) * 9 * H};
+                    default: return ByteRange{reinterpret_cast<const uint8_t*>(Q.router_w), (long long)a.E * H * 4};
+                }
+            },
+            c.b, c.G, lane);
+    }
 }
 
 // ---------------------------------------------------------------- step 4
@@ -593,7 +769,7 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // > 0 for every non-NaN value
 }
 
-__device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l) {
+__device__ __noinline__ bool st_topk_plan(const StackArgs& a, StackCta& c, int l) {
     const int ctid = threadIdx.x, warp = ctid >> 5, lane = ctid & 31;
     const int T = a.T, E = a.E, k = a.k;
     if (ctid < 8) c.plan.bits[ctid] = 0u;
@@ -605,16 +781,19 @@ __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l
     // sigma = 1 / (1 + exp(-z)) and the order key of sigma + bias, one
     // (token, expert) per thread
     uint32_t* const keys = reinterpret_cast<uint32_t*>(c.tk_c);
-    const float* const z = a.ws.z + (size_t)l * T * E;
+    const unsigned long long* const z = a.ws.zt + (size_t)l * T * E;
+    bool ok = true;
 #pragma unroll 1
-    for (int i = ctid; i < T * E; i += kConsumerThreads) {
-        const float s = __frcp_rn(__fadd_rn(1.0f, expf(-__ldcg(z + i))));
+    for (int i = ctid; i < T * E && ok; i += kConsumerThreads) {
+        float zi = 0.0f;
+        ok = poll_logit(z + i, c.tag0 + l, zi, abort_flag(a));
+        const float s = __frcp_rn(__fadd_rn(1.0f, expf(-zi)));
         float v = __fadd_rn(s, c.bias_s[i % E]);
         if (v != v) v = -INFINITY;
         c.tk_s[i] = s;
         keys[i] = order_key(__fadd_rn(v, 0.0f));  // -0 and +0 compare equal
     }
-    consumer_bar();
+    if (consumer_bar_or(!ok || cta_abort(c))) return false;
     if (warp < T) {
         const int t = warp;
         uint32_t key[kTopkPerLane];
@@ -686,7 +865,9 @@ __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l
         for (int w = 0; w < 8; ++w) u += __popc(c.plan.bits[w]);
         c.plan.U = u;
     }
+    if (ctid < kDecodeMaxT) c.amax_s[ctid] = 0u;
     consumer_bar();
+    return true;
 }
 
 // Step 4 for one token: the sigmoids and keys as in st_topk_plan (one expert
@@ -695,19 +876,21 @@ __device__ __noinline__ void st_topk_plan(const StackArgs& a, StackCta& c, int l
 // id, as in the general plan) and the unique experts' per-tensor globals; one
 // CTA barrier publishes it (three fewer than the general plan and
 // st_layer_globals).
-__device__ __noinline__ void st_topk_plan_t1(const StackArgs& a, StackCta& c, int l) {
+__device__ __noinline__ bool st_topk_plan_t1(const StackArgs& a, StackCta& c, int l) {
     const int ctid = threadIdx.x, lane = ctid & 31;
     const int E = a.E, k = a.k;
     uint32_t* const keys = reinterpret_cast<uint32_t*>(c.tk_c);
-    const float* const z = a.ws.z + (size_t)l * E;
+    bool ok = true;
     if (ctid < E) {
-        const float s = __frcp_rn(__fadd_rn(1.0f, expf(-__ldcg(z + ctid))));
+        float zi = 0.0f;
+        ok = poll_logit(a.ws.zt + (size_t)l * E + ctid, c.tag0 + l, zi, abort_flag(a));
+        const float s = __frcp_rn(__fadd_rn(1.0f, expf(-zi)));
         float v = __fadd_rn(s, c.bias_s[ctid]);
         if (v != v) v = -INFINITY;
         c.tk_s[ctid] = s;
         keys[ctid] = order_key(__fadd_rn(v, 0.0f));  // -0 and +0 compare equal
     }
-    consumer_bar();
+    if (consumer_bar_or(!ok || cta_abort(c))) return false;
     if (ctid < 32) {
         uint32_t key[kTopkPerLane];
         float sg[kTopkPerLane];
@@ -767,6 +950,7 @@ __device__ __noinline__ void st_topk_plan_t1(const StackArgs& a, StackCta& c, in
             c.up_g[slot] = c.upg_s[my_e];
             c.down_g[slot] = c.dng_s[my_e];
         }
+        if (lane < kDecodeMaxT) c.amax_s[lane] = 0u;
         __syncwarp();
         if (lane == 0) {
             c.plan.U = k;
@@ -774,6 +958,7 @@ __device__ __noinline__ void st_topk_plan_t1(const StackArgs& a, StackCta& c, in
         }
     }
     consumer_bar();
+    return true;
 }
 
 // The per-tensor globals of the layer's unique experts, from the staged
@@ -838,10 +1023,9 @@ template <bool W4A4>
 __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l, int base, int n, int ex) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
-    const int T = a.T, k = a.k, H = a.H;
+    const int T = a.T, H = a.H;
     const bool routed = ex >= 0;
     const int u = routed ? ex : 0;
-    unsigned int* const amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
     const __half* bcol = g < T ? c.xq + (size_t)g * H : nullptr;
     const int end = base + n;
 #pragma unroll 1
@@ -859,14 +1043,14 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
             if (t >= T) continue;
             const int j = routed ? c.plan.choice[u][t] : 0;
             if (j < 0) continue;
-            const float gs = W4A4 ? __fmul_rn(gw, c.gx[t]) : gw;
+            const float gs = __fmul_rn(gw, c.gx[t]);  // gx: W4A4 row global, W4A16 row prescale
             const float rl = fmaxf(__fmul_rn(acc[v], gs), 0.0f);
             const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
             c.uact[((size_t)(li - base) * T + t) * kUnitRows + g + 8 * (v >> 1)] =
                 *reinterpret_cast<const uint16_t*>(&bv);
             m[v & 1] = fmaxf(m[v & 1], __bfloat162float(bv));
         }
-        if (W4A4) {
+        {  // the CTA's amax per token (the W4A4 row global; the W4A16 prescale)
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {
                 m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], o));
@@ -877,12 +1061,7 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
                 for (int p = 0; p < 2; ++p) {
                     const int t = 2 * q + p;
                     if (t >= T) continue;
-                    if (routed) {
-                        const int j = c.plan.choice[u][t];
-                        if (j >= 0) atomicMax(amax + t * k + j, __float_as_uint(m[p]));
-                    } else {
-                        atomicMax(amax + T * k + t, __float_as_uint(m[p]));
-                    }
+                    if (!routed || c.plan.choice[u][t] >= 0) atomicMax(&c.amax_s[t], __float_as_uint(m[p]));
                 }
             }
         }
@@ -902,22 +1081,35 @@ __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l,
 // failed.
 template <bool W4A4>
 __device__ __noinline__ bool st_down_prep(const StackArgs& a, StackCta& c, int l) {
-    const int ctid = threadIdx.x;
-    const int T = a.T, k = a.k, RI = a.I >> 4, RS = a.S >> 4;
-    int* const cnt = layer_cnt(a, l);
+    const int ctid = threadIdx.x, warp = ctid >> 5, lane = ctid & 31;
+    const int T = a.T;
     const int ex = c.ex, nu = c.ue - c.ub;
-    int* const ecnt = cnt + (ex < 0 ? kCntShUp : kCntUp + ex);
+    const uint32_t tag = c.tag0 + l;
     consumer_bar();  // every up tile of this CTA is done
+    // W4A4: post this CTA's amax per token as a tagged word, then poll the
+    // words of every CTA of the expert: their max is the row amax, final
+    if (W4A4 && ctid < T) st_relaxed_u64(a.ws.amx + (size_t)c.b * T + ctid, tagged_f32(__uint_as_float(c.amax_s[ctid]), tag));
     bool ok = true;
-    if (ctid == 0) {
-        if (nu > 0) {
-            red_release_add(ecnt, nu);
-            if (W4A4) ok = wait_geq(ecnt, ex < 0 ? RS : RI, abort_flag(a));
-        }
-        // the factor per token (the amax is final once the count is)
-        const unsigned int* amax = a.ws.amax + (size_t)(l & 1) * c.amax_stride;
+    if (warp < T) {
+        const int t = warp;
+        float gB = 0.0f;
+        if (W4A4) {
+            const int c0 = ex < 0 ? 0 : c.cs + (c.G - c.cs) * ex / c.plan.U;
+            const int c1 = ex < 0 ? c.cs : c.cs + (c.G - c.cs) * (ex + 1) / c.plan.U;
+            float m = 0.0f;
 #pragma unroll 1
-        for (int t = 0; t < T; ++t) {
+            for (int j = c0 + lane; j < c1 && ok; j += 32) {
+                float v = 0.0f;
+                ok = poll_logit(a.ws.amx + (size_t)j * T + t, tag, v, abort_flag(a));
+                m = fmaxf(m, v);
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            gB = __fdiv_rn(warp_max(m), 2688.0f);
+        }
+        // W4A16: this CTA's own units convert under the prescale of their
+        // amax (its partial carries the matching factor)
+        const float pre = W4A4 ? gB : w4a16_row_scale(__uint_as_float(c.amax_s[t]));
+        if (lane == 0) {
             int jj = 0;
             float gate = 1.0f, dg = c.shd_g;
             if (ex >= 0) {
@@ -926,13 +1118,8 @@ __device__ __noinline__ bool st_down_prep(const StackArgs& a, StackCta& c, int l
                 dg = c.down_g[ex];
             }
             float f = 0.0f;
-            if (ok && jj >= 0 && nu > 0) {
-                const float gB =
-                    W4A4 ? __fdiv_rn(__uint_as_float(__ldcg(ex < 0 ? amax + T * k + t : amax + t * k + jj)), 2688.0f)
-                         : 0.0f;
-                f = __fmul_rn(gate, W4A4 ? __fmul_rn(dg, gB) : dg);
-                c.gb[t] = gB;
-            }
+            if (ok && jj >= 0 && nu > 0) f = __fmul_rn(gate, __fmul_rn(dg, pre));
+            c.gb[t] = W4A4 ? gB : w4a16_row_inv_scale(__uint_as_float(c.amax_s[t]));
             c.fct[t] = f;
         }
     }
@@ -946,8 +1133,7 @@ __device__ __noinline__ bool st_down_prep(const StackArgs& a, StackCta& c, int l
             u0 = src[0];
             u1 = src[1];
         }
-        b_block_store<W4A4>(u0, u1, W4A4 ? c.gb[t] : 0.0f,
-                            reinterpret_cast<uint4*>(c.ubq + ((size_t)j * T + t) * kUnitRows));
+        b_block_store<W4A4>(u0, u1, c.gb[t], reinterpret_cast<uint4*>(c.ubq + ((size_t)j * T + t) * kUnitRows));
     }
     consumer_bar();
     return true;
@@ -1031,8 +1217,9 @@ __device__ __noinline__ bool st_down_units(const StackArgs& a, StackCta& c, int 
     // each 16-row tile for tokens 2q, 2q + 1
     const bool t0 = 2 * q < T, t1 = 2 * q + 1 < T;
     const float f0 = t0 ? c.fct[2 * q] : 0.0f, f1 = t1 ? c.fct[2 * q + 1] : 0.0f;
-    float* const d0 = a.ws.part + ((size_t)c.b * T + 2 * q) * H + 32 * p0 + g;
-    float* const d1 = d0 + H;
+    unsigned long long* const d0 = a.ws.part + ((size_t)c.b * T + 2 * q) * H + 32 * p0 + g;
+    unsigned long long* const d1 = d0 + H;
+    const uint32_t tag = c.tag0 + l;
 #pragma unroll
     for (int p = 0; p < kDownMaxPairs; ++p) {
         if (p >= np) break;
@@ -1042,14 +1229,13 @@ __device__ __noinline__ bool st_down_units(const StackArgs& a, StackCta& c, int 
             for (int v = 0; v < 4; ++v) {
                 const int o = 32 * p + 16 * mt + 8 * (v >> 1);
                 if (v & 1) {
-                    if (t1) __stcg(d1 + o, __fmul_rn(f1, acc[p][mt][v]));
+                    if (t1) st_relaxed_u64(d1 + o, tagged_f32(__fmul_rn(f1, acc[p][mt][v]), tag));
                 } else if (t0) {
-                    __stcg(d0 + o, __fmul_rn(f0, acc[p][mt][v]));
+                    st_relaxed_u64(d0 + o, tagged_f32(__fmul_rn(f0, acc[p][mt][v]), tag));
                 }
             }
     }
     if (consumer_bar_or(!ok || cta_abort(c))) return false;
-    if (threadIdx.x == 0) red_release_add(layer_cnt(a, l) + kCntPart, 1);
     return true;
 }
 
@@ -1076,34 +1262,43 @@ __device__ __noinline__ bool st_reduce(const StackArgs& a, StackCta& c, int l) {
         const int t = ctid / nr, row = h0 + ctid - t * nr;
         resv = bf16_bits_to_float(__ldcg(res + (size_t)t * H + row));
     }
-    bool ok = true;
-    if (ctid == 0) ok = wait_geq(layer_cnt(a, l) + kCntPart, G, abort_flag(a));
-    if (consumer_bar_or(!ok || cta_abort(c))) return false;
-    if (c.b == 0) {
-        unsigned int* am = a.ws.amax + (size_t)((l + 1) & 1) * c.amax_stride;
-#pragma unroll 1
-        for (int i = ctid; i < c.amax_stride; i += kConsumerThreads) am[i] = 0u;
-    }
     // the chunk sums, [chunk][item], over the (dead) layer input and up B
-    // operand: T nr nch <= T (H/G + 1)(G/8 + 1) floats, within their T H
+    // operand: T nr nch <= T (H/G + 1)(G/8 + 1) floats, within their T H;
+    // the partials are tagged words, polled until every one is this layer's
+    bool ok = true;
+    const uint32_t tag = c.tag0 + l;
     float* const csum = reinterpret_cast<float*>(c.X);
 #pragma unroll 1
-    for (int i = ctid; i < items * nch; i += kConsumerThreads) {
+    for (int i = ctid; i < items * nch && ok; i += kConsumerThreads) {
         const int ch = i / items, it = i - ch * items;
         const int t = it / nr, row = h0 + it - t * nr;
-        const float* src = a.ws.part + (size_t)t * H + row;
+        const unsigned long long* src = a.ws.part + (size_t)t * H + row + (size_t)kPartChunk * ch * T * H;
+        const int n = min(kPartChunk, G - kPartChunk * ch);
         float v[kPartChunk];
+        unsigned long long t0 = 0;
+        for (int it2 = 0;; ++it2) {
+            unsigned long long w[kPartChunk];
 #pragma unroll
-        for (int j = 0; j < kPartChunk; ++j) {
-            const int b2 = kPartChunk * ch + j;
-            v[j] = b2 < G ? __ldcg(src + (size_t)b2 * T * H) : 0.0f;
+            for (int j = 0; j < kPartChunk; ++j) w[j] = j < n ? ld_relaxed_u64(src + (size_t)j * T * H) : 0ull;
+            bool all = true;
+#pragma unroll
+            for (int j = 0; j < kPartChunk; ++j) {
+                all = all && (j >= n || static_cast<uint32_t>(w[j] >> 32) == tag);
+                v[j] = j < n ? __uint_as_float(static_cast<uint32_t>(w[j])) : 0.0f;
+            }
+            if (all) break;
+            if ((it2 & 15) == 0 && poll_give_up(t0, it2, abort_flag(a))) {
+                ok = false;
+                break;
+            }
         }
         float s = v[0];
 #pragma unroll
         for (int j = 1; j < kPartChunk; ++j) s = __fadd_rn(s, v[j]);
         csum[ch * items + it] = s;
     }
-    consumer_bar();
+    STACK_TRACE(ctid == 0, c.b, l, kTrParts);
+    if (consumer_bar_or(!ok || cta_abort(c))) return false;
     if (ctid < items) {
         const int t = ctid / nr, row = h0 + ctid - t * nr;
         float s = csum[ctid];
@@ -1111,10 +1306,11 @@ __device__ __noinline__ bool st_reduce(const StackArgs& a, StackCta& c, int l) {
         for (int ch = 1; ch < nch; ++ch) s = __fadd_rn(s, csum[ch * items + ctid]);
         const float h = __fadd_rn(s, resv);
         const __nv_bfloat16 ob = __float2bfloat16_rn(h);
-        out[(size_t)t * H + row] = *reinterpret_cast<const uint16_t*>(&ob);
+        const uint32_t bits = *reinterpret_cast<const uint16_t*>(&ob);
+        out[(size_t)t * H + row] = static_cast<uint16_t>(bits);
+        if (l + 1 < a.L) st_relaxed_u32(a.ws.hx + (size_t)t * H + row, bits | (((c.tag0 + l) & 0xFFFFu) << 16));
     }
     consumer_bar();
-    if (ctid == 0) red_release_add(layer_cnt(a, l) + kCntHDone, 1);
     return true;
 }
 
@@ -1205,6 +1401,8 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
                     ++tail;
                 }
                 if (!alive) break;
+                STACK_TRACE(it == 0, b, l, kTrProdFirst);
+                STACK_TRACE(it == 2 * n - 1, b, l, kTrProdLast);
                 const int s = pli & (kSlots - 1);
                 r.vs[s] = vhead;
                 r.off[s] = static_cast<uint32_t>(phys);
@@ -1230,56 +1428,60 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
 template <bool W4A4>
 __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
     const int ctid = threadIdx.x;
-    const int T = a.T, E = a.E, H = a.H, I = a.I, RI = I >> 4;
+    const int T = a.T, H = a.H, I = a.I, RI = I >> 4;
     const int G = c.G, b = c.b;
     int base = 0;  // first ring item of the current step
     bool bad = false;
     const bool one_token = T == 1 && H <= 8 * kConsumerThreads && c.ng <= kT1MaxNg;
 #pragma unroll 1
     for (int l = 0; l < a.L; ++l) {
-        int* const cnt = layer_cnt(a, l);
-        // 1-2. the layer input, once every CTA's rows of it are final
-        if (l > 0) {
-            bool ok = true;
-            if (ctid == 0) ok = wait_geq(layer_cnt(a, l - 1) + kCntHDone, G, abort_flag(a));
-            if (consumer_bar_or(!ok || cta_abort(c))) {
-                bad = true;
-                break;
-            }
-        }
-        const uint16_t* const hin = l == 0 ? a.hidden_in : a.hidden_out + (size_t)(l - 1) * T * H;
+        STACK_TRACE(ctid == 0, b, l, kTrStart);
+        // 1-2. the layer input (tagged words: the read waits until every CTA's
+        // rows of it are final)
         if (one_token) {  // 1-3 for one token from registers
-            if (!st_input_router_t1<W4A4>(a, c, hin, l)) {
+            if (!st_input_router_t1<W4A4>(a, c, l)) {
                 bad = true;
                 break;
             }
         } else {
-            st_input<W4A4>(a, c, hin, l);
+            if (!st_input<W4A4>(a, c, l)) {
+                bad = true;
+                break;
+            }
             // 3. router logits (the wait also covers the staged bias)
             if (!st_router(a, c, l)) {
                 bad = true;
                 break;
             }
         }
-        // 4. top-k and plan as soon as every logit is posted (and the producer
-        // has stopped reading the previous plan), so that the routed weights
-        // start streaming while this CTA still works on the shared tiles
+        STACK_TRACE(ctid == 0, b, l, kTrRouter);
+        // 4. top-k and plan (the logits are tagged words: the read waits until
+        // all are posted) once the producer has stopped reading the previous
+        // plan, so that the routed weights start streaming while this CTA
+        // still works on the shared tiles
         {
             bool ok = true;
-            if (ctid == 0) ok = wait_geq(cnt + kCntLogits, E, abort_flag(a));
             if (l > 0 && !mbar_wait_abortable(&c.qbar, static_cast<uint32_t>((l - 1) & 1), &c.abort_s)) ok = false;
             if (consumer_bar_or(!ok || cta_abort(c))) {
                 bad = true;
                 break;
             }
         }
+        STACK_TRACE(ctid == 0, b, l, kTrLogits);
         if (one_token) {
-            st_topk_plan_t1(a, c, l);
+            if (!st_topk_plan_t1(a, c, l)) {
+                bad = true;
+                break;
+            }
         } else {
-            st_topk_plan(a, c, l);
+            if (!st_topk_plan(a, c, l)) {
+                bad = true;
+                break;
+            }
             st_layer_globals(c);
         }
         if (ctid == 0 && !one_token) mbar_arrive(&c.pbar);  // the producer may stream the routed weights now
+        STACK_TRACE(ctid == 0, b, l, kTrPlan);
         // 5. up tiles of this CTA's units (one expert)
         const UnitRange ur = stack_units(b, G, c.cs, a.S >> 4, RI, c.plan.U);
         const int nu = ur.ue - ur.ub;
@@ -1289,23 +1491,27 @@ __device__ __noinline__ void st_consumers(const StackArgs& a, StackCta& c) {
             c.ue = ur.ue;
         }
         if (!st_up_tiles<W4A4>(a, c, l, base, nu, ur.ex)) set_cta_abort(c);
+        STACK_TRACE(ctid == 0, b, l, kTrUp);
         base += nu;
         // 6. the units' down B operands
         if (!st_down_prep<W4A4>(a, c, l)) {
             bad = true;
             break;
         }
+        STACK_TRACE(ctid == 0, b, l, kTrAmax);
         // 7. the units' down column blocks -> this CTA's partial
         if (!st_down_units(a, c, l, base)) {
             bad = true;
             break;
         }
+        STACK_TRACE(ctid == 0, b, l, kTrDown);
         base += nu;
         // 8. this CTA's rows of h_{l+1}
         if (!st_reduce(a, c, l)) {
             bad = true;
             break;
         }
+        STACK_TRACE(ctid == 0, b, l, kTrReduce);
     }
     if (bad && ctid == 0) {
         set_cta_abort(c);
@@ -1340,11 +1546,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant
         fence_mbar_init();
         c.abort_s = 0;
         c.gate_issued = 0;
+        c.tag0 = 32u * static_cast<uint32_t>(__ldcg(epoch_word(a))) + 1u;
         c.G = G;
         c.b = b;
         c.ring_cap = a.ring_cap;
         c.ng = b < a.E ? (a.E - b + G - 1) / G : 0;
-        c.amax_stride = a.T * a.k + a.T;
         const int RS = a.S >> 4;
         c.cs = stack_shared_ctas(G, RS, a.I >> 4, min(a.T * a.k, a.E));
         c.ex = c.ub = c.ue = 0;
@@ -1374,24 +1580,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_stack(const __grid_constant
     }
     if (threadIdx.x == 0 && c.gate_issued > 0 && !mbar_wait_bounded(&c.gbar, (c.gate_issued - 1) & 1))
         set_dev_error(kErrWaitDrain);
-    // the last CTA to leave resets the counters and the row amax for the next
-    // call (from the kernel parameters: stores through the workspace pointers
-    // would make every read of the shared copy a reload)
-    const int ncnt = args.L * stack_cnt_per_layer(args.H);
-    int* const cnt_exit = args.ws.cnt + ncnt;
+    // the last CTA to leave clears the abort flag and the exit count and
+    // advances the epoch for the next call (from the kernel parameters:
+    // stores through the workspace pointers would make every read of the
+    // shared copy a reload)
+    int* const ctl = args.ws.cnt;
     if (threadIdx.x == 0) {
         __threadfence();
-        c.last_cta = atomicAdd(cnt_exit, 1) == G - 1;
-    }
-    __syncthreads();
-    if (c.last_cta) {
-        for (int i = threadIdx.x; i < ncnt; i += blockDim.x) args.ws.cnt[i] = 0;
-        for (int i = threadIdx.x; i < 2 * (args.T * args.k + args.T); i += blockDim.x) args.ws.amax[i] = 0u;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            cnt_exit[1] = 0;
+        if (atomicAdd(ctl + kCtlExit, 1) == G - 1) {
+            ctl[kCtlAbort] = 0;
+            ctl[kCtlEpoch] += 1;  // the next call's tags differ from every word this one wrote
             __threadfence();
-            *cnt_exit = 0;
+            ctl[kCtlExit] = 0;
         }
     }
 }

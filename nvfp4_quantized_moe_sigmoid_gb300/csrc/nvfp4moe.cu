@@ -3,10 +3,14 @@
 // kernels in the headers below. One translation unit, so that the device
 // error word is a single object.
 #include "nvfp4moe.h"
+#if defined(NVFP4MOE_TRACE)
+#include "nvfp4moe_trace.h"
+#endif
 
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <utility>
 
 #include "common.cuh"
@@ -31,10 +35,14 @@ int current_device() {
     return d;
 }
 
+// The host-side caches below are shared by every thread that calls the
+// library; each is read and filled under its own mutex.
 int num_sms() {
     static int cache[kMaxDevices] = {0};
+    static std::mutex mu;
     const int d = current_device();
     if (d < 0 || d >= kMaxDevices) return 1;
+    std::lock_guard<std::mutex> lock(mu);
     if (cache[d] == 0) {
         int v = 0;
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d);
@@ -45,8 +53,10 @@ int num_sms() {
 
 int smem_optin() {
     static int cache[kMaxDevices] = {0};
+    static std::mutex mu;
     const int d = current_device();
     if (d < 0 || d >= kMaxDevices) return 48 * 1024;
+    std::lock_guard<std::mutex> lock(mu);
     if (cache[d] == 0) {
         int v = 0;
         cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
@@ -66,7 +76,9 @@ int dyn_smem_limit(const void* kernel) {
     };
     static Entry table[256];
     static int used = 0;
+    static std::mutex mu;
     const int d = current_device();
+    std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (table[i].fn == kernel && table[i].dev == d) return table[i].lim;
     cudaFuncAttributes at;
@@ -195,6 +207,15 @@ nvfp4_status nvfp4_last_device_error(cudaStream_t stream) {
     }
     return NVFP4_OK;
 }
+
+#if defined(NVFP4MOE_TRACE)
+nvfp4_status nvfp4moe_stack_trace_read(void* dst, size_t bytes) {
+    if (!dst) return NVFP4_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4_ERR_CUDA;
+    const size_t n = std::min(bytes, sizeof(g_stack_trace));
+    return cudaMemcpyFromSymbol(dst, g_stack_trace, n) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+#endif
 
 nvfp4_status nvfp4_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t cols,
                             nvfp4_global_mode mode, float* global_scale, uint8_t* codes,
@@ -474,16 +495,15 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled() {
     static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+    });
     return fn;
 }
 
@@ -921,24 +941,65 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NVFP4MOE_NOALLO
 
 namespace {
 
-// Device address of g_noalloc_scratch, looked up once per device with that
-// device current (in host code the symbol itself is only a host-side handle).
+// Unique id of the calling thread's current CUDA context (never reused
+// within the process), from the driver; 0 if the driver does not provide it.
+unsigned long long current_context_id() {
+    using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+    using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_noalloc_scratch in the current context. In host code
+// the symbol is only a host-side handle; its device address is looked up with
+// cudaGetSymbolAddress once per (device, context) and cached under that
+// context's id, so that a context made later (after cudaDeviceReset, or with
+// cuCtxCreate) gets its own lookup. Without a context id every call looks it
+// up again.
 void* noalloc_scratch(nvfp4_status* st) {
-    static void* cache[kMaxDevices] = {nullptr};
+    struct Entry {
+        unsigned long long ctx;
+        int dev;
+        void* p;
+    };
+    static Entry table[64];
+    static int used = 0;
+    static std::mutex mu;
     const int d = current_device();
-    if (d < 0 || d >= kMaxDevices) {
+    // 0 before the runtime has made a context current (the lookup below does)
+    const unsigned long long ctx = current_context_id();
+    std::lock_guard<std::mutex> lock(mu);
+    if (ctx != 0)
+        for (int i = 0; i < used; ++i)
+            if (table[i].ctx == ctx && table[i].dev == d) return table[i].p;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
         *st = NVFP4_ERR_CUDA;
         return nullptr;
     }
-    if (cache[d] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-            *st = NVFP4_ERR_CUDA;
-            return nullptr;
-        }
-        cache[d] = p;
+    if (ctx != 0) {
+        if (used < 64) table[used++] = Entry{ctx, d, p};
+        else table[ctx % 64] = Entry{ctx, d, p};
     }
-    return cache[d];
+    return p;
 }
 
 }  // namespace
@@ -948,7 +1009,12 @@ extern "C" nvfp4_status moe_expert_forward_noalloc(const moe_layer_weights* w, c
                                                    int32_t T, int32_t k, nvfp4_act_mode mode,
                                                    float rms_eps, const void* residual, void* out,
                                                    cudaStream_t stream) {
-    if (!w || T < 1 || k < 1) return NVFP4_ERR_INVALID_ARG;
+    // the same argument checks as moe_expert_forward, before the size is derived from them
+    nvfp4_status cs = check_layer(w);
+    if (cs != NVFP4_OK) return cs;
+    if (!hidden || !topk_idx || !topk_w || !out || T < 1 || k < 1 || k > w->num_experts)
+        return NVFP4_ERR_INVALID_ARG;
+    if (mode != NVFP4_W4A16 && mode != NVFP4_W4A4) return NVFP4_ERR_INVALID_ARG;
     const size_t need = moe_expert_forward_workspace_size(w, T, k, mode);
     if (need == 0) return NVFP4_ERR_INVALID_ARG;
     if (need > NVFP4MOE_NOALLOC_SCRATCH_BYTES) return NVFP4_ERR_WORKSPACE;  // beyond the fixed scratch
@@ -1022,7 +1088,7 @@ extern "C" nvfp4_status nvfp4_colblock_layout(const uint8_t* codes, const uint8_
 namespace {
 
 struct StackWsOffsets {
-    size_t cnt, z, amax, part, total;
+    size_t cnt, z, hx, amx, part, total;
 };
 
 // G: the grid (one CTA per SM), whose partials of each layer output meet in
@@ -1035,10 +1101,11 @@ StackWsOffsets stack_ws(int L, int T, int k, int E, int H, int G) {
         off += align256(bytes);
         return at;
     };
-    o.cnt = take(sizeof(int) * ((size_t)L * stack_cnt_per_layer(H) + 2));
-    o.amax = take(sizeof(unsigned int) * 2 * (size_t)(T * k + T));
-    o.z = take(sizeof(float) * (size_t)L * T * E);
-    o.part = take(sizeof(float) * (size_t)G * T * H);
+    o.cnt = take(sizeof(int) * kCtlWords);  // exit count, abort flag, epoch
+    o.amx = take(sizeof(unsigned long long) * (size_t)G * T);
+    o.z = take(sizeof(unsigned long long) * (size_t)L * T * E);
+    o.hx = take(sizeof(unsigned int) * (size_t)T * H);
+    o.part = take(sizeof(unsigned long long) * (size_t)G * T * H);
     o.total = off;
     return o;
 }
@@ -1188,9 +1255,10 @@ extern "C" nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t
     a.topk_w = topk_w;
     uint8_t* base = static_cast<uint8_t*>(workspace);
     a.ws.cnt = reinterpret_cast<int*>(base + o.cnt);
-    a.ws.z = reinterpret_cast<float*>(base + o.z);
-    a.ws.amax = reinterpret_cast<unsigned int*>(base + o.amax);
-    a.ws.part = reinterpret_cast<float*>(base + o.part);
+    a.ws.zt = reinterpret_cast<unsigned long long*>(base + o.z);
+    a.ws.hx = reinterpret_cast<unsigned int*>(base + o.hx);
+    a.ws.amx = reinterpret_cast<unsigned long long*>(base + o.amx);
+    a.ws.part = reinterpret_cast<unsigned long long*>(base + o.part);
     a.ring_cap = sm.ring_cap;
     a.off_gate = sm.off_gate;
     a.off_uni = sm.off_uni;
@@ -1221,7 +1289,7 @@ extern "C" nvfp4_status moe_stack_forward(const moe_stack_layer* layers, int32_t
 namespace {
 
 struct LmWsOffsets {
-    size_t zero, xq, total;
+    size_t zero, xq, gx, total;
 };
 
 LmWsOffsets lm_ws(int T, int H) {
@@ -1231,6 +1299,8 @@ LmWsOffsets lm_ws(int T, int H) {
     off += 256;
     o.xq = off;
     off += align256((size_t)T * H * 2);
+    o.gx = off;  // per token: the W4A16 row prescale (1 unless the row's amax reaches 2^15)
+    off += align256((size_t)T * 4);
     o.total = off;
     return o;
 }
@@ -1261,8 +1331,9 @@ extern "C" nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidde
     // no routed group: its tile count reads as 0
     if (cudaMemsetAsync(ws + o.zero, 0, 4, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     __half* xq = reinterpret_cast<__half*>(ws + o.xq);
+    float* gx = reinterpret_cast<float*>(ws + o.gx);
     k_prep_rows<false><<<T, kGThreads, (size_t)H * 2, stream>>>(static_cast<const uint16_t*>(hidden), H, T, rms_eps,
-                                                                 nullptr, xq, nullptr);
+                                                                 nullptr, xq, gx);
     if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
     GroupedArgs ga{};
     ga.E = 0;
@@ -1277,6 +1348,7 @@ extern "C" nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidde
     ga.T = T;
     ga.k = 1;
     ga.b_shared = xq;
+    ga.g_shared = gx;
     ga.ysh = logits;
     const size_t gsmem = (size_t)kGStages * kGStageBytes;
     if (dyn_smem_limit(k_grouped<false, kGroupedDown>) < (int)gsmem) return NVFP4_ERR_UNSUPPORTED_SHAPE;
