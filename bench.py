@@ -300,7 +300,7 @@ def time_graph(g, iters, warm=2):
     return e0.elapsed_time(e1) / iters
 
 
-def measure_other_config(cfg_id, base, nm, rf, peak, iters=10):
+def measure_other_config(cfg_id, base, nm, rf, peak, fp4_peak, iters=10):
     """One more configuration on the weights already registered for the
     headline (the configs share seed-0 weights; the prefill config has its
     own router bias): µs/token, algorithmic GB/s and their fraction of the
@@ -335,7 +335,52 @@ def measure_other_config(cfg_id, base, nm, rf, peak, iters=10):
     out = {"workload": c["name"], "path": st.path, "T": T, "layers": L, "mode": "W4A4" if c["w4a4"] else "W4A16",
            "ms_per_step": ms, "us_per_token": ms * 1e3 / T, "step_bytes": b, "gbs": gbs, "frac_of_measured_hbm": gbs / peak,
            "unique_experts_mean": sum(uniques) / len(uniques)}
+    if st.path != "stack" and c["w4a4"]:
+        # the grouped expert GEMMs run on the FP4 tensor pipe: their flops
+        # against this GPU's measured dense FP4 throughput
+        fl = rf.moe_fp4_flops(T, L, H, I, S, K)
+        out["fp4_moe_flops"] = fl
+        out["fp4_tflops_over_step"] = fl / (ms * 1e-3) / 1e12
+        out["fp4_frac_of_measured_peak"] = out["fp4_tflops_over_step"] / fp4_peak if fp4_peak else None
     del st, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_spec_step(base, nm, rf, peak, iters=10):
+    """One self-speculative step with the MTP drafter (worklog Step 5 and
+    Step 6): k = 3 draft passes (the drafter's own 128-expert NVFP4 MoE layer
+    at one token, then the lm_head) and the verify pass (the 23 main layers
+    and the lm_head over k + 1 tokens), on the headline's weights and a
+    drafter layer of its own."""
+    import torch
+    from gen import configs, fill
+    from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack, SpecDecodeStep, register_layer
+
+    c = dict(configs.shape(2))
+    K = configs.SPEC_K
+    main = MoEDecodeStack(c["layers"], c["E"], c["H"], c["I"], c["S"], c["K"], K + 1, w4a4=True, V=c["V"],
+                          rms_eps=c["rms_eps"], weights_from=base)
+    main.make_workspace()
+    fill.hidden(main.h[0], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+    d = nm.MoELayer(c["E"], c["H"], c["I"], c["S"])
+    register_layer(d, configs.DRAFTER_LAYER, *fill.fillers(c["seed"], c["bias"]))
+    step = SpecDecodeStep(main, d, K)
+    fill.hidden(step.hd[0], c["seed"], layer=configs.DRAFTER_LAYER)
+    torch.cuda.synchronize()
+    g = step.capture()
+    ms = time_graph(g, iters, warm=3)
+    assert nm.nvfp4_last_device_error() == 0
+    uniques = main.unique_experts()
+    b = (rf.step_bytes(K + 1, uniques, c["E"], c["H"], c["I"], c["S"], c["K"], c["V"])
+         + K * (rf.layer_bytes(1, c["K"], c["E"], c["H"], c["I"], c["S"], c["K"]) + rf.lm_head_bytes(1, c["V"], c["H"])))
+    out = {"workload": "spec_decode_k3_step: %d drafter passes (1 MoE layer + lm_head, 1 token) + verify "
+                       "(%d layers + lm_head, %d tokens)" % (K, c["layers"], K + 1),
+           "ms_per_step": ms, "us_per_verified_position": ms * 1e3 / (K + 1), "step_bytes": b,
+           "gbs": b / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": b / (ms * 1e-3) / 1e9 / peak,
+           "context": "at the pages' ~2.8 accepted tokens per step (real text, RTX PRO 6000) this step would "
+                      "give %.1f us per accepted token" % (ms * 1e3 / 2.8)}
+    del step, main, g
     torch.cuda.empty_cache()
     return out
 
@@ -465,11 +510,17 @@ def run_ours(args, ws, rank, local):
     # the other configurations, on the same weights (parity cases elsewhere;
     # reported here so that every number comes from this run)
     others = None
+    fp4 = None
     if rank == 0 and not args.no_other_configs and args.layers == 0 and args.config == 1:
+        # the dense FP4 tensor-pipe peak of this GPU (block-scaled tcgen05 MMAs on every SM)
+        fp4 = {"tflops": max(nm.nvfp4_fp4_mma_peak(n, 1, 20000) for n in (128, 256)),
+               "kind": "measured: nvfp4_fp4_mma_peak, tcgen05.mma kind::mxf4nvf4 M=128 K=64, N=128 and 256, "
+                       "best of the two"}
         others = {}
         st.graph = None
         for oc in (0, 2, 3, 4):
-            others[configs.shape(oc)["name"]] = measure_other_config(oc, st, nm, rf, peak)
+            others[configs.shape(oc)["name"]] = measure_other_config(oc, st, nm, rf, peak, fp4["tflops"])
+        others["spec_decode_k3_step"] = measure_spec_step(st, nm, rf, peak)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -494,13 +545,14 @@ def run_ours(args, ws, rank, local):
                 "unique_experts_per_layer": uniques,
                 "roofline": roof, "cpu_baseline": cpu, "clocks": clk.summary(), "e2e": e2e,
                 "gpu_launches": args.steps * launches_per_step(st, T, L, c["lm_head"]),
-                "other_configs": others, **extra}
+                "other_configs": others, "fp4_peak": fp4, **extra}
         print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ phase trace
 TRACE_EVENTS = ["layer start", "h_l final (all CTAs)", "router logits posted", "all logits posted",
-                "plan written", "up tiles done", "row amax final", "down units done", "all partials posted",
+                "plan written", "routed up tiles done", "shared down + routed operands", "routed down units done",
+                "all partials read",
                 "rows of h_l+1 written", "producer: first item", "producer: last item"]
 
 

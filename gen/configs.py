@@ -35,3 +35,10 @@ def shape(cfg):
     c = dict(CONFIGS[cfg]) if isinstance(cfg, int) else dict(cfg)
     c.update(H=H, I=I, S=S, E=E, K=K, V=V)
     return c
+
+# The model's MTP head (worklog Step 5 and Step 6) has its own 128-expert MoE
+# of the same shapes; its tensors are drawn under this layer id. It drafts
+# SPEC_K tokens per step, and the main model verifies SPEC_K + 1 positions.
+DRAFTER_LAYER = 100
+SPEC_K = 3
+

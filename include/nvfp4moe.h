@@ -410,6 +410,35 @@ size_t lm_head_forward_workspace_size(const nvfp4_matrix* w, int32_t T);
 nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidden, int32_t T, float rms_eps, float* logits,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * nvfp4_fp4_mma_peak - measures this GPU's dense FP4 tensor-pipe throughput
+ * (no operation of the pages: the denominator of the FP4 roofline fraction
+ * reported for the grouped W4A4 path, [super-q] "Deployment" Blackwell W4A4).
+ * One CTA per SM issues `iters` tcgen05.mma kind::mxf4nvf4 block-scaled MMAs
+ * (M = 128, N = n, K = 64, E2M1 x E2M1 with E4M3 scales per 16 elements) from
+ * shared-memory operands into `chains` tensor-memory accumulators; a warm-up
+ * launch, then one launch timed with CUDA events on `stream`.
+ *   n       32 .. 256, a multiple of 32;  chains >= 1 with chains * n <= 448
+ *   iters   MMAs per CTA (>= 1; ~20000 keeps a launch near a millisecond)
+ *   tflops  host out: 2 * 128 * n * 64 * iters * SMs / seconds / 1e12
+ * Synchronises `stream`. Allocates no device memory (two CUDA events).
+ * Returns NVFP4_ERR_INVALID_ARG for arguments outside these ranges,
+ * NVFP4_ERR_CUDA if a launch or the timing fails.
+ */
+nvfp4_status nvfp4_fp4_mma_peak(int32_t n, int32_t chains, int32_t iters, double* tflops, cudaStream_t stream);
+
+/* Sets, on the current device, the limit of the device waits of one CTA on
+ * another CTA's progress (moe_stack_forward's polls of its tagged words):
+ * `ns` nanoseconds, or the default 1 s when ns is 0. A wait that runs out
+ * ends every CTA of its call early, and the next nvfp4_last_device_error
+ * returns NVFP4_ERR_TIMEOUT; the context stays usable, and a workspace
+ * re-initialised with moe_expert_forward_workspace_init serves the next call.
+ * Waits on a CTA's own staging copies keep 1 s. Not an operation of the
+ * pages: a watchdog setting (a short limit makes the failure path testable).
+ * Synchronous; affects calls launched afterwards. Returns NVFP4_ERR_CUDA if
+ * the device copy fails. */
+nvfp4_status nvfp4_set_peer_wait_limit(uint64_t ns);
+
 /* Human-readable name of a status code (static string). */
 const char* nvfp4_status_string(nvfp4_status status);
 

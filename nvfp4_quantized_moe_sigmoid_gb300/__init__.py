@@ -61,6 +61,19 @@ def nvfp4_last_device_error(stream=None) -> int:
     return _L.nvfp4_last_device_error(_stream(stream))
 
 
+def nvfp4_set_peer_wait_limit(ns=0):
+    """Limit (ns) of the stack kernel's waits on other CTAs; 0 restores 1 s."""
+    _check(_L.nvfp4_set_peer_wait_limit(int(ns)), "nvfp4_set_peer_wait_limit")
+
+
+def nvfp4_fp4_mma_peak(n=256, chains=1, iters=20000, stream=None) -> float:
+    """Dense FP4 tensor-pipe throughput of this GPU in TFLOP/s (block-scaled
+    tcgen05 MMAs, M = 128, N = n, K = 64, on every SM)."""
+    out = ctypes.c_double(0.0)
+    _check(_L.nvfp4_fp4_mma_peak(n, chains, iters, ctypes.byref(out), _stream(stream)), "nvfp4_fp4_mma_peak")
+    return out.value
+
+
 class NVFP4Matrix:
     """An NVFP4 matrix [n][k] in the canonical layout (device tensors)."""
 

@@ -16,7 +16,8 @@ EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_siz
            "moe_layer_forward", "moe_layer_forward_workspace_size",
            "moe_stack_forward", "moe_stack_forward_workspace_size", "moe_permute",
            "lm_head_gemv", "lm_head_forward", "lm_head_forward_workspace_size",
-           "nvfp4_colblock_layout", "nvfp4_status_string", "nvfp4_last_device_error"]
+           "nvfp4_colblock_layout", "nvfp4_status_string", "nvfp4_last_device_error",
+           "nvfp4_fp4_mma_peak", "nvfp4_set_peer_wait_limit"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20  # NVFP4MOE_NOALLOC_SCRATCH_BYTES
 STACK_MAX_LAYERS = 32  # NVFP4MOE_STACK_MAX_LAYERS
@@ -92,5 +93,9 @@ def load(path: str = LIB_PATH):
     L.nvfp4_status_string.restype = ctypes.c_char_p
     L.nvfp4_last_device_error.argtypes = [P]
     L.nvfp4_last_device_error.restype = ctypes.c_int
+    L.nvfp4_fp4_mma_peak.argtypes = [I32, I32, I32, ctypes.POINTER(ctypes.c_double), P]
+    L.nvfp4_fp4_mma_peak.restype = ctypes.c_int
+    L.nvfp4_set_peer_wait_limit.argtypes = [ctypes.c_uint64]
+    L.nvfp4_set_peer_wait_limit.restype = ctypes.c_int
     _lib = L
     return L

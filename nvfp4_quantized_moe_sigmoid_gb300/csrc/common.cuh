@@ -28,6 +28,12 @@ enum : unsigned int {
 // 1 s: device waits in this library normally take microseconds.
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
 
+// Limit of the waits of one CTA on another's progress (the stack kernel's
+// polls of tagged words), in ns: kWaitTimeoutNs unless changed with
+// nvfp4_set_peer_wait_limit. Waits on this CTA's own staging copies keep the
+// fixed 1 s, so that a CTA never leaves with copies still landing.
+__device__ unsigned long long g_peer_wait_ns = kWaitTimeoutNs;
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

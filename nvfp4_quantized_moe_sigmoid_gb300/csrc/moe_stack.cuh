@@ -147,15 +147,19 @@ __device__ __forceinline__ void st_relaxed_u32(unsigned int* p, unsigned int v) 
     asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Poll-and-read of tagged words (StackWs): false if the abort flag rose or the
-// wait expired (flags the error word and the abort flag).
+// Poll-and-read of tagged words (StackWs), called after every poll that
+// found a word not yet written: true (give up) if the wait expired (flags the
+// error word and the abort flag) or the abort flag rose. Both are checked on
+// the second poll and then every 16 (so that even a short wait sees a short
+// limit set by nvfp4_set_peer_wait_limit).
 __device__ __forceinline__ bool poll_give_up(unsigned long long& t0, int it, const int* abort_g) {
     if (it == 0) {
         t0 = globaltimer();
         return false;
     }
+    if (it != 1 && (it & 15) != 0) return false;
     if (ld_acquire_gpu(abort_g)) return true;
-    if (globaltimer() - t0 > kWaitTimeoutNs) {
+    if (globaltimer() - t0 > g_peer_wait_ns) {
         set_dev_error(kErrWaitPeer);
         atomicExch(const_cast<int*>(abort_g), 1);
         return true;
@@ -175,7 +179,7 @@ __device__ __noinline__ bool poll_h8(const unsigned int* p, uint32_t tag16, uint
                              (b.z & 0xFFFFu) | (b.w << 16));
             return true;
         }
-        if ((it & 15) == 0 && poll_give_up(t0, it, abort_g)) return false;
+        if (poll_give_up(t0, it, abort_g)) return false;
     }
 }
 // One tagged router logit.
@@ -187,7 +191,7 @@ __device__ __noinline__ bool poll_logit(const unsigned long long* p, uint32_t ta
             out = __uint_as_float(static_cast<uint32_t>(w));
             return true;
         }
-        if ((it & 15) == 0 && poll_give_up(t0, it, abort_g)) return false;
+        if (poll_give_up(t0, it, abort_g)) return false;
     }
 }
 __device__ __forceinline__ unsigned long long tagged_logit(float z, uint32_t tag) {
@@ -246,49 +250,6 @@ __device__ unsigned long long g_stack_trace[kTraceMaxCtas * kStackMaxLayers * kT
     do {                            \
     } while (0)
 #endif
-
-// ---------------------------------------------------------------- L2 prefetch
-// Decode streams each layer's weights once; the experts a layer routes to are
-// known only once its plan is written, and one CTA alone pulls its own units'
-// tiles at a few tens of GB/s. So, as soon as the plan exists, every CTA asks
-// L2 for its 1/G share (by bytes) of everything the layer will still read
-// from HBM: the routed experts' up rows and down column blocks, then the next
-// layer's shared expert and router rows. The whole GPU then streams them at
-// the HBM rate, and each CTA's own staging copies find them in L2.
-__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-struct ByteRange {
-    const uint8_t* p;
-    long long n;  // a multiple of 16 bytes; p 16-byte aligned
-};
-
-constexpr long long kPrefetchChunk = 65536;
-
-// The share of CTA b of G of the concatenation of ranges range(0 .. nr - 1),
-// split over the 32 lanes of the calling warp.
-template <typename F>
-__device__ __forceinline__ void l2_prefetch_share(int nr, F range, int b, int G, int lane) {
-    long long tot = 0;
-#pragma unroll 1
-    for (int i = 0; i < nr; ++i) tot += range(i).n;
-    const long long per = (tot + 16LL * G - 1) / (16LL * G) * 16;
-    const long long s0 = per * b, s1 = min(tot, s0 + per);
-    if (s0 >= s1) return;
-    const long long pl = (s1 - s0 + 16LL * 32 - 1) / (16LL * 32) * 16;
-    const long long l0 = s0 + pl * lane, l1 = min(s1, l0 + pl);
-    long long base = 0;
-#pragma unroll 1
-    for (int i = 0; i < nr && base < l1; ++i) {
-        const ByteRange r = range(i);
-        const long long x0 = max(base, l0), x1 = min(base + r.n, l1);
-#pragma unroll 1
-        for (long long x = x0; x < x1; x += kPrefetchChunk)
-            l2_prefetch(r.p + (x - base), static_cast<uint32_t>(min(kPrefetchChunk, x1 - x)));
-        base += r.n;
-    }
-}
 
 // ---------------------------------------------------------------- staging ring
 // A byte ring over the CTA's free shared memory. Items of 9 H bytes (an up
@@ -718,42 +679,6 @@ __device__ __noinline__ bool st_input_router_t1(const StackArgs& a, StackCta& c,
         b_block_store<W4A4>(make_uint4(w[0], w[1], w[2], w[3]), make_uint4(p[0], p[1], p[2], p[3]), g,
                             reinterpret_cast<uint4*>(c.xq + i));
     return true;
-}
-
-// ---------------------------------------------------------------- L2 prefetch of a layer
-// By one warp, once the plan of layer l is in shared memory: this CTA's share
-// of the routed experts' up rows (codes, scales), then of their down column
-// blocks, then of the next layer's shared expert and router rows (each group
-// split over all CTAs on its own, so that the up rows are asked for first).
-__device__ __noinline__ void st_prefetch_layer(const StackArgs& a, const StackCta& c, int l) {
-    const int lane = threadIdx.x & 31;
-    const StackLayer& P = a.layer[l];
-    const int U = c.plan.U, H = a.H, I = a.I, RI = I >> 4;
-    const long long upc = (long long)I * (H >> 1), ups = (long long)I * (H >> 4), dnb = (long long)RI * 9 * H;
-    l2_prefetch_share(
-        2 * U,
-        [&](int i) {
-            const long long e = c.plan.expert[i >> 1];
-            return (i & 1) ? ByteRange{P.up_scales + e * ups, ups} : ByteRange{P.up_codes + e * upc, upc};
-        },
-        c.b, c.G, lane);
-    l2_prefetch_share(
-        U, [&](int i) { return ByteRange{P.down_cb + (long long)c.plan.expert[i] * dnb, dnb}; }, c.b, c.G, lane);
-    if (l + 1 < a.L) {
-        const StackLayer& Q = a.layer[l + 1];
-        const int S = a.S;
-        l2_prefetch_share(
-            4,
-            [&](int i) {
-                switch (i) {
-                    case 0: return ByteRange{Q.shu_codes, (long long)S * (H >> 1)};
-                    case 1: return ByteRange{Q.shu_scales, (long long)S * (H >> 4)};
-                    case 2: return ByteRange{Q.shd_cb, (long long)(S >> 4) * 9 * H};
-                    default: return ByteRange{reinterpret_cast<const uint8_t*>(Q.router_w), (long long)a.E * H * 4};
-                }
-            },
-            c.b, c.G, lane);
-    }
 }
 
 // ---------------------------------------------------------------- step 4
@@ -1287,7 +1212,7 @@ __device__ __noinline__ bool st_reduce(const StackArgs& a, StackCta& c, int l) {
                 v[j] = j < n ? __uint_as_float(static_cast<uint32_t>(w[j])) : 0.0f;
             }
             if (all) break;
-            if ((it2 & 15) == 0 && poll_give_up(t0, it2, abort_flag(a))) {
+            if (poll_give_up(t0, it2, abort_flag(a))) {
                 ok = false;
                 break;
             }

@@ -14,7 +14,9 @@
 #include <utility>
 
 #include "common.cuh"
+#include "fp4_peak.cuh"
 #include "lm_head.cuh"
+#include "lm_head_tc.cuh"
 #include "moe_decode.cuh"
 #include "moe_grouped.cuh"
 #include "moe_grouped_tc.cuh"
@@ -195,6 +197,11 @@ const char* nvfp4_status_string(nvfp4_status s) {
     return "unknown status";
 }
 
+nvfp4_status nvfp4_set_peer_wait_limit(uint64_t ns) {
+    const unsigned long long v = ns == 0 ? kWaitTimeoutNs : static_cast<unsigned long long>(ns);
+    return cudaMemcpyToSymbol(g_peer_wait_ns, &v, sizeof(v)) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 nvfp4_status nvfp4_last_device_error(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     unsigned int v = 0;
@@ -255,6 +262,12 @@ nvfp4_status nvfp4_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t 
     return launch_status();
 }
 
+// From this many tokens on the router runs as k_route_rows (one CTA per 8
+// tokens and every expert: a single wave of T / 8 CTAs that read the gate
+// rows from L2) instead of clusters that split the experts (T / 8 x 8 CTAs,
+// several waves at prefill sizes).
+constexpr int kRouteManyTokens = 512;
+
 nvfp4_status moe_route_topk(const void* hidden, const float* router_w, const float* bias, int32_t T,
                             int32_t H, int32_t E, int32_t k, float rms_eps, int32_t* topk_idx,
                             float* topk_w, cudaStream_t stream) {
@@ -278,6 +291,13 @@ nvfp4_status moe_route_topk(const void* hidden, const float* router_w, const flo
                           topk_idx, topk_w, static_cast<DecodePlan*>(nullptr), static_cast<__half*>(nullptr),
                           static_cast<float*>(nullptr), 0);
     };
+    if (T >= kRouteManyTokens) {  // many tokens: one CTA per 8 tokens and every expert
+        const int smem = kRouteRowsTile * H * 2;
+        if (smem > dyn_smem_limit(k_route_rows)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        return launch_pdl(k_route_rows, (T + kRouteRowsTile - 1) / kRouteRowsTile, kConsumerThreads, smem, stream,
+                          static_cast<const uint16_t*>(hidden), router_w, bias, T, H, E, k, rms_eps, topk_idx,
+                          topk_w);
+    }
     return launch(k_route<8>, 8);
 }
 
@@ -505,6 +525,21 @@ EncodeTiledFn encode_tiled() {
             fn = reinterpret_cast<EncodeTiledFn>(p);
     });
     return fn;
+}
+
+// A row-major matrix of `rows` rows of `row_bytes` bytes as a 2-D byte
+// tensor, boxes of {box_bytes, box_rows}.
+bool byte_map(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows, int box_bytes, int box_rows,
+              CUtensorMapSwizzle swz) {
+    const EncodeTiledFn enc = encode_tiled();
+    if (!enc || !aligned(base, 16) || row_bytes % 16 || rows < 1) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Row-major [rows][K/2] NVFP4 code matrix as a 2-D byte tensor; a box
@@ -1297,8 +1332,8 @@ LmWsOffsets lm_ws(int T, int H) {
     size_t off = 0;
     o.zero = off;
     off += 256;
-    o.xq = off;
-    off += align256((size_t)T * H * 2);
+    o.xq = off;  // rows padded to a multiple of 16: the tensor-core GEMM reads whole 16-row groups
+    off += align256((size_t)((T + 15) & ~15) * H * 2);
     o.gx = off;  // per token: the W4A16 row prescale (1 unless the row's amax reaches 2^15)
     off += align256((size_t)T * 4);
     o.total = off;
@@ -1335,6 +1370,35 @@ extern "C" nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidde
     k_prep_rows<false><<<T, kGThreads, (size_t)H * 2, stream>>>(static_cast<const uint16_t*>(hidden), H, T, rms_eps,
                                                                  nullptr, xq, gx);
     if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    // the tensor-core GEMM (tcgen05 kind::f16), up to 256 tokens per launch
+    if (w->n % kLmTcRows == 0 && encode_tiled() != nullptr) {
+        const int lim = dyn_smem_limit(k_lm_head_tc);
+        const int V = static_cast<int>(w->n);
+        bool ok = lim >= 1024 + kLmTcStages * lm_tc_stage_bytes(kLmTcMaxN);
+        LmTcArgs la{};
+        ok = ok && byte_map(&la.a_map, w->codes, H / 2, V, 32, kLmTcRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (ok) {
+            la.scales = w->scales;
+            la.global = w->global_scale;
+            la.ld = V;
+            la.V = V;
+            la.H = H;
+            for (int t0 = 0; t0 < T; t0 += kLmTcMaxN) {
+                const int n = std::min(kLmTcMaxN, T - t0);
+                la.T = n;
+                la.N = (n + 15) & ~15;
+                la.gx = gx + t0;
+                la.logits = logits + (int64_t)t0 * V;
+                // rows n .. N - 1 (padding) feed only the MMA columns that are not stored
+                if (!byte_map(&la.b_map, xq + (size_t)t0 * H, 2 * H, la.N, 128, la.N, CU_TENSOR_MAP_SWIZZLE_128B))
+                    return NVFP4_ERR_CUDA;
+                const size_t smem = 1024 + (size_t)kLmTcStages * lm_tc_stage_bytes(la.N);
+                k_lm_head_tc<<<std::min(num_sms(), V / kLmTcRows), kLmTcThreads, smem, stream>>>(la);
+                if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+            }
+            return NVFP4_OK;
+        }
+    }
     GroupedArgs ga{};
     ga.E = 0;
     ga.M = 0;
@@ -1354,4 +1418,30 @@ extern "C" nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidde
     if (dyn_smem_limit(k_grouped<false, kGroupedDown>) < (int)gsmem) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     k_grouped<false, kGroupedDown><<<num_sms() * 2, kGThreads, gsmem, stream>>>(ga);
     return launch_status();
+}
+
+// ------------------------------------------------ FP4 tensor-pipe peak
+extern "C" nvfp4_status nvfp4_fp4_mma_peak(int32_t n, int32_t chains, int32_t iters, double* tflops,
+                                           cudaStream_t stream) {
+    if (!tflops || n < 32 || n > 256 || n % 32 || chains < 1 || chains * n > 448 || iters < 1)
+        return NVFP4_ERR_INVALID_ARG;
+    const size_t smem = 1024 + kPeakSmemA + kPeakSmemB;
+    if (dyn_smem_limit(k_fp4_peak) < static_cast<int>(smem)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const int grid = num_sms();
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return NVFP4_ERR_CUDA;
+    nvfp4_status st = NVFP4_OK;
+    k_fp4_peak<<<grid, kPeakThreads, smem, stream>>>(n, chains, iters);  // warm-up
+    cudaEventRecord(e0, stream);
+    k_fp4_peak<<<grid, kPeakThreads, smem, stream>>>(n, chains, iters);
+    cudaEventRecord(e1, stream);
+    float ms = 0.0f;
+    if (cudaGetLastError() != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess || ms <= 0.0f)
+        st = NVFP4_ERR_CUDA;
+    else
+        *tflops = 2.0 * 128.0 * n * 64.0 * static_cast<double>(iters) * grid / (ms * 1e-3) / 1e12;
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return st;
 }

@@ -211,4 +211,144 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteWa
     if (stage_w && !wok && threadIdx.x == 0 && !mbar_wait_bounded(&wbar, 0)) set_dev_error(kErrWaitDrain);
 }
 
+// ---------------------------------------------------------------- many tokens
+// The router for prefill and many concurrent tokens: one CTA per 8 tokens and
+// every expert, in one wave of T / 8 CTAs. The gate matrix (1.4 MB at the
+// pages' shape) stays in L2 after the first CTAs have read it, and every CTA
+// streams it from there; each warp takes two experts at a time so that every
+// hidden value it loads from shared memory serves two dot products. Logits,
+// sigmoid, biased top-k and the renormalised gates as in k_route (every
+// summation order agrees with the oracle within the binary32 bound).
+constexpr int kRouteRowsTile = 8;
+
+__global__ void __launch_bounds__(kConsumerThreads) k_route_rows(
+    const uint16_t* __restrict__ hidden, const float* __restrict__ Wg, const float* __restrict__ bias, int T, int H,
+    int E, int k, float rms_eps, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+    extern __shared__ __align__(16) unsigned char rr_smem[];
+    uint16_t* hs = reinterpret_cast<uint16_t*>(rr_smem);  // [8][H] bf16 (normalised)
+    __shared__ float zs[kRouteRowsTile][256];
+    const int t0 = blockIdx.x * kRouteRowsTile;
+    const int nt = min(kRouteRowsTile, T - t0);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
+    for (int t = warp; t < nt; t += kConsumerWarps) {
+        if (rms_eps > 0.0f)
+            warp_rmsnorm_row(hidden + (int64_t)(t0 + t) * H, hs + (size_t)t * H, H, rms_eps);
+        else
+            warp_copy_row(hidden + (int64_t)(t0 + t) * H, hs + (size_t)t * H, H);
+    }
+    __syncthreads();
+    const int H4 = H >> 2;
+    for (int e0 = 2 * warp; e0 < E; e0 += 2 * kConsumerWarps) {
+        const bool two = e0 + 1 < E;
+        const float4* w0 = reinterpret_cast<const float4*>(Wg + (int64_t)e0 * H);
+        const float4* w1 = reinterpret_cast<const float4*>(Wg + (int64_t)(two ? e0 + 1 : e0) * H);
+        float a0[kRouteRowsTile], a1[kRouteRowsTile];
+#pragma unroll
+        for (int t = 0; t < kRouteRowsTile; ++t) a0[t] = a1[t] = 0.0f;
+        for (int i0 = lane; i0 < H4; i0 += 32 * 4) {
+            float4 x0[4], x1[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + 32 * u;
+                x0[u] = i < H4 ? __ldg(w0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x1[u] = i < H4 ? __ldg(w1 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + 32 * u;
+                if (i >= H4) break;
+#pragma unroll
+                for (int t = 0; t < kRouteRowsTile; ++t) {
+                    if (t < nt) {
+                        const uint2 hv = *reinterpret_cast<const uint2*>(hs + (size_t)t * H + 4 * i);
+                        const float h0 = __uint_as_float(hv.x << 16), h1 = __uint_as_float(hv.x & 0xFFFF0000u);
+                        const float h2 = __uint_as_float(hv.y << 16), h3 = __uint_as_float(hv.y & 0xFFFF0000u);
+                        a0[t] = fmaf(x0[u].x, h0, a0[t]);
+                        a0[t] = fmaf(x0[u].y, h1, a0[t]);
+                        a0[t] = fmaf(x0[u].z, h2, a0[t]);
+                        a0[t] = fmaf(x0[u].w, h3, a0[t]);
+                        a1[t] = fmaf(x1[u].x, h0, a1[t]);
+                        a1[t] = fmaf(x1[u].y, h1, a1[t]);
+                        a1[t] = fmaf(x1[u].z, h2, a1[t]);
+                        a1[t] = fmaf(x1[u].w, h3, a1[t]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kRouteRowsTile; ++t) {
+            float v0 = a0[t], v1 = a1[t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                v0 += __shfl_xor_sync(0xffffffffu, v0, o);
+                v1 += __shfl_xor_sync(0xffffffffu, v1, o);
+            }
+            if (lane == 0 && t < nt) {
+                zs[t][e0] = v0;
+                if (two) zs[t][e0 + 1] = v1;
+            }
+        }
+    }
+    __syncthreads();
+    // top-k: one warp per token; lane l holds experts l, l + 32, ...
+    for (int t = warp; t < nt; t += kConsumerWarps) {
+        constexpr int kPer = 8;  // E <= 256
+        float c[kPer], sg[kPer];
+        bool taken[kPer];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int e = lane + 32 * q;
+            taken[q] = true;
+            c[q] = -INFINITY;
+            sg[q] = 0.0f;
+            if (e < E) {
+                sg[q] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-zs[t][e])));
+                c[q] = __fadd_rn(sg[q], __ldg(bias + e));
+                taken[q] = false;
+            }
+        }
+        float ssum = 0.0f, selsig = 0.0f;
+        int selidx = 0;
+        for (int j = 0; j < k; ++j) {
+            float bc = -INFINITY;
+            int be = 0x7FFFFFFF;
+            float bs = 0.0f;
+#pragma unroll
+            for (int q = 0; q < kPer; ++q) {
+                const int e = lane + 32 * q;
+                if (!taken[q] && (c[q] > bc || (c[q] == bc && e < be))) {
+                    bc = c[q];
+                    be = e;
+                    bs = sg[q];
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float oc = __shfl_xor_sync(0xffffffffu, bc, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+                if (oc > bc || (oc == bc && oe < be)) {
+                    bc = oc;
+                    be = oe;
+                    bs = os;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kPer; ++q)
+                if (lane + 32 * q == be) taken[q] = true;
+            ssum = __fadd_rn(ssum, bs);
+            if (lane == j) {
+                selidx = be;
+                selsig = bs;
+            }
+        }
+        if (lane < k) {
+            topk_idx[(int64_t)(t0 + t) * k + lane] = selidx;
+            topk_w[(int64_t)(t0 + t) * k + lane] = __fdiv_rn(selsig, ssum);
+        }
+    }
+}
+
 }  // namespace nvfp4moe

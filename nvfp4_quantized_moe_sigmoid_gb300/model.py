@@ -23,6 +23,30 @@ from . import (MoELayer, NVFP4Matrix, PER_TENSOR, W4A4, W4A16, _stack_layers, lm
                moe_layer_forward, moe_route_topk, moe_stack_forward, nvfp4_quantize)
 
 
+def register_layer(Lw: MoELayer, layer_id, fill_bf16, fill_router, fill_bias):
+    """Fills one MoE layer's router and quantises its bf16 master weights
+    (drawn under layer_id) to NVFP4 on the device."""
+    E, H, I, S = Lw.E, Lw.H, Lw.I, Lw.S
+    tmp = torch.empty(max(I * H, S * H), dtype=torch.bfloat16, device=Lw.up_codes.device)
+    fill_router(layer_id, Lw.router_w)
+    fill_bias(layer_id, Lw.router_b)
+    for e in range(E):
+        m = tmp[:I * H].view(I, H)
+        fill_bf16("up", layer_id, e, m)
+        nvfp4_quantize(m, PER_TENSOR, out=Lw.expert_up(e))
+        m = tmp[:H * I].view(H, I)
+        fill_bf16("down", layer_id, e, m)
+        nvfp4_quantize(m, PER_TENSOR, out=Lw.expert_down(e))
+    m = tmp[:S * H].view(S, H)
+    fill_bf16("sh_up", layer_id, 0, m)
+    nvfp4_quantize(m, PER_TENSOR, out=Lw.shared_up)
+    m = tmp[:H * S].view(H, S)
+    fill_bf16("sh_down", layer_id, 0, m)
+    nvfp4_quantize(m, PER_TENSOR, out=Lw.shared_down)
+    Lw.down_cb = None  # column-block copies are made again from these weights on first use
+    del tmp
+
+
 class MoEDecodeStack:
     def __init__(self, layers, E, H, I, S, k, T, w4a4=True, V=None, device="cuda",
                  weights_from=None, rms_eps=1e-5):
@@ -51,30 +75,14 @@ class MoEDecodeStack:
     def register(self, fill_bf16, fill_router, fill_bias):
         """fill_bf16(kind, layer, index, t) writes a bf16 master into t;
         fill_router(layer, t) / fill_bias(layer, t) write the fp32 router."""
-        H, I, S = self.H, self.I, self.S
-        tmp = torch.empty(max(I * H, S * H), dtype=torch.bfloat16, device=self.device)
+        H = self.H
         for l, Lw in enumerate(self.layers):
-            fill_router(l, Lw.router_w)
-            fill_bias(l, Lw.router_b)
-            for e in range(self.E):
-                m = tmp[:I * H].view(I, H)
-                fill_bf16("up", l, e, m)
-                nvfp4_quantize(m, PER_TENSOR, out=Lw.expert_up(e))
-                m = tmp[:H * I].view(H, I)
-                fill_bf16("down", l, e, m)
-                nvfp4_quantize(m, PER_TENSOR, out=Lw.expert_down(e))
-            m = tmp[:S * H].view(S, H)
-            fill_bf16("sh_up", l, 0, m)
-            nvfp4_quantize(m, PER_TENSOR, out=Lw.shared_up)
-            m = tmp[:H * S].view(H, S)
-            fill_bf16("sh_down", l, 0, m)
-            nvfp4_quantize(m, PER_TENSOR, out=Lw.shared_down)
+            register_layer(Lw, l, fill_bf16, fill_router, fill_bias)
         if self.lm is not None:
             full = torch.empty((self.V, H), dtype=torch.bfloat16, device=self.device)
             fill_bf16("lm_head", 0, 0, full)
             nvfp4_quantize(full, PER_TENSOR, out=self.lm)
             del full
-        del tmp
         self.make_workspace()
 
     def make_workspace(self):
@@ -131,3 +139,72 @@ class MoEDecodeStack:
         """Per layer, the number of distinct experts selected this step."""
         idx = self.topk_idx.view(self.L, -1).cpu()
         return [int(torch.unique(idx[l]).numel()) for l in range(self.L)]
+
+
+def graph_sizes_not_multiple(sizes, k):
+    """The CUDA-graph batch sizes that a speculative step with k drafts cannot
+    replay: every step verifies k + 1 positions per sequence, so only
+    multiples of k + 1 match a step's shape ("cudagraph_capture_sizes must be
+    multiples of k+1" in the W4A4 card's serving notes; a size that matches
+    none falls back to an uncaptured step)."""
+    return [s for s in sizes if s % (k + 1)]
+
+
+class SpecDecodeStep:
+    """One self-speculative decode step ("Let's optimize Nemotron 3.5
+    Lightning - a worklog", Step 5 and Step 6): the model's MTP head drafts k
+    tokens one pass at a time, then the main stack verifies k + 1 positions
+    in one pass.
+
+    Only the hot path is modelled. A draft pass is the drafter's own NVFP4
+    MoE layer (128 experts, the same kernels, its own weights) on one token,
+    then the lm_head over it; the verify pass is the main stack's MoE layers
+    on k + 1 tokens, then the lm_head over them. The attention, embedding and
+    sampling steps in between are not on this path: a draft pass here takes
+    the previous pass's output as its input.
+
+    main: a MoEDecodeStack with T = k + 1 (the verify pass); drafter: a
+    registered MoELayer of the main stack's shapes."""
+
+    def __init__(self, main: MoEDecodeStack, drafter: MoELayer, k: int):
+        if main.T != k + 1:
+            raise ValueError(f"the verify pass takes k + 1 = {k + 1} tokens, the stack has {main.T}")
+        if graph_sizes_not_multiple([main.T], k):
+            raise ValueError("verify batch is not a multiple of k + 1")
+        self.main, self.drafter, self.k = main, drafter, k
+        dev = main.device
+        H = main.H
+        self.hd = torch.zeros((k + 1, 1, H), dtype=torch.bfloat16, device=dev)  # draft pass inputs / outputs
+        self.d_idx = torch.zeros((k, 1, 1, main.k), dtype=torch.int32, device=dev)
+        self.d_w = torch.zeros((k, 1, 1, main.k), dtype=torch.float32, device=dev)
+        self.d_logits = (torch.zeros((k, 1, main.V), dtype=torch.float32, device=dev) if main.V else None)
+        self.d_layers = [drafter]
+        self.d_ws = make_stack_workspace(self.d_layers, 1, main.k, main.mode)
+        self.d_c = _stack_layers(self.d_layers)
+        self.d_lm_ws = make_lm_head_workspace(main.lm, 1) if main.lm is not None else None
+        self.graph = None
+
+    def step(self, stream=None):
+        m = self.main
+        for d in range(self.k):
+            moe_stack_forward(self.d_layers, self.hd[d], m.k, m.mode, hidden_out=self.hd[d + 1:d + 2],
+                              topk_idx=self.d_idx[d], topk_w=self.d_w[d], workspace=self.d_ws,
+                              rms_eps=m.rms_eps, stream=stream, c_layers=self.d_c)
+            if m.lm is not None:
+                lm_head_forward(m.lm, self.hd[d + 1], self.d_logits[d], workspace=self.d_lm_ws,
+                                rms_eps=m.rms_eps, stream=stream)
+        m.step(stream)
+
+    def capture(self):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.step()
+        torch.cuda.synchronize()
+        return self.graph
+

@@ -52,6 +52,13 @@ def step_bytes(T, uniques, E, H, I, S, k, V=None):
     return b
 
 
+def moe_fp4_flops(T, L, H, I, S, k):
+    """FP4 tensor-core flops of the expert GEMMs of L MoE layers (W4A4): the
+    routed experts' up and down for T k (token, choice) pairs and the shared
+    expert's for T tokens."""
+    return L * (2 * T * k * 2 * I * H + 2 * T * 2 * S * H)
+
+
 def step_flops(T, L, E, H, I, S, k, V=None):
     f = L * (2 * T * E * H + 2 * T * k * 2 * I * H + 2 * T * 2 * S * H)
     if V:

@@ -47,11 +47,12 @@ def test_full_lm_head_sampled_rows(nm, T):
     assert_close(got[:, rows], ref, "sampled logits")
 
 
-@pytest.mark.parametrize("T", [9, 64, 100])
+@pytest.mark.parametrize("T", [9, 64, 100, 300])
 @pytest.mark.parametrize("eps", [0.0, 1e-5])
 def test_small_lm_head_forward_gemm(nm, T, eps):
-    """lm_head_forward above 8 tokens (dense GEMM over 64-token tiles, ragged
-    last tile) against the oracle, with and without the final RMS norm."""
+    """lm_head_forward above 8 tokens (the tensor-core GEMM: N = tokens rounded
+    up to 16, up to 256 per launch; 300 tokens take two launches) against the
+    oracle, with and without the final RMS norm."""
     V, H = 1024, 2688
     tid = gen.tensor_id(gen.KIND_LM_HEAD, 2, V)
     master = gen.normal_bf16(V * H, 4, tid, gen.WEIGHT_SIGMA).reshape(V, H)

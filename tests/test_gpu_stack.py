@@ -116,3 +116,29 @@ def test_stack_rejects_bad_shapes(nm, small_stack):
     assert ei.value.status == 4
     torch.cuda.synchronize()
     assert nm.nvfp4_last_device_error() == 0
+
+
+def test_peer_wait_expiry_is_reported_and_recoverable(nm, small_stack):
+    """A wait that runs out (a 1 ns limit on the waits for other CTAs' tagged
+    words: no word is ever ready in time) ends the call early with
+    NVFP4_ERR_TIMEOUT and leaves the context usable: after the workspace is
+    re-initialised, the default limit gives the undisturbed result."""
+    layers, _ = small_stack
+    T, k, mode = 1, 4, nm.W4A4
+    hd = to_dev_bf16(gen.hidden_bf16(T, SMALL["H"], 5, layer=13))
+    ws = nm.make_stack_workspace(layers, T, k, mode)
+    ref, ridx, _ = nm.moe_stack_forward(layers, hd, k, mode, workspace=ws, rms_eps=1e-5)
+    torch.cuda.synchronize()
+    assert nm.nvfp4_last_device_error() == 0
+    try:
+        nm.nvfp4_set_peer_wait_limit(1)
+        nm.moe_stack_forward(layers, hd, k, mode, workspace=ws, rms_eps=1e-5)
+        torch.cuda.synchronize()
+        assert nm.nvfp4_last_device_error() == 6  # NVFP4_ERR_TIMEOUT
+    finally:
+        nm.nvfp4_set_peer_wait_limit(0)
+    nm.moe_expert_forward_workspace_init(ws)
+    out, idx, _ = nm.moe_stack_forward(layers, hd, k, mode, workspace=ws, rms_eps=1e-5)
+    torch.cuda.synchronize()
+    assert nm.nvfp4_last_device_error() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16)) and torch.equal(idx, ridx)
