@@ -427,6 +427,16 @@ nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidden, int32_t 
  */
 nvfp4_status nvfp4_fp4_mma_peak(int32_t n, int32_t chains, int32_t iters, double* tflops, cudaStream_t stream);
 
+/* Backend choice by batch size ([super-q] "Deployment": per-quantization GEMM
+ * backend selection at intermediate batch sizes): moe_expert_forward runs
+ * 1 .. t tokens on the decode GEMV kernels (weights decoded in registers,
+ * tokens as MMA columns) and more on the grouped tensor-core path (W4A4:
+ * tcgen05 block-scaled MMA; W4A16: the f16 grouped GEMM). t in 0 .. 4,
+ * default 4. Process-wide; moe_expert_forward_workspace_size follows it, so
+ * size workspaces after setting it (a smaller workspace is rejected with
+ * NVFP4_ERR_WORKSPACE). Returns NVFP4_ERR_INVALID_ARG for t outside 0 .. 4. */
+nvfp4_status nvfp4_set_decode_max_tokens(int32_t t);
+
 /* Sets, on the current device, the limit of the device waits of one CTA on
  * another CTA's progress (moe_stack_forward's polls of its tagged words):
  * `ns` nanoseconds, or the default 1 s when ns is 0. A wait that runs out

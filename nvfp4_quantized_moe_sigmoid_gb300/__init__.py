@@ -61,6 +61,12 @@ def nvfp4_last_device_error(stream=None) -> int:
     return _L.nvfp4_last_device_error(_stream(stream))
 
 
+def nvfp4_set_decode_max_tokens(t=4):
+    """moe_expert_forward runs up to t tokens (0..4) on the decode GEMV kernels,
+    more on the grouped path."""
+    _check(_L.nvfp4_set_decode_max_tokens(int(t)), "nvfp4_set_decode_max_tokens")
+
+
 def nvfp4_set_peer_wait_limit(ns=0):
     """Limit (ns) of the stack kernel's waits on other CTAs; 0 restores 1 s."""
     _check(_L.nvfp4_set_peer_wait_limit(int(ns)), "nvfp4_set_peer_wait_limit")

@@ -17,7 +17,7 @@ EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_siz
            "moe_stack_forward", "moe_stack_forward_workspace_size", "moe_permute",
            "lm_head_gemv", "lm_head_forward", "lm_head_forward_workspace_size",
            "nvfp4_colblock_layout", "nvfp4_status_string", "nvfp4_last_device_error",
-           "nvfp4_fp4_mma_peak", "nvfp4_set_peer_wait_limit"]
+           "nvfp4_fp4_mma_peak", "nvfp4_set_peer_wait_limit", "nvfp4_set_decode_max_tokens"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20  # NVFP4MOE_NOALLOC_SCRATCH_BYTES
 STACK_MAX_LAYERS = 32  # NVFP4MOE_STACK_MAX_LAYERS
@@ -97,5 +97,7 @@ def load(path: str = LIB_PATH):
     L.nvfp4_fp4_mma_peak.restype = ctypes.c_int
     L.nvfp4_set_peer_wait_limit.argtypes = [ctypes.c_uint64]
     L.nvfp4_set_peer_wait_limit.restype = ctypes.c_int
+    L.nvfp4_set_decode_max_tokens.argtypes = [I32]
+    L.nvfp4_set_decode_max_tokens.restype = ctypes.c_int
     _lib = L
     return L

@@ -8,6 +8,7 @@
 #endif
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -153,8 +154,12 @@ nvfp4_status grouped_forward(const moe_layer_weights* w, const void* hidden, con
                              const float* topk_w, int T, int k, bool w4a4, float rms_eps, const void* residual,
                              void* out, uint8_t* ws, cudaStream_t stream);
 
+// The largest token count moe_expert_forward runs on the decode GEMV kernels
+// (nvfp4_set_decode_max_tokens); more tokens take the grouped path.
+std::atomic<int> g_decode_max_t{kDecodeMaxT};
+
 bool decode_path(const moe_layer_weights* w, int T, int k) {
-    return T >= 1 && T <= kDecodeMaxT && k <= kDecodeMaxK && w->num_experts <= 256;
+    return T >= 1 && T <= g_decode_max_t.load(std::memory_order_relaxed) && k <= kDecodeMaxK && w->num_experts <= 256;
 }
 
 nvfp4_status check_matrix(const nvfp4_matrix& m, int64_t n, int64_t k) {
@@ -195,6 +200,12 @@ const char* nvfp4_status_string(nvfp4_status s) {
         case NVFP4_ERR_TIMEOUT: return "device wait timed out";
     }
     return "unknown status";
+}
+
+nvfp4_status nvfp4_set_decode_max_tokens(int32_t t) {
+    if (t < 0 || t > kDecodeMaxT) return NVFP4_ERR_INVALID_ARG;
+    g_decode_max_t.store(t, std::memory_order_relaxed);
+    return NVFP4_OK;
 }
 
 nvfp4_status nvfp4_set_peer_wait_limit(uint64_t ns) {

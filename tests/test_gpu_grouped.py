@@ -137,3 +137,23 @@ def test_grouped_workspace_too_small(nm, small_layer):
     with pytest.raises(nm.NVFP4Error) as ei:
         nm.moe_expert_forward(L, hd, idx, w, nm.W4A4, workspace=ws)
     assert ei.value.status == 4
+
+
+@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("w4a4", [False, True])
+def test_grouped_path_at_decode_sizes(nm, T, w4a4):
+    """With nvfp4_set_decode_max_tokens(0) even 1..4 tokens take the grouped
+    path (the backend choice the concurrency sweep measures); it matches the
+    oracle like the decode kernels do."""
+    from tests.test_gpu_moe import SMALL, run_layer
+    from tests.gpu_fixtures import device_layer
+    from oracle.workload import OracleLayer
+    c = SMALL
+    L = device_layer(nm, 7, 2, c["E"], c["H"], c["I"], c["S"], (-0.1, 0.1))
+    OL = OracleLayer(7, 2, c["H"], c["I"], c["S"], c["E"], (-0.1, 0.1))
+    h = gen.hidden_bf16(T, c["H"], 7, layer=2, rho=0.5)
+    try:
+        nm.nvfp4_set_decode_max_tokens(0)
+        run_layer(nm, L, OL, h, 4, w4a4, True)
+    finally:
+        nm.nvfp4_set_decode_max_tokens(4)
