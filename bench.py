@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="time only the chosen config (by default the headline run also times configs 0, 2, 3, 4)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="one MoE layer across token counts on each path (decode GEMV, stack, grouped tcgen05): "
+                         "prints the crossover table instead of the JSON line")
     ap.add_argument("--trace", action="store_true",
                     help="per-phase timeline of the stack kernel (1-4 token configs) from the phase-trace build "
                          "of the library; prints a table instead of the JSON line")
@@ -550,10 +553,10 @@ def run_ours(args, ws, rank, local):
 
 
 # ------------------------------------------------------------------ phase trace
-TRACE_EVENTS = ["layer start", "h_l final (all CTAs)", "router logits posted", "all logits posted",
-                "plan written", "routed up tiles done", "shared down + routed operands", "routed down units done",
-                "all partials read",
-                "rows of h_l+1 written", "producer: first item", "producer: last item"]
+TRACE_EVENTS = ["layer start", "h_l read (tagged words)", "router logits posted", "producer's plan free",
+                "plan written", "up tiles done", "row amax final, down operands", "down units done",
+                "all partials read", "rows of h_l+1 written", "producer: first item", "producer: last item",
+                "producer: plan seen"]
 
 
 def run_trace(args, local):
@@ -629,9 +632,85 @@ def run_trace(args, local):
         print(f"layer period: median {np.median(period):.2f} us, min {period.min():.2f}, max {period.max():.2f}")
 
 
+# ------------------------------------------------------------------ concurrency sweep
+SWEEP_T = [1, 2, 3, 4, 5, 8, 16, 32, 64, 128, 256, 512, 1024]
+
+
+def run_sweep(args, local):
+    """One W4A4 MoE layer at the pages' shapes (layer 0 of the seed-0
+    weights, router bias U(-0.1, 0.1)) across token counts, on every path the
+    library has for it: the decode GEMV kernels and the one-layer stack kernel
+    (up to 4 tokens) and the grouped tensor-core path (any count; forced at
+    1..4 with nvfp4_set_decode_max_tokens(0)). Each number is one route +
+    experts + combine pass timed in a graph of 5 back-to-back passes. Prints
+    a table: the measured crossover of the backend choice."""
+    import torch
+
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_quantized_moe_sigmoid_gb300 as nm
+    from nvfp4_quantized_moe_sigmoid_gb300 import roofline as rf
+    from nvfp4_quantized_moe_sigmoid_gb300.model import register_layer
+    from gen import configs, fill
+
+    c = configs.shape(1)
+    E, H, I, S, K = c["E"], c["H"], c["I"], c["S"], c["K"]
+    L0 = nm.MoELayer(E, H, I, S)
+    register_layer(L0, 0, *fill.fillers(c["seed"], c["bias"]))
+    torch.cuda.synchronize()
+    peak, _ = measured_peaks()
+    rows = []
+    for T in SWEEP_T:
+        h = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        fill.hidden(h, c["seed"], layer=configs.HIDDEN_LAYER)
+        out = torch.empty_like(h)
+        idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        res = {}
+        for path in ("decode", "stack", "grouped"):
+            if path != "grouped" and T > 4:
+                continue
+            nm.nvfp4_set_decode_max_tokens(4 if path == "decode" else 0)
+            if path == "stack":
+                ws_ = nm.make_stack_workspace([L0], T, K, nm.W4A4)
+                hout = torch.empty((1, T, H), dtype=torch.bfloat16, device="cuda")
+                sidx = torch.empty((1, T, K), dtype=torch.int32, device="cuda")
+                sw = torch.empty((1, T, K), dtype=torch.float32, device="cuda")
+                fn = (lambda: nm.moe_stack_forward([L0], h, K, nm.W4A4, hidden_out=hout, topk_idx=sidx,
+                                                   topk_w=sw, workspace=ws_, rms_eps=c["rms_eps"]))
+            else:
+                ws_ = nm.make_workspace(L0, T, K, nm.W4A4)
+                fn = (lambda: (nm.moe_route_topk(h, L0.router_w, L0.router_b, K, idx, w, rms_eps=c["rms_eps"]),
+                               nm.moe_expert_forward(L0, h, idx, w, nm.W4A4, residual=h, out=out, workspace=ws_,
+                                                     rms_eps=c["rms_eps"])))
+            g = graph_of(fn, 5)
+            ms = time_graph(g, 4) / 5
+            del g
+            assert nm.nvfp4_last_device_error() == 0
+            res[path] = ms * 1e3
+        nm.nvfp4_set_decode_max_tokens(4)
+        u = int(torch.unique(idx if "decode" in res or "grouped" in res else sidx).numel())
+        b = rf.layer_bytes(T, u, E, H, I, S, K)
+        rows.append((T, u, res, b))
+    print("concurrency sweep: one W4A4 MoE layer (hidden %d, %d experts of %d, top-%d, shared %d), "
+          "us per layer (us per token)" % (H, E, I, K, S))
+    print("| T | unique experts | decode GEMV | stack (1 layer) | grouped tcgen05 | best | best GB/s (frac of %.0f) |" % peak)
+    print("|---|---|---|---|---|---|---|")
+    for T, u, res, b in rows:
+        cell = lambda p: ("%.1f (%.2f)" % (res[p], res[p] / T)) if p in res else "-"
+        best = min(res, key=res.get)
+        gbs = b / (res[best] * 1e-6) / 1e9
+        print("| %d | %d | %s | %s | %s | %s | %.0f (%.2f) |" % (T, u, cell("decode"), cell("stack"), cell("grouped"),
+                                                          best, gbs, gbs / peak))
+
+
 def main():
     args = parse()
     ws, rank, local = dist_init()
+    if args.sweep:
+        run_sweep(args, local)
+        return
     if args.trace:
         run_trace(args, local)
         return

@@ -224,17 +224,18 @@ __device__ __noinline__ bool mbar_wait_abortable(uint64_t* b, uint32_t parity, v
 // Without the flag the trace points compile to nothing.
 enum StackTraceEvent : int {
     kTrStart = 0,    // layer begins (consumer)
-    kTrHReady,       // every CTA's rows of h_l are final
+    kTrHReady,       // thread 0 has read its elements of h_l (tagged words)
     kTrRouter,       // input, norm and this CTA's router logits posted
-    kTrLogits,       // all E logits posted
+    kTrLogits,       // the producer has released the previous layer's plan
     kTrPlan,         // top-k and the plan of unique experts written
     kTrUp,           // this CTA's up tiles done
     kTrAmax,         // (W4A4) the expert's row amax final; down operands ready
     kTrDown,         // this CTA's down units done, partial posted
-    kTrParts,        // every CTA's partial posted
+    kTrParts,        // every CTA's partial of this CTA's rows read
     kTrReduce,       // this CTA's rows of h_{l+1} written
     kTrProdFirst,    // producer: first item of the layer issued
     kTrProdLast,     // producer: last item of the layer issued
+    kTrProdPlan,     // producer: the plan of the layer seen
     kTrEvents = 16
 };
 constexpr int kTraceMaxCtas = 256;
@@ -270,10 +271,6 @@ __device__ unsigned long long g_stack_trace[kTraceMaxCtas * kStackMaxLayers * kT
 // an item it waits until the item that last used the slot, and every older
 // item whose bytes the new one would overwrite, have been released.
 constexpr int kGroups = 4;
-// The up tiles of a step are split over all consumer warps by 128-k chunks
-// (st_up_tiles); one warp's share spans at most 1 + ceil(n / 12) items of the
-// step, n <= kMaxUnits.
-constexpr int kUpMaxTouch = 1 + (kMaxUnits + kConsumerWarps - 1) / kConsumerWarps;
 constexpr int kGroupWarps = kConsumerWarps / kGroups;
 constexpr int kSlots = 16;
 static_assert(kConsumerWarps % kGroups == 0 && kSlots % kGroups == 0, "ring groups");
@@ -285,9 +282,9 @@ struct BRing {
     uint32_t off[kSlots];  // byte offset of the slot's current item
     int vs[kSlots];        // its virtual start (producer side)
     int uses[kSlots];      // fills of the slot (producer side)
-    // partial up tiles: per warp, per item it touches (in order), the 16
-    // lanes that hold MMA columns 0..3 (lane = 4 g + q, q < 2; index 2 g + q)
-    float4 xr[kConsumerWarps][kUpMaxTouch][16];
+    // partial tiles handed from ranks 1.. of a group to its rank 0, double
+    // buffered by the group's item parity; warp w >= kGroups uses w - kGroups
+    float4 xred[kConsumerWarps - kGroups][2][32];
 };
 
 constexpr int kNormMaxChunks = 64;  // H <= 16384
@@ -339,6 +336,55 @@ struct StackCta {
 
 __device__ __forceinline__ bool cta_abort(StackCta& c) { return *static_cast<volatile int*>(&c.abort_s) != 0; }
 __device__ __forceinline__ void set_cta_abort(StackCta& c) { *static_cast<volatile int*>(&c.abort_s) = 1; }
+
+// Consumers: item li by its warp group (see the ring above); the group's
+// rank-0 warp gets lead = 1 and the finished 16 x 8 tile, ok = 0 in every
+// warp of the group if any of them timed out.
+__device__ __noinline__ TileOut bgroup_tile_core(StackCta* cp, int li, int K, const __half* bcol) {
+    BRing& r = cp->br;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = warp % kGroups, rank = warp / kGroups;
+    const int s = li % kSlots;
+    const bool waited = mbar_wait_bounded(&r.full[s], static_cast<uint32_t>((li / kSlots) & 1));
+    const bool got = __all_sync(0xffffffffu, waited);
+    if (!got && lane == 0) set_dev_error(kErrWaitFull);
+    const int nc = (K + 127) >> 7;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (got) {
+        const uint8_t* st = cp->ring_base + r.off[s];
+        tile_mma_16x8(st, st + 8 * K, K, bcol, nc * rank / kGroupWarps, nc * (rank + 1) / kGroupWarps, acc);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cnt(&r.empty[s], kGroups);
+    TileOut o;
+    o.acc = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    const int u = (li / kGroups) & 1;
+    if (rank) r.xred[warp - kGroups][u][lane] = o.acc;
+    o.ok = group_bar_and(g, kGroupWarps, got);
+    o.lead = 0;
+    if (rank || !o.ok) return o;
+#pragma unroll
+    for (int p = 1; p < kGroupWarps; ++p) {
+        const float4 x = r.xred[g + (p - 1) * kGroups][u][lane];
+        o.acc.x += x.x;
+        o.acc.y += x.y;
+        o.acc.z += x.z;
+        o.acc.w += x.w;
+    }
+    o.lead = 1;
+    return o;
+}
+
+__device__ __forceinline__ bool bgroup_tile(StackCta& c, int li, int K, const __half* bcol, float (&acc)[4],
+                                            bool& ok) {
+    const TileOut o = bgroup_tile_core(&c, li, K, bcol);
+    acc[0] = o.acc.x;
+    acc[1] = o.acc.y;
+    acc[2] = o.acc.z;
+    acc[3] = o.acc.w;
+    ok = o.ok != 0;
+    return o.lead != 0;
+}
 
 __device__ __forceinline__ int* abort_flag(const StackArgs& a) { return a.ws.cnt + kCtlAbort; }
 __device__ __forceinline__ int* epoch_word(const StackArgs& a) { return a.ws.cnt + kCtlEpoch; }
@@ -899,88 +945,22 @@ __device__ __forceinline__ UnitRange stack_units(int b, int G, int cs, int RS, i
 // routed slot). relu^2 -> bf16 values of each unit (shared memory), their
 // amax per (expert, token) (W4A4; counted once per CTA in step 6). Returns
 // false on a timeout.
-// The C = n nch 128-k chunks of the step's up tiles (items base .. base +
-// n - 1, nch chunks each) go evenly to the consumer warps: warp w computes
-// chunks [C w / 12, C (w + 1) / 12), which may span several items, and keeps
-// one partial 16 x 8 tile per item it touches. Every warp waits for the items
-// up to its last one in order (a parity wait must never run ahead of the
-// slot's previous use), and releases each item it touched; the first warp of
-// an item releases it for the warps that do not touch it. After a barrier,
-// the first warp of each item adds its partials in warp order.
-__device__ __forceinline__ int up_chunk_warp(int x, int C) {  // the warp whose share holds chunk x
-    int w = static_cast<int>((static_cast<long long>(x) * kConsumerWarps) / C);
-    while (w > 0 && C * w / kConsumerWarps > x) --w;
-    while (w + 1 < kConsumerWarps && C * (w + 1) / kConsumerWarps <= x) ++w;
-    return w;
-}
-// Whether warp w's share of C chunks is empty (only when C < 12).
-__device__ __forceinline__ bool up_share_empty(int w, int C) {
-    return C * (w + 1) / kConsumerWarps == C * w / kConsumerWarps;
-}
-
-// Up tiles [base, base + n): the CTA's units (of expert ex: -1 shared, else
-// routed slot). relu^2 -> bf16 values of each unit (shared memory), their
-// amax per (expert, token) (W4A4; counted once per CTA in step 6). Returns
-// false on a timeout.
 template <bool W4A4>
 __device__ __noinline__ bool st_up_tiles(const StackArgs& a, StackCta& c, int l, int base, int n, int ex) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     const int T = a.T, H = a.H;
-    BRing& r = c.br;
     const bool routed = ex >= 0;
     const int u = routed ? ex : 0;
     const __half* bcol = g < T ? c.xq + (size_t)g * H : nullptr;
-    const int nch = (H + 127) >> 7, C = n * nch;
-    const int cb = C * warp / kConsumerWarps, ce = C * (warp + 1) / kConsumerWarps;
-    bool ok = true;
-    if (ce > cb) {
-        const int i0 = cb / nch, i1 = (ce - 1) / nch;
+    const int end = base + n;
 #pragma unroll 1
-        for (int i = 0; i <= i1; ++i) {
-            const int li = base + i, s = li % kSlots;
-            const bool waited = mbar_wait_bounded(&r.full[s], static_cast<uint32_t>((li / kSlots) & 1));
-            if (!__all_sync(0xffffffffu, waited)) {
-                if (lane == 0) set_dev_error(kErrWaitFull);
-                ok = false;
-                break;
-            }
-            if (i < i0) continue;  // waited for in order only
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const uint8_t* st = c.ring_base + r.off[s];
-            tile_mma_16x8(st, st + 8 * H, H, bcol, max(cb, i * nch) - i * nch, min(ce, (i + 1) * nch) - i * nch,
-                          acc);
-            if (q < 2) r.xr[warp][i - i0][2 * g + q] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            __syncwarp();
-            if (lane == 0) {
-                // the first warp of the item also arrives for every warp that does not touch it
-                const int wlo = up_chunk_warp(i * nch, C), whi = up_chunk_warp((i + 1) * nch - 1, C);
-                int touching = 0;
-                for (int ww = wlo; ww <= whi; ++ww) touching += up_share_empty(ww, C) ? 0 : 1;
-                mbar_arrive_cnt(&r.empty[s], warp == wlo ? kConsumerWarps - (touching - 1) : 1u);
-            }
-        }
-    }
-    if (consumer_bar_or(!ok || cta_abort(c))) return false;
-    // the epilogue of every item this warp leads (it holds the item's first chunk)
-#pragma unroll 1
-    for (int i = 0; i < n; ++i) {
-        const int wlo = up_chunk_warp(i * nch, C);
-        if (wlo != warp) continue;
-        const int whi = up_chunk_warp((i + 1) * nch - 1, C);
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (q < 2) {
-#pragma unroll 1
-            for (int ww = wlo; ww <= whi; ++ww) {
-                if (up_share_empty(ww, C)) continue;
-                const float4 x = r.xr[ww][i - (C * ww / kConsumerWarps) / nch][2 * g + q];
-                acc[0] += x.x;
-                acc[1] += x.y;
-                acc[2] += x.z;
-                acc[3] += x.w;
-            }
-        }
-        const int li = base + i;
+    for (int li = first_item(base, warp % kGroups, kGroups); li < end; li += kGroups) {
+        float acc[4];
+        bool ok;
+        const bool lead = bgroup_tile(c, li, H, bcol, acc, ok);
+        if (!ok) return false;
+        if (!lead) continue;
         const float gw = routed ? c.up_g[u] : c.shu_g;
         float m[2] = {0.0f, 0.0f};
 #pragma unroll
@@ -1303,6 +1283,7 @@ __device__ __noinline__ void st_producer(const StackArgs& a, StackCta& c) {
                 alive = false;
                 break;
             }
+            STACK_TRACE(ph == 1, b, l, kTrProdPlan);
             if ((ph == 0) != sh) continue;
             // the units' up tiles (16 rows of W_up: codes, then scales, from
             // two arrays), then their down column blocks (codes, then scales,
