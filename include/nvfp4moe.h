@@ -449,6 +449,56 @@ nvfp4_status nvfp4_set_decode_max_tokens(int32_t t);
  * the device copy fails. */
 nvfp4_status nvfp4_set_peer_wait_limit(uint64_t ns);
 
+/* Inspection of the activation rows a call leaves in its workspace (no
+ * operation of the pages: it lets a test compare the NVFP4 activation rows
+ * the kernels build in flight, [worklog] Step 3 "W4A4", with a reference
+ * quantiser bit for bit). After moe_expert_forward (call 0) or
+ * moe_layer_forward (call 1) with the same w, T, k and mode, `view` gets the
+ * place of region `region` in the workspace:
+ *   NVFP4_WS_X        the layer input rows as the up GEMMs take them [T][H]
+ *                     (after the RMS norm when rms_eps > 0)
+ *   NVFP4_WS_ACT      the routed intermediate relu(up)^2 in bf16 [T*k][I]
+ *   NVFP4_WS_ACT_Q    the same rows quantised, as the down GEMMs take them
+ *   NVFP4_WS_SH_ACT   the shared expert's intermediate in bf16 [T][S]
+ *   NVFP4_WS_SH_ACT_Q the same rows quantised
+ * format NVFP4_WS_BF16: bf16 values. NVFP4_WS_CODES: E2M1 codes [rows][cols/2]
+ * (low nibble = even element) with E4M3 scales at scales_offset, scales_pitch
+ * bytes per row, and per-row FP32 globals at global_offset (W4A4).
+ * NVFP4_WS_F16_DEQUANT: per element the f16 value E2M1 code x E4M3 scale (exact),
+ * per-row globals at global_offset. Rows are in (token, choice) order, or
+ * in the permuted position order (grouped by expert) when position_order = 1;
+ * row p of ACT and of ACT_Q are the same row either way.
+ * Regions a path keeps only in shared memory (the decode GEMV path's
+ * quantised rows; every quantised row of a W4A16 call; the W4A16 grouped
+ * path) give NVFP4_ERR_UNSUPPORTED_SHAPE. Host only; reads no device memory.
+ * Returns NVFP4_ERR_INVALID_ARG for a null w or view or an unknown call,
+ * mode or region. */
+typedef enum {
+    NVFP4_WS_X = 0,
+    NVFP4_WS_ACT = 1,
+    NVFP4_WS_ACT_Q = 2,
+    NVFP4_WS_SH_ACT = 3,
+    NVFP4_WS_SH_ACT_Q = 4
+} nvfp4_ws_region;
+
+typedef enum { NVFP4_WS_BF16 = 0, NVFP4_WS_CODES = 1, NVFP4_WS_F16_DEQUANT = 2 } nvfp4_ws_format;
+
+typedef struct {
+    uint64_t offset;         /* byte offset of row 0 */
+    int64_t rows, cols;      /* elements */
+    int64_t pitch;           /* bytes between rows */
+    uint64_t scales_offset;  /* NVFP4_WS_CODES: E4M3 scales of row 0 */
+    int64_t scales_pitch;    /* bytes between scale rows */
+    uint64_t global_offset;  /* FP32 [rows] per-row globals when has_global */
+    int32_t format;          /* nvfp4_ws_format */
+    int32_t has_global;
+    int32_t position_order;
+    int32_t reserved;
+} nvfp4_ws_view;
+
+nvfp4_status nvfp4_workspace_view(int32_t call, const moe_layer_weights* w, int32_t T, int32_t k,
+                                  nvfp4_act_mode mode, int32_t region, nvfp4_ws_view* view);
+
 /* Human-readable name of a status code (static string). */
 const char* nvfp4_status_string(nvfp4_status status);
 

@@ -19,7 +19,7 @@ __all__ = ["NVFP4Matrix", "MoELayer", "NVFP4Error", "nvfp4_quantize", "moe_route
            "moe_layer_forward_workspace_size", "moe_stack_forward", "moe_stack_forward_workspace_size",
            "make_stack_workspace", "nvfp4_colblock_layout", "moe_permute", "lm_head_gemv", "lm_head_forward",
            "make_lm_head_workspace",
-           "nvfp4_status_string", "nvfp4_last_device_error",
+           "nvfp4_status_string", "nvfp4_last_device_error", "nvfp4_workspace_view",
            "W4A16", "W4A4", "PER_TENSOR", "PER_ROW", "GIVEN", "lib"]
 
 W4A16, W4A4 = 0, 1
@@ -190,6 +190,21 @@ def moe_expert_forward_workspace_size(layer: MoELayer, T, k, mode=W4A4) -> int:
 def moe_expert_forward_workspace_init(workspace, stream=None):
     _check(_L.moe_expert_forward_workspace_init(_ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_expert_forward_workspace_init")
+
+
+WS_X, WS_ACT, WS_ACT_Q, WS_SH_ACT, WS_SH_ACT_Q = 0, 1, 2, 3, 4
+WS_BF16, WS_CODES, WS_F16_DEQUANT = 0, 1, 2
+CALL_EXPERT_FORWARD, CALL_LAYER_FORWARD = 0, 1
+
+
+def nvfp4_workspace_view(call, layer: MoELayer, T, k, mode, region) -> dict:
+    """Where region `region` (WS_*) of a moe_expert_forward (call 0) or
+    moe_layer_forward (call 1) workspace lies: the fields of nvfp4_ws_view."""
+    w = layer.c()
+    v = _abi.WsView()
+    _check(_L.nvfp4_workspace_view(call, ctypes.byref(w), T, k, mode, region, ctypes.byref(v)),
+           "nvfp4_workspace_view")
+    return {f: getattr(v, f) for f, _ in _abi.WsView._fields_}
 
 
 def make_workspace(layer: MoELayer, T, k, mode=W4A4, stream=None):

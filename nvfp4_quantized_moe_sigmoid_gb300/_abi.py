@@ -17,7 +17,8 @@ EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_siz
            "moe_stack_forward", "moe_stack_forward_workspace_size", "moe_permute",
            "lm_head_gemv", "lm_head_forward", "lm_head_forward_workspace_size",
            "nvfp4_colblock_layout", "nvfp4_status_string", "nvfp4_last_device_error",
-           "nvfp4_fp4_mma_peak", "nvfp4_set_peer_wait_limit", "nvfp4_set_decode_max_tokens"]
+           "nvfp4_fp4_mma_peak", "nvfp4_set_peer_wait_limit", "nvfp4_set_decode_max_tokens",
+           "nvfp4_workspace_view"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20  # NVFP4MOE_NOALLOC_SCRATCH_BYTES
 STACK_MAX_LAYERS = 32  # NVFP4MOE_STACK_MAX_LAYERS
@@ -36,6 +37,12 @@ class MoeLayerWeights(ctypes.Structure):
                 ("up_codes", P), ("up_scales", P), ("up_global", P),
                 ("down_codes", P), ("down_scales", P), ("down_global", P),
                 ("shared_up", NVFP4Matrix), ("shared_down", NVFP4Matrix)]
+
+
+class WsView(ctypes.Structure):
+    _fields_ = [("offset", ctypes.c_uint64), ("rows", I64), ("cols", I64), ("pitch", I64),
+                ("scales_offset", ctypes.c_uint64), ("scales_pitch", I64), ("global_offset", ctypes.c_uint64),
+                ("format", I32), ("has_global", I32), ("position_order", I32), ("reserved", I32)]
 
 
 class MoeStackLayer(ctypes.Structure):
@@ -99,5 +106,8 @@ def load(path: str = LIB_PATH):
     L.nvfp4_set_peer_wait_limit.restype = ctypes.c_int
     L.nvfp4_set_decode_max_tokens.argtypes = [I32]
     L.nvfp4_set_decode_max_tokens.restype = ctypes.c_int
+    L.nvfp4_workspace_view.argtypes = [I32, ctypes.POINTER(MoeLayerWeights), I32, I32, ctypes.c_int, I32,
+                                       ctypes.POINTER(WsView)]
+    L.nvfp4_workspace_view.restype = ctypes.c_int
     _lib = L
     return L

@@ -22,8 +22,10 @@
 // Warp roles (one CTA per SM, persistent over the 128-row tiles):
 //   warp 0      producer (TMA, cp.async of the scales)
 //   warp 1      tensor memory allocation; lane 0 issues the MMAs
-//   warps 2-5   decoders: thread r decodes row r of each stage's tile
-//   warps 6-9   epilogue (lane quarter = warp % 4), accumulator double-
+//   warps 2-9   decoders: threads 2r and 2r + 1 decode the two 32-k halves
+//               of row r of each stage's tile (two warps per scheduler, so
+//               that one warp's conversion latency hides behind the other's)
+//   warps 10-13 epilogue (lane quarter = warp % 4), accumulator double-
 //               buffered in tensor memory so that a tile's epilogue overlaps
 //               the next tile's MMAs
 // Every wait is bounded (1 s); a role that gives up flags the error word and
@@ -34,7 +36,8 @@
 
 namespace nvfp4moe {
 
-constexpr int kLmTcThreads = 320;
+constexpr int kLmTcThreads = 448;
+constexpr int kLmTcDecWarps = 8;
 constexpr int kLmTcRows = 128;  // weight rows per tile (MMA M)
 constexpr int kLmTcK = 64;      // k per stage: one 128-byte row of f16
 constexpr int kLmTcStages = 4;
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < kLmTcStages; ++s) {
             mbar_init(&full[s], 33);  // the producer's expect_tx + one cp.async arrival per lane
-            mbar_init(&decoded[s], 4);
+            mbar_init(&decoded[s], kLmTcDecWarps);
             mbar_init(&empty[s], 1);
         }
         for (int d = 0; d < 2; ++d) {
@@ -185,9 +188,9 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
             if (!mbar_wait_bounded(&drain, 0)) set_dev_error(kErrWaitDrain);
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ---- decoders: thread r = row r of every stage's tile
-        const int r = threadIdx.x - 64;
+    } else if (warp < 2 + kLmTcDecWarps) {
+        // ---- decoders: thread d = half d % 2 of row d / 2 of every stage's tile
+        const int d = threadIdx.x - 64, r = d >> 1, hf = d & 1;
         int g = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
@@ -200,17 +203,17 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
                     break;
                 }
                 uint8_t* const base = smem + (size_t)s * stage;
-                const uint8_t* raw = base + kLmTcA + N * 128 + 32 * r;
-                const uint4 c0 = *reinterpret_cast<const uint4*>(raw), c1 = *reinterpret_cast<const uint4*>(raw + 16);
-                const uint32_t sw = *reinterpret_cast<const uint32_t*>(base + kLmTcA + N * 128 + kLmTcRaw + 4 * r);
-                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                const uint4 c0 = *reinterpret_cast<const uint4*>(base + kLmTcA + N * 128 + 16 * d);
+                const uint32_t sw = *reinterpret_cast<const uint16_t*>(base + kLmTcA + N * 128 + kLmTcRaw + 4 * r + 2 * hf);
+                const uint32_t cw[4] = {c0.x, c0.y, c0.z, c0.w};
                 uint8_t* const arow = base + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {  // chunk c: k = 8c .. 8c + 7, scale block c / 2
-                    const uint32_t s2 = e4m3x2_to_f16x2((sw >> (8 * (c >> 1))) & 0xFFu);
+                for (int i = 0; i < 4; ++i) {  // chunk c = 4 hf + i: k = 8c .. 8c + 7, scale block c / 2
+                    const int c = 4 * hf + i;
+                    const uint32_t s2 = e4m3x2_to_f16x2((sw >> (8 * (i >> 1))) & 0xFFu);
                     const uint32_t sv = bcast_lo(s2);
                     uint32_t f[4];
-                    e2m1x8_to_f16x8(cw[c], f);
+                    e2m1x8_to_f16x8(cw[i], f);
                     *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) =
                         make_uint4(hmul2(f[0], sv), hmul2(f[1], sv), hmul2(f[2], sv), hmul2(f[3], sv));
                 }

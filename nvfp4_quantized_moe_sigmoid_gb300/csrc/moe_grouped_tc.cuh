@@ -208,15 +208,25 @@ struct TcItem {
 // them in order.
 __device__ __forceinline__ int tc_chains(int ng, int nks) { return min(min(4 / ng, 4), nks); }
 
-__device__ __forceinline__ int tc_seg_items(const TcSeg& s) {
+// The position ranges and chunk prefixes of both segments, copied to shared
+// memory at the start: every role looks an item up at every item start (a
+// binary search of dependent reads), which from global memory would stall
+// each role for several round trips per item.
+constexpr int kTcMaxExperts = 256;
+struct TcTab {
+    int off[2][kTcMaxExperts + 1];
+    int chk[2][kTcMaxExperts + 1];
+};
+
+__device__ __forceinline__ int tc_seg_items(const TcSeg& s, const int* chk) {
     const int MT = (s.M + kTcRows - 1) / kTcRows;
-    const int nch = s.offsets ? __ldg(s.chunks + s.nexp) : (s.npos + kTcPos - 1) / kTcPos;
+    const int nch = s.offsets ? chk[s.nexp] : (s.npos + kTcPos - 1) / kTcPos;
     return nch * MT;
 }
 
 // Item i: m-major inside a chunk of positions, so that consecutive items (on
 // neighbouring CTAs at about the same time) share their B rows in L2.
-__device__ __forceinline__ TcItem tc_item(const TcSeg* segs, int i, int items0) {
+__device__ __forceinline__ TcItem tc_item(const TcSeg* segs, const TcTab& tab, int i, int items0) {
     TcItem it;
     it.seg = i < items0 ? 0 : 1;
     if (it.seg) i -= items0;
@@ -225,15 +235,17 @@ __device__ __forceinline__ TcItem tc_item(const TcSeg* segs, int i, int items0) 
     const int ch = i / MT;
     it.mt = i - ch * MT;
     if (s.offsets) {
+        const int* chunks = tab.chk[it.seg];
+        const int* offsets = tab.off[it.seg];
         int lo = 0, hi = s.nexp;  // chunks[lo] <= ch < chunks[hi]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (__ldg(s.chunks + mid) <= ch) lo = mid;
+            if (chunks[mid] <= ch) lo = mid;
             else hi = mid;
         }
         it.e = lo;
-        it.row0 = __ldg(s.offsets + lo) + (ch - __ldg(s.chunks + lo)) * kTcPos;
-        it.n = min(kTcPos, __ldg(s.offsets + lo + 1) - it.row0);
+        it.row0 = offsets[lo] + (ch - chunks[lo]) * kTcPos;
+        it.n = min(kTcPos, offsets[lo + 1] - it.row0);
     } else {
         it.e = 0;
         it.row0 = ch * kTcPos;
@@ -261,6 +273,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
     static_assert(sizeof(TcSeg) % 8 == 0, "TcSeg copy");
     for (int i = threadIdx.x; i < (int)(2 * sizeof(TcSeg) / 8); i += blockDim.x)
         reinterpret_cast<uint64_t*>(segs)[i] = reinterpret_cast<const uint64_t*>(a.seg)[i];
+    __shared__ TcTab tab;
+    for (int sg = 0; sg < a.nseg; ++sg) {
+        const TcSeg& s = a.seg[sg];
+        if (!s.offsets) continue;
+        for (int i = threadIdx.x; i <= s.nexp; i += blockDim.x) {
+            tab.off[sg][i] = __ldg(s.offsets + i);
+            tab.chk[sg][i] = __ldg(s.chunks + i);
+        }
+    }
     __shared__ __align__(8) uint64_t dfull[2], dempty[2], drain;
     __shared__ __align__(8) uint64_t scfull[2], scempty[2];  // per-item weight scale blocks
     __shared__ uint32_t tmem_s;
@@ -288,8 +309,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
     tc_fence_after();
     const uint32_t tmem = tmem_s;
     volatile int* ab = &abort_s;
-    const int items0 = tc_seg_items(segs[0]);
-    const int total = items0 + (a.nseg > 1 ? tc_seg_items(segs[1]) : 0);
+    const int items0 = tc_seg_items(segs[0], tab.chk[0]);
+    const int total = items0 + (a.nseg > 1 ? tc_seg_items(segs[1], tab.chk[1]) : 0);
 
     if (warp == 0) {
         // ---- producer
@@ -308,7 +329,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
         __syncwarp();
         bool ok = true;
         for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
-            const TcItem it = tc_item(segs, i, items0);
+            const TcItem it = tc_item(segs, tab, i, items0);
             const TcSeg& s = segs[it.seg];
             const int nstage = ((s.K >> 6) + 3) >> 2, ng = (it.n + 31) >> 5;
             const int arow0 = it.e * s.M + it.mt * kTcRows;
@@ -388,7 +409,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
             int g = 0, n_it = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
-                const TcItem it = tc_item(segs, i, items0);
+                const TcItem it = tc_item(segs, tab, i, items0);
                 const TcSeg& s = segs[it.seg];
                 const int nks = s.K >> 6, nstage = (nks + 3) >> 2, ng = (it.n + 31) >> 5;
                 const int db = n_it & 1;
@@ -431,7 +452,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
         int g = 0, n_it = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
-            const TcItem it = tc_item(segs, i, items0);
+            const TcItem it = tc_item(segs, tab, i, items0);
             const TcSeg& s = segs[it.seg];
             const int nstage = ((s.K >> 6) + 3) >> 2, ng = (it.n + 31) >> 5;
             const int sp = s.K >> 4;
@@ -483,7 +504,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
         const uint32_t lb = (uint32_t)(32 * q) << 16;
         int n_it = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ++n_it) {
-            const TcItem it = tc_item(segs, i, items0);
+            const TcItem it = tc_item(segs, tab, i, items0);
             const TcSeg& s = segs[it.seg];
             const int db = n_it & 1;
             bool w = true;

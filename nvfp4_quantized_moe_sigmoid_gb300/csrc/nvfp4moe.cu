@@ -584,7 +584,7 @@ int tc_ring_cap() {
 // W4A4 grouped path on the tensor cores (tcgen05 kind::mxf4nvf4).
 bool tc_path_ok(const moe_layer_weights* w) {
     const int H = w->hidden, I = w->inter, S = w->shared_inter;
-    if (H % 64 || I % 64 || S % 64) return false;
+    if (H % 64 || I % 64 || S % 64 || w->num_experts > kTcMaxExperts) return false;
     const void* p[] = {w->up_codes, w->down_codes, w->shared_up.codes, w->shared_down.codes};
     for (const void* q : p)
         if (!aligned(q, 16)) return false;
@@ -1455,4 +1455,68 @@ extern "C" nvfp4_status nvfp4_fp4_mma_peak(int32_t n, int32_t chains, int32_t it
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
     return st;
+}
+
+// ------------------------------------------------------------ workspace inspection
+extern "C" nvfp4_status nvfp4_workspace_view(int32_t call, const moe_layer_weights* w, int32_t T, int32_t k,
+                                             nvfp4_act_mode mode, int32_t region, nvfp4_ws_view* view) {
+    nvfp4_status st = check_layer(w);
+    if (st != NVFP4_OK) return st;
+    if (!view || T < 1 || k < 1 || k > w->num_experts) return NVFP4_ERR_INVALID_ARG;
+    if (mode != NVFP4_W4A16 && mode != NVFP4_W4A4) return NVFP4_ERR_INVALID_ARG;
+    if (region < NVFP4_WS_X || region > NVFP4_WS_SH_ACT_Q) return NVFP4_ERR_INVALID_ARG;
+    const int E = w->num_experts, H = w->hidden, I = w->inter, S = w->shared_inter;
+    const int64_t P = (int64_t)T * k;
+    const bool w4a4 = mode == NVFP4_W4A4;
+    nvfp4_ws_view v{};
+    auto rows_of = [&](int r) -> int64_t { return (r == NVFP4_WS_X || r >= NVFP4_WS_SH_ACT) ? T : P; };
+    auto cols_of = [&](int r) -> int64_t {
+        return r == NVFP4_WS_X ? H : (r >= NVFP4_WS_SH_ACT ? S : I);
+    };
+    v.rows = rows_of(region);
+    v.cols = cols_of(region);
+    if (call == 1) {  // moe_layer_forward
+        if (T > kDecodeMaxT || k > kDecodeMaxK || E > 256) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        const LayerWsOffsets o = layer_ws(T, k, H, I, S);
+        const bool quantised = region == NVFP4_WS_X || region == NVFP4_WS_ACT_Q || region == NVFP4_WS_SH_ACT_Q;
+        if (quantised && !w4a4) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // W4A16 rows are prescaled, not quantised
+        switch (region) {
+            case NVFP4_WS_X: v.offset = o.xq; v.global_offset = o.gx; break;
+            case NVFP4_WS_ACT: v.offset = o.act; break;
+            case NVFP4_WS_ACT_Q: v.offset = o.aq; v.global_offset = o.ga; break;
+            case NVFP4_WS_SH_ACT: v.offset = o.act_sh; break;
+            default: v.offset = o.aq_sh; v.global_offset = o.gsh; break;
+        }
+        v.format = quantised ? NVFP4_WS_F16_DEQUANT : NVFP4_WS_BF16;
+        v.pitch = 2 * v.cols;
+        v.has_global = quantised ? 1 : 0;
+    } else if (call == 0) {  // moe_expert_forward
+        if (decode_path(w, T, k)) {
+            if (region != NVFP4_WS_ACT && region != NVFP4_WS_SH_ACT) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+            const DecodeWs o = decode_ws(T, k, H, I, S);
+            v.offset = region == NVFP4_WS_ACT ? o.act : o.act_sh;
+            v.format = NVFP4_WS_BF16;
+            v.pitch = 2 * v.cols;
+        } else {
+            if (!(w4a4 && k <= kDecodeMaxK && tc_path_ok(w)) || E > 256) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+            const GroupedWsOffsets o = grouped_ws(T, k, E, H, I, S);
+            switch (region) {
+                case NVFP4_WS_X: v.offset = o.tq_c; v.scales_offset = o.tq_s; v.global_offset = o.gx; break;
+                case NVFP4_WS_ACT: v.offset = o.act; break;
+                case NVFP4_WS_ACT_Q: v.offset = o.aq_c; v.scales_offset = o.aq_s; v.global_offset = o.ga; break;
+                case NVFP4_WS_SH_ACT: v.offset = o.act_sh; break;
+                default: v.offset = o.as_c; v.scales_offset = o.as_s; v.global_offset = o.gsh; break;
+            }
+            const bool quantised = region == NVFP4_WS_X || region == NVFP4_WS_ACT_Q || region == NVFP4_WS_SH_ACT_Q;
+            v.format = quantised ? NVFP4_WS_CODES : NVFP4_WS_BF16;
+            v.pitch = quantised ? v.cols / 2 : 2 * v.cols;
+            v.scales_pitch = quantised ? spitch16((int)v.cols) : 0;
+            v.has_global = quantised ? 1 : 0;
+            v.position_order = region == NVFP4_WS_ACT || region == NVFP4_WS_ACT_Q ? 1 : 0;
+        }
+    } else {
+        return NVFP4_ERR_INVALID_ARG;
+    }
+    *view = v;
+    return NVFP4_OK;
 }

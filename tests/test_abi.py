@@ -127,3 +127,36 @@ def test_colblock_references_agree():
         np.testing.assert_array_equal(a, colblock_vectorised(codes, scales))
         # every input byte lands exactly once
         assert sorted(a.reshape(-1).tolist()) == sorted(codes.reshape(-1).tolist() + scales.reshape(-1).tolist())
+
+
+def test_workspace_view_of_the_layer_call(abi):
+    """nvfp4_workspace_view (host arithmetic only): the regions of a
+    moe_layer_forward workspace lie inside it, do not overlap, and the
+    quantised regions of a W4A16 call are refused."""
+    L = abi.load()
+    sh_up = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 3712, 2688)
+    sh_dn = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 2688, 3712)
+    w = abi.MoeLayerWeights(128, 2688, 1856, 3712, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000,
+                            0x10000, sh_up, sh_dn)
+    for T in (1, 4):
+        total = L.moe_layer_forward_workspace_size(ctypes.byref(w), T, 6, 1)
+        spans = []
+        for region, (rows, cols) in enumerate([(T, 2688), (6 * T, 1856), (6 * T, 1856), (T, 3712), (T, 3712)]):
+            v = abi.WsView()
+            assert L.nvfp4_workspace_view(1, ctypes.byref(w), T, 6, 1, region, ctypes.byref(v)) == 0
+            assert (v.rows, v.cols, v.pitch) == (rows, cols, 2 * cols)
+            assert v.format == (0 if region in (1, 3) else 2) and v.has_global == (region not in (1, 3))
+            spans.append((v.offset, v.offset + rows * v.pitch))
+            if v.has_global:
+                spans.append((v.global_offset, v.global_offset + 4 * rows))
+        spans.sort()
+        assert spans[-1][1] <= total
+        assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:])), spans
+        v = abi.WsView()
+        assert L.nvfp4_workspace_view(1, ctypes.byref(w), T, 6, 0, 0, ctypes.byref(v)) == 2
+        assert L.nvfp4_workspace_view(1, ctypes.byref(w), T, 6, 0, 1, ctypes.byref(v)) == 0
+    v = abi.WsView()
+    assert L.nvfp4_workspace_view(1, ctypes.byref(w), 5, 6, 1, 0, ctypes.byref(v)) == 2
+    assert L.nvfp4_workspace_view(2, ctypes.byref(w), 1, 6, 1, 0, ctypes.byref(v)) == 1
+    assert L.nvfp4_workspace_view(1, ctypes.byref(w), 1, 6, 1, 5, ctypes.byref(v)) == 1
+    assert L.nvfp4_workspace_view(1, ctypes.byref(w), 1, 6, 1, 0, None) == 1

@@ -142,3 +142,19 @@ def test_full_fused_layer(nm, full_layer):
     run_fused(nm, L, OL, h, c["K"], True, True, 1e-5)
     h4 = gen.hidden_bf16(4, c["H"], 0, layer=configs.HIDDEN_LAYER, rho=0.5)
     run_fused(nm, L, OL, h4, c["K"], True, True, 1e-5)
+
+
+def test_full_layer_w4a16_stack_one_token(nm, full_layer):
+    """The one-token W4A16 single-layer step as the benchmark times it: one
+    moe_stack_forward call over one layer of the pages' shapes (no norm), the
+    residual added; routing and output against the oracle."""
+    c, L, OL = full_layer
+    h = gen.hidden_bf16(1, c["H"], 0, layer=configs.HIDDEN_LAYER)
+    hd = to_dev_bf16(h)
+    ws = nm.make_stack_workspace([L], 1, c["K"], nm.W4A16)
+    hout, idx, w = nm.moe_stack_forward([L], hd, c["K"], nm.W4A16, workspace=ws, rms_eps=c["rms_eps"])
+    torch.cuda.synchronize()
+    assert nm.nvfp4_last_device_error() == 0
+    ref, _, r = OL.forward(h, c["K"], False, True, rms_eps=c["rms_eps"])
+    assert check_routing(idx[0].cpu().numpy(), w[0].cpu().numpy(), r, c["K"]) == 0
+    assert_close(bf16_to_f64(bf16_bits(hout[0])), bf16_to_f64(ref), "one-layer W4A16 stack")

@@ -134,3 +134,37 @@ def test_offgrid_boundary_cases_exact(nm):
             cq, sq, _ = gpu_quant(nm, xa, orc.GIVEN, float(g))
             assert int(sq[0, 0]) == s
             assert bytes(cq[0]) == codes
+
+
+def test_division_next_to_every_midpoint_for_many_divisors(nm):
+    """x / d with d = E4M3 scale x global (binary32 products) for 300 random
+    globals and every positive finite E4M3 scale, x within two ulps of each
+    E2M1 rounding midpoint m d: the kernels' division (a corrected
+    reciprocal) must give the codes of a correctly rounded binary32 quotient,
+    which the oracle takes by plain division. Many quotients land exactly on
+    a midpoint (even-code ties), the rest one or two ulps to either side."""
+    rng = np.random.default_rng(17)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    e4m3 = np.array([orc.e4m3_value(b) for b in range(1, 127)], np.float32)
+    exact_ties = 0
+    for _ in range(300):
+        g = np.float32(np.ldexp(rng.uniform(1.0, 2.0), int(rng.integers(-16, 0))))
+        blocks = []
+        for s in e4m3:
+            d = np.float32(s * g)
+            x0 = (mids * d).astype(np.float32)
+            near = [x0]
+            up, dn = x0.copy(), x0.copy()
+            for _k in range(2):
+                up = np.nextafter(up, np.float32(np.inf))
+                dn = np.nextafter(dn, np.float32(0))
+                near += [up, dn]
+            x = np.concatenate(near) * rng.choice(np.float32([-1, 1]), 35)
+            amax = np.float32(6 * d)
+            x = np.concatenate([x, np.zeros(10, np.float32)]).reshape(3, 15)
+            blocks.append(np.concatenate([np.full((3, 1), amax, np.float32), x], axis=1))
+            q = np.abs(np.concatenate(near)) / d
+            exact_ties += int(np.isin(q, mids).sum())
+        row = np.concatenate(blocks).reshape(1, -1).astype(np.float32)
+        same(nm, row, orc.GIVEN, g=float(g))
+    assert exact_ties > 300 * 126 * 2
