@@ -590,7 +590,7 @@ def run_trace(args, local):
         c["layers"] = min(c["layers"], args.layers)
     T, L = c["T"], c["layers"]
     if T > 4:
-        raise SystemExit("--trace covers the stack kernel (1-4 tokens)")
+        return run_trace_tc(args, local, c)
     st = MoEDecodeStack(L, c["E"], c["H"], c["I"], c["S"], c["K"], T, w4a4=c["w4a4"],
                         V=c["V"] if c["lm_head"] else None, rms_eps=c["rms_eps"])
     st.register(*fill.fillers(c["seed"], c["bias"]))
@@ -631,6 +631,76 @@ def run_trace(args, local):
         print(f"{name:34s} {a:11.2f} {b:10.2f}")
     if period.size:
         print(f"layer period: median {np.median(period):.2f} us, min {period.min():.2f}, max {period.max():.2f}")
+
+
+TC_TRACE_MHZ = 2070.0  # the SM clock under load (clocks sampled by the benchmark)
+TC_TRACE_KERNELS = ["grouped up GEMM (k_grouped_tc, last layer)", "grouped down GEMM (k_grouped_tc, last layer)",
+                    "lm_head GEMM (k_lm_head_tc, last chunk)"]
+
+
+def run_trace_tc(args, local, c):
+    """The stage trace of the tensor-core kernels (trace build): for CTAs
+    0..3 of the last launch of each, the medians over pipeline stages of the
+    hand-off intervals, and the per-item times."""
+    import ctypes
+    import numpy as np
+    import torch
+    import nvfp4_quantized_moe_sigmoid_gb300 as nm
+    from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
+    from gen import configs, fill
+
+    T, L = c["T"], c["layers"]
+    st = MoEDecodeStack(L, c["E"], c["H"], c["I"], c["S"], c["K"], T, w4a4=c["w4a4"],
+                        V=c["V"] if c["lm_head"] else None, rms_eps=c["rms_eps"])
+    st.register(*fill.fillers(c["seed"], c["bias"]))
+    fill.hidden(st.h[0], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+    lib = nm._L
+    lib.nvfp4moe_tc_trace_read.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t]
+    lib.nvfp4moe_tc_trace_read.restype = ctypes.c_int
+    buf = np.zeros(4 * 11 * 1024, dtype=np.uint64)
+    for _ in range(max(3, args.warmup)):
+        st.step()
+    torch.cuda.synchronize()
+    for k in range(3):  # clears what the warm-up left
+        assert lib.nvfp4moe_tc_trace_read(k, buf.ctypes.data, buf.nbytes) == 0
+    st.step()
+    torch.cuda.synchronize()
+    assert nm.nvfp4_last_device_error() == 0
+    print(f"stage trace: {c['name']}, {L} layers, T={T}; per kernel, CTAs 0-3, medians over stages (us)")
+    for k, name in enumerate(TC_TRACE_KERNELS):
+        assert lib.nvfp4moe_tc_trace_read(k, buf.ctypes.data, buf.nbytes) == 0
+        tr = buf.reshape(4, 11, 1024).astype(np.float64) / TC_TRACE_MHZ  # SM clocks -> us
+        if not (tr[:, 4] > 0).any():
+            continue
+        # an entry not written by this launch is 0 (the read clears)
+        print(f"-- {name}")
+        for cta in range(4):
+            t = tr[cta]
+            ns = int((t[4] > 0).sum())
+            ni = int((t[5] > 0).sum())
+            if ns < 2:
+                continue
+            t0 = t[0][0]
+            g = np.arange(ns)
+            mma = t[4][:ns]
+            span = mma[-1] - t0
+            med = lambda x: float(np.median(x)) if len(x) else float("nan")
+            print(f"   CTA {cta}: {ns} stages, {ni} items, span {span:.1f}; MMA-issue interval {med(np.diff(mma)):.3f}"
+                  f" (mean {np.mean(np.diff(mma)):.3f}); producer space wait {med(t[1][:ns] - t[0][:ns]):.3f};"
+                  f" copies landed after issue {med(t[2][:ns] - t[1][:ns]):.3f}; operands prepared {med(t[3][:ns] - t[2][:ns]):.3f};"
+                  f" MMA issue after prepared {med(mma - t[3][:ns]):.3f}; issue-to-MMA lead {med(mma - t[1][:ns]):.3f}")
+            if ni > 1:
+                it, e0, e1 = t[5][:ni], t[6][:ni], t[7][:ni]
+                print(f"          item period {med(np.diff(it)):.2f}, epilogue {med(e1 - e0):.2f},"
+                      f" epilogue start after item start {med(e0 - it):.2f}")
+            print(f"          producer: space free {med(t[8][:ns] - t[0][:ns]):.3f}, tensor copies issued"
+                  f" {med(t[9][:ns] - t[8][:ns]):.3f}, scale copies issued {med(t[10][:ns] - t[9][:ns]):.3f},"
+                  f" arrive {med(t[1][:ns] - t[10][:ns]):.3f}, next stage {med(t[0][1:ns] - t[1][:ns - 1]):.3f}")
+            if cta == 0:
+                rel = lambda x: " ".join(f"{v - t0:6.2f}" for v in x[:12])
+                print(f"          first stages, producer issued: {rel(t[1])}")
+                print(f"                        landed:          {rel(t[2])}")
+                print(f"                        MMA issued:      {rel(mma)}")
 
 
 # ------------------------------------------------------------------ concurrency sweep

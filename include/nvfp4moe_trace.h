@@ -27,6 +27,19 @@ extern "C" {
  * fails. */
 nvfp4_status nvfp4moe_stack_trace_read(void* dst, size_t bytes);
 
+/* Copies the stage trace of the last launch of one tensor-core kernel to host
+ * memory `dst`: kernel 0 the grouped up GEMM, 1 the grouped down GEMM (both
+ * of moe_expert_forward above 4 tokens, W4A4), 2 the lm_head GEMM of
+ * lm_head_forward above 8 tokens. Unsigned 64-bit SM clock readings (clock64)
+ * [4 CTAs][11 events][1024 stages or items] (TcTraceEvent in
+ * moe_grouped_tc.cuh: the producer's steps, operands landed and prepared,
+ * MMAs issued per stage; item start, epilogue start and end per item).
+ * Synchronises the device; at most 352 KiB are copied, and the kernel's
+ * trace is then cleared (zeros: entries the next launch does not reach). Returns
+ * NVFP4_ERR_INVALID_ARG for a null dst or an unknown kernel, NVFP4_ERR_CUDA
+ * if the copy fails. */
+nvfp4_status nvfp4moe_tc_trace_read(int32_t kernel, void* dst, size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif

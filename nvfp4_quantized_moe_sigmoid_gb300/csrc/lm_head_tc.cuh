@@ -125,22 +125,27 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
             for (int ks = 0; ks < nks; ++ks, ++g) {
                 const int s = g % kLmTcStages;
                 bool w = true;
+                TC_TRACE(lane == 0, 2, kTcTrProdWait, g);
                 if (lane == 0 && g >= kLmTcStages) w = tc_wait(&empty[s], ((g / kLmTcStages) - 1) & 1, ab);
                 if (!__shfl_sync(0xffffffffu, w, 0)) {
                     ok = false;
                     break;
                 }
                 uint8_t* const base = smem + (size_t)s * stage;
+                TC_TRACE(lane == 0, 2, kTcTrProdSpace, g);
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(kLmTcRaw + N * 128));
                     tma_load_2d(base + kLmTcA + N * 128, &a.a_map, ks * 32, row0, &full[s]);
                     tma_load_2d(base + kLmTcA, &a.b_map, ks * 128, 0, &full[s]);
                 }
+                TC_TRACE(lane == 0, 2, kTcTrProdTma, g);
                 // the stage's block scales: row r's four bytes (k / 16 = 4 ks .. 4 ks + 3)
                 uint8_t* const sc = base + kLmTcA + N * 128 + kLmTcRaw;
                 for (int r = lane; r < kLmTcRows; r += 32)
                     cp_async4(sc + 4 * r, a.scales + (size_t)(row0 + r) * sp + 4 * ks);
+                TC_TRACE(lane == 0, 2, kTcTrProdCpa, g);
                 cp_async_mbar_arrive(&full[s]);
+                TC_TRACE(lane == 0, 2, kTcTrProdIssued, g);
             }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
@@ -162,6 +167,7 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
                 const int db = n_it & 1;
                 if (n_it >= 2 && !tc_wait(&dempty[db], ((n_it >> 1) - 1) & 1, ab)) break;
                 tc_fence_after();
+                TC_TRACE(true, 2, kTcTrItemStart, n_it);
                 const uint32_t dcol = tmem + 256u * db;
                 for (int ks = 0; ks < nks; ++ks, ++g) {
                     const int s = g % kLmTcStages;
@@ -171,6 +177,7 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
                         break;
                     }
                     tc_fence_after();
+                    TC_TRACE(true, 2, kTcTrMmaIssue, g);
                     const uint32_t sbase = smem_u32(smem + (size_t)s * stage);
 #pragma unroll
                     for (int kk = 0; kk < kLmTcK / 16; ++kk) {
@@ -202,6 +209,7 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
                     ok = false;
                     break;
                 }
+                TC_TRACE(warp == 2 && lane == 0, 2, kTcTrFullSeen, g);
                 uint8_t* const base = smem + (size_t)s * stage;
                 const uint4 c0 = *reinterpret_cast<const uint4*>(base + kLmTcA + N * 128 + 16 * d);
                 const uint32_t sw = *reinterpret_cast<const uint16_t*>(base + kLmTcA + N * 128 + kLmTcRaw + 4 * r + 2 * hf);
@@ -221,6 +229,7 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&decoded[s]);
+                TC_TRACE(warp == 2 && lane == 0, 2, kTcTrPrepDone, g);
             }
         }
     } else {
@@ -235,6 +244,7 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
             if (lane == 0) w = tc_wait(&dfull[db], (n_it >> 1) & 1, ab);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
             tc_fence_after();
+            TC_TRACE(q == 0 && lane == 0, 2, kTcTrEpiStart, n_it);
             const int64_t row = (int64_t)tile * kLmTcRows + 32 * q + lane;
             for (int c0 = 0; c0 < N; c0 += 16) {
                 uint32_t v[16];
@@ -250,6 +260,7 @@ __global__ void __launch_bounds__(kLmTcThreads, 1) k_lm_head_tc(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&dempty[db]);
+            TC_TRACE(q == 0 && lane == 0, 2, kTcTrEpiEnd, n_it);
         }
     }
     tc_fence_before();

@@ -169,6 +169,40 @@ __device__ __noinline__ bool tc_wait(uint64_t* b, uint32_t parity, volatile int*
     }
 }
 
+// ---------------------------------------------------------------- stage trace
+// Built with -DNVFP4MOE_TRACE, CTAs 0 .. kTcTrCtas - 1 of the tensor-core
+// kernels record the SM clock (clock64) at the hand-offs of each pipeline stage and
+// work item into g_tc_trace[kernel][CTA][event][index] (kernel 0: grouped up,
+// 1: grouped down, 2: lm_head GEMM), read back by nvfp4moe_tc_trace_read.
+// Without the flag the trace points compile to nothing.
+enum TcTraceEvent : int {
+    kTcTrProdWait = 0,  // producer: before waiting for the stage's space (index: stage)
+    kTcTrProdIssued,    // producer: stage copies issued
+    kTcTrFullSeen,      // scale / decoder warp 2: the stage's bytes landed
+    kTcTrPrepDone,      // scale / decoder warp 2: the stage's operands ready for the MMA
+    kTcTrMmaIssue,      // MMA thread: the stage's waits passed, MMAs issued
+    kTcTrItemStart,     // MMA thread: accumulator free, item begins (index: item)
+    kTcTrEpiStart,      // epilogue warp (quarter 0): the item's accumulator complete
+    kTcTrEpiEnd,        // epilogue warp (quarter 0): the item's outputs written
+    kTcTrProdSpace,     // producer: the stage's space is free
+    kTcTrProdTma,       // producer: the stage's tensor copies issued
+    kTcTrProdCpa,       // producer: the stage's scale copies issued
+    kTcTrEvents
+};
+constexpr int kTcTrCtas = 4, kTcTrIdx = 1024;
+#if defined(NVFP4MOE_TRACE)
+__device__ unsigned long long g_tc_trace[3][kTcTrCtas][kTcTrEvents][kTcTrIdx];
+#define TC_TRACE(cond, kern, ev, idx)                                                               \
+    do {                                                                                           \
+        if ((cond) && blockIdx.x < kTcTrCtas && (idx) < kTcTrIdx)                                   \
+            g_tc_trace[kern][blockIdx.x][ev][idx] = clock64();                                      \
+    } while (0)
+#else
+#define TC_TRACE(cond, kern, ev, idx) \
+    do {                              \
+    } while (0)
+#endif
+
 // ---------------------------------------------------------------- arguments
 // A segment is one weight tensor over its positions: the routed experts
 // (positions grouped by expert) or the shared expert (all tokens in order).
@@ -360,6 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
                 // older stage whose bytes this one overwrites
                 const int lim = v + size - cap;
                 bool w = true;
+                TC_TRACE(lane == 0, KIND, kTcTrProdWait, g);
                 if (lane == 0) {
                     while (tail < g && (tail <= g - kTcSlots || vs[tail % kTcSlots] < lim)) {
                         w = tc_wait(&empty[tail % kTcSlots], (tail / kTcSlots) & 1, ab);
@@ -372,6 +407,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
                     break;
                 }
                 tail = __shfl_sync(0xffffffffu, tail, 0);
+                TC_TRACE(lane == 0, KIND, kTcTrProdSpace, g);
                 if (lane == 0) vs[st] = v;  // read by lane 0 only
                 vhead = v + size;
                 const uint32_t off = (uint32_t)(kTcOffRing + v % cap);
@@ -382,6 +418,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
                     tma_load_2d(base, amap, ks * 128, arow0, &full[st]);
                     tma_load_2d(base + kTcOffB, bmap, ks * 128, it.row0, &full[st]);
                 }
+                TC_TRACE(lane == 0, KIND, kTcTrProdTma, g);
                 // B scales: 32 ng rows x 16 bytes
                 for (int r = lane; r < 32 * ng; r += 32) {
                     const int row = it.row0 + r;
@@ -389,7 +426,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
                     cp_async16(base + kTcOffB + 4096 * ng + 16 * r,
                                in ? b_scales + (size_t)row * b_spitch + ks * 16 : b_scales, in ? 16 : 0);
                 }
+                TC_TRACE(lane == 0, KIND, kTcTrProdCpa, g);
                 cp_async_mbar_arrive(&full[st]);
+                TC_TRACE(lane == 0, KIND, kTcTrProdIssued, g);
                 if (lane == 0) uses[st] += 1;
             }
         }
@@ -415,6 +454,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
                 const int db = n_it & 1;
                 if (n_it >= 2 && !tc_wait(&dempty[db], ((n_it >> 1) - 1) & 1, ab)) break;
                 tc_fence_after();
+                TC_TRACE(true, KIND, kTcTrItemStart, n_it);
                 const uint32_t idesc = umma_idesc_mxf4(32 * ng);
                 const uint32_t dcol = tmem + 128u * db;
                 const int nc = tc_chains(ng, nks);
@@ -426,6 +466,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
                         break;
                     }
                     tc_fence_after();
+                    TC_TRACE(true, KIND, kTcTrMmaIssue, g);
                     const uint32_t sbase = smem_u32(smem + stage_off[st]);
                     const int nk = min(4, nks - 4 * ks);
                     for (int kk = 0; kk < nk; ++kk) {
@@ -471,6 +512,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
                     ok = false;
                     break;
                 }
+                TC_TRACE(warp == 2 && lane == 0, KIND, kTcTrFullSeen, g);
                 const uint8_t* base = smem + stage_off[st];
                 // A: row 32 q + lane, step kk -> column sfa(kk) + q
                 const uint32_t* sw = reinterpret_cast<const uint32_t*>(scrow + 16 * ks);
@@ -494,6 +536,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sfready[st]);
+                TC_TRACE(warp == 2 && lane == 0, KIND, kTcTrPrepDone, g);
             }
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(&scempty[b]);  // done with this item's scale block
@@ -511,6 +554,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
             if (lane == 0) w = tc_wait(&dfull[db], (n_it >> 1) & 1, ab);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
             tc_fence_after();
+            TC_TRACE(q == 0 && lane == 0, KIND, kTcTrEpiStart, n_it);
             const float gw = __ldg(s.a_global + it.e);
             const int m = it.mt * kTcRows + 32 * q + lane;
             // the item's column factors, every load in flight at once (one
@@ -569,6 +613,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
             tc_fence_before();
             __syncwarp();  // also: this warp's column factors may be rewritten
             if (lane == 0) mbar_arrive(&dempty[db]);
+            TC_TRACE(q == 0 && lane == 0, KIND, kTcTrEpiEnd, n_it);
         }
     }
     tc_fence_before();

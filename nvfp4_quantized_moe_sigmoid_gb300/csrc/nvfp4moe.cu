@@ -233,6 +233,18 @@ nvfp4_status nvfp4moe_stack_trace_read(void* dst, size_t bytes) {
     const size_t n = std::min(bytes, sizeof(g_stack_trace));
     return cudaMemcpyFromSymbol(dst, g_stack_trace, n) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
+
+nvfp4_status nvfp4moe_tc_trace_read(int32_t kernel, void* dst, size_t bytes) {
+    if (!dst || kernel < 0 || kernel > 2) return NVFP4_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4_ERR_CUDA;
+    const size_t one = sizeof(g_tc_trace) / 3;
+    const size_t n = std::min(bytes, one);
+    if (cudaMemcpyFromSymbol(dst, g_tc_trace, n, one * kernel) != cudaSuccess) return NVFP4_ERR_CUDA;
+    void* base = nullptr;  // cleared, so that the next read holds only the next launch's entries
+    if (cudaGetSymbolAddress(&base, g_tc_trace) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaMemset(static_cast<uint8_t*>(base) + one * kernel, 0, one) != cudaSuccess) return NVFP4_ERR_CUDA;
+    return cudaDeviceSynchronize() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
 #endif
 
 nvfp4_status nvfp4_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t cols,
