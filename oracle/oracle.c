@@ -434,6 +434,93 @@ void orc_lm_head_rows(const orc_mat* W, const uint16_t* h, int32_t T, const int6
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* FP8 (E4M3) per-tensor W8A8: the shared expert of the W4A4 card            */
+/* ------------------------------------------------------------------------ */
+
+/* Quantise x[rows][cols] to E4M3 with one FP32 scale (W4A4 card precision
+ * table: "Mamba in_proj / out_proj, shared experts: FP8 per-tensor W8A8";
+ * worklog Step 3 yaml: shared experts "num_bits: e4m3"):
+ *   g   = amax / 448                  one binary32 division
+ *   q_i = E4M3_rn_satfinite( x_i / g )   one binary32 division
+ * Reading: g = 0 (an all-zero tensor or row) gives q = 0 with the sign kept.
+ * mode 0: one scale for the tensor (weights), written to g_io[0];
+ * mode 1: one scale per row (activations: the dynamic per-token reading of
+ *         "per-tensor" for the inputs, as for NVFP4), written to g_io[r];
+ * mode 2: the scale is given in g_io[0]. Returns 0, or -1 on a bad argument. */
+int orc_fp8_quantize(const float* x, int64_t rows, int64_t cols, int mode, float* g_io, uint8_t* q) {
+    if (rows < 0 || cols < 1 || mode < 0 || mode > 2) return -1;
+    float gt = 0.0f;
+    if (mode == 0) {
+        gt = orc_amax(x, rows * cols) / 448.0f;
+        g_io[0] = gt;
+    } else if (mode == 2) {
+        gt = g_io[0];
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        float g = gt;
+        if (mode == 1) {
+            g = orc_amax(x + r * cols, cols) / 448.0f;
+            g_io[r] = g;
+        }
+        for (int64_t i = 0; i < cols; ++i) {
+            const float v = x[r * cols + i];
+            q[r * cols + i] = (uint8_t)(g == 0.0f ? (signbit(v) ? 0x80 : 0) : orc_e4m3_encode(v / g));
+        }
+    }
+    return 0;
+}
+
+/* y[n] = sum_j E4M3(W[n][j]) * x[j] (binary64; the scales are applied by the
+ * caller). */
+static void orc_fp8_matvec(const uint8_t* W, int64_t n, int64_t k, const double* x, double* y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < k; ++j) acc += orc_e4m3_value(W[r * k + j]) * x[j];
+        y[r] = acc;
+    }
+}
+
+/* The shared expert in FP8 W8A8 for T tokens (non-gated, as the NVFP4 one:
+ * card-int4 "Checkpoint layout"):
+ *   x_q = FP8(x) per row, scale g_x;   u = g_up * g_x * (W_up . E4M3(x_q))
+ *   a   = bf16(relu(u)^2)              (the bf16 intermediate, reading 5)
+ *   a_q = FP8(a) per row, scale g_a;   y = g_dn * g_a * (W_dn . E4M3(a_q))
+ * x: bf16 [T][H] (already normalised when the block is pre-normed);
+ * W_up [S][H], W_dn [H][S] E4M3 with per-tensor scales g_up, g_dn.
+ * Outputs y [T][H] (binary64) and the bf16 intermediate act [T][S]. */
+void orc_shared_fp8(const uint16_t* x, int32_t T, int64_t H, int64_t S, const uint8_t* w_up, float g_up,
+                    const uint8_t* w_dn, float g_dn, double* y, uint16_t* act) {
+    float* xf = (float*)malloc(sizeof(float) * (size_t)(H > S ? H : S));
+    uint8_t* q = (uint8_t*)malloc((size_t)(H > S ? H : S));
+    double* v = (double*)malloc(sizeof(double) * (size_t)(H > S ? H : S));
+    double* u = (double*)malloc(sizeof(double) * (size_t)S);
+    for (int32_t t = 0; t < T; ++t) {
+        float gx = 0.0f, ga = 0.0f;
+        for (int64_t i = 0; i < H; ++i) xf[i] = (float)orc_bf16_value(x[(int64_t)t * H + i]);
+        orc_fp8_quantize(xf, 1, H, 1, &gx, q);
+        for (int64_t i = 0; i < H; ++i) v[i] = orc_e4m3_value(q[i]);
+        orc_fp8_matvec(w_up, S, H, v, u);
+        for (int64_t j = 0; j < S; ++j) {
+            double uj = u[j] * (double)g_up * (double)gx;
+            double r = uj > 0.0 ? uj : 0.0;
+            uint16_t b = orc_bf16_round(r * r);
+            act[(int64_t)t * S + j] = b;
+            xf[j] = (float)orc_bf16_value(b);
+        }
+        orc_fp8_quantize(xf, 1, S, 1, &ga, q);
+        for (int64_t j = 0; j < S; ++j) v[j] = orc_e4m3_value(q[j]);
+        orc_fp8_matvec(w_dn, H, S, v, y + (int64_t)t * H);
+        for (int64_t i = 0; i < H; ++i) y[(int64_t)t * H + i] *= (double)g_dn * (double)ga;
+    }
+    free(xf);
+    free(q);
+    free(v);
+    free(u);
+}
+
 void orc_set_threads(int n) {
 #ifdef _OPENMP
     omp_set_num_threads(n > 0 ? n : 1);

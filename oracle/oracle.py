@@ -53,6 +53,11 @@ def lib():
         L.orc_lm_head.argtypes = [P, P, ctypes.c_int32, P]
         L.orc_lm_head_rows.restype = None
         L.orc_lm_head_rows.argtypes = [P, P, ctypes.c_int32, P, ctypes.c_int64, P]
+        L.orc_fp8_quantize.restype = ctypes.c_int
+        L.orc_fp8_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P]
+        L.orc_shared_fp8.restype = None
+        L.orc_shared_fp8.argtypes = [P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_float, P,
+                                     ctypes.c_float, P, P]
         L.orc_set_threads.restype = None
         L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_get_threads.restype = ctypes.c_int
@@ -266,3 +271,35 @@ def lm_head_rows(W: Mat, h_bf16, rows) -> np.ndarray:
     m = W.c()
     lib().orc_lm_head_rows(ctypes.byref(m), _p(h), T, _p(rows), rows.size, _p(out))
     return out
+
+
+# ---- FP8 shared expert ------------------------------------------------------
+def fp8_quantize(x: np.ndarray, mode: int = PER_TENSOR, g: float = None):
+    """x: float32 [rows][cols] (or uint16 bf16). Returns (codes uint8 [rows][cols], g)."""
+    if x.dtype == np.uint16:
+        x = bf16_to_f32(x)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    rows, cols = x.shape
+    q = np.zeros((rows, cols), np.uint8)
+    gio = np.zeros(rows if mode == PER_ROW else 1, np.float32)
+    if mode == GIVEN:
+        gio[0] = g
+    if lib().orc_fp8_quantize(_p(x), rows, cols, mode, _p(gio), _p(q)) != 0:
+        raise ValueError("orc_fp8_quantize rejected its arguments")
+    return q, gio
+
+
+def shared_fp8(x_bf16, w_up, g_up, w_dn, g_dn):
+    """The FP8 W8A8 shared expert on bf16 rows x [T][H]: returns (y f64 [T][H],
+    act bf16 bits [T][S])."""
+    x = np.ascontiguousarray(x_bf16, np.uint16)
+    T, H = x.shape
+    w_up = np.ascontiguousarray(w_up, np.uint8)
+    w_dn = np.ascontiguousarray(w_dn, np.uint8)
+    S = w_up.shape[0]
+    y = np.zeros((T, H), np.float64)
+    act = np.zeros((T, S), np.uint16)
+    lib().orc_shared_fp8(_p(x), T, H, S, _p(w_up), float(g_up), _p(w_dn), float(g_dn), _p(y), _p(act))
+    return y, act
