@@ -389,6 +389,52 @@ def measure_spec_step(base, nm, rf, peak, iters=10):
     return out
 
 
+def measure_shared_fp8(nm, peak, iters=10):
+    """The FP8 W8A8 shared expert (the W4A4 card's precision for the shared
+    experts) at 1 and 4 tokens: moe_shared_fp8_forward on the pages' shared
+    expert (3712 x 2688 up, 2688 x 3712 down, E4M3, per-tensor scales) with
+    the residual add, timed in a graph of 5 back-to-back calls."""
+    import torch
+    from gen import configs, fill
+
+    c = configs.shape(1)
+    H, S = c["H"], c["S"]
+    fb, _, _ = fill.fillers(c["seed"], c["bias"])
+    up_m = torch.empty((S, H), dtype=torch.bfloat16, device="cuda")
+    dn_m = torch.empty((H, S), dtype=torch.bfloat16, device="cuda")
+    fb("sh_up", 0, 0, up_m)
+    fb("sh_down", 0, 0, dn_m)
+    up, dn = nm.fp8_quantize(up_m, nm.PER_TENSOR), nm.fp8_quantize(dn_m, nm.PER_TENSOR)
+    del up_m, dn_m
+    # 8 copies (160 MB, more than L2): the back-to-back calls of a graph each
+    # stream their own copy
+    copies = [(nm.FP8Matrix(up.codes.clone(), up.global_scale), nm.FP8Matrix(dn.codes.clone(), dn.global_scale))
+              for _ in range(8)]
+    out = {}
+    for T in (1, 4):
+        h = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        fill.hidden(h, c["seed"], layer=configs.HIDDEN_LAYER)
+        o = torch.empty_like(h)
+        ws_ = torch.empty(nm.moe_shared_fp8_workspace_size(up, T), dtype=torch.uint8, device="cuda")
+        turn = iter(range(1 << 30))
+
+        def call():
+            u, d = copies[next(turn) % len(copies)]
+            nm.moe_shared_fp8_forward(u, d, h, residual=h, out=o, workspace=ws_, rms_eps=c["rms_eps"])
+
+        g = graph_of(call, 5)
+        us = time_graph(g, iters) / 5 * 1e3
+        del g
+        assert nm.nvfp4_last_device_error() == 0
+        b = 2 * S * H + 8 + T * H * 2 * 3
+        out["%d_tokens" % T] = {"us": us, "bytes": b, "gbs": b / (us * 1e-6) / 1e9,
+                                "frac_of_measured_hbm": b / (us * 1e-6) / 1e9 / peak}
+    out["workload"] = ("FP8 W8A8 shared expert (moe_shared_fp8_forward: E4M3 up %d x %d and down %d x %d, "
+                       "per-token E4M3 activations, RMS norm, residual add; each call on its own copy of "
+                       "the weights, 8 copies > L2)" % (S, H, H, S))
+    return out
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args, ws, rank, local):
     import torch
@@ -525,6 +571,7 @@ def run_ours(args, ws, rank, local):
         for oc in (0, 2, 3, 4):
             others[configs.shape(oc)["name"]] = measure_other_config(oc, st, nm, rf, peak, fp4["tflops"])
         others["spec_decode_k3_step"] = measure_spec_step(st, nm, rf, peak)
+        others["shared_expert_fp8"] = measure_shared_fp8(nm, peak)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -499,6 +499,57 @@ typedef struct {
 nvfp4_status nvfp4_workspace_view(int32_t call, const moe_layer_weights* w, int32_t T, int32_t k,
                                   nvfp4_act_mode mode, int32_t region, nvfp4_ws_view* view);
 
+/* ---------------------------------------------------------------- FP8 W8A8
+ * The shared expert in FP8 per-tensor W8A8, the precision the W4A4 card's
+ * table gives the shared experts ([card-w4a4] precision table: "Mamba
+ * in_proj / out_proj, shared experts: FP8 per-tensor W8A8"; [worklog] Step 3
+ * quant config: shared experts "num_bits: e4m3").
+ *
+ * FP8 tensor: codes uint8 [n][k] E4M3 (OCP "FN"), one FP32 scale;
+ * value(r, c) = E4M3(code) * scale. Quantisation (this library's reading,
+ * binary32, ties to even):
+ *   scale = amax / 448;   code_i = E4M3_rn_satfinite( x_i / scale )
+ * a scale of 0 (an all-zero tensor or row) gives codes 0 with the sign kept.
+ */
+typedef struct {
+    const uint8_t* codes;      /* [n][k] E4M3 */
+    const float* global_scale; /* [1] */
+    int64_t n, k;
+} fp8_matrix;
+
+/* fp8_quantize - x [rows][cols] (bf16 if x_is_bf16, else fp32; device,
+ * 16-byte aligned, cols % 16 == 0) to E4M3 codes [rows][cols] (device,
+ * 16-byte aligned) with the scale of `mode`: NVFP4_GLOBAL_PER_TENSOR writes
+ * amax / 448 to global_scale[0]; PER_ROW writes one per row to
+ * global_scale[r]; GIVEN reads global_scale[0]. Asynchronous on `stream`.
+ * Returns NVFP4_ERR_UNSUPPORTED_SHAPE for cols % 16, NVFP4_ERR_MISALIGNED,
+ * NVFP4_ERR_INVALID_ARG for null pointers or an unknown mode. */
+nvfp4_status fp8_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t cols, nvfp4_global_mode mode,
+                          float* global_scale, uint8_t* codes, cudaStream_t stream);
+
+/* moe_shared_fp8_forward - the shared expert in FP8 W8A8 for T tokens:
+ *   x   = RMSNorm(hidden) when rms_eps > 0 (the same unit-weight norm as the
+ *         other calls), else hidden
+ *   x_q = FP8(x) per token row;   u = up . x_q  (scales applied in FP32)
+ *   a   = bf16(relu(u)^2);        a_q = FP8(a) per token row
+ *   out = bf16(down . a_q + residual)   (residual may be null)
+ * A layer whose shared expert is FP8 adds it to the routed experts' output by
+ * passing that output as `residual` (two bf16 roundings: this library's
+ * reading of a separately launched FP8 GEMM).
+ *   up        fp8_matrix [S][H];  down fp8_matrix [H][S]; H, S % 64 == 0,
+ *             H, S <= 2^20 and 8 * max(H, S) bytes within a CTA's shared
+ *             memory
+ *   hidden    device bf16 [T][H], 16-byte aligned; residual, out bf16 [T][H]
+ *   workspace device, >= moe_shared_fp8_workspace_size(up, T) bytes,
+ *             256-byte aligned (no zeroing needed)
+ * Tokens run in chunks of 8 (the MMA's columns). Asynchronous on `stream`.
+ * Returns NVFP4_ERR_INVALID_ARG / _UNSUPPORTED_SHAPE / _MISALIGNED /
+ * _WORKSPACE on bad arguments, before any launch. */
+size_t moe_shared_fp8_workspace_size(const fp8_matrix* up, int32_t T);
+nvfp4_status moe_shared_fp8_forward(const fp8_matrix* up, const fp8_matrix* down, const void* hidden, int32_t T,
+                                    float rms_eps, const void* residual, void* out, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* nvfp4_status_string(nvfp4_status status);
 

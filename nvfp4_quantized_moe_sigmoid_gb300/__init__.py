@@ -20,6 +20,7 @@ __all__ = ["NVFP4Matrix", "MoELayer", "NVFP4Error", "nvfp4_quantize", "moe_route
            "make_stack_workspace", "nvfp4_colblock_layout", "moe_permute", "lm_head_gemv", "lm_head_forward",
            "make_lm_head_workspace",
            "nvfp4_status_string", "nvfp4_last_device_error", "nvfp4_workspace_view",
+           "FP8Matrix", "fp8_quantize", "moe_shared_fp8_workspace_size", "moe_shared_fp8_forward",
            "W4A16", "W4A4", "PER_TENSOR", "PER_ROW", "GIVEN", "lib"]
 
 W4A16, W4A4 = 0, 1
@@ -101,6 +102,22 @@ class NVFP4Matrix:
         return self.codes.numel() + self.scales.numel()
 
 
+class FP8Matrix:
+    """An FP8 (E4M3) matrix [n][k] with one FP32 scale (device tensors)."""
+
+    def __init__(self, codes, global_scale):
+        self.codes, self.global_scale = codes, global_scale
+        self.n, self.k = codes.shape[-2], codes.shape[-1]
+
+    @staticmethod
+    def empty(n, k, device="cuda"):
+        return FP8Matrix(torch.empty((n, k), dtype=torch.uint8, device=device),
+                         torch.empty(1, dtype=torch.float32, device=device))
+
+    def c(self):
+        return _abi.FP8Matrix(self.codes.data_ptr(), self.global_scale.data_ptr(), self.n, self.k)
+
+
 class MoELayer:
     """Device weights of one MoE layer: router (fp32 gate + fp32 bias), stacked
     routed experts (NVFP4 up [E][I][H], down [E][H][I]) and one shared expert."""
@@ -166,6 +183,44 @@ def nvfp4_quantize(x, mode=PER_TENSOR, out: NVFP4Matrix = None, global_scale=Non
     st = _L.nvfp4_quantize(_ptr(x), int(x.dtype == torch.bfloat16), rows, cols, mode,
                            _ptr(out.global_scale), _ptr(out.codes), _ptr(out.scales), _stream(stream))
     _check(st, "nvfp4_quantize")
+    return out
+
+
+def fp8_quantize(x, mode=PER_TENSOR, out: FP8Matrix = None, global_scale=None, stream=None):
+    """Quantise x [rows][cols] (bf16 or float32, CUDA) to E4M3 with one scale
+    (PER_TENSOR, GIVEN) or one per row (PER_ROW). Returns an FP8Matrix."""
+    x = x.contiguous()
+    rows, cols = x.shape
+    if out is None:
+        out = FP8Matrix.empty(rows, cols, x.device)
+        if mode == PER_ROW:
+            out.global_scale = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if mode == GIVEN:
+        out.global_scale.copy_(global_scale)
+    st = _L.fp8_quantize(_ptr(x), int(x.dtype == torch.bfloat16), rows, cols, mode, _ptr(out.global_scale),
+                         _ptr(out.codes), _stream(stream))
+    _check(st, "fp8_quantize")
+    return out
+
+
+def moe_shared_fp8_workspace_size(up: FP8Matrix, T) -> int:
+    u = up.c()
+    return int(_L.moe_shared_fp8_workspace_size(ctypes.byref(u), T))
+
+
+def moe_shared_fp8_forward(up: FP8Matrix, down: FP8Matrix, hidden, residual=None, out=None, workspace=None,
+                           rms_eps=0.0, stream=None):
+    """The FP8 W8A8 shared expert: out = bf16(down . bf16(relu(up . x)^2) +
+    residual) with per-token E4M3 activations."""
+    T = hidden.shape[0]
+    if out is None:
+        out = torch.empty_like(hidden)
+    if workspace is None:
+        workspace = torch.empty(moe_shared_fp8_workspace_size(up, T), dtype=torch.uint8, device=hidden.device)
+    u, d = up.c(), down.c()
+    st = _L.moe_shared_fp8_forward(ctypes.byref(u), ctypes.byref(d), _ptr(hidden), T, float(rms_eps), _ptr(residual),
+                                   _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "moe_shared_fp8_forward")
     return out
 
 

@@ -18,7 +18,8 @@ EXPORTS = ["nvfp4_quantize", "moe_route_topk", "moe_expert_forward_workspace_siz
            "lm_head_gemv", "lm_head_forward", "lm_head_forward_workspace_size",
            "nvfp4_colblock_layout", "nvfp4_status_string", "nvfp4_last_device_error",
            "nvfp4_fp4_mma_peak", "nvfp4_set_peer_wait_limit", "nvfp4_set_decode_max_tokens",
-           "nvfp4_workspace_view"]
+           "nvfp4_workspace_view", "fp8_quantize", "moe_shared_fp8_workspace_size",
+           "moe_shared_fp8_forward"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20  # NVFP4MOE_NOALLOC_SCRATCH_BYTES
 STACK_MAX_LAYERS = 32  # NVFP4MOE_STACK_MAX_LAYERS
@@ -37,6 +38,10 @@ class MoeLayerWeights(ctypes.Structure):
                 ("up_codes", P), ("up_scales", P), ("up_global", P),
                 ("down_codes", P), ("down_scales", P), ("down_global", P),
                 ("shared_up", NVFP4Matrix), ("shared_down", NVFP4Matrix)]
+
+
+class FP8Matrix(ctypes.Structure):
+    _fields_ = [("codes", P), ("global_scale", P), ("n", I64), ("k", I64)]
 
 
 class WsView(ctypes.Structure):
@@ -109,5 +114,12 @@ def load(path: str = LIB_PATH):
     L.nvfp4_workspace_view.argtypes = [I32, ctypes.POINTER(MoeLayerWeights), I32, I32, ctypes.c_int, I32,
                                        ctypes.POINTER(WsView)]
     L.nvfp4_workspace_view.restype = ctypes.c_int
+    L.fp8_quantize.argtypes = [P, ctypes.c_int, I64, I64, ctypes.c_int, P, P, P]
+    L.fp8_quantize.restype = ctypes.c_int
+    L.moe_shared_fp8_workspace_size.argtypes = [ctypes.POINTER(FP8Matrix), I32]
+    L.moe_shared_fp8_workspace_size.restype = ctypes.c_size_t
+    L.moe_shared_fp8_forward.argtypes = [ctypes.POINTER(FP8Matrix), ctypes.POINTER(FP8Matrix), P, I32, ctypes.c_float,
+                                         P, P, P, ctypes.c_size_t, P]
+    L.moe_shared_fp8_forward.restype = ctypes.c_int
     _lib = L
     return L

@@ -16,6 +16,7 @@
 
 #include "common.cuh"
 #include "fp4_peak.cuh"
+#include "fp8.cuh"
 #include "lm_head.cuh"
 #include "lm_head_tc.cuh"
 #include "moe_decode.cuh"
@@ -1531,4 +1532,141 @@ extern "C" nvfp4_status nvfp4_workspace_view(int32_t call, const moe_layer_weigh
     }
     *view = v;
     return NVFP4_OK;
+}
+
+// ------------------------------------------------------------ FP8 shared expert
+namespace {
+
+struct Fp8WsOffsets {
+    size_t xn, qx, gx, act, qa, ga, total;
+};
+
+Fp8WsOffsets fp8_ws(int T, int H, int S) {
+    Fp8WsOffsets o{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    const int tc = std::min(T, kF8MaxT);  // tokens per chunk
+    o.xn = take((size_t)tc * H * 2);
+    o.qx = take((size_t)tc * H);
+    o.gx = take((size_t)tc * 4);
+    o.act = take((size_t)tc * S * 2);
+    o.qa = take((size_t)tc * S);
+    o.ga = take((size_t)tc * 4);
+    o.total = off;
+    return o;
+}
+
+nvfp4_status check_fp8_matrix(const fp8_matrix* m, int64_t n, int64_t k) {
+    if (!m || !m->codes || !m->global_scale) return NVFP4_ERR_INVALID_ARG;
+    if (m->n != n || m->k != k) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(m->codes, 16)) return NVFP4_ERR_MISALIGNED;
+    return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" nvfp4_status fp8_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t cols,
+                                     nvfp4_global_mode mode, float* global_scale, uint8_t* codes,
+                                     cudaStream_t stream) {
+    if (!global_scale || rows < 0 || cols <= 0) return NVFP4_ERR_INVALID_ARG;
+    if (mode != NVFP4_GLOBAL_PER_TENSOR && mode != NVFP4_GLOBAL_PER_ROW && mode != NVFP4_GLOBAL_GIVEN)
+        return NVFP4_ERR_INVALID_ARG;
+    if (cols % 16) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) {
+        if (mode == NVFP4_GLOBAL_PER_TENSOR && cudaMemsetAsync(global_scale, 0, sizeof(float), stream) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        return NVFP4_OK;
+    }
+    if (!x || !codes) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(codes, 16)) return NVFP4_ERR_MISALIGNED;
+    const int64_t nblocks = rows * (cols / 16);
+    const int maxg = num_sms() * 8;
+    const int grid = static_cast<int>(std::min<int64_t>((nblocks + 255) / 256, maxg));
+    const bool bf16 = x_is_bf16 != 0;
+    if (mode == NVFP4_GLOBAL_PER_ROW) {
+        const int rgrid = static_cast<int>(std::min<int64_t>((rows + 7) / 8, maxg));
+        if (bf16) k_fp8_quantize_rows<true><<<rgrid, 256, 0, stream>>>(x, rows, cols, global_scale, codes);
+        else k_fp8_quantize_rows<false><<<rgrid, 256, 0, stream>>>(x, rows, cols, global_scale, codes);
+        return launch_status();
+    }
+    if (mode == NVFP4_GLOBAL_PER_TENSOR) {
+        if (cudaMemsetAsync(global_scale, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+        unsigned int* bits = reinterpret_cast<unsigned int*>(global_scale);
+        if (bf16) k_amax<true><<<grid, 256, 0, stream>>>(x, nblocks, bits);
+        else k_amax<false><<<grid, 256, 0, stream>>>(x, nblocks, bits);
+    }
+    const int from_amax = mode == NVFP4_GLOBAL_PER_TENSOR ? 1 : 0;
+    if (bf16) k_fp8_quantize_global<true><<<grid, 256, 0, stream>>>(x, nblocks, global_scale, from_amax, codes);
+    else k_fp8_quantize_global<false><<<grid, 256, 0, stream>>>(x, nblocks, global_scale, from_amax, codes);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (from_amax) k_fp8_finalize_global<<<1, 1, 0, stream>>>(global_scale);
+    return launch_status();
+}
+
+extern "C" size_t moe_shared_fp8_workspace_size(const fp8_matrix* up, int32_t T) {
+    if (!up || T < 1) return 0;
+    return fp8_ws(T, static_cast<int>(up->k), static_cast<int>(up->n)).total;
+}
+
+extern "C" nvfp4_status moe_shared_fp8_forward(const fp8_matrix* up, const fp8_matrix* down, const void* hidden,
+                                               int32_t T, float rms_eps, const void* residual, void* out,
+                                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!up || !down || !hidden || !out || !workspace || T < 1) return NVFP4_ERR_INVALID_ARG;
+    const int64_t S = up->n, H = up->k;
+    nvfp4_status st = check_fp8_matrix(up, S, H);
+    if (st != NVFP4_OK) return st;
+    if ((st = check_fp8_matrix(down, H, S)) != NVFP4_OK) return st;
+    if (S < 1 || H < 1 || H % 64 || S % 64 || H > (1 << 20) || S > (1 << 20)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(out, 4) || !aligned(workspace, 256) || (residual && !aligned(residual, 4)))
+        return NVFP4_ERR_MISALIGNED;
+    const Fp8WsOffsets o = fp8_ws(T, static_cast<int>(H), static_cast<int>(S));
+    if (workspace_bytes < o.total) return NVFP4_ERR_WORKSPACE;
+    const size_t smem = (size_t)kF8MaxT * std::max(H, S);
+    if ((int64_t)smem > dyn_smem_limit(k_fp8_gemv<kGroupedUp>) || (int64_t)smem > dyn_smem_limit(k_fp8_gemv<kGroupedDown>))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint16_t* xn = reinterpret_cast<uint16_t*>(ws + o.xn);
+    uint8_t* qx = ws + o.qx;
+    float* gx = reinterpret_cast<float*>(ws + o.gx);
+    uint16_t* act = reinterpret_cast<uint16_t*>(ws + o.act);
+    uint8_t* qa = ws + o.qa;
+    float* ga = reinterpret_cast<float*>(ws + o.ga);
+    for (int t0 = 0; t0 < T; t0 += kF8MaxT) {  // chunks of up to 8 tokens: the MMA's columns
+        const int tc = std::min(kF8MaxT, T - t0);
+        const uint16_t* h = static_cast<const uint16_t*>(hidden) + (size_t)t0 * H;
+        const uint16_t* xin = h;
+        if (rms_eps > 0.0f) {
+            k_fp8_rmsnorm_rows<<<(tc + 7) / 8, 256, 0, stream>>>(h, tc, static_cast<int>(H), rms_eps, xn);
+            xin = xn;
+        }
+        k_fp8_quantize_rows<true><<<(tc + 7) / 8, 256, 0, stream>>>(xin, tc, H, gx, qx);
+        Fp8GemvArgs ua{};
+        ua.w = up->codes;
+        ua.gw = up->global_scale;
+        ua.n = static_cast<int>(S);
+        ua.K = static_cast<int>(H);
+        ua.xq = qx;
+        ua.gx = gx;
+        ua.T = tc;
+        ua.act = act;
+        k_fp8_gemv<kGroupedUp><<<static_cast<int>(S / 16), kF8Threads, (size_t)tc * H, stream>>>(ua);
+        k_fp8_quantize_rows<true><<<(tc + 7) / 8, 256, 0, stream>>>(act, tc, S, ga, qa);
+        Fp8GemvArgs da{};
+        da.w = down->codes;
+        da.gw = down->global_scale;
+        da.n = static_cast<int>(H);
+        da.K = static_cast<int>(S);
+        da.xq = qa;
+        da.gx = ga;
+        da.T = tc;
+        da.residual = residual ? static_cast<const uint16_t*>(residual) + (size_t)t0 * H : nullptr;
+        da.out = static_cast<uint16_t*>(out) + (size_t)t0 * H;
+        k_fp8_gemv<kGroupedDown><<<static_cast<int>(H / 16), kF8Threads, (size_t)tc * S, stream>>>(da);
+        if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    return launch_status();
 }
