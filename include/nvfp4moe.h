@@ -537,12 +537,14 @@ nvfp4_status fp8_quantize(const void* x, int x_is_bf16, int64_t rows, int64_t co
  * passing that output as `residual` (two bf16 roundings: this library's
  * reading of a separately launched FP8 GEMM).
  *   up        fp8_matrix [S][H];  down fp8_matrix [H][S]; H, S % 64 == 0,
- *             H, S <= 2^20 and 8 * max(H, S) bytes within a CTA's shared
- *             memory
+ *             H, S <= 2^20; 8 * H and 8 * S bytes within a CTA's shared
+ *             memory (each CTA quantises the token rows its GEMV needs
+ *             itself)
  *   hidden    device bf16 [T][H], 16-byte aligned; residual, out bf16 [T][H]
  *   workspace device, >= moe_shared_fp8_workspace_size(up, T) bytes,
- *             256-byte aligned (no zeroing needed)
- * Tokens run in chunks of 8 (the MMA's columns). Asynchronous on `stream`.
+ *             256-byte aligned (the bf16 intermediate; no zeroing needed)
+ * Tokens run in chunks of 8 (the MMA's columns), two launches per chunk.
+ * Asynchronous on `stream`.
  * Returns NVFP4_ERR_INVALID_ARG / _UNSUPPORTED_SHAPE / _MISALIGNED /
  * _WORKSPACE on bad arguments, before any launch. */
 size_t moe_shared_fp8_workspace_size(const fp8_matrix* up, int32_t T);

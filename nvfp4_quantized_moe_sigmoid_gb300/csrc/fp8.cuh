@@ -10,12 +10,14 @@
 //
 // E4M3 x E4M3 products are exact, so mma.sync m16n8k32 (e4m3 in, FP32
 // accumulate) takes the weight bytes straight from memory: nothing is
-// decoded. A CTA owns one 16-row tile of W; its eight warps split the
-// reduction by 64-k steps (warp w takes steps w, w + 8, ...) and their
-// accumulators are added in warp order. In a step, lane (g, q) loads 16
-// contiguous weight bytes of rows g and g + 8 and the same 16 bytes of the
-// activation row of token g, so the reduction index is permuted alike for
-// both operands. Up to 8 tokens are the MMA's columns.
+// decoded. Two launches per 8 tokens (up, then down). Each CTA first
+// quantises the token rows its GEMV needs into shared memory (warp t: row t,
+// after the RMS norm for the up projection), then owns one 16-row tile of W;
+// its eight warps split the reduction by 64-k steps (warp w takes steps w,
+// w + 8, ...) and their accumulators are added in warp order. In a step,
+// lane (g, q) loads 16 contiguous weight bytes of rows g and g + 8 and the
+// same 16 bytes of the activation row of token g, so the reduction index is
+// permuted alike for both operands. Up to 8 tokens are the MMA's columns.
 #pragma once
 
 #include "quantize.cuh"
@@ -96,14 +98,6 @@ __global__ void __launch_bounds__(256) k_fp8_quantize_rows(const void* x, int64_
     }
 }
 
-// One warp per token row: the unit-weight RMS norm of the pre-normed block
-// (the same arithmetic as the other kernels' norm) into dst.
-__global__ void __launch_bounds__(256) k_fp8_rmsnorm_rows(const uint16_t* src, int T, int K, float eps,
-                                                          uint16_t* dst) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (warp < T) warp_rmsnorm_row(src + (size_t)warp * K, dst + (size_t)warp * K, K, eps);
-}
-
 // D += A(16 x 32, e4m3, row) * B(32 x 8, e4m3, col), FP32 accumulate.
 __device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
@@ -118,39 +112,144 @@ struct Fp8GemvArgs {
     const uint8_t* w;      // [n][K] E4M3
     const float* gw;       // [1] per-tensor scale
     int n, K;              // K % 64 == 0
-    const uint8_t* xq;     // [T][K] E4M3 activation rows
-    const float* gx;       // [T] their scales
+    const uint16_t* src;   // [T][K] bf16 activation rows, quantised per row in the prologue
+    float rms_eps;         // > 0: RMS-normalise the rows first
     int T;                 // <= 8
-    // up: act[t][r] = bf16(relu(u)^2), amax[t] (float bits of the bf16 values)
+    // up: act[t][r] = bf16(relu(u)^2)
     uint16_t* act;
     // down: out[t][r] = bf16(y + residual[t][r]) (residual may be null)
     const uint16_t* residual;
     uint16_t* out;
 };
 
+// 16 bf16 values from shared or global memory (16-byte aligned)
+__device__ __forceinline__ void bf16x16(const uint16_t* p, float (&v)[16]) {
+    const uint4 x = reinterpret_cast<const uint4*>(p)[0], y = reinterpret_cast<const uint4*>(p)[1];
+    const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// A warp's weight steps held in registers at once (K <= 64 * 8 * kF8Steps in
+// one pass; longer rows take several passes).
+constexpr int kF8Steps = 8;
+
+// dynamic shared memory: [T][K] E4M3 rows
 template <int KIND>
 __global__ void __launch_bounds__(kF8Threads) k_fp8_gemv(const Fp8GemvArgs a) {
-    extern __shared__ __align__(16) uint8_t f8_smem[];  // [T][K] activation bytes
+    extern __shared__ __align__(16) uint8_t f8_smem[];
     __shared__ float4 part[kF8Warps][32];
+    __shared__ float gx_s[kF8MaxT], inv_s[kF8MaxT];
+    __shared__ float red[2][kF8Warps][kF8MaxT];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     const int K = a.K, T = a.T;
-    for (int i = threadIdx.x; i < T * K / 16; i += kF8Threads)
-        reinterpret_cast<uint4*>(f8_smem)[i] = __ldg(reinterpret_cast<const uint4*>(a.xq) + i);
-    __syncthreads();
     const int r0 = 16 * blockIdx.x;
     const uint8_t* wa = a.w + (size_t)(r0 + g) * K + 16 * q;
     const uint8_t* wb = a.w + (size_t)(r0 + g + 8) * K + 16 * q;
+    const int steps = K >> 6;
+    // the first pass of weight loads is issued before the activation rows are
+    // prepared: the weights do not depend on them
+    uint4 ua[kF8Steps], ub[kF8Steps];
+#pragma unroll
+    for (int i = 0; i < kF8Steps; ++i) {
+        const int s = warp + kF8Warps * i;
+        if (s < steps) {
+            ua[i] = __ldg(reinterpret_cast<const uint4*>(wa + 64 * s));
+            ub[i] = __ldg(reinterpret_cast<const uint4*>(wb + 64 * s));
+        }
+    }
+    // token rows -> E4M3 in shared memory, all threads on all rows at once:
+    // per row the sum of squares and the amax (in warp order), then (the RMS
+    // norm: y = bf16(x inv), whose amax is bf16(amax(x) inv) as rounding is
+    // monotonic) the row scale and the codes
+    const bool norm = a.rms_eps > 0.0f;
+    const int nb = K / 16;
+    {
+        float ss[kF8MaxT], mx[kF8MaxT];
+#pragma unroll
+        for (int t = 0; t < kF8MaxT; ++t) ss[t] = mx[t] = 0.0f;
+        for (int b = threadIdx.x; b < nb; b += kF8Threads) {
+#pragma unroll
+            for (int t = 0; t < kF8MaxT; ++t) {
+                if (t >= T) break;
+                float v[16];
+                bf16x16(a.src + (size_t)t * K + 16 * b, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    ss[t] = __fmaf_rn(v[i], v[i], ss[t]);
+                    mx[t] = fmaxf(mx[t], fabsf(v[i]));
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kF8MaxT; ++t) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                ss[t] = __fadd_rn(ss[t], __shfl_xor_sync(0xffffffffu, ss[t], o));
+                mx[t] = fmaxf(mx[t], __shfl_xor_sync(0xffffffffu, mx[t], o));
+            }
+            if (lane == 0) {
+                red[0][warp][t] = ss[t];
+                red[1][warp][t] = mx[t];
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+        const int t = threadIdx.x;
+        float ss = 0.0f, m = 0.0f;
+        for (int w = 0; w < kF8Warps; ++w) {  // in warp order
+            ss = __fadd_rn(ss, red[0][w][t]);
+            m = fmaxf(m, red[1][w][t]);
+        }
+        const float inv = norm ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), a.rms_eps)))
+                               : 1.0f;
+        const float amax = norm ? __bfloat162float(__float2bfloat16_rn(__fmul_rn(m, inv))) : m;
+        inv_s[t] = inv;
+        gx_s[t] = __fdiv_rn(amax, 448.0f);
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < nb; b += kF8Threads) {
+#pragma unroll
+        for (int t = 0; t < kF8MaxT; ++t) {
+            if (t >= T) break;
+            float v[16];
+            bf16x16(a.src + (size_t)t * K + 16 * b, v);
+            if (norm) {
+                const float inv = inv_s[t];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(v[i], inv)));
+            }
+            reinterpret_cast<uint4*>(f8_smem + (size_t)t * K)[b] = fp8_block16(v, gx_s[t]);
+        }
+    }
+    __syncthreads();
     const uint8_t* xb = g < T ? f8_smem + (size_t)g * K + 16 * q : nullptr;
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const int steps = K >> 6;
-#pragma unroll 2
-    for (int s = warp; s < steps; s += kF8Warps) {
-        const uint4 ua = __ldg(reinterpret_cast<const uint4*>(wa + 64 * s));
-        const uint4 ub = __ldg(reinterpret_cast<const uint4*>(wb + 64 * s));
-        const uint4 bx = xb ? *reinterpret_cast<const uint4*>(xb + 64 * s) : make_uint4(0, 0, 0, 0);
-        mma_e4m3_16832(acc, ua.x, ub.x, ua.y, ub.y, bx.x, bx.y);
-        mma_e4m3_16832(acc, ua.z, ub.z, ua.w, ub.w, bx.z, bx.w);
+    for (int p0 = 0; p0 < steps; p0 += kF8Warps * kF8Steps) {
+        if (p0 > 0) {  // the next pass of weight loads
+#pragma unroll
+            for (int i = 0; i < kF8Steps; ++i) {
+                const int s = p0 + warp + kF8Warps * i;
+                if (s < steps) {
+                    ua[i] = __ldg(reinterpret_cast<const uint4*>(wa + 64 * s));
+                    ub[i] = __ldg(reinterpret_cast<const uint4*>(wb + 64 * s));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kF8Steps; ++i) {
+            const int s = p0 + warp + kF8Warps * i;
+            if (s < steps) {
+                const uint4 bx = xb ? *reinterpret_cast<const uint4*>(xb + 64 * s) : make_uint4(0, 0, 0, 0);
+                mma_e4m3_16832(acc, ua[i].x, ub[i].x, ua[i].y, ub[i].y, bx.x, bx.y);
+                mma_e4m3_16832(acc, ua[i].z, ub[i].z, ua[i].w, ub[i].w, bx.z, bx.w);
+            }
+        }
     }
     part[warp][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     __syncthreads();
@@ -169,7 +268,7 @@ __global__ void __launch_bounds__(kF8Threads) k_fp8_gemv(const Fp8GemvArgs a) {
     for (int v = 0; v < 4; ++v) {
         const int t = 2 * q + (v & 1), r = r0 + g + 8 * (v >> 1);
         if (t >= T) continue;
-        const float y = __fmul_rn(__fmul_rn(d[v], gw), __ldg(a.gx + t));
+        const float y = __fmul_rn(__fmul_rn(d[v], gw), gx_s[t]);
         if (KIND == kGroupedUp) {
             const float rl = fmaxf(y, 0.0f);
             const __nv_bfloat16 b = __float2bfloat16_rn(__fmul_rn(rl, rl));

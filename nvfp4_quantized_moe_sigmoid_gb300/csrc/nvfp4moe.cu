@@ -1538,25 +1538,15 @@ extern "C" nvfp4_status nvfp4_workspace_view(int32_t call, const moe_layer_weigh
 namespace {
 
 struct Fp8WsOffsets {
-    size_t xn, qx, gx, act, qa, ga, total;
+    size_t act, total;
 };
 
 Fp8WsOffsets fp8_ws(int T, int H, int S) {
+    (void)H;
     Fp8WsOffsets o{};
-    size_t off = 0;
-    auto take = [&](size_t bytes) {
-        const size_t at = off;
-        off += align256(bytes);
-        return at;
-    };
     const int tc = std::min(T, kF8MaxT);  // tokens per chunk
-    o.xn = take((size_t)tc * H * 2);
-    o.qx = take((size_t)tc * H);
-    o.gx = take((size_t)tc * 4);
-    o.act = take((size_t)tc * S * 2);
-    o.qa = take((size_t)tc * S);
-    o.ga = take((size_t)tc * 4);
-    o.total = off;
+    o.act = 0;
+    o.total = align256((size_t)tc * S * 2);
     return o;
 }
 
@@ -1625,43 +1615,29 @@ extern "C" nvfp4_status moe_shared_fp8_forward(const fp8_matrix* up, const fp8_m
         return NVFP4_ERR_MISALIGNED;
     const Fp8WsOffsets o = fp8_ws(T, static_cast<int>(H), static_cast<int>(S));
     if (workspace_bytes < o.total) return NVFP4_ERR_WORKSPACE;
-    const size_t smem = (size_t)kF8MaxT * std::max(H, S);
-    if ((int64_t)smem > dyn_smem_limit(k_fp8_gemv<kGroupedUp>) || (int64_t)smem > dyn_smem_limit(k_fp8_gemv<kGroupedDown>))
+    const size_t smem_up = (size_t)kF8MaxT * H, smem_dn = (size_t)kF8MaxT * S;
+    if ((int64_t)smem_up > dyn_smem_limit(k_fp8_gemv<kGroupedUp>) ||
+        (int64_t)smem_dn > dyn_smem_limit(k_fp8_gemv<kGroupedDown>))
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    uint16_t* xn = reinterpret_cast<uint16_t*>(ws + o.xn);
-    uint8_t* qx = ws + o.qx;
-    float* gx = reinterpret_cast<float*>(ws + o.gx);
-    uint16_t* act = reinterpret_cast<uint16_t*>(ws + o.act);
-    uint8_t* qa = ws + o.qa;
-    float* ga = reinterpret_cast<float*>(ws + o.ga);
+    uint16_t* act = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + o.act);
     for (int t0 = 0; t0 < T; t0 += kF8MaxT) {  // chunks of up to 8 tokens: the MMA's columns
         const int tc = std::min(kF8MaxT, T - t0);
-        const uint16_t* h = static_cast<const uint16_t*>(hidden) + (size_t)t0 * H;
-        const uint16_t* xin = h;
-        if (rms_eps > 0.0f) {
-            k_fp8_rmsnorm_rows<<<(tc + 7) / 8, 256, 0, stream>>>(h, tc, static_cast<int>(H), rms_eps, xn);
-            xin = xn;
-        }
-        k_fp8_quantize_rows<true><<<(tc + 7) / 8, 256, 0, stream>>>(xin, tc, H, gx, qx);
         Fp8GemvArgs ua{};
         ua.w = up->codes;
         ua.gw = up->global_scale;
         ua.n = static_cast<int>(S);
         ua.K = static_cast<int>(H);
-        ua.xq = qx;
-        ua.gx = gx;
+        ua.src = static_cast<const uint16_t*>(hidden) + (size_t)t0 * H;
+        ua.rms_eps = rms_eps;
         ua.T = tc;
         ua.act = act;
         k_fp8_gemv<kGroupedUp><<<static_cast<int>(S / 16), kF8Threads, (size_t)tc * H, stream>>>(ua);
-        k_fp8_quantize_rows<true><<<(tc + 7) / 8, 256, 0, stream>>>(act, tc, S, ga, qa);
         Fp8GemvArgs da{};
         da.w = down->codes;
         da.gw = down->global_scale;
         da.n = static_cast<int>(H);
         da.K = static_cast<int>(S);
-        da.xq = qa;
-        da.gx = ga;
+        da.src = act;
         da.T = tc;
         da.residual = residual ? static_cast<const uint16_t*>(residual) + (size_t)t0 * H : nullptr;
         da.out = static_cast<uint16_t*>(out) + (size_t)t0 * H;
