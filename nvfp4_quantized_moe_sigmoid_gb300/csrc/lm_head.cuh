@@ -3,11 +3,13 @@
 // matrix read once per step; "nemotron35-w4a4-v13" card, precision table:
 // lm_head NVFP4 weight-only W4A16).
 //
-// A pure HBM stream of the weight matrix: persistent CTAs each take a
-// contiguous range of 16-row tiles; one producer thread stages them with bulk
-// TMA copies (the first ring-full before waiting on the previous kernel),
-// eight warp pairs run the tensor-core tile with up to 8 token columns
-// (bf16 activations, RMS-normalised when asked, converted once per CTA to f16).
+// A pure HBM stream of the weight matrix: persistent CTAs, two per SM, each
+// take a contiguous range of 16-row tiles; one producer thread stages them
+// with bulk TMA copies (the first ring-full before waiting on the previous
+// kernel), the twelve consumer warps run the tensor-core tile with up to 8
+// token columns (bf16 activations, RMS-normalised when asked, converted once
+// per CTA to f16). The FP4 -> f16 conversion, not the copy, sets the pace, so
+// two CTAs per SM give it more warps.
 #pragma once
 
 #include "gemv_tile.cuh"
@@ -15,6 +17,7 @@
 namespace nvfp4moe {
 
 constexpr int kLmMaxT = 8;
+constexpr int kLmStaticSmem = 12288;  // the kernel's static shared memory, rounded up
 
 struct LmArgs {
     const uint8_t* codes;   // [V][H/2]
@@ -30,7 +33,7 @@ struct LmArgs {
     int ring_bytes;          // shared memory for the staging ring; B rows follow it
 };
 
-__global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) k_lm_head(const LmArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Ring ring;
     __shared__ const uint16_t* srcs[kLmMaxT];
@@ -49,7 +52,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lm_head(const LmArgs a) {
     const int n = static_cast<int>(ie - ib);
     uint8_t* ring_base = smem;
     __half* xb = reinterpret_cast<__half*>(smem + a.ring_bytes);             // [T][H] f16
-    uint16_t* xn = reinterpret_cast<uint16_t*>(xb + (size_t)kLmMaxT * a.H);  // [T][H] bf16
+    uint16_t* xn = reinterpret_cast<uint16_t*>(xb + (size_t)a.T * a.H);  // [T][H] bf16
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {

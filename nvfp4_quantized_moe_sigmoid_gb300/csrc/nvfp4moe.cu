@@ -453,14 +453,20 @@ nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, 
     la.H = H;
     la.ld = w->n;
     la.rms_eps = rms_eps;
-    const int lim = dyn_smem_limit(k_lm_head);
-    const int bbytes = 2 * kLmMaxT * H * 2;  // f16 B rows + normalised bf16 rows
+    // two CTAs per SM (24 decoding warps) when half of the SM's shared
+    // memory (less the static part and the per-CTA reserve) still holds three
+    // stages besides the token rows, else one
+    const int bbytes = 2 * std::min(T, kLmMaxT) * H * 2;  // f16 B rows + normalised bf16 rows
     const int stage = 9 * H;
+    const int lim1 = dyn_smem_limit(k_lm_head);
+    const int lim2 = std::min(lim1, smem_optin() / 2 - kLmStaticSmem - 1024);
+    const bool two = lim2 - bbytes >= 3 * stage;
+    const int lim = two ? lim2 : lim1;
     la.ring_bytes = std::min(kMaxStages * stage, ((lim - bbytes) / 128) * 128);
     if (la.ring_bytes < 2 * stage) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     const int smem = la.ring_bytes + bbytes;
     const int64_t tiles = w->n / 16;
-    const int grid = static_cast<int>(std::min<int64_t>(num_sms(), tiles));
+    const int grid = static_cast<int>(std::min<int64_t>((two ? 2 : 1) * num_sms(), tiles));
     for (int t0 = 0; t0 < T; t0 += kLmMaxT) {
         la.T = std::min(kLmMaxT, T - t0);
         la.hidden = static_cast<const uint16_t*>(hidden) + (size_t)t0 * H;
