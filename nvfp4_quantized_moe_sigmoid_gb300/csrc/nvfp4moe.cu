@@ -69,28 +69,62 @@ int smem_optin() {
     return cache[d];
 }
 
+// Unique id of the calling thread's current CUDA context (never reused
+// within the process), from the driver; 0 if the driver does not provide it.
+unsigned long long current_context_id() {
+    using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+    using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 // Largest dynamic shared memory a kernel may use (opt-in limit minus its
 // static shared memory); raises the kernel's limit to that value once per
-// (kernel, device). Kernels are told apart by address: template instances
-// with one signature share a type.
+// (kernel, device, context): a kernel's attributes belong to the module
+// loaded in one context. Kernels are told apart by address: template
+// instances with one signature share a type.
 int dyn_smem_limit(const void* kernel) {
     struct Entry {
         const void* fn;
+        unsigned long long ctx;
         int dev, lim;
     };
     static Entry table[256];
     static int used = 0;
     static std::mutex mu;
     const int d = current_device();
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < used; ++i)
-        if (table[i].fn == kernel && table[i].dev == d) return table[i].lim;
+    if (ctx != 0)
+        for (int i = 0; i < used; ++i)
+            if (table[i].fn == kernel && table[i].dev == d && table[i].ctx == ctx) return table[i].lim;
     cudaFuncAttributes at;
     if (cudaFuncGetAttributes(&at, kernel) != cudaSuccess) return 0;
     const int lim = smem_optin() - static_cast<int>(at.sharedSizeBytes) - 64;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim) != cudaSuccess)
         return 0;
-    if (used < 256) table[used++] = Entry{kernel, d, lim};
+    if (ctx != 0) {
+        if (used < 256) table[used++] = Entry{kernel, ctx, d, lim};
+        else table[ctx % 256] = Entry{kernel, ctx, d, lim};
+    }
     return lim;
 }
 
@@ -1005,33 +1039,6 @@ extern "C" nvfp4_status moe_layer_forward(const moe_layer_weights* w, const floa
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NVFP4MOE_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-
-// Unique id of the calling thread's current CUDA context (never reused
-// within the process), from the driver; 0 if the driver does not provide it.
-unsigned long long current_context_id() {
-    using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-    using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-    static CtxGetCurrentFn get_current = nullptr;
-    static CtxGetIdFn get_id = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
-        p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            get_id = reinterpret_cast<CtxGetIdFn>(p);
-    });
-    CUcontext ctx = nullptr;
-    unsigned long long id = 0;
-    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
-        get_id(ctx, &id) != CUDA_SUCCESS)
-        return 0;
-    return id;
-}
 
 // Device address of g_noalloc_scratch in the current context. In host code
 // the symbol is only a host-side handle; its device address is looked up with
