@@ -126,3 +126,44 @@ def test_free_running_graph(nm, stack):
     torch.cuda.synchronize()
     assert_close(bf16_to_f64(bf16_bits(out)), bf16_to_f64(bf16_bits(first[0])), "layer 0: layer call vs stack")
     assert nm.nvfp4_last_device_error() == 0
+
+
+def test_concurrent_256_step_teacher_forced(nm, stack):
+    """The 256-token concurrent step as the benchmark runs it (23 W4A4 layers
+    on the grouped tensor-core path, then the lm_head GEMM), one free-running
+    step on the GPU; the oracle, teacher-forced on the GPU's own h_l, checks
+    the routing and h_{l+1} of 4 sampled tokens in every layer, and the
+    logits of those tokens at sampled vocabulary rows."""
+    from nvfp4_quantized_moe_sigmoid_gb300.model import MoEDecodeStack
+    c0, st4 = stack
+    c = configs.shape(4)
+    T, L = c["T"], c["layers"]
+    st = MoEDecodeStack(L, c["E"], c["H"], c["I"], c["S"], c["K"], T, w4a4=True, V=c["V"], weights_from=st4,
+                        rms_eps=c["rms_eps"])
+    st.make_workspace()
+    assert st.path == "split"
+    h0 = gen.hidden_bf16(T, c["H"], c["seed"], layer=configs.HIDDEN_LAYER, rho=c["rho"])
+    st.h[0].copy_(to_dev_bf16(h0))
+    st.step()
+    torch.cuda.synchronize()
+    assert nm.nvfp4_last_device_error() == 0
+    hs = bf16_bits(st.h)  # [L + 1][T][H]
+    idx, w = st.topk_idx.cpu().numpy(), st.topk_w.cpu().numpy()
+    tok = np.array([0, 1, 131, 255])
+    exempt = 0
+    for l in range(L):
+        OL = OracleLayer(c["seed"], l, c["H"], c["I"], c["S"], c["E"], c["bias"])
+        ref, _, r = OL.forward(hs[l][tok], c["K"], True, True, rms_eps=c["rms_eps"])
+        e = check_routing(idx[l][tok], w[l][tok], r, c["K"])
+        exempt += e
+        if e == 0:
+            assert_close(bf16_to_f64(hs[l + 1][tok]), bf16_to_f64(ref), f"layer {l}")
+    assert exempt <= 1
+    V, H = c["V"], c["H"]
+    rows = np.unique(np.concatenate([np.arange(16), np.random.default_rng(3).integers(0, V, 256)]))
+    host = gen.lm_head_master(c["seed"], V, H)
+    g = np.float32(np.abs(gen.bf16_bits_to_f32(host)).max()) / np.float32(2688.0)
+    cc, ss, _ = orc.quantize(host[rows], orc.GIVEN, g=float(g))
+    hn = orc.rms_norm(hs[L][tok], c["rms_eps"])
+    logits = st.logits.cpu().numpy()[tok][:, rows]
+    assert_close(logits, orc.lm_head(orc.Mat(cc, ss, g), hn), "logits")
