@@ -65,13 +65,16 @@ def parse():
 
 
 # ------------------------------------------------------------------ dist
-def dist_init():
+# N > 1: one process per GPU, each an independent replica of the step (the
+# path does not shard on one GPU's worth of work: no data-path collective);
+# the process group carries only the timing barrier and the max over ranks.
+def dist_init(backend=None):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        dist.init_process_group(backend or os.environ.get("NVFP4MOE_DIST_BACKEND", "nccl"))
     return ws, rank, local
 
 
@@ -86,9 +89,16 @@ def max_over_ranks(x, ws):
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_us_per_token(ms_slowest_rank, steps, T, ws):
+    """µs per token of the whole job: ws replicas each ran T tokens per step,
+    timed by the slowest rank."""
+    return ms_slowest_rank / steps * 1e3 / (T * ws)
 
 
 # ------------------------------------------------------------------ clocks
@@ -481,7 +491,7 @@ def run_ours(args, ws, rank, local):
         barrier(ws)
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), ws)
     ms_step = ms_total / args.steps
-    us_token = ms_step * 1e3 / (T * ws)  # whole job: ws replicas each ran T tokens per step
+    us_token = whole_job_us_per_token(ms_total, args.steps, T, ws)
     step_b = rf.step_bytes(T, uniques, E, H, I, S, K, V if c["lm_head"] else None)
     peak, peak_kind = measured_peaks()
     gbs_step = step_b / (ms_step * 1e-3) / 1e9
