@@ -34,15 +34,22 @@ constexpr int kGThreads = 256;
 // expert e and chunks[e] the first 128-position chunk (tiles[E], chunks[E] =
 // their totals; either is skipped when null). Expert ids outside [0, E) are
 // counted as expert 0 and flagged in the error word.
+//
+// One CTA; warp w owns the contiguous pairs [w seg, (w + 1) seg). Three
+// steps with a barrier after each: every warp counts its pairs per expert;
+// per expert the warps' counts become their first positions (an exclusive
+// prefix over warps, then the experts' offsets by a warp scan); every warp
+// places its pairs in order, 32 at a time (match_any gives each lane its rank
+// among the lanes of its expert, the expert's leader advances the warp's
+// running position). So the order of equal experts is the pair order.
 __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restrict__ idx, int P, int E,
                                                           int32_t* __restrict__ offsets, int32_t* __restrict__ tiles,
                                                           int32_t* __restrict__ chunks, int32_t* __restrict__ perm,
                                                           int32_t* __restrict__ inv) {
-    __shared__ int cnt[256];
-    __shared__ int running[256];
-    __shared__ int wcnt[kPermWarps][256];
+    __shared__ int wpos[kPermWarps][256];  // per warp and expert: its count, then its next position
+    __shared__ int first[256];             // per expert: its first position
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int e = tid; e < E; e += kPermThreads) cnt[e] = 0;
+    for (int i = tid; i < kPermWarps * 256; i += kPermThreads) (&wpos[0][0])[i] = 0;
     __syncthreads();
     auto expert_of = [&](int p) {
         int e = __ldg(idx + p);
@@ -52,28 +59,66 @@ __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restr
         }
         return e;
     };
-    for (int p = tid; p < P; p += kPermThreads) atomicAdd(&cnt[expert_of(p)], 1);
+    const int seg = (P + kPermWarps - 1) / kPermWarps;
+    const int s0 = min(P, warp * seg), s1 = min(P, s0 + seg);
+    for (int p = s0 + lane; p < s1; p += 32) atomicAdd(&wpos[warp][expert_of(p)], 1);
     __syncthreads();
-    if (tid == 0) {
-        int off = 0, toff = 0, coff = 0;
-        for (int e = 0; e < E; ++e) {
-            offsets[e] = off;
-            if (tiles) tiles[e] = toff;
-            if (chunks) chunks[e] = coff;
-            running[e] = off;
-            off += cnt[e];
-            toff += (cnt[e] + kGTile - 1) / kGTile;
-            coff += (cnt[e] + 127) / 128;
+    // per expert: the warps' counts -> their positions relative to the expert's first
+    for (int e = tid; e < E; e += kPermThreads) {
+        int run = 0;
+        for (int w = 0; w < kPermWarps; ++w) {
+            const int c = wpos[w][e];
+            wpos[w][e] = run;
+            run += c;
         }
-        offsets[E] = off;
-        if (tiles) tiles[E] = toff;
-        if (chunks) chunks[E] = coff;
+        first[e] = run;  // the expert's count for now
     }
-    for (int p0 = 0; p0 < P; p0 += kPermThreads) {
-        for (int i = tid; i < kPermWarps * E; i += kPermThreads) (&wcnt[0][0])[(i / E) * 256 + i % E] = 0;
-        __syncthreads();
-        const int p = p0 + tid;
-        const bool valid = p < P;
+    __syncthreads();
+    if (warp == 0) {  // offsets, tiles, chunks: exclusive scans over the experts, 8 per lane
+        int cnt[8], ls = 0, lt = 0, lc = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = 8 * lane + i;
+            cnt[i] = e < E ? first[e] : 0;
+            ls += cnt[i];
+            lt += (cnt[i] + kGTile - 1) / kGTile;
+            lc += (cnt[i] + 127) / 128;
+        }
+        int xs = ls, xt = lt, xc = lc;  // inclusive warp scans
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, xs, o), b = __shfl_up_sync(0xffffffffu, xt, o),
+                      d = __shfl_up_sync(0xffffffffu, xc, o);
+            if (lane >= o) {
+                xs += a;
+                xt += b;
+                xc += d;
+            }
+        }
+        int off = xs - ls, toff = xt - lt, coff = xc - lc;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = 8 * lane + i;
+            if (e < E) {
+                offsets[e] = off;
+                if (tiles) tiles[e] = toff;
+                if (chunks) chunks[e] = coff;
+                first[e] = off;
+            }
+            off += cnt[i];
+            toff += (cnt[i] + kGTile - 1) / kGTile;
+            coff += (cnt[i] + 127) / 128;
+        }
+        if (lane == 31) {
+            offsets[E] = off;
+            if (tiles) tiles[E] = toff;
+            if (chunks) chunks[E] = coff;
+        }
+    }
+    __syncthreads();
+    for (int p0 = s0; p0 < s1; p0 += 32) {
+        const int p = p0 + lane;
+        const bool valid = p < s1;
         const int e = valid ? expert_of(p) : -1;
         const unsigned act = __ballot_sync(0xffffffffu, valid);
         unsigned peers = 0;
@@ -81,26 +126,13 @@ __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restr
         if (valid) {
             peers = __match_any_sync(act, e);
             lrank = __popc(peers & ((1u << lane) - 1u));
-            if (lrank == 0) wcnt[warp][e] = __popc(peers);
-        }
-        __syncthreads();
-        // per expert: exclusive prefix over warps, then advance the running offset
-        for (int ee = tid; ee < E; ee += kPermThreads) {
-            int run = running[ee];
-            for (int w = 0; w < kPermWarps; ++w) {
-                const int c = wcnt[w][ee];
-                wcnt[w][ee] = run;
-                run += c;
-            }
-            running[ee] = run;
-        }
-        __syncthreads();
-        if (valid) {
-            const int pos = wcnt[warp][e] + lrank;
+            const int pos = first[e] + wpos[warp][e] + lrank;
             perm[pos] = p;
             inv[p] = pos;
         }
-        __syncthreads();
+        __syncwarp();
+        if (valid && lrank == 0) wpos[warp][e] += __popc(peers);
+        __syncwarp();
     }
 }
 
