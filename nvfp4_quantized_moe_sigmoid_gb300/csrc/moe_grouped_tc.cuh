@@ -260,10 +260,32 @@ __device__ __forceinline__ int tc_seg_items(const TcSeg& s, const int* chk) {
 
 // Item i: m-major inside a chunk of positions, so that consecutive items (on
 // neighbouring CTAs at about the same time) share their B rows in L2.
-__device__ __forceinline__ TcItem tc_item(const TcSeg* segs, const TcTab& tab, int i, int items0) {
+// Work item i of the launch goes to CTA i % G. The second segment's items
+// (the shared expert: all tokens, so the widest, up to 128 positions) take
+// the slots [r0, r0 + n1) of the order, r0 = total % G, so that they land on
+// CTAs that get one item fewer than the others; the first segment's items
+// fill the rest in their order. (When they do not fit there, the segments
+// stay in order.)
+struct TcOrder {
+    int items0, n1, r0;
+};
+__device__ __forceinline__ TcOrder tc_order(int items0, int total, int G) {
+    TcOrder o;
+    o.items0 = items0;
+    o.n1 = total - items0;
+    o.r0 = total % G;
+    if (o.n1 > G - o.r0 || o.r0 + o.n1 > total) o.r0 = items0;  // the segments in order
+    return o;
+}
+__device__ __forceinline__ TcItem tc_item(const TcSeg* segs, const TcTab& tab, int i, const TcOrder& ord) {
     TcItem it;
-    it.seg = i < items0 ? 0 : 1;
-    if (it.seg) i -= items0;
+    if (i >= ord.r0 && i < ord.r0 + ord.n1) {
+        it.seg = 1;
+        i -= ord.r0;
+    } else {
+        it.seg = 0;
+        if (i >= ord.r0 + ord.n1) i -= ord.n1;
+    }
     const TcSeg& s = segs[it.seg];
     const int MT = (s.M + kTcRows - 1) / kTcRows;
     const int ch = i / MT;
@@ -345,6 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
     volatile int* ab = &abort_s;
     const int items0 = tc_seg_items(segs[0], tab.chk[0]);
     const int total = items0 + (a.nseg > 1 ? tc_seg_items(segs[1], tab.chk[1]) : 0);
+    const TcOrder ord = tc_order(items0, total, gridDim.x);
 
     if (warp == 0) {
         // ---- producer
@@ -363,7 +386,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
         __syncwarp();
         bool ok = true;
         for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
-            const TcItem it = tc_item(segs, tab, i, items0);
+            const TcItem it = tc_item(segs, tab, i, ord);
             const TcSeg& s = segs[it.seg];
             const int nstage = ((s.K >> 6) + 3) >> 2, ng = (it.n + 31) >> 5;
             const int arow0 = it.e * s.M + it.mt * kTcRows;
@@ -448,7 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
             int g = 0, n_it = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
-                const TcItem it = tc_item(segs, tab, i, items0);
+                const TcItem it = tc_item(segs, tab, i, ord);
                 const TcSeg& s = segs[it.seg];
                 const int nks = s.K >> 6, nstage = (nks + 3) >> 2, ng = (it.n + 31) >> 5;
                 const int db = n_it & 1;
@@ -493,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
         int g = 0, n_it = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++n_it) {
-            const TcItem it = tc_item(segs, tab, i, items0);
+            const TcItem it = tc_item(segs, tab, i, ord);
             const TcSeg& s = segs[it.seg];
             const int nstage = ((s.K >> 6) + 3) >> 2, ng = (it.n + 31) >> 5;
             const int sp = s.K >> 4;
@@ -547,7 +570,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
         const uint32_t lb = (uint32_t)(32 * q) << 16;
         int n_it = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ++n_it) {
-            const TcItem it = tc_item(segs, tab, i, items0);
+            const TcItem it = tc_item(segs, tab, i, ord);
             const TcSeg& s = segs[it.seg];
             const int db = n_it & 1;
             bool w = true;
