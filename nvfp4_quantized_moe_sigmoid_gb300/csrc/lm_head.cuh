@@ -3,8 +3,10 @@
 // matrix read once per step; "nemotron35-w4a4-v13" card, precision table:
 // lm_head NVFP4 weight-only W4A16).
 //
-// A pure HBM stream of the weight matrix: persistent CTAs, two per SM, each
-// take a contiguous range of 16-row tiles; one producer thread stages them
+// A pure HBM stream of the weight matrix: persistent CTAs (two per SM when
+// half an SM's shared memory holds three stages besides the token rows: one
+// or two tokens at the pages' width) each take a contiguous range of 16-row
+// tiles; one producer thread stages them
 // with bulk TMA copies (the first ring-full before waiting on the previous
 // kernel), the twelve consumer warps run the tensor-core tile with up to 8
 // token columns (bf16 activations, RMS-normalised when asked, converted once
