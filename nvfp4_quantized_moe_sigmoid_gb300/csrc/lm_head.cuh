@@ -6,12 +6,12 @@
 // A pure HBM stream of the weight matrix: persistent CTAs (two per SM when
 // half an SM's shared memory holds three stages besides the token rows: one
 // or two tokens at the pages' width) each take a contiguous range of 16-row
-// tiles; one producer thread stages them
-// with bulk TMA copies (the first ring-full before waiting on the previous
-// kernel), the twelve consumer warps run the tensor-core tile with up to 8
-// token columns (bf16 activations, RMS-normalised when asked, converted once
-// per CTA to f16). The FP4 -> f16 conversion, not the copy, sets the pace, so
-// two CTAs per SM give it more warps.
+// tiles; one producer thread stages them with bulk TMA copies (the first
+// ring-full before waiting on the previous kernel), the twelve consumer warps
+// run the tensor-core tile with up to 8 token columns (bf16 activations,
+// RMS-normalised when asked, converted once per CTA to f16). The FP4 -> f16
+// conversion, not the copy, sets the pace, so two CTAs per SM give it more
+// warps.
 #pragma once
 
 #include "gemv_tile.cuh"
