@@ -110,20 +110,22 @@ __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes
 // ------------------------------------------------------------------ staging
 // A ring of `nstages` shared-memory stages, each holding one 16-row tile
 // (codes then scales), filled by one producer thread with bulk TMA copies.
-// Stage s is owned by the group of consumer warps w with w % nstages == s
-// (16 / nstages warps, rounded): local item li goes to stage li % nstages,
-// whose warps each take a contiguous share of the tile's k-chunks and all
-// release the stage; so every warp is busy whatever the stage count. Every
-// use of a stage is waited on, in order, by the same warps (an mbarrier parity
-// wait names the current or the immediately preceding phase; a waiter for use
-// u must not start while the barrier is still in phase u - 2, which fixed
-// ownership guarantees).
+// The consumer warps are dealt into `groups` groups (warp w in group
+// w % groups; nstages a multiple of groups): local item li goes to stage
+// li % nstages and to group li % groups, whose warps each take a contiguous
+// share of the tile's k-chunks and all release the stage. A group thus owns
+// nstages / groups stages and computes on one while the next ones land.
+// Every use of a stage is waited on, in order, by the same warps (an mbarrier
+// parity wait names the current or the immediately preceding phase; a waiter
+// for use u must not start while the barrier is still in phase u - 2, which
+// fixed ownership guarantees).
 constexpr int kConsumerWarps = 12;
 constexpr int kMaxStages = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 
-__device__ __forceinline__ int group_size(int s, int nstages) { return (kConsumerWarps - s + nstages - 1) / nstages; }
+// Warps of group g when the consumer warps are dealt into `groups` groups (w % groups).
+__device__ __forceinline__ int group_size(int g, int groups) { return (kConsumerWarps - g + groups - 1) / groups; }
 
 struct Ring {
     uint64_t full[kMaxStages];
@@ -131,16 +133,16 @@ struct Ring {
     int uses[kMaxStages];  // producer-side count of fills per stage
     int abort;
     // partial tiles handed from the non-leading warps of a group to its
-    // leader, double-buffered by use parity; warp w >= nstages uses slot
-    // w - nstages
+    // leader, double-buffered by the parity of the group's item count; warp
+    // w >= groups uses slot w - groups
     float4 xred[kConsumerWarps - 1][2][32];
 };
 
-__device__ __forceinline__ void ring_init(Ring& r, int nstages) {
+__device__ __forceinline__ void ring_init(Ring& r, int nstages, int groups) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
             mbar_init(&r.full[s], 1);
-            mbar_init(&r.empty[s], group_size(s, nstages));
+            mbar_init(&r.empty[s], group_size(s % groups, groups));
             r.uses[s] = 0;
         }
         r.abort = 0;
@@ -244,10 +246,10 @@ struct TileOut {
     int lead, ok;
 };
 
-__device__ __noinline__ TileOut group_tile_core(Ring* r, int nstages, int li, const uint8_t* st, int K,
-                                                const __half* bcol) {
+__device__ __noinline__ TileOut group_tile_core(Ring* r, int nstages, int groups, int li, const uint8_t* st,
+                                                int K, const __half* bcol) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int s = warp % nstages, rank = warp / nstages, gs = group_size(s, nstages);
+    const int s = warp % groups, rank = warp / groups, gs = group_size(s, groups);
     const int nc = (K + 127) >> 7;
     const bool got = ring_acquire(*r, nstages, li);
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -260,13 +262,13 @@ __device__ __noinline__ TileOut group_tile_core(Ring* r, int nstages, int li, co
         o.lead = got;
         return o;
     }
-    const int u = static_cast<int>((li / nstages) & 1);
-    if (rank) r->xred[warp - nstages][u][lane] = o.acc;
+    const int u = static_cast<int>((li / groups) & 1);
+    if (rank) r->xred[warp - groups][u][lane] = o.acc;
     o.ok = group_bar_and(s, gs, got);
     o.lead = 0;
     if (rank || !o.ok) return o;
     for (int p = 1; p < gs; ++p) {
-        const float4 x = r->xred[s + p * nstages - nstages][u][lane];
+        const float4 x = r->xred[s + p * groups - groups][u][lane];
         o.acc.x += x.x;
         o.acc.y += x.y;
         o.acc.z += x.z;
@@ -276,9 +278,46 @@ __device__ __noinline__ TileOut group_tile_core(Ring* r, int nstages, int li, co
     return o;
 }
 
-__device__ __forceinline__ bool group_tile(Ring& r, int nstages, int li, const uint8_t* st, int K,
+// The same for a caller that carries the item's stage s, its phase ph, the
+// group's item parity u and this warp's k-chunk share [c0, c1) along instead
+// of deriving them from li (grp, rank, gs: this warp's group, its rank there,
+// the group's size; groups in all).
+__device__ __noinline__ TileOut group_tile_at(Ring* r, int s, uint32_t ph, uint32_t u, int grp, int rank, int gs,
+                                              int groups, const uint8_t* st, int K, const __half* bcol, int c0,
+                                              int c1) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool waited = mbar_wait_bounded(&r->full[s], ph);
+    const bool got = __all_sync(0xffffffffu, waited);
+    if (!got && lane == 0) set_dev_error(kErrWaitFull);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (got) tile_mma_16x8(st, st + 16 * (K >> 1), K, bcol, c0, c1, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&r->empty[s]);
+    TileOut o;
+    o.acc = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    if (gs == 1) {
+        o.ok = got;
+        o.lead = got;
+        return o;
+    }
+    if (rank) r->xred[warp - groups][u][lane] = o.acc;
+    o.ok = group_bar_and(grp, gs, got);
+    o.lead = 0;
+    if (rank || !o.ok) return o;
+    for (int p = 1; p < gs; ++p) {
+        const float4 x = r->xred[grp + p * groups - groups][u][lane];
+        o.acc.x += x.x;
+        o.acc.y += x.y;
+        o.acc.z += x.z;
+        o.acc.w += x.w;
+    }
+    o.lead = 1;
+    return o;
+}
+
+__device__ __forceinline__ bool group_tile(Ring& r, int nstages, int groups, int li, const uint8_t* st, int K,
                                            const __half* bcol, float (&acc)[4], bool& ok) {
-    const TileOut o = group_tile_core(&r, nstages, li, st, K, bcol);
+    const TileOut o = group_tile_core(&r, nstages, groups, li, st, K, bcol);
     acc[0] = o.acc.x;
     acc[1] = o.acc.y;
     acc[2] = o.acc.z;

@@ -33,6 +33,7 @@ struct LmArgs {
     float* logits;           // [T][ld]
     int64_t ld;
     int ring_bytes;          // shared memory for the staging ring; B rows follow it
+    int groups;              // consumer warp groups (a divisor of the stage count)
 };
 
 __global__ void __launch_bounds__(kThreads, 2) k_lm_head(const LmArgs a) {
@@ -45,7 +46,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_lm_head(const LmArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stage_bytes = 9 * a.H;
     const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
-    ring_init(ring, nst);
+    const int ngr = a.groups >= 1 && nst % a.groups == 0 ? a.groups : nst;
+    ring_init(ring, nst, ngr);
     pdl_trigger();
     __syncthreads();
 
@@ -59,13 +61,31 @@ __global__ void __launch_bounds__(kThreads, 2) k_lm_head(const LmArgs a) {
     if (warp == kConsumerWarps) {
         if (lane == 0) {
             // the weights do not depend on the previous kernel: a ring-full is
-            // issued before waiting on it
+            // issued before waiting on it. Stage and phase of item li
+            // (li % nst, li / nst) are carried along, not divided out.
+            const uint32_t cbytes = 16u * (uint32_t)(a.H >> 1), sbytes = 16u * (uint32_t)(a.H >> 4);
+            const uint8_t* cw = a.codes + 16 * ib * (a.H >> 1);
+            const uint8_t* sw = a.scales + 16 * ib * (a.H >> 4);
+            int s = 0;
+            uint32_t ph = 0;
             for (int li = 0; li < n; ++li) {
                 if (li == nst) pdl_wait();
-                const int64_t row = 16 * (ib + li);
-                if (!ring_fill(ring, ring_base, stage_bytes, nst, li, a.codes + row * (a.H >> 1),
-                               a.scales + row * (a.H >> 4), a.H))
+                if (li >= nst && !mbar_wait_bounded(&ring.empty[s], ph ^ 1u)) {
+                    set_dev_error(kErrWaitEmpty);
+                    ring.abort = 1;
                     break;
+                }
+                uint8_t* dst = ring_base + (size_t)s * stage_bytes;
+                mbar_arrive_expect_tx(&ring.full[s], cbytes + sbytes);
+                bulk_g2s(dst, cw, cbytes, &ring.full[s]);
+                bulk_g2s(dst + cbytes, sw, sbytes, &ring.full[s]);
+                ring.uses[s] += 1;
+                cw += cbytes;
+                sw += sbytes;
+                if (++s == nst) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
         pdl_wait();
@@ -83,14 +103,23 @@ __global__ void __launch_bounds__(kThreads, 2) k_lm_head(const LmArgs a) {
         const float gw = __ldg(a.global);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
-        const int s = warp % nst;
-        for (int li = s; li < n; li += nst) {
-            const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
-            float acc[4];
-            bool ok;
-            const bool mine = group_tile(ring, nst, li, st, a.H, bcol, acc, ok);
-            if (!ok) break;
-            if (!mine) continue;
+        // this warp's group, rank and k-chunk share (the same for every
+        // tile), and the stage / phase of its current item carried along
+        const int grp = warp % ngr, rank = warp / ngr, gs = group_size(grp, ngr);
+        const int nc = (a.H + 127) >> 7, c0 = nc * rank / gs, c1 = nc * (rank + 1) / gs;
+        int s = grp;
+        uint32_t ph = 0, u = 0;
+        for (int li = grp; li < n; li += ngr) {
+            const TileOut o = group_tile_at(&ring, s, ph, u, grp, rank, gs, ngr, ring_base + (size_t)s * stage_bytes,
+                                            a.H, bcol, c0, c1);
+            if ((s += ngr) >= nst) {
+                s -= nst;
+                ph ^= 1u;
+            }
+            u ^= 1u;
+            if (!o.ok) break;
+            if (!o.lead) continue;
+            const float acc[4] = {o.acc.x, o.acc.y, o.acc.z, o.acc.w};
             const int64_t row0 = 16 * (ib + li);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_up_decode(const UpArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stage_bytes = 9 * a.H;  // 16 rows x (H/2 code bytes + H/16 scale bytes)
     const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
-    ring_init(ring, nst);
+    ring_init(ring, nst, nst);
     pdl_trigger();
     __syncthreads();
 
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_up_decode(const UpArgs a) {
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = group_tile(ring, nst, li, st, a.H, bcol, acc, ok);
+            const bool mine = group_tile(ring, nst, nst, li, st, a.H, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const bool routed = li >= n_sh;
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
     const int kmax = n_sh > 0 ? max(a.I, a.S) : a.I;
     const int stage_bytes = 9 * kmax;
     const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
-    ring_init(ring, nst);
+    ring_init(ring, nst, nst);
     pdl_trigger();
     __syncthreads();
 
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down_decode(const DownArgs 
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = group_tile(ring, nst, li, st, K, bcol, acc, ok);
+            const bool mine = group_tile(ring, nst, nst, li, st, K, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const float gw = routed ? __ldg(a.global + plan.expert[u]) : __ldg(a.sh_global);

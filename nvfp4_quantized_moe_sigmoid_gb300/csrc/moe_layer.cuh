@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_up(const LayerUpArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stage_bytes = 9 * a.H;
     const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
-    ring_init(ring, nst);
+    ring_init(ring, nst, nst);
     if (threadIdx.x == 0) mbar_init(&bbar, 1);
     pdl_trigger();
     __syncthreads();
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_up(const LayerUpArgs a) {
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = group_tile(ring, nst, li, st, a.H, bcol, acc, ok);
+            const bool mine = group_tile(ring, nst, nst, li, st, a.H, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const bool routed = li >= n_sh;
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_down(const LayerDownArgs 
     const int kmax = n_sh > 0 ? max(a.I, a.S) : a.I;
     const int stage_bytes = 9 * kmax;
     const int nst = min(kMaxStages, a.ring_bytes / stage_bytes);
-    ring_init(ring, nst);
+    ring_init(ring, nst, nst);
     if (threadIdx.x == 0) mbar_init(&bbar, 1);
     pdl_trigger();
     __syncthreads();
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_down(const LayerDownArgs 
             const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = group_tile(ring, nst, li, st, K, bcol, acc, ok);
+            const bool mine = group_tile(ring, nst, nst, li, st, K, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const float gw = routed ? __ldg(a.global + plan.expert[u]) : __ldg(a.sh_global);

@@ -498,6 +498,7 @@ nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, 
     const int lim = two ? lim2 : lim1;
     la.ring_bytes = std::min(kMaxStages * stage, ((lim - bbytes) / 128) * 128);
     if (la.ring_bytes < 2 * stage) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    la.groups = std::min(kMaxStages, la.ring_bytes / stage);
     const int smem = la.ring_bytes + bbytes;
     const int64_t tiles = w->n / 16;
     const int grid = static_cast<int>(std::min<int64_t>((two ? 2 : 1) * num_sms(), tiles));
