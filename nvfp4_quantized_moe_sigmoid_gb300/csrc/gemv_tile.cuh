@@ -150,12 +150,24 @@ __device__ __forceinline__ void ring_init(Ring& r, int nstages, int groups) {
     }
 }
 
-// Producer side: fill the stage of local item li with a 16-row tile.
+// Producer side. The position of the next local item li is carried from one
+// item to the next (stage li % nstages, phase (li / nstages) & 1), so that no
+// item divides by the run-time stage count.
+struct FillCursor {
+    int li, s;
+    uint32_t ph;
+};
+
+__device__ __forceinline__ FillCursor fill_cursor(int li, int nstages) {
+    return FillCursor{li, li % nstages, static_cast<uint32_t>((li / nstages) & 1)};
+}
+
+// Fill the stage of item f.li with a 16-row tile and move f to the next item.
 // Returns false (and flags the ring) if the stage never became free.
-__device__ __forceinline__ bool ring_fill(Ring& r, uint8_t* ring_base, int stage_bytes, int nstages,
-                                          int li, const uint8_t* codes, const uint8_t* scales, int K) {
-    const int s = static_cast<int>(li % nstages);
-    if (li >= nstages && !mbar_wait_bounded(&r.empty[s], static_cast<uint32_t>(((li / nstages) - 1) & 1))) {
+__device__ __forceinline__ bool ring_fill(Ring& r, uint8_t* ring_base, int stage_bytes, int nstages, FillCursor& f,
+                                          const uint8_t* codes, const uint8_t* scales, int K) {
+    const int s = f.s;
+    if (f.li >= nstages && !mbar_wait_bounded(&r.empty[s], f.ph ^ 1u)) {
         set_dev_error(kErrWaitEmpty);
         r.abort = 1;
         return false;
@@ -166,21 +178,12 @@ __device__ __forceinline__ bool ring_fill(Ring& r, uint8_t* ring_base, int stage
     bulk_g2s(dst, codes, cbytes, &r.full[s]);
     bulk_g2s(dst + cbytes, scales, sbytes, &r.full[s]);
     r.uses[s] += 1;
+    ++f.li;
+    if (++f.s == nstages) {
+        f.s = 0;
+        f.ph ^= 1u;
+    }
     return true;
-}
-
-// Consumer side (whole warp): wait for local item li. False on timeout.
-__device__ __forceinline__ bool ring_acquire(Ring& r, int nstages, int li) {
-    const int s = static_cast<int>(li % nstages);
-    const bool ok = mbar_wait_bounded(&r.full[s], static_cast<uint32_t>((li / nstages) & 1));
-    const bool all_ok = __all_sync(0xffffffffu, ok);
-    if (!all_ok && (threadIdx.x & 31) == 0) set_dev_error(kErrWaitFull);
-    return all_ok;
-}
-
-__device__ __forceinline__ void ring_release(Ring& r, int nstages, int li) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[li % nstages]);
 }
 
 // After every warp is done (call after __syncthreads): make sure no bulk copy
@@ -234,54 +237,61 @@ __device__ __forceinline__ int first_item(int base, int s, int nstages) {
     return base + ((s - base % nstages) + nstages) % nstages;
 }
 
-// One staged tile, split between the warps of its stage group: rank p of gs
+// One staged tile, split between the warps of its group: rank p of gs
 // computes k-chunks [nc p / gs, nc (p + 1) / gs); the other warps hand their
 // partials to the leader (rank 0), which adds them in rank order. The leader
 // gets lead = 1 and the finished tile in acc; ok = 0 for every warp of the
 // group if any of them timed out waiting. Kept out of line: every kernel calls
 // it from several loops, and one shared copy keeps the instruction footprint
 // small.
+//
+// A consumer warp carries its group's place in the ring from one item to the
+// next: the stage s = li % nstages of the group's current item li, its phase
+// (li / nstages) & 1 and the group's item parity (li / groups) & 1, and its
+// k-chunk share of the (at most two) tile widths the kernel uses, so that no
+// tile divides by a run-time count.
+struct GroupCursor {
+    int li, s, grp, rank, gs, groups, nstages;
+    uint32_t ph, u;
+    int k0, c00, c10, k1, c01, c11;  // widths and this warp's chunk shares of them
+};
+
+__device__ __forceinline__ GroupCursor group_cursor(int nstages, int groups, int K0, int K1) {
+    GroupCursor c;
+    const int warp = threadIdx.x >> 5;
+    c.grp = warp % groups;
+    c.rank = warp / groups;
+    c.gs = group_size(c.grp, groups);
+    c.groups = groups;
+    c.nstages = nstages;
+    c.li = c.grp;
+    c.s = c.grp;
+    c.ph = 0;
+    c.u = 0;
+    const int n0 = (K0 + 127) >> 7, n1 = (K1 + 127) >> 7;
+    c.k0 = K0;
+    c.c00 = n0 * c.rank / c.gs;
+    c.c10 = n0 * (c.rank + 1) / c.gs;
+    c.k1 = K1;
+    c.c01 = n1 * c.rank / c.gs;
+    c.c11 = n1 * (c.rank + 1) / c.gs;
+    return c;
+}
+
+__device__ __forceinline__ void cursor_next(GroupCursor& c) {
+    c.li += c.groups;
+    if ((c.s += c.groups) >= c.nstages) {
+        c.s -= c.nstages;
+        c.ph ^= 1u;
+    }
+    c.u ^= 1u;
+}
+
 struct TileOut {
     float4 acc;
     int lead, ok;
 };
 
-__device__ __noinline__ TileOut group_tile_core(Ring* r, int nstages, int groups, int li, const uint8_t* st,
-                                                int K, const __half* bcol) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int s = warp % groups, rank = warp / groups, gs = group_size(s, groups);
-    const int nc = (K + 127) >> 7;
-    const bool got = ring_acquire(*r, nstages, li);
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (got) tile_mma_16x8(st, st + 16 * (K >> 1), K, bcol, nc * rank / gs, nc * (rank + 1) / gs, acc);
-    ring_release(*r, nstages, li);
-    TileOut o;
-    o.acc = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    if (gs == 1) {
-        o.ok = got;
-        o.lead = got;
-        return o;
-    }
-    const int u = static_cast<int>((li / groups) & 1);
-    if (rank) r->xred[warp - groups][u][lane] = o.acc;
-    o.ok = group_bar_and(s, gs, got);
-    o.lead = 0;
-    if (rank || !o.ok) return o;
-    for (int p = 1; p < gs; ++p) {
-        const float4 x = r->xred[s + p * groups - groups][u][lane];
-        o.acc.x += x.x;
-        o.acc.y += x.y;
-        o.acc.z += x.z;
-        o.acc.w += x.w;
-    }
-    o.lead = 1;
-    return o;
-}
-
-// The same for a caller that carries the item's stage s, its phase ph, the
-// group's item parity u and this warp's k-chunk share [c0, c1) along instead
-// of deriving them from li (grp, rank, gs: this warp's group, its rank there,
-// the group's size; groups in all).
 __device__ __noinline__ TileOut group_tile_at(Ring* r, int s, uint32_t ph, uint32_t u, int grp, int rank, int gs,
                                               int groups, const uint8_t* st, int K, const __half* bcol, int c0,
                                               int c1) {
@@ -315,9 +325,14 @@ __device__ __noinline__ TileOut group_tile_at(Ring* r, int s, uint32_t ph, uint3
     return o;
 }
 
-__device__ __forceinline__ bool group_tile(Ring& r, int nstages, int groups, int li, const uint8_t* st, int K,
+// The group's current item (cursor c, tile width K: one of the two the cursor
+// was made for) into acc; the caller then moves the cursor on.
+__device__ __forceinline__ bool group_tile(Ring& r, const GroupCursor& c, uint8_t* ring_base, int stage_bytes, int K,
                                            const __half* bcol, float (&acc)[4], bool& ok) {
-    const TileOut o = group_tile_core(&r, nstages, groups, li, st, K, bcol);
+    const bool w0 = K == c.k0;
+    const TileOut o = group_tile_at(&r, c.s, c.ph, c.u, c.grp, c.rank, c.gs, c.groups,
+                                    ring_base + (size_t)c.s * stage_bytes, K, bcol, w0 ? c.c00 : c.c01,
+                                    w0 ? c.c10 : c.c11);
     acc[0] = o.acc.x;
     acc[1] = o.acc.y;
     acc[2] = o.acc.z;

@@ -61,31 +61,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_lm_head(const LmArgs a) {
     if (warp == kConsumerWarps) {
         if (lane == 0) {
             // the weights do not depend on the previous kernel: a ring-full is
-            // issued before waiting on it. Stage and phase of item li
-            // (li % nst, li / nst) are carried along, not divided out.
+            // issued before waiting on it
             const uint32_t cbytes = 16u * (uint32_t)(a.H >> 1), sbytes = 16u * (uint32_t)(a.H >> 4);
             const uint8_t* cw = a.codes + 16 * ib * (a.H >> 1);
             const uint8_t* sw = a.scales + 16 * ib * (a.H >> 4);
-            int s = 0;
-            uint32_t ph = 0;
+            FillCursor f = fill_cursor(0, nst);
             for (int li = 0; li < n; ++li) {
                 if (li == nst) pdl_wait();
-                if (li >= nst && !mbar_wait_bounded(&ring.empty[s], ph ^ 1u)) {
-                    set_dev_error(kErrWaitEmpty);
-                    ring.abort = 1;
-                    break;
-                }
-                uint8_t* dst = ring_base + (size_t)s * stage_bytes;
-                mbar_arrive_expect_tx(&ring.full[s], cbytes + sbytes);
-                bulk_g2s(dst, cw, cbytes, &ring.full[s]);
-                bulk_g2s(dst + cbytes, sw, sbytes, &ring.full[s]);
-                ring.uses[s] += 1;
+                if (!ring_fill(ring, ring_base, stage_bytes, nst, f, cw, sw, a.H)) break;
                 cw += cbytes;
                 sw += sbytes;
-                if (++s == nst) {
-                    s = 0;
-                    ph ^= 1u;
-                }
             }
         }
         pdl_wait();
@@ -103,24 +88,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_lm_head(const LmArgs a) {
         const float gw = __ldg(a.global);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = g < a.T ? xb + (size_t)g * a.H : nullptr;
-        // this warp's group, rank and k-chunk share (the same for every
-        // tile), and the stage / phase of its current item carried along
-        const int grp = warp % ngr, rank = warp / ngr, gs = group_size(grp, ngr);
-        const int nc = (a.H + 127) >> 7, c0 = nc * rank / gs, c1 = nc * (rank + 1) / gs;
-        int s = grp;
-        uint32_t ph = 0, u = 0;
-        for (int li = grp; li < n; li += ngr) {
-            const TileOut o = group_tile_at(&ring, s, ph, u, grp, rank, gs, ngr, ring_base + (size_t)s * stage_bytes,
-                                            a.H, bcol, c0, c1);
-            if ((s += ngr) >= nst) {
-                s -= nst;
-                ph ^= 1u;
-            }
-            u ^= 1u;
-            if (!o.ok) break;
-            if (!o.lead) continue;
-            const float acc[4] = {o.acc.x, o.acc.y, o.acc.z, o.acc.w};
-            const int64_t row0 = 16 * (ib + li);
+        GroupCursor cur = group_cursor(nst, ngr, a.H, a.H);
+        for (; cur.li < n; cursor_next(cur)) {
+            float acc[4];
+            bool ok;
+            const bool lead = group_tile(ring, cur, ring_base, stage_bytes, a.H, bcol, acc, ok);
+            if (!ok) break;
+            if (!lead) continue;
+            const int64_t row0 = 16 * (ib + cur.li);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
                 const int t = 2 * q + (v & 1);

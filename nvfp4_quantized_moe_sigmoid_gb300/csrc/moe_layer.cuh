@@ -130,11 +130,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_up(const LayerUpArgs a) {
         s = a.sh_scales + 16 * r * (a.H >> 4);
     };
     const int pre = min(n_sh, nst);
+    FillCursor fc = fill_cursor(0, nst);  // the producer's next item
     if (warp == kConsumerWarps && lane == 0) {
         for (int li = 0; li < pre; ++li) {
             const uint8_t *c, *s;
             sh_tile(sb + li, c, s);
-            ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, a.H);
+            ring_fill(ring, ring_base, stage_bytes, nst, fc, c, s, a.H);
         }
     }
     pdl_wait();
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_up(const LayerUpArgs a) {
         if (li < n_sh) {
             sh_tile(sb + li, c, s);
         } else {
-            const int64_t i = rb + (li - n_sh);
+            const int i = static_cast<int>(rb) + (li - n_sh);  // U x rows < 2^31
             const int u = static_cast<int>(i / RI), r = static_cast<int>(i % RI);
             const int64_t row = (int64_t)plan.expert[u] * a.I + 16 * r;
             c = a.codes + row * (a.H >> 1);
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_up(const LayerUpArgs a) {
             for (int li = pre; li < n; ++li) {
                 const uint8_t *c, *s;
                 item(li, c, s);
-                if (!ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, a.H)) break;
+                if (!ring_fill(ring, ring_base, stage_bytes, nst, fc, c, s, a.H)) break;
             }
         }
     } else {
@@ -179,18 +180,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_up(const LayerUpArgs a) {
         if (!bok && lane == 0) set_dev_error(kErrWaitFull);
         const int g = lane >> 2, q = lane & 3;
         const __half* bcol = (bok && g < a.T) ? xb + (size_t)g * a.H : nullptr;
-        const int s = warp % nst;
-        for (int li = s; li < n; li += nst) {
-            const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
+        GroupCursor cur = group_cursor(nst, nst, a.H, a.H);
+        for (; cur.li < n; cursor_next(cur)) {
+            const int li = cur.li;
             float acc[4];
             bool ok;
-            const bool mine = group_tile(ring, nst, nst, li, st, a.H, bcol, acc, ok);
+            const bool mine = group_tile(ring, cur, ring_base, stage_bytes, a.H, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const bool routed = li >= n_sh;
             int u = 0, r;
             if (routed) {
-                const int64_t i = rb + (li - n_sh);
+                const int i = static_cast<int>(rb) + (li - n_sh);  // U x rows < 2^31
                 u = static_cast<int>(i / RI);
                 r = static_cast<int>(i % RI);
             } else {
@@ -308,11 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_down(const LayerDownArgs 
         s = a.sh_scales + 16 * r * (a.S >> 4);
     };
     const int pre = min(n_sh, nst);
+    FillCursor fc = fill_cursor(0, nst);  // the producer's next item
     if (warp == kConsumerWarps && lane == 0) {
         for (int li = 0; li < pre; ++li) {
             const uint8_t *c, *s;
             sh_tile(sb + li, c, s);
-            ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, a.S);
+            ring_fill(ring, ring_base, stage_bytes, nst, fc, c, s, a.S);
         }
     }
     pdl_wait();
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_down(const LayerDownArgs 
             sh_tile(sb + li, c, s);
             K = a.S;
         } else {
-            const int64_t i = rb + (li - n_sh);
+            const int i = static_cast<int>(rb) + (li - n_sh);  // U x rows < 2^31
             const int u = static_cast<int>(i / RH), r = static_cast<int>(i % RH);
             const int64_t row = (int64_t)plan.expert[u] * a.H + 16 * r;
             c = a.codes + row * (a.I >> 1);
@@ -383,19 +385,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_down(const LayerDownArgs 
                 const uint8_t *c, *s;
                 int K;
                 item(li, c, s, K);
-                if (!ring_fill(ring, ring_base, stage_bytes, nst, li, c, s, K)) break;
+                if (!ring_fill(ring, ring_base, stage_bytes, nst, fc, c, s, K)) break;
             }
         }
     } else {
         const bool bok = __all_sync(0xffffffffu, mbar_wait_bounded(&bbar, 0));
         if (!bok && lane == 0) set_dev_error(kErrWaitFull);
         const int g = lane >> 2, q = lane & 3;
-        const int s = warp % nst;
-        for (int li = s; li < n; li += nst) {
+        GroupCursor cur = group_cursor(nst, nst, a.I, a.S);
+        for (; cur.li < n; cursor_next(cur)) {
+            const int li = cur.li;
             const bool routed = li >= n_sh;
             int u = -1, r, sl, K;
             if (routed) {
-                const int64_t i = rb + (li - n_sh);
+                const int i = static_cast<int>(rb) + (li - n_sh);  // U x rows < 2^31
                 u = static_cast<int>(i / RH);
                 r = static_cast<int>(i % RH);
                 sl = u == slot_u[0] ? 0 : (u == slot_u[1] ? 1 : -1);
@@ -409,10 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_down(const LayerDownArgs 
             __half* const bs = sl == 0 ? bslot0 : (sl == 1 ? bslot1 : bslot2);
             const __half* bcol = nullptr;
             if (bok && sl >= 0 && g < a.T && (!routed || plan.choice[u][g] >= 0)) bcol = bs + (size_t)g * K;
-            const uint8_t* st = ring_base + (size_t)(li % nst) * stage_bytes;
             float acc[4];
             bool ok;
-            const bool mine = group_tile(ring, nst, nst, li, st, K, bcol, acc, ok);
+            const bool mine = group_tile(ring, cur, ring_base, stage_bytes, K, bcol, acc, ok);
             if (!ok) break;
             if (!mine) continue;
             const float gw = routed ? __ldg(a.global + plan.expert[u]) : __ldg(a.sh_global);
