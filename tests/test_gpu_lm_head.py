@@ -49,11 +49,13 @@ def test_full_lm_head_sampled_rows(nm, T):
 
 @pytest.mark.parametrize("T", [9, 64, 100, 300])
 @pytest.mark.parametrize("eps", [0.0, 1e-5])
-def test_small_lm_head_forward_gemm(nm, T, eps):
+@pytest.mark.parametrize("V", [1024, 1152, 128])
+def test_small_lm_head_forward_gemm(nm, T, eps, V):
     """lm_head_forward above 8 tokens (the tensor-core GEMM: N = tokens rounded
-    up to 16, up to 256 per launch; 300 tokens take two launches) against the
-    oracle, with and without the final RMS norm."""
-    V, H = 1024, 2688
+    up to 16, up to 256 per launch; 300 tokens take two launches; 1152 and
+    128 rows give fewer 128-row tiles than CTAs) against the oracle, with and
+    without the final RMS norm."""
+    H = 2688
     tid = gen.tensor_id(gen.KIND_LM_HEAD, 2, V)
     master = gen.normal_bf16(V * H, 4, tid, gen.WEIGHT_SIGMA).reshape(V, H)
     W = orc.Mat.from_master(master)
