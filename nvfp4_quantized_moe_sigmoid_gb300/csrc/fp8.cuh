@@ -162,6 +162,11 @@ __global__ void __launch_bounds__(kF8Threads) k_fp8_gemv(const Fp8GemvArgs a) {
             ub[i] = __ldg(reinterpret_cast<const uint4*>(wb + 64 * s));
         }
     }
+    // the rows (and, for the down projection, the up kernel's output) are an
+    // earlier kernel's: with programmatic dependent launch this kernel may
+    // start, and its weight loads run, while that kernel finishes
+    pdl_trigger();
+    pdl_wait();
     // token rows -> E4M3 in shared memory, all threads on all rows at once:
     // per row the sum of squares and the amax (in warp order), then (the RMS
     // norm: y = bf16(x inv), whose amax is bf16(amax(x) inv) as rounding is

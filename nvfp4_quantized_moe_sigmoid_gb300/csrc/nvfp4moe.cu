@@ -1645,7 +1645,9 @@ extern "C" nvfp4_status moe_shared_fp8_forward(const fp8_matrix* up, const fp8_m
         ua.rms_eps = rms_eps;
         ua.T = tc;
         ua.act = act;
-        k_fp8_gemv<kGroupedUp><<<static_cast<int>(S / 16), kF8Threads, (size_t)tc * H, stream>>>(ua);
+        nvfp4_status st = launch_pdl(k_fp8_gemv<kGroupedUp>, static_cast<int>(S / 16), kF8Threads, (size_t)tc * H,
+                                     stream, ua);
+        if (st != NVFP4_OK) return st;
         Fp8GemvArgs da{};
         da.w = down->codes;
         da.gw = down->global_scale;
@@ -1655,8 +1657,8 @@ extern "C" nvfp4_status moe_shared_fp8_forward(const fp8_matrix* up, const fp8_m
         da.T = tc;
         da.residual = residual ? static_cast<const uint16_t*>(residual) + (size_t)t0 * H : nullptr;
         da.out = static_cast<uint16_t*>(out) + (size_t)t0 * H;
-        k_fp8_gemv<kGroupedDown><<<static_cast<int>(H / 16), kF8Threads, (size_t)tc * S, stream>>>(da);
-        if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+        st = launch_pdl(k_fp8_gemv<kGroupedDown>, static_cast<int>(H / 16), kF8Threads, (size_t)tc * S, stream, da);
+        if (st != NVFP4_OK) return st;
     }
     return launch_status();
 }
