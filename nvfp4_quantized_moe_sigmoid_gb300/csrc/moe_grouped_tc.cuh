@@ -134,6 +134,20 @@ __device__ __forceinline__ void tc_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 32 consecutive columns of a lane quarter in one load (one wait)
+__device__ __forceinline__ void tc_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor of tcgen05.mma for the K-major 128-byte
 // swizzled layout: start address (16-byte units), leading byte offset 16
 // (unused by this layout), stride byte offset 1024 (8-row groups),
@@ -607,29 +621,64 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const __grid_const
             unsigned int* const amax = s.amax;
             float* const yout = s.y;
             const bool gated = s.gate != nullptr;
-            for (int c0 = 0; c0 < it.n; c0 += 16) {
-                uint32_t r[16];
-                tc_ld_x16(tmem + lb + 128u * db + c0, r);
-                for (int c = 1; c < nc; ++c) {  // the other accumulators, added in order
-                    uint32_t r2[16];
-                    tc_ld_x16(tmem + lb + 128u * db + 32u * ng * c + c0, r2);
+            // wide items (more than 64 positions): 32 columns per TMEM load (one
+            // wait), and the warp's maximum of column c0 + j kept in lane j,
+            // which posts it (one atomic per lane per 32 columns); narrow
+            // items: 16 columns per load, lane 0 posting each column's maximum
+            if (it.n > 64) {
+                for (int c0 = 0; c0 < it.n; c0 += 32) {
+                    uint32_t r[32];
+                    tc_ld_x32(tmem + lb + 128u * db + c0, r);
+                    for (int c = 1; c < nc; ++c) {  // the other accumulators, added in order
+                        uint32_t r2[32];
+                        tc_ld_x32(tmem + lb + 128u * db + 32u * ng * c + c0, r2);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), __uint_as_float(r2[j])));
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), __uint_as_float(r2[j])));
+                    }
+                    unsigned int mine = 0u;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int p = it.row0 + c0 + j;
+                        if (c0 + j >= it.n) break;
+                        const float v = __fmul_rn(__uint_as_float(r[j]), ep_scale[q][c0 + j]);
+                        if (KIND == kGroupedUp) {
+                            const float rl = fmaxf(v, 0.0f);
+                            const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
+                            if (mv) act[(size_t)p * M + m] = *reinterpret_cast<const uint16_t*>(&bv);
+                            const unsigned int mx =
+                                __reduce_max_sync(0xffffffffu, mv ? __float_as_uint(__bfloat162float(bv)) : 0u);
+                            if (lane == j) mine = mx;
+                        } else {
+                            if (mv) yout[(size_t)p * M + m] = gated ? __fmul_rn(ep_gate[q][c0 + j], v) : v;
+                        }
+                    }
+                    if (KIND == kGroupedUp && mine != 0u) atomicMax(amax + it.row0 + c0 + lane, mine);
                 }
+            } else {
+                for (int c0 = 0; c0 < it.n; c0 += 16) {
+                    uint32_t r[16];
+                    tc_ld_x16(tmem + lb + 128u * db + c0, r);
+                    for (int c = 1; c < nc; ++c) {  // the other accumulators, added in order
+                        uint32_t r2[16];
+                        tc_ld_x16(tmem + lb + 128u * db + 32u * ng * c + c0, r2);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int p = it.row0 + c0 + j;
-                    if (c0 + j >= it.n) break;
-                    const float v = __fmul_rn(__uint_as_float(r[j]), ep_scale[q][c0 + j]);
-                    if (KIND == kGroupedUp) {
-                        const float rl = fmaxf(v, 0.0f);
-                        const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
-                        if (mv) act[(size_t)p * M + m] = *reinterpret_cast<const uint16_t*>(&bv);
-                        const unsigned int mx =
-                            __reduce_max_sync(0xffffffffu, mv ? __float_as_uint(__bfloat162float(bv)) : 0u);
-                        if (lane == 0 && mx != 0u) atomicMax(amax + p, mx);
-                    } else {
-                        if (mv) yout[(size_t)p * M + m] = gated ? __fmul_rn(ep_gate[q][c0 + j], v) : v;
+                        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), __uint_as_float(r2[j])));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int p = it.row0 + c0 + j;
+                        if (c0 + j >= it.n) break;
+                        const float v = __fmul_rn(__uint_as_float(r[j]), ep_scale[q][c0 + j]);
+                        if (KIND == kGroupedUp) {
+                            const float rl = fmaxf(v, 0.0f);
+                            const __nv_bfloat16 bv = __float2bfloat16_rn(__fmul_rn(rl, rl));
+                            if (mv) act[(size_t)p * M + m] = *reinterpret_cast<const uint16_t*>(&bv);
+                            const unsigned int mx =
+                                __reduce_max_sync(0xffffffffu, mv ? __float_as_uint(__bfloat162float(bv)) : 0u);
+                            if (lane == 0 && mx != 0u) atomicMax(amax + p, mx);
+                        } else {
+                            if (mv) yout[(size_t)p * M + m] = gated ? __fmul_rn(ep_gate[q][c0 + j], v) : v;
+                        }
                     }
                 }
             }
