@@ -180,7 +180,9 @@ nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace
  * norm of the pre-norm model the pages serve, whose norms stay in bf16
  * ([card-int4] "Left at bfloat16"); the residual is added un-normalised.
  *   w          weights (host struct holding device pointers); shapes must
- *              satisfy hidden, inter, shared_inter % 64 == 0
+ *              satisfy hidden, inter, shared_inter % 16 == 0 (the NVFP4
+ *              block); widths that are not all multiples of 64 take the
+ *              generic kernels (below), every other call here needs % 64
  *   hidden     device bf16 [T][H], 16-byte aligned
  *   topk_idx   device int32 [T][k], entries in [0, E) and distinct per token
  *   topk_w     device float [T][k]
@@ -198,8 +200,10 @@ nvfp4_status moe_expert_forward_workspace_init(void* workspace, size_t workspace
  * persistent GEMV kernels (batch-1 decode and the 4-token verify, [worklog]
  * Interlude and Step 5); T > 4 groups the (token, choice) pairs by expert
  * (moe_permute) and runs the experts as one ragged grouped GEMM ([worklog]
- * Step 3). Both compute the same arithmetic; their FP32 summation orders
- * differ. */
+ * Step 3). Widths off the 64 grid (any T) take generic kernels: one CTA per
+ * (token, choice) and per token for the shared expert, a warp per output
+ * row, then a combine kernel; the workspace is the T <= 4 path's. All paths
+ * compute the same arithmetic; their FP32 summation orders differ. */
 nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
                                 const int32_t* topk_idx, const float* topk_w, int32_t T,
                                 int32_t k, nvfp4_act_mode mode, float rms_eps, const void* residual,

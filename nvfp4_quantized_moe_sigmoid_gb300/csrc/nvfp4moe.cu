@@ -21,6 +21,7 @@
 #include "lm_head_tc.cuh"
 #include "moe_decode.cuh"
 #include "moe_grouped.cuh"
+#include "moe_generic.cuh"
 #include "moe_grouped_tc.cuh"
 #include "moe_layer.cuh"
 #include "moe_stack.cuh"
@@ -183,6 +184,64 @@ DecodeWs decode_ws(int T, int k, int H, int I, int S) {
     return w;
 }
 
+// Widths that are multiples of 16 but not of 64 (moe_generic.cuh): up for
+// every (token, slot) and the shared expert, then down, then the combine.
+nvfp4_status generic_forward(const moe_layer_weights* w, const void* hidden, const int32_t* topk_idx,
+                             const float* topk_w, int T, int k, bool w4a4, float rms_eps, const void* residual,
+                             void* out, uint8_t* ws, cudaStream_t stream) {
+    const int H = w->hidden, I = w->inter, S = w->shared_inter;
+    const DecodeWs o = decode_ws(T, k, H, I, S);
+    const size_t smem_up = ((2 * (size_t)H + 15) & ~size_t(15)) + 4 * (size_t)H;
+    const size_t smem_dn = 4 * (size_t)std::max(I, S);
+    if ((int64_t)smem_up > dyn_smem_limit(k_gen_up) || (int64_t)smem_dn > dyn_smem_limit(k_gen_down))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)T * (k + 1) > (1LL << 30) || (int64_t)T * H > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    GenArgs ua{};
+    ua.codes = w->up_codes;
+    ua.scales = w->up_scales;
+    ua.global = w->up_global;
+    ua.sh_codes = w->shared_up.codes;
+    ua.sh_scales = w->shared_up.scales;
+    ua.sh_global = w->shared_up.global_scale;
+    ua.E = w->num_experts;
+    ua.n = I;
+    ua.K = H;
+    ua.n_sh = S;
+    ua.K_sh = H;
+    ua.src = static_cast<const uint16_t*>(hidden);
+    ua.rms_eps = rms_eps;
+    ua.topk_idx = topk_idx;
+    ua.topk_w = topk_w;
+    ua.T = T;
+    ua.k = k;
+    ua.w4a4 = w4a4;
+    ua.act = reinterpret_cast<uint16_t*>(ws + o.act);
+    ua.act_sh = reinterpret_cast<uint16_t*>(ws + o.act_sh);
+    k_gen_up<<<T * (k + 1), kGenThreads, smem_up, stream>>>(ua);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    GenArgs da = ua;
+    da.codes = w->down_codes;
+    da.scales = w->down_scales;
+    da.global = w->down_global;
+    da.sh_codes = w->shared_down.codes;
+    da.sh_scales = w->shared_down.scales;
+    da.sh_global = w->shared_down.global_scale;
+    da.n = H;
+    da.K = I;
+    da.n_sh = H;
+    da.K_sh = S;
+    da.src = ua.act;
+    da.src_sh = ua.act_sh;
+    da.rms_eps = 0.0f;
+    da.ypart = reinterpret_cast<float*>(ws + o.ypart);
+    da.ysh = reinterpret_cast<float*>(ws + o.ysh);
+    k_gen_down<<<T * (k + 1), kGenThreads, smem_dn, stream>>>(da);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    k_gen_combine<<<(T * H + kGenThreads - 1) / kGenThreads, kGenThreads, 0, stream>>>(
+        da.ypart, da.ysh, T, k, H, static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(out));
+    return launch_status();
+}
+
 // The grouped path (T > 4, moe_grouped.cuh), defined below.
 size_t grouped_ws_total(int T, int k, int E, int H, int I, int S);
 nvfp4_status grouped_forward(const moe_layer_weights* w, const void* hidden, const int32_t* topk_idx,
@@ -204,14 +263,20 @@ nvfp4_status check_matrix(const nvfp4_matrix& m, int64_t n, int64_t k) {
     return NVFP4_OK;
 }
 
-nvfp4_status check_layer(const moe_layer_weights* w) {
+// A layer whose widths are multiples of 16 but not all of 64: only
+// moe_expert_forward takes it (the generic kernels); every other layer call
+// needs multiples of 64.
+bool generic_shape(const moe_layer_weights* w) { return w->hidden % 64 || w->inter % 64 || w->shared_inter % 64; }
+
+// kmod: the multiple the widths must be (64; 16 for moe_expert_forward)
+nvfp4_status check_layer(const moe_layer_weights* w, int kmod = 64) {
     if (!w) return NVFP4_ERR_INVALID_ARG;
     if (w->num_experts < 1 || w->hidden < 1 || w->inter < 1 || w->shared_inter < 1)
         return NVFP4_ERR_INVALID_ARG;
     if (!w->up_codes || !w->up_scales || !w->up_global || !w->down_codes || !w->down_scales ||
         !w->down_global)
         return NVFP4_ERR_INVALID_ARG;
-    if (w->hidden % 64 || w->inter % 64 || w->shared_inter % 64) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (w->hidden % kmod || w->inter % kmod || w->shared_inter % kmod) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(w->up_codes, 16) || !aligned(w->up_scales, 16) || !aligned(w->down_codes, 16) ||
         !aligned(w->down_scales, 16))
         return NVFP4_ERR_MISALIGNED;
@@ -363,7 +428,7 @@ size_t moe_expert_forward_workspace_size(const moe_layer_weights* w, int32_t T, 
                                          nvfp4_act_mode mode) {
     (void)mode;
     if (!w || T < 1 || k < 1) return 0;
-    if (decode_path(w, T, k)) return decode_ws(T, k, w->hidden, w->inter, w->shared_inter).total;
+    if (decode_path(w, T, k) || generic_shape(w)) return decode_ws(T, k, w->hidden, w->inter, w->shared_inter).total;
     return grouped_ws_total(T, k, w->num_experts, w->hidden, w->inter, w->shared_inter);
 }
 
@@ -377,7 +442,7 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
                                 const int32_t* topk_idx, const float* topk_w, int32_t T, int32_t k,
                                 nvfp4_act_mode mode, float rms_eps, const void* residual, void* out,
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    nvfp4_status st = check_layer(w);
+    nvfp4_status st = check_layer(w, 16);
     if (st != NVFP4_OK) return st;
     if (!hidden || !topk_idx || !topk_w || !out || !workspace) return NVFP4_ERR_INVALID_ARG;
     if (T < 1 || k < 1 || k > w->num_experts) return NVFP4_ERR_INVALID_ARG;
@@ -386,6 +451,12 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
         (residual && !aligned(residual, 4)))
         return NVFP4_ERR_MISALIGNED;
     if (hidden == out && residual != hidden) return NVFP4_ERR_INVALID_ARG;
+    if (generic_shape(w)) {
+        if (workspace_bytes < decode_ws(T, k, w->hidden, w->inter, w->shared_inter).total)
+            return NVFP4_ERR_WORKSPACE;
+        return generic_forward(w, hidden, topk_idx, topk_w, T, k, mode == NVFP4_W4A4, rms_eps, residual, out,
+                               static_cast<uint8_t*>(workspace), stream);
+    }
     if (!decode_path(w, T, k)) {
         // more than 4 tokens: grouped GEMM over the tokens each expert received
         if (w->num_experts > 256) return NVFP4_ERR_UNSUPPORTED_SHAPE;

@@ -78,6 +78,17 @@ def test_host_validation_rejects_bad_arguments(abi):
                               0x10000, sh_up, sh_dn)
     assert L.moe_expert_forward(ctypes.byref(bad), fake, fake, fake, 1, 6, 1, 0.0, null, fake, fake, need,
                                 null) == 2
+    # widths that are multiples of 16 but not of 64 (I = 1840): moe_expert_forward takes them (the
+    # generic kernels, any token count, the decode workspace), the fused layer call does not
+    sh_up16 = abi.NVFP4Matrix(0x10000, 0x10000, 0x10000, 3712, 2688)
+    w16 = abi.MoeLayerWeights(128, 2688, 1840, 3712, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000,
+                              0x10000, sh_up16, sh_dn)
+    need16 = L.moe_expert_forward_workspace_size(ctypes.byref(w16), 8, 6, 1)
+    assert need16 >= 8 * 6 * 1840 * 2 + 8 * 6 * 2688 * 4
+    assert L.moe_expert_forward(ctypes.byref(w16), fake, fake, fake, 8, 6, 1, 0.0, null, ctypes.c_void_p(0x20000),
+                                ctypes.c_void_p(0x30000), need16 - 1, null) == 4
+    assert L.moe_layer_forward(ctypes.byref(w16), fake, fake, fake, 1, 6, 1, 0.0, null, fake, fake, fake,
+                               ctypes.c_void_p(0x30000), need16, null) == 2
     nul = abi.MoeLayerWeights(128, 2688, 1856, 3712, 0, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000,
                               sh_up, sh_dn)
     assert L.moe_expert_forward(ctypes.byref(nul), fake, fake, fake, 1, 6, 1, 0.0, null, fake, fake, need,
