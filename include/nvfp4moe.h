@@ -390,7 +390,9 @@ nvfp4_status moe_expert_forward_noalloc(const moe_layer_weights* w, const void* 
  *   logits[t][v] = sum_j W[v][j] * h[t][j], FP32 accumulation and output;
  *   h is the hidden row, or its unit-weight RMS norm (the final norm before
  *   the head) when rms_eps > 0.
- *   w        NVFP4 matrix [V][H] (device pointers), V % 16 == 0, H % 64 == 0
+ *   w        NVFP4 matrix [V][H] (device pointers), V % 16 == 0, H % 16 == 0
+ *            (H % 64 != 0 runs a generic kernel: a CTA per 64 rows x 8
+ *            tokens, a warp per row; correct, not fast)
  *   hidden   device bf16 [T][H], 16-byte aligned;  T >= 1
  *   rms_eps  > 0: normalise each hidden row first; <= 0: use it as is
  *   logits   device float [T][V]
@@ -405,8 +407,9 @@ nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, 
  * a dense GEMM over 64-token tiles (the 256-sequence concurrent decode of
  * the [card-w4a4] serving numbers), reading each weight tile once per 64
  * tokens instead of once per 8.
- *   w, hidden, T, rms_eps, logits: as lm_head_gemv; for T > 8 also
- *              V % 64 == 0 and logits 16-byte aligned
+ *   w, hidden, T, rms_eps, logits: as lm_head_gemv; for T > 8 and
+ *              H % 64 == 0 also V % 64 == 0 and logits 16-byte aligned
+ *              (H % 64 != 0: the generic kernel for every T)
  *   workspace  device, >= lm_head_forward_workspace_size(w, T) bytes,
  *              256-byte aligned (unused for T <= 8)
  */

@@ -205,4 +205,60 @@ __global__ void __launch_bounds__(kGenThreads) k_gen_combine(const float* __rest
     out[i] = *reinterpret_cast<const uint16_t*>(&ob);
 }
 
+// The lm_head (weight-only NVFP4, bf16 activations) for a hidden width that
+// is a multiple of 16 but not of 64: logits[t][v] = g_w sum_k W[v][k] x_t[k]
+// (x_t RMS-normalised first when asked). Grid (V / 64 rows, T / 8 tokens):
+// a CTA holds up to 8 token rows as FP32 in shared memory, a warp takes
+// vocabulary rows and decodes each weight block once for all its tokens.
+constexpr int kGenLmTok = 8, kGenLmRows = 64;
+
+__global__ void __launch_bounds__(kGenThreads) k_gen_lm_head(const uint8_t* __restrict__ codes,
+                                                             const uint8_t* __restrict__ scales,
+                                                             const float* __restrict__ global, int V, int H,
+                                                             const uint16_t* __restrict__ hidden, int T,
+                                                             float rms_eps, float* __restrict__ logits,
+                                                             int64_t ld) {
+    extern __shared__ __align__(16) uint8_t gsm[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.y * kGenLmTok, nt = min(kGenLmTok, T - t0);
+    uint16_t* rows = reinterpret_cast<uint16_t*>(gsm);                               // [8][H] bf16
+    float* xs = reinterpret_cast<float*>(gsm + (size_t)kGenLmTok * H * 2);           // [8][H]
+    if (warp < nt) {
+        if (rms_eps > 0.0f)
+            warp_rmsnorm_row(hidden + (size_t)(t0 + warp) * H, rows + (size_t)warp * H, H, rms_eps);
+        else
+            warp_copy_row(hidden + (size_t)(t0 + warp) * H, rows + (size_t)warp * H, H);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nt * H; i += kGenThreads) xs[i] = bf16_bits_to_float(rows[i]);
+    __syncthreads();
+    const float gw = __ldg(global);
+    const int v1 = min(V, (blockIdx.x + 1) * kGenLmRows);
+    for (int v = blockIdx.x * kGenLmRows + warp; v < v1; v += kGenThreads / 32) {
+        const uint8_t* cr = codes + (size_t)v * (H >> 1);
+        const uint8_t* sr = scales + (size_t)v * (H >> 4);
+        float acc[kGenLmTok];
+#pragma unroll
+        for (int t = 0; t < kGenLmTok; ++t) acc[t] = 0.0f;
+        for (int b = lane; b < (H >> 4); b += 32) {
+            const float s = e4m3_to_float(sr[b]);
+            const uint2 c = *reinterpret_cast<const uint2*>(cr + 8 * b);
+            const uint32_t w2[2] = {c.x, c.y};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float wv = __fmul_rn(e2m1_to_float((w2[i >> 3] >> (4 * (i & 7))) & 15u), s);
+#pragma unroll
+                for (int t = 0; t < kGenLmTok; ++t)
+                    if (t < nt) acc[t] = __fmaf_rn(wv, xs[(size_t)t * H + 16 * b + i], acc[t]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kGenLmTok; ++t) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[t] = __fadd_rn(acc[t], __shfl_xor_sync(0xffffffffu, acc[t], o));
+            if (lane == 0 && t < nt) logits[(size_t)(t0 + t) * ld + v] = __fmul_rn(acc[t], gw);
+        }
+    }
+}
+
 }  // namespace nvfp4moe

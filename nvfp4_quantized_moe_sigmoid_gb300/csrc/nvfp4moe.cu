@@ -541,14 +541,29 @@ nvfp4_status moe_expert_forward(const moe_layer_weights* w, const void* hidden,
     return st;
 }
 
+// The lm_head for a hidden width that is a multiple of 16 but not of 64
+// (moe_generic.cuh), any token count.
+nvfp4_status lm_head_generic(const nvfp4_matrix* w, const void* hidden, int32_t T, float rms_eps, float* logits,
+                             cudaStream_t stream) {
+    const int H = static_cast<int>(w->k), V = static_cast<int>(w->n);
+    const size_t smem = (size_t)kGenLmTok * H * 6;
+    if ((int64_t)smem > dyn_smem_limit(k_gen_lm_head) || w->n > (1 << 30) || (T + kGenLmTok - 1) / kGenLmTok > 65535)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const dim3 grid((V + kGenLmRows - 1) / kGenLmRows, (T + kGenLmTok - 1) / kGenLmTok);
+    k_gen_lm_head<<<grid, kGenThreads, smem, stream>>>(w->codes, w->scales, w->global_scale, V, H,
+                                                       static_cast<const uint16_t*>(hidden), T, rms_eps, logits, V);
+    return launch_status();
+}
+
 nvfp4_status lm_head_gemv(const nvfp4_matrix* w, const void* hidden, int32_t T, float rms_eps,
                           float* logits, cudaStream_t stream) {
     if (!w || !hidden || !logits || T < 1) return NVFP4_ERR_INVALID_ARG;
-    if (!w->codes || !w->scales || !w->global_scale || w->n < 16 || w->k < 64)
+    if (!w->codes || !w->scales || !w->global_scale || w->n < 16 || w->k < 16)
         return NVFP4_ERR_INVALID_ARG;
-    if (w->n % 16 || w->k % 64 || w->k > (1 << 20)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (w->n % 16 || w->k % 16 || w->k > (1 << 20)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(w->codes, 16) || !aligned(w->scales, 16) || !aligned(hidden, 16) || !aligned(logits, 4))
         return NVFP4_ERR_MISALIGNED;
+    if (w->k % 64) return lm_head_generic(w, hidden, T, rms_eps, logits, stream);
     const int H = static_cast<int>(w->k);
     LmArgs la{};
     la.codes = w->codes;
@@ -1452,8 +1467,8 @@ LmWsOffsets lm_ws(int T, int H) {
 }  // namespace
 
 extern "C" size_t lm_head_forward_workspace_size(const nvfp4_matrix* w, int32_t T) {
-    if (!w || T < 1 || w->k < 64) return 0;
-    if (T <= kLmMaxT) return 256;
+    if (!w || T < 1 || w->k < 16) return 0;
+    if (T <= kLmMaxT || w->k % 64) return 256;
     return lm_ws(T, static_cast<int>(w->k)).total;
 }
 
@@ -1461,7 +1476,7 @@ extern "C" nvfp4_status lm_head_forward(const nvfp4_matrix* w, const void* hidde
                                         float* logits, void* workspace, size_t workspace_bytes,
                                         cudaStream_t stream) {
     if (!w || !hidden || !logits || T < 1) return NVFP4_ERR_INVALID_ARG;
-    if (T <= kLmMaxT) return lm_head_gemv(w, hidden, T, rms_eps, logits, stream);
+    if (T <= kLmMaxT || (w->k % 64 && w->k % 16 == 0)) return lm_head_gemv(w, hidden, T, rms_eps, logits, stream);
     if (!workspace) return NVFP4_ERR_INVALID_ARG;
     if (!w->codes || !w->scales || !w->global_scale || w->n < 64 || w->k < 64) return NVFP4_ERR_INVALID_ARG;
     if (w->n % 64 || w->k % 64 || w->k > (1 << 20) || w->n > (1 << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;

@@ -41,3 +41,30 @@ def test_generic_rms_norm_residual(nm):
     h3 = (gen.bf16_bits_to_f32(h) * 3.0).astype(np.float32).view(np.uint32) >> 16
     for w4a4 in (False, True):
         run_layer(nm, L, OL, h3.astype(np.uint16), 2, w4a4, True, rms_eps=1e-5)
+
+
+@pytest.mark.parametrize("V,H", [(48, 80), (160, 208)])
+@pytest.mark.parametrize("T", [1, 5, 11])
+@pytest.mark.parametrize("eps", [0.0, 1e-5])
+def test_generic_lm_head(nm, V, H, T, eps):
+    """lm_head_gemv and lm_head_forward at a hidden width off the 64 grid (the
+    generic kernel, any token count) against the oracle."""
+    import torch
+    from gen import configs
+    from oracle import oracle as orc
+    from tests.helpers import assert_close, to_dev_bf16
+    tid = gen.tensor_id(gen.KIND_LM_HEAD, 3, V)
+    master = gen.normal_bf16(V * H, 5, tid, gen.WEIGHT_SIGMA).reshape(V, H)
+    W = orc.Mat.from_master(master)
+    m = nm.nvfp4_quantize(to_dev_bf16(master), nm.PER_TENSOR)
+    h = gen.hidden_bf16(T, H, 5, layer=configs.LM_INPUT_LAYER)
+    x = orc.rms_norm(h, eps) if eps > 0 else h
+    ref = orc.lm_head(W, x)
+    got = nm.lm_head_forward(m, to_dev_bf16(h), rms_eps=eps)
+    torch.cuda.synchronize()
+    assert nm.nvfp4_last_device_error() == 0
+    assert_close(got.cpu().numpy(), ref, "logits")
+    if T <= 8:
+        got2 = nm.lm_head_gemv(m, to_dev_bf16(h), rms_eps=eps)
+        torch.cuda.synchronize()
+        assert np.array_equal(got2.cpu().numpy(), got.cpu().numpy())
