@@ -114,7 +114,9 @@ __device__ __forceinline__ void tile_mma_16x8(const uint8_t* __restrict__ tcodes
 // w % groups; nstages a multiple of groups): local item li goes to stage
 // li % nstages and to group li % groups, whose warps each take a contiguous
 // share of the tile's k-chunks and all release the stage. A group thus owns
-// nstages / groups stages and computes on one while the next ones land.
+// nstages / groups stages (one in every kernel here: with the warps of two
+// CTAs per SM sharing the issue slots, more groups measured faster than
+// deeper buffering per group).
 // Every use of a stage is waited on, in order, by the same warps (an mbarrier
 // parity wait names the current or the immediately preceding phase; a waiter
 // for use u must not start while the barrier is still in phase u - 2, which
