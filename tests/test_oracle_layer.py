@@ -53,8 +53,8 @@ def ref_layer(L: OracleLayer, h, r, w4a4, residual):
 
 
 @pytest.mark.parametrize("w4a4,residual", [(False, False), (True, False), (True, True)])
-def test_tiny_layer_matches_dense_numpy(w4a4, residual):
-    H, I, S, E, k = 32, 16, 48, 8, 2
+@pytest.mark.parametrize("H,I,S,E,k", [(32, 16, 48, 8, 2), (80, 48, 112, 8, 3)])
+def test_tiny_layer_matches_dense_numpy(w4a4, residual, H, I, S, E, k):
     L = OracleLayer(3, 1, H, I, S, E, (-0.1, 0.1))
     h = gen.hidden_bf16(4, H, 3, layer=1)
     out, outf, r = L.forward(h, k, w4a4, residual)
